@@ -1,0 +1,19 @@
+"""Beam MoE layer (group-limited routed experts) for GB300 / sm_103a.
+
+The compute path is the C-ABI library ``libbeam_moe.so`` (hand-written CUDA);
+this package only marshals arguments to it.  ``inputs`` draws seeded synthetic
+workloads.  Importing the package does not load the library; the first call
+of an entry point does, and fails loudly when it is missing.
+"""
+from .config import BeamMoEConfig  # noqa: F401
+
+
+def __getattr__(name):
+    # the binding is loaded lazily so that the input generator can be imported
+    # on machines without the compiled library
+    if name in ("route", "forward", "forward_routed", "forward_nvfp4", "workspace_size",
+                "Workspace", "check_status", "BeamError", "library_path", "topk_from_logits",
+                "set_stage_events", "layout"):
+        from . import api
+        return getattr(api, name)
+    raise AttributeError(name)

@@ -1,0 +1,264 @@
+"""CPU oracle for the Beam MoE layer -- TEST INFRASTRUCTURE ONLY.
+
+A plain, slow, obviously correct C implementation (``beam_oracle.c``) of what
+the CUDA path computes, loaded through ``ctypes``.  Only ``tests/``,
+``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline / reference legs may
+import it.  The product package never imports it and shares no code with it;
+the two meet only through the seeded input generator and plain arrays.
+
+BF16 arrays cross this boundary as ``numpy.uint16`` bit patterns.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "beam_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "libbeam_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+_P = ctypes.c_void_p
+_I32 = ctypes.c_int32
+_I64 = ctypes.c_int64
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (OpenMP, no FMA contraction)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math",
+           "-fopenmp", "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        lib = ctypes.CDLL(build())
+        lib.oracle_router_logits.argtypes = [_P, _P, _I64, _I32, _I32, _P]
+        lib.oracle_route.argtypes = [_P, _P, _I64, _I32, _I32, _I32, _I32, ctypes.c_float,
+                                     _P, _P, _P, _P, _P, _P, _P]
+        lib.oracle_experts_bf16.argtypes = [_P, _I64, _I32, _I32, _I32, _I32, _P, _P,
+                                            _P, _P, _P, _P, _I64, _P]
+        lib.oracle_experts_nvfp4.argtypes = [_P, _I64, _I32, _I32, _I32, _I32, _P, _P,
+                                             _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                             _I32, _P, _I64, _P]
+        for name in ("oracle_e2m1_value", "oracle_e4m3_value"):
+            getattr(lib, name).argtypes = [ctypes.c_uint8]
+            getattr(lib, name).restype = ctypes.c_double
+        for name in ("oracle_e2m1_encode", "oracle_e4m3_encode"):
+            getattr(lib, name).argtypes = [ctypes.c_float]
+            getattr(lib, name).restype = ctypes.c_uint8
+        lib.oracle_bf16_round.argtypes = [ctypes.c_float]
+        lib.oracle_bf16_round.restype = ctypes.c_uint16
+        lib.oracle_nvfp4_quantize.argtypes = [_P, _I64, _P, _P]
+        lib.oracle_num_threads.restype = ctypes.c_int
+        lib.oracle_set_threads.argtypes = [ctypes.c_int]
+        _lib = lib
+        return lib
+
+
+def _ptr(a: np.ndarray | None):
+    return None if a is None else a.ctypes.data
+
+
+def _c(a, dtype) -> np.ndarray:
+    a = np.ascontiguousarray(a, dtype=dtype)
+    return a
+
+
+def num_threads() -> int:
+    return int(_load().oracle_num_threads())
+
+
+def set_threads(n: int) -> None:
+    _load().oracle_set_threads(int(n))
+
+
+# --------------------------------------------------------------------------
+# scalars
+# --------------------------------------------------------------------------
+def e2m1_value(code: int) -> float:
+    return float(_load().oracle_e2m1_value(code))
+
+
+def e4m3_value(code: int) -> float:
+    return float(_load().oracle_e4m3_value(code))
+
+
+def e2m1_encode(v: float) -> int:
+    return int(_load().oracle_e2m1_encode(v))
+
+
+def e4m3_encode(v: float) -> int:
+    return int(_load().oracle_e4m3_encode(v))
+
+
+def bf16_round(v: float) -> int:
+    return int(_load().oracle_bf16_round(v))
+
+
+def nvfp4_quantize(v: np.ndarray):
+    """Activation quantiser: returns (packed codes uint8 [n/2], scales uint8 [n/16])."""
+    v = _c(v, np.float32).reshape(-1)
+    q = np.zeros(v.size // 2, np.uint8)
+    sf = np.zeros(v.size // 16, np.uint8)
+    rc = _load().oracle_nvfp4_quantize(_ptr(v), v.size, _ptr(q), _ptr(sf))
+    if rc:
+        raise ValueError("length must be a multiple of 16")
+    return q, sf
+
+
+# --------------------------------------------------------------------------
+# the layer
+# --------------------------------------------------------------------------
+def router_logits(x_bf16: np.ndarray, wr: np.ndarray) -> np.ndarray:
+    """FP32 logits [T, E] of BF16 hidden rows x [T, d] against W_r [E, d]."""
+    x = _c(x_bf16, np.uint16)
+    wr = _c(wr, np.float32)
+    T, d = x.shape
+    E = wr.shape[0]
+    assert wr.shape[1] == d
+    out = np.zeros((T, E), np.float32)
+    rc = _load().oracle_router_logits(_ptr(x), _ptr(wr), T, d, E, _ptr(out))
+    if rc:
+        raise ValueError(f"oracle_router_logits failed ({rc})")
+    return out
+
+
+def route(logits: np.ndarray, bias: np.ndarray, n_groups: int, topk_groups: int,
+          topk: int, routed_scale: float) -> dict:
+    """Group-limited selection.  Returns idx [T,k] int32, w [T,k] f32, the
+    scores s and c [T,E], the kept-group mask [T,G] and the two margins."""
+    lg = _c(logits, np.float32)
+    b = _c(bias, np.float32)
+    T, E = lg.shape
+    idx = np.zeros((T, topk), np.int32)
+    w = np.zeros((T, topk), np.float32)
+    s = np.zeros((T, E), np.float32)
+    c = np.zeros((T, E), np.float32)
+    keep = np.zeros((T, n_groups), np.uint8)
+    em = np.zeros(T, np.float64)
+    gm = np.zeros(T, np.float64)
+    rc = _load().oracle_route(_ptr(lg), _ptr(b), T, E, n_groups, topk_groups, topk,
+                              float(routed_scale), _ptr(idx), _ptr(w), _ptr(s), _ptr(c),
+                              _ptr(keep), _ptr(em), _ptr(gm))
+    if rc:
+        raise ValueError(f"oracle_route failed ({rc})")
+    return {"idx": idx, "w": w, "s": s, "c": c, "keep": keep.astype(bool),
+            "expert_margin": em, "group_margin": gm}
+
+
+def _expert_ptrs(ws, E: int):
+    """Per-expert pointer table from a 3-D array or a list/dict of 2-D arrays
+    (None / missing entries for experts nobody uses)."""
+    arr = (ctypes.c_void_p * E)()
+    keep = []
+    if isinstance(ws, np.ndarray):
+        ws = np.ascontiguousarray(ws)
+        keep.append(ws)
+        for e in range(E):
+            arr[e] = ws[e].ctypes.data
+        return arr, keep
+    items = ws.items() if isinstance(ws, dict) else enumerate(ws)
+    for e, a in items:
+        if a is None:
+            continue
+        a = np.ascontiguousarray(a)
+        keep.append(a)
+        arr[e] = a.ctypes.data
+    return arr, keep
+
+
+def experts_bf16(x_bf16, idx, w, wg, wu, wd, n_experts: int, tokens=None,
+                 out: np.ndarray | None = None) -> np.ndarray:
+    """Weighted SwiGLU experts + combine for BF16 weights; returns BF16 [T, d].
+    wg/wu: per expert [F, d] uint16; wd: per expert [d, F] uint16."""
+    x = _c(x_bf16, np.uint16)
+    T, d = x.shape
+    idx = _c(idx, np.int32)
+    w = _c(w, np.float32)
+    k = idx.shape[1]
+    pg, kg_ = _expert_ptrs(wg, n_experts)
+    pu, ku_ = _expert_ptrs(wu, n_experts)
+    pd, kd_ = _expert_ptrs(wd, n_experts)
+    F = _infer_F(wg, d)
+    if out is None:
+        out = np.zeros((T, d), np.uint16)
+    tok = None if tokens is None else _c(tokens, np.int64)
+    rc = _load().oracle_experts_bf16(_ptr(x), T, d, F, k, n_experts, _ptr(idx), _ptr(w),
+                                     ctypes.cast(pg, _P), ctypes.cast(pu, _P),
+                                     ctypes.cast(pd, _P), _ptr(tok),
+                                     0 if tok is None else tok.size, _ptr(out))
+    if rc:
+        raise ValueError(f"oracle_experts_bf16 failed ({rc})")
+    return out
+
+
+def experts_nvfp4(x_bf16, idx, w, gate, up, down, n_experts: int, act_quant: bool = True,
+                  tokens=None, out: np.ndarray | None = None) -> np.ndarray:
+    """NVFP4 experts.  gate/up/down are dicts with per-expert 'q' (packed
+    codes [N, K/2]), 'sf' (E4M3 codes [N, K/16]) and 'gs' (float32 [E])."""
+    x = _c(x_bf16, np.uint16)
+    T, d = x.shape
+    idx = _c(idx, np.int32)
+    w = _c(w, np.float32)
+    k = idx.shape[1]
+    keep = []
+    tabs = []
+    for p in (gate, up, down):
+        q, kq = _expert_ptrs(p["q"], n_experts)
+        sf, ks = _expert_ptrs(p["sf"], n_experts)
+        gs = _c(p["gs"], np.float32)
+        keep += kq + ks + [gs]
+        tabs += [ctypes.cast(q, _P), ctypes.cast(sf, _P), _ptr(gs)]
+    F = _infer_F(gate["q"], d // 2)
+    if out is None:
+        out = np.zeros((T, d), np.uint16)
+    tok = None if tokens is None else _c(tokens, np.int64)
+    rc = _load().oracle_experts_nvfp4(_ptr(x), T, d, F, k, n_experts, _ptr(idx), _ptr(w),
+                                      *tabs, int(bool(act_quant)), _ptr(tok),
+                                      0 if tok is None else tok.size, _ptr(out))
+    if rc:
+        raise ValueError(f"oracle_experts_nvfp4 failed ({rc})")
+    return out
+
+
+def _infer_F(ws, inner: int) -> int:
+    if isinstance(ws, np.ndarray):
+        return int(ws.shape[1])
+    items = ws.values() if isinstance(ws, dict) else ws
+    for a in items:
+        if a is not None:
+            return int(np.asarray(a).shape[0])
+    raise ValueError("no expert weights given")
+
+
+def forward_bf16(x_bf16, wr, bias, wg, wu, wd, n_groups, topk_groups, topk,
+                 routed_scale, tokens=None):
+    """Whole layer: router -> selection -> experts -> combine.
+    Returns (out uint16 [T,d], routing dict, logits)."""
+    logits = router_logits(x_bf16, wr)
+    r = route(logits, bias, n_groups, topk_groups, topk, routed_scale)
+    out = experts_bf16(x_bf16, r["idx"], r["w"], wg, wu, wd, logits.shape[1], tokens=tokens)
+    return out, r, logits
+
+
+def bf16_to_f64(a: np.ndarray) -> np.ndarray:
+    """BF16 bit patterns -> float64 (exact)."""
+    a = np.asarray(a, np.uint16)
+    return (a.astype(np.uint32) << 16).view(np.float32).astype(np.float64)

@@ -1,0 +1,495 @@
+/*
+ * Beam MoE layer: plain CPU oracle.  TEST INFRASTRUCTURE ONLY.
+ *
+ * This is the slow, obviously correct reference the CUDA path is checked
+ * against.  Only the tests, the package smoke check and the benchmark's CPU
+ * baseline load it; the product path never does.  It shares no code, header,
+ * table or constant generator with the CUDA library.
+ *
+ * Sources (page title, section):
+ *   [SGL]  "SGLang 原生支持 Reflection 的 Beam 并驱动其生产 API",
+ *          sections "Dense Layers and Grouped MoE Routing",
+ *          "BF16 MoE Kernel Optimization", "Fusion Optimizations".
+ *   [VLLM] "vLLM 实现 Reflection Beam 501B MoE 模型 Day 0 支持",
+ *          section "MoE and residual stream".
+ *   [HF]   "Reflection 发布 501B 开源模型 Beam，Apache 2.0 许可",
+ *          sections "专家混合" (mixture of experts) and "残差流" (residual
+ *          stream: router and SwiGLU product computed in FP32).
+ *   [HWC]  "Reflection Beam 技术笔记：501B MoE 如何把「大容量」和「可部署」拧在一起",
+ *          section 1 (sparse MoE).
+ *
+ * Precision convention: every dot product accumulates in double and is
+ * rounded once to the precision the pages fix (FP32 router logits, FP32
+ * gate/up accumulators, FP32 SwiGLU product, BF16 activation h, FP32 routing
+ * weights, BF16 layer output).  Where the pages leave a step open the reading
+ * taken is stated at the function.  Built with -ffp-contract=off so that no
+ * multiply-add is fused and x86-64 and aarch64 give identical bits.
+ *
+ * Parity status: every function here is pinned by the CPU test-suite
+ * (library routines, brute force, closed forms, invariants); none is
+ * "parity unpinned".
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* ------------------------------------------------------------------------ */
+/* Scalar formats                                                            */
+/* ------------------------------------------------------------------------ */
+
+/* BF16 is the top half of an IEEE binary32. */
+static double bf16_value(uint16_t b) {
+  uint32_t u = (uint32_t)b << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return (double)f;
+}
+
+/* Round a binary32 to the nearest BF16, ties to even (NaN stays NaN). */
+static uint16_t bf16_round(float f) {
+  uint32_t u;
+  memcpy(&u, &f, sizeof u);
+  if ((u & 0x7f800000u) == 0x7f800000u && (u & 0x007fffffu) != 0u)
+    return (uint16_t)((u >> 16) | 0x0040u);
+  uint32_t keep = u >> 16;
+  uint32_t rest = u & 0xffffu;
+  if (rest > 0x8000u || (rest == 0x8000u && (keep & 1u))) keep += 1u;
+  return (uint16_t)keep;
+}
+
+/* E2M1 (FP4): 1 sign bit, 2 exponent bits (bias 1), 1 mantissa bit.
+ * Magnitudes of codes 0..7 written out from the format definition. */
+static double e2m1_value(uint8_t code) {
+  static const double mag[8] = {0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0};
+  double m = mag[code & 7u];
+  return (code & 8u) ? -m : m;
+}
+
+/* E4M3 (FP8, "fn" flavour): 1 sign, 4 exponent bits (bias 7), 3 mantissa
+ * bits, no infinities, S.1111.111 is NaN, largest finite 448. */
+static double e4m3_value(uint8_t code) {
+  int sign = (code >> 7) & 1;
+  int ex = (code >> 3) & 15;
+  int man = code & 7;
+  double v;
+  if (ex == 15 && man == 7) return NAN;
+  if (ex == 0)
+    v = ldexp((double)man / 8.0, -6);
+  else
+    v = ldexp(1.0 + (double)man / 8.0, ex - 7);
+  return sign ? -v : v;
+}
+
+/* Nearest code by exhaustive search over the format's finite magnitudes,
+ * ties to the even code (the one whose lowest bit is 0); values beyond the
+ * largest finite magnitude saturate to it (satfinite).  Brute force on
+ * purpose: it is the definition of round-to-nearest-even. */
+static uint8_t nearest_code(double a, double (*val)(uint8_t), int n_finite) {
+  int best = 0;
+  double best_err = fabs(a - val(0));
+  for (int c = 1; c < n_finite; ++c) {
+    double err = fabs(a - val((uint8_t)c));
+    if (err < best_err || (err == best_err && (best & 1) && !(c & 1))) {
+      best = c;
+      best_err = err;
+    }
+  }
+  return (uint8_t)best;
+}
+
+static uint8_t e2m1_encode(float v) {
+  if (isnan(v)) return 0;
+  if (isinf(v)) return (uint8_t)(v < 0 ? 15u : 7u);
+  uint8_t c = nearest_code(fabs((double)v), e2m1_value, 8);
+  return (uint8_t)(signbit(v) ? (c | 8u) : c);
+}
+
+static uint8_t e4m3_encode(float v) {
+  if (isnan(v)) return 0x7f;
+  if (isinf(v)) return (uint8_t)(v < 0 ? 0xfeu : 0x7eu);
+  uint8_t c = nearest_code(fabs((double)v), e4m3_value, 127);
+  return (uint8_t)(signbit(v) ? (c | 0x80u) : c);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Router: [SGL] "The router computes FP32 logits"; [VLLM] "FP32 router.  The */
+/* 5120 x 256 router weights, accumulation, and logits are all FP32".        */
+/* logits[t,e] = sum_j x[t,j] * W_r[e,j], accumulated in double, rounded     */
+/* once to FP32.  W_r is stored [E, d] (nn.Linear layout).                   */
+/* ------------------------------------------------------------------------ */
+int oracle_router_logits(const uint16_t *x, const float *wr, int64_t T,
+                         int32_t d, int32_t E, float *logits) {
+  if (T < 0 || d <= 0 || E <= 0) return -1;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t t = 0; t < T; ++t) {
+    const uint16_t *xr = x + t * (int64_t)d;
+    for (int32_t e = 0; e < E; ++e) {
+      const float *wrow = wr + (int64_t)e * d;
+      double acc = 0.0;
+      for (int32_t j = 0; j < d; ++j) acc += bf16_value(xr[j]) * (double)wrow[j];
+      logits[t * (int64_t)E + e] = (float)acc;
+    }
+  }
+  return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Group-limited selection.                                                  */
+/*   [SGL] grouped top-k uses sigmoid scores and an expert correction bias   */
+/*         to choose the experts; FP32 routing coefficients; the routed      */
+/*         scale is applied at combine or carried in the weights.            */
+/*   [VLLM] sigmoid scores plus a correction bias pick the best 4 of 8       */
+/*         groups, then the top 8 experts; renormalised weights x 2.5; no    */
+/*         shared expert.                                                    */
+/*   [HF]  groups ranked by the sum of each group's top two scores.          */
+/* Readings where the pages are silent:                                      */
+/*   - the group score and the expert choice use c = s + b (one FP32 add);  */
+/*   - the combine weights use s, not c (the bias only chooses);             */
+/*   - ties: the order is total on (value descending, index ascending);      */
+/*   - the scale 2.5 is carried in the FP32 weights;                         */
+/*   - slot order of the chosen experts is that same (c desc, e asc) order.  */
+/* Per token it also reports the two margins parity tests exempt on:         */
+/*   expert_margin = c(k-th chosen) - c(best unchosen candidate in the kept  */
+/*   groups), group_margin = gs(kg-th kept) - gs(best dropped group); +inf   */
+/*   when nothing is left to compare with.                                   */
+/* ------------------------------------------------------------------------ */
+static int ranks_before(float va, int32_t ia, float vb, int32_t ib) {
+  return va > vb || (va == vb && ia < ib);
+}
+
+int oracle_route(const float *logits, const float *bias, int64_t T, int32_t E,
+                 int32_t G, int32_t kg, int32_t k, float alpha, int32_t *idx,
+                 float *w, float *s_out, float *c_out, uint8_t *keep_out,
+                 double *expert_margin, double *group_margin) {
+  if (T < 0 || E <= 0 || G <= 0 || E % G != 0) return -1;
+  const int32_t S = E / G;
+  if (S < 2 || kg < 1 || kg > G || k < 1 || k > kg * S) return -1;
+  int err = 0;
+#pragma omp parallel
+  {
+    float *s = (float *)malloc(sizeof(float) * (size_t)E);
+    float *c = (float *)malloc(sizeof(float) * (size_t)E);
+    float *gs = (float *)malloc(sizeof(float) * (size_t)G);
+    uint8_t *keep = (uint8_t *)malloc((size_t)G);
+    uint8_t *taken = (uint8_t *)malloc((size_t)E);
+    if (!s || !c || !gs || !keep || !taken) {
+#pragma omp atomic write
+      err = -3;
+    } else {
+#pragma omp for schedule(static)
+      for (int64_t t = 0; t < T; ++t) {
+        const float *lg = logits + t * (int64_t)E;
+        /* scores and choice scores */
+        for (int32_t e = 0; e < E; ++e) {
+          s[e] = (float)(1.0 / (1.0 + exp(-(double)lg[e])));
+          c[e] = s[e] + bias[e];
+        }
+        /* group score = top-1 + top-2 choice score inside the group */
+        for (int32_t g = 0; g < G; ++g) {
+          int32_t b1 = -1, b2 = -1;
+          for (int32_t e = g * S; e < (g + 1) * S; ++e) {
+            if (b1 < 0 || ranks_before(c[e], e, c[b1], b1)) {
+              b2 = b1;
+              b1 = e;
+            } else if (b2 < 0 || ranks_before(c[e], e, c[b2], b2)) {
+              b2 = e;
+            }
+          }
+          gs[g] = c[b1] + c[b2];
+        }
+        /* keep the best kg groups */
+        memset(keep, 0, (size_t)G);
+        int32_t last_kept = -1;
+        for (int32_t r = 0; r < kg; ++r) {
+          int32_t best = -1;
+          for (int32_t g = 0; g < G; ++g)
+            if (!keep[g] && (best < 0 || ranks_before(gs[g], g, gs[best], best))) best = g;
+          keep[best] = 1;
+          last_kept = best;
+        }
+        {
+          int32_t next = -1;
+          for (int32_t g = 0; g < G; ++g)
+            if (!keep[g] && (next < 0 || ranks_before(gs[g], g, gs[next], next))) next = g;
+          group_margin[t] = next < 0 ? INFINITY : (double)gs[last_kept] - (double)gs[next];
+        }
+        /* top-k experts among the kept groups' members */
+        memset(taken, 0, (size_t)E);
+        double ssum = 0.0;
+        int32_t *ti = idx + t * (int64_t)k;
+        for (int32_t r = 0; r < k; ++r) {
+          int32_t best = -1;
+          for (int32_t e = 0; e < E; ++e)
+            if (keep[e / S] && !taken[e] && (best < 0 || ranks_before(c[e], e, c[best], best)))
+              best = e;
+          taken[best] = 1;
+          ti[r] = best;
+          ssum += (double)s[best];
+        }
+        {
+          int32_t next = -1;
+          for (int32_t e = 0; e < E; ++e)
+            if (keep[e / S] && !taken[e] && (next < 0 || ranks_before(c[e], e, c[next], next)))
+              next = e;
+          expert_margin[t] = next < 0 ? INFINITY : (double)c[ti[k - 1]] - (double)c[next];
+        }
+        /* renormalised weights over s, times the routed scale */
+        for (int32_t r = 0; r < k; ++r)
+          w[t * (int64_t)k + r] = (float)((double)alpha * (double)s[ti[r]] / ssum);
+        if (s_out) memcpy(s_out + t * (int64_t)E, s, sizeof(float) * (size_t)E);
+        if (c_out) memcpy(c_out + t * (int64_t)E, c, sizeof(float) * (size_t)E);
+        if (keep_out) memcpy(keep_out + t * (int64_t)G, keep, (size_t)G);
+      }
+    }
+    free(s);
+    free(c);
+    free(gs);
+    free(keep);
+    free(taken);
+  }
+  return err;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Experts and combine.                                                      */
+/*   [HF] each expert is a SwiGLU MLP of intermediate size 2560; the         */
+/*        SwiGLU product is computed in FP32; outputs are combined with the  */
+/*        normalised router weights times 2.5 ([VLLM]: no shared expert).    */
+/*   [SGL] "BF16 MoE Kernel Optimization": gate/up and activation keep BF16  */
+/*        rounding boundaries; FP32 routing weights are applied before the   */
+/*        down output is rounded; [SGL] "Fusion Optimizations": local expert */
+/*        summation, routed scaling and BF16 rounding.                       */
+/* Readings: SwiGLU(x) = silu(x W_g^T) * (x W_u^T), silu(z) = z/(1+e^-z);    */
+/* g and u are the FP32-rounded accumulators (not rounded to BF16); the      */
+/* product is rounded to FP32 and then to BF16 (h, the down GEMM's input);   */
+/* the down accumulation, the weighting and the sum over the k slots stay in */
+/* double; the output is rounded to FP32 and then to BF16.                   */
+/* Weight layouts (nn.Linear): W_g, W_u [F, d] and W_d [d, F] per expert,    */
+/* passed as one pointer per expert (NULL for experts nobody uses).          */
+/* tokens: optional list of rows to compute (NULL = all T rows); rows not    */
+/* listed are left untouched in out.                                         */
+/* ------------------------------------------------------------------------ */
+typedef struct {
+  /* BF16 weights */
+  const uint16_t *const *wg, *const *wu, *const *wd;
+  /* NVFP4 weights: packed E2M1 codes (low nibble = even column), one E4M3
+   * scale per 16 consecutive elements along K, one FP32 global scale per
+   * expert and projection. */
+  const uint8_t *const *qg, *const *qu, *const *qd;
+  const uint8_t *const *sfg, *const *sfu, *const *sfd;
+  const float *gsg, *gsu, *gsd;
+  int fp4;
+  int act_quant;
+} weights_t;
+
+/* One NVFP4 block of 16: the activation rule used on both GEMM inputs of the
+ * NVFP4 path (global scale 1): scale = E4M3(amax / 6), code_i =
+ * E2M1(v_i / scale) with FP32 divisions, all-zero codes when the scale
+ * rounds to 0.  Writes the dequantised values. */
+static void nvfp4_block_roundtrip(const float *v, double *out16) {
+  float amax = 0.0f;
+  for (int i = 0; i < 16; ++i) {
+    float a = fabsf(v[i]);
+    if (a > amax) amax = a;
+  }
+  uint8_t sf = e4m3_encode(amax / 6.0f);
+  float scale = (float)e4m3_value(sf);
+  for (int i = 0; i < 16; ++i) {
+    uint8_t q = scale > 0.0f ? e2m1_encode(v[i] / scale) : 0;
+    out16[i] = e2m1_value(q) * (double)scale;
+  }
+}
+
+static double fp4_weight(const uint8_t *q, const uint8_t *sf, float gs,
+                         int64_t row, int64_t col, int64_t K) {
+  int64_t flat = row * K + col;
+  uint8_t byte = q[flat >> 1];
+  uint8_t code = (flat & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 15u);
+  return e2m1_value(code) * e4m3_value(sf[row * (K / 16) + col / 16]) * (double)gs;
+}
+
+static int experts_impl(const uint16_t *x, int64_t T, int32_t d, int32_t F,
+                        int32_t k, int32_t E, const int32_t *idx, const float *w,
+                        const weights_t *W, const int64_t *tokens,
+                        int64_t n_tokens, uint16_t *out) {
+  if (T < 0 || d <= 0 || F <= 0 || k <= 0 || (d % 16) || (F % 16)) return -1;
+  const int64_t n = tokens ? n_tokens : T;
+  int err = 0;
+  /* every referenced expert must have its weights */
+  for (int64_t i = 0; i < n && !err; ++i) {
+    int64_t t = tokens ? tokens[i] : i;
+    if (t < 0 || t >= T) { err = -1; break; }
+    for (int32_t j = 0; j < k; ++j) {
+      int32_t e = idx[t * k + j];
+      if (e < 0 || e >= E) { err = -1; break; }
+      if (W->fp4 ? (!W->qg[e] || !W->qu[e] || !W->qd[e]) : (!W->wg[e] || !W->wu[e] || !W->wd[e])) {
+        err = -2;
+        break;
+      }
+    }
+  }
+  if (err) return err;
+#pragma omp parallel
+  {
+    double *xin = (double *)malloc(sizeof(double) * (size_t)d);
+    float *hf = (float *)malloc(sizeof(float) * (size_t)F);
+    double *hin = (double *)malloc(sizeof(double) * (size_t)F);
+    double *acc = (double *)malloc(sizeof(double) * (size_t)d);
+    float *tmp = (float *)malloc(sizeof(float) * (size_t)(d > F ? d : F));
+    if (!xin || !hf || !hin || !acc || !tmp) {
+#pragma omp atomic write
+      err = -3;
+    } else {
+#pragma omp for schedule(dynamic, 1)
+      for (int64_t i = 0; i < n; ++i) {
+        int64_t t = tokens ? tokens[i] : i;
+        const uint16_t *xr = x + t * (int64_t)d;
+        /* the expert input row (NVFP4 path may quantise it) */
+        if (W->fp4 && W->act_quant) {
+          for (int32_t j = 0; j < d; ++j) tmp[j] = (float)bf16_value(xr[j]);
+          for (int32_t j = 0; j < d; j += 16) nvfp4_block_roundtrip(tmp + j, xin + j);
+        } else {
+          for (int32_t j = 0; j < d; ++j) xin[j] = bf16_value(xr[j]);
+        }
+        for (int32_t j = 0; j < d; ++j) acc[j] = 0.0;
+        for (int32_t slot = 0; slot < k; ++slot) {
+          const int32_t e = idx[t * k + slot];
+          const double wt = (double)w[t * k + slot];
+          /* gate/up accumulators (FP32) and the SwiGLU product (FP32) */
+          for (int32_t f = 0; f < F; ++f) {
+            double ga = 0.0, ua = 0.0;
+            if (W->fp4) {
+              for (int32_t j = 0; j < d; ++j) {
+                ga += xin[j] * fp4_weight(W->qg[e], W->sfg[e], W->gsg[e], f, j, d);
+                ua += xin[j] * fp4_weight(W->qu[e], W->sfu[e], W->gsu[e], f, j, d);
+              }
+            } else {
+              const uint16_t *gr = W->wg[e] + (int64_t)f * d;
+              const uint16_t *ur = W->wu[e] + (int64_t)f * d;
+              for (int32_t j = 0; j < d; ++j) {
+                ga += xin[j] * bf16_value(gr[j]);
+                ua += xin[j] * bf16_value(ur[j]);
+              }
+            }
+            const double g = (double)(float)ga;
+            const double u = (double)(float)ua;
+            const double silu = g / (1.0 + exp(-g));
+            hf[f] = (float)(silu * u);
+          }
+          /* the down GEMM's input */
+          if (W->fp4 && W->act_quant) {
+            for (int32_t f = 0; f < F; f += 16) nvfp4_block_roundtrip(hf + f, hin + f);
+          } else {
+            for (int32_t f = 0; f < F; ++f) hin[f] = bf16_value(bf16_round(hf[f]));
+          }
+          /* down projection, weighted, summed over the slots in double */
+          for (int32_t r = 0; r < d; ++r) {
+            double ya = 0.0;
+            if (W->fp4) {
+              for (int32_t f = 0; f < F; ++f)
+                ya += hin[f] * fp4_weight(W->qd[e], W->sfd[e], W->gsd[e], r, f, F);
+            } else {
+              const uint16_t *dr = W->wd[e] + (int64_t)r * F;
+              for (int32_t f = 0; f < F; ++f) ya += hin[f] * bf16_value(dr[f]);
+            }
+            acc[r] += wt * ya;
+          }
+        }
+        for (int32_t r = 0; r < d; ++r) out[t * (int64_t)d + r] = bf16_round((float)acc[r]);
+      }
+    }
+    free(xin);
+    free(hf);
+    free(hin);
+    free(acc);
+    free(tmp);
+  }
+  return err;
+}
+
+int oracle_experts_bf16(const uint16_t *x, int64_t T, int32_t d, int32_t F,
+                        int32_t k, int32_t E, const int32_t *idx, const float *w,
+                        const uint16_t *const *wg, const uint16_t *const *wu,
+                        const uint16_t *const *wd, const int64_t *tokens,
+                        int64_t n_tokens, uint16_t *out) {
+  weights_t W;
+  memset(&W, 0, sizeof W);
+  W.wg = wg;
+  W.wu = wu;
+  W.wd = wd;
+  return experts_impl(x, T, d, F, k, E, idx, w, &W, tokens, n_tokens, out);
+}
+
+/* NVFP4 experts ([SGL] Highlights: "ModelOpt NVFP4" checkpoints; [VLLM]:
+ * the 256 routed experts are NVFP4).  Each weight is the exact product
+ * E2M1 code x E4M3 block scale x FP32 global scale.  act_quant = 1 also
+ * quantises both GEMM inputs (x along d, the FP32 SwiGLU product along F) to
+ * NVFP4 with the per-16 rule of nvfp4_block_roundtrip (the "quantization"
+ * step of the NVFP4 MoE path, vLLM post, section "The fused graph");
+ * act_quant = 0 keeps BF16 activations exactly as in the BF16 path. */
+int oracle_experts_nvfp4(const uint16_t *x, int64_t T, int32_t d, int32_t F,
+                         int32_t k, int32_t E, const int32_t *idx, const float *w,
+                         const uint8_t *const *qg, const uint8_t *const *sfg, const float *gsg,
+                         const uint8_t *const *qu, const uint8_t *const *sfu, const float *gsu,
+                         const uint8_t *const *qd, const uint8_t *const *sfd, const float *gsd,
+                         int32_t act_quant, const int64_t *tokens, int64_t n_tokens,
+                         uint16_t *out) {
+  weights_t W;
+  memset(&W, 0, sizeof W);
+  W.qg = qg; W.sfg = sfg; W.gsg = gsg;
+  W.qu = qu; W.sfu = sfu; W.gsu = gsu;
+  W.qd = qd; W.sfd = sfd; W.gsd = gsd;
+  W.fp4 = 1;
+  W.act_quant = act_quant;
+  return experts_impl(x, T, d, F, k, E, idx, w, &W, tokens, n_tokens, out);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Scalar entry points for the pins.                                         */
+/* ------------------------------------------------------------------------ */
+double oracle_e2m1_value(uint8_t code) { return e2m1_value(code); }
+double oracle_e4m3_value(uint8_t code) { return e4m3_value(code); }
+uint8_t oracle_e2m1_encode(float v) { return e2m1_encode(v); }
+uint8_t oracle_e4m3_encode(float v) { return e4m3_encode(v); }
+uint16_t oracle_bf16_round(float v) { return bf16_round(v); }
+
+/* NVFP4 activation quantiser on a row of n values (n % 16 == 0): packed codes
+ * (low nibble = even index) and one E4M3 scale per 16. */
+int oracle_nvfp4_quantize(const float *v, int64_t n, uint8_t *q, uint8_t *sf) {
+  if (n < 0 || n % 16) return -1;
+  for (int64_t b = 0; b < n / 16; ++b) {
+    float amax = 0.0f;
+    for (int i = 0; i < 16; ++i) {
+      float a = fabsf(v[b * 16 + i]);
+      if (a > amax) amax = a;
+    }
+    sf[b] = e4m3_encode(amax / 6.0f);
+    float scale = (float)e4m3_value(sf[b]);
+    for (int i = 0; i < 16; i += 2) {
+      uint8_t lo = scale > 0.0f ? e2m1_encode(v[b * 16 + i] / scale) : 0;
+      uint8_t hi = scale > 0.0f ? e2m1_encode(v[b * 16 + i + 1] / scale) : 0;
+      q[(b * 16 + i) / 2] = (uint8_t)(lo | (hi << 4));
+    }
+  }
+  return 0;
+}
+
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}
+
+void oracle_set_threads(int n) {
+#ifdef _OPENMP
+  if (n > 0) omp_set_num_threads(n);
+#else
+  (void)n;
+#endif
+}

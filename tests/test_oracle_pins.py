@@ -1,0 +1,356 @@
+"""Pins for the CPU oracle: each test checks the oracle against something other
+than itself -- a library routine, brute force, a closed form, an invariant or
+a special case the pages fix.  CPU only."""
+import itertools
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from group_limited_routed_gb300 import inputs
+
+RNG = np.random.default_rng(1234)
+
+
+def f32_ulp_close(a, b, ulps=1):
+    a = np.asarray(a, np.float32)
+    b = np.asarray(b, np.float32)
+    sp = np.spacing(np.maximum(np.abs(a), np.abs(b))).astype(np.float64)
+    return np.all(np.abs(a.astype(np.float64) - b.astype(np.float64)) <= ulps * sp)
+
+
+# ---------------------------------------------------------------- formats
+def test_bf16_round_matches_torch():
+    vals = np.concatenate([
+        RNG.standard_normal(20000).astype(np.float32) * np.float32(3.0),
+        RNG.standard_normal(2000).astype(np.float32) * np.float32(1e-30),
+        # exact ties: lower 16 bits == 0x8000 with both parities of the kept lsb
+        (np.arange(0x3f800000, 0x3f800000 + 64 * 0x10000, 0x10000, dtype=np.uint32)
+         + np.uint32(0x8000)).view(np.float32),
+        np.array([0.0, -0.0, 1.0, -1.0, 3.3895314e38, np.inf, -np.inf], np.float32),
+    ])
+    got = np.array([oracle.bf16_round(float(v)) for v in vals], np.uint16)
+    ref = torch.from_numpy(vals).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(got, ref)
+
+
+def _minifloat(code, ebits, mbits, bias):
+    """Generic minifloat decoder (sign | exponent | mantissa), no inf/nan."""
+    sign = -1.0 if code >> (ebits + mbits) & 1 else 1.0
+    e = (code >> mbits) & ((1 << ebits) - 1)
+    m = code & ((1 << mbits) - 1)
+    if e == 0:
+        return sign * (m / (1 << mbits)) * 2.0 ** (1 - bias)
+    return sign * (1 + m / (1 << mbits)) * 2.0 ** (e - bias)
+
+
+def test_e2m1_values_from_format_definition():
+    for c in range(16):
+        assert oracle.e2m1_value(c) == _minifloat(c, 2, 1, 1)
+    mags = sorted({abs(oracle.e2m1_value(c)) for c in range(16)})
+    assert mags == [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+
+
+def test_e4m3_all_256_codes_vs_torch():
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    ref = codes.view(torch.float8_e4m3fn).float().numpy()
+    for c in range(256):
+        v = oracle.e4m3_value(c)
+        if math.isnan(ref[c]):
+            assert math.isnan(v), c
+        else:
+            assert v == float(ref[c]), (c, v, ref[c])
+
+
+def test_e4m3_encode_vs_torch_rne():
+    v = np.concatenate([
+        np.exp(RNG.uniform(np.log(2.0 ** -12), np.log(448.0), 20000)).astype(np.float32),
+        # midpoints between neighbouring codes (ties)
+        np.array([(oracle.e4m3_value(c) + oracle.e4m3_value(c + 1)) / 2 for c in range(0, 126)],
+                 np.float32),
+        np.array([0.0, 448.0, 2.0 ** -9, 2.0 ** -10], np.float32),
+    ])
+    got = np.array([oracle.e4m3_encode(float(x)) for x in v], np.uint8)
+    ref = torch.from_numpy(v).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(got, ref)
+    # satfinite above the largest finite value, sign kept
+    assert oracle.e4m3_encode(1000.0) == 0x7E
+    assert oracle.e4m3_encode(-1000.0) == 0xFE
+
+
+def test_e2m1_encode_vs_independent_rounding():
+    grid = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+    mids = (grid[1:] + grid[:-1]) / 2
+    v = np.concatenate([RNG.uniform(-7, 7, 5000), mids, -mids, grid, -grid[1:], [6.5, -9.0]])
+    v = v.astype(np.float32)
+    got = np.array([oracle.e2m1_encode(float(x)) for x in v], np.uint8)
+    ref = inputs._e2m1_codes(torch.from_numpy(v)).numpy()
+    # +0 and -0 decode alike; compare the decoded values and the codes elsewhere
+    dec_got = np.array([oracle.e2m1_value(int(c)) for c in got])
+    dec_ref = np.array([oracle.e2m1_value(int(c)) for c in ref])
+    assert np.array_equal(dec_got, dec_ref)
+    nz = dec_got != 0
+    assert np.array_equal(got[nz], ref[nz])
+    # ties go to the even code: 0.25->0, 0.75->1.0, 1.25->1.0, 1.75->2, 2.5->2, 3.5->4, 5->4
+    for x, want in [(0.25, 0.0), (0.75, 1.0), (1.25, 1.0), (1.75, 2.0), (2.5, 2.0), (3.5, 4.0),
+                    (5.0, 4.0), (7.0, 6.0)]:
+        assert oracle.e2m1_value(oracle.e2m1_encode(x)) == want
+
+
+def test_nvfp4_activation_quantizer_vs_torch():
+    v = (RNG.standard_normal(16 * 512) * np.repeat(np.exp(RNG.uniform(-6, 3, 512)), 16))
+    v = v.astype(np.float32)
+    v[:16] = 0.0                      # an all-zero block
+    q, sf = oracle.nvfp4_quantize(v)
+    tv = torch.from_numpy(v).reshape(-1, 16)
+    amax = tv.abs().amax(dim=1)
+    sf_ref = (amax / 6.0).to(torch.float8_e4m3fn)
+    scale = sf_ref.float().unsqueeze(1)
+    codes_ref = torch.where(scale > 0, inputs._e2m1_codes(tv / torch.where(scale > 0, scale, 1.0)),
+                            torch.zeros_like(tv, dtype=torch.uint8))
+    assert np.array_equal(sf, sf_ref.view(torch.uint8).numpy())
+    codes = np.stack([q & 15, q >> 4], axis=1).reshape(-1)
+    dec = np.array([oracle.e2m1_value(int(c)) for c in codes])
+    dec_ref = np.array([oracle.e2m1_value(int(c)) for c in codes_ref.reshape(-1).numpy()])
+    assert np.array_equal(dec, dec_ref)
+
+
+# ---------------------------------------------------------------- router
+def _bf16_matrix(shape, scale=1.0):
+    a = torch.from_numpy((RNG.standard_normal(shape) * scale).astype(np.float32))
+    return a.to(torch.bfloat16)
+
+
+def test_router_logits_vs_numpy_fp64():
+    x = _bf16_matrix((37, 512))
+    wr = (RNG.standard_normal((64, 512)) / np.sqrt(512)).astype(np.float32)
+    got = oracle.router_logits(inputs.bf16_bits(x), wr)
+    ref = (x.double().numpy() @ wr.astype(np.float64).T).astype(np.float32)
+    assert f32_ulp_close(got, ref, 1)
+
+
+def test_router_one_hot_picks_a_weight_column():
+    d, E = 256, 32
+    wr = (RNG.standard_normal((E, d))).astype(np.float32)
+    x = torch.zeros(d, d, dtype=torch.bfloat16)
+    x[torch.arange(d), torch.arange(d)] = 1.0
+    got = oracle.router_logits(inputs.bf16_bits(x), wr)
+    assert np.array_equal(got, wr.T)
+
+
+# ---------------------------------------------------------------- selection
+def _route(logits, bias, G, kg, k, alpha=2.5):
+    return oracle.route(logits.astype(np.float32), bias.astype(np.float32), G, kg, k, alpha)
+
+
+def test_sigmoid_scores_vs_scipy():
+    from scipy.special import expit
+    lg = np.concatenate([RNG.standard_normal((50, 64)) * 4, np.zeros((1, 64))]).astype(np.float32)
+    r = _route(lg, np.zeros(64), 8, 4, 8)
+    ref = expit(lg.astype(np.float64)).astype(np.float32)
+    assert f32_ulp_close(r["s"], ref, 1)
+    assert np.all(r["s"][-1] == np.float32(0.5))
+
+
+def _brute_force(c, G, kg, k):
+    """Best kg groups by the sum of the group scores (each the best pair sum
+    in the group), then best k experts by the sum of their c."""
+    E = c.size
+    S = E // G
+    gs = []
+    for g in range(G):
+        m = c[g * S:(g + 1) * S]
+        gs.append(max(np.float32(m[i]) + np.float32(m[j])
+                      for i in range(S) for j in range(S) if i != j))
+    best_groups = max(itertools.combinations(range(G), kg),
+                      key=lambda sub: sum(float(gs[g]) for g in sub))
+    cand = [e for e in range(E) if e // S in best_groups]
+    best = max(itertools.combinations(cand, k), key=lambda sub: sum(float(c[e]) for e in sub))
+    return set(best_groups), set(best)
+
+
+@pytest.mark.parametrize("E,G,kg,k", [(16, 8, 4, 3), (32, 4, 2, 4), (24, 6, 3, 5), (64, 8, 4, 8)])
+def test_selection_brute_force(E, G, kg, k):
+    T = 40 if E < 64 else 6
+    lg = (RNG.standard_normal((T, E)) * 1.5).astype(np.float32)
+    bias = RNG.uniform(-0.05, 0.05, E).astype(np.float32)
+    r = _route(lg, bias, G, kg, k)
+    for t in range(T):
+        if E == 64:
+            # C(32,8) subsets is too many: brute-force the groups only, then
+            # check the experts are the k best candidates by a sort.
+            S = E // G
+            gsets, _ = _brute_force(r["c"][t], G, kg, 1)
+            cand = np.array([e for e in range(E) if e // S in gsets])
+            order = cand[np.argsort(-r["c"][t][cand], kind="stable")]
+            assert set(r["idx"][t]) == set(order[:k])
+        else:
+            gsets, eset = _brute_force(r["c"][t], G, kg, k)
+            assert set(np.nonzero(r["keep"][t])[0]) == gsets
+            assert set(r["idx"][t]) == eset
+
+
+def test_keep_all_groups_is_plain_topk():
+    E, G, k = 64, 8, 8
+    lg = (RNG.standard_normal((100, E)) * 2).astype(np.float32)
+    bias = RNG.uniform(-0.05, 0.05, E).astype(np.float32)
+    r = _route(lg, bias, G, G, k)
+    ref = np.argsort(-r["c"], axis=1, kind="stable")[:, :k]
+    assert np.array_equal(r["idx"], ref)
+    assert np.all(np.isinf(r["group_margin"]))
+
+
+def test_all_equal_scores_tie_rule():
+    for E, G in [(64, 8), (256, 8)]:
+        r = _route(np.zeros((3, E)), np.zeros(E), G, 4, 8)
+        assert np.array_equal(r["idx"], np.tile(np.arange(8), (3, 1)))
+        assert np.array_equal(r["keep"], np.tile(np.arange(G) < 4, (3, 1)))
+        assert np.all(r["w"] == np.float32(2.5 / 8))
+        assert np.all(r["expert_margin"] == 0) and np.all(r["group_margin"] == 0)
+
+
+def test_combine_weights_use_scores_not_bias():
+    from scipy.special import expit
+    E = 64
+    lg = (RNG.standard_normal((20, E))).astype(np.float32)
+    bias = RNG.uniform(-0.05, 0.05, E).astype(np.float32)
+    bias[:8] += 3.0       # forces the choice, must not leak into the weights
+    r = _route(lg, bias, 8, 4, 8)
+    s = expit(lg.astype(np.float64))
+    sel = np.take_along_axis(s, r["idx"].astype(np.int64), 1)
+    ref = 2.5 * sel / sel.sum(1, keepdims=True)
+    assert np.allclose(r["w"], ref, rtol=2e-7, atol=0)
+    assert np.all(np.sort(r["idx"], 1) == np.arange(8))
+
+
+def test_invariants_on_tiny_config():
+    cfg = inputs.CONFIGS["tiny"]
+    t = inputs.generate(cfg, "cpu", weights=False)
+    lg = oracle.router_logits(inputs.bf16_bits(t["hidden"]), t["router_w"].numpy())
+    r = oracle.route(lg, t["corr_bias"].numpy(), cfg.n_groups, cfg.topk_groups, cfg.topk,
+                     cfg.routed_scale)
+    S = cfg.n_experts // cfg.n_groups
+    idx = r["idx"]
+    for row, keep in zip(idx, r["keep"]):
+        assert len(set(row)) == cfg.topk
+        assert all(keep[e // S] for e in row)
+        assert keep.sum() == cfg.topk_groups
+    assert np.all(r["w"] > 0)
+    assert np.all(np.abs(r["w"].astype(np.float64).sum(1) - 2.5) <= 1e-6)
+    assert np.all(r["expert_margin"] >= 0) and np.all(r["group_margin"] >= 0)
+    # slots in descending choice score
+    cs = np.take_along_axis(r["c"], idx.astype(np.int64), 1)
+    assert np.all(np.diff(cs, axis=1) <= 0)
+
+
+# ---------------------------------------------------------------- experts
+def _torch_expert(x, wg, wu, wd):
+    """Dense SwiGLU expert in float64 with the layer's rounding points,
+    using torch's matmul and silu."""
+    g = (x.double() @ wg.double().T).float().double()
+    u = (x.double() @ wu.double().T).float().double()
+    h = (torch.nn.functional.silu(g) * u).float().to(torch.bfloat16)
+    return h.double() @ wd.double().T
+
+
+def _tiny_weights(E, F, d):
+    wg = _bf16_matrix((E, F, d), 0.02)
+    wu = _bf16_matrix((E, F, d), 0.02)
+    wd = _bf16_matrix((E, d, F), 0.02)
+    return wg, wu, wd
+
+
+def test_identical_experts_closed_form():
+    T, d, F, E = 12, 128, 64, 16
+    x = _bf16_matrix((T, d))
+    wg, wu, wd = _tiny_weights(1, F, d)
+    wg, wu, wd = (a.expand(E, *a.shape[1:]).contiguous() for a in (wg, wu, wd))
+    lg = (RNG.standard_normal((T, E))).astype(np.float32)
+    r = _route(lg, RNG.uniform(-0.05, 0.05, E), 8, 4, 4)
+    out = oracle.experts_bf16(inputs.bf16_bits(x), r["idx"], r["w"], inputs.bf16_bits(wg),
+                              inputs.bf16_bits(wu), inputs.bf16_bits(wd), E)
+    y = _torch_expert(x, wg[0], wu[0], wd[0])
+    ref = (2.5 * y).float().to(torch.bfloat16)
+    got = torch.from_numpy(out.view(np.int16)).view(torch.bfloat16)
+    # the weights sum to 2.5 up to FP32 rounding: at most one BF16 step apart
+    diff = (got.float() - ref.float()).abs()
+    assert torch.all(diff <= ref.float().abs() * 2 ** -7 + 1e-30)
+    assert (got == ref).float().mean() > 0.97
+
+
+def test_forced_routing_matches_dense_torch_experts():
+    T, d, F, E, G = 10, 128, 64, 32, 8
+    x = _bf16_matrix((T, d))
+    wg, wu, wd = _tiny_weights(E, F, d)
+    chosen = [1, 2, 9, 10, 17, 18, 30, 31]          # groups 0, 2, 4, 7 (S=4)
+    bias = RNG.uniform(-0.05, 0.05, E).astype(np.float32)
+    bias[chosen] += 10.0
+    lg = oracle.router_logits(inputs.bf16_bits(x), (RNG.standard_normal((E, d)) / 12).astype(np.float32))
+    r = _route(lg, bias, G, 4, 8)
+    assert np.all(np.sort(r["idx"], 1) == chosen)
+    out = oracle.experts_bf16(inputs.bf16_bits(x), r["idx"], r["w"], inputs.bf16_bits(wg),
+                              inputs.bf16_bits(wu), inputs.bf16_bits(wd), E)
+    ref = torch.zeros(T, d, dtype=torch.float64)
+    for t in range(T):
+        for j in range(8):
+            e = int(r["idx"][t, j])
+            ref[t] += float(r["w"][t, j]) * _torch_expert(x[t:t + 1], wg[e], wu[e], wd[e])[0]
+    ref16 = ref.float().to(torch.bfloat16)
+    got = torch.from_numpy(out.view(np.int16)).view(torch.bfloat16)
+    diff = (got.float() - ref16.float()).abs()
+    assert torch.all(diff <= ref16.float().abs() * 2 ** -7 + 1e-6)
+    assert (got == ref16).float().mean() > 0.97
+
+
+def test_token_subset_matches_full_run():
+    T, d, F, E = 9, 64, 32, 16
+    x = _bf16_matrix((T, d))
+    wg, wu, wd = _tiny_weights(E, F, d)
+    r = _route(RNG.standard_normal((T, E)), np.zeros(E), 8, 4, 4)
+    args = (inputs.bf16_bits(x), r["idx"], r["w"], inputs.bf16_bits(wg), inputs.bf16_bits(wu),
+            inputs.bf16_bits(wd), E)
+    full = oracle.experts_bf16(*args)
+    sub = oracle.experts_bf16(*args, tokens=np.array([7, 2]))
+    assert np.array_equal(sub[[2, 7]], full[[2, 7]])
+    assert np.all(sub[[0, 1, 3, 4, 5, 6, 8]] == 0)
+
+
+def test_nvfp4_weights_equal_bf16_when_exactly_representable():
+    """E2M1 (2 significant bits) x E4M3 (4 bits) x a power of two fits BF16's
+    8 bits exactly, so with BF16 activations both oracle paths agree bit for bit."""
+    T, d, F, E = 6, 64, 32, 8
+    x = _bf16_matrix((T, d))
+    r = _route(RNG.standard_normal((T, E)), np.zeros(E), 4, 2, 3)
+    gate, up, down, deq = {}, {}, {}, {}
+    for name, (n, kk), dst in (("g", (F, d), gate), ("u", (F, d), up), ("d", (d, F), down)):
+        q = RNG.integers(0, 256, (E, n, kk // 2), dtype=np.uint8)
+        sf = RNG.integers(0x20, 0x48, (E, n, kk // 16), dtype=np.uint8)   # normal, modest scales
+        gs = np.full(E, 2.0 ** -9, np.float32)
+        dst.update(q=q, sf=sf, gs=gs)
+        codes = np.stack([q & 15, q >> 4], -1).reshape(E, n, kk)
+        val = np.vectorize(oracle.e2m1_value)(codes) * np.repeat(
+            np.vectorize(oracle.e4m3_value)(sf), 16, axis=2) * 2.0 ** -9
+        t = torch.from_numpy(val).to(torch.bfloat16)
+        assert torch.equal(t.double(), torch.from_numpy(val))
+        deq[name] = inputs.bf16_bits(t)
+    a = oracle.experts_nvfp4(inputs.bf16_bits(x), r["idx"], r["w"], gate, up, down, E,
+                             act_quant=False)
+    b = oracle.experts_bf16(inputs.bf16_bits(x), r["idx"], r["w"], deq["g"], deq["u"], deq["d"], E)
+    assert np.array_equal(a, b)
+
+
+def test_nvfp4_generator_weights_round_trip_grid_values():
+    """Weights already on an NVFP4 grid come back unchanged from the
+    checkpoint quantiser the generator uses."""
+    n, kk = 8, 64
+    codes = torch.from_numpy(RNG.integers(0, 16, (n, kk)).astype(np.uint8))
+    vals = torch.tensor([oracle.e2m1_value(int(c)) for c in codes.reshape(-1)]).reshape(n, kk)
+    vals[:, ::16] = 6.0                   # every block hits the grid's top value
+    w = (vals * 2.0 ** -6).float()
+    q, sf, gs = inputs.quantize_nvfp4_weight(w)
+    dec = np.stack([q.numpy() & 15, q.numpy() >> 4], -1).reshape(n, kk)
+    back = np.vectorize(oracle.e2m1_value)(dec) * np.repeat(
+        np.vectorize(oracle.e4m3_value)(sf.numpy()), 16, 1) * float(gs)
+    assert np.allclose(back, w.double().numpy(), rtol=1e-6, atol=0)
