@@ -11,9 +11,9 @@ from .config import BeamMoEConfig  # noqa: F401
 def __getattr__(name):
     # the binding is loaded lazily so that the input generator can be imported
     # on machines without the compiled library
-    if name in ("route", "forward", "forward_routed", "forward_nvfp4", "workspace_size",
-                "Workspace", "check_status", "BeamError", "library_path", "topk_from_logits",
-                "set_stage_events", "layout"):
+    if name in ("route", "select", "forward", "forward_routed", "workspace_size", "Workspace",
+                "check_status", "BeamError", "library_path", "lib", "set_stage_events",
+                "set_debug", "layout", "kernels_per_forward", "EXPORTS"):
         from . import api
         return getattr(api, name)
     raise AttributeError(name)

@@ -1,0 +1,261 @@
+"""Thin Python binding of libbeam_moe.so (argument marshalling only).
+
+Every step of the layer runs in the library's CUDA kernels; this module only
+checks tensor dtypes/devices, hands raw device pointers and the current torch
+stream to the C ABI, and raises ``BeamError`` on a non-OK status.  There is no
+fallback: without the compiled library every entry point raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from .config import BeamMoEConfig, CConfig
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "_build", "libbeam_moe.so")
+_lock = threading.Lock()
+_lib = None
+
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_SZ = ctypes.c_size_t
+_ST = ctypes.c_int
+
+STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "workspace too small",
+          4: "CUDA error", 5: "device-side wait timed out", 6: "device-side check failed"}
+
+EXPORTS = ("beam_moe_workspace_size", "beam_moe_workspace_layout", "beam_moe_route",
+           "beam_moe_select", "beam_moe_forward", "beam_moe_forward_routed",
+           "beam_moe_check_status", "beam_moe_set_stage_events", "beam_moe_set_debug",
+           "beam_moe_kernels_per_forward", "beam_status_string")
+
+
+class BeamError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        super().__init__(f"{where}: {STATUS.get(code, 'unknown')} (status {code})")
+        self.code = code
+
+
+class _Layout(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_size_t) for n in (
+        "status", "logits", "topk_idx", "topk_w", "counts", "offsets", "perm_src", "pair_row",
+        "perm_w", "x_perm", "h", "y", "total")]
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def lib():
+    """Load libbeam_moe.so; raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(
+                f"{_LIB_PATH} is missing: build it with group_limited_routed_gb300.build.build() "
+                "(there is no non-CUDA fallback)")
+        L = ctypes.CDLL(_LIB_PATH)
+        cfgp = ctypes.POINTER(CConfig)
+        L.beam_moe_workspace_size.argtypes = [cfgp, _I64, ctypes.c_int32]
+        L.beam_moe_workspace_size.restype = _SZ
+        L.beam_moe_workspace_layout.argtypes = [cfgp, _I64, ctypes.c_int32, ctypes.POINTER(_Layout)]
+        L.beam_moe_workspace_layout.restype = _ST
+        L.beam_moe_route.argtypes = [cfgp, _P, _P, _P, _I64, _P, _P, _P, _P, _SZ, _P]
+        L.beam_moe_route.restype = _ST
+        L.beam_moe_select.argtypes = [cfgp, _P, _P, _I64, _P, _P, _P, _SZ, _P]
+        L.beam_moe_select.restype = _ST
+        L.beam_moe_forward.argtypes = [cfgp, _P, _P, _P, _P, _P, _P, _P, _I64, _P, _SZ, _P]
+        L.beam_moe_forward.restype = _ST
+        L.beam_moe_forward_routed.argtypes = [cfgp, _P, _P, _P, _P, _P, _P, _P, _I64, _P, _SZ, _P]
+        L.beam_moe_forward_routed.restype = _ST
+        L.beam_moe_check_status.argtypes = [_P, _P]
+        L.beam_moe_check_status.restype = _ST
+        L.beam_moe_set_stage_events.argtypes = [ctypes.POINTER(_P), ctypes.c_int32]
+        L.beam_moe_set_stage_events.restype = _ST
+        L.beam_moe_set_debug.argtypes = [ctypes.c_uint32, ctypes.c_int32]
+        L.beam_moe_set_debug.restype = _ST
+        L.beam_moe_kernels_per_forward.argtypes = [cfgp, _I64]
+        L.beam_moe_kernels_per_forward.restype = ctypes.c_int32
+        L.beam_status_string.argtypes = [_ST]
+        L.beam_status_string.restype = ctypes.c_char_p
+        _lib = L
+        return L
+
+
+def _cfg(cfg) -> CConfig:
+    return CConfig.of(cfg)
+
+
+def _check(code: int, where: str):
+    if code != 0:
+        raise BeamError(code, where)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _dev(t: torch.Tensor, dtype, name: str) -> int:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def workspace_size(cfg, T_max: int, weight_fmt: int = 0) -> int:
+    c = _cfg(cfg)
+    n = lib().beam_moe_workspace_size(ctypes.byref(c), int(T_max), int(weight_fmt))
+    if n == 0:
+        raise BeamError(1, "beam_moe_workspace_size")
+    return int(n)
+
+
+def layout(cfg, T_max: int, weight_fmt: int = 0) -> dict:
+    c = _cfg(cfg)
+    out = _Layout()
+    _check(lib().beam_moe_workspace_layout(ctypes.byref(c), int(T_max), int(weight_fmt),
+                                           ctypes.byref(out)), "beam_moe_workspace_layout")
+    return {n: int(getattr(out, n)) for n, _ in _Layout._fields_}
+
+
+class Workspace:
+    """Caller-owned device workspace sized for up to T_max tokens."""
+
+    def __init__(self, cfg, T_max: int, device=None, weight_fmt: int = 0):
+        self.cfg = cfg
+        self.T_max = int(T_max)
+        self.nbytes = workspace_size(cfg, T_max, weight_fmt)
+        self.buf = torch.zeros(self.nbytes, dtype=torch.uint8,
+                               device=device if device is not None else torch.device("cuda"))
+        self.layout = layout(cfg, T_max, weight_fmt)
+
+    @property
+    def ptr(self) -> int:
+        return self.buf.data_ptr()
+
+    def view(self, name: str, dtype, shape) -> torch.Tensor:
+        """A tensor view of one intermediate buffer (see beam_moe_ws_layout_t)."""
+        off = self.layout[name]
+        n = 1
+        for s in shape:
+            n *= int(s)
+        nbytes = n * torch.tensor([], dtype=dtype).element_size()
+        return self.buf[off:off + nbytes].view(dtype).view(*shape)
+
+
+def _ws(cfg, T, ws, device):
+    if ws is None:
+        ws = Workspace(cfg, max(int(T), 1), device)
+    return ws
+
+
+def route(cfg, hidden, router_w, corr_bias, ws: Workspace | None = None, want_logits=False,
+          stream=None):
+    """Router + group-limited selection -> (idx [T,k] int32, w [T,k] f32[, logits])."""
+    T = hidden.shape[0]
+    ws = _ws(cfg, T, ws, hidden.device)
+    idx = torch.empty(T, cfg.topk, dtype=torch.int32, device=hidden.device)
+    w = torch.empty(T, cfg.topk, dtype=torch.float32, device=hidden.device)
+    logits = torch.empty(T, cfg.n_experts, dtype=torch.float32, device=hidden.device) \
+        if want_logits else None
+    c = _cfg(cfg)
+    _check(lib().beam_moe_route(ctypes.byref(c), _dev(hidden, torch.bfloat16, "hidden"),
+                                _dev(router_w, torch.float32, "router_w"),
+                                _dev(corr_bias, torch.float32, "corr_bias"), T, idx.data_ptr(),
+                                w.data_ptr(), None if logits is None else logits.data_ptr(),
+                                ws.ptr, ws.nbytes, _stream(stream)), "beam_moe_route")
+    return (idx, w, logits) if want_logits else (idx, w)
+
+
+def select(cfg, logits, corr_bias, ws: Workspace | None = None, stream=None):
+    """Selection alone on given FP32 logits -> (idx, w)."""
+    T = logits.shape[0]
+    ws = _ws(cfg, T, ws, logits.device)
+    idx = torch.empty(T, cfg.topk, dtype=torch.int32, device=logits.device)
+    w = torch.empty(T, cfg.topk, dtype=torch.float32, device=logits.device)
+    c = _cfg(cfg)
+    _check(lib().beam_moe_select(ctypes.byref(c), _dev(logits, torch.float32, "logits"),
+                                 _dev(corr_bias, torch.float32, "corr_bias"), T, idx.data_ptr(),
+                                 w.data_ptr(), ws.ptr, ws.nbytes, _stream(stream)),
+           "beam_moe_select")
+    return idx, w
+
+
+def forward(cfg, hidden, router_w, corr_bias, w_gate, w_up, w_down, out=None,
+            ws: Workspace | None = None, stream=None):
+    """The whole layer.  ``hidden`` may be a (pinned) host tensor: it is then
+    copied to the weights' device and the output copied back to the host."""
+    host_in = not hidden.is_cuda
+    dev = w_gate.device
+    x = hidden.to(dev, non_blocking=True) if host_in else hidden
+    T = x.shape[0]
+    ws = _ws(cfg, T, ws, dev)
+    o = torch.empty(T, cfg.d, dtype=torch.bfloat16, device=dev) if (out is None or host_in) else out
+    c = _cfg(cfg)
+    _check(lib().beam_moe_forward(ctypes.byref(c), _dev(x, torch.bfloat16, "hidden"),
+                                  _dev(router_w, torch.float32, "router_w"),
+                                  _dev(corr_bias, torch.float32, "corr_bias"),
+                                  _dev(w_gate, torch.bfloat16, "w_gate"),
+                                  _dev(w_up, torch.bfloat16, "w_up"),
+                                  _dev(w_down, torch.bfloat16, "w_down"), o.data_ptr(), T,
+                                  ws.ptr, ws.nbytes, _stream(stream)), "beam_moe_forward")
+    if host_in:
+        if out is None:
+            out = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+        out.copy_(o, non_blocking=True)
+        return out
+    return o
+
+
+def forward_routed(cfg, hidden, topk_idx, topk_w, w_gate, w_up, w_down, out=None,
+                   ws: Workspace | None = None, stream=None):
+    """Experts + combine with a given routing (routing replay)."""
+    T = hidden.shape[0]
+    ws = _ws(cfg, T, ws, hidden.device)
+    o = torch.empty(T, cfg.d, dtype=torch.bfloat16, device=hidden.device) if out is None else out
+    c = _cfg(cfg)
+    _check(lib().beam_moe_forward_routed(ctypes.byref(c), _dev(hidden, torch.bfloat16, "hidden"),
+                                         _dev(topk_idx, torch.int32, "topk_idx"),
+                                         _dev(topk_w, torch.float32, "topk_w"),
+                                         _dev(w_gate, torch.bfloat16, "w_gate"),
+                                         _dev(w_up, torch.bfloat16, "w_up"),
+                                         _dev(w_down, torch.bfloat16, "w_down"), o.data_ptr(), T,
+                                         ws.ptr, ws.nbytes, _stream(stream)),
+           "beam_moe_forward_routed")
+    return o
+
+
+def check_status(ws: Workspace, stream=None) -> int:
+    """Synchronise and return (and clear) the latched device status code."""
+    return int(lib().beam_moe_check_status(ws.ptr, _stream(stream)))
+
+
+def set_stage_events(events) -> None:
+    """Record 8 torch.cuda.Event objects at the step boundaries of later calls
+    (None switches it off)."""
+    if events is None:
+        _check(lib().beam_moe_set_stage_events(None, 0), "beam_moe_set_stage_events")
+        return
+    arr = (_P * len(events))(*[e.cuda_event for e in events])
+    _check(lib().beam_moe_set_stage_events(arr, len(events)), "beam_moe_set_stage_events")
+
+
+def set_debug(wait_limit_us: int = 0, withhold_first_load: bool = False) -> None:
+    _check(lib().beam_moe_set_debug(int(wait_limit_us), int(bool(withhold_first_load))),
+           "beam_moe_set_debug")
+
+
+def kernels_per_forward(cfg, T: int) -> int:
+    c = _cfg(cfg)
+    return int(lib().beam_moe_kernels_per_forward(ctypes.byref(c), int(T)))

@@ -1,0 +1,472 @@
+// Host side of the C ABI declared in include/beam_moe.h: argument checks,
+// workspace carve-up, tensor-map encoding and the launch sequence on the
+// caller's stream.  No allocation, no host/device synchronisation (except in
+// beam_moe_check_status).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/beam_moe.h"
+#include "common.cuh"
+
+namespace {
+
+using beam::GemmArgs;
+
+constexpr size_t kAlign = 256;
+constexpr int kMinRows = 128;  // token-operand buffers hold at least one full tile
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;
+
+size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+// ---------------------------------------------------------------- settings
+cudaEvent_t g_events[8];
+int g_num_events = 0;
+uint64_t g_wait_ns = kDefaultWaitNs;
+int g_withhold = 0;
+
+// ---------------------------------------------------------------- driver entry
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool encoder() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  });
+  return g_encode != nullptr;
+}
+
+// 2-D BF16 tensor [rows, cols] (cols contiguous), box {64, box_rows}, 128-byte swizzle.
+bool tmap_bf16(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+
+// ---------------------------------------------------------------- device facts
+struct DevInfo {
+  int sms = 0;
+  bool supported = false;
+};
+
+bool device_info(DevInfo* out) {
+  static DevInfo cache[64];
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache[dev].sms == 0) {
+    int sms = 0, major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return false;
+    cache[dev].sms = sms;
+    cache[dev].supported = (major == 10 && minor == 3);
+  }
+  *out = cache[dev];
+  return true;
+}
+
+// ---------------------------------------------------------------- shapes
+bool is_pow2(int v) { return v > 0 && (v & (v - 1)) == 0; }
+
+bool valid_cfg(const beam_moe_config_t* c) {
+  if (!c) return false;
+  if (c->d <= 0 || c->d % 128 || c->d_ff <= 0 || c->d_ff % 128) return false;
+  if (c->n_experts <= 0 || c->n_experts % 32 || c->n_experts > 256) return false;
+  if (c->n_groups <= 0 || c->n_experts % c->n_groups) return false;
+  const int S = c->n_experts / c->n_groups;
+  if (S < 2 || S > 32 || !is_pow2(S)) return false;
+  if (c->topk_groups < 1 || c->topk_groups > c->n_groups) return false;
+  if (c->topk < 1 || c->topk > 32 || c->topk > c->topk_groups * S) return false;
+  if (!(c->routed_scale > 0.f)) return false;
+  return true;
+}
+
+int router_ksplit(const beam_moe_config_t& c, int64_t T) {
+  const int64_t blocks = static_cast<int64_t>((c.n_experts + 63) / 64) * ((T + 31) / 32);
+  const int64_t want = (2 * 152 + blocks - 1) / std::max<int64_t>(blocks, 1);
+  const int64_t ks = std::max<int64_t>(1, std::min<int64_t>(c.d / 128, want));
+  // K range per split, a multiple of 32
+  const int64_t chunk = ((c.d + ks - 1) / ks + 31) / 32 * 32;
+  return static_cast<int>((c.d + chunk - 1) / chunk);
+}
+
+int router_chunk(const beam_moe_config_t& c, int ks) {
+  return static_cast<int>(((c.d + ks - 1) / ks + 31) / 32 * 32);
+}
+
+int token_tile(const beam_moe_config_t& c, int64_t TK) {
+  return TK <= 4LL * c.n_experts ? 16 : 128;
+}
+
+struct Layout {
+  size_t status, part, logits, idx, w, counts, offsets, perm_src, pair_row, perm_w, x_perm, h, y,
+      total;
+};
+
+Layout make_layout(const beam_moe_config_t& c, int64_t T_max) {
+  const int64_t E = c.n_experts, k = c.topk;
+  const int64_t TK = T_max * k;
+  const int64_t rows = std::max<int64_t>(TK, kMinRows);
+  int64_t part_rows = 0;  // max over T <= T_max of ksplit(T) * T
+  for (int64_t nb = 1; nb <= (T_max + 31) / 32; ++nb) {
+    const int64_t Tn = std::min<int64_t>(T_max, nb * 32);
+    part_rows = std::max<int64_t>(part_rows, router_ksplit(c, Tn) * Tn);
+  }
+  Layout L;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off = align_up(off + bytes);
+    return at;
+  };
+  L.status = take(kAlign);
+  L.part = take(static_cast<size_t>(part_rows) * E * 4);
+  L.logits = take(static_cast<size_t>(T_max) * E * 4);
+  L.idx = take(static_cast<size_t>(TK) * 4);
+  L.w = take(static_cast<size_t>(TK) * 4);
+  L.counts = take(static_cast<size_t>(E) * 4);
+  L.offsets = take(static_cast<size_t>(E + 1) * 4);
+  L.perm_src = take(static_cast<size_t>(TK) * 4);
+  L.pair_row = take(static_cast<size_t>(TK) * 4);
+  L.perm_w = take(static_cast<size_t>(TK) * 4);
+  L.x_perm = take(static_cast<size_t>(rows) * c.d * 2);
+  L.h = take(static_cast<size_t>(rows) * c.d_ff * 2);
+  L.y = take(static_cast<size_t>(rows) * c.d * 4);
+  L.total = off;
+  return L;
+}
+
+bool aligned16(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+template <typename T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
+}
+
+void record(int i, cudaStream_t s) {
+  if (g_num_events >= 8) cudaEventRecord(g_events[i], s);
+}
+
+beam_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? BEAM_OK : BEAM_ERR_CUDA; }
+
+// BEAM_OK with *empty set for a valid call of zero tokens (nothing to check
+// further, nothing to launch).
+beam_status_t common_checks(const beam_moe_config_t* cfg, int64_t T, void* ws, size_t ws_bytes,
+                            Layout* L, DevInfo* dev, bool* empty) {
+  if (!valid_cfg(cfg) || T < 0 || T > (int64_t(1) << 31) / 64) return BEAM_ERR_INVALID_ARG;
+  *empty = (T == 0);
+  if (*empty) return BEAM_OK;
+  if (!aligned16(ws)) return BEAM_ERR_INVALID_ARG;
+  *L = make_layout(*cfg, T);
+  if (ws_bytes < L->total) return BEAM_ERR_WORKSPACE;
+  if (!device_info(dev)) return BEAM_ERR_CUDA;
+  if (!dev->supported) return BEAM_ERR_UNSUPPORTED;
+  return BEAM_OK;
+}
+
+// router + selection into idx/w (and logits)
+beam_status_t run_route(const beam_moe_config_t& c, const void* hidden, const float* router_w,
+                        const float* bias, int64_t T, int32_t* idx, float* w, float* logits,
+                        void* ws, const Layout& L, cudaStream_t s) {
+  const int ks = router_ksplit(c, T);
+  beam::RouterArgs ra;
+  ra.x = static_cast<const uint16_t*>(hidden);
+  ra.w = router_w;
+  ra.part = at<float>(ws, L.part);
+  ra.T = T;
+  ra.d = c.d;
+  ra.E = c.n_experts;
+  ra.k_chunk = router_chunk(c, ks);
+  beam::launch_router(ra, ks, s);
+  record(1, s);
+  beam::SelectArgs sa;
+  sa.part = ra.part;
+  sa.ksplit = ks;
+  sa.bias = bias;
+  sa.T = T;
+  sa.E = c.n_experts;
+  sa.G = c.n_groups;
+  sa.kg = c.topk_groups;
+  sa.k = c.topk;
+  sa.alpha = c.routed_scale;
+  sa.idx = idx;
+  sa.w = w;
+  sa.logits = logits;
+  beam::launch_select(sa, s);
+  record(2, s);
+  return cuda_status(cudaGetLastError());
+}
+
+// permute + gather + expert GEMMs + combine
+beam_status_t run_experts(const beam_moe_config_t& c, const void* hidden, const int32_t* idx,
+                          const float* w, const void* w_gate, const void* w_up,
+                          const void* w_down, void* out, int64_t T, void* ws, const Layout& L,
+                          const DevInfo& dev, cudaStream_t s) {
+  const int64_t TK = T * c.topk;
+  const int64_t rows = std::max<int64_t>(TK, kMinRows);
+  const int nt = token_tile(c, TK);
+  uint32_t* status = at<uint32_t>(ws, L.status);
+
+  beam::PermuteArgs pa;
+  pa.idx = idx;
+  pa.w = w;
+  pa.TK = TK;
+  pa.E = c.n_experts;
+  pa.counts = at<int32_t>(ws, L.counts);
+  pa.offsets = at<int32_t>(ws, L.offsets);
+  pa.perm_src = at<int32_t>(ws, L.perm_src);
+  pa.pair_row = at<int32_t>(ws, L.pair_row);
+  pa.perm_w = at<float>(ws, L.perm_w);
+  pa.status = status;
+  beam::launch_permute(pa, s);
+  record(3, s);
+  uint16_t* xp = at<uint16_t>(ws, L.x_perm);
+  beam::launch_gather(static_cast<const uint16_t*>(hidden), pa.perm_src, pa.offsets + c.n_experts,
+                      TK, c.topk, c.d, xp, s);
+  record(4, s);
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return BEAM_ERR_CUDA;
+
+  const int64_t EF = static_cast<int64_t>(c.n_experts) * c.d_ff;
+  const int64_t ED = static_cast<int64_t>(c.n_experts) * c.d;
+  uint16_t* h = at<uint16_t>(ws, L.h);
+  float* y = at<float>(ws, L.y);
+  CUtensorMap tm_wg, tm_wu, tm_wd, tm_xp, tm_h;
+  if (!tmap_bf16(&tm_wg, w_gate, EF, c.d, 128) || !tmap_bf16(&tm_wu, w_up, EF, c.d, 128) ||
+      !tmap_bf16(&tm_wd, w_down, ED, c.d_ff, 128) || !tmap_bf16(&tm_xp, xp, rows, c.d, nt) ||
+      !tmap_bf16(&tm_h, h, rows, c.d_ff, nt))
+    return BEAM_ERR_CUDA;
+
+  GemmArgs ga;
+  ga.counts = pa.counts;
+  ga.offsets = pa.offsets;
+  ga.perm_w = pa.perm_w;
+  ga.E = c.n_experts;
+  ga.status = status;
+  ga.wait_limit_ns = g_wait_ns;
+  ga.withhold_first_load = g_withhold;
+  g_withhold = 0;
+
+  // upper bound of the tile count, to size the persistent grid
+  auto grid_for = [&](int m_blocks) {
+    const int64_t tiles = static_cast<int64_t>(m_blocks) * (c.n_experts + (TK + nt - 1) / nt);
+    return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(dev.sms, tiles)));
+  };
+
+  ga.h_out = h;
+  ga.y_out = nullptr;
+  ga.out_ld = c.d_ff;
+  ga.rows_per_expert = c.d_ff;
+  ga.m_blocks = c.d_ff / 128;
+  ga.k_blocks = c.d / 64;
+  err = beam::launch_gateup(tm_wg, tm_wu, tm_xp, ga, nt, grid_for(ga.m_blocks), s);
+  if (err != cudaSuccess) return BEAM_ERR_CUDA;
+  record(5, s);
+
+  ga.withhold_first_load = 0;
+  ga.h_out = nullptr;
+  ga.y_out = y;
+  ga.out_ld = c.d;
+  ga.rows_per_expert = c.d;
+  ga.m_blocks = c.d / 128;
+  ga.k_blocks = c.d_ff / 64;
+  err = beam::launch_down(tm_wd, tm_h, ga, nt, grid_for(ga.m_blocks), s);
+  if (err != cudaSuccess) return BEAM_ERR_CUDA;
+  record(6, s);
+
+  beam::launch_combine(y, pa.pair_row, T, c.topk, c.d, static_cast<uint16_t*>(out), s);
+  record(7, s);
+  return cuda_status(cudaGetLastError());
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t beam_moe_workspace_size(const beam_moe_config_t* cfg, int64_t T_max, int32_t weight_fmt) {
+  if (!valid_cfg(cfg) || T_max < 0 || weight_fmt != BEAM_WEIGHTS_BF16) return 0;
+  return make_layout(*cfg, T_max).total;
+}
+
+beam_status_t beam_moe_workspace_layout(const beam_moe_config_t* cfg, int64_t T_max,
+                                        int32_t weight_fmt, beam_moe_ws_layout_t* out) {
+  if (!out || !valid_cfg(cfg) || T_max < 0 || weight_fmt != BEAM_WEIGHTS_BF16)
+    return BEAM_ERR_INVALID_ARG;
+  const Layout L = make_layout(*cfg, T_max);
+  out->status = L.status;
+  out->logits = L.logits;
+  out->topk_idx = L.idx;
+  out->topk_w = L.w;
+  out->counts = L.counts;
+  out->offsets = L.offsets;
+  out->perm_src = L.perm_src;
+  out->pair_row = L.pair_row;
+  out->perm_w = L.perm_w;
+  out->x_perm = L.x_perm;
+  out->h = L.h;
+  out->y = L.y;
+  out->total = L.total;
+  return BEAM_OK;
+}
+
+beam_status_t beam_moe_route(const beam_moe_config_t* cfg, const void* hidden,
+                             const float* router_w, const float* corr_bias, int64_t T,
+                             int32_t* topk_idx, float* topk_w, float* logits, void* workspace,
+                             size_t ws_bytes, void* stream) {
+  Layout L;
+  DevInfo dev;
+  bool empty = false;
+  beam_status_t st = common_checks(cfg, T, workspace, ws_bytes, &L, &dev, &empty);
+  if (st != BEAM_OK || empty) return st;
+  if (!aligned16(hidden) || !aligned16(router_w) || !aligned16(corr_bias) ||
+      !aligned16(topk_idx) || !aligned16(topk_w) || (logits && !aligned16(logits)))
+    return BEAM_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return run_route(*cfg, hidden, router_w, corr_bias, T, topk_idx, topk_w,
+                   logits ? logits : at<float>(workspace, L.logits), workspace, L, s);
+}
+
+beam_status_t beam_moe_select(const beam_moe_config_t* cfg, const float* logits,
+                              const float* corr_bias, int64_t T, int32_t* topk_idx, float* topk_w,
+                              void* workspace, size_t ws_bytes, void* stream) {
+  Layout L;
+  DevInfo dev;
+  bool empty = false;
+  beam_status_t st = common_checks(cfg, T, workspace, ws_bytes, &L, &dev, &empty);
+  if (st != BEAM_OK || empty) return st;
+  if (!aligned16(logits) || !aligned16(corr_bias) || !aligned16(topk_idx) || !aligned16(topk_w))
+    return BEAM_ERR_INVALID_ARG;
+  beam::SelectArgs sa;
+  sa.part = logits;
+  sa.ksplit = 1;
+  sa.bias = corr_bias;
+  sa.T = T;
+  sa.E = cfg->n_experts;
+  sa.G = cfg->n_groups;
+  sa.kg = cfg->topk_groups;
+  sa.k = cfg->topk;
+  sa.alpha = cfg->routed_scale;
+  sa.idx = topk_idx;
+  sa.w = topk_w;
+  sa.logits = nullptr;
+  beam::launch_select(sa, static_cast<cudaStream_t>(stream));
+  return cuda_status(cudaGetLastError());
+}
+
+beam_status_t beam_moe_forward(const beam_moe_config_t* cfg, const void* hidden,
+                               const float* router_w, const float* corr_bias, const void* w_gate,
+                               const void* w_up, const void* w_down, void* out, int64_t T,
+                               void* workspace, size_t ws_bytes, void* stream) {
+  Layout L;
+  DevInfo dev;
+  bool empty = false;
+  beam_status_t st = common_checks(cfg, T, workspace, ws_bytes, &L, &dev, &empty);
+  if (st != BEAM_OK || empty) return st;
+  if (!aligned16(hidden) || !aligned16(router_w) || !aligned16(corr_bias) || !aligned16(w_gate) ||
+      !aligned16(w_up) || !aligned16(w_down) || !aligned16(out))
+    return BEAM_ERR_INVALID_ARG;
+  if (!encoder()) return BEAM_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  record(0, s);
+  int32_t* idx = at<int32_t>(workspace, L.idx);
+  float* w = at<float>(workspace, L.w);
+  st = run_route(*cfg, hidden, router_w, corr_bias, T, idx, w, at<float>(workspace, L.logits),
+                 workspace, L, s);
+  if (st != BEAM_OK) return st;
+  return run_experts(*cfg, hidden, idx, w, w_gate, w_up, w_down, out, T, workspace, L, dev, s);
+}
+
+beam_status_t beam_moe_forward_routed(const beam_moe_config_t* cfg, const void* hidden,
+                                      const int32_t* topk_idx, const float* topk_w,
+                                      const void* w_gate, const void* w_up, const void* w_down,
+                                      void* out, int64_t T, void* workspace, size_t ws_bytes,
+                                      void* stream) {
+  Layout L;
+  DevInfo dev;
+  bool empty = false;
+  beam_status_t st = common_checks(cfg, T, workspace, ws_bytes, &L, &dev, &empty);
+  if (st != BEAM_OK || empty) return st;
+  if (!aligned16(hidden) || !aligned16(topk_idx) || !aligned16(topk_w) || !aligned16(w_gate) ||
+      !aligned16(w_up) || !aligned16(w_down) || !aligned16(out))
+    return BEAM_ERR_INVALID_ARG;
+  if (!encoder()) return BEAM_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  record(0, s);
+  record(1, s);
+  record(2, s);
+  return run_experts(*cfg, hidden, topk_idx, topk_w, w_gate, w_up, w_down, out, T, workspace, L,
+                     dev, s);
+}
+
+beam_status_t beam_moe_check_status(void* workspace, void* stream) {
+  if (!aligned16(workspace)) return BEAM_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint32_t v = 0;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return BEAM_ERR_CUDA;
+  // the status word sits at offset 0 of every layout
+  if (cudaMemcpy(&v, workspace, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return BEAM_ERR_CUDA;
+  if (v != 0 && cudaMemset(workspace, 0, sizeof v) != cudaSuccess) return BEAM_ERR_CUDA;
+  return static_cast<beam_status_t>(v);
+}
+
+beam_status_t beam_moe_set_stage_events(void* const* events, int32_t n) {
+  if (n == 0) {
+    g_num_events = 0;
+    return BEAM_OK;
+  }
+  if (!events || n < 8) return BEAM_ERR_INVALID_ARG;
+  for (int i = 0; i < 8; ++i) {
+    if (!events[i]) return BEAM_ERR_INVALID_ARG;
+    g_events[i] = static_cast<cudaEvent_t>(events[i]);
+  }
+  g_num_events = 8;
+  return BEAM_OK;
+}
+
+beam_status_t beam_moe_set_debug(uint32_t wait_limit_us, int32_t withhold_first_load) {
+  g_wait_ns = wait_limit_us ? static_cast<uint64_t>(wait_limit_us) * 1000ull : kDefaultWaitNs;
+  g_withhold = withhold_first_load ? 1 : 0;
+  return BEAM_OK;
+}
+
+int32_t beam_moe_kernels_per_forward(const beam_moe_config_t* cfg, int64_t T) {
+  if (!valid_cfg(cfg) || T <= 0) return 0;
+  return 7;
+}
+
+const char* beam_status_string(beam_status_t s) {
+  switch (s) {
+    case BEAM_OK: return "ok";
+    case BEAM_ERR_INVALID_ARG: return "invalid argument";
+    case BEAM_ERR_UNSUPPORTED: return "unsupported (needs an sm_103 GPU)";
+    case BEAM_ERR_WORKSPACE: return "workspace too small";
+    case BEAM_ERR_CUDA: return "CUDA error";
+    case BEAM_ERR_TIMEOUT: return "device-side wait timed out";
+    case BEAM_ERR_DEVICE_CHECK: return "device-side argument check failed";
+  }
+  return "unknown status";
+}
+
+}  // extern "C"

@@ -1,0 +1,402 @@
+// Grouped expert GEMMs on the 5th-generation tensor cores (tcgen05 + TMEM),
+// operands staged by TMA.
+//
+//   gate/up : for every expert e and every row r of its permuted tokens,
+//             g = x_r W_g[e]^T, u = x_r W_u[e]^T (FP32 accumulators in TMEM),
+//             h_r = bf16(silu(g) * u) with the SwiGLU product in FP32
+//             ("Reflection 发布 501B 开源模型 Beam，Apache 2.0 许可", section
+//             "残差流": the SwiGLU product is computed in FP32; SGLang post
+//             "SGLang 原生支持 Reflection 的 Beam 并驱动其生产 API", section "BF16 MoE
+//             Kernel Optimization": the activation keeps its BF16 rounding).
+//   down    : y_r = w_r * (h_r W_d[e]^T) in FP32 (the FP32 routing weight is
+//             applied before anything is rounded; the BF16 rounding happens
+//             once, after the local sum over a token's experts -- SGLang post,
+//             section "Fusion Optimizations").
+//
+// Tiling ("swap AB"): the MMA's M side is 128 weight rows, its N side is a
+// tile of NT permuted token rows (NT = 16 for decode-sized batches, 128 for
+// prefill-sized ones), K steps of 64 (one 128-byte swizzle row of BF16).
+// gate/up issue two MMAs per K step into two TMEM accumulators (gate, up) that
+// share the token operand, so one thread holds g and u of the same (f, token)
+// and the SwiGLU epilogue is local.
+//
+// Persistent CTAs (one per SM) walk a tile list derived on the device from
+// the per-expert row counts: tile -> (expert, weight block, token block),
+// ordered so the token blocks of one weight block run on neighbouring CTAs at
+// the same time (their weight tiles are then read from HBM once and from L2
+// after).  Warp roles: warp 0 issues TMA loads into a STAGES-deep ring, warp 1
+// owns TMEM and issues tcgen05.mma from one thread, warps 2-5 drain the
+// double-buffered accumulators.  Every mbarrier wait is bounded: when one runs
+// out the CTA latches BEAM_ERR_TIMEOUT, stops, lets its copies in flight land,
+// frees its TMEM and returns.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace beam {
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+constexpr int BM = 128;
+constexpr int BK = 64;
+constexpr int UMMA_K = 16;
+constexpr int kThreads = 192;
+constexpr int kMaxE = 256;
+constexpr uint32_t kTileBudget = 216 * 1024;
+
+constexpr uint32_t pow2_at_least(uint32_t v) {
+  uint32_t p = 32;
+  while (p < v) p <<= 1;
+  return p;
+}
+
+template <int NT, bool GATEUP>
+struct Cfg {
+  static constexpr int NUM_A = GATEUP ? 2 : 1;
+  static constexpr uint32_t A_BYTES = BM * BK * 2;
+  static constexpr uint32_t B_BYTES = NT * BK * 2;
+  static constexpr uint32_t STAGE_BYTES = NUM_A * A_BYTES + B_BYTES;
+  static constexpr int STAGES_RAW = static_cast<int>(kTileBudget / STAGE_BYTES);
+  static constexpr int STAGES = STAGES_RAW > 16 ? 16 : STAGES_RAW;
+  static constexpr uint32_t ACC_COLS = NUM_A * NT;
+  static constexpr uint32_t TMEM_COLS = pow2_at_least(2 * ACC_COLS);
+  static constexpr uint32_t NUM_BARS = 2 * STAGES + 5;
+  static constexpr uint32_t MISC_BYTES = 16 + 4 * (3 * kMaxE + 1);
+  static constexpr uint32_t SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + NUM_BARS * 8 + MISC_BYTES;
+  static_assert(B_BYTES % 1024 == 0, "token tile must keep 1024-byte stage alignment");
+  static_assert(TMEM_COLS <= 512, "TMEM has 512 columns");
+  static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+  static_assert(NT % 16 == 0 && NT >= 16 && NT <= 256, "MMA N for M = 128");
+};
+
+__device__ __forceinline__ uint16_t f32_to_bf16(float v) {
+  __nv_bfloat16 b = __float2bfloat16_rn(v);
+  return *reinterpret_cast<uint16_t*>(&b);
+}
+
+struct Waiter {
+  volatile int32_t* abort_flag;
+  uint32_t* status;
+  uint64_t limit_ns;
+
+  // Wait for the phase of `parity`; false if another role aborted or the
+  // wait ran out (then this CTA aborts and the status is latched).
+  __device__ bool wait(uint32_t bar, uint32_t parity) const {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = ptx::globaltimer();
+    for (uint32_t n = 1;; ++n) {
+      if (ptx::mbar_try_wait(bar, parity)) return true;
+      if ((n & 63u) == 0) {
+        if (*abort_flag) return false;
+        if (ptx::globaltimer() - t0 > limit_ns) {
+          *abort_flag = 1;
+          latch_status(status, kStatusTimeout);
+          return false;
+        }
+      }
+    }
+  }
+
+  // Wait that ignores the abort flag (used to let issued work finish).
+  __device__ bool wait_final(uint32_t bar, uint32_t parity) const {
+    const uint64_t t0 = ptx::globaltimer();
+    for (uint32_t n = 0;; ++n) {
+      if (ptx::mbar_try_wait(bar, parity)) return true;
+      if ((n & 63u) == 63u && ptx::globaltimer() - t0 > limit_ns) {
+        latch_status(status, kStatusTimeout);
+        return false;
+      }
+    }
+  }
+};
+
+struct TileInfo {
+  int expert, mblock, row0, nvalid;
+};
+
+// tile index -> (expert, weight block, first permuted row, valid rows)
+template <int NT>
+__device__ __forceinline__ TileInfo decode_tile(int tile, const int32_t* s_start,
+                                                const int32_t* s_cnt, const int32_t* s_off,
+                                                int E) {
+  int lo = 0, hi = E;  // s_start[lo] <= tile < s_start[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (s_start[mid] <= tile)
+      lo = mid;
+    else
+      hi = mid;
+  }
+  const int local = tile - s_start[lo];
+  const int cnt = s_cnt[lo];
+  const int ntb = (cnt + NT - 1) / NT;
+  const int tb = local % ntb;
+  TileInfo ti;
+  ti.expert = lo;
+  ti.mblock = local / ntb;
+  ti.row0 = s_off[lo] + tb * NT;
+  ti.nvalid = min(NT, cnt - tb * NT);
+  return ti;
+}
+
+template <int NT, bool GATEUP>
+__global__ void __launch_bounds__(kThreads, 1)
+    expert_gemm_kernel(const __grid_constant__ CUtensorMap tm_a0,
+                       const __grid_constant__ CUtensorMap tm_a1,
+                       const __grid_constant__ CUtensorMap tm_b, const GemmArgs p,
+                       const int weight_evict_first) {
+  using C = Cfg<NT, GATEUP>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = ptx::smem_addr(smem_raw);
+  const uint32_t pad = (1024u - (raw_addr & 1023u)) & 1023u;
+  uint8_t* smem = smem_raw + pad;
+  const uint32_t tiles = raw_addr + pad;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
+  int32_t* misc = reinterpret_cast<int32_t*>(bars + C::NUM_BARS);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc);
+  volatile int32_t* abort_flag = misc + 1;
+  int32_t* s_cnt = misc + 4;
+  int32_t* s_off = s_cnt + kMaxE;
+  int32_t* s_start = s_off + kMaxE;
+
+  const uint32_t bar0 = ptx::smem_addr(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (C::STAGES + s); };
+  auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * C::STAGES + a); };
+  auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * C::STAGES + 2 + a); };
+  const uint32_t done_bar = bar0 + 8u * (2 * C::STAGES + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int E = p.E;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      ptx::mbar_init(full_bar(s), 1);
+      ptx::mbar_init(empty_bar(s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      ptx::mbar_init(tfull_bar(a), 1);
+      ptx::mbar_init(tempty_bar(a), 128);
+    }
+    ptx::mbar_init(done_bar, 1);
+    *abort_flag = 0;
+    ptx::fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    ptx::prefetch_tmap(&tm_a0);
+    if (GATEUP) ptx::prefetch_tmap(&tm_a1);
+    ptx::prefetch_tmap(&tm_b);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(ptx::smem_addr(tmem_slot), C::TMEM_COLS);
+    ptx::tmem_relinquish();
+  }
+  for (int e = threadIdx.x; e < E; e += kThreads) {
+    s_cnt[e] = p.counts[e];
+    s_off[e] = p.offsets[e];
+  }
+  __syncthreads();
+  if (warp == 0) {  // exclusive scan of tiles per expert
+    int running = 0;
+    for (int base = 0; base < E; base += 32) {
+      const int e = base + lane;
+      const int v = e < E ? p.m_blocks * ((s_cnt[e] + NT - 1) / NT) : 0;
+      int incl = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(kFull, incl, o);
+        if (lane >= o) incl += n;
+      }
+      if (e < E) s_start[e] = running + incl - v;
+      running += __shfl_sync(kFull, incl, 31);
+    }
+    if (lane == 0) s_start[E] = running;
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int num_tiles = s_start[E];
+  const Waiter W{abort_flag, p.status, p.wait_limit_ns};
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      const uint64_t pol_w = weight_evict_first ? ptx::policy_evict_first() : ptx::policy_evict_normal();
+      const uint64_t pol_b = ptx::policy_evict_last();
+      int last_parity[C::STAGES];
+#pragma unroll
+      for (int s = 0; s < C::STAGES; ++s) last_parity[s] = -1;
+      int stage = 0;
+      uint32_t phase = 0;
+      bool withhold = p.withhold_first_load != 0 && blockIdx.x == 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+        const TileInfo ti = decode_tile<NT>(tile, s_start, s_cnt, s_off, E);
+        const int a_row = ti.expert * p.rows_per_expert + ti.mblock * BM;
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (!W.wait(empty_bar(stage), phase ^ 1u)) {
+            ok = false;
+            break;
+          }
+          if (withhold) {
+            withhold = false;  // test aid: this stage never fills
+          } else {
+            const uint32_t st = tiles + stage * C::STAGE_BYTES;
+            ptx::mbar_arrive_expect_tx(full_bar(stage), C::STAGE_BYTES);
+            ptx::tma_load_2d(st, &tm_a0, full_bar(stage), kb * BK, a_row, pol_w);
+            if (GATEUP)
+              ptx::tma_load_2d(st + C::A_BYTES, &tm_a1, full_bar(stage), kb * BK, a_row, pol_w);
+            ptx::tma_load_2d(st + C::NUM_A * C::A_BYTES, &tm_b, full_bar(stage), kb * BK, ti.row0,
+                             pol_b);
+            last_parity[stage] = static_cast<int>(phase);
+          }
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // the CTA may not exit while a copy into its shared memory is in flight
+#pragma unroll
+      for (int s = 0; s < C::STAGES; ++s)
+        if (last_parity[s] >= 0) W.wait_final(full_bar(s), static_cast<uint32_t>(last_parity[s]));
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = ptx::idesc_bf16_f32(BM, NT);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+        if (!W.wait(tempty_bar(acc), acc_phase ^ 1u)) break;
+        ptx::tc_fence_after();
+        const uint32_t d0 = tmem_base + acc * C::ACC_COLS;
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (!W.wait(full_bar(stage), phase)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t st = tiles + stage * C::STAGE_BYTES;
+          const uint32_t b_base = st + C::NUM_A * C::A_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+            const uint32_t accum = (kb | kk) ? 1u : 0u;
+            const uint64_t bd = ptx::sdesc_sw128(b_base + kk * 32);
+            ptx::mma_bf16(d0, ptx::sdesc_sw128(st + kk * 32), bd, idesc, accum);
+            if (GATEUP)
+              ptx::mma_bf16(d0 + NT, ptx::sdesc_sw128(st + C::A_BYTES + kk * 32), bd, idesc, accum);
+          }
+          ptx::mma_commit(empty_bar(stage));  // frees the stage once these MMAs read it
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        ptx::mma_commit(tfull_bar(acc));
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      // every MMA this thread issued completes before TMEM is released
+      ptx::mma_commit(done_bar);
+      W.wait_final(done_bar, 0);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int m = q * 32 + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+      const TileInfo ti = decode_tile<NT>(tile, s_start, s_cnt, s_off, E);
+      if (!W.wait(tfull_bar(acc), acc_phase)) break;
+      ptx::tc_fence_after();
+      const uint32_t tq = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * C::ACC_COLS;
+      const int col = ti.mblock * BM + m;
+#pragma unroll 1
+      for (int c0 = 0; c0 < NT; c0 += 16) {
+        if (c0 >= ti.nvalid) break;
+        uint32_t ra[16];
+        ptx::tmem_ld16(tq + c0, ra);
+        if constexpr (GATEUP) {
+          uint32_t rb[16];
+          ptx::tmem_ld16(tq + NT + c0, rb);
+          ptx::tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            if (c0 + j < ti.nvalid) {
+              const float g = __uint_as_float(ra[j]);
+              const float u = __uint_as_float(rb[j]);
+              const float h = g / (1.0f + expf(-g)) * u;
+              p.h_out[static_cast<int64_t>(ti.row0 + c0 + j) * p.out_ld + col] = f32_to_bf16(h);
+            }
+          }
+        } else {
+          ptx::tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            if (c0 + j < ti.nvalid) {
+              const int row = ti.row0 + c0 + j;
+              p.y_out[static_cast<int64_t>(row) * p.out_ld + col] =
+                  __uint_as_float(ra[j]) * p.perm_w[row];
+            }
+          }
+        }
+      }
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(tempty_bar(acc));
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem_base, C::TMEM_COLS);
+  }
+}
+
+template <int NT, bool GATEUP>
+cudaError_t launch_impl(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b,
+                        const GemmArgs& p, int num_sms, int evict_first, cudaStream_t s) {
+  using C = Cfg<NT, GATEUP>;
+  auto kern = expert_gemm_kernel<NT, GATEUP>;
+  cudaError_t err =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  if (err != cudaSuccess) return err;
+  kern<<<num_sms, kThreads, C::SMEM_BYTES, s>>>(a0, a1, b, p, evict_first);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gateup(const CUtensorMap& wg, const CUtensorMap& wu, const CUtensorMap& xp,
+                          const GemmArgs& a, int nt, int num_sms, cudaStream_t s) {
+  if (nt == 16) return launch_impl<16, true>(wg, wu, xp, a, num_sms, 1, s);
+  if (nt == 128) return launch_impl<128, true>(wg, wu, xp, a, num_sms, 0, s);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_down(const CUtensorMap& wd, const CUtensorMap& h, const GemmArgs& a, int nt,
+                        int num_sms, cudaStream_t s) {
+  if (nt == 16) return launch_impl<16, false>(wd, wd, h, a, num_sms, 1, s);
+  if (nt == 128) return launch_impl<128, false>(wd, wd, h, a, num_sms, 0, s);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace beam

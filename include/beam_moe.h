@@ -1,0 +1,179 @@
+/*
+ * beam_moe.h -- C ABI of the Beam MoE layer for NVIDIA GB300 (sm_103a).
+ *
+ * The layer is the sparse feed-forward block of the Beam 501B-A23B model:
+ *   1. an FP32 router, logits = x W_r^T
+ *      ("SGLang 原生支持 Reflection 的 Beam 并驱动其生产 API", section "Dense
+ *      Layers and Grouped MoE Routing"; "vLLM 实现 Reflection Beam 501B MoE
+ *      模型 Day 0 支持", section "MoE and residual stream": router weights,
+ *      accumulation and logits all FP32);
+ *   2. DeepSeek-V3-style group-limited selection: sigmoid scores s plus a
+ *      correction bias b give choice scores c = s + b; groups are ranked by the
+ *      sum of their two best c; the best topk_groups groups are kept; the topk
+ *      best experts of the kept groups are chosen; their s are renormalised
+ *      and multiplied by routed_scale (vLLM post, same section; "Reflection
+ *      发布 501B 开源模型 Beam，Apache 2.0 许可", section "专家混合");
+ *   3. SwiGLU experts h = silu(x W_g^T) * (x W_u^T) with the product in FP32,
+ *      rounded to BF16, then y = h W_d^T (HF post, sections "专家混合" and
+ *      "残差流"; SGLang post, section "BF16 MoE Kernel Optimization");
+ *   4. the weighted combine out = bf16(sum_k w_k y_k): FP32 routing weights
+ *      applied to FP32 expert outputs, summed locally in FP32 in slot order
+ *      and rounded once to BF16 (SGLang post, sections "BF16 MoE Kernel
+ *      Optimization" and "Fusion Optimizations").
+ *   There is no shared expert.
+ *
+ * Conventions shared by every entry point
+ *   - Every pointer except `stream` is DEVICE memory on the current device,
+ *     allocated and owned by the caller; the library never frees or keeps it
+ *     past the call and allocates no device memory of its own.
+ *   - Row-major layouts, nn.Linear weight convention ([out, in], K contiguous):
+ *       hidden   [T, d]      BF16
+ *       router_w [E, d]      FP32
+ *       corr_bias[E]         FP32
+ *       w_gate   [E, F, d]   BF16      (F = d_ff)
+ *       w_up     [E, F, d]   BF16
+ *       w_down   [E, d, F]   BF16
+ *       out      [T, d]      BF16
+ *       topk_idx [T, topk]   int32, slots in descending choice score
+ *       topk_w   [T, topk]   FP32, includes routed_scale (sums to it)
+ *   - Pointers must be 16-byte aligned.  Shapes: d % 128 == 0,
+ *     d_ff % 128 == 0, n_experts % 32 == 0 and <= 256, n_groups divides
+ *     n_experts with 2 <= n_experts/n_groups <= 32 a power of two,
+ *     1 <= topk_groups <= n_groups, 1 <= topk <= min(32, topk_groups *
+ *     n_experts / n_groups), T >= 0.
+ *   - All work is enqueued on `stream` (a cudaStream_t; NULL = the legacy
+ *     default stream).  No entry point synchronises or copies between host
+ *     and device, except beam_moe_check_status.
+ *   - Every entry point returns a status and never aborts or prints.  Invalid
+ *     arguments are rejected before anything is launched (outputs untouched).
+ *     T == 0 with a valid cfg returns BEAM_OK at once: nothing is launched
+ *     and no pointer is looked at.  Errors found by the kernels
+ *     (a wait that ran out of time, an expert index out of range) are latched
+ *     in the workspace's status word and reported by beam_moe_check_status.
+ *   - Results are deterministic: no floating-point atomics; every reduction
+ *     runs in a fixed order.
+ */
+#ifndef BEAM_MOE_H_
+#define BEAM_MOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  BEAM_OK = 0,
+  BEAM_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, bad shape, T < 0   */
+  BEAM_ERR_UNSUPPORTED = 2,   /* valid but not implemented (e.g. no sm_103)  */
+  BEAM_ERR_WORKSPACE = 3,     /* workspace smaller than beam_moe_workspace_size */
+  BEAM_ERR_CUDA = 4,          /* a CUDA call or launch failed                */
+  BEAM_ERR_TIMEOUT = 5,       /* a device-side bounded wait ran out          */
+  BEAM_ERR_DEVICE_CHECK = 6   /* a device-side argument check failed         */
+} beam_status_t;
+
+/* Layer shape.  Beam: {5120, 256, 8, 4, 8, 2560, 2.5f}. */
+typedef struct {
+  int32_t d;             /* hidden size                                   */
+  int32_t n_experts;     /* routed experts E                              */
+  int32_t n_groups;      /* expert groups G                               */
+  int32_t topk_groups;   /* groups kept per token                         */
+  int32_t topk;          /* experts chosen per token                      */
+  int32_t d_ff;          /* expert intermediate size F                    */
+  float routed_scale;    /* factor on the renormalised weights (2.5)      */
+} beam_moe_config_t;
+
+/* Weight formats for beam_moe_workspace_size. */
+#define BEAM_WEIGHTS_BF16 0
+#define BEAM_WEIGHTS_NVFP4 1
+
+/* Bytes of device workspace a call with up to T_max tokens needs (256-byte
+ * aligned).  Returns 0 for an invalid configuration. */
+size_t beam_moe_workspace_size(const beam_moe_config_t *cfg, int64_t T_max,
+                               int32_t weight_fmt);
+
+/* Byte offsets of the intermediate buffers inside the workspace (for
+ * inspection in tests and tools; the layout depends on cfg and T_max).
+ * perm_* arrays are indexed by "permuted row": the (token, slot) pairs sorted
+ * stably by expert, then token, then slot. */
+typedef struct {
+  size_t status;        /* uint32 status word (BEAM_OK or the first error)   */
+  size_t logits;        /* FP32 [T, E] (router output as the selection read it) */
+  size_t topk_idx;      /* int32 [T, topk]                                    */
+  size_t topk_w;        /* FP32 [T, topk]                                     */
+  size_t counts;        /* int32 [E] rows per expert                          */
+  size_t offsets;       /* int32 [E + 1] first permuted row of each expert    */
+  size_t perm_src;      /* int32 [T*topk] permuted row -> token*topk + slot   */
+  size_t pair_row;      /* int32 [T*topk] token*topk + slot -> permuted row   */
+  size_t perm_w;        /* FP32 [T*topk] routing weight of each permuted row  */
+  size_t x_perm;        /* BF16 [T*topk, d] gathered expert inputs            */
+  size_t h;             /* BF16 [T*topk, F] SwiGLU activations                */
+  size_t y;             /* FP32 [T*topk, d] weighted expert outputs           */
+  size_t total;         /* == beam_moe_workspace_size                         */
+} beam_moe_ws_layout_t;
+
+beam_status_t beam_moe_workspace_layout(const beam_moe_config_t *cfg, int64_t T_max,
+                                        int32_t weight_fmt, beam_moe_ws_layout_t *out);
+
+/* Steps 1-2 only (router + group-limited selection), e.g. to record routes
+ * for routing replay (SGLang post, section "Reinforcement learning in Miles":
+ * recorded expert choices reused instead of recomputing top-k).
+ * Writes topk_idx [T, topk], topk_w [T, topk] and, when `logits` is not
+ * NULL, the FP32 router logits [T, E]. */
+beam_status_t beam_moe_route(const beam_moe_config_t *cfg, const void *hidden,
+                             const float *router_w, const float *corr_bias, int64_t T,
+                             int32_t *topk_idx, float *topk_w, float *logits,
+                             void *workspace, size_t ws_bytes, void *stream);
+
+/* Step 2 alone on given FP32 logits [T, E] (selection tested in isolation). */
+beam_status_t beam_moe_select(const beam_moe_config_t *cfg, const float *logits,
+                              const float *corr_bias, int64_t T, int32_t *topk_idx,
+                              float *topk_w, void *workspace, size_t ws_bytes,
+                              void *stream);
+
+/* The whole layer, steps 1-4: out [T, d] BF16. */
+beam_status_t beam_moe_forward(const beam_moe_config_t *cfg, const void *hidden,
+                               const float *router_w, const float *corr_bias,
+                               const void *w_gate, const void *w_up, const void *w_down,
+                               void *out, int64_t T, void *workspace, size_t ws_bytes,
+                               void *stream);
+
+/* Steps 3-4 with a given routing (topk_idx/topk_w as beam_moe_route writes
+ * them; routing replay).  Indices outside [0, E) latch
+ * BEAM_ERR_DEVICE_CHECK and contribute nothing. */
+beam_status_t beam_moe_forward_routed(const beam_moe_config_t *cfg, const void *hidden,
+                                      const int32_t *topk_idx, const float *topk_w,
+                                      const void *w_gate, const void *w_up,
+                                      const void *w_down, void *out, int64_t T,
+                                      void *workspace, size_t ws_bytes, void *stream);
+
+/* Synchronises `stream`, returns the workspace's latched status and clears
+ * it.  The only entry point that waits for the device. */
+beam_status_t beam_moe_check_status(void *workspace, void *stream);
+
+/* Profiling aid: when n >= 8 events (cudaEvent_t) are given, every later
+ * beam_moe_forward / beam_moe_forward_routed records them on its stream at
+ * the step boundaries: [0] start, [1] router, [2] selection, [3] permute,
+ * [4] gather, [5] gate/up GEMM, [6] down GEMM, [7] combine (each after its
+ * step).  Steps a call does not run record at the same point as the previous
+ * one.  n == 0 switches it off.  Process-wide; not thread-safe. */
+beam_status_t beam_moe_set_stage_events(void *const *events, int32_t n);
+
+/* Test aid for the bounded waits: wait_limit_us bounds every device-side
+ * wait of the expert GEMMs (0 restores the default of two seconds);
+ * withhold_first_load != 0 makes the first CTA of the next gate/up GEMM skip
+ * its first operand load, so its MMA wait runs out and the call latches
+ * BEAM_ERR_TIMEOUT without faulting.  Process-wide; not thread-safe. */
+beam_status_t beam_moe_set_debug(uint32_t wait_limit_us, int32_t withhold_first_load);
+
+/* Number of kernels a forward call of T tokens launches (for accounting). */
+int32_t beam_moe_kernels_per_forward(const beam_moe_config_t *cfg, int64_t T);
+
+const char *beam_status_string(beam_status_t s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BEAM_MOE_H_ */

@@ -53,10 +53,10 @@ def _load():
         lib.oracle_route.argtypes = [_P, _P, _I64, _I32, _I32, _I32, _I32, ctypes.c_float,
                                      _P, _P, _P, _P, _P, _P, _P]
         lib.oracle_experts_bf16.argtypes = [_P, _I64, _I32, _I32, _I32, _I32, _P, _P,
-                                            _P, _P, _P, _P, _I64, _P]
+                                            _P, _P, _P, _P, _I64, _P, _P]
         lib.oracle_experts_nvfp4.argtypes = [_P, _I64, _I32, _I32, _I32, _I32, _P, _P,
                                              _P, _P, _P, _P, _P, _P, _P, _P, _P,
-                                             _I32, _P, _I64, _P]
+                                             _I32, _P, _I64, _P, _P]
         for name in ("oracle_e2m1_value", "oracle_e4m3_value"):
             getattr(lib, name).argtypes = [ctypes.c_uint8]
             getattr(lib, name).restype = ctypes.c_double
@@ -185,8 +185,9 @@ def _expert_ptrs(ws, E: int):
 
 
 def experts_bf16(x_bf16, idx, w, wg, wu, wd, n_experts: int, tokens=None,
-                 out: np.ndarray | None = None) -> np.ndarray:
-    """Weighted SwiGLU experts + combine for BF16 weights; returns BF16 [T, d].
+                 out: np.ndarray | None = None, exact: bool = False):
+    """Weighted SwiGLU experts + combine for BF16 weights; returns BF16 [T, d]
+    (and, with ``exact``, also the float64 output before its final rounding).
     wg/wu: per expert [F, d] uint16; wd: per expert [d, F] uint16."""
     x = _c(x_bf16, np.uint16)
     T, d = x.shape
@@ -199,18 +200,19 @@ def experts_bf16(x_bf16, idx, w, wg, wu, wd, n_experts: int, tokens=None,
     F = _infer_F(wg, d)
     if out is None:
         out = np.zeros((T, d), np.uint16)
+    ex = np.zeros((T, d), np.float64) if exact else None
     tok = None if tokens is None else _c(tokens, np.int64)
     rc = _load().oracle_experts_bf16(_ptr(x), T, d, F, k, n_experts, _ptr(idx), _ptr(w),
                                      ctypes.cast(pg, _P), ctypes.cast(pu, _P),
                                      ctypes.cast(pd, _P), _ptr(tok),
-                                     0 if tok is None else tok.size, _ptr(out))
+                                     0 if tok is None else tok.size, _ptr(out), _ptr(ex))
     if rc:
         raise ValueError(f"oracle_experts_bf16 failed ({rc})")
-    return out
+    return (out, ex) if exact else out
 
 
 def experts_nvfp4(x_bf16, idx, w, gate, up, down, n_experts: int, act_quant: bool = True,
-                  tokens=None, out: np.ndarray | None = None) -> np.ndarray:
+                  tokens=None, out: np.ndarray | None = None, exact: bool = False):
     """NVFP4 experts.  gate/up/down are dicts with per-expert 'q' (packed
     codes [N, K/2]), 'sf' (E4M3 codes [N, K/16]) and 'gs' (float32 [E])."""
     x = _c(x_bf16, np.uint16)
@@ -229,13 +231,14 @@ def experts_nvfp4(x_bf16, idx, w, gate, up, down, n_experts: int, act_quant: boo
     F = _infer_F(gate["q"], d // 2)
     if out is None:
         out = np.zeros((T, d), np.uint16)
+    ex = np.zeros((T, d), np.float64) if exact else None
     tok = None if tokens is None else _c(tokens, np.int64)
     rc = _load().oracle_experts_nvfp4(_ptr(x), T, d, F, k, n_experts, _ptr(idx), _ptr(w),
                                       *tabs, int(bool(act_quant)), _ptr(tok),
-                                      0 if tok is None else tok.size, _ptr(out))
+                                      0 if tok is None else tok.size, _ptr(out), _ptr(ex))
     if rc:
         raise ValueError(f"oracle_experts_nvfp4 failed ({rc})")
-    return out
+    return (out, ex) if exact else out
 
 
 def _infer_F(ws, inner: int) -> int:

@@ -271,7 +271,8 @@ int oracle_route(const float *logits, const float *bias, int64_t T, int32_t E,
 /* Weight layouts (nn.Linear): W_g, W_u [F, d] and W_d [d, F] per expert,    */
 /* passed as one pointer per expert (NULL for experts nobody uses).          */
 /* tokens: optional list of rows to compute (NULL = all T rows); rows not    */
-/* listed are left untouched in out.                                         */
+/* listed are left untouched in out.  out_exact (optional, [T, d] double)    */
+/* receives the output before its final rounding.                            */
 /* ------------------------------------------------------------------------ */
 typedef struct {
   /* BF16 weights */
@@ -315,7 +316,7 @@ static double fp4_weight(const uint8_t *q, const uint8_t *sf, float gs,
 static int experts_impl(const uint16_t *x, int64_t T, int32_t d, int32_t F,
                         int32_t k, int32_t E, const int32_t *idx, const float *w,
                         const weights_t *W, const int64_t *tokens,
-                        int64_t n_tokens, uint16_t *out) {
+                        int64_t n_tokens, uint16_t *out, double *out_exact) {
   if (T < 0 || d <= 0 || F <= 0 || k <= 0 || (d % 16) || (F % 16)) return -1;
   const int64_t n = tokens ? n_tokens : T;
   int err = 0;
@@ -400,6 +401,8 @@ static int experts_impl(const uint16_t *x, int64_t T, int32_t d, int32_t F,
           }
         }
         for (int32_t r = 0; r < d; ++r) out[t * (int64_t)d + r] = bf16_round((float)acc[r]);
+        if (out_exact)
+          for (int32_t r = 0; r < d; ++r) out_exact[t * (int64_t)d + r] = acc[r];
       }
     }
     free(xin);
@@ -415,13 +418,13 @@ int oracle_experts_bf16(const uint16_t *x, int64_t T, int32_t d, int32_t F,
                         int32_t k, int32_t E, const int32_t *idx, const float *w,
                         const uint16_t *const *wg, const uint16_t *const *wu,
                         const uint16_t *const *wd, const int64_t *tokens,
-                        int64_t n_tokens, uint16_t *out) {
+                        int64_t n_tokens, uint16_t *out, double *out_exact) {
   weights_t W;
   memset(&W, 0, sizeof W);
   W.wg = wg;
   W.wu = wu;
   W.wd = wd;
-  return experts_impl(x, T, d, F, k, E, idx, w, &W, tokens, n_tokens, out);
+  return experts_impl(x, T, d, F, k, E, idx, w, &W, tokens, n_tokens, out, out_exact);
 }
 
 /* NVFP4 experts ([SGL] Highlights: "ModelOpt NVFP4" checkpoints; [VLLM]:
@@ -437,7 +440,7 @@ int oracle_experts_nvfp4(const uint16_t *x, int64_t T, int32_t d, int32_t F,
                          const uint8_t *const *qu, const uint8_t *const *sfu, const float *gsu,
                          const uint8_t *const *qd, const uint8_t *const *sfd, const float *gsd,
                          int32_t act_quant, const int64_t *tokens, int64_t n_tokens,
-                         uint16_t *out) {
+                         uint16_t *out, double *out_exact) {
   weights_t W;
   memset(&W, 0, sizeof W);
   W.qg = qg; W.sfg = sfg; W.gsg = gsg;
@@ -445,7 +448,7 @@ int oracle_experts_nvfp4(const uint16_t *x, int64_t T, int32_t d, int32_t F,
   W.qd = qd; W.sfd = sfd; W.gsd = gsd;
   W.fp4 = 1;
   W.act_quant = act_quant;
-  return experts_impl(x, T, d, F, k, E, idx, w, &W, tokens, n_tokens, out);
+  return experts_impl(x, T, d, F, k, E, idx, w, &W, tokens, n_tokens, out, out_exact);
 }
 
 /* ------------------------------------------------------------------------ */

@@ -1,0 +1,125 @@
+"""Shared helpers of the GPU parity tests: run the oracle on the same seeded
+inputs and compare with the tolerances the layer's specification states
+(router logits within 1e-5 relative; expert indices exact except where the
+oracle's k-th/(k+1)-th margin is below 1e-6; BF16 outputs within
+max-abs 1e-2 * RMS(out)).
+
+Output tolerance, as read here: the bound 1e-2 * RMS(out) applies to the
+arithmetic error, measured against the oracle's exact (float64) output
+before its final rounding; the BF16 output format adds its own rounding of
+at most half a unit in the last place of each value on top (one BF16 step
+of a value above about 2.6 * RMS is already larger than 1e-2 * RMS, so no
+BF16 result could meet the bound against a BF16-rounded reference)."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+from group_limited_routed_gb300 import inputs
+
+LOGIT_RTOL = 1e-5
+MARGIN = 1e-6
+OUT_TOL = 1e-2
+
+
+def host(t: torch.Tensor) -> np.ndarray:
+    if t.dtype == torch.bfloat16:
+        return inputs.bf16_bits(t)
+    return t.detach().cpu().numpy()
+
+
+def oracle_route(cfg, tens):
+    lg = oracle.router_logits(host(tens["hidden"]), host(tens["router_w"]))
+    r = oracle.route(lg, host(tens["corr_bias"]), cfg.n_groups, cfg.topk_groups, cfg.topk,
+                     cfg.routed_scale)
+    return lg, r
+
+
+def check_logits(got: np.ndarray, ref: np.ndarray):
+    """|got - ref| <= 1e-5 * max(|ref|, RMS of the reference row)."""
+    rms = np.sqrt((ref.astype(np.float64) ** 2).mean(axis=1, keepdims=True))
+    bound = LOGIT_RTOL * np.maximum(np.abs(ref), rms)
+    err = np.abs(got.astype(np.float64) - ref.astype(np.float64))
+    bad = err > bound
+    assert not bad.any(), f"{bad.sum()} logits out of tolerance; worst {(err / bound).max():.3g}x"
+
+
+def exempt_tokens(r) -> np.ndarray:
+    return (r["expert_margin"] < MARGIN) | (r["group_margin"] < MARGIN)
+
+
+# Routing-weight tolerance when the GPU computed its own logits: a logit off
+# by up to 1e-5 * max(|logit|, RMS) moves s = sigmoid(logit) by (1 - s) times
+# that, relatively, and w = 2.5 s / sum(s) by at most twice it; logits reach a
+# few units, so 1e-4 covers it.  Fed the oracle's logits, only the FP32
+# sigmoid's last-place differences remain (1e-6).
+W_RTOL_ROUTE = 1e-4
+W_RTOL_SELECT = 1e-6
+
+
+def check_routing(cfg, idx: np.ndarray, w: np.ndarray, r, w_rtol=W_RTOL_ROUTE):
+    """Indices bit-exact (slot order included) on non-exempt tokens; exempt
+    tokens must still pick a valid near-tie set; weights close."""
+    ex = exempt_tokens(r)
+    ok = ~ex
+    assert np.array_equal(idx[ok], r["idx"][ok]), \
+        f"{(idx[ok] != r['idx'][ok]).any(axis=1).sum()} tokens route differently"
+    assert np.allclose(w[ok], r["w"][ok], rtol=w_rtol, atol=0)
+    S = cfg.n_experts // cfg.n_groups
+    for t in np.nonzero(ex)[0]:
+        row = idx[t]
+        assert len(set(row.tolist())) == cfg.topk
+        c = r["c"][t]
+        kth = np.sort(c[r["idx"][t]])[0]
+        # every chosen expert is at most a margin away from the oracle's k-th
+        assert np.all(c[row] >= kth - 4 * MARGIN)
+        assert len({int(e) // S for e in row}) <= cfg.topk_groups
+    assert np.all(np.abs(w.astype(np.float64).sum(1) - cfg.routed_scale) <= 1e-5)
+    return ex
+
+
+def half_ulp_bf16(v: np.ndarray) -> np.ndarray:
+    """Half the BF16 spacing at |v| (8 significant bits)."""
+    _, e = np.frexp(np.abs(v))
+    return np.where(v == 0, 0.0, np.ldexp(1.0, e - 9))
+
+
+def check_out(got, ref, rows=None, tol=OUT_TOL):
+    """ref = (bf16 bits, exact float64) as the oracle returns them.  Asserts
+    |got - exact| <= tol * RMS(exact) + half a BF16 step of exact; returns
+    (max |got - exact|, RMS, fraction bit-identical to the oracle's BF16)."""
+    bits, exact = ref
+    g = got.double().cpu().numpy() if isinstance(got, torch.Tensor) else got
+    o16 = oracle.bf16_to_f64(bits)
+    if rows is not None:
+        g, exact, o16 = g[rows], exact[rows], o16[rows]
+    if g.size == 0:
+        return 0.0, 0.0, 1.0
+    rms = np.sqrt((exact ** 2).mean())
+    err = np.abs(g - exact)
+    excess = err - (tol * rms + half_ulp_bf16(exact))
+    print(f"  arithmetic error beyond BF16 rounding: {max(0.0, float((err - half_ulp_bf16(exact)).max())) / rms:.2e} * RMS")
+    worst = np.unravel_index(np.argmax(excess), excess.shape)
+    assert excess.max() <= 0, (f"err {err[worst]:.4g} at {worst} (value {exact[worst]:.4g}) > "
+                               f"{tol} * RMS {rms:.4g} + half BF16 step")
+    return float(err.max()), float(rms), float((g == o16).mean())
+
+
+def expert_weights_host(tens, experts):
+    """Host copies of the BF16 weights of the listed experts (dict e -> arr)."""
+    wg, wu, wd = {}, {}, {}
+    for e in sorted({int(x) for x in experts}):
+        wg[e] = host(tens["w_gate"][e])
+        wu[e] = host(tens["w_up"][e])
+        wd[e] = host(tens["w_down"][e])
+    return wg, wu, wd
+
+
+def oracle_out(cfg, tens, idx, w, tokens=None):
+    """Oracle expert output for the given routing, only for `tokens` rows
+    (None = all), fetching only the weights those rows use."""
+    rows = np.arange(idx.shape[0]) if tokens is None else np.asarray(tokens)
+    wg, wu, wd = expert_weights_host(tens, idx[rows].reshape(-1))
+    return oracle.experts_bf16(host(tens["hidden"]), idx, w, wg, wu, wd, cfg.n_experts,
+                               tokens=None if tokens is None else rows, exact=True)

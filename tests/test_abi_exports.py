@@ -1,0 +1,55 @@
+"""The C-ABI library builds for sm_103a, loads without a GPU and exports
+every entry point include/beam_moe.h declares (no compute calls here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "beam_moe.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(beam_[a-z0-9_]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from group_limited_routed_gb300 import build
+    path = build.build()
+    return ctypes.CDLL(path)
+
+
+def test_header_declares_the_layer_entry_points():
+    names = _declared()
+    for n in ("beam_moe_route", "beam_moe_forward", "beam_moe_forward_routed",
+              "beam_moe_workspace_size", "beam_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    missing = [n for n in _declared() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_python_binding_names_match_exports(lib):
+    from group_limited_routed_gb300 import api
+    assert set(api.EXPORTS) <= set(_declared())
+
+
+def test_host_only_queries(lib):
+    from group_limited_routed_gb300 import api
+    from group_limited_routed_gb300.inputs import CONFIGS
+    beam = CONFIGS["decode"]
+    n = api.workspace_size(beam, 8192)
+    lay = api.layout(beam, 8192)
+    assert lay["total"] == n and n % 256 == 0
+    offs = sorted(v for k, v in lay.items() if k != "total")
+    assert offs[0] == 0 and all(o % 256 == 0 for o in offs)
+    assert api.kernels_per_forward(beam, 32) == 7
+    with pytest.raises(api.BeamError):
+        api.workspace_size(beam.replace(n_groups=7), 32)
+    lib.beam_status_string.restype = ctypes.c_char_p
+    assert lib.beam_status_string(5) == b"device-side wait timed out"

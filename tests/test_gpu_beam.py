@@ -1,0 +1,55 @@
+"""GPU parity at the full Beam layer sizes (d=5120, 256 experts, d_ff=2560),
+in the launch configuration the benchmark times.  Routing is compared on
+every token; expert outputs on every token of the decode batch and on a
+seeded sample of tokens of the larger batches (the oracle computes them one
+by one)."""
+import gc
+
+import numpy as np
+import pytest
+import torch
+
+import group_limited_routed_gb300 as pkg
+from group_limited_routed_gb300 import inputs
+
+from _parity import check_logits, check_out, check_routing, exempt_tokens, host, oracle_out, \
+    oracle_route
+
+pytestmark = pytest.mark.gpu
+
+
+def _sample(T, n, seed):
+    if T <= n:
+        return np.arange(T)
+    rng = np.random.default_rng(seed)
+    s = np.sort(rng.choice(T, n - 2, replace=False))
+    return np.unique(np.concatenate([[0, T - 1], s]))   # first and last token always
+
+
+@pytest.mark.parametrize("name,n_sample", [("decode", 32), ("prefill", 8), ("skewed", 8)])
+def test_beam_config_parity(name, n_sample):
+    cfg = inputs.CONFIGS[name]
+    t = inputs.generate(cfg, "cuda")
+    try:
+        lg, r = oracle_route(cfg, t)
+        ws = pkg.Workspace(cfg, cfg.T)
+        idx, w, logits = pkg.route(cfg, t["hidden"], t["router_w"], t["corr_bias"], ws=ws,
+                                   want_logits=True)
+        check_logits(host(logits), lg)
+        check_routing(cfg, host(idx), host(w), r)
+        out = pkg.forward(cfg, t["hidden"], t["router_w"], t["corr_bias"], t["w_gate"],
+                          t["w_up"], t["w_down"], ws=ws)
+        assert pkg.check_status(ws) == 0
+        rows = _sample(cfg.T, n_sample, seed=len(name))
+        rows = rows[~exempt_tokens(r)[rows]]
+        ref = oracle_out(cfg, t, r["idx"], r["w"], tokens=rows)
+        err, rms, same = check_out(out, ref, rows=rows)
+        print(f"{name}: {len(rows)} tokens, max|err| {err:.3e}, RMS {rms:.3e}, "
+              f"bit-identical {same:.4f}")
+        if name == "skewed":
+            counts = np.bincount(host(idx).reshape(-1), minlength=cfg.n_experts)
+            assert counts.max() > cfg.T // 2       # a few experts take most tokens
+    finally:
+        del t
+        gc.collect()
+        torch.cuda.empty_cache()

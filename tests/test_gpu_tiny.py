@@ -1,0 +1,174 @@
+"""GPU parity on the small workload and its variants: every step of the CUDA
+path against the CPU oracle on the same seeded inputs, through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import group_limited_routed_gb300 as pkg
+from group_limited_routed_gb300 import inputs
+
+from _parity import (W_RTOL_SELECT, check_logits, check_out, check_routing, exempt_tokens, host,
+                     oracle_out, oracle_route)
+
+pytestmark = pytest.mark.gpu
+CFG = inputs.CONFIGS["tiny"]
+
+
+@pytest.fixture(scope="module")
+def tiny():
+    dev = torch.device("cuda")
+    t = inputs.generate(CFG, dev)
+    lg, r = oracle_route(CFG, t)
+    return t, lg, r
+
+
+def test_route_matches_oracle(tiny):
+    t, lg, r = tiny
+    idx, w, logits = pkg.route(CFG, t["hidden"], t["router_w"], t["corr_bias"], want_logits=True)
+    check_logits(host(logits), lg)
+    check_routing(CFG, host(idx), host(w), r)
+
+
+def test_select_alone_on_oracle_logits(tiny):
+    t, lg, r = tiny
+    idx, w = pkg.select(CFG, torch.from_numpy(lg).cuda(), t["corr_bias"])
+    check_routing(CFG, host(idx), host(w), r, w_rtol=W_RTOL_SELECT)
+
+
+def test_forward_routed_matches_oracle(tiny):
+    t, lg, r = tiny
+    out = pkg.forward_routed(CFG, t["hidden"], torch.from_numpy(r["idx"]).cuda(),
+                             torch.from_numpy(r["w"]).cuda(), t["w_gate"], t["w_up"], t["w_down"])
+    ref = oracle_out(CFG, t, r["idx"], r["w"])
+    check_out(out, ref)
+
+
+def test_forward_matches_oracle(tiny):
+    t, lg, r = tiny
+    ws = pkg.Workspace(CFG, CFG.T)
+    out = pkg.forward(CFG, t["hidden"], t["router_w"], t["corr_bias"], t["w_gate"], t["w_up"],
+                      t["w_down"], ws=ws)
+    assert pkg.check_status(ws) == 0
+    ref = oracle_out(CFG, t, r["idx"], r["w"])
+    keep = ~exempt_tokens(r)
+    check_out(out, ref, rows=keep)
+
+
+def test_permutation_is_a_stable_counting_sort(tiny):
+    t, lg, r = tiny
+    ws = pkg.Workspace(CFG, CFG.T)
+    pkg.forward_routed(CFG, t["hidden"], torch.from_numpy(r["idx"]).cuda(),
+                       torch.from_numpy(r["w"]).cuda(), t["w_gate"], t["w_up"], t["w_down"], ws=ws)
+    torch.cuda.synchronize()
+    TK = CFG.T * CFG.topk
+    E = CFG.n_experts
+    flat = r["idx"].reshape(-1)
+    order = np.argsort(flat, kind="stable")
+    counts = np.bincount(flat, minlength=E)
+    assert np.array_equal(host(ws.view("counts", torch.int32, (E,))), counts)
+    assert np.array_equal(host(ws.view("offsets", torch.int32, (E + 1,))),
+                          np.concatenate([[0], np.cumsum(counts)]))
+    assert np.array_equal(host(ws.view("perm_src", torch.int32, (TK,))), order)
+    inv = np.empty(TK, np.int64)
+    inv[order] = np.arange(TK)
+    assert np.array_equal(host(ws.view("pair_row", torch.int32, (TK,))), inv)
+    assert np.array_equal(host(ws.view("perm_w", torch.float32, (TK,))), r["w"].reshape(-1)[order])
+    xp = ws.view("x_perm", torch.bfloat16, (TK, CFG.d))
+    assert torch.equal(xp, t["hidden"][torch.from_numpy(order // CFG.topk).cuda()])
+
+
+def test_deterministic_bitwise(tiny):
+    t, _, _ = tiny
+    args = (CFG, t["hidden"], t["router_w"], t["corr_bias"], t["w_gate"], t["w_up"], t["w_down"])
+    a = pkg.forward(*args)
+    b = pkg.forward(*args)
+    assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("T", [1, 2, 5, 37, 130, 300])
+def test_ragged_token_counts(T):
+    """Token counts that fill no tile evenly (and, at 300, the 128-wide tile)."""
+    cfg = CFG.replace(T=T, seed=10 + T)
+    t = inputs.generate(cfg, "cuda")
+    lg, r = oracle_route(cfg, t)
+    out = pkg.forward(cfg, t["hidden"], t["router_w"], t["corr_bias"], t["w_gate"], t["w_up"],
+                      t["w_down"])
+    ref = oracle_out(cfg, t, r["idx"], r["w"])
+    check_out(out, ref, rows=~exempt_tokens(r))
+    idx, w = pkg.route(cfg, t["hidden"], t["router_w"], t["corr_bias"])
+    check_routing(cfg, host(idx), host(w), r)
+
+
+def test_zero_tokens_is_a_no_op():
+    t = inputs.generate(CFG, "cuda", T=4)
+    out = torch.full((0, CFG.d), 7, dtype=torch.bfloat16, device="cuda")
+    x = t["hidden"][:0]
+    o = pkg.forward(CFG, x, t["router_w"], t["corr_bias"], t["w_gate"], t["w_up"], t["w_down"],
+                    out=out)
+    assert o.shape == (0, CFG.d)
+
+
+def test_all_tokens_on_one_expert_and_idle_experts():
+    """Bias forces every token onto the same 8 experts: one expert gets all T
+    rows (several token tiles), 56 experts get none."""
+    cfg = CFG.replace(T=300, seed=77)
+    t = inputs.generate(cfg, "cuda")
+    b = t["corr_bias"].clone()
+    b[[3, 4, 9, 12, 17, 18, 25, 26]] += 5.0
+    t["corr_bias"] = b
+    lg, r = oracle_route(cfg, t)
+    assert np.all(np.sort(r["idx"], 1) == [3, 4, 9, 12, 17, 18, 25, 26])
+    out = pkg.forward(cfg, t["hidden"], t["router_w"], t["corr_bias"], t["w_gate"], t["w_up"],
+                      t["w_down"])
+    ref = oracle_out(cfg, t, r["idx"], r["w"])
+    check_out(out, ref, rows=~exempt_tokens(r))
+
+
+def test_all_equal_scores_follow_the_tie_rule():
+    """Zero router and zero bias: every score ties; lower indices win."""
+    t = inputs.generate(CFG, "cuda", T=33)
+    idx, w = pkg.route(CFG, t["hidden"], torch.zeros_like(t["router_w"]),
+                       torch.zeros_like(t["corr_bias"]))
+    assert np.array_equal(host(idx), np.tile(np.arange(8), (33, 1)))
+    assert np.all(host(w) == np.float32(2.5 / 8))
+
+
+def test_identical_experts_give_scaled_single_expert():
+    """All experts equal => out = bf16(2.5 * y(x)) whatever the routing."""
+    cfg = CFG.replace(T=40, seed=5)
+    t = inputs.generate(cfg, "cuda")
+    for k in ("w_gate", "w_up", "w_down"):
+        t[k] = t[k][:1].expand_as(t[k]).contiguous()
+    out = pkg.forward(cfg, t["hidden"], t["router_w"], t["corr_bias"], t["w_gate"], t["w_up"],
+                      t["w_down"])
+    one = np.zeros((cfg.T, 1), np.int32)
+    ref = oracle.experts_bf16(host(t["hidden"]), one, np.full((cfg.T, 1), 2.5, np.float32),
+                              {0: host(t["w_gate"][0])}, {0: host(t["w_up"][0])},
+                              {0: host(t["w_down"][0])}, cfg.n_experts, exact=True)
+    check_out(out, ref)
+
+
+def test_invalid_routed_index_latches_device_check():
+    t = inputs.generate(CFG, "cuda", T=8)
+    ws = pkg.Workspace(CFG, 8)
+    idx = torch.zeros(8, CFG.topk, dtype=torch.int32, device="cuda")
+    idx[:, :] = torch.arange(CFG.topk, dtype=torch.int32, device="cuda")
+    idx[3, 2] = CFG.n_experts + 5
+    w = torch.full((8, CFG.topk), 0.25, device="cuda")
+    pkg.forward_routed(CFG, t["hidden"], idx, w, t["w_gate"], t["w_up"], t["w_down"], ws=ws)
+    assert pkg.check_status(ws) == 6
+    assert pkg.check_status(ws) == 0   # cleared by the read
+
+
+def test_host_side_argument_errors():
+    t = inputs.generate(CFG, "cuda", T=4)
+    bad = CFG.replace(d=500)
+    with pytest.raises(pkg.BeamError) as e:
+        pkg.workspace_size(bad, 4)
+    assert e.value.code == 1
+    ws = pkg.Workspace(CFG, 2)
+    with pytest.raises(pkg.BeamError) as e:
+        pkg.forward(CFG, t["hidden"], t["router_w"], t["corr_bias"], t["w_gate"], t["w_up"],
+                    t["w_down"], ws=ws)
+    assert e.value.code == 3
