@@ -1,0 +1,368 @@
+"""Benchmark of the Beam MoE layer on GB300 (one JSON line on stdout).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config decode]
+    python bench.py --impl reference ...      # the CPU oracle as the reference arm
+
+A step is one call of the whole layer (router, selection, permute, gather,
+gate/up GEMM, down GEMM, combine) on one batch of the workload, with every
+input resident in device memory.  Metric: layer tokens/s.  The expert weights
+a step touches (about 12 GB for the decode batch) are far larger than L2, so
+no flush is needed between steps.  Timing: CUDA events on the launching
+stream around the K timed steps, bracketed by a barrier and a device
+synchronisation, max over ranks.  Per-kernel durations come from events the
+library records at its step boundaries during the same timed steps.
+
+Multi-GPU: the layer's token batches are independent; under torchrun each
+rank runs its own replica on its own GPU (replicas only, no collective on the
+data path; the process group only aggregates timings).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import group_limited_routed_gb300 as pkg  # noqa: E402
+from group_limited_routed_gb300 import inputs  # noqa: E402
+
+METRIC = "Beam MoE-layer tokens/s"
+UNIT = "tokens/s"
+STAGES = ["router", "select", "permute", "gather", "gate_up", "down", "combine"]
+DOMINANT = "gate_up"
+DOMINANT_SRC = [os.path.join(ROOT, "group_limited_routed_gb300", "csrc", f)
+                for f in ("expert_gemm.cu", "ptx.cuh", "common.cuh")]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+# ------------------------------------------------------------------ helpers
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")), ws
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        return {"hbm_gbs": float(j["hbm_gbs"]), "bf16_tflops": float(j["bf16_tflops"]),
+                "bf16_tflops_sustained": float(j.get("bf16_tflops_sustained", j["bf16_tflops"])),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples while the timed region runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100", "-f", self.path],
+                stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                p = [x.strip() for x in line.split(",")]
+                if len(p) >= 9:
+                    rows.append(p)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+def touched_experts(ws, cfg) -> int:
+    idx = ws.view("topk_idx", torch.int32, (cfg.T, cfg.topk))
+    return int(torch.unique(idx).numel())
+
+
+def file_sha(paths) -> str:
+    h = hashlib.sha256()
+    for p in paths:
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu capture, when the kernel's
+    source is unchanged since it was taken."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    with open(TRAFFIC_FILE) as f:
+        j = json.load(f)
+    ent = j.get(kernel, {}).get(workload)
+    if not ent or ent.get("source_sha") != file_sha(DOMINANT_SRC):
+        return None
+    return ent.get("bytes_per_launch")
+
+
+# ------------------------------------------------------------------ CPU oracle
+def oracle_sample(cfg, t, n_tokens: int, seed: int = 0):
+    """Runs the CPU oracle (router + selection for the whole batch, experts
+    and combine for n_tokens sampled tokens); returns (seconds, sampled)."""
+    import oracle
+    rng = np.random.default_rng(seed)
+    rows = np.sort(rng.choice(cfg.T, size=min(n_tokens, cfg.T), replace=False))
+    x = inputs.bf16_bits(t["hidden"])
+    wr = t["router_w"].cpu().numpy()
+    b = t["corr_bias"].cpu().numpy()
+    # weights the sample needs, fetched before the clock starts
+    lg = oracle.router_logits(x, wr)
+    r = oracle.route(lg, b, cfg.n_groups, cfg.topk_groups, cfg.topk, cfg.routed_scale)
+    need = sorted({int(e) for e in r["idx"][rows].reshape(-1)})
+    wg = {e: inputs.bf16_bits(t["w_gate"][e]) for e in need}
+    wu = {e: inputs.bf16_bits(t["w_up"][e]) for e in need}
+    wd = {e: inputs.bf16_bits(t["w_down"][e]) for e in need}
+    t0 = time.perf_counter()
+    lg = oracle.router_logits(x[rows], wr)
+    r = oracle.route(lg, b, cfg.n_groups, cfg.topk_groups, cfg.topk, cfg.routed_scale)
+    oracle.experts_bf16(x[rows], r["idx"], r["w"], wg, wu, wd, cfg.n_experts)
+    return time.perf_counter() - t0, len(rows)
+
+
+def cpu_baseline(cfg, t, budget_s: float = 12.0) -> dict:
+    """The oracle on about budget_s seconds of the same workload: sampled
+    tokens of the batch, or the whole batch repeated when it is quicker."""
+    import oracle
+    sec1, n1 = oracle_sample(cfg, t, 1, seed=1)
+    per_tok = sec1 / n1
+    n = int(max(1, min(cfg.T, budget_s / max(per_tok, 1e-6))))
+    reps = 1
+    if n == cfg.T:
+        full, _ = oracle_sample(cfg, t, cfg.T, seed=2)
+        reps = int(max(1, min(100, budget_s / max(full, 1e-6))))
+    sec = 0.0
+    toks = 0
+    for r in range(reps):
+        s, m = oracle_sample(cfg, t, n, seed=2 + r)
+        sec += s
+        toks += m
+    what = (f"the whole {cfg.T}-token {cfg.name} batch, {reps} times" if n == cfg.T
+            else f"{n} of the {cfg.T} tokens of one {cfg.name} batch")
+    return {"value": toks / sec, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": (f"{what}: FP32 router and group-limited selection, the tokens' 8 SwiGLU "
+                       f"experts and the combine, FP64 accumulation; {sec:.1f} s of CPU work")}
+
+
+# ------------------------------------------------------------------ arms
+def run_reference(args, cfg):
+    rank, local, world = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    dev = torch.device("cuda", local) if torch.cuda.is_available() else torch.device("cpu")
+    gen_cfg = cfg if dev.type == "cuda" else cfg.replace(cpu_generator=True)
+    t = inputs.generate(gen_cfg, dev)
+    # size each step so the whole run stays within about two minutes
+    sec1, _ = oracle_sample(cfg, t, 1, seed=1)
+    per_step_budget = 120.0 / max(1, args.steps + args.warmup)
+    n = int(max(1, min(cfg.T, per_step_budget / max(sec1, 1e-6))))
+    for i in range(args.warmup):
+        oracle_sample(cfg, t, n, seed=100 + i)
+    secs = 0.0
+    toks = 0
+    for i in range(args.steps):
+        s, m = oracle_sample(cfg, t, n, seed=1000 + i)
+        secs += s
+        toks += m
+    value = toks / secs
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": config_record(cfg, None),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(),
+                             "kind": "oracle",
+                             "sample": f"{n} sampled tokens of the {cfg.T}-token batch per step"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_record(cfg, touched):
+    rec = {"workload": cfg.description, "T": cfg.T, "d": cfg.d, "n_experts": cfg.n_experts,
+           "n_groups": cfg.n_groups, "topk_groups": cfg.topk_groups, "topk": cfg.topk,
+           "d_ff": cfg.d_ff, "routed_scale": cfg.routed_scale, "weights": cfg.weight_fmt,
+           "seed": cfg.seed, "parallelism": "replicas (one independent layer per GPU)",
+           "l2": "no flush: each step streams the touched experts' weights, far larger than "
+                 "the 129 MB L2"}
+    if touched is not None:
+        rec["touched_experts"] = touched
+    return rec
+
+
+def run_gpu(args, cfg):
+    rank, local, world = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    use_dist = world > 1
+    if use_dist:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    t = inputs.generate(cfg.replace(seed=cfg.seed + 1000 * rank) if rank else cfg, dev)
+    ws = pkg.Workspace(cfg, cfg.T, dev)
+    stream = torch.cuda.current_stream()
+    out = torch.empty(cfg.T, cfg.d, dtype=torch.bfloat16, device=dev)
+    args_l = (cfg, t["hidden"], t["router_w"], t["corr_bias"], t["w_gate"], t["w_up"], t["w_down"])
+
+    def step(o=out):
+        return pkg.forward(*args_l, out=o, ws=ws, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if pkg.check_status(ws) != 0:
+        raise RuntimeError("device status after warm-up")
+    touched = touched_experts(ws, cfg)
+
+    # per-step stage events (created and recorded once so the handles exist)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(args.steps)]
+    for row in evs:
+        for e in row:
+            e.record(stream)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local)
+    sampler.start()
+    for _ in range(max(3, args.warmup)):
+        step()
+    if use_dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_start.record(stream)
+    for i in range(args.steps):
+        pkg.set_stage_events(evs[i])
+        step()
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if use_dist:
+        dist.barrier()
+    pkg.set_stage_events(None)
+    clocks = sampler.stop()
+    ms = t_start.elapsed_time(t_end)
+    stage_ms = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(7)]
+                         for i in range(args.steps)]).mean(axis=0)
+    if pkg.check_status(ws) != 0:
+        raise RuntimeError("device status after the timed region")
+
+    # end to end through the public API: pinned host in, pinned host out
+    x_host = t["hidden"].cpu().pin_memory()
+    o_host = torch.empty(cfg.T, cfg.d, dtype=torch.bfloat16).pin_memory()
+    e2e_steps = max(3, min(args.steps, 200))
+    for _ in range(3):
+        pkg.forward(cfg, x_host, *args_l[2:], out=o_host, ws=ws, stream=stream)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        pkg.forward(cfg, x_host, *args_l[2:], out=o_host, ws=ws, stream=stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+
+    times = torch.tensor([ms, e2e_ms], device=dev)
+    if use_dist:
+        dist.all_reduce(times, op=dist.ReduceOp.MAX)
+    ms, e2e_ms = float(times[0]), float(times[1])
+    value = world * cfg.T * args.steps / (ms / 1e3)
+    e2e_value = world * cfg.T * e2e_steps / (e2e_ms / 1e3)
+
+    pk = peaks()
+    E_b = cfg.d * cfg.d_ff * 2
+    gu_bytes = touched * 2 * E_b + cfg.T * cfg.topk * (cfg.d + cfg.d_ff) * 2
+    gu_gbs = gu_bytes / (stage_ms[4] / 1e3) / 1e9
+    layer_bytes = touched * 3 * E_b + cfg.n_experts * cfg.d * 4 + cfg.n_experts * 4 \
+        + 2 * cfg.T * cfg.d * 2
+    layer_ms = ms / args.steps
+    layer_flops = 2 * cfg.T * cfg.d * cfg.n_experts + 6 * cfg.T * cfg.topk * cfg.d * cfg.d_ff
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": layer_ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": config_record(cfg, touched),
+        "roofline": {"bound": "hbm", "kernel": DOMINANT, "achieved": gu_gbs,
+                     "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": gu_gbs / pk["hbm_gbs"],
+                     "peak_source": pk["source"],
+                     "traffic": traffic_for(DOMINANT, cfg.name),
+                     "algorithmic_bytes_per_launch": gu_bytes},
+        "layer_roofline": {"bound": "hbm", "algorithmic_bytes": layer_bytes,
+                           "achieved": layer_bytes / (layer_ms / 1e3) / 1e9,
+                           "peak": pk["hbm_gbs"], "unit": "GB/s",
+                           "frac": layer_bytes / (layer_ms / 1e3) / 1e9 / pk["hbm_gbs"],
+                           "tflops": layer_flops / (layer_ms / 1e3) / 1e12},
+        "stage_us": {n: round(float(v) * 1e3, 1) for n, v in zip(STAGES, stage_ms)},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": cfg.T * cfg.d * 2,
+                "d2h_bytes_per_step": cfg.T * cfg.d * 2},
+        "gpu_launches": args.steps * pkg.kernels_per_forward(cfg, cfg.T),
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(cfg, t)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if use_dist:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--config", default="decode", choices=sorted(inputs.CONFIGS))
+    ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    args.warmup = max(3, args.warmup)
+    cfg = inputs.CONFIGS[args.config]
+    if args.impl == "reference":
+        return run_reference(args, cfg)
+    return run_gpu(args, cfg)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

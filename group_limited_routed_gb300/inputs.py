@@ -62,6 +62,12 @@ CONFIGS = {
                         **_BEAM,
                         description="Beam MoE layer skewed routing T=4096, bias +2.0 on "
                                     "16 random experts"),
+    # profiling case: the Beam expert shapes with 32 experts (2.5 GB held on
+    # the device, more than 1 GB of gate/up weights streamed per call)
+    "profile_small": MoEConfig(name="profile_small", T=8, d=5120, n_experts=32, n_groups=8,
+                               topk_groups=4, topk=8, d_ff=2560, seed=5,
+                               description="Beam expert shapes, 32 experts (8x4), T=8 "
+                                           "(profiling case)"),
     "nvfp4": MoEConfig(name="nvfp4", T=128, seed=4, weight_fmt="nvfp4", **_BEAM,
                        description="Beam MoE layer NVFP4 experts T=128 (E2M1 + E4M3 per "
                                    "16 along K + FP32 per-tensor scale)"),
