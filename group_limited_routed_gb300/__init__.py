@@ -13,7 +13,7 @@ def __getattr__(name):
     # on machines without the compiled library
     if name in ("route", "select", "forward", "forward_routed", "workspace_size", "Workspace",
                 "check_status", "BeamError", "library_path", "lib", "set_stage_events",
-                "set_debug", "layout", "kernels_per_forward", "EXPORTS"):
+                "set_debug", "layout", "kernels_per_forward", "EXPORTS", "forward_noalloc"):
         from . import api
         return getattr(api, name)
     raise AttributeError(name)

@@ -30,6 +30,7 @@ STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "workspace too sm
 
 EXPORTS = ("beam_moe_workspace_size", "beam_moe_workspace_layout", "beam_moe_route",
            "beam_moe_select", "beam_moe_forward", "beam_moe_forward_routed",
+           "beam_moe_forward_noalloc",
            "beam_moe_check_status", "beam_moe_set_stage_events", "beam_moe_set_debug",
            "beam_moe_kernels_per_forward", "beam_status_string")
 
@@ -74,6 +75,8 @@ def lib():
         L.beam_moe_forward.restype = _ST
         L.beam_moe_forward_routed.argtypes = [cfgp, _P, _P, _P, _P, _P, _P, _P, _I64, _P, _SZ, _P]
         L.beam_moe_forward_routed.restype = _ST
+        L.beam_moe_forward_noalloc.argtypes = [cfgp, _P, _P, _P, _P, _P, _P, _P, _I64, _P]
+        L.beam_moe_forward_noalloc.restype = _ST
         L.beam_moe_check_status.argtypes = [_P, _P]
         L.beam_moe_check_status.restype = _ST
         L.beam_moe_set_stage_events.argtypes = [ctypes.POINTER(_P), ctypes.c_int32]
@@ -233,6 +236,25 @@ def forward_routed(cfg, hidden, topk_idx, topk_w, w_gate, w_up, w_down, out=None
                                          _dev(w_down, torch.bfloat16, "w_down"), o.data_ptr(), T,
                                          ws.ptr, ws.nbytes, _stream(stream)),
            "beam_moe_forward_routed")
+    return o
+
+
+def forward_noalloc(cfg, hidden, router_w, corr_bias, w_gate, w_up, w_down, out=None,
+                    stream=None):
+    """The whole layer without a workspace: for callers that cannot allocate
+    device memory (the library's fixed 32 MiB device array holds the
+    intermediates; small batches only, see beam_moe.h).  Calls overlapping on
+    the GPU race on that array."""
+    T = hidden.shape[0]
+    o = torch.empty(T, cfg.d, dtype=torch.bfloat16, device=hidden.device) if out is None else out
+    c = _cfg(cfg)
+    _check(lib().beam_moe_forward_noalloc(ctypes.byref(c), _dev(hidden, torch.bfloat16, "hidden"),
+                                          _dev(router_w, torch.float32, "router_w"),
+                                          _dev(corr_bias, torch.float32, "corr_bias"),
+                                          _dev(w_gate, torch.bfloat16, "w_gate"),
+                                          _dev(w_up, torch.bfloat16, "w_up"),
+                                          _dev(w_down, torch.bfloat16, "w_down"), o.data_ptr(),
+                                          T, _stream(stream)), "beam_moe_forward_noalloc")
     return o
 
 

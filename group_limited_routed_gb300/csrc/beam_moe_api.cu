@@ -300,6 +300,30 @@ beam_status_t run_experts(const beam_moe_config_t& c, const void* hidden, const 
   return cuda_status(cudaGetLastError());
 }
 
+// ---------------------------------------------------------------- no-allocation scratch
+// Scratch for beam_moe_forward_noalloc, which serves callers that cannot
+// allocate device memory.  A fixed-size device array takes the place of the
+// caller's workspace.  Every GPU that loads this library's module holds it
+// until the process exits.  In host code `g_noalloc_scratch` only names the
+// symbol: its device address comes from cudaGetSymbolAddress, taken once per
+// device with that device current.
+constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;  // 32 MiB
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+void* noalloc_scratch_address() {
+  static void* addr[64] = {};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
+    addr[dev] = p;
+  }
+  return addr[dev];
+}
+
 }  // namespace
 
 extern "C" {
@@ -417,6 +441,22 @@ beam_status_t beam_moe_forward_routed(const beam_moe_config_t* cfg, const void* 
   record(2, s);
   return run_experts(*cfg, hidden, topk_idx, topk_w, w_gate, w_up, w_down, out, T, workspace, L,
                      dev, s);
+}
+
+beam_status_t beam_moe_forward_noalloc(const beam_moe_config_t* cfg, const void* hidden,
+                                       const float* router_w, const float* corr_bias,
+                                       const void* w_gate, const void* w_up, const void* w_down,
+                                       void* out, int64_t T, void* stream) {
+  if (!valid_cfg(cfg) || T < 0 || T > (int64_t(1) << 31) / 64) return BEAM_ERR_INVALID_ARG;
+  if (T == 0) return BEAM_OK;
+  if (make_layout(*cfg, T).total > kNoAllocScratchBytes) return BEAM_ERR_WORKSPACE;
+  void* scratch = noalloc_scratch_address();
+  if (!scratch) return BEAM_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // the status word latches the first kernel-side error: it must start at 0
+  if (cudaMemsetAsync(scratch, 0, kAlign, s) != cudaSuccess) return BEAM_ERR_CUDA;
+  return beam_moe_forward(cfg, hidden, router_w, corr_bias, w_gate, w_up, w_down, out, T,
+                          scratch, kNoAllocScratchBytes, stream);
 }
 
 beam_status_t beam_moe_check_status(void* workspace, void* stream) {

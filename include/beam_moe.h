@@ -148,6 +148,34 @@ beam_status_t beam_moe_forward_routed(const beam_moe_config_t *cfg, const void *
                                       const void *w_down, void *out, int64_t T,
                                       void *workspace, size_t ws_bytes, void *stream);
 
+/* beam_moe_forward without a caller workspace and without any allocation.
+ * The pages have no counterpart: this entry point exists for callers that
+ * cannot allocate device memory at all -- a plugin inside a host application
+ * that owns the whole device-memory budget and forbids allocations, or code
+ * that must never enter cudaMalloc's implicit device synchronisation.  They
+ * still pass every input and the output as device pointers, as for
+ * beam_moe_forward; the intermediate buffers live in one fixed 32 MiB device
+ * array inside this library (held on every GPU that loads the library until
+ * the process exits).
+ *   - Size limit: calls whose beam_moe_workspace_size(cfg, T, BEAM_WEIGHTS_BF16)
+ *     exceeds 32 MiB return BEAM_ERR_WORKSPACE before anything is launched
+ *     (Beam shapes: up to 108 tokens).
+ *   - The first call on a device looks up the array's device address (one
+ *     cudaGetSymbolAddress with that device current); make that first call
+ *     before any stream capture.
+ *   - Every call shares the one array and it keeps the previous call's
+ *     contents; the call clears the status word it needs at zero.  Calls
+ *     whose work overlaps on the GPU (other streams, other host threads) race
+ *     on it: serialise them.
+ *   - Kernel-side errors latch in that private array; the return value
+ *     reports argument and launch errors only.
+ *   - No cudaMalloc, cudaFree or allocating library routine is called. */
+beam_status_t beam_moe_forward_noalloc(const beam_moe_config_t *cfg, const void *hidden,
+                                       const float *router_w, const float *corr_bias,
+                                       const void *w_gate, const void *w_up,
+                                       const void *w_down, void *out, int64_t T,
+                                       void *stream);
+
 /* Synchronises `stream`, returns the workspace's latched status and clears
  * it.  The only entry point that waits for the device. */
 beam_status_t beam_moe_check_status(void *workspace, void *stream);
