@@ -3,8 +3,9 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config decode]
     python bench.py --impl reference ...      # the CPU oracle as the reference arm
 
-A step is one call of the whole layer (router, selection, permute, gather,
-gate/up GEMM, down GEMM, combine) on one batch of the workload, with every
+A step is one call of the whole layer (router, selection, permute, gather of
+the token rows (inside the gate/up GEMM for decode-sized batches), gate/up
+GEMM, down GEMM, combine) on one batch of the workload, with every
 input resident in device memory.  Metric: layer tokens/s.  The expert weights
 a step touches (about 12 GB for the decode batch) are far larger than L2, so
 no flush is needed between steps.  Timing: CUDA events on the launching

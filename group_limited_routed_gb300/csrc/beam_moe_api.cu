@@ -18,7 +18,8 @@ namespace {
 using beam::GemmArgs;
 
 constexpr size_t kAlign = 256;
-constexpr int kMinRows = 128;  // token-operand buffers hold at least one full tile
+constexpr int kMinRows = 256;  // token-operand buffers hold at least one full tile
+constexpr int64_t kTensorRouterMinT = 256;  // from here on the router runs on tensor cores
 constexpr uint64_t kDefaultWaitNs = 2000000000ull;
 
 size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
@@ -115,13 +116,20 @@ int router_chunk(const beam_moe_config_t& c, int ks) {
   return static_cast<int>(((c.d + ks - 1) / ks + 31) / 32 * 32);
 }
 
-int token_tile(const beam_moe_config_t& c, int64_t TK) {
-  return TK <= 4LL * c.n_experts ? 16 : 128;
+// Token-block widths of the two expert GEMMs: 16 when experts see a few rows
+// each (weight streaming), else 128 (gate/up, two accumulators) and 256
+// (down) for the compute-bound regime.
+bool small_batch(const beam_moe_config_t& c, int64_t TK) { return TK <= 4LL * c.n_experts; }
+int gateup_tile(const beam_moe_config_t& c, int64_t TK) { return small_batch(c, TK) ? 16 : 128; }
+int down_tile(const beam_moe_config_t& c, int64_t TK) { return small_batch(c, TK) ? 16 : 256; }
+
+bool tensor_router(const beam_moe_config_t& c, int64_t T) {
+  return T >= kTensorRouterMinT && c.n_experts % 128 == 0;
 }
 
 struct Layout {
   size_t status, part, logits, idx, w, counts, offsets, perm_src, pair_row, perm_w, x_perm, h, y,
-      total;
+      router_planes, total;
 };
 
 Layout make_layout(const beam_moe_config_t& c, int64_t T_max) {
@@ -150,9 +158,10 @@ Layout make_layout(const beam_moe_config_t& c, int64_t T_max) {
   L.perm_src = take(static_cast<size_t>(TK) * 4);
   L.pair_row = take(static_cast<size_t>(TK) * 4);
   L.perm_w = take(static_cast<size_t>(TK) * 4);
-  L.x_perm = take(static_cast<size_t>(rows) * c.d * 2);
+  L.x_perm = take(small_batch(c, TK) ? 0 : static_cast<size_t>(rows) * c.d * 2);
   L.h = take(static_cast<size_t>(rows) * c.d_ff * 2);
   L.y = take(static_cast<size_t>(rows) * c.d * 4);
+  L.router_planes = take(T_max >= kTensorRouterMinT ? static_cast<size_t>(E) * 3 * c.d * 2 : 0);
   L.total = off;
   return L;
 }
@@ -188,20 +197,35 @@ beam_status_t common_checks(const beam_moe_config_t* cfg, int64_t T, void* ws, s
 // router + selection into idx/w (and logits)
 beam_status_t run_route(const beam_moe_config_t& c, const void* hidden, const float* router_w,
                         const float* bias, int64_t T, int32_t* idx, float* w, float* logits,
-                        void* ws, const Layout& L, cudaStream_t s) {
-  const int ks = router_ksplit(c, T);
-  beam::RouterArgs ra;
-  ra.x = static_cast<const uint16_t*>(hidden);
-  ra.w = router_w;
-  ra.part = at<float>(ws, L.part);
-  ra.T = T;
-  ra.d = c.d;
-  ra.E = c.n_experts;
-  ra.k_chunk = router_chunk(c, ks);
-  beam::launch_router(ra, ks, s);
+                        void* ws, const Layout& L, const DevInfo& dev, cudaStream_t s) {
+  int ks = 1;
+  float* part = at<float>(ws, L.part);
+  if (tensor_router(c, T)) {
+    // BF16x3 on the tensor cores: W_r split into three BF16 planes
+    uint16_t* planes = at<uint16_t>(ws, L.router_planes);
+    beam::launch_router_split(router_w, c.n_experts, c.d, planes, s);
+    CUtensorMap tm_w, tm_x;
+    if (!tmap_bf16(&tm_w, planes, c.n_experts, 3LL * c.d, 128) ||
+        !tmap_bf16(&tm_x, hidden, T, c.d, 128))
+      return BEAM_ERR_CUDA;
+    if (beam::launch_router_tc(tm_w, tm_x, part, T, c.n_experts, c.d, at<uint32_t>(ws, L.status),
+                               g_wait_ns, dev.sms, s) != cudaSuccess)
+      return BEAM_ERR_CUDA;
+  } else {
+    ks = router_ksplit(c, T);
+    beam::RouterArgs ra;
+    ra.x = static_cast<const uint16_t*>(hidden);
+    ra.w = router_w;
+    ra.part = part;
+    ra.T = T;
+    ra.d = c.d;
+    ra.E = c.n_experts;
+    ra.k_chunk = router_chunk(c, ks);
+    beam::launch_router(ra, ks, s);
+  }
   record(1, s);
   beam::SelectArgs sa;
-  sa.part = ra.part;
+  sa.part = part;
   sa.ksplit = ks;
   sa.bias = bias;
   sa.T = T;
@@ -225,7 +249,8 @@ beam_status_t run_experts(const beam_moe_config_t& c, const void* hidden, const 
                           const DevInfo& dev, cudaStream_t s) {
   const int64_t TK = T * c.topk;
   const int64_t rows = std::max<int64_t>(TK, kMinRows);
-  const int nt = token_tile(c, TK);
+  const int nt_gu = gateup_tile(c, TK);
+  const int nt_dn = down_tile(c, TK);
   uint32_t* status = at<uint32_t>(ws, L.status);
 
   beam::PermuteArgs pa;
@@ -241,9 +266,12 @@ beam_status_t run_experts(const beam_moe_config_t& c, const void* hidden, const 
   pa.status = status;
   beam::launch_permute(pa, s);
   record(3, s);
+  // decode-sized batches: the gate/up GEMM gathers its token rows itself
+  const bool row_gather = small_batch(c, TK);
   uint16_t* xp = at<uint16_t>(ws, L.x_perm);
-  beam::launch_gather(static_cast<const uint16_t*>(hidden), pa.perm_src, pa.offsets + c.n_experts,
-                      TK, c.topk, c.d, xp, s);
+  if (!row_gather)
+    beam::launch_gather(static_cast<const uint16_t*>(hidden), pa.perm_src,
+                        pa.offsets + c.n_experts, TK, c.topk, c.d, xp, s);
   record(4, s);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return BEAM_ERR_CUDA;
@@ -254,44 +282,51 @@ beam_status_t run_experts(const beam_moe_config_t& c, const void* hidden, const 
   float* y = at<float>(ws, L.y);
   CUtensorMap tm_wg, tm_wu, tm_wd, tm_xp, tm_h;
   if (!tmap_bf16(&tm_wg, w_gate, EF, c.d, 128) || !tmap_bf16(&tm_wu, w_up, EF, c.d, 128) ||
-      !tmap_bf16(&tm_wd, w_down, ED, c.d_ff, 128) || !tmap_bf16(&tm_xp, xp, rows, c.d, nt) ||
-      !tmap_bf16(&tm_h, h, rows, c.d_ff, nt))
+      !tmap_bf16(&tm_wd, w_down, ED, c.d_ff, 128) || !(row_gather ? tmap_bf16(&tm_xp, hidden, T, c.d, 1)
+                  : tmap_bf16(&tm_xp, xp, rows, c.d, nt_gu)) ||
+      !tmap_bf16(&tm_h, h, rows, c.d_ff, nt_dn))
     return BEAM_ERR_CUDA;
 
-  GemmArgs ga;
+  GemmArgs ga{};
   ga.counts = pa.counts;
+  ga.perm_src = pa.perm_src;
+  ga.topk = c.topk;
   ga.offsets = pa.offsets;
   ga.perm_w = pa.perm_w;
   ga.E = c.n_experts;
   ga.status = status;
   ga.wait_limit_ns = g_wait_ns;
   ga.withhold_first_load = g_withhold;
+  ga.weight_evict_first = small_batch(c, TK) ? 1 : 0;
   g_withhold = 0;
 
   // upper bound of the tile count, to size the persistent grid
-  auto grid_for = [&](int m_blocks) {
+  auto grid_for = [&](int m_blocks, int nt) {
     const int64_t tiles = static_cast<int64_t>(m_blocks) * (c.n_experts + (TK + nt - 1) / nt);
     return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(dev.sms, tiles)));
   };
 
   ga.h_out = h;
-  ga.y_out = nullptr;
   ga.out_ld = c.d_ff;
   ga.rows_per_expert = c.d_ff;
   ga.m_blocks = c.d_ff / 128;
   ga.k_blocks = c.d / 64;
-  err = beam::launch_gateup(tm_wg, tm_wu, tm_xp, ga, nt, grid_for(ga.m_blocks), s);
+  ga.b_k_blocks = ga.k_blocks;
+  err = beam::launch_grouped_gemm(beam::kModeGateUp, nt_gu, tm_wg, tm_wu, tm_xp, ga,
+                                  grid_for(ga.m_blocks, nt_gu), s);
   if (err != cudaSuccess) return BEAM_ERR_CUDA;
   record(5, s);
 
   ga.withhold_first_load = 0;
   ga.h_out = nullptr;
-  ga.y_out = y;
+  ga.f32_out = y;
   ga.out_ld = c.d;
   ga.rows_per_expert = c.d;
   ga.m_blocks = c.d / 128;
   ga.k_blocks = c.d_ff / 64;
-  err = beam::launch_down(tm_wd, tm_h, ga, nt, grid_for(ga.m_blocks), s);
+  ga.b_k_blocks = ga.k_blocks;
+  err = beam::launch_grouped_gemm(beam::kModeDown, nt_dn, tm_wd, tm_wd, tm_h, ga,
+                                  grid_for(ga.m_blocks, nt_dn), s);
   if (err != cudaSuccess) return BEAM_ERR_CUDA;
   record(6, s);
 
@@ -367,8 +402,9 @@ beam_status_t beam_moe_route(const beam_moe_config_t* cfg, const void* hidden,
       !aligned16(topk_idx) || !aligned16(topk_w) || (logits && !aligned16(logits)))
     return BEAM_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (tensor_router(*cfg, T) && !encoder()) return BEAM_ERR_CUDA;
   return run_route(*cfg, hidden, router_w, corr_bias, T, topk_idx, topk_w,
-                   logits ? logits : at<float>(workspace, L.logits), workspace, L, s);
+                   logits ? logits : at<float>(workspace, L.logits), workspace, L, dev, s);
 }
 
 beam_status_t beam_moe_select(const beam_moe_config_t* cfg, const float* logits,
@@ -416,7 +452,7 @@ beam_status_t beam_moe_forward(const beam_moe_config_t* cfg, const void* hidden,
   int32_t* idx = at<int32_t>(workspace, L.idx);
   float* w = at<float>(workspace, L.w);
   st = run_route(*cfg, hidden, router_w, corr_bias, T, idx, w, at<float>(workspace, L.logits),
-                 workspace, L, s);
+                 workspace, L, dev, s);
   if (st != BEAM_OK) return st;
   return run_experts(*cfg, hidden, idx, w, w_gate, w_up, w_down, out, T, workspace, L, dev, s);
 }
@@ -493,7 +529,8 @@ beam_status_t beam_moe_set_debug(uint32_t wait_limit_us, int32_t withhold_first_
 
 int32_t beam_moe_kernels_per_forward(const beam_moe_config_t* cfg, int64_t T) {
   if (!valid_cfg(cfg) || T <= 0) return 0;
-  return 7;
+  // router (+ plane split), select, permute, (gather), gate/up, down, combine
+  return 6 + (tensor_router(*cfg, T) ? 1 : 0) + (small_batch(*cfg, T * cfg->topk) ? 0 : 1);
 }
 
 const char* beam_status_string(beam_status_t s) {

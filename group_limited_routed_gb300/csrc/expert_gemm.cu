@@ -1,5 +1,5 @@
-// Grouped expert GEMMs on the 5th-generation tensor cores (tcgen05 + TMEM),
-// operands staged by TMA.
+// Grouped GEMMs on the 5th-generation tensor cores (tcgen05 + TMEM), operands
+// staged by TMA.  One kernel template, two epilogues:
 //
 //   gate/up : for every expert e and every row r of its permuted tokens,
 //             g = x_r W_g[e]^T, u = x_r W_u[e]^T (FP32 accumulators in TMEM),
@@ -13,12 +13,18 @@
 //             once, after the local sum over a token's experts -- SGLang post,
 //             section "Fusion Optimizations").
 //
-// Tiling ("swap AB"): the MMA's M side is 128 weight rows, its N side is a
-// tile of NT permuted token rows (NT = 16 for decode-sized batches, 128 for
-// prefill-sized ones), K steps of 64 (one 128-byte swizzle row of BF16).
-// gate/up issue two MMAs per K step into two TMEM accumulators (gate, up) that
-// share the token operand, so one thread holds g and u of the same (f, token)
-// and the SwiGLU epilogue is local.
+// Tiling ("swap AB"): the MMA's M side is 128 weight rows, its N side a block
+// of the expert's permuted token rows (up to NT; the MMA's N is the block's
+// row count rounded up to 16), K steps of 64 (one 128-byte swizzle row of
+// BF16).  gate/up issue two MMAs per K step into two TMEM accumulators (gate,
+// up) that share the token operand, so one thread holds g and u of the same
+// (f, token) and the SwiGLU epilogue is local.  An expert's rows are split
+// into ceil(rows / NT) blocks of nearly equal size.  With 16-row token
+// blocks (decode-sized batches) gate/up gathers its token rows from the
+// hidden states with per-row TMA loads, so no permuted copy of x is made;
+// rows past a block's last valid row are not loaded and the MMA columns they
+// feed are never read.  Larger blocks read a gathered copy of x with tile
+// loads (hundreds of 128-byte TMA requests per stage would starve the MMA).
 //
 // Persistent CTAs (one per SM) walk a tile list derived on the device from
 // the per-expert row counts: tile -> (expert, weight block, token block),
@@ -26,9 +32,10 @@
 // the same time (their weight tiles are then read from HBM once and from L2
 // after).  Warp roles: warp 0 issues TMA loads into a STAGES-deep ring, warp 1
 // owns TMEM and issues tcgen05.mma from one thread, warps 2-5 drain the
-// double-buffered accumulators.  Every mbarrier wait is bounded: when one runs
-// out the CTA latches BEAM_ERR_TIMEOUT, stops, lets its copies in flight land,
-// frees its TMEM and returns.
+// accumulators (double-buffered when they fit in TMEM's 512 columns).  Every
+// mbarrier wait is bounded: when one runs out the CTA latches
+// BEAM_ERR_TIMEOUT, stops, lets its copies in flight land, frees its TMEM and
+// returns.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -55,17 +62,18 @@ constexpr uint32_t pow2_at_least(uint32_t v) {
   return p;
 }
 
-template <int NT, bool GATEUP>
+template <int NT, int MODE>
 struct Cfg {
-  static constexpr int NUM_A = GATEUP ? 2 : 1;
+  static constexpr int NUM_A = MODE == kModeGateUp ? 2 : 1;
   static constexpr uint32_t A_BYTES = BM * BK * 2;
   static constexpr uint32_t B_BYTES = NT * BK * 2;
   static constexpr uint32_t STAGE_BYTES = NUM_A * A_BYTES + B_BYTES;
   static constexpr int STAGES_RAW = static_cast<int>(kTileBudget / STAGE_BYTES);
   static constexpr int STAGES = STAGES_RAW > 16 ? 16 : STAGES_RAW;
   static constexpr uint32_t ACC_COLS = NUM_A * NT;
-  static constexpr uint32_t TMEM_COLS = pow2_at_least(2 * ACC_COLS);
-  static constexpr uint32_t NUM_BARS = 2 * STAGES + 5;
+  static constexpr int ACC_BUFS = 2 * ACC_COLS <= 512 ? 2 : 1;
+  static constexpr uint32_t TMEM_COLS = pow2_at_least(ACC_BUFS * ACC_COLS);
+  static constexpr uint32_t NUM_BARS = 2 * STAGES + 2 * ACC_BUFS + 1;
   static constexpr uint32_t MISC_BYTES = 16 + 4 * (3 * kMaxE + 1);
   static constexpr uint32_t SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + NUM_BARS * 8 + MISC_BYTES;
   static_assert(B_BYTES % 1024 == 0, "token tile must keep 1024-byte stage alignment");
@@ -116,10 +124,23 @@ struct Waiter {
 };
 
 struct TileInfo {
-  int expert, mblock, row0, nvalid;
+  int expert, mblock, row0, nvalid, n_mma;
 };
 
-// tile index -> (expert, weight block, first permuted row, valid rows)
+// Token blocks of one expert: ceil(cnt / NT) blocks of nearly equal size,
+// each a multiple of 16 rows (the last one takes the remainder).
+template <int NT>
+__device__ __forceinline__ int token_blocks(int cnt) {
+  return (cnt + NT - 1) / NT;
+}
+
+template <int NT>
+__device__ __forceinline__ int block_rows(int cnt, int ntb) {
+  const int per = (cnt + ntb - 1) / ntb;
+  return min(NT, (per + 15) & ~15);
+}
+
+// tile index -> (expert, weight block, first permuted row, valid rows, MMA N)
 template <int NT>
 __device__ __forceinline__ TileInfo decode_tile(int tile, const int32_t* s_start,
                                                 const int32_t* s_cnt, const int32_t* s_off,
@@ -134,23 +155,28 @@ __device__ __forceinline__ TileInfo decode_tile(int tile, const int32_t* s_start
   }
   const int local = tile - s_start[lo];
   const int cnt = s_cnt[lo];
-  const int ntb = (cnt + NT - 1) / NT;
+  const int ntb = token_blocks<NT>(cnt);
+  const int bs = block_rows<NT>(cnt, ntb);
   const int tb = local % ntb;
   TileInfo ti;
   ti.expert = lo;
   ti.mblock = local / ntb;
-  ti.row0 = s_off[lo] + tb * NT;
-  ti.nvalid = min(NT, cnt - tb * NT);
+  ti.row0 = s_off[lo] + tb * bs;
+  ti.nvalid = min(bs, cnt - tb * bs);
+  ti.n_mma = (ti.nvalid + 15) & ~15;
   return ti;
 }
 
-template <int NT, bool GATEUP>
+template <int NT, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     expert_gemm_kernel(const __grid_constant__ CUtensorMap tm_a0,
                        const __grid_constant__ CUtensorMap tm_a1,
-                       const __grid_constant__ CUtensorMap tm_b, const GemmArgs p,
-                       const int weight_evict_first) {
-  using C = Cfg<NT, GATEUP>;
+                       const __grid_constant__ CUtensorMap tm_b, const GemmArgs p) {
+  using C = Cfg<NT, MODE>;
+  constexpr bool GATEUP = MODE == kModeGateUp;
+  // decode-sized token blocks gather their rows from the hidden states with
+  // per-row TMA loads; larger blocks load whole tiles of a gathered copy
+  constexpr bool ROW_GATHER = GATEUP && NT <= 32;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = ptx::smem_addr(smem_raw);
   const uint32_t pad = (1024u - (raw_addr & 1023u)) & 1023u;
@@ -168,8 +194,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (C::STAGES + s); };
   auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * C::STAGES + a); };
-  auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * C::STAGES + 2 + a); };
-  const uint32_t done_bar = bar0 + 8u * (2 * C::STAGES + 4);
+  auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * C::STAGES + C::ACC_BUFS + a); };
+  const uint32_t done_bar = bar0 + 8u * (2 * C::STAGES + 2 * C::ACC_BUFS);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -180,7 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(full_bar(s), 1);
       ptx::mbar_init(empty_bar(s), 1);
     }
-    for (int a = 0; a < 2; ++a) {
+    for (int a = 0; a < C::ACC_BUFS; ++a) {
       ptx::mbar_init(tfull_bar(a), 1);
       ptx::mbar_init(tempty_bar(a), 128);
     }
@@ -206,7 +232,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int running = 0;
     for (int base = 0; base < E; base += 32) {
       const int e = base + lane;
-      const int v = e < E ? p.m_blocks * ((s_cnt[e] + NT - 1) / NT) : 0;
+      const int v = e < E ? p.m_blocks * token_blocks<NT>(s_cnt[e]) : 0;
       int incl = v;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -227,43 +253,76 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      const uint64_t pol_w = weight_evict_first ? ptx::policy_evict_first() : ptx::policy_evict_normal();
-      const uint64_t pol_b = ptx::policy_evict_last();
-      int last_parity[C::STAGES];
+    // Lane 0 waits, arms the stage and loads the weight tiles.  With
+    // ROW_GATHER the token operand is gathered straight from the hidden rows:
+    // every lane issues one 128-byte row load per token it owns (box 64 x 1;
+    // the row lands at its swizzled place in the tile).  Otherwise the token
+    // operand (x gathered into expert order, or h) comes as one tile load.
+    constexpr int RPL = (NT + 31) / 32;  // token rows per lane
+    const uint64_t pol_w =
+        p.weight_evict_first ? ptx::policy_evict_first() : ptx::policy_evict_normal();
+    const uint64_t pol_b = ptx::policy_evict_last();
+    int last_parity[C::STAGES];
 #pragma unroll
-      for (int s = 0; s < C::STAGES; ++s) last_parity[s] = -1;
-      int stage = 0;
-      uint32_t phase = 0;
-      bool withhold = p.withhold_first_load != 0 && blockIdx.x == 0;
-      bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-        const TileInfo ti = decode_tile<NT>(tile, s_start, s_cnt, s_off, E);
-        const int a_row = ti.expert * p.rows_per_expert + ti.mblock * BM;
-        for (int kb = 0; kb < p.k_blocks; ++kb) {
-          if (!W.wait(empty_bar(stage), phase ^ 1u)) {
-            ok = false;
-            break;
-          }
-          if (withhold) {
-            withhold = false;  // test aid: this stage never fills
-          } else {
-            const uint32_t st = tiles + stage * C::STAGE_BYTES;
-            ptx::mbar_arrive_expect_tx(full_bar(stage), C::STAGE_BYTES);
+    for (int s = 0; s < C::STAGES; ++s) last_parity[s] = -1;
+    int stage = 0;
+    uint32_t phase = 0;
+    bool withhold = p.withhold_first_load != 0 && blockIdx.x == 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+      const TileInfo ti = decode_tile<NT>(tile, s_start, s_cnt, s_off, E);
+      if (ti.nvalid <= 0) continue;
+      const int a_row = ti.expert * p.rows_per_expert + ti.mblock * BM;
+      int tok[RPL];
+      if constexpr (ROW_GATHER) {
+#pragma unroll
+        for (int j = 0; j < RPL; ++j) {
+          const int r = lane + 32 * j;
+          tok[j] = r < ti.nvalid ? p.perm_src[ti.row0 + r] / p.topk : -1;
+        }
+      }
+      const uint32_t tx_bytes =
+          ROW_GATHER ? C::NUM_A * C::A_BYTES + static_cast<uint32_t>(ti.nvalid) * BK * 2
+                     : C::STAGE_BYTES;
+      for (int kb = 0; kb < p.k_blocks; ++kb) {
+        int okw = 1;
+        if (lane == 0) okw = W.wait(empty_bar(stage), phase ^ 1u) ? 1 : 0;
+        okw = __shfl_sync(kFull, okw, 0);
+        if (!okw) {
+          ok = false;
+          break;
+        }
+        const uint32_t st = tiles + stage * C::STAGE_BYTES;
+        const uint32_t b_dst = st + C::NUM_A * C::A_BYTES;
+        if (withhold) {
+          withhold = false;  // test aid: this stage never fills
+        } else {
+          if (lane == 0) {
+            ptx::mbar_arrive_expect_tx(full_bar(stage), tx_bytes);
             ptx::tma_load_2d(st, &tm_a0, full_bar(stage), kb * BK, a_row, pol_w);
             if (GATEUP)
               ptx::tma_load_2d(st + C::A_BYTES, &tm_a1, full_bar(stage), kb * BK, a_row, pol_w);
-            ptx::tma_load_2d(st + C::NUM_A * C::A_BYTES, &tm_b, full_bar(stage), kb * BK, ti.row0,
-                             pol_b);
-            last_parity[stage] = static_cast<int>(phase);
+            if (!ROW_GATHER)
+              ptx::tma_load_2d(b_dst, &tm_b, full_bar(stage), kb * BK, ti.row0, pol_b);
           }
-          if (++stage == C::STAGES) {
-            stage = 0;
-            phase ^= 1u;
+          if constexpr (ROW_GATHER) {
+            __syncwarp();
+#pragma unroll
+            for (int j = 0; j < RPL; ++j)
+              if (tok[j] >= 0)
+                ptx::tma_load_2d(b_dst + (lane + 32 * j) * (BK * 2), &tm_b, full_bar(stage),
+                                 kb * BK, tok[j], pol_b);
           }
+          last_parity[stage] = static_cast<int>(phase);
+        }
+        if (++stage == C::STAGES) {
+          stage = 0;
+          phase ^= 1u;
         }
       }
-      // the CTA may not exit while a copy into its shared memory is in flight
+    }
+    // the CTA may not exit while a copy into its shared memory is in flight
+    if (lane == 0) {
 #pragma unroll
       for (int s = 0; s < C::STAGES; ++s)
         if (last_parity[s] >= 0) W.wait_final(full_bar(s), static_cast<uint32_t>(last_parity[s]));
@@ -272,13 +331,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc = ptx::idesc_bf16_f32(BM, NT);
+      constexpr uint32_t idesc_m = ptx::idesc_bf16_f32(BM, 0);
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+        const TileInfo ti = decode_tile<NT>(tile, s_start, s_cnt, s_off, E);
+        if (ti.nvalid <= 0) continue;
+        const uint32_t idesc = idesc_m | (static_cast<uint32_t>(ti.n_mma >> 3) << 17);
         if (!W.wait(tempty_bar(acc), acc_phase ^ 1u)) break;
         ptx::tc_fence_after();
         const uint32_t d0 = tmem_base + acc * C::ACC_COLS;
@@ -306,8 +368,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!ok) break;
         ptx::mma_commit(tfull_bar(acc));
-        acc ^= 1;
-        if (acc == 0) acc_phase ^= 1u;
+        if (++acc == C::ACC_BUFS) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
       }
       // every MMA this thread issued completes before TMEM is released
       ptx::mma_commit(done_bar);
@@ -322,13 +386,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
       const TileInfo ti = decode_tile<NT>(tile, s_start, s_cnt, s_off, E);
+      if (ti.nvalid <= 0) continue;
       if (!W.wait(tfull_bar(acc), acc_phase)) break;
       ptx::tc_fence_after();
       const uint32_t tq = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * C::ACC_COLS;
       const int col = ti.mblock * BM + m;
 #pragma unroll 1
-      for (int c0 = 0; c0 < NT; c0 += 16) {
-        if (c0 >= ti.nvalid) break;
+      for (int c0 = 0; c0 < ti.nvalid; c0 += 16) {
         uint32_t ra[16];
         ptx::tmem_ld16(tq + c0, ra);
         if constexpr (GATEUP) {
@@ -350,7 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < 16; ++j) {
             if (c0 + j < ti.nvalid) {
               const int row = ti.row0 + c0 + j;
-              p.y_out[static_cast<int64_t>(row) * p.out_ld + col] =
+              p.f32_out[static_cast<int64_t>(row) * p.out_ld + col] =
                   __uint_as_float(ra[j]) * p.perm_w[row];
             }
           }
@@ -358,8 +422,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ptx::tc_fence_before();
       ptx::mbar_arrive(tempty_bar(acc));
-      acc ^= 1;
-      if (acc == 0) acc_phase ^= 1u;
+      if (++acc == C::ACC_BUFS) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
     }
   }
 
@@ -371,31 +437,33 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int NT, bool GATEUP>
+template <int NT, int MODE>
 cudaError_t launch_impl(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b,
-                        const GemmArgs& p, int num_sms, int evict_first, cudaStream_t s) {
-  using C = Cfg<NT, GATEUP>;
-  auto kern = expert_gemm_kernel<NT, GATEUP>;
+                        const GemmArgs& p, int grid, cudaStream_t s) {
+  using C = Cfg<NT, MODE>;
+  auto kern = expert_gemm_kernel<NT, MODE>;
   cudaError_t err =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (err != cudaSuccess) return err;
-  kern<<<num_sms, kThreads, C::SMEM_BYTES, s>>>(a0, a1, b, p, evict_first);
+  kern<<<grid, kThreads, C::SMEM_BYTES, s>>>(a0, a1, b, p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_gateup(const CUtensorMap& wg, const CUtensorMap& wu, const CUtensorMap& xp,
-                          const GemmArgs& a, int nt, int num_sms, cudaStream_t s) {
-  if (nt == 16) return launch_impl<16, true>(wg, wu, xp, a, num_sms, 1, s);
-  if (nt == 128) return launch_impl<128, true>(wg, wu, xp, a, num_sms, 0, s);
-  return cudaErrorInvalidValue;
-}
-
-cudaError_t launch_down(const CUtensorMap& wd, const CUtensorMap& h, const GemmArgs& a, int nt,
-                        int num_sms, cudaStream_t s) {
-  if (nt == 16) return launch_impl<16, false>(wd, wd, h, a, num_sms, 1, s);
-  if (nt == 128) return launch_impl<128, false>(wd, wd, h, a, num_sms, 0, s);
+cudaError_t launch_grouped_gemm(int mode, int nt, const CUtensorMap& a0, const CUtensorMap& a1,
+                                const CUtensorMap& b, const GemmArgs& a, int grid,
+                                cudaStream_t s) {
+  switch (mode) {
+    case kModeGateUp:
+      if (nt == 16) return launch_impl<16, kModeGateUp>(a0, a1, b, a, grid, s);
+      if (nt == 128) return launch_impl<128, kModeGateUp>(a0, a1, b, a, grid, s);
+      break;
+    case kModeDown:
+      if (nt == 16) return launch_impl<16, kModeDown>(a0, a0, b, a, grid, s);
+      if (nt == 256) return launch_impl<256, kModeDown>(a0, a0, b, a, grid, s);
+      break;
+  }
   return cudaErrorInvalidValue;
 }
 

@@ -34,7 +34,9 @@ __device__ __forceinline__ uint16_t f32_to_bf16(float v) {
 
 // ------------------------------------------------------------------ router
 // Block: 32 tokens x 64 experts over one K range; 256 threads, each 2 tokens
-// x 4 experts, FP32 FMA in ascending K order (fixed order => deterministic).
+// x 4 experts, FP32 FMA in ascending K order, summed per 32-wide slice first
+// (blocked summation keeps the rounding error of the 5120-term sum near
+// 1e-7); fixed order => deterministic.
 constexpr int kRtTok = 32;
 constexpr int kRtExp = 64;
 constexpr int kRtK = 32;
@@ -55,50 +57,64 @@ __global__ void __launch_bounds__(256) router_kernel(RouterArgs a) {
 #pragma unroll
     for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
 
-  for (int kc = k_begin; kc < k_end; kc += kRtK) {
-    {  // x tile: 32 tokens x 32 k, 4 bf16 per thread
-      const int r = tid >> 3;
-      const int c = (tid & 7) * 4;
-      const int64_t t = t0 + r;
-      float v[4] = {0.f, 0.f, 0.f, 0.f};
-      if (t < a.T) {
-        const uint2 raw = *reinterpret_cast<const uint2*>(a.x + t * a.d + kc + c);
-        v[0] = bf16_to_f32(static_cast<uint16_t>(raw.x & 0xffffu));
-        v[1] = bf16_to_f32(static_cast<uint16_t>(raw.x >> 16));
-        v[2] = bf16_to_f32(static_cast<uint16_t>(raw.y & 0xffffu));
-        v[3] = bf16_to_f32(static_cast<uint16_t>(raw.y >> 16));
-      }
+  // register prefetch of the next 32-wide K slice overlaps its load latency
+  // with the FMAs of the current one
+  const int xr_row = tid >> 3, xr_col = (tid & 7) * 4;
+  const bool x_ok = t0 + xr_row < a.T;
+  const uint16_t* xsrc = a.x + (t0 + xr_row) * a.d + xr_col;
+  uint2 xreg = make_uint2(0u, 0u);
+  float4 wreg[2];
+  auto load_slice = [&](int kc) {
+    if (x_ok) xreg = *reinterpret_cast<const uint2*>(xsrc + kc);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) xs[c + i][r] = v[i];
-    }
-#pragma unroll
-    for (int rep = 0; rep < 2; ++rep) {  // W tile: 64 experts x 32 k
+    for (int rep = 0; rep < 2; ++rep) {
       const int li = tid + rep * 256;
       const int r = li >> 3;
       const int c = (li & 7) * 4;
-      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      wreg[rep] = make_float4(0.f, 0.f, 0.f, 0.f);
       if (e0 + r < a.E)
-        v = *reinterpret_cast<const float4*>(a.w + static_cast<int64_t>(e0 + r) * a.d + kc + c);
-      ws[c + 0][r] = v.x;
-      ws[c + 1][r] = v.y;
-      ws[c + 2][r] = v.z;
-      ws[c + 3][r] = v.w;
+        wreg[rep] =
+            *reinterpret_cast<const float4*>(a.w + static_cast<int64_t>(e0 + r) * a.d + kc + c);
+    }
+  };
+  if (k_begin < k_end) load_slice(k_begin);
+  for (int kc = k_begin; kc < k_end; kc += kRtK) {
+    xs[xr_col + 0][xr_row] = bf16_to_f32(static_cast<uint16_t>(xreg.x & 0xffffu));
+    xs[xr_col + 1][xr_row] = bf16_to_f32(static_cast<uint16_t>(xreg.x >> 16));
+    xs[xr_col + 2][xr_row] = bf16_to_f32(static_cast<uint16_t>(xreg.y & 0xffffu));
+    xs[xr_col + 3][xr_row] = bf16_to_f32(static_cast<uint16_t>(xreg.y >> 16));
+#pragma unroll
+    for (int rep = 0; rep < 2; ++rep) {
+      const int li = tid + rep * 256;
+      const int r = li >> 3;
+      const int c = (li & 7) * 4;
+      ws[c + 0][r] = wreg[rep].x;
+      ws[c + 1][r] = wreg[rep].y;
+      ws[c + 2][r] = wreg[rep].z;
+      ws[c + 3][r] = wreg[rep].w;
     }
     __syncthreads();
+    if (kc + kRtK < k_end) load_slice(kc + kRtK);
+    // blocked summation: each 32-wide slice is summed on its own, then added
+    float sl[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
     for (int kk = 0; kk < kRtK; ++kk) {
       const float x0 = xs[kk][ty * 2];
       const float x1 = xs[kk][ty * 2 + 1];
       const float4 wv = *reinterpret_cast<const float4*>(&ws[kk][tx * 4]);
-      acc[0][0] = fmaf(x0, wv.x, acc[0][0]);
-      acc[0][1] = fmaf(x0, wv.y, acc[0][1]);
-      acc[0][2] = fmaf(x0, wv.z, acc[0][2]);
-      acc[0][3] = fmaf(x0, wv.w, acc[0][3]);
-      acc[1][0] = fmaf(x1, wv.x, acc[1][0]);
-      acc[1][1] = fmaf(x1, wv.y, acc[1][1]);
-      acc[1][2] = fmaf(x1, wv.z, acc[1][2]);
-      acc[1][3] = fmaf(x1, wv.w, acc[1][3]);
+      sl[0][0] = fmaf(x0, wv.x, sl[0][0]);
+      sl[0][1] = fmaf(x0, wv.y, sl[0][1]);
+      sl[0][2] = fmaf(x0, wv.z, sl[0][2]);
+      sl[0][3] = fmaf(x0, wv.w, sl[0][3]);
+      sl[1][0] = fmaf(x1, wv.x, sl[1][0]);
+      sl[1][1] = fmaf(x1, wv.y, sl[1][1]);
+      sl[1][2] = fmaf(x1, wv.z, sl[1][2]);
+      sl[1][3] = fmaf(x1, wv.w, sl[1][3]);
     }
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) acc[i][j] += sl[i][j];
     __syncthreads();
   }
 #pragma unroll
@@ -113,15 +129,43 @@ __global__ void __launch_bounds__(256) router_kernel(RouterArgs a) {
 }
 
 // --------------------------------------------------------------- selection
-// One warp per token.  Lane l holds experts j*32 + l (j < E/32).  Groups are
-// S = E/G consecutive experts, S a power of two <= 32, so a group is an
-// aligned segment of S lanes of one register.
-__global__ void __launch_bounds__(256) select_kernel(SelectArgs a) {
+// Phase 1 (whole block): thread e sums the router's split-K partials of
+// expert e for each token of the block, in split order, into shared memory.
+// Phase 2: one warp per token.  Lane l holds experts j*32 + l (j < E/32).
+// Groups are S = E/G consecutive experts, S a power of two <= 32, so a group
+// is an aligned segment of S lanes of one register.
+constexpr int kSelMaxTok = 8;
+
+__global__ void __launch_bounds__(256) select_kernel(SelectArgs a, int tok_per_block) {
+  __shared__ float s_logit[kSelMaxTok][256];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int64_t t = static_cast<int64_t>(blockIdx.x) * 8 + warp;
-  if (t >= a.T) return;
+  const int64_t t0 = static_cast<int64_t>(blockIdx.x) * tok_per_block;
   const int E = a.E;
+  for (int tk = 0; tk < tok_per_block; ++tk) {
+    const int64_t t = t0 + tk;
+    const int e = threadIdx.x;
+    if (t < a.T && e < E) {
+      const float* src = a.part + t * E + e;
+      const int64_t stride = a.T * E;
+      float lg = src[0];
+      int sp = 1;
+      for (; sp + 8 <= a.ksplit; sp += 8) {
+        float v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) v[u] = src[(sp + u) * stride];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) lg += v[u];
+      }
+      for (; sp < a.ksplit; ++sp) lg += src[sp * stride];
+      s_logit[tk][e] = lg;
+      if (a.logits) a.logits[t * E + e] = lg;
+    }
+  }
+  __syncthreads();
+  if (warp >= tok_per_block) return;
+  const int64_t t = t0 + warp;
+  if (t >= a.T) return;
   const int epl = E >> 5;
   const int S = E / a.G;
 
@@ -132,9 +176,7 @@ __global__ void __launch_bounds__(256) select_kernel(SelectArgs a) {
     c[j] = -FLT_MAX;
     if (j < epl) {
       const int e = j * 32 + lane;
-      float lg = a.part[t * E + e];
-      for (int sp = 1; sp < a.ksplit; ++sp) lg += a.part[(static_cast<int64_t>(sp) * a.T + t) * E + e];
-      if (a.logits) a.logits[t * E + e] = lg;
+      const float lg = s_logit[warp][e];
       s[j] = 1.0f / (1.0f + expf(-lg));
       c[j] = s[j] + a.bias[e];
     }
@@ -228,9 +270,50 @@ __global__ void __launch_bounds__(256) select_kernel(SelectArgs a) {
   }
 }
 
+// ------------------------------------------------------------ router split
+// planes[e] = for each 64-wide K range r: [hi | mid | lo] of that range, with
+// hi = bf16(w), mid = bf16(w - hi), lo = bf16(w - hi - mid): each product with
+// a BF16 x is exact in FP32, and hi + mid + lo equals w to within 2^-24
+// relative.
+__global__ void __launch_bounds__(256) router_split_kernel(const float* __restrict__ w, int32_t E,
+                                                           int32_t d, uint16_t* __restrict__ planes) {
+  const int64_t n = static_cast<int64_t>(E) * d;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t e = i / d, j = i % d;
+    const float v = w[i];
+    const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+    const float r1 = v - __bfloat162float(hi);
+    const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+    const float r2 = r1 - __bfloat162float(mid);
+    const __nv_bfloat16 lo = __float2bfloat16_rn(r2);
+    uint16_t* blk = planes + e * 3 * d + (j / 64) * 192 + (j % 64);
+    blk[0] = *reinterpret_cast<const uint16_t*>(&hi);
+    blk[64] = *reinterpret_cast<const uint16_t*>(&mid);
+    blk[128] = *reinterpret_cast<const uint16_t*>(&lo);
+  }
+}
+
 // ----------------------------------------------------------------- permute
 // Block e: counts its rows, finds its first permuted row (entries with a
-// smaller expert index) and writes its rows in (token, slot) order.
+// smaller expert index) and writes its rows in (token, slot) order.  Each
+// thread takes 8 consecutive entries per step; a block-wide exclusive scan of
+// the per-thread match counts keeps the order stable.
+constexpr int kPermPer = 8;
+
+__device__ __forceinline__ void load8(const int32_t* __restrict__ idx, int64_t i0, int64_t n,
+                                      int (&v)[kPermPer]) {
+  if (i0 + kPermPer <= n) {
+    const int4 a = *reinterpret_cast<const int4*>(idx + i0);
+    const int4 b = *reinterpret_cast<const int4*>(idx + i0 + 4);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+  } else {
+#pragma unroll
+    for (int j = 0; j < kPermPer; ++j) v[j] = i0 + j < n ? idx[i0 + j] : -1;
+  }
+}
+
 __global__ void __launch_bounds__(256) permute_kernel(PermuteArgs a) {
   const int e = blockIdx.x;
   const int tid = threadIdx.x;
@@ -238,19 +321,27 @@ __global__ void __launch_bounds__(256) permute_kernel(PermuteArgs a) {
   const int warp = tid >> 5;
   __shared__ int s_cnt[8], s_below[8], s_warp[8];
   __shared__ int s_tot[2];
+  constexpr int64_t kStep = 256 * kPermPer;
 
   int cnt = 0, below = 0;
-  for (int64_t i = tid; i < a.TK; i += 256) {
-    const int v = a.idx[i];
-    if (static_cast<unsigned>(v) >= static_cast<unsigned>(a.E)) {
-      if (e == 0) {
-        a.pair_row[i] = -1;
-        latch_status(a.status, kStatusDeviceCheck);
+  for (int64_t base = 0; base < a.TK; base += kStep) {
+    const int64_t i0 = base + static_cast<int64_t>(tid) * kPermPer;
+    if (i0 >= a.TK) continue;
+    int v[kPermPer];
+    load8(a.idx, i0, a.TK, v);
+#pragma unroll
+    for (int j = 0; j < kPermPer; ++j) {
+      if (i0 + j >= a.TK) break;
+      if (static_cast<unsigned>(v[j]) >= static_cast<unsigned>(a.E)) {
+        if (e == 0) {
+          a.pair_row[i0 + j] = -1;
+          latch_status(a.status, kStatusDeviceCheck);
+        }
+        continue;
       }
-      continue;
+      cnt += (v[j] == e);
+      below += (v[j] < e);
     }
-    cnt += (v == e);
-    below += (v < e);
   }
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1) {
@@ -278,12 +369,27 @@ __global__ void __launch_bounds__(256) permute_kernel(PermuteArgs a) {
   const int total = s_tot[0];
   const int first = s_tot[1];
   int running = 0;
-  for (int64_t base = 0; base < a.TK && running < total; base += 256) {
-    const int64_t i = base + tid;
-    const bool f = (i < a.TK) && (a.idx[i] == e);
-    const unsigned m = __ballot_sync(kFull, f);
-    const int wpre = __popc(m & ((1u << lane) - 1u));
-    if (lane == 0) s_warp[warp] = __popc(m);
+  for (int64_t base = 0; base < a.TK && running < total; base += kStep) {
+    const int64_t i0 = base + static_cast<int64_t>(tid) * kPermPer;
+    int v[kPermPer];
+    if (i0 < a.TK) {
+      load8(a.idx, i0, a.TK, v);
+    } else {
+#pragma unroll
+      for (int j = 0; j < kPermPer; ++j) v[j] = -1;
+    }
+    unsigned mask = 0;
+#pragma unroll
+    for (int j = 0; j < kPermPer; ++j) mask |= (v[j] == e ? 1u : 0u) << j;
+    const int mine = __popc(mask);
+    // exclusive scan of `mine` over the block (thread order = entry order)
+    int incl = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(kFull, incl, o);
+      if (lane >= o) incl += n;
+    }
+    if (lane == 31) s_warp[warp] = incl;
     __syncthreads();
     int woff = 0, tot = 0;
 #pragma unroll
@@ -292,11 +398,16 @@ __global__ void __launch_bounds__(256) permute_kernel(PermuteArgs a) {
       woff += (w < warp) ? cw : 0;
       tot += cw;
     }
-    if (f) {
-      const int row = first + running + woff + wpre;
-      a.perm_src[row] = static_cast<int>(i);
-      a.pair_row[i] = row;
-      a.perm_w[row] = a.w[i];
+    int row = first + running + woff + incl - mine;
+#pragma unroll
+    for (int j = 0; j < kPermPer; ++j) {
+      if (mask & (1u << j)) {
+        const int64_t i = i0 + j;
+        a.perm_src[row] = static_cast<int>(i);
+        a.pair_row[i] = row;
+        a.perm_w[row] = a.w[i];
+        ++row;
+      }
     }
     running += tot;
     __syncthreads();
@@ -304,7 +415,8 @@ __global__ void __launch_bounds__(256) permute_kernel(PermuteArgs a) {
 }
 
 // ------------------------------------------------------------------ gather
-// x_perm[row] = x[token of row]; rows past the last valid one are skipped.
+// x_perm[row] = x[token of row] for the larger token blocks; rows past the
+// last valid one are skipped.
 __global__ void __launch_bounds__(128) gather_kernel(const uint16_t* __restrict__ x,
                                                      const int32_t* __restrict__ perm_src,
                                                      const int32_t* __restrict__ n_valid,
@@ -362,7 +474,13 @@ void launch_router(const RouterArgs& a, int ksplit, cudaStream_t s) {
 }
 
 void launch_select(const SelectArgs& a, cudaStream_t s) {
-  select_kernel<<<static_cast<unsigned>((a.T + 7) / 8), 256, 0, s>>>(a);
+  // one token per block while split-K partials need reducing, else 8
+  const int tpb = a.ksplit > 1 ? 1 : kSelMaxTok;
+  select_kernel<<<static_cast<unsigned>((a.T + tpb - 1) / tpb), 256, 0, s>>>(a, tpb);
+}
+
+void launch_router_split(const float* w, int32_t E, int32_t d, uint16_t* planes, cudaStream_t s) {
+  router_split_kernel<<<512, 256, 0, s>>>(w, E, d, planes);
 }
 
 void launch_permute(const PermuteArgs& a, cudaStream_t s) {

@@ -68,6 +68,12 @@ CONFIGS = {
                                topk_groups=4, topk=8, d_ff=2560, seed=5,
                                description="Beam expert shapes, 32 experts (8x4), T=8 "
                                            "(profiling case)"),
+    # profiling case for the compute-bound regime: 32 experts, 256 rows each
+    # on average (the Beam prefill's rows per expert), 2.5 GB on the device
+    "profile_prefill": MoEConfig(name="profile_prefill", T=1024, d=5120, n_experts=32,
+                                 n_groups=8, topk_groups=4, topk=8, d_ff=2560, seed=6,
+                                 description="Beam expert shapes, 32 experts (8x4), T=1024 "
+                                             "(profiling case, prefill regime)"),
     "nvfp4": MoEConfig(name="nvfp4", T=128, seed=4, weight_fmt="nvfp4", **_BEAM,
                        description="Beam MoE layer NVFP4 experts T=128 (E2M1 + E4M3 per "
                                    "16 along K + FP32 per-tensor scale)"),

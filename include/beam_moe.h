@@ -107,7 +107,8 @@ typedef struct {
   size_t perm_src;      /* int32 [T*topk] permuted row -> token*topk + slot   */
   size_t pair_row;      /* int32 [T*topk] token*topk + slot -> permuted row   */
   size_t perm_w;        /* FP32 [T*topk] routing weight of each permuted row  */
-  size_t x_perm;        /* BF16 [T*topk, d] gathered expert inputs            */
+  size_t x_perm;        /* BF16 [T*topk, d] gathered expert inputs (only when
+                           T*topk > 4*E; smaller batches gather in the GEMM) */
   size_t h;             /* BF16 [T*topk, F] SwiGLU activations                */
   size_t y;             /* FP32 [T*topk, d] weighted expert outputs           */
   size_t total;         /* == beam_moe_workspace_size                         */
@@ -159,7 +160,7 @@ beam_status_t beam_moe_forward_routed(const beam_moe_config_t *cfg, const void *
  * the process exits).
  *   - Size limit: calls whose beam_moe_workspace_size(cfg, T, BEAM_WEIGHTS_BF16)
  *     exceeds 32 MiB return BEAM_ERR_WORKSPACE before anything is launched
- *     (Beam shapes: up to 108 tokens).
+ *     (Beam shapes: up to 128 tokens).
  *   - The first call on a device looks up the array's device address (one
  *     cudaGetSymbolAddress with that device current); make that first call
  *     before any stream capture.
@@ -183,7 +184,8 @@ beam_status_t beam_moe_check_status(void *workspace, void *stream);
 /* Profiling aid: when n >= 8 events (cudaEvent_t) are given, every later
  * beam_moe_forward / beam_moe_forward_routed records them on its stream at
  * the step boundaries: [0] start, [1] router, [2] selection, [3] permute,
- * [4] gather, [5] gate/up GEMM, [6] down GEMM, [7] combine (each after its
+ * [4] gather (only when T*topk > 4*E; smaller batches gather inside the
+ * gate/up GEMM), [5] gate/up GEMM, [6] down GEMM, [7] combine (each after its
  * step).  Steps a call does not run record at the same point as the previous
  * one.  n == 0 switches it off.  Process-wide; not thread-safe. */
 beam_status_t beam_moe_set_stage_events(void *const *events, int32_t n);

@@ -42,6 +42,7 @@ def check_logits(got: np.ndarray, ref: np.ndarray):
     bound = LOGIT_RTOL * np.maximum(np.abs(ref), rms)
     err = np.abs(got.astype(np.float64) - ref.astype(np.float64))
     bad = err > bound
+    print(f"  logits: max |err| {err.max():.3g}, worst {(err / bound).max():.3g} of the bound")
     assert not bad.any(), f"{bad.sum()} logits out of tolerance; worst {(err / bound).max():.3g}x"
 
 

@@ -48,7 +48,8 @@ def test_host_only_queries(lib):
     assert lay["total"] == n and n % 256 == 0
     offs = sorted(v for k, v in lay.items() if k != "total")
     assert offs[0] == 0 and all(o % 256 == 0 for o in offs)
-    assert api.kernels_per_forward(beam, 32) == 7
+    assert api.kernels_per_forward(beam, 32) == 6        # CUDA-core router, fused gather
+    assert api.kernels_per_forward(beam, 8192) == 8      # plane split, tensor router, gather
     with pytest.raises(api.BeamError):
         api.workspace_size(beam.replace(n_groups=7), 32)
     lib.beam_status_string.restype = ctypes.c_char_p
