@@ -153,13 +153,19 @@ def oracle_sample(cfg, t, n_tokens: int, seed: int = 0):
     lg = oracle.router_logits(x, wr)
     r = oracle.route(lg, b, cfg.n_groups, cfg.topk_groups, cfg.topk, cfg.routed_scale)
     need = sorted({int(e) for e in r["idx"][rows].reshape(-1)})
-    wg = {e: inputs.bf16_bits(t["w_gate"][e]) for e in need}
-    wu = {e: inputs.bf16_bits(t["w_up"][e]) for e in need}
-    wd = {e: inputs.bf16_bits(t["w_down"][e]) for e in need}
+    if cfg.weight_fmt == "nvfp4":
+        proj = [{"q": {e: p["q"][e].cpu().numpy() for e in need},
+                 "sf": {e: p["sf"][e].cpu().numpy() for e in need},
+                 "gs": p["gs"].cpu().numpy()} for p in (t["w_gate"], t["w_up"], t["w_down"])]
+    else:
+        proj = [{e: inputs.bf16_bits(t[n][e]) for e in need} for n in ("w_gate", "w_up", "w_down")]
     t0 = time.perf_counter()
     lg = oracle.router_logits(x[rows], wr)
     r = oracle.route(lg, b, cfg.n_groups, cfg.topk_groups, cfg.topk, cfg.routed_scale)
-    oracle.experts_bf16(x[rows], r["idx"], r["w"], wg, wu, wd, cfg.n_experts)
+    if cfg.weight_fmt == "nvfp4":
+        oracle.experts_nvfp4(x[rows], r["idx"], r["w"], *proj, cfg.n_experts, act_quant=True)
+    else:
+        oracle.experts_bf16(x[rows], r["idx"], r["w"], *proj, cfg.n_experts)
     return time.perf_counter() - t0, len(rows)
 
 
@@ -243,13 +249,23 @@ def run_gpu(args, cfg):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
     t = inputs.generate(cfg.replace(seed=cfg.seed + 1000 * rank) if rank else cfg, dev)
-    ws = pkg.Workspace(cfg, cfg.T, dev)
+    fp4 = cfg.weight_fmt == "nvfp4"
+    ws = pkg.Workspace(cfg, cfg.T, dev, weight_fmt=pkg.NVFP4 if fp4 else 0)
     stream = torch.cuda.current_stream()
     out = torch.empty(cfg.T, cfg.d, dtype=torch.bfloat16, device=dev)
-    args_l = (cfg, t["hidden"], t["router_w"], t["corr_bias"], t["w_gate"], t["w_up"], t["w_down"])
+    if fp4:
+        wts = [pkg.Fp4Weight.of(t[n]) for n in ("w_gate", "w_up", "w_down")]
+
+        def layer(x, o):
+            return pkg.forward_nvfp4(cfg, x, t["router_w"], t["corr_bias"], *wts, out=o, ws=ws,
+                                     stream=stream)
+    else:
+        def layer(x, o):
+            return pkg.forward(cfg, x, t["router_w"], t["corr_bias"], t["w_gate"], t["w_up"],
+                               t["w_down"], out=o, ws=ws, stream=stream)
 
     def step(o=out):
-        return pkg.forward(*args_l, out=o, ws=ws, stream=stream)
+        return layer(t["hidden"], o)
 
     for _ in range(args.warmup):
         step()
@@ -291,15 +307,22 @@ def run_gpu(args, cfg):
     # end to end through the public API: pinned host in, pinned host out
     x_host = t["hidden"].cpu().pin_memory()
     o_host = torch.empty(cfg.T, cfg.d, dtype=torch.bfloat16).pin_memory()
+    x_dev = torch.empty_like(t["hidden"])
+
+    def e2e_step():
+        x_dev.copy_(x_host, non_blocking=True)
+        layer(x_dev, out)
+        o_host.copy_(out, non_blocking=True)
+
     e2e_steps = max(3, min(args.steps, 200))
     for _ in range(3):
-        pkg.forward(cfg, x_host, *args_l[2:], out=o_host, ws=ws, stream=stream)
+        e2e_step()
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(e2e_steps):
-        pkg.forward(cfg, x_host, *args_l[2:], out=o_host, ws=ws, stream=stream)
+        e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1)
@@ -312,8 +335,10 @@ def run_gpu(args, cfg):
     e2e_value = world * cfg.T * e2e_steps / (e2e_ms / 1e3)
 
     pk = peaks()
-    E_b = cfg.d * cfg.d_ff * 2
-    gu_bytes = touched * 2 * E_b + cfg.T * cfg.topk * (cfg.d + cfg.d_ff) * 2
+    # weight bytes of one projection of one expert: BF16, or E2M1 + E4M3 per 16
+    E_b = cfg.d * cfg.d_ff * 2 if not fp4 else cfg.d * cfg.d_ff // 2 + cfg.d * cfg.d_ff // 16
+    tok_b = 2 if not fp4 else 0.5625
+    gu_bytes = touched * 2 * E_b + cfg.T * cfg.topk * (cfg.d + cfg.d_ff) * tok_b
     gu_gbs = gu_bytes / (stage_ms[4] / 1e3) / 1e9
     layer_bytes = touched * 3 * E_b + cfg.n_experts * cfg.d * 4 + cfg.n_experts * 4 \
         + 2 * cfg.T * cfg.d * 2
@@ -322,7 +347,8 @@ def run_gpu(args, cfg):
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": layer_ms, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "nvfp4 (e2m1 x e4m3 per 16)" if fp4 else "bf16", "data": "synthetic",
         "config": config_record(cfg, touched),
         "roofline": {"bound": "hbm", "kernel": DOMINANT, "achieved": gu_gbs,
                      "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": gu_gbs / pk["hbm_gbs"],

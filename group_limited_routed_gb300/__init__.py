@@ -13,7 +13,8 @@ def __getattr__(name):
     # on machines without the compiled library
     if name in ("route", "select", "forward", "forward_routed", "workspace_size", "Workspace",
                 "check_status", "BeamError", "library_path", "lib", "set_stage_events",
-                "set_debug", "layout", "kernels_per_forward", "EXPORTS", "forward_noalloc"):
+                "set_debug", "layout", "kernels_per_forward", "EXPORTS", "forward_noalloc",
+                "forward_nvfp4", "pack_scales", "Fp4Weight", "NVFP4"):
         from . import api
         return getattr(api, name)
     raise AttributeError(name)

@@ -30,7 +30,7 @@ STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "workspace too sm
 
 EXPORTS = ("beam_moe_workspace_size", "beam_moe_workspace_layout", "beam_moe_route",
            "beam_moe_select", "beam_moe_forward", "beam_moe_forward_routed",
-           "beam_moe_forward_noalloc",
+           "beam_moe_forward_noalloc", "beam_moe_forward_nvfp4", "beam_moe_nvfp4_pack_scales",
            "beam_moe_check_status", "beam_moe_set_stage_events", "beam_moe_set_debug",
            "beam_moe_kernels_per_forward", "beam_status_string")
 
@@ -44,7 +44,11 @@ class BeamError(RuntimeError):
 class _Layout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in (
         "status", "logits", "topk_idx", "topk_w", "counts", "offsets", "perm_src", "pair_row",
-        "perm_w", "x_perm", "h", "y", "total")]
+        "perm_w", "x_perm", "h", "x_fp4", "x_sf", "h_fp4", "h_sf", "y", "total")]
+
+
+class _Fp4Weight(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("sf", ctypes.c_void_p), ("global_scale", ctypes.c_void_p)]
 
 
 def library_path() -> str:
@@ -77,6 +81,12 @@ def lib():
         L.beam_moe_forward_routed.restype = _ST
         L.beam_moe_forward_noalloc.argtypes = [cfgp, _P, _P, _P, _P, _P, _P, _P, _I64, _P]
         L.beam_moe_forward_noalloc.restype = _ST
+        fp4p = ctypes.POINTER(_Fp4Weight)
+        L.beam_moe_forward_nvfp4.argtypes = [cfgp, _P, _P, _P, fp4p, fp4p, fp4p, _P, _I64, _P,
+                                             _SZ, _P]
+        L.beam_moe_forward_nvfp4.restype = _ST
+        L.beam_moe_nvfp4_pack_scales.argtypes = [_P, _I64, _I64, _P, _P]
+        L.beam_moe_nvfp4_pack_scales.restype = _ST
         L.beam_moe_check_status.argtypes = [_P, _P]
         L.beam_moe_check_status.restype = _ST
         L.beam_moe_set_stage_events.argtypes = [ctypes.POINTER(_P), ctypes.c_int32]
@@ -255,6 +265,55 @@ def forward_noalloc(cfg, hidden, router_w, corr_bias, w_gate, w_up, w_down, out=
                                           _dev(w_up, torch.bfloat16, "w_up"),
                                           _dev(w_down, torch.bfloat16, "w_down"), o.data_ptr(),
                                           T, _stream(stream)), "beam_moe_forward_noalloc")
+    return o
+
+
+NVFP4 = 1
+
+
+def pack_scales(sf: torch.Tensor, stream=None) -> torch.Tensor:
+    """E4M3 block scales [..., rows, S] (uint8, row-major) -> the blocked order
+    the tensor cores take (beam_moe_nvfp4_pack_scales); same shape and dtype."""
+    src = sf.contiguous()
+    S = src.shape[-1]
+    rows = src.numel() // S
+    dst = torch.empty_like(src)
+    _check(lib().beam_moe_nvfp4_pack_scales(_dev(src, torch.uint8, "sf"), rows, S,
+                                            dst.data_ptr(), _stream(stream)),
+           "beam_moe_nvfp4_pack_scales")
+    return dst
+
+
+class Fp4Weight:
+    """One NVFP4 projection: codes q [E, N, K/2], blocked scales, global scales [E]."""
+
+    def __init__(self, q: torch.Tensor, sf_rowmajor: torch.Tensor, gs: torch.Tensor,
+                 stream=None):
+        self.q = q.contiguous()
+        self.sf = pack_scales(sf_rowmajor, stream)
+        self.gs = gs.contiguous().float()
+        self._c = _Fp4Weight(_dev(self.q, torch.uint8, "q"), self.sf.data_ptr(),
+                             _dev(self.gs, torch.float32, "global_scale"))
+
+    @classmethod
+    def of(cls, d: dict, stream=None) -> "Fp4Weight":
+        return cls(d["q"], d["sf"], d["gs"], stream)
+
+
+def forward_nvfp4(cfg, hidden, router_w, corr_bias, gate: Fp4Weight, up: Fp4Weight,
+                  down: Fp4Weight, out=None, ws: Workspace | None = None, stream=None):
+    """The whole layer with NVFP4 experts (activations quantised to NVFP4)."""
+    T = hidden.shape[0]
+    if ws is None:
+        ws = Workspace(cfg, max(int(T), 1), hidden.device, weight_fmt=NVFP4)
+    o = torch.empty(T, cfg.d, dtype=torch.bfloat16, device=hidden.device) if out is None else out
+    c = _cfg(cfg)
+    _check(lib().beam_moe_forward_nvfp4(ctypes.byref(c), _dev(hidden, torch.bfloat16, "hidden"),
+                                        _dev(router_w, torch.float32, "router_w"),
+                                        _dev(corr_bias, torch.float32, "corr_bias"),
+                                        ctypes.byref(gate._c), ctypes.byref(up._c),
+                                        ctypes.byref(down._c), o.data_ptr(), T, ws.ptr, ws.nbytes,
+                                        _stream(stream)), "beam_moe_forward_nvfp4")
     return o
 
 

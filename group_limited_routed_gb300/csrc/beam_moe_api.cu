@@ -62,6 +62,21 @@ bool tmap_bf16(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, u
          CUDA_SUCCESS;
 }
 
+// 2-D byte tensor [rows, cols], box {box_cols, box_rows}; 128-byte swizzle
+// when box_cols is 128, none otherwise.
+bool tmap_u8(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_cols,
+             uint32_t box_rows) {
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
+                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  box_cols == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+
 // ---------------------------------------------------------------- device facts
 struct DevInfo {
   int sms = 0;
@@ -129,10 +144,14 @@ bool tensor_router(const beam_moe_config_t& c, int64_t T) {
 
 struct Layout {
   size_t status, part, logits, idx, w, counts, offsets, perm_src, pair_row, perm_w, x_perm, h, y,
-      router_planes, total;
+      router_planes, x_fp4, x_sf, h_fp4, h_sf, total;
 };
 
-Layout make_layout(const beam_moe_config_t& c, int64_t T_max) {
+// NVFP4 token-block width: the token scales are read row-major, 32 rows at most
+int fp4_tile(const beam_moe_config_t& c, int64_t TK) { return small_batch(c, TK) ? 16 : 32; }
+
+Layout make_layout(const beam_moe_config_t& c, int64_t T_max, int32_t fmt = BEAM_WEIGHTS_BF16) {
+  const bool fp4 = fmt == BEAM_WEIGHTS_NVFP4;
   const int64_t E = c.n_experts, k = c.topk;
   const int64_t TK = T_max * k;
   const int64_t rows = std::max<int64_t>(TK, kMinRows);
@@ -158,10 +177,14 @@ Layout make_layout(const beam_moe_config_t& c, int64_t T_max) {
   L.perm_src = take(static_cast<size_t>(TK) * 4);
   L.pair_row = take(static_cast<size_t>(TK) * 4);
   L.perm_w = take(static_cast<size_t>(TK) * 4);
-  L.x_perm = take(small_batch(c, TK) ? 0 : static_cast<size_t>(rows) * c.d * 2);
-  L.h = take(static_cast<size_t>(rows) * c.d_ff * 2);
+  L.x_perm = take(fp4 || small_batch(c, TK) ? 0 : static_cast<size_t>(rows) * c.d * 2);
+  L.h = take(fp4 ? 0 : static_cast<size_t>(rows) * c.d_ff * 2);
   L.y = take(static_cast<size_t>(rows) * c.d * 4);
   L.router_planes = take(T_max >= kTensorRouterMinT ? static_cast<size_t>(E) * 3 * c.d * 2 : 0);
+  L.x_fp4 = take(fp4 ? static_cast<size_t>(rows) * c.d / 2 : 0);
+  L.x_sf = take(fp4 ? static_cast<size_t>(rows) * c.d / 4 : 0);
+  L.h_fp4 = take(fp4 ? static_cast<size_t>(rows) * c.d_ff / 2 : 0);
+  L.h_sf = take(fp4 ? static_cast<size_t>(rows) * c.d_ff / 4 : 0);
   L.total = off;
   return L;
 }
@@ -182,12 +205,14 @@ beam_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? BEAM_OK : B
 // BEAM_OK with *empty set for a valid call of zero tokens (nothing to check
 // further, nothing to launch).
 beam_status_t common_checks(const beam_moe_config_t* cfg, int64_t T, void* ws, size_t ws_bytes,
-                            Layout* L, DevInfo* dev, bool* empty) {
+                            Layout* L, DevInfo* dev, bool* empty,
+                            int32_t fmt = BEAM_WEIGHTS_BF16) {
   if (!valid_cfg(cfg) || T < 0 || T > (int64_t(1) << 31) / 64) return BEAM_ERR_INVALID_ARG;
+  if (fmt == BEAM_WEIGHTS_NVFP4 && (cfg->d % 256 || cfg->d_ff % 256)) return BEAM_ERR_INVALID_ARG;
   *empty = (T == 0);
   if (*empty) return BEAM_OK;
   if (!aligned16(ws)) return BEAM_ERR_INVALID_ARG;
-  *L = make_layout(*cfg, T);
+  *L = make_layout(*cfg, T, fmt);
   if (ws_bytes < L->total) return BEAM_ERR_WORKSPACE;
   if (!device_info(dev)) return BEAM_ERR_CUDA;
   if (!dev->supported) return BEAM_ERR_UNSUPPORTED;
@@ -335,6 +360,99 @@ beam_status_t run_experts(const beam_moe_config_t& c, const void* hidden, const 
   return cuda_status(cudaGetLastError());
 }
 
+// permute + quantise token rows + FP4 gate/up (quantising h) + FP4 down + combine
+beam_status_t run_experts_nvfp4(const beam_moe_config_t& c, const void* hidden, const int32_t* idx,
+                                const float* w, const beam_fp4_weight_t& gate,
+                                const beam_fp4_weight_t& up, const beam_fp4_weight_t& down,
+                                void* out, int64_t T, void* ws, const Layout& L,
+                                const DevInfo& dev, cudaStream_t s) {
+  const int64_t TK = T * c.topk;
+  const int64_t rows = std::max<int64_t>(TK, kMinRows);
+  const int nt = fp4_tile(c, TK);
+  uint32_t* status = at<uint32_t>(ws, L.status);
+  beam::PermuteArgs pa;
+  pa.idx = idx;
+  pa.w = w;
+  pa.TK = TK;
+  pa.E = c.n_experts;
+  pa.counts = at<int32_t>(ws, L.counts);
+  pa.offsets = at<int32_t>(ws, L.offsets);
+  pa.perm_src = at<int32_t>(ws, L.perm_src);
+  pa.pair_row = at<int32_t>(ws, L.pair_row);
+  pa.perm_w = at<float>(ws, L.perm_w);
+  pa.status = status;
+  beam::launch_permute(pa, s);
+  record(3, s);
+  uint8_t* xq = at<uint8_t>(ws, L.x_fp4);
+  uint8_t* xsf = at<uint8_t>(ws, L.x_sf);
+  uint8_t* hq = at<uint8_t>(ws, L.h_fp4);
+  uint8_t* hsf = at<uint8_t>(ws, L.h_sf);
+  float* y = at<float>(ws, L.y);
+  beam::launch_quantize_rows(static_cast<const uint16_t*>(hidden), pa.perm_src,
+                             pa.offsets + c.n_experts, TK, c.topk, c.d, xq, xsf, s);
+  record(4, s);
+  if (cudaGetLastError() != cudaSuccess) return BEAM_ERR_CUDA;
+
+  const int64_t EF = static_cast<int64_t>(c.n_experts) * c.d_ff;
+  const int64_t ED = static_cast<int64_t>(c.n_experts) * c.d;
+  CUtensorMap tm_g, tm_u, tm_d, tm_x, tm_xsf, tm_h, tm_hsf;
+  if (!tmap_u8(&tm_g, gate.q, EF, c.d / 2, 128, 128) ||
+      !tmap_u8(&tm_u, up.q, EF, c.d / 2, 128, 128) ||
+      !tmap_u8(&tm_d, down.q, ED, c.d_ff / 2, 128, 128) ||
+      !tmap_u8(&tm_x, xq, rows, c.d / 2, 128, nt) || !tmap_u8(&tm_xsf, xsf, rows, c.d / 4, 16, 32) ||
+      !tmap_u8(&tm_h, hq, rows, c.d_ff / 2, 128, nt) ||
+      !tmap_u8(&tm_hsf, hsf, rows, c.d_ff / 4, 16, 32))
+    return BEAM_ERR_CUDA;
+  beam::Fp4GemmArgs fa{};
+  fa.counts = pa.counts;
+  fa.offsets = pa.offsets;
+  fa.perm_w = pa.perm_w;
+  fa.E = c.n_experts;
+  fa.status = status;
+  fa.wait_limit_ns = g_wait_ns;
+  fa.weight_evict_first = small_batch(c, TK) ? 1 : 0;
+  auto grid_for = [&](int m_blocks) {
+    const int64_t tiles = static_cast<int64_t>(m_blocks) * (c.n_experts + (TK + nt - 1) / nt);
+    return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(dev.sms, tiles)));
+  };
+  fa.sfa0 = gate.sf;
+  fa.sfa1 = up.sf;
+  fa.gs0 = gate.global_scale;
+  fa.gs1 = up.global_scale;
+  fa.hq = hq;
+  fa.hsf = hsf;
+  fa.out_ld = c.d_ff;
+  fa.rows_per_expert = c.d_ff;
+  fa.m_blocks = c.d_ff / 128;
+  fa.k_blocks = c.d / 256;
+  if (beam::launch_fp4_gemm(true, nt, tm_g, tm_u, tm_x, tm_xsf, fa, grid_for(fa.m_blocks), s) !=
+      cudaSuccess)
+    return BEAM_ERR_CUDA;
+  record(5, s);
+  fa.sfa0 = down.sf;
+  fa.sfa1 = nullptr;
+  fa.gs0 = down.global_scale;
+  fa.gs1 = nullptr;
+  fa.hq = nullptr;
+  fa.hsf = nullptr;
+  fa.y = y;
+  fa.out_ld = c.d;
+  fa.rows_per_expert = c.d;
+  fa.m_blocks = c.d / 128;
+  fa.k_blocks = c.d_ff / 256;
+  if (beam::launch_fp4_gemm(false, nt, tm_d, tm_d, tm_h, tm_hsf, fa, grid_for(fa.m_blocks), s) !=
+      cudaSuccess)
+    return BEAM_ERR_CUDA;
+  record(6, s);
+  beam::launch_combine(y, pa.pair_row, T, c.topk, c.d, static_cast<uint16_t*>(out), s);
+  record(7, s);
+  return cuda_status(cudaGetLastError());
+}
+
+bool valid_fp4_weight(const beam_fp4_weight_t* w) {
+  return w && aligned16(w->q) && aligned16(w->sf) && aligned16(w->global_scale);
+}
+
 // ---------------------------------------------------------------- no-allocation scratch
 // Scratch for beam_moe_forward_noalloc, which serves callers that cannot
 // allocate device memory.  A fixed-size device array takes the place of the
@@ -364,15 +482,17 @@ void* noalloc_scratch_address() {
 extern "C" {
 
 size_t beam_moe_workspace_size(const beam_moe_config_t* cfg, int64_t T_max, int32_t weight_fmt) {
-  if (!valid_cfg(cfg) || T_max < 0 || weight_fmt != BEAM_WEIGHTS_BF16) return 0;
-  return make_layout(*cfg, T_max).total;
+  if (!valid_cfg(cfg) || T_max < 0) return 0;
+  if (weight_fmt != BEAM_WEIGHTS_BF16 && weight_fmt != BEAM_WEIGHTS_NVFP4) return 0;
+  return make_layout(*cfg, T_max, weight_fmt).total;
 }
 
 beam_status_t beam_moe_workspace_layout(const beam_moe_config_t* cfg, int64_t T_max,
                                         int32_t weight_fmt, beam_moe_ws_layout_t* out) {
-  if (!out || !valid_cfg(cfg) || T_max < 0 || weight_fmt != BEAM_WEIGHTS_BF16)
+  if (!out || !valid_cfg(cfg) || T_max < 0 ||
+      (weight_fmt != BEAM_WEIGHTS_BF16 && weight_fmt != BEAM_WEIGHTS_NVFP4))
     return BEAM_ERR_INVALID_ARG;
-  const Layout L = make_layout(*cfg, T_max);
+  const Layout L = make_layout(*cfg, T_max, weight_fmt);
   out->status = L.status;
   out->logits = L.logits;
   out->topk_idx = L.idx;
@@ -384,6 +504,10 @@ beam_status_t beam_moe_workspace_layout(const beam_moe_config_t* cfg, int64_t T_
   out->perm_w = L.perm_w;
   out->x_perm = L.x_perm;
   out->h = L.h;
+  out->x_fp4 = L.x_fp4;
+  out->x_sf = L.x_sf;
+  out->h_fp4 = L.h_fp4;
+  out->h_sf = L.h_sf;
   out->y = L.y;
   out->total = L.total;
   return BEAM_OK;
@@ -493,6 +617,44 @@ beam_status_t beam_moe_forward_noalloc(const beam_moe_config_t* cfg, const void*
   if (cudaMemsetAsync(scratch, 0, kAlign, s) != cudaSuccess) return BEAM_ERR_CUDA;
   return beam_moe_forward(cfg, hidden, router_w, corr_bias, w_gate, w_up, w_down, out, T,
                           scratch, kNoAllocScratchBytes, stream);
+}
+
+beam_status_t beam_moe_nvfp4_pack_scales(const uint8_t* sf_rowmajor, int64_t rows, int64_t S,
+                                         uint8_t* sf_blocked, void* stream) {
+  if (rows < 0 || S <= 0 || rows % 128 || S % 4) return BEAM_ERR_INVALID_ARG;
+  if (rows == 0) return BEAM_OK;
+  if (!aligned16(sf_rowmajor) || !aligned16(sf_blocked)) return BEAM_ERR_INVALID_ARG;
+  DevInfo dev;
+  if (!device_info(&dev)) return BEAM_ERR_CUDA;
+  if (!dev.supported) return BEAM_ERR_UNSUPPORTED;
+  beam::launch_pack_scales(sf_rowmajor, rows, S, sf_blocked, static_cast<cudaStream_t>(stream));
+  return cuda_status(cudaGetLastError());
+}
+
+beam_status_t beam_moe_forward_nvfp4(const beam_moe_config_t* cfg, const void* hidden,
+                                     const float* router_w, const float* corr_bias,
+                                     const beam_fp4_weight_t* gate, const beam_fp4_weight_t* up,
+                                     const beam_fp4_weight_t* down, void* out, int64_t T,
+                                     void* workspace, size_t ws_bytes, void* stream) {
+  Layout L;
+  DevInfo dev;
+  bool empty = false;
+  beam_status_t st = common_checks(cfg, T, workspace, ws_bytes, &L, &dev, &empty,
+                                   BEAM_WEIGHTS_NVFP4);
+  if (st != BEAM_OK || empty) return st;
+  if (!aligned16(hidden) || !aligned16(router_w) || !aligned16(corr_bias) ||
+      !valid_fp4_weight(gate) || !valid_fp4_weight(up) || !valid_fp4_weight(down) ||
+      !aligned16(out))
+    return BEAM_ERR_INVALID_ARG;
+  if (!encoder()) return BEAM_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  record(0, s);
+  int32_t* idx = at<int32_t>(workspace, L.idx);
+  float* w = at<float>(workspace, L.w);
+  st = run_route(*cfg, hidden, router_w, corr_bias, T, idx, w, at<float>(workspace, L.logits),
+                 workspace, L, dev, s);
+  if (st != BEAM_OK) return st;
+  return run_experts_nvfp4(*cfg, hidden, idx, w, *gate, *up, *down, out, T, workspace, L, dev, s);
 }
 
 beam_status_t beam_moe_check_status(void* workspace, void* stream) {

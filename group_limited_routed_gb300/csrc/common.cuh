@@ -98,4 +98,38 @@ cudaError_t launch_router_tc(const CUtensorMap& w_planes, const CUtensorMap& x, 
                              int64_t T, int32_t E, int32_t d, uint32_t* status,
                              uint64_t wait_limit_ns, int num_sms, cudaStream_t s);
 
+// ---------------------------------------------------------------- NVFP4
+struct Fp4GemmArgs {
+  const int32_t* counts;
+  const int32_t* offsets;
+  const float* perm_w;     // [rows] routing weight (down)
+  const uint8_t* sfa0;     // blocked E4M3 weight scales (gate or down)
+  const uint8_t* sfa1;     // blocked E4M3 weight scales (up)
+  const float* gs0;        // [E] FP32 scale (gate or down)
+  const float* gs1;        // [E] FP32 scale (up)
+  uint8_t* hq;             // gate/up out: h codes [rows, F/2]
+  uint8_t* hsf;            // gate/up out: h scales [rows, F/4] (16-byte slot per 64)
+  float* y;                // down out: [rows, d]
+  int32_t out_ld;          // F (gate/up) or d (down), in elements
+  int32_t E;
+  int32_t rows_per_expert;
+  int32_t m_blocks;
+  int32_t k_blocks;        // K / 256
+  int32_t weight_evict_first;
+  uint32_t* status;
+  uint64_t wait_limit_ns;
+};
+
+// [rows, S] row-major E4M3 scales -> 128-row x 4-scale blocks (see nvfp4.cu)
+void launch_pack_scales(const uint8_t* src, int64_t rows, int64_t S, uint8_t* dst, cudaStream_t s);
+// permuted token rows -> NVFP4 codes [rows, d/2] and scales [rows, d/4]
+// (one 16-byte slot, 4 scales + padding, per 64 elements)
+void launch_quantize_rows(const uint16_t* x, const int32_t* perm_src, const int32_t* n_valid,
+                          int64_t TK, int32_t k, int32_t d, uint8_t* xq, uint8_t* xsf,
+                          cudaStream_t s);
+// block-scaled FP4 grouped GEMM, nt = 16 | 32; sfb maps the token scales
+cudaError_t launch_fp4_gemm(bool gateup, int nt, const CUtensorMap& a0, const CUtensorMap& a1,
+                            const CUtensorMap& b, const CUtensorMap& sfb, const Fp4GemmArgs& p,
+                            int grid, cudaStream_t s);
+
 }  // namespace beam

@@ -121,6 +121,52 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint6
       : "memory");
 }
 
+// D[tmem] (+)= (A * SFA)[smem] * (B * SFB)[smem]^T, kind::mxf4nvf4: packed E2M1
+// A and B (two per byte, K-major), one UE4M3 scale per 16 elements along K
+// (scale_vec::4X), FP32 D.  K per instruction = 64.  For M = 128 (or N <= 128
+// for B) row r's four scales of the K chunk are the 32-bit TMEM word at lane
+// r % 32 (of any lane quarter) and column sf + r / 32, byte g = scale of the
+// g-th 16 elements.
+__device__ __forceinline__ void mma_fp4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                        uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                        uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X "
+      "[%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// Copy 32 rows x 16 bytes of shared memory into TMEM (4 columns), the same
+// rows into each of the four lane quarters (lane 32q + j <- row j).
+__device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t src_desc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(src_desc)
+               : "memory");
+}
+
+// Shared-memory descriptor of an unswizzled operand whose 16-byte rows are
+// contiguous (8-row core matrices 128 bytes apart).
+__device__ __forceinline__ uint64_t sdesc_rows16(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(128u >> 4) << 16;
+  d |= static_cast<uint64_t>(128u >> 4) << 32;
+  d |= static_cast<uint64_t>(1u) << 46;
+  return d;
+}
+
+// 1-D bulk copy global -> shared (16-byte aligned, size a multiple of 16).
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05 operation this thread issued so far
 // has completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
@@ -167,6 +213,12 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
 //   bits 17-22 N >> 3              bits 24-28 M >> 4
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+
+// Instruction descriptor, kind::mxf4nvf4: E2M1 A and B (format code 1, both
+// K-major), UE4M3 scales (bit 23 = 0), FP32 D; N >> 3 at bit 17, M >> 4 at 24.
+__host__ __device__ constexpr uint32_t idesc_fp4_f32(uint32_t M, uint32_t N) {
+  return (1u << 7) | (1u << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 
 }  // namespace ptx

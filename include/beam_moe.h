@@ -110,6 +110,11 @@ typedef struct {
   size_t x_perm;        /* BF16 [T*topk, d] gathered expert inputs (only when
                            T*topk > 4*E; smaller batches gather in the GEMM) */
   size_t h;             /* BF16 [T*topk, F] SwiGLU activations                */
+  size_t x_fp4;         /* NVFP4 path: token rows, E2M1 codes [T*topk, d/2]   */
+  size_t x_sf;          /*   their E4M3 scales [T*topk, d/4]: per 64 elements a
+                             16-byte slot, 4 scales then padding             */
+  size_t h_fp4;         /*   SwiGLU activations [T*topk, F/2]                  */
+  size_t h_sf;          /*   and their scales [T*topk, F/4], same slots        */
   size_t y;             /* FP32 [T*topk, d] weighted expert outputs           */
   size_t total;         /* == beam_moe_workspace_size                         */
 } beam_moe_ws_layout_t;
@@ -176,6 +181,42 @@ beam_status_t beam_moe_forward_noalloc(const beam_moe_config_t *cfg, const void 
                                        const void *w_gate, const void *w_up,
                                        const void *w_down, void *out, int64_t T,
                                        void *stream);
+
+/* NVFP4 expert weights of one projection (gate, up or down), N output rows
+ * and K inputs per expert ("ModelOpt NVFP4" checkpoints, SGLang post, section
+ * "Highlights"; vLLM post, "MoE and residual stream": NVFP4 experts).
+ * A weight is q * sf * global_scale[e]. */
+typedef struct {
+  const uint8_t *q;             /* E2M1 codes [E, N, K/2], two per byte, low nibble = even k */
+  const uint8_t *sf;            /* E4M3 scales, one per 16 along K, of the [E*N, K/16]
+                                   row-major matrix in the blocked order that
+                                   beam_moe_nvfp4_pack_scales writes             */
+  const float *global_scale;    /* [E] FP32                                        */
+} beam_fp4_weight_t;
+
+/* Reorders row-major E4M3 block scales [rows, S] (rows % 128 == 0,
+ * S % 4 == 0) into blocks of 128 rows x 4 scales, 512 bytes each, block
+ * (row/128, s/4) at ((row/128) * (S/4) + s/4) * 512 and byte
+ * (r % 32) * 16 + (r / 32) * 4 + s % 4 inside it (r = row % 128): the order in
+ * which the tensor cores take weight scales.  Run once per weight tensor when
+ * the weights are loaded; `dst` is a device buffer of rows * S bytes.  No
+ * counterpart on the pages (the storage order is this library's). */
+beam_status_t beam_moe_nvfp4_pack_scales(const uint8_t *sf_rowmajor, int64_t rows, int64_t S,
+                                         uint8_t *sf_blocked, void *stream);
+
+/* The whole layer with NVFP4 experts.  Router and selection as in
+ * beam_moe_forward; both expert GEMM inputs are quantised to NVFP4 (per 16
+ * elements: scale = E4M3(amax / 6), codes = E2M1(value / scale), round to
+ * nearest even, saturating; global scale 1) -- x along d before the gate/up
+ * GEMM, the FP32 SwiGLU product along d_ff before the down GEMM -- and the
+ * GEMMs run as block-scaled FP4 MMAs with FP32 accumulation; the per-expert
+ * FP32 scales multiply the accumulators.  Extra shape rules: d % 256 == 0,
+ * d_ff % 256 == 0.  Workspace: beam_moe_workspace_size(cfg, T, BEAM_WEIGHTS_NVFP4). */
+beam_status_t beam_moe_forward_nvfp4(const beam_moe_config_t *cfg, const void *hidden,
+                                     const float *router_w, const float *corr_bias,
+                                     const beam_fp4_weight_t *gate, const beam_fp4_weight_t *up,
+                                     const beam_fp4_weight_t *down, void *out, int64_t T,
+                                     void *workspace, size_t ws_bytes, void *stream);
 
 /* Synchronises `stream`, returns the workspace's latched status and clears
  * it.  The only entry point that waits for the device. */
