@@ -48,6 +48,20 @@ TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 
 
 # ------------------------------------------------------------------ helpers
+def reduce_max(values, use_dist: bool, device="cpu"):
+    """Element-wise max over ranks (the job's time is its slowest rank's)."""
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    if use_dist:
+        import torch.distributed as dist
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def job_throughput(world: int, tokens_per_rank: int, steps: int, ms: float) -> float:
+    """Whole-job tokens/s: every rank's tokens over the slowest rank's time."""
+    return world * tokens_per_rank * steps / (ms / 1e3)
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     return int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")), ws
@@ -327,12 +341,9 @@ def run_gpu(args, cfg):
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1)
 
-    times = torch.tensor([ms, e2e_ms], device=dev)
-    if use_dist:
-        dist.all_reduce(times, op=dist.ReduceOp.MAX)
-    ms, e2e_ms = float(times[0]), float(times[1])
-    value = world * cfg.T * args.steps / (ms / 1e3)
-    e2e_value = world * cfg.T * e2e_steps / (e2e_ms / 1e3)
+    ms, e2e_ms = reduce_max([ms, e2e_ms], use_dist, dev)
+    value = job_throughput(world, cfg.T, args.steps, ms)
+    e2e_value = job_throughput(world, cfg.T, e2e_steps, e2e_ms)
 
     pk = peaks()
     # weight bytes of one projection of one expert: BF16, or E2M1 + E4M3 per 16

@@ -74,6 +74,11 @@ CONFIGS = {
                                  n_groups=8, topk_groups=4, topk=8, d_ff=2560, seed=6,
                                  description="Beam expert shapes, 32 experts (8x4), T=1024 "
                                              "(profiling case, prefill regime)"),
+    # profiling case for the NVFP4 kernels: 32 experts, decode-sized batch
+    "profile_fp4": MoEConfig(name="profile_fp4", T=16, d=5120, n_experts=32, n_groups=8,
+                             topk_groups=4, topk=8, d_ff=2560, seed=8, weight_fmt="nvfp4",
+                             description="Beam expert shapes, 32 NVFP4 experts (8x4), T=16 "
+                                         "(profiling case)"),
     "nvfp4": MoEConfig(name="nvfp4", T=128, seed=4, weight_fmt="nvfp4", **_BEAM,
                        description="Beam MoE layer NVFP4 experts T=128 (E2M1 + E4M3 per "
                                    "16 along K + FP32 per-tensor scale)"),
