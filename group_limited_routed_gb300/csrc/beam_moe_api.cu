@@ -132,10 +132,10 @@ int router_chunk(const beam_moe_config_t& c, int ks) {
 }
 
 // Token-block widths of the two expert GEMMs: 16 when experts see a few rows
-// each (weight streaming), else 128 (gate/up, two accumulators) and 256
-// (down) for the compute-bound regime.
+// each (weight streaming), else 256 for the compute-bound regime (fewer
+// re-reads of each weight tile from L2).
 bool small_batch(const beam_moe_config_t& c, int64_t TK) { return TK <= 4LL * c.n_experts; }
-int gateup_tile(const beam_moe_config_t& c, int64_t TK) { return small_batch(c, TK) ? 16 : 128; }
+int gateup_tile(const beam_moe_config_t& c, int64_t TK) { return small_batch(c, TK) ? 16 : 256; }
 int down_tile(const beam_moe_config_t& c, int64_t TK) { return small_batch(c, TK) ? 16 : 256; }
 
 bool tensor_router(const beam_moe_config_t& c, int64_t T) {

@@ -30,9 +30,12 @@
 // the per-expert row counts: tile -> (expert, weight block, token block),
 // ordered so the token blocks of one weight block run on neighbouring CTAs at
 // the same time (their weight tiles are then read from HBM once and from L2
-// after).  Warp roles: warp 0 issues TMA loads into a STAGES-deep ring, warp 1
-// owns TMEM and issues tcgen05.mma from one thread, warps 2-5 drain the
-// accumulators (double-buffered when they fit in TMEM's 512 columns).  Every
+// after).  Warp roles: warp 0 streams weight tiles and warp 2 token tiles,
+// each into its own ring, warp 1
+// owns TMEM and issues tcgen05.mma from one thread, the remaining warps (4,
+// or 8 for 256-row token blocks: two per TMEM lane quarter, each draining half
+// of the columns) drain the accumulators, double-buffered when two fit in
+// TMEM's 512 columns.  Every
 // mbarrier wait is bounded: when one runs out the CTA latches
 // BEAM_ERR_TIMEOUT, stops, lets its copies in flight land, frees its TMEM and
 // returns.
@@ -59,7 +62,8 @@ constexpr unsigned kFull = 0xffffffffu;
 constexpr int BM = 128;
 constexpr int BK = 64;
 constexpr int UMMA_K = 16;
-constexpr int kThreads = 192;
+// warps: weight producer, MMA issuer, token producer, then the epilogue warps
+constexpr int threads_for(int nt) { return 96 + 32 * (nt >= 256 ? 8 : 4); }
 constexpr int kMaxE = 256;
 constexpr uint32_t kTileBudget = 216 * 1024;
 
@@ -69,23 +73,32 @@ constexpr uint32_t pow2_at_least(uint32_t v) {
   return p;
 }
 
+// Two rings of equal depth, one per producer warp: weight tiles and token
+// tiles (both may come from HBM: the gathered token copy and h are far larger
+// than L2), as many stages as fit.
 template <int NT, int MODE>
 struct Cfg {
   static constexpr int NUM_A = MODE == kModeGateUp ? 2 : 1;
   static constexpr uint32_t A_BYTES = BM * BK * 2;
-  static constexpr uint32_t B_BYTES = NT * BK * 2;
-  static constexpr uint32_t STAGE_BYTES = NUM_A * A_BYTES + B_BYTES;
-  static constexpr int STAGES_RAW = static_cast<int>(kTileBudget / STAGE_BYTES);
-  static constexpr int STAGES = STAGES_RAW > 16 ? 16 : STAGES_RAW;
+  static constexpr uint32_t A_STAGE = NUM_A * A_BYTES;
+  static constexpr uint32_t B_STAGE = NT * BK * 2;
+  static constexpr int SA_RAW = static_cast<int>(kTileBudget / (A_STAGE + B_STAGE));
+  static constexpr int SA = SA_RAW > 16 ? 16 : SA_RAW;
+  static constexpr int SB = SA;
+  static constexpr uint32_t B_RING = SA * A_STAGE;               // offset of the token ring
+  static constexpr int EPI_WARPS = NT >= 256 ? 8 : 4;
+  static constexpr int THREADS = 96 + 32 * EPI_WARPS;
   static constexpr uint32_t ACC_COLS = NUM_A * NT;
   static constexpr int ACC_BUFS = 2 * ACC_COLS <= 512 ? 2 : 1;
   static constexpr uint32_t TMEM_COLS = pow2_at_least(ACC_BUFS * ACC_COLS);
-  static constexpr uint32_t NUM_BARS = 2 * STAGES + 2 * ACC_BUFS + 1;
+  static constexpr uint32_t NUM_BARS = 2 * SA + 2 * SB + 2 * ACC_BUFS + 1;
   static constexpr uint32_t MISC_BYTES = 16 + 4 * (3 * kMaxE + 1);
-  static constexpr uint32_t SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + NUM_BARS * 8 + MISC_BYTES;
-  static_assert(B_BYTES % 1024 == 0, "token tile must keep 1024-byte stage alignment");
+  static constexpr uint32_t SMEM_BYTES =
+      1024 + SA * A_STAGE + SB * B_STAGE + NUM_BARS * 8 + MISC_BYTES;
+  static_assert(B_STAGE % 1024 == 0, "token tile must keep 1024-byte alignment");
   static_assert(TMEM_COLS <= 512, "TMEM has 512 columns");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+  static_assert(SB >= 2, "token ring needs two stages");
   static_assert(NT % 16 == 0 && NT >= 16 && NT <= 256, "MMA N for M = 128");
 };
 
@@ -95,7 +108,7 @@ __device__ __forceinline__ uint16_t f32_to_bf16(float v) {
 }
 
 template <int NT, int MODE>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(threads_for(NT), 1)
     expert_gemm_kernel(const __grid_constant__ CUtensorMap tm_a0,
                        const __grid_constant__ CUtensorMap tm_a1,
                        const __grid_constant__ CUtensorMap tm_b, const GemmArgs p) {
@@ -108,8 +121,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t raw_addr = ptx::smem_addr(smem_raw);
   const uint32_t pad = (1024u - (raw_addr & 1023u)) & 1023u;
   uint8_t* smem = smem_raw + pad;
-  const uint32_t tiles = raw_addr + pad;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
+  const uint32_t a_ring = raw_addr + pad;
+  const uint32_t b_ring = a_ring + C::B_RING;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::SA * C::A_STAGE + C::SB * C::B_STAGE);
   int32_t* misc = reinterpret_cast<int32_t*>(bars + C::NUM_BARS);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc);
   volatile int32_t* abort_flag = misc + 1;
@@ -118,24 +132,30 @@ __global__ void __launch_bounds__(kThreads, 1)
   int32_t* s_start = s_off + kMaxE;
 
   const uint32_t bar0 = ptx::smem_addr(bars);
-  auto full_bar = [&](int s) { return bar0 + 8u * s; };
-  auto empty_bar = [&](int s) { return bar0 + 8u * (C::STAGES + s); };
-  auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * C::STAGES + a); };
-  auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * C::STAGES + C::ACC_BUFS + a); };
-  const uint32_t done_bar = bar0 + 8u * (2 * C::STAGES + 2 * C::ACC_BUFS);
+  auto fullA = [&](int s) { return bar0 + 8u * s; };
+  auto emptyA = [&](int s) { return bar0 + 8u * (C::SA + s); };
+  auto fullB = [&](int s) { return bar0 + 8u * (2 * C::SA + s); };
+  auto emptyB = [&](int s) { return bar0 + 8u * (2 * C::SA + C::SB + s); };
+  auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * C::SA + 2 * C::SB + a); };
+  auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * C::SA + 2 * C::SB + C::ACC_BUFS + a); };
+  const uint32_t done_bar = bar0 + 8u * (2 * C::SA + 2 * C::SB + 2 * C::ACC_BUFS);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int E = p.E;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < C::STAGES; ++s) {
-      ptx::mbar_init(full_bar(s), 1);
-      ptx::mbar_init(empty_bar(s), 1);
+    for (int s = 0; s < C::SA; ++s) {
+      ptx::mbar_init(fullA(s), 1);
+      ptx::mbar_init(emptyA(s), 1);
+    }
+    for (int s = 0; s < C::SB; ++s) {
+      ptx::mbar_init(fullB(s), 1);
+      ptx::mbar_init(emptyB(s), 1);
     }
     for (int a = 0; a < C::ACC_BUFS; ++a) {
       ptx::mbar_init(tfull_bar(a), 1);
-      ptx::mbar_init(tempty_bar(a), 128);
+      ptx::mbar_init(tempty_bar(a), 32 * C::EPI_WARPS);
     }
     ptx::mbar_init(done_bar, 1);
     *abort_flag = 0;
@@ -150,7 +170,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tmem_alloc(ptx::smem_addr(tmem_slot), C::TMEM_COLS);
     ptx::tmem_relinquish();
   }
-  for (int e = threadIdx.x; e < E; e += kThreads) {
+  for (int e = threadIdx.x; e < E; e += C::THREADS) {
     s_cnt[e] = p.counts[e];
     s_off[e] = p.offsets[e];
   }
@@ -179,27 +199,65 @@ __global__ void __launch_bounds__(kThreads, 1)
   const Waiter W{abort_flag, p.status, p.wait_limit_ns};
 
   if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
-    // Lane 0 waits, arms the stage and loads the weight tiles.  With
-    // ROW_GATHER the token operand is gathered straight from the hidden rows:
-    // every lane issues one 128-byte row load per token it owns (box 64 x 1;
-    // the row lands at its swizzled place in the tile).  Otherwise the token
-    // operand (x gathered into expert order, or h) comes as one tile load.
-    constexpr int RPL = (NT + 31) / 32;  // token rows per lane
-    const uint64_t pol_w =
-        p.weight_evict_first ? ptx::policy_evict_first() : ptx::policy_evict_normal();
-    const uint64_t pol_b = ptx::policy_evict_last();
-    int last_parity[C::STAGES];
+    // ------------------------------------------------------ weight producer
+    if (lane == 0) {
+      const uint64_t pol_w =
+          p.weight_evict_first ? ptx::policy_evict_first() : ptx::policy_evict_normal();
+      int last_parity[C::SA];
 #pragma unroll
-    for (int s = 0; s < C::STAGES; ++s) last_parity[s] = -1;
+      for (int s = 0; s < C::SA; ++s) last_parity[s] = -1;
+      int stage = 0;
+      uint32_t phase = 0;
+      bool withhold = p.withhold_first_load != 0 && blockIdx.x == 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+        const TileInfo ti = decode_tile<NT>(tile, s_start, s_cnt, s_off, E);
+        if (ti.nvalid <= 0) continue;
+        const int a_row = ti.expert * p.rows_per_expert + ti.mblock * BM;
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (!W.wait(emptyA(stage), phase ^ 1u)) {
+            ok = false;
+            break;
+          }
+          if (withhold) {
+            withhold = false;  // test aid: this stage never fills
+          } else {
+            const uint32_t st = a_ring + stage * C::A_STAGE;
+            ptx::mbar_arrive_expect_tx(fullA(stage), C::A_STAGE);
+            ptx::tma_load_2d(st, &tm_a0, fullA(stage), kb * BK, a_row, pol_w);
+            if (GATEUP)
+              ptx::tma_load_2d(st + C::A_BYTES, &tm_a1, fullA(stage), kb * BK, a_row, pol_w);
+            last_parity[stage] = static_cast<int>(phase);
+          }
+          if (++stage == C::SA) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // the CTA may not exit while a copy into its shared memory is in flight
+#pragma unroll
+      for (int s = 0; s < C::SA; ++s)
+        if (last_parity[s] >= 0) W.wait_final(fullA(s), static_cast<uint32_t>(last_parity[s]));
+    }
+    __syncwarp();
+  } else if (warp == 2) {
+    // ------------------------------------------------------- token producer
+    // With ROW_GATHER every lane issues one 128-byte row load per token it
+    // owns (box 64 x 1; the row lands at its swizzled place in the tile);
+    // otherwise lane 0 loads the whole token tile (x gathered into expert
+    // order, or h).
+    constexpr int RPL = (NT + 31) / 32;  // token rows per lane
+    const uint64_t pol_b = ptx::policy_evict_last();
+    int last_parity[C::SB];
+#pragma unroll
+    for (int s = 0; s < C::SB; ++s) last_parity[s] = -1;
     int stage = 0;
     uint32_t phase = 0;
-    bool withhold = p.withhold_first_load != 0 && blockIdx.x == 0;
     bool ok = true;
     for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
       const TileInfo ti = decode_tile<NT>(tile, s_start, s_cnt, s_off, E);
       if (ti.nvalid <= 0) continue;
-      const int a_row = ti.expert * p.rows_per_expert + ti.mblock * BM;
       int tok[RPL];
       if constexpr (ROW_GATHER) {
 #pragma unroll
@@ -209,58 +267,47 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       const uint32_t tx_bytes =
-          ROW_GATHER ? C::NUM_A * C::A_BYTES + static_cast<uint32_t>(ti.nvalid) * BK * 2
-                     : C::STAGE_BYTES;
+          ROW_GATHER ? static_cast<uint32_t>(ti.nvalid) * BK * 2 : C::B_STAGE;
       for (int kb = 0; kb < p.k_blocks; ++kb) {
         int okw = 1;
-        if (lane == 0) okw = W.wait(empty_bar(stage), phase ^ 1u) ? 1 : 0;
+        if (lane == 0) okw = W.wait(emptyB(stage), phase ^ 1u) ? 1 : 0;
         okw = __shfl_sync(kFull, okw, 0);
         if (!okw) {
           ok = false;
           break;
         }
-        const uint32_t st = tiles + stage * C::STAGE_BYTES;
-        const uint32_t b_dst = st + C::NUM_A * C::A_BYTES;
-        if (withhold) {
-          withhold = false;  // test aid: this stage never fills
-        } else {
-          if (lane == 0) {
-            ptx::mbar_arrive_expect_tx(full_bar(stage), tx_bytes);
-            ptx::tma_load_2d(st, &tm_a0, full_bar(stage), kb * BK, a_row, pol_w);
-            if (GATEUP)
-              ptx::tma_load_2d(st + C::A_BYTES, &tm_a1, full_bar(stage), kb * BK, a_row, pol_w);
-            if (!ROW_GATHER)
-              ptx::tma_load_2d(b_dst, &tm_b, full_bar(stage), kb * BK, ti.row0, pol_b);
-          }
-          if constexpr (ROW_GATHER) {
-            __syncwarp();
-#pragma unroll
-            for (int j = 0; j < RPL; ++j)
-              if (tok[j] >= 0)
-                ptx::tma_load_2d(b_dst + (lane + 32 * j) * (BK * 2), &tm_b, full_bar(stage),
-                                 kb * BK, tok[j], pol_b);
-          }
-          last_parity[stage] = static_cast<int>(phase);
+        const uint32_t st = b_ring + stage * C::B_STAGE;
+        if (lane == 0) {
+          ptx::mbar_arrive_expect_tx(fullB(stage), tx_bytes);
+          if (!ROW_GATHER) ptx::tma_load_2d(st, &tm_b, fullB(stage), kb * BK, ti.row0, pol_b);
         }
-        if (++stage == C::STAGES) {
+        if constexpr (ROW_GATHER) {
+          __syncwarp();
+#pragma unroll
+          for (int j = 0; j < RPL; ++j)
+            if (tok[j] >= 0)
+              ptx::tma_load_2d(st + (lane + 32 * j) * (BK * 2), &tm_b, fullB(stage), kb * BK,
+                               tok[j], pol_b);
+        }
+        last_parity[stage] = static_cast<int>(phase);
+        if (++stage == C::SB) {
           stage = 0;
           phase ^= 1u;
         }
       }
     }
-    // the CTA may not exit while a copy into its shared memory is in flight
     if (lane == 0) {
 #pragma unroll
-      for (int s = 0; s < C::STAGES; ++s)
-        if (last_parity[s] >= 0) W.wait_final(full_bar(s), static_cast<uint32_t>(last_parity[s]));
+      for (int s = 0; s < C::SB; ++s)
+        if (last_parity[s] >= 0) W.wait_final(fullB(s), static_cast<uint32_t>(last_parity[s]));
     }
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc_m = ptx::idesc_bf16_f32(BM, 0);
-      int stage = 0;
-      uint32_t phase = 0;
+      int sa = 0, sb = 0;
+      uint32_t pa = 0, pb = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
@@ -272,25 +319,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tc_fence_after();
         const uint32_t d0 = tmem_base + acc * C::ACC_COLS;
         for (int kb = 0; kb < p.k_blocks; ++kb) {
-          if (!W.wait(full_bar(stage), phase)) {
+          if (!W.wait(fullA(sa), pa) || !W.wait(fullB(sb), pb)) {
             ok = false;
             break;
           }
           ptx::tc_fence_after();
-          const uint32_t st = tiles + stage * C::STAGE_BYTES;
-          const uint32_t b_base = st + C::NUM_A * C::A_BYTES;
+          const uint32_t st = a_ring + sa * C::A_STAGE;
+          const uint32_t bt = b_ring + sb * C::B_STAGE;
 #pragma unroll
           for (int kk = 0; kk < BK / UMMA_K; ++kk) {
             const uint32_t accum = (kb | kk) ? 1u : 0u;
-            const uint64_t bd = ptx::sdesc_sw128(b_base + kk * 32);
+            const uint64_t bd = ptx::sdesc_sw128(bt + kk * 32);
             ptx::mma_bf16(d0, ptx::sdesc_sw128(st + kk * 32), bd, idesc, accum);
             if (GATEUP)
               ptx::mma_bf16(d0 + NT, ptx::sdesc_sw128(st + C::A_BYTES + kk * 32), bd, idesc, accum);
           }
-          ptx::mma_commit(empty_bar(stage));  // frees the stage once these MMAs read it
-          if (++stage == C::STAGES) {
-            stage = 0;
-            phase ^= 1u;
+          // free both stages once these MMAs have read them
+          ptx::mma_commit(emptyA(sa));
+          ptx::mma_commit(emptyB(sb));
+          if (++sa == C::SA) {
+            sa = 0;
+            pa ^= 1u;
+          }
+          if (++sb == C::SB) {
+            sb = 0;
+            pb ^= 1u;
           }
         }
         if (!ok) break;
@@ -309,6 +362,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int m = q * 32 + lane;
+    // with 8 epilogue warps, warps 3-6 take the first half of the columns
+    constexpr int COLS_PER_WARP = NT / (C::EPI_WARPS / 4);
+    const int col_begin = ((warp - 3) >> 2) * COLS_PER_WARP;
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
@@ -319,7 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t tq = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * C::ACC_COLS;
       const int col = ti.mblock * BM + m;
 #pragma unroll 1
-      for (int c0 = 0; c0 < ti.nvalid; c0 += 16) {
+      for (int c0 = col_begin; c0 < min(ti.nvalid, col_begin + COLS_PER_WARP); c0 += 16) {
         uint32_t ra[16];
         ptx::tmem_ld16(tq + c0, ra);
         if constexpr (GATEUP) {
@@ -372,7 +428,7 @@ cudaError_t launch_impl(const CUtensorMap& a0, const CUtensorMap& a1, const CUte
   cudaError_t err =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (err != cudaSuccess) return err;
-  kern<<<grid, kThreads, C::SMEM_BYTES, s>>>(a0, a1, b, p);
+  kern<<<grid, C::THREADS, C::SMEM_BYTES, s>>>(a0, a1, b, p);
   return cudaGetLastError();
 }
 
@@ -385,6 +441,7 @@ cudaError_t launch_grouped_gemm(int mode, int nt, const CUtensorMap& a0, const C
     case kModeGateUp:
       if (nt == 16) return launch_impl<16, kModeGateUp>(a0, a1, b, a, grid, s);
       if (nt == 128) return launch_impl<128, kModeGateUp>(a0, a1, b, a, grid, s);
+      if (nt == 256) return launch_impl<256, kModeGateUp>(a0, a1, b, a, grid, s);
       break;
     case kModeDown:
       if (nt == 16) return launch_impl<16, kModeDown>(a0, a0, b, a, grid, s);
