@@ -242,7 +242,7 @@ def run_reference(args, cfg):
     return 0
 
 
-def config_record(cfg, touched):
+def config_record(cfg, touched, routed=False):
     rec = {"workload": cfg.description, "T": cfg.T, "d": cfg.d, "n_experts": cfg.n_experts,
            "n_groups": cfg.n_groups, "topk_groups": cfg.topk_groups, "topk": cfg.topk,
            "d_ff": cfg.d_ff, "routed_scale": cfg.routed_scale, "weights": cfg.weight_fmt,
@@ -251,6 +251,8 @@ def config_record(cfg, touched):
                  "the 129 MB L2"}
     if touched is not None:
         rec["touched_experts"] = touched
+    if routed:
+        rec["routing"] = "replayed (recorded once; steps run experts + combine)"
     return rec
 
 
@@ -273,6 +275,14 @@ def run_gpu(args, cfg):
         def layer(x, o):
             return pkg.forward_nvfp4(cfg, x, t["router_w"], t["corr_bias"], *wts, out=o, ws=ws,
                                      stream=stream)
+    elif args.routed:
+        # routing replay: the routes are recorded once, the timed steps run
+        # the experts and the combine on them
+        ridx, rw = pkg.route(cfg, t["hidden"], t["router_w"], t["corr_bias"], stream=stream)
+
+        def layer(x, o):
+            return pkg.forward_routed(cfg, x, ridx, rw, t["w_gate"], t["w_up"], t["w_down"],
+                                      out=o, ws=ws, stream=stream)
     else:
         def layer(x, o):
             return pkg.forward(cfg, x, t["router_w"], t["corr_bias"], t["w_gate"], t["w_up"],
@@ -286,7 +296,10 @@ def run_gpu(args, cfg):
     torch.cuda.synchronize()
     if pkg.check_status(ws) != 0:
         raise RuntimeError("device status after warm-up")
-    touched = touched_experts(ws, cfg)
+    if args.routed:
+        touched = int(torch.unique(ridx).numel())
+    else:
+        touched = touched_experts(ws, cfg)
 
     # per-step stage events (created and recorded once so the handles exist)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(args.steps)]
@@ -360,7 +373,7 @@ def run_gpu(args, cfg):
         "warmup": args.warmup, "ms_per_step": layer_ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
         "dtype": "nvfp4 (e2m1 x e4m3 per 16)" if fp4 else "bf16", "data": "synthetic",
-        "config": config_record(cfg, touched),
+        "config": config_record(cfg, touched, args.routed),
         "roofline": {"bound": "hbm", "kernel": DOMINANT, "achieved": gu_gbs,
                      "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": gu_gbs / pk["hbm_gbs"],
                      "peak_source": pk["source"],
@@ -374,10 +387,11 @@ def run_gpu(args, cfg):
         "stage_us": {n: round(float(v) * 1e3, 1) for n, v in zip(STAGES, stage_ms)},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": cfg.T * cfg.d * 2,
                 "d2h_bytes_per_step": cfg.T * cfg.d * 2},
-        "gpu_launches": args.steps * pkg.kernels_per_forward(cfg, cfg.T),
+        "gpu_launches": args.steps * pkg.kernels_per_forward(
+            cfg, cfg.T, pkg.NVFP4 if fp4 else 0, args.routed),
         "clocks": clocks,
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.routed:
         line["cpu_baseline"] = cpu_baseline(cfg, t)
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -394,6 +408,8 @@ def main(argv=None):
     ap.add_argument("--config", default="decode", choices=sorted(inputs.CONFIGS))
     ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--routed", action="store_true",
+                    help="time beam_moe_forward_routed on recorded routes (routing replay)")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)
     cfg = inputs.CONFIGS[args.config]

@@ -93,7 +93,7 @@ def lib():
         L.beam_moe_set_stage_events.restype = _ST
         L.beam_moe_set_debug.argtypes = [ctypes.c_uint32, ctypes.c_int32]
         L.beam_moe_set_debug.restype = _ST
-        L.beam_moe_kernels_per_forward.argtypes = [cfgp, _I64]
+        L.beam_moe_kernels_per_forward.argtypes = [cfgp, _I64, ctypes.c_int32, ctypes.c_int32]
         L.beam_moe_kernels_per_forward.restype = ctypes.c_int32
         L.beam_status_string.argtypes = [_ST]
         L.beam_status_string.restype = ctypes.c_char_p
@@ -337,6 +337,7 @@ def set_debug(wait_limit_us: int = 0, withhold_first_load: bool = False) -> None
            "beam_moe_set_debug")
 
 
-def kernels_per_forward(cfg, T: int) -> int:
+def kernels_per_forward(cfg, T: int, weight_fmt: int = 0, routed: bool = False) -> int:
     c = _cfg(cfg)
-    return int(lib().beam_moe_kernels_per_forward(ctypes.byref(c), int(T)))
+    return int(lib().beam_moe_kernels_per_forward(ctypes.byref(c), int(T), int(weight_fmt),
+                                                  int(bool(routed))))

@@ -142,6 +142,13 @@ bool tensor_router(const beam_moe_config_t& c, int64_t T) {
   return T >= kTensorRouterMinT && c.n_experts % 128 == 0;
 }
 
+// Below the tensor-router threshold the router, the selection and the
+// permutation run as one cooperative launch (decode-sized batches, where
+// each of the three would be a few microseconds of mostly launch latency).
+bool fused_routing(const beam_moe_config_t& c, int64_t T) {
+  return T < kTensorRouterMinT && c.n_experts <= 256;
+}
+
 struct Layout {
   size_t status, part, logits, idx, w, counts, offsets, perm_src, pair_row, perm_w, x_perm, h, y,
       router_planes, x_fp4, x_sf, h_fp4, h_sf, total;
@@ -219,12 +226,33 @@ beam_status_t common_checks(const beam_moe_config_t* cfg, int64_t T, void* ws, s
   return BEAM_OK;
 }
 
-// router + selection into idx/w (and logits)
+beam::PermuteArgs permute_args(const beam_moe_config_t& c, const int32_t* idx, const float* w,
+                               int64_t T, void* ws, const Layout& L) {
+  beam::PermuteArgs pa;
+  pa.idx = idx;
+  pa.w = w;
+  pa.TK = T * c.topk;
+  pa.E = c.n_experts;
+  pa.counts = at<int32_t>(ws, L.counts);
+  pa.offsets = at<int32_t>(ws, L.offsets);
+  pa.perm_src = at<int32_t>(ws, L.perm_src);
+  pa.pair_row = at<int32_t>(ws, L.pair_row);
+  pa.perm_w = at<float>(ws, L.perm_w);
+  pa.status = at<uint32_t>(ws, L.status);
+  return pa;
+}
+
+// router + selection into idx/w (and logits).  With `permuted` given and a
+// decode-sized batch, the permutation runs in the same cooperative launch and
+// *permuted is set.
 beam_status_t run_route(const beam_moe_config_t& c, const void* hidden, const float* router_w,
                         const float* bias, int64_t T, int32_t* idx, float* w, float* logits,
-                        void* ws, const Layout& L, const DevInfo& dev, cudaStream_t s) {
+                        void* ws, const Layout& L, const DevInfo& dev, cudaStream_t s,
+                        bool* permuted = nullptr) {
   int ks = 1;
   float* part = at<float>(ws, L.part);
+  if (permuted) *permuted = false;
+  beam::RouterArgs ra;
   if (tensor_router(c, T)) {
     // BF16x3 on the tensor cores: W_r split into three BF16 planes
     uint16_t* planes = at<uint16_t>(ws, L.router_planes);
@@ -238,7 +266,6 @@ beam_status_t run_route(const beam_moe_config_t& c, const void* hidden, const fl
       return BEAM_ERR_CUDA;
   } else {
     ks = router_ksplit(c, T);
-    beam::RouterArgs ra;
     ra.x = static_cast<const uint16_t*>(hidden);
     ra.w = router_w;
     ra.part = part;
@@ -246,9 +273,7 @@ beam_status_t run_route(const beam_moe_config_t& c, const void* hidden, const fl
     ra.d = c.d;
     ra.E = c.n_experts;
     ra.k_chunk = router_chunk(c, ks);
-    beam::launch_router(ra, ks, s);
   }
-  record(1, s);
   beam::SelectArgs sa;
   sa.part = part;
   sa.ksplit = ks;
@@ -262,6 +287,17 @@ beam_status_t run_route(const beam_moe_config_t& c, const void* hidden, const fl
   sa.idx = idx;
   sa.w = w;
   sa.logits = logits;
+  if (!tensor_router(c, T) && permuted && fused_routing(c, T)) {
+    const beam::PermuteArgs pa = permute_args(c, idx, w, T, ws, L);
+    if (beam::launch_fused_route(ra, ks, sa, pa, dev.sms, s) != cudaSuccess) return BEAM_ERR_CUDA;
+    *permuted = true;
+    record(1, s);
+    record(2, s);
+    record(3, s);
+    return BEAM_OK;
+  }
+  if (!tensor_router(c, T)) beam::launch_router(ra, ks, s);
+  record(1, s);
   beam::launch_select(sa, s);
   record(2, s);
   return cuda_status(cudaGetLastError());
@@ -271,26 +307,18 @@ beam_status_t run_route(const beam_moe_config_t& c, const void* hidden, const fl
 beam_status_t run_experts(const beam_moe_config_t& c, const void* hidden, const int32_t* idx,
                           const float* w, const void* w_gate, const void* w_up,
                           const void* w_down, void* out, int64_t T, void* ws, const Layout& L,
-                          const DevInfo& dev, cudaStream_t s) {
+                          const DevInfo& dev, cudaStream_t s, bool permuted = false) {
   const int64_t TK = T * c.topk;
   const int64_t rows = std::max<int64_t>(TK, kMinRows);
   const int nt_gu = gateup_tile(c, TK);
   const int nt_dn = down_tile(c, TK);
   uint32_t* status = at<uint32_t>(ws, L.status);
 
-  beam::PermuteArgs pa;
-  pa.idx = idx;
-  pa.w = w;
-  pa.TK = TK;
-  pa.E = c.n_experts;
-  pa.counts = at<int32_t>(ws, L.counts);
-  pa.offsets = at<int32_t>(ws, L.offsets);
-  pa.perm_src = at<int32_t>(ws, L.perm_src);
-  pa.pair_row = at<int32_t>(ws, L.pair_row);
-  pa.perm_w = at<float>(ws, L.perm_w);
-  pa.status = status;
-  beam::launch_permute(pa, s);
-  record(3, s);
+  const beam::PermuteArgs pa = permute_args(c, idx, w, T, ws, L);
+  if (!permuted) {
+    beam::launch_permute(pa, s);
+    record(3, s);
+  }
   // decode-sized batches: the gate/up GEMM gathers its token rows itself
   const bool row_gather = small_batch(c, TK);
   uint16_t* xp = at<uint16_t>(ws, L.x_perm);
@@ -365,24 +393,16 @@ beam_status_t run_experts_nvfp4(const beam_moe_config_t& c, const void* hidden, 
                                 const float* w, const beam_fp4_weight_t& gate,
                                 const beam_fp4_weight_t& up, const beam_fp4_weight_t& down,
                                 void* out, int64_t T, void* ws, const Layout& L,
-                                const DevInfo& dev, cudaStream_t s) {
+                                const DevInfo& dev, cudaStream_t s, bool permuted = false) {
   const int64_t TK = T * c.topk;
   const int64_t rows = std::max<int64_t>(TK, kMinRows);
   const int nt = fp4_tile(c, TK);
   uint32_t* status = at<uint32_t>(ws, L.status);
-  beam::PermuteArgs pa;
-  pa.idx = idx;
-  pa.w = w;
-  pa.TK = TK;
-  pa.E = c.n_experts;
-  pa.counts = at<int32_t>(ws, L.counts);
-  pa.offsets = at<int32_t>(ws, L.offsets);
-  pa.perm_src = at<int32_t>(ws, L.perm_src);
-  pa.pair_row = at<int32_t>(ws, L.pair_row);
-  pa.perm_w = at<float>(ws, L.perm_w);
-  pa.status = status;
-  beam::launch_permute(pa, s);
-  record(3, s);
+  const beam::PermuteArgs pa = permute_args(c, idx, w, T, ws, L);
+  if (!permuted) {
+    beam::launch_permute(pa, s);
+    record(3, s);
+  }
   uint8_t* xq = at<uint8_t>(ws, L.x_fp4);
   uint8_t* xsf = at<uint8_t>(ws, L.x_sf);
   uint8_t* hq = at<uint8_t>(ws, L.h_fp4);
@@ -575,10 +595,12 @@ beam_status_t beam_moe_forward(const beam_moe_config_t* cfg, const void* hidden,
   record(0, s);
   int32_t* idx = at<int32_t>(workspace, L.idx);
   float* w = at<float>(workspace, L.w);
+  bool permuted = false;
   st = run_route(*cfg, hidden, router_w, corr_bias, T, idx, w, at<float>(workspace, L.logits),
-                 workspace, L, dev, s);
+                 workspace, L, dev, s, &permuted);
   if (st != BEAM_OK) return st;
-  return run_experts(*cfg, hidden, idx, w, w_gate, w_up, w_down, out, T, workspace, L, dev, s);
+  return run_experts(*cfg, hidden, idx, w, w_gate, w_up, w_down, out, T, workspace, L, dev, s,
+                     permuted);
 }
 
 beam_status_t beam_moe_forward_routed(const beam_moe_config_t* cfg, const void* hidden,
@@ -651,10 +673,12 @@ beam_status_t beam_moe_forward_nvfp4(const beam_moe_config_t* cfg, const void* h
   record(0, s);
   int32_t* idx = at<int32_t>(workspace, L.idx);
   float* w = at<float>(workspace, L.w);
+  bool permuted = false;
   st = run_route(*cfg, hidden, router_w, corr_bias, T, idx, w, at<float>(workspace, L.logits),
-                 workspace, L, dev, s);
+                 workspace, L, dev, s, &permuted);
   if (st != BEAM_OK) return st;
-  return run_experts_nvfp4(*cfg, hidden, idx, w, *gate, *up, *down, out, T, workspace, L, dev, s);
+  return run_experts_nvfp4(*cfg, hidden, idx, w, *gate, *up, *down, out, T, workspace, L, dev, s,
+                           permuted);
 }
 
 beam_status_t beam_moe_check_status(void* workspace, void* stream) {
@@ -689,10 +713,19 @@ beam_status_t beam_moe_set_debug(uint32_t wait_limit_us, int32_t withhold_first_
   return BEAM_OK;
 }
 
-int32_t beam_moe_kernels_per_forward(const beam_moe_config_t* cfg, int64_t T) {
+int32_t beam_moe_kernels_per_forward(const beam_moe_config_t* cfg, int64_t T, int32_t weight_fmt,
+                                     int32_t routed) {
   if (!valid_cfg(cfg) || T <= 0) return 0;
-  // router (+ plane split), select, permute, (gather), gate/up, down, combine
-  return 6 + (tensor_router(*cfg, T) ? 1 : 0) + (small_batch(*cfg, T * cfg->topk) ? 0 : 1);
+  if (weight_fmt != BEAM_WEIGHTS_BF16 && weight_fmt != BEAM_WEIGHTS_NVFP4) return 0;
+  if (routed && weight_fmt != BEAM_WEIGHTS_BF16) return 0;
+  // experts: permute, gather (BF16, larger batches) or row quantisation
+  // (NVFP4), gate/up, down, combine
+  const bool small = small_batch(*cfg, T * cfg->topk);
+  const int experts = weight_fmt == BEAM_WEIGHTS_NVFP4 ? 5 : 4 + (small ? 0 : 1);
+  if (routed) return experts;
+  // routing: router (+ plane split), select; decode-sized batches run router,
+  // select and permute as one launch
+  return experts + 2 + (tensor_router(*cfg, T) ? 1 : 0) - (fused_routing(*cfg, T) ? 2 : 0);
 }
 
 const char* beam_status_string(beam_status_t s) {

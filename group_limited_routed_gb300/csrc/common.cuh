@@ -53,6 +53,9 @@ struct PermuteArgs {
 void launch_router(const RouterArgs& a, int ksplit, cudaStream_t s);
 void launch_select(const SelectArgs& a, cudaStream_t s);
 void launch_permute(const PermuteArgs& a, cudaStream_t s);
+// router partials + selection + permutation in one cooperative launch
+cudaError_t launch_fused_route(const RouterArgs& ra, int ksplit, const SelectArgs& sa,
+                               const PermuteArgs& pa, int num_sms, cudaStream_t s);
 void launch_gather(const uint16_t* x, const int32_t* perm_src, const int32_t* n_valid, int64_t TK,
                    int32_t k, int32_t d, uint16_t* x_perm, cudaStream_t s);
 void launch_combine(const float* y, const int32_t* pair_row, int64_t T, int32_t k, int32_t d,

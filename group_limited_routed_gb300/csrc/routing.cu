@@ -10,6 +10,7 @@
 // expert outputs in slot order, rounded once to BF16 (SGLang post, section
 // "Fusion Optimizations": local expert summation, routed scaling, BF16
 // rounding).
+#include <cooperative_groups.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -21,6 +22,7 @@
 namespace beam {
 namespace {
 
+namespace cg = cooperative_groups;
 constexpr unsigned kFull = 0xffffffffu;
 
 __device__ __forceinline__ float bf16_to_f32(uint16_t v) {
@@ -40,13 +42,14 @@ __device__ __forceinline__ uint16_t f32_to_bf16(float v) {
 constexpr int kRtTok = 32;
 constexpr int kRtExp = 64;
 constexpr int kRtK = 32;
+constexpr int kRtDepth = 4;  // K slices whose loads are in flight together
 
-__global__ void __launch_bounds__(256) router_kernel(RouterArgs a) {
+__device__ __forceinline__ void router_tile(const RouterArgs& a, int bx, int by, int bz) {
   __shared__ float xs[kRtK][kRtTok + 1];
   __shared__ __align__(16) float ws[kRtK][kRtExp + 4];
-  const int e0 = blockIdx.x * kRtExp;
-  const int64_t t0 = static_cast<int64_t>(blockIdx.y) * kRtTok;
-  const int k_begin = blockIdx.z * a.k_chunk;
+  const int e0 = bx * kRtExp;
+  const int64_t t0 = static_cast<int64_t>(by) * kRtTok;
+  const int k_begin = bz * a.k_chunk;
   const int k_end = min(a.d, k_begin + a.k_chunk);
   const int tid = threadIdx.x;
   const int tx = tid & 15;
@@ -57,216 +60,195 @@ __global__ void __launch_bounds__(256) router_kernel(RouterArgs a) {
 #pragma unroll
     for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
 
-  // register prefetch of the next 32-wide K slice overlaps its load latency
-  // with the FMAs of the current one
+  // the loads of up to four 32-wide K slices are issued together, so a
+  // decode-sized K range (128) costs one memory round trip
   const int xr_row = tid >> 3, xr_col = (tid & 7) * 4;
   const bool x_ok = t0 + xr_row < a.T;
   const uint16_t* xsrc = a.x + (t0 + xr_row) * a.d + xr_col;
-  uint2 xreg = make_uint2(0u, 0u);
-  float4 wreg[2];
-  auto load_slice = [&](int kc) {
-    if (x_ok) xreg = *reinterpret_cast<const uint2*>(xsrc + kc);
+  uint2 xreg[kRtDepth];
+  float4 wreg[kRtDepth][2];
+  for (int kc0 = k_begin; kc0 < k_end; kc0 += kRtDepth * kRtK) {
 #pragma unroll
-    for (int rep = 0; rep < 2; ++rep) {
-      const int li = tid + rep * 256;
-      const int r = li >> 3;
-      const int c = (li & 7) * 4;
-      wreg[rep] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (e0 + r < a.E)
-        wreg[rep] =
-            *reinterpret_cast<const float4*>(a.w + static_cast<int64_t>(e0 + r) * a.d + kc + c);
-    }
-  };
-  if (k_begin < k_end) load_slice(k_begin);
-  for (int kc = k_begin; kc < k_end; kc += kRtK) {
-    xs[xr_col + 0][xr_row] = bf16_to_f32(static_cast<uint16_t>(xreg.x & 0xffffu));
-    xs[xr_col + 1][xr_row] = bf16_to_f32(static_cast<uint16_t>(xreg.x >> 16));
-    xs[xr_col + 2][xr_row] = bf16_to_f32(static_cast<uint16_t>(xreg.y & 0xffffu));
-    xs[xr_col + 3][xr_row] = bf16_to_f32(static_cast<uint16_t>(xreg.y >> 16));
+    for (int q = 0; q < kRtDepth; ++q) {
+      const int kc = kc0 + q * kRtK;
+      xreg[q] = make_uint2(0u, 0u);
+      wreg[q][0] = wreg[q][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (kc < k_end) {
+        if (x_ok) xreg[q] = *reinterpret_cast<const uint2*>(xsrc + kc);
 #pragma unroll
-    for (int rep = 0; rep < 2; ++rep) {
-      const int li = tid + rep * 256;
-      const int r = li >> 3;
-      const int c = (li & 7) * 4;
-      ws[c + 0][r] = wreg[rep].x;
-      ws[c + 1][r] = wreg[rep].y;
-      ws[c + 2][r] = wreg[rep].z;
-      ws[c + 3][r] = wreg[rep].w;
-    }
-    __syncthreads();
-    if (kc + kRtK < k_end) load_slice(kc + kRtK);
-    // blocked summation: each 32-wide slice is summed on its own, then added
-    float sl[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll
-    for (int kk = 0; kk < kRtK; ++kk) {
-      const float x0 = xs[kk][ty * 2];
-      const float x1 = xs[kk][ty * 2 + 1];
-      const float4 wv = *reinterpret_cast<const float4*>(&ws[kk][tx * 4]);
-      sl[0][0] = fmaf(x0, wv.x, sl[0][0]);
-      sl[0][1] = fmaf(x0, wv.y, sl[0][1]);
-      sl[0][2] = fmaf(x0, wv.z, sl[0][2]);
-      sl[0][3] = fmaf(x0, wv.w, sl[0][3]);
-      sl[1][0] = fmaf(x1, wv.x, sl[1][0]);
-      sl[1][1] = fmaf(x1, wv.y, sl[1][1]);
-      sl[1][2] = fmaf(x1, wv.z, sl[1][2]);
-      sl[1][3] = fmaf(x1, wv.w, sl[1][3]);
+        for (int rep = 0; rep < 2; ++rep) {
+          const int li = tid + rep * 256;
+          const int r = li >> 3;
+          const int c = (li & 7) * 4;
+          if (e0 + r < a.E)
+            wreg[q][rep] = *reinterpret_cast<const float4*>(a.w + static_cast<int64_t>(e0 + r) * a.d +
+                                                            kc + c);
+        }
+      }
     }
 #pragma unroll
-    for (int i = 0; i < 2; ++i)
+    for (int q = 0; q < kRtDepth; ++q) {
+      if (kc0 + q * kRtK >= k_end) break;
+      xs[xr_col + 0][xr_row] = bf16_to_f32(static_cast<uint16_t>(xreg[q].x & 0xffffu));
+      xs[xr_col + 1][xr_row] = bf16_to_f32(static_cast<uint16_t>(xreg[q].x >> 16));
+      xs[xr_col + 2][xr_row] = bf16_to_f32(static_cast<uint16_t>(xreg[q].y & 0xffffu));
+      xs[xr_col + 3][xr_row] = bf16_to_f32(static_cast<uint16_t>(xreg[q].y >> 16));
 #pragma unroll
-      for (int j = 0; j < 4; ++j) acc[i][j] += sl[i][j];
-    __syncthreads();
+      for (int rep = 0; rep < 2; ++rep) {
+        const int li = tid + rep * 256;
+        const int r = li >> 3;
+        const int c = (li & 7) * 4;
+        ws[c + 0][r] = wreg[q][rep].x;
+        ws[c + 1][r] = wreg[q][rep].y;
+        ws[c + 2][r] = wreg[q][rep].z;
+        ws[c + 3][r] = wreg[q][rep].w;
+      }
+      __syncthreads();
+      // blocked summation: each 32-wide slice is summed on its own, then added
+      float sl[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+      for (int kk = 0; kk < kRtK; ++kk) {
+        const float x0 = xs[kk][ty * 2];
+        const float x1 = xs[kk][ty * 2 + 1];
+        const float4 wv = *reinterpret_cast<const float4*>(&ws[kk][tx * 4]);
+        sl[0][0] = fmaf(x0, wv.x, sl[0][0]);
+        sl[0][1] = fmaf(x0, wv.y, sl[0][1]);
+        sl[0][2] = fmaf(x0, wv.z, sl[0][2]);
+        sl[0][3] = fmaf(x0, wv.w, sl[0][3]);
+        sl[1][0] = fmaf(x1, wv.x, sl[1][0]);
+        sl[1][1] = fmaf(x1, wv.y, sl[1][1]);
+        sl[1][2] = fmaf(x1, wv.z, sl[1][2]);
+        sl[1][3] = fmaf(x1, wv.w, sl[1][3]);
+      }
+#pragma unroll
+      for (int i = 0; i < 2; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] += sl[i][j];
+      __syncthreads();
+    }
   }
 #pragma unroll
   for (int i = 0; i < 2; ++i) {
     const int64_t t = t0 + ty * 2 + i;
     const int e = e0 + tx * 4;
     if (t < a.T && e < a.E) {
-      float* dst = a.part + (static_cast<int64_t>(blockIdx.z) * a.T + t) * a.E + e;
+      float* dst = a.part + (static_cast<int64_t>(bz) * a.T + t) * a.E + e;
       *reinterpret_cast<float4*>(dst) = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
     }
   }
 }
 
 // --------------------------------------------------------------- selection
-// Phase 1 (whole block): thread e sums the router's split-K partials of
-// expert e for each token of the block, in split order, into shared memory.
-// Phase 2: one warp per token.  Lane l holds experts j*32 + l (j < E/32).
-// Groups are S = E/G consecutive experts, S a power of two <= 32, so a group
-// is an aligned segment of S lanes of one register.
-constexpr int kSelMaxTok = 8;
+// One token per block, thread e owns expert e (E <= 256 = blockDim).
+//  1. logit: the router's split-K partials of expert e summed in split order;
+//     score s = sigmoid(logit), choice score c = s + bias.
+//  2. group score: top-1 + top-2 of c inside each group of S = E/G
+//     consecutive experts (S a power of two <= 32, so a group is an aligned
+//     segment of S lanes of one warp: a butterfly of log2(S) steps).
+//  3. group g is kept when fewer than kg groups precede it in the order
+//     (score desc, group asc).
+//  4. expert e of a kept group takes slot r = the number of experts of kept
+//     groups that precede it in the order (c desc, expert asc); r < k selects
+//     it.  This ranking gives the same slots as k rounds of argmax.  The kept
+//     groups' scores are first packed into one array for vector loads.
+//  5. weights: alpha * s / (sum of the k selected s in slot order), in FP64,
+//     rounded once to FP32.
+constexpr int kSelMaxG = 128;
 
-__global__ void __launch_bounds__(256) select_kernel(SelectArgs a, int tok_per_block) {
-  __shared__ float s_logit[kSelMaxTok][256];
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  const int64_t t0 = static_cast<int64_t>(blockIdx.x) * tok_per_block;
+__device__ __forceinline__ void select_token(const SelectArgs& a, int64_t t) {
+  __shared__ float s_gs[kSelMaxG];
+  __shared__ int s_pos[kSelMaxG];
+  __shared__ __align__(16) float s_kc[256];
+  __shared__ __align__(16) int s_ke[256];
+  __shared__ int s_slot_e[32];
+  __shared__ float s_slot_s[32];
+  const int e = threadIdx.x;
+  const int lane = e & 31;
   const int E = a.E;
-  for (int tk = 0; tk < tok_per_block; ++tk) {
-    const int64_t t = t0 + tk;
-    const int e = threadIdx.x;
-    if (t < a.T && e < E) {
-      const float* src = a.part + t * E + e;
-      const int64_t stride = a.T * E;
-      float lg = src[0];
-      int sp = 1;
-      for (; sp + 8 <= a.ksplit; sp += 8) {
-        float v[8];
+  const int S = E / a.G;
+  const bool live = e < E;
+  const float bias = live ? a.bias[e] : 0.f;
+
+  float lg = 0.f;
+  if (live) {
+    const float* src = a.part + t * E + e;
+    const int64_t stride = a.T * E;
+    lg = src[0];
+    int sp = 1;
+    for (; sp + 16 <= a.ksplit; sp += 16) {
+      float v[16];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) v[u] = src[(sp + u) * stride];
+      for (int u = 0; u < 16; ++u) v[u] = src[(sp + u) * stride];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) lg += v[u];
-      }
-      for (; sp < a.ksplit; ++sp) lg += src[sp * stride];
-      s_logit[tk][e] = lg;
-      if (a.logits) a.logits[t * E + e] = lg;
+      for (int u = 0; u < 16; ++u) lg += v[u];
+    }
+    for (; sp < a.ksplit; ++sp) lg += src[sp * stride];
+    if (a.logits) a.logits[t * E + e] = lg;
+  }
+  const float sc = live ? 1.0f / (1.0f + expf(-lg)) : 0.f;
+  const float c = live ? sc + bias : -FLT_MAX;
+
+  float m1 = c, m2 = -FLT_MAX;
+  for (int o = S >> 1; o >= 1; o >>= 1) {
+    const float b1 = __shfl_xor_sync(kFull, m1, o);
+    const float b2 = __shfl_xor_sync(kFull, m2, o);
+    const float n1 = fmaxf(m1, b1);
+    const float n2 = fmaxf(fminf(m1, b1), fmaxf(m2, b2));
+    m1 = n1;
+    m2 = n2;
+  }
+  if (live && (lane & (S - 1)) == 0) s_gs[e / S] = m1 + m2;
+  __syncthreads();
+  // a kept group's place among the kept groups: its rank, below kg
+  if (e < a.G) {
+    const float v = s_gs[e];
+    int before = 0;
+    for (int h = 0; h < a.G; ++h) {
+      const float u = s_gs[h];
+      before += (u > v || (u == v && h < e)) ? 1 : 0;
+    }
+    s_pos[e] = before < a.kg ? before : -1;
+  }
+  __syncthreads();
+  // the kept groups' choice scores, packed (any order: ties compare indices),
+  // padded to a multiple of four with entries that precede nothing
+  const int pos = live ? s_pos[e / S] : -1;
+  const int n = a.kg * S;
+  const int n4 = (n + 3) & ~3;
+  if (pos >= 0) {
+    s_kc[pos * S + (e & (S - 1))] = c;
+    s_ke[pos * S + (e & (S - 1))] = e;
+  }
+  if (e >= n && e < n4) {
+    s_kc[e] = -FLT_MAX;
+    s_ke[e] = 1 << 30;
+  }
+  __syncthreads();
+  if (pos >= 0) {
+    int rank = 0;
+    const float4* kc = reinterpret_cast<const float4*>(s_kc);
+    const int4* ke = reinterpret_cast<const int4*>(s_ke);
+#pragma unroll 4
+    for (int i = 0; i < n4 / 4; ++i) {
+      const float4 u = kc[i];
+      const int4 f = ke[i];
+      rank += (u.x > c || (u.x == c && f.x < e)) ? 1 : 0;
+      rank += (u.y > c || (u.y == c && f.y < e)) ? 1 : 0;
+      rank += (u.z > c || (u.z == c && f.z < e)) ? 1 : 0;
+      rank += (u.w > c || (u.w == c && f.w < e)) ? 1 : 0;
+    }
+    if (rank < a.k) {
+      s_slot_e[rank] = e;
+      s_slot_s[rank] = sc;
     }
   }
   __syncthreads();
-  if (warp >= tok_per_block) return;
-  const int64_t t = t0 + warp;
-  if (t >= a.T) return;
-  const int epl = E >> 5;
-  const int S = E / a.G;
-
-  float s[8], c[8];
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    s[j] = 0.f;
-    c[j] = -FLT_MAX;
-    if (j < epl) {
-      const int e = j * 32 + lane;
-      const float lg = s_logit[warp][e];
-      s[j] = 1.0f / (1.0f + expf(-lg));
-      c[j] = s[j] + a.bias[e];
-    }
-  }
-
-  // group score: top-1 + top-2 choice score inside each S-lane segment
-  float gs_reg[8];
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    float m1 = c[j], m2 = -FLT_MAX;
-    for (int o = S >> 1; o >= 1; o >>= 1) {
-      const float b1 = __shfl_xor_sync(kFull, m1, o);
-      const float b2 = __shfl_xor_sync(kFull, m2, o);
-      const float n1 = fmaxf(m1, b1);
-      const float n2 = fmaxf(fminf(m1, b1), fmaxf(m2, b2));
-      m1 = n1;
-      m2 = n2;
-    }
-    gs_reg[j] = m1 + m2;
-  }
-  // lane g (< G) takes group g's score
-  float my_gs = -FLT_MAX;
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const float v = __shfl_sync(kFull, gs_reg[j], (lane * S) & 31);
-    if (lane < a.G && ((lane * S) >> 5) == j) my_gs = v;
-  }
-  // keep the best kg groups: (score desc, group asc)
-  uint32_t keep_mask = 0;
-  bool kept = false;
-  for (int r = 0; r < a.kg; ++r) {
-    const bool cand = lane < a.G && !kept;
-    float v = cand ? my_gs : -FLT_MAX;
-    int id = cand ? lane : (1 << 30);
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) {
-      const float ov = __shfl_xor_sync(kFull, v, o);
-      const int oi = __shfl_xor_sync(kFull, id, o);
-      if (ov > v || (ov == v && oi < id)) {
-        v = ov;
-        id = oi;
-      }
-    }
-    if (lane == id) kept = true;
-    keep_mask |= 1u << (id & 31);
-  }
-  // top-k experts of the kept groups: (choice score desc, expert asc)
-  uint32_t taken = 0;
-  int slot_e = 0;
-  float slot_s = 0.f;
-  for (int r = 0; r < a.k; ++r) {
-    float bv = -FLT_MAX;
-    int be = 1 << 30;
-    float bs = 0.f;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      if (j < epl) {
-        const int e = j * 32 + lane;
-        const bool el = ((keep_mask >> (e / S)) & 1u) && !((taken >> j) & 1u);
-        if (el && (c[j] > bv || (c[j] == bv && e < be))) {
-          bv = c[j];
-          be = e;
-          bs = s[j];
-        }
-      }
-    }
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) {
-      const float ov = __shfl_xor_sync(kFull, bv, o);
-      const int oe = __shfl_xor_sync(kFull, be, o);
-      const float os = __shfl_xor_sync(kFull, bs, o);
-      if (ov > bv || (ov == bv && oe < be)) {
-        bv = ov;
-        be = oe;
-        bs = os;
-      }
-    }
-    if ((be & 31) == lane) taken |= 1u << ((be >> 5) & 31);
-    if (lane == r) {
-      slot_e = be;
-      slot_s = bs;
-    }
-  }
-  // renormalise over the sigmoid scores in slot order, times the routed scale
-  double ssum = 0.0;
-  for (int r = 0; r < a.k; ++r) ssum += static_cast<double>(__shfl_sync(kFull, slot_s, r));
-  if (lane < a.k) {
-    a.idx[t * a.k + lane] = slot_e;
-    a.w[t * a.k + lane] =
-        static_cast<float>(static_cast<double>(a.alpha) * static_cast<double>(slot_s) / ssum);
+  if (e < a.k) {
+    double ssum = 0.0;
+    for (int r = 0; r < a.k; ++r) ssum += static_cast<double>(s_slot_s[r]);
+    a.idx[t * a.k + e] = s_slot_e[e];
+    a.w[t * a.k + e] =
+        static_cast<float>(static_cast<double>(a.alpha) * static_cast<double>(s_slot_s[e]) / ssum);
   }
 }
 
@@ -314,8 +296,7 @@ __device__ __forceinline__ void load8(const int32_t* __restrict__ idx, int64_t i
   }
 }
 
-__global__ void __launch_bounds__(256) permute_kernel(PermuteArgs a) {
-  const int e = blockIdx.x;
+__device__ __forceinline__ void permute_expert(const PermuteArgs& a, int e) {
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   const int warp = tid >> 5;
@@ -466,6 +447,41 @@ __global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ 
   reinterpret_cast<uint4*>(out + t * d)[c8] = o;
 }
 
+__global__ void __launch_bounds__(256) router_kernel(RouterArgs a) {
+  router_tile(a, blockIdx.x, blockIdx.y, blockIdx.z);
+}
+
+__global__ void __launch_bounds__(256) select_kernel(SelectArgs a) { select_token(a, blockIdx.x); }
+
+__global__ void __launch_bounds__(256) permute_kernel(PermuteArgs a) { permute_expert(a, blockIdx.x); }
+
+// Router partials, selection and permutation in one cooperative launch (all
+// blocks resident): grid-wide syncs separate the three steps, which removes
+// two launches from a decode-sized call.
+__global__ void __launch_bounds__(256) fused_route_kernel(RouterArgs ra, int ksplit, SelectArgs sa,
+                                                          PermuteArgs pa) {
+  cg::grid_group grid = cg::this_grid();
+  const int nbx = (ra.E + kRtExp - 1) / kRtExp;
+  const int nby = static_cast<int>((ra.T + kRtTok - 1) / kRtTok);
+  const int tiles = nbx * nby * ksplit;
+  // the block-wide syncs between iterations keep one item's shared-memory
+  // reads ahead of the next item's writes
+  for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
+    router_tile(ra, tile % nbx, (tile / nbx) % nby, tile / (nbx * nby));
+    __syncthreads();
+  }
+  grid.sync();
+  for (int64_t t = blockIdx.x; t < sa.T; t += gridDim.x) {
+    select_token(sa, t);
+    __syncthreads();
+  }
+  grid.sync();
+  for (int e = blockIdx.x; e < pa.E; e += gridDim.x) {
+    permute_expert(pa, e);
+    __syncthreads();
+  }
+}
+
 }  // namespace
 
 void launch_router(const RouterArgs& a, int ksplit, cudaStream_t s) {
@@ -474,13 +490,33 @@ void launch_router(const RouterArgs& a, int ksplit, cudaStream_t s) {
 }
 
 void launch_select(const SelectArgs& a, cudaStream_t s) {
-  // one token per block while split-K partials need reducing, else 8
-  const int tpb = a.ksplit > 1 ? 1 : kSelMaxTok;
-  select_kernel<<<static_cast<unsigned>((a.T + tpb - 1) / tpb), 256, 0, s>>>(a, tpb);
+  select_kernel<<<static_cast<unsigned>(a.T), 256, 0, s>>>(a);
 }
 
 void launch_router_split(const float* w, int32_t E, int32_t d, uint16_t* planes, cudaStream_t s) {
   router_split_kernel<<<512, 256, 0, s>>>(w, E, d, planes);
+}
+
+cudaError_t launch_fused_route(const RouterArgs& ra, int ksplit, const SelectArgs& sa,
+                               const PermuteArgs& pa, int num_sms, cudaStream_t s) {
+  static int per_sm = 0;
+  if (per_sm == 0 &&
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fused_route_kernel, 256, 0) !=
+          cudaSuccess)
+    return cudaErrorUnknown;
+  const int64_t tiles = static_cast<int64_t>((ra.E + kRtExp - 1) / kRtExp) *
+                        ((ra.T + kRtTok - 1) / kRtTok) * ksplit;
+  int64_t want = tiles;
+  if (sa.T > want) want = sa.T;
+  if (pa.E > want) want = pa.E;
+  const int64_t cap = static_cast<int64_t>(per_sm) * num_sms;
+  const int grid = static_cast<int>(want < cap ? want : cap);
+  RouterArgs a0 = ra;
+  SelectArgs a1 = sa;
+  PermuteArgs a2 = pa;
+  void* args[] = {&a0, &ksplit, &a1, &a2};
+  return cudaLaunchCooperativeKernel(reinterpret_cast<void*>(fused_route_kernel), dim3(grid),
+                                     dim3(256), args, 0, s);
 }
 
 void launch_permute(const PermuteArgs& a, cudaStream_t s) {

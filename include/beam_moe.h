@@ -228,7 +228,10 @@ beam_status_t beam_moe_check_status(void *workspace, void *stream);
  * [4] gather (only when T*topk > 4*E; smaller batches gather inside the
  * gate/up GEMM), [5] gate/up GEMM, [6] down GEMM, [7] combine (each after its
  * step).  Steps a call does not run record at the same point as the previous
- * one.  n == 0 switches it off.  Process-wide; not thread-safe. */
+ * one.  Below 256 tokens (at most 256 experts) the router, the selection and
+ * the permutation are one cooperative launch: [1], [2] and [3] are all
+ * recorded after it.  n == 0 switches it off.  Process-wide; not
+ * thread-safe. */
 beam_status_t beam_moe_set_stage_events(void *const *events, int32_t n);
 
 /* Test aid for the bounded waits: wait_limit_us bounds every device-side
@@ -238,8 +241,13 @@ beam_status_t beam_moe_set_stage_events(void *const *events, int32_t n);
  * BEAM_ERR_TIMEOUT without faulting.  Process-wide; not thread-safe. */
 beam_status_t beam_moe_set_debug(uint32_t wait_limit_us, int32_t withhold_first_load);
 
-/* Number of kernels a forward call of T tokens launches (for accounting). */
-int32_t beam_moe_kernels_per_forward(const beam_moe_config_t *cfg, int64_t T);
+/* Number of kernels one call of T tokens launches (for accounting):
+ * beam_moe_forward (and beam_moe_forward_noalloc) for weight_fmt
+ * BEAM_WEIGHTS_BF16, beam_moe_forward_nvfp4 for BEAM_WEIGHTS_NVFP4, and with
+ * routed != 0 beam_moe_forward_routed (BF16 only).  Returns 0 for an invalid
+ * configuration, T <= 0 or an unknown combination.  Host-only. */
+int32_t beam_moe_kernels_per_forward(const beam_moe_config_t *cfg, int64_t T, int32_t weight_fmt,
+                                     int32_t routed);
 
 const char *beam_status_string(beam_status_t s);
 

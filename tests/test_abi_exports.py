@@ -48,8 +48,15 @@ def test_host_only_queries(lib):
     assert lay["total"] == n and n % 256 == 0
     offs = sorted(v for k, v in lay.items() if k != "total")
     assert offs[0] == 0 and all(o % 256 == 0 for o in offs)
-    assert api.kernels_per_forward(beam, 32) == 6        # CUDA-core router, fused gather
-    assert api.kernels_per_forward(beam, 8192) == 8      # plane split, tensor router, gather
+    # routing+permute as one launch, gate/up (gathering), down, combine
+    assert api.kernels_per_forward(beam, 32) == 4
+    # plane split, tensor router, select, permute, gather, gate/up, down, combine
+    assert api.kernels_per_forward(beam, 8192) == 8
+    assert api.kernels_per_forward(beam, 32, routed=True) == 4       # permute .. combine
+    assert api.kernels_per_forward(beam, 8192, routed=True) == 5
+    assert api.kernels_per_forward(beam, 128, weight_fmt=api.NVFP4) == 5
+    assert api.kernels_per_forward(beam, 4096, weight_fmt=api.NVFP4) == 8
+    assert api.kernels_per_forward(beam, 32, weight_fmt=api.NVFP4, routed=True) == 0
     with pytest.raises(api.BeamError):
         api.workspace_size(beam.replace(n_groups=7), 32)
     lib.beam_status_string.restype = ctypes.c_char_p

@@ -187,3 +187,22 @@ def test_tensor_core_router_mid_sized_layer(T):
     rows = np.nonzero(~exempt_tokens(r))[0][:64]
     ref = oracle_out(cfg, t, r["idx"], r["w"], tokens=rows)
     check_out(out, ref, rows=rows)
+
+
+@pytest.mark.parametrize("E,G,kg,k", [(256, 128, 16, 8), (128, 64, 8, 8), (64, 2, 1, 6),
+                                      (96, 3, 2, 4), (256, 16, 4, 8), (32, 16, 3, 5)])
+def test_group_shapes(E, G, kg, k):
+    """Selection for group sizes from 2 to 32 experts and up to 128 groups,
+    alone on the oracle's logits and inside the fused decode-sized routing of
+    a forward call."""
+    cfg = CFG.replace(T=20, n_experts=E, n_groups=G, topk_groups=kg, topk=k, seed=E + G + k)
+    t = inputs.generate(cfg, "cuda")
+    lg, r = oracle_route(cfg, t)
+    idx, w = pkg.select(cfg, torch.from_numpy(lg).cuda(), t["corr_bias"])
+    check_routing(cfg, host(idx), host(w), r, w_rtol=W_RTOL_SELECT)
+    ws = pkg.Workspace(cfg, cfg.T)
+    pkg.forward(cfg, t["hidden"], t["router_w"], t["corr_bias"], t["w_gate"], t["w_up"],
+                t["w_down"], ws=ws)
+    assert pkg.check_status(ws) == 0
+    check_routing(cfg, host(ws.view("topk_idx", torch.int32, (cfg.T, k))),
+                  host(ws.view("topk_w", torch.float32, (cfg.T, k))), r)
