@@ -63,7 +63,12 @@ constexpr int BM = 128;
 constexpr int BK = 64;
 constexpr int UMMA_K = 16;
 // warps: weight producer, MMA issuer, token producer, then the epilogue warps
-constexpr int threads_for(int nt) { return 96 + 32 * (nt >= 256 ? 8 : 4); }
+// (four per TMEM lane quarter for the single-buffered 256-token gate/up tile,
+// whose epilogue the MMA waits for)
+constexpr int epi_warps_for(int nt, int mode) {
+  return nt >= 256 ? (mode == kModeGateUp ? 16 : 8) : 4;
+}
+constexpr int threads_for(int nt, int mode) { return 96 + 32 * epi_warps_for(nt, mode); }
 constexpr int kMaxE = 256;
 constexpr uint32_t kTileBudget = 216 * 1024;
 
@@ -86,7 +91,7 @@ struct Cfg {
   static constexpr int SA = SA_RAW > 16 ? 16 : SA_RAW;
   static constexpr int SB = SA;
   static constexpr uint32_t B_RING = SA * A_STAGE;               // offset of the token ring
-  static constexpr int EPI_WARPS = NT >= 256 ? 8 : 4;
+  static constexpr int EPI_WARPS = epi_warps_for(NT, MODE);
   static constexpr int THREADS = 96 + 32 * EPI_WARPS;
   static constexpr uint32_t ACC_COLS = NUM_A * NT;
   static constexpr int ACC_BUFS = 2 * ACC_COLS <= 512 ? 2 : 1;
@@ -108,7 +113,7 @@ __device__ __forceinline__ uint16_t f32_to_bf16(float v) {
 }
 
 template <int NT, int MODE>
-__global__ void __launch_bounds__(threads_for(NT), 1)
+__global__ void __launch_bounds__(threads_for(NT, MODE), 1)
     expert_gemm_kernel(const __grid_constant__ CUtensorMap tm_a0,
                        const __grid_constant__ CUtensorMap tm_a1,
                        const __grid_constant__ CUtensorMap tm_b, const GemmArgs p) {
@@ -362,7 +367,8 @@ __global__ void __launch_bounds__(threads_for(NT), 1)
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int m = q * 32 + lane;
-    // with 8 epilogue warps, warps 3-6 take the first half of the columns
+    // with more than 4 epilogue warps, warps 3-6 take the first columns,
+    // warps 7-10 the next ones, and so on
     constexpr int COLS_PER_WARP = NT / (C::EPI_WARPS / 4);
     const int col_begin = ((warp - 3) >> 2) * COLS_PER_WARP;
     int acc = 0;
@@ -387,7 +393,9 @@ __global__ void __launch_bounds__(threads_for(NT), 1)
             if (c0 + j < ti.nvalid) {
               const float g = __uint_as_float(ra[j]);
               const float u = __uint_as_float(rb[j]);
-              const float h = g / (1.0f + expf(-g)) * u;
+              // fast exp and divide: relative error near 1e-6, far below the
+              // BF16 rounding of h that follows
+              const float h = __fdividef(g, 1.0f + __expf(-g)) * u;
               p.h_out[static_cast<int64_t>(ti.row0 + c0 + j) * p.out_ld + col] = f32_to_bf16(h);
             }
           }
