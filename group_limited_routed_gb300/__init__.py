@@ -14,7 +14,8 @@ def __getattr__(name):
     if name in ("route", "select", "forward", "forward_routed", "workspace_size", "Workspace",
                 "check_status", "BeamError", "library_path", "lib", "set_stage_events",
                 "set_debug", "layout", "kernels_per_forward", "EXPORTS", "forward_noalloc",
-                "forward_nvfp4", "pack_scales", "Fp4Weight", "NVFP4"):
+                "forward_nvfp4", "pack_scales", "Fp4Weight", "NVFP4", "ep_dispatch",
+                "ep_experts", "ep_combine", "EpWorkspace"):
         from . import api
         return getattr(api, name)
     raise AttributeError(name)

@@ -32,7 +32,8 @@ EXPORTS = ("beam_moe_workspace_size", "beam_moe_workspace_layout", "beam_moe_rou
            "beam_moe_select", "beam_moe_forward", "beam_moe_forward_routed",
            "beam_moe_forward_noalloc", "beam_moe_forward_nvfp4", "beam_moe_nvfp4_pack_scales",
            "beam_moe_check_status", "beam_moe_set_stage_events", "beam_moe_set_debug",
-           "beam_moe_kernels_per_forward", "beam_status_string")
+           "beam_moe_kernels_per_forward", "beam_status_string", "beam_moe_ep_dispatch",
+           "beam_moe_ep_workspace_size", "beam_moe_ep_experts", "beam_moe_ep_combine")
 
 
 class BeamError(RuntimeError):
@@ -95,6 +96,16 @@ def lib():
         L.beam_moe_set_debug.restype = _ST
         L.beam_moe_kernels_per_forward.argtypes = [cfgp, _I64, ctypes.c_int32, ctypes.c_int32]
         L.beam_moe_kernels_per_forward.restype = ctypes.c_int32
+        L.beam_moe_ep_dispatch.argtypes = [cfgp, _P, _P, _P, _I64, ctypes.c_int32, _P, _P, _P, _P,
+                                           _P, _SZ, _P]
+        L.beam_moe_ep_dispatch.restype = _ST
+        L.beam_moe_ep_workspace_size.argtypes = [cfgp, ctypes.c_int32, _I64]
+        L.beam_moe_ep_workspace_size.restype = _SZ
+        L.beam_moe_ep_experts.argtypes = [cfgp, ctypes.c_int32, ctypes.c_int32, _P, _P, _P, _P, _P,
+                                          _P, _P, _I64, _P, _SZ, _P]
+        L.beam_moe_ep_experts.restype = _ST
+        L.beam_moe_ep_combine.argtypes = [cfgp, _P, _I64, _P, _P, _SZ, _P]
+        L.beam_moe_ep_combine.restype = _ST
         L.beam_status_string.argtypes = [_ST]
         L.beam_status_string.restype = ctypes.c_char_p
         _lib = L
@@ -341,3 +352,82 @@ def kernels_per_forward(cfg, T: int, weight_fmt: int = 0, routed: bool = False) 
     c = _cfg(cfg)
     return int(lib().beam_moe_kernels_per_forward(ctypes.byref(c), int(T), int(weight_fmt),
                                                   int(bool(routed))))
+
+
+# ------------------------------------------------------------ expert parallelism
+def ep_dispatch(cfg, hidden, router_w, corr_bias, n_ranks: int, ws: Workspace | None = None,
+                stream=None):
+    """Route this rank's tokens and pack one row per (token, slot) pair in
+    owner order -> (send_x [T*k, d] bf16, send_expert [T*k] int32,
+    send_w [T*k] f32, send_counts [n_ranks] int32, ws).  Keep ``ws`` for
+    :func:`ep_combine`."""
+    T = hidden.shape[0]
+    dev = hidden.device
+    ws = _ws(cfg, T, ws, dev)
+    TK = T * cfg.topk
+    send_x = torch.empty(TK, cfg.d, dtype=torch.bfloat16, device=dev)
+    send_e = torch.empty(TK, dtype=torch.int32, device=dev)
+    send_w = torch.empty(TK, dtype=torch.float32, device=dev)
+    counts = torch.empty(n_ranks, dtype=torch.int32, device=dev)
+    c = _cfg(cfg)
+    _check(lib().beam_moe_ep_dispatch(ctypes.byref(c), _dev(hidden, torch.bfloat16, "hidden"),
+                                      _dev(router_w, torch.float32, "router_w"),
+                                      _dev(corr_bias, torch.float32, "corr_bias"), T,
+                                      int(n_ranks), send_x.data_ptr(), send_e.data_ptr(),
+                                      send_w.data_ptr(), counts.data_ptr(), ws.ptr, ws.nbytes,
+                                      _stream(stream)), "beam_moe_ep_dispatch")
+    return send_x, send_e, send_w, counts, ws
+
+
+class EpWorkspace:
+    """Device workspace of :func:`ep_experts` for up to M_max received rows."""
+
+    def __init__(self, cfg, n_ranks: int, M_max: int, device=None):
+        c = _cfg(cfg)
+        self.nbytes = int(lib().beam_moe_ep_workspace_size(ctypes.byref(c), int(n_ranks),
+                                                           int(M_max)))
+        if self.nbytes == 0:
+            raise BeamError(1, "beam_moe_ep_workspace_size")
+        self.M_max = int(M_max)
+        self.buf = torch.zeros(self.nbytes, dtype=torch.uint8,
+                               device=device if device is not None else torch.device("cuda"))
+
+    @property
+    def ptr(self) -> int:
+        return self.buf.data_ptr()
+
+
+def ep_experts(cfg, n_ranks: int, rank: int, x_recv, expert_recv, w_recv, w_gate, w_up, w_down,
+               ws: EpWorkspace | None = None, out=None, stream=None):
+    """This rank's experts on its received rows -> y_recv [M, d] f32 (weighted)."""
+    M = x_recv.shape[0]
+    dev = x_recv.device
+    if ws is None or ws.M_max < M:
+        ws = EpWorkspace(cfg, n_ranks, max(M, 1), dev)
+    y = torch.empty(M, cfg.d, dtype=torch.float32, device=dev) if out is None else out
+    if M == 0:
+        return y
+    c = _cfg(cfg)
+    _check(lib().beam_moe_ep_experts(ctypes.byref(c), int(n_ranks), int(rank),
+                                     _dev(x_recv, torch.bfloat16, "x_recv"),
+                                     _dev(expert_recv, torch.int32, "expert_recv"),
+                                     _dev(w_recv, torch.float32, "w_recv"),
+                                     _dev(w_gate, torch.bfloat16, "w_gate"),
+                                     _dev(w_up, torch.bfloat16, "w_up"),
+                                     _dev(w_down, torch.bfloat16, "w_down"),
+                                     _dev(y, torch.float32, "y_recv"), M, ws.ptr, ws.nbytes,
+                                     _stream(stream)), "beam_moe_ep_experts")
+    return y
+
+
+def ep_combine(cfg, y_back, T: int, ws: Workspace, out=None, stream=None):
+    """The owner's combine of the returned rows -> out [T, d] bf16."""
+    dev = ws.buf.device
+    o = torch.empty(T, cfg.d, dtype=torch.bfloat16, device=dev) if out is None else out
+    if T == 0:
+        return o
+    c = _cfg(cfg)
+    _check(lib().beam_moe_ep_combine(ctypes.byref(c), _dev(y_back, torch.float32, "y_back"), T,
+                                     o.data_ptr(), ws.ptr, ws.nbytes, _stream(stream)),
+           "beam_moe_ep_combine")
+    return o

@@ -239,6 +239,7 @@ beam::PermuteArgs permute_args(const beam_moe_config_t& c, const int32_t* idx, c
   pa.pair_row = at<int32_t>(ws, L.pair_row);
   pa.perm_w = at<float>(ws, L.perm_w);
   pa.status = at<uint32_t>(ws, L.status);
+  pa.id_base = 0;
   return pa;
 }
 
@@ -303,18 +304,22 @@ beam_status_t run_route(const beam_moe_config_t& c, const void* hidden, const fl
   return cuda_status(cudaGetLastError());
 }
 
-// permute + gather + expert GEMMs + combine
+// permute + gather + expert GEMMs + combine.  With y_pairs given, the down
+// GEMM writes each pair's weighted FP32 row there (pair order) and there is
+// no combine; idx then holds ids from id_base on.
 beam_status_t run_experts(const beam_moe_config_t& c, const void* hidden, const int32_t* idx,
                           const float* w, const void* w_gate, const void* w_up,
                           const void* w_down, void* out, int64_t T, void* ws, const Layout& L,
-                          const DevInfo& dev, cudaStream_t s, bool permuted = false) {
+                          const DevInfo& dev, cudaStream_t s, bool permuted = false,
+                          float* y_pairs = nullptr, int32_t id_base = 0) {
   const int64_t TK = T * c.topk;
   const int64_t rows = std::max<int64_t>(TK, kMinRows);
   const int nt_gu = gateup_tile(c, TK);
   const int nt_dn = down_tile(c, TK);
   uint32_t* status = at<uint32_t>(ws, L.status);
 
-  const beam::PermuteArgs pa = permute_args(c, idx, w, T, ws, L);
+  beam::PermuteArgs pa = permute_args(c, idx, w, T, ws, L);
+  pa.id_base = id_base;
   if (!permuted) {
     beam::launch_permute(pa, s);
     record(3, s);
@@ -372,7 +377,8 @@ beam_status_t run_experts(const beam_moe_config_t& c, const void* hidden, const 
 
   ga.withhold_first_load = 0;
   ga.h_out = nullptr;
-  ga.f32_out = y;
+  ga.f32_out = y_pairs ? y_pairs : y;
+  ga.out_rows = y_pairs ? pa.perm_src : nullptr;
   ga.out_ld = c.d;
   ga.rows_per_expert = c.d;
   ga.m_blocks = c.d / 128;
@@ -383,7 +389,7 @@ beam_status_t run_experts(const beam_moe_config_t& c, const void* hidden, const 
   if (err != cudaSuccess) return BEAM_ERR_CUDA;
   record(6, s);
 
-  beam::launch_combine(y, pa.pair_row, T, c.topk, c.d, static_cast<uint16_t*>(out), s);
+  if (!y_pairs) beam::launch_combine(y, pa.pair_row, T, c.topk, c.d, static_cast<uint16_t*>(out), s);
   record(7, s);
   return cuda_status(cudaGetLastError());
 }
@@ -679,6 +685,111 @@ beam_status_t beam_moe_forward_nvfp4(const beam_moe_config_t* cfg, const void* h
   if (st != BEAM_OK) return st;
   return run_experts_nvfp4(*cfg, hidden, idx, w, *gate, *up, *down, out, T, workspace, L, dev, s,
                            permuted);
+}
+
+// ------------------------------------------------------- expert parallelism
+namespace {
+
+bool valid_ep(const beam_moe_config_t* c, int32_t n_ranks) {
+  return valid_cfg(c) && n_ranks >= 1 && n_ranks <= c->n_experts && c->n_experts % n_ranks == 0;
+}
+
+// the expert computation of one rank: its E / n_ranks experts, one row per
+// received (token, slot) pair
+beam_moe_config_t local_cfg(const beam_moe_config_t& c, int32_t n_ranks) {
+  beam_moe_config_t l = c;
+  l.n_experts = c.n_experts / n_ranks;
+  l.n_groups = 1;
+  l.topk_groups = 1;
+  l.topk = 1;
+  return l;
+}
+
+}  // namespace
+
+beam_status_t beam_moe_ep_dispatch(const beam_moe_config_t* cfg, const void* hidden,
+                                   const float* router_w, const float* corr_bias, int64_t T,
+                                   int32_t n_ranks, void* send_x, int32_t* send_expert,
+                                   float* send_w, int32_t* send_counts, void* workspace,
+                                   size_t ws_bytes, void* stream) {
+  if (!valid_ep(cfg, n_ranks) || !aligned16(send_counts)) return BEAM_ERR_INVALID_ARG;
+  Layout L;
+  DevInfo dev;
+  bool empty = false;
+  beam_status_t st = common_checks(cfg, T, workspace, ws_bytes, &L, &dev, &empty);
+  if (st != BEAM_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (empty)  // a rank without tokens still reports its (zero) counts
+    return cuda_status(cudaMemsetAsync(send_counts, 0, sizeof(int32_t) * n_ranks, s));
+  if (!aligned16(hidden) || !aligned16(router_w) || !aligned16(corr_bias) || !aligned16(send_x) ||
+      !aligned16(send_expert) || !aligned16(send_w))
+    return BEAM_ERR_INVALID_ARG;
+  if (!encoder()) return BEAM_ERR_CUDA;
+  record(0, s);
+  int32_t* idx = at<int32_t>(workspace, L.idx);
+  float* w = at<float>(workspace, L.w);
+  bool permuted = false;
+  st = run_route(*cfg, hidden, router_w, corr_bias, T, idx, w, at<float>(workspace, L.logits),
+                 workspace, L, dev, s, &permuted);
+  if (st != BEAM_OK) return st;
+  const beam::PermuteArgs pa = permute_args(*cfg, idx, w, T, workspace, L);
+  if (!permuted) beam::launch_permute(pa, s);
+  record(3, s);
+  const int64_t TK = T * cfg->topk;
+  beam::launch_gather(static_cast<const uint16_t*>(hidden), pa.perm_src, pa.offsets + cfg->n_experts,
+                      TK, cfg->topk, cfg->d, static_cast<uint16_t*>(send_x), s);
+  beam::launch_ep_pack(idx, pa.perm_src, pa.perm_w, pa.offsets, TK, cfg->n_experts, n_ranks,
+                       send_expert, send_w, send_counts, s);
+  record(4, s);
+  return cuda_status(cudaGetLastError());
+}
+
+size_t beam_moe_ep_workspace_size(const beam_moe_config_t* cfg, int32_t n_ranks, int64_t M_max) {
+  if (!valid_ep(cfg, n_ranks) || M_max < 0 || M_max > (int64_t(1) << 31) / 64) return 0;
+  return make_layout(local_cfg(*cfg, n_ranks), std::max<int64_t>(M_max, 1)).total;
+}
+
+beam_status_t beam_moe_ep_experts(const beam_moe_config_t* cfg, int32_t n_ranks, int32_t rank,
+                                  const void* x_recv, const int32_t* expert_recv,
+                                  const float* w_recv, const void* w_gate, const void* w_up,
+                                  const void* w_down, float* y_recv, int64_t M, void* workspace,
+                                  size_t ws_bytes, void* stream) {
+  if (!valid_ep(cfg, n_ranks) || rank < 0 || rank >= n_ranks || M < 0 ||
+      M > (int64_t(1) << 31) / 64)
+    return BEAM_ERR_INVALID_ARG;
+  if (M == 0) return BEAM_OK;
+  const beam_moe_config_t lc = local_cfg(*cfg, n_ranks);
+  if (!aligned16(workspace) || !aligned16(x_recv) || !aligned16(expert_recv) ||
+      !aligned16(w_recv) || !aligned16(w_gate) || !aligned16(w_up) || !aligned16(w_down) ||
+      !aligned16(y_recv))
+    return BEAM_ERR_INVALID_ARG;
+  const Layout L = make_layout(lc, M);
+  if (ws_bytes < L.total) return BEAM_ERR_WORKSPACE;
+  DevInfo dev;
+  if (!device_info(&dev)) return BEAM_ERR_CUDA;
+  if (!dev.supported) return BEAM_ERR_UNSUPPORTED;
+  if (!encoder()) return BEAM_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  record(0, s);
+  record(1, s);
+  record(2, s);
+  return run_experts(lc, x_recv, expert_recv, w_recv, w_gate, w_up, w_down, nullptr, M, workspace,
+                     L, dev, s, false, y_recv, rank * lc.n_experts);
+}
+
+beam_status_t beam_moe_ep_combine(const beam_moe_config_t* cfg, const float* y_back, int64_t T,
+                                  void* out, void* workspace, size_t ws_bytes, void* stream) {
+  Layout L;
+  DevInfo dev;
+  bool empty = false;
+  beam_status_t st = common_checks(cfg, T, workspace, ws_bytes, &L, &dev, &empty);
+  if (st != BEAM_OK || empty) return st;
+  if (!aligned16(y_back) || !aligned16(out)) return BEAM_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  beam::launch_combine(y_back, at<int32_t>(workspace, L.pair_row), T, cfg->topk, cfg->d,
+                       static_cast<uint16_t*>(out), s);
+  record(7, s);
+  return cuda_status(cudaGetLastError());
 }
 
 beam_status_t beam_moe_check_status(void* workspace, void* stream) {

@@ -48,11 +48,17 @@ struct PermuteArgs {
   int32_t* pair_row;       // [TK]
   float* perm_w;           // [TK]
   uint32_t* status;
+  int32_t id_base;         // idx holds expert ids id_base .. id_base + E - 1
 };
 
 void launch_router(const RouterArgs& a, int ksplit, cudaStream_t s);
 void launch_select(const SelectArgs& a, cudaStream_t s);
 void launch_permute(const PermuteArgs& a, cudaStream_t s);
+// expert-parallel dispatch metadata: per packed row its expert and weight,
+// and the rows bound for each of n_ranks owners
+void launch_ep_pack(const int32_t* idx, const int32_t* perm_src, const float* perm_w,
+                    const int32_t* offsets, int64_t TK, int32_t E, int32_t n_ranks,
+                    int32_t* send_expert, float* send_w, int32_t* send_counts, cudaStream_t s);
 // router partials + selection + permutation in one cooperative launch
 cudaError_t launch_fused_route(const RouterArgs& ra, int ksplit, const SelectArgs& sa,
                                const PermuteArgs& pa, int num_sms, cudaStream_t s);
@@ -73,6 +79,7 @@ struct GemmArgs {
   const float* perm_w;     // [rows] routing weight per row (down)
   uint16_t* h_out;         // gate/up: h [rows, F] BF16
   float* f32_out;          // down: y [rows, d] FP32
+  const int32_t* out_rows; // down: output row of each permuted row (nullptr: the same row)
   int32_t out_ld;          // elements per output row
   int32_t E;               // experts in the tile list
   int32_t rows_per_expert; // weight rows of one expert (A operand)

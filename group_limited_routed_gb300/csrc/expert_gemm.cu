@@ -405,7 +405,8 @@ __global__ void __launch_bounds__(threads_for(NT, MODE), 1)
           for (int j = 0; j < 16; ++j) {
             if (c0 + j < ti.nvalid) {
               const int row = ti.row0 + c0 + j;
-              p.f32_out[static_cast<int64_t>(row) * p.out_ld + col] =
+              const int orow = p.out_rows ? p.out_rows[row] : row;
+              p.f32_out[static_cast<int64_t>(orow) * p.out_ld + col] =
                   __uint_as_float(ra[j]) * p.perm_w[row];
             }
           }

@@ -311,6 +311,8 @@ __device__ __forceinline__ void permute_expert(const PermuteArgs& a, int e) {
     int v[kPermPer];
     load8(a.idx, i0, a.TK, v);
 #pragma unroll
+    for (int j = 0; j < kPermPer; ++j) v[j] -= a.id_base;
+#pragma unroll
     for (int j = 0; j < kPermPer; ++j) {
       if (i0 + j >= a.TK) break;
       if (static_cast<unsigned>(v[j]) >= static_cast<unsigned>(a.E)) {
@@ -355,6 +357,8 @@ __device__ __forceinline__ void permute_expert(const PermuteArgs& a, int e) {
     int v[kPermPer];
     if (i0 < a.TK) {
       load8(a.idx, i0, a.TK, v);
+#pragma unroll
+      for (int j = 0; j < kPermPer; ++j) v[j] -= a.id_base;
     } else {
 #pragma unroll
       for (int j = 0; j < kPermPer; ++j) v[j] = -1;
@@ -447,6 +451,29 @@ __global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ 
   reinterpret_cast<uint4*>(out + t * d)[c8] = o;
 }
 
+// ------------------------------------------------------- expert-parallel pack
+// Packed row r (expert order, hence grouped by owning rank) carries its
+// expert and its routing weight; block 0 also counts the rows per owner.
+__global__ void __launch_bounds__(256) ep_pack_kernel(const int32_t* __restrict__ idx,
+                                                      const int32_t* __restrict__ perm_src,
+                                                      const float* __restrict__ perm_w,
+                                                      const int32_t* __restrict__ offsets,
+                                                      int64_t TK, int32_t E, int32_t n_ranks,
+                                                      int32_t* __restrict__ send_expert,
+                                                      float* __restrict__ send_w,
+                                                      int32_t* __restrict__ send_counts) {
+  const int64_t r = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (r < TK) {
+    send_expert[r] = idx[perm_src[r]];
+    send_w[r] = perm_w[r];
+  }
+  if (blockIdx.x == 0) {
+    const int per = E / n_ranks;
+    for (int q = threadIdx.x; q < n_ranks; q += blockDim.x)
+      send_counts[q] = offsets[(q + 1) * per] - offsets[q * per];
+  }
+}
+
 __global__ void __launch_bounds__(256) router_kernel(RouterArgs a) {
   router_tile(a, blockIdx.x, blockIdx.y, blockIdx.z);
 }
@@ -517,6 +544,14 @@ cudaError_t launch_fused_route(const RouterArgs& ra, int ksplit, const SelectArg
   void* args[] = {&a0, &ksplit, &a1, &a2};
   return cudaLaunchCooperativeKernel(reinterpret_cast<void*>(fused_route_kernel), dim3(grid),
                                      dim3(256), args, 0, s);
+}
+
+void launch_ep_pack(const int32_t* idx, const int32_t* perm_src, const float* perm_w,
+                    const int32_t* offsets, int64_t TK, int32_t E, int32_t n_ranks,
+                    int32_t* send_expert, float* send_w, int32_t* send_counts, cudaStream_t s) {
+  const int64_t blocks = TK > 0 ? (TK + 255) / 256 : 1;
+  ep_pack_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+      idx, perm_src, perm_w, offsets, TK, E, n_ranks, send_expert, send_w, send_counts);
 }
 
 void launch_permute(const PermuteArgs& a, cudaStream_t s) {

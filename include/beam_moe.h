@@ -218,6 +218,65 @@ beam_status_t beam_moe_forward_nvfp4(const beam_moe_config_t *cfg, const void *h
                                      const beam_fp4_weight_t *down, void *out, int64_t T,
                                      void *workspace, size_t ws_bytes, void *stream);
 
+/* ---------------------------------------------------- expert parallelism
+ * Expert parallelism over n_ranks ranks ("SGLang 原生支持 Reflection 的 Beam
+ * 并驱动其生产 API", section "Fusion Optimizations", the MegaMoE item and the
+ * token-ownership figure after it: the experts are partitioned over the
+ * ranks, a token's rows travel to the ranks that own its experts with
+ * explicit expert ids and routing weights, every rank takes part even
+ * without local tokens, and the complete outputs return to the token's
+ * owning rank).  Rank q owns experts [q*E/n_ranks, (q+1)*E/n_ranks)
+ * (n_ranks divides E).  One forward on n_ranks ranks is:
+ *   1. beam_moe_ep_dispatch on every rank for its own tokens;
+ *   2. an all-to-all of the packed rows, experts and weights (send_counts
+ *      gives the split; the library performs no communication);
+ *   3. beam_moe_ep_experts on every rank for the rows it received;
+ *   4. the reverse all-to-all of the FP32 output rows, which come back in
+ *      the order they were sent;
+ *   5. beam_moe_ep_combine on every rank.
+ * The result equals beam_moe_forward on the same tokens: the same
+ * per-row arithmetic, the same slot-order FP32 sum and one BF16 rounding. */
+
+/* Steps 1-2 of the layer on the tokens' owner, then the packing: one row per
+ * (token, slot) pair, ordered by (expert, token, slot), which groups the rows
+ * by owning rank.
+ *   send_x      [T*topk, d] BF16  the pair's hidden row
+ *   send_expert [T*topk]    int32 the pair's (global) expert
+ *   send_w      [T*topk]    FP32  the pair's routing weight (alpha included)
+ *   send_counts [n_ranks]   int32 rows bound for each rank, in rank order
+ * All device buffers, caller-owned, 16-byte aligned.  The workspace is the
+ * one beam_moe_workspace_size(cfg, T, BEAM_WEIGHTS_BF16) sizes; it must be
+ * passed unchanged to beam_moe_ep_combine for the same T.  T == 0 writes
+ * zero counts.  Asynchronous on `stream`. */
+beam_status_t beam_moe_ep_dispatch(const beam_moe_config_t *cfg, const void *hidden,
+                                   const float *router_w, const float *corr_bias, int64_t T,
+                                   int32_t n_ranks, void *send_x, int32_t *send_expert,
+                                   float *send_w, int32_t *send_counts, void *workspace,
+                                   size_t ws_bytes, void *stream);
+
+/* Workspace bytes of beam_moe_ep_experts for up to M_max received rows;
+ * 0 for an invalid configuration. */
+size_t beam_moe_ep_workspace_size(const beam_moe_config_t *cfg, int32_t n_ranks, int64_t M_max);
+
+/* Steps 3-4 of the layer on rank `rank` for M received rows:
+ *   y_recv[i] = w_recv[i] * down(h), h = bf16(silu(x W_g^T) * (x W_u^T)),
+ * with the expert expert_recv[i], x = x_recv[i] (BF16 [M, d]), in FP32
+ * ([M, d], row i for received row i).  w_gate / w_up [E/n_ranks, d_ff, d]
+ * and w_down [E/n_ranks, d, d_ff] hold this rank's experts only.  An
+ * expert id outside the rank's range latches BEAM_ERR_DEVICE_CHECK and its
+ * row is not written.  M == 0 launches nothing. */
+beam_status_t beam_moe_ep_experts(const beam_moe_config_t *cfg, int32_t n_ranks, int32_t rank,
+                                  const void *x_recv, const int32_t *expert_recv,
+                                  const float *w_recv, const void *w_gate, const void *w_up,
+                                  const void *w_down, float *y_recv, int64_t M, void *workspace,
+                                  size_t ws_bytes, void *stream);
+
+/* The owner's combine: out[t] = bf16(sum over slots, in slot order, of the
+ * returned FP32 rows), y_back [T*topk, d] in the order beam_moe_ep_dispatch
+ * packed them.  `workspace` is the dispatch call's, unchanged. */
+beam_status_t beam_moe_ep_combine(const beam_moe_config_t *cfg, const float *y_back, int64_t T,
+                                  void *out, void *workspace, size_t ws_bytes, void *stream);
+
 /* Synchronises `stream`, returns the workspace's latched status and clears
  * it.  The only entry point that waits for the device. */
 beam_status_t beam_moe_check_status(void *workspace, void *stream);

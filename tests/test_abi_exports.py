@@ -61,3 +61,17 @@ def test_host_only_queries(lib):
         api.workspace_size(beam.replace(n_groups=7), 32)
     lib.beam_status_string.restype = ctypes.c_char_p
     assert lib.beam_status_string(5) == b"device-side wait timed out"
+
+
+def test_ep_workspace_query(lib):
+    from group_limited_routed_gb300 import api
+    from group_limited_routed_gb300.inputs import CONFIGS
+    beam = CONFIGS["decode"]
+    c = api.CConfig.of(beam)
+    size = lib.beam_moe_ep_workspace_size
+    size.restype = ctypes.c_size_t
+    size.argtypes = [ctypes.POINTER(api.CConfig), ctypes.c_int32, ctypes.c_int64]
+    assert size(ctypes.byref(c), 8, 256) % 256 == 0 and size(ctypes.byref(c), 8, 256) > 0
+    assert size(ctypes.byref(c), 8, 1024) >= size(ctypes.byref(c), 8, 256)
+    assert size(ctypes.byref(c), 3, 256) == 0        # 3 does not divide 256 experts
+    assert size(ctypes.byref(c), 512, 256) == 0      # more ranks than experts
