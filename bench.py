@@ -43,7 +43,7 @@ UNIT = "tokens/s"
 STAGES = ["router", "select", "permute", "gather", "gate_up", "down", "combine"]
 DOMINANT = "gate_up"
 DOMINANT_SRC = [os.path.join(ROOT, "group_limited_routed_gb300", "csrc", f)
-                for f in ("expert_gemm.cu", "ptx.cuh", "common.cuh")]
+                for f in ("expert_gemm.cu", "expert_gemm.cuh", "gemm_common.cuh", "ptx.cuh")]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 
 

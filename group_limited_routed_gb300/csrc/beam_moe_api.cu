@@ -12,6 +12,7 @@
 
 #include "../../include/beam_moe.h"
 #include "common.cuh"
+#include "expert_gemm.cuh"
 
 namespace {
 

@@ -67,37 +67,6 @@ void launch_gather(const uint16_t* x, const int32_t* perm_src, const int32_t* n_
 void launch_combine(const float* y, const int32_t* pair_row, int64_t T, int32_t k, int32_t d,
                     uint16_t* out, cudaStream_t s);
 
-// ---------------------------------------------------------------- grouped GEMMs
-constexpr int kModeDown = 0;    // y = w * (h W_d^T), FP32 out
-constexpr int kModeGateUp = 1;  // h = bf16(silu(x W_g^T) * (x W_u^T))
-
-struct GemmArgs {
-  const int32_t* counts;   // [E] rows per expert
-  const int32_t* perm_src; // [rows] permuted row -> token * topk + slot (gate/up gather)
-  int32_t topk;
-  const int32_t* offsets;  // [E+1] first row of each expert in the token operand
-  const float* perm_w;     // [rows] routing weight per row (down)
-  uint16_t* h_out;         // gate/up: h [rows, F] BF16
-  float* f32_out;          // down: y [rows, d] FP32
-  const int32_t* out_rows; // down: output row of each permuted row (nullptr: the same row)
-  int32_t out_ld;          // elements per output row
-  int32_t E;               // experts in the tile list
-  int32_t rows_per_expert; // weight rows of one expert (A operand)
-  int32_t m_blocks;        // rows_per_expert / 128
-  int32_t k_blocks;        // A's K / 64
-  int32_t b_k_blocks;      // token operand's K / 64 (== k_blocks)
-  int32_t weight_evict_first;
-  uint32_t* status;
-  uint64_t wait_limit_ns;
-  int32_t withhold_first_load;
-};
-
-// Persistent grouped GEMM; `nt` is the token-block width (gate/up 16 | 128,
-// down 16 | 256).  Tensor maps are encoded by the caller.
-cudaError_t launch_grouped_gemm(int mode, int nt, const CUtensorMap& a0, const CUtensorMap& a1,
-                                const CUtensorMap& b, const GemmArgs& a, int grid,
-                                cudaStream_t s);
-
 // W_r [E, d] FP32 -> planes [E, 3d] BF16 (hi | mid | lo, W = hi + mid + lo to
 // within 2^-24 relative).
 void launch_router_split(const float* w, int32_t E, int32_t d, uint16_t* planes, cudaStream_t s);

@@ -46,6 +46,7 @@
 #include <cstdint>
 
 #include "common.cuh"
+#include "expert_gemm.cuh"
 #include "gemm_common.cuh"
 #include "ptx.cuh"
 

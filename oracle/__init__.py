@@ -65,6 +65,10 @@ def _load():
             getattr(lib, name).restype = ctypes.c_uint8
         lib.oracle_bf16_round.argtypes = [ctypes.c_float]
         lib.oracle_bf16_round.restype = ctypes.c_uint16
+        lib.oracle_bf16_round_double.argtypes = [ctypes.c_double]
+        lib.oracle_bf16_round_double.restype = ctypes.c_uint16
+        lib.oracle_boundary.argtypes = [_P, _P, _P, _P, _I64, _I32, ctypes.c_double,
+                                        ctypes.c_float, ctypes.c_float, _P, _P]
         lib.oracle_nvfp4_quantize.argtypes = [_P, _I64, _P, _P]
         lib.oracle_num_threads.restype = ctypes.c_int
         lib.oracle_set_threads.argtypes = [ctypes.c_int]
@@ -110,6 +114,41 @@ def e4m3_encode(v: float) -> int:
 
 def bf16_round(v: float) -> int:
     return int(_load().oracle_bf16_round(v))
+
+
+def bf16_round_double(v: float) -> int:
+    """Nearest BF16 of a double (one rounding, ties to even)."""
+    return int(_load().oracle_bf16_round_double(v))
+
+
+def residual_coefficients(n: int) -> tuple[np.float32, np.float32]:
+    """(c_h, c_x) of the n-th depth-scaled residual add: FP32 roundings of
+    sqrt((n-1)/n) and 1/sqrt(n) ("vLLM 实现 Reflection Beam 501B MoE 模型 Day 0
+    支持", section "MoE and residual stream")."""
+    if n < 1:
+        raise ValueError("the residual adds are numbered from 1")
+    return np.float32(np.sqrt((n - 1) / n)), np.float32(1.0 / np.sqrt(n))
+
+
+def boundary(m_bf16, h_bf16, g_post, g_pre, eps: float, n: int):
+    """The sublayer boundary after the MoE branch (post-norm, n-th depth-scaled
+    residual add, next pre-norm); BF16 bit patterns in and out ->
+    (new residual h' [T, d], next input x [T, d])."""
+    m = _c(m_bf16, np.uint16)
+    h = _c(h_bf16, np.uint16)
+    gp = _c(g_post, np.uint16).reshape(-1)
+    gq = _c(g_pre, np.uint16).reshape(-1)
+    T, d = m.shape
+    assert h.shape == (T, d) and gp.size == d and gq.size == d
+    c_h, c_x = residual_coefficients(n)
+    h_out = np.zeros((T, d), np.uint16)
+    x_out = np.zeros((T, d), np.uint16)
+    rc = _load().oracle_boundary(_ptr(m), _ptr(h), _ptr(gp), _ptr(gq), T, d,
+                                 float(np.float32(eps)), float(c_h), float(c_x), _ptr(h_out),
+                                 _ptr(x_out))
+    if rc:
+        raise ValueError(f"oracle_boundary failed ({rc})")
+    return h_out, x_out
 
 
 def nvfp4_quantize(v: np.ndarray):

@@ -9,9 +9,10 @@
  * Sources (page title, section):
  *   [SGL]  "SGLang 原生支持 Reflection 的 Beam 并驱动其生产 API",
  *          sections "Dense Layers and Grouped MoE Routing",
- *          "BF16 MoE Kernel Optimization", "Fusion Optimizations".
+ *          "BF16 MoE Kernel Optimization", "Fusion Optimizations",
+ *          "Sandwich Normalization and Depth-Scaled Residuals".
  *   [VLLM] "vLLM 实现 Reflection Beam 501B MoE 模型 Day 0 支持",
- *          section "MoE and residual stream".
+ *          sections "MoE and residual stream", "Agent-driven optimization".
  *   [HF]   "Reflection 发布 501B 开源模型 Beam，Apache 2.0 许可",
  *          sections "专家混合" (mixture of experts) and "残差流" (residual
  *          stream: router and SwiGLU product computed in FP32).
@@ -452,6 +453,65 @@ int oracle_experts_nvfp4(const uint16_t *x, int64_t T, int32_t d, int32_t F,
 }
 
 /* ------------------------------------------------------------------------ */
+/* The sublayer boundary after the MoE branch                                */
+/* ------------------------------------------------------------------------ */
+
+/* Nearest BF16 of a double, ties to even, with one rounding: the double is
+ * first brought to binary32 by rounding to odd (truncate, then set the last
+ * bit when inexact), which keeps the later rounding to 8 bits correct. */
+static uint16_t bf16_round_double(double v) {
+  float f = (float)v;
+  if ((double)f != v) {
+    if (fabs((double)f) > fabs(v)) f = nextafterf(f, 0.0f);
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    u |= 1u;
+    memcpy(&f, &u, sizeof f);
+  }
+  return bf16_round(f);
+}
+
+/* One token's boundary after the MoE branch, [VLLM] "MoE and residual
+ * stream" (sandwich norm: an RMSNorm after every sublayer and one before the
+ * next; depth-scaled residual: the n-th add is h <- sqrt((n-1)/n) h + x/sqrt(n))
+ * and "Agent-driven optimization" item 1 (post-norm, scaled residual add and
+ * next pre-norm as one step, FP32 math, BF16 rounding points); [SGL]
+ * "Sandwich Normalization and Depth-Scaled Residuals" (both scaled operands
+ * are rounded to BF16 before the addition).  Per token, with m the layer's
+ * BF16 output and h the BF16 residual stream:
+ *   p  = bf16( m * g_post / sqrt(mean(m^2) + eps) )
+ *   a  = bf16( c_h * h ),   b = bf16( c_x * p )
+ *   h' = bf16( a + b )
+ *   x  = bf16( h' * g_pre / sqrt(mean(h'^2) + eps) )
+ * [reading] c_h = fp32(sqrt((n-1)/n)) and c_x = fp32(1/sqrt(n)) are given;
+ * the arithmetic is FP64 with one rounding at each point listed. */
+int oracle_boundary(const uint16_t *m, const uint16_t *h, const uint16_t *g_post,
+                    const uint16_t *g_pre, int64_t T, int32_t d, double eps, float c_h,
+                    float c_x, uint16_t *h_out, uint16_t *x_out) {
+  if (T < 0 || d <= 0) return -1;
+#pragma omp parallel for schedule(static)
+  for (int64_t t = 0; t < T; ++t) {
+    const uint16_t *mt = m + t * d, *ht = h + t * d;
+    uint16_t *ho = h_out + t * d, *xo = x_out + t * d;
+    double ss = 0.0;
+    for (int32_t i = 0; i < d; ++i) ss += bf16_value(mt[i]) * bf16_value(mt[i]);
+    const double r = 1.0 / sqrt(ss / d + eps);
+    double ss2 = 0.0;
+    for (int32_t i = 0; i < d; ++i) {
+      const uint16_t p = bf16_round_double(bf16_value(mt[i]) * bf16_value(g_post[i]) * r);
+      const uint16_t a = bf16_round_double((double)c_h * bf16_value(ht[i]));
+      const uint16_t b = bf16_round_double((double)c_x * bf16_value(p));
+      ho[i] = bf16_round_double(bf16_value(a) + bf16_value(b));
+      ss2 += bf16_value(ho[i]) * bf16_value(ho[i]);
+    }
+    const double r2 = 1.0 / sqrt(ss2 / d + eps);
+    for (int32_t i = 0; i < d; ++i)
+      xo[i] = bf16_round_double(bf16_value(ho[i]) * bf16_value(g_pre[i]) * r2);
+  }
+  return 0;
+}
+
+/* ------------------------------------------------------------------------ */
 /* Scalar entry points for the pins.                                         */
 /* ------------------------------------------------------------------------ */
 double oracle_e2m1_value(uint8_t code) { return e2m1_value(code); }
@@ -459,6 +519,7 @@ double oracle_e4m3_value(uint8_t code) { return e4m3_value(code); }
 uint8_t oracle_e2m1_encode(float v) { return e2m1_encode(v); }
 uint8_t oracle_e4m3_encode(float v) { return e4m3_encode(v); }
 uint16_t oracle_bf16_round(float v) { return bf16_round(v); }
+uint16_t oracle_bf16_round_double(double v) { return bf16_round_double(v); }
 
 /* NVFP4 activation quantiser on a row of n values (n % 16 == 0): packed codes
  * (low nibble = even index) and one E4M3 scale per 16. */

@@ -354,3 +354,99 @@ def test_nvfp4_generator_weights_round_trip_grid_values():
     back = np.vectorize(oracle.e2m1_value)(dec) * np.repeat(
         np.vectorize(oracle.e4m3_value)(sf.numpy()), 16, 1) * float(gs)
     assert np.allclose(back, w.double().numpy(), rtol=1e-6, atol=0)
+
+
+# ------------------------------------------------- sublayer boundary (post-norm,
+# depth-scaled residual add, next pre-norm)
+def _bf16_value(bits):
+    return np.asarray(bits, np.uint16).astype(np.uint32).__lshift__(16).view(np.float32) \
+        .astype(np.float64)
+
+
+def _rand_bf16(shape, scale=1.0, seed=0):
+    g = torch.Generator().manual_seed(seed)
+    return inputs.bf16_bits((torch.randn(*shape, generator=g) * scale).to(torch.bfloat16))
+
+
+def _within_half_step(bits, ref):
+    """bits (BF16) is a correct rounding of the float64 values ref."""
+    v = _bf16_value(bits)
+    _, e = np.frexp(np.abs(ref))
+    half = np.where(ref == 0, 0.0, np.ldexp(1.0, e - 9))
+    return np.all(np.abs(v - ref) <= half * (1 + 1e-12))
+
+
+def test_bf16_round_double_is_one_correct_rounding():
+    """Against exact rational arithmetic: the nearest BF16, ties to even."""
+    from fractions import Fraction
+    rng = np.random.default_rng(5)
+    vals = list(rng.standard_normal(3000) * 7.0)
+    # exact ties and values a hair above / below a tie
+    for k in range(0x3f80, 0x3f80 + 40):
+        lo = float(_bf16_value(np.uint16(k)))
+        hi = float(_bf16_value(np.uint16(k + 1)))
+        mid = (lo + hi) / 2
+        vals += [mid, np.nextafter(mid, np.inf), np.nextafter(mid, -np.inf)]
+    for v in vals:
+        got = oracle.bf16_round_double(float(v))
+        b32 = np.float32(v).view(np.uint32) >> np.uint32(16)
+        cands = [int(b32) + j for j in (-1, 0, 1, 2) if 0 <= int(b32) + j < 0x7f80 or v < 0]
+        best = min(cands, key=lambda c: (abs(Fraction(float(_bf16_value(np.uint16(c & 0xffff))))
+                                             - Fraction(float(v))), c & 1))
+        assert got == (best & 0xffff), (v, got, best)
+
+
+def test_boundary_norms_match_torch_rms_norm():
+    """n = 1: the residual add keeps only the post-normed branch (c_h = 0,
+    c_x = 1), so h' is RMSNorm(m) and x is RMSNorm(h'): torch's rms_norm in
+    FP64, each rounded once."""
+    T, d, eps = 6, 512, 1e-6
+    m = _rand_bf16((T, d), 3.0, seed=1)
+    h = _rand_bf16((T, d), 1.0, seed=2)
+    gp = _rand_bf16((d,), 0.3, seed=3)
+    gq = _rand_bf16((d,), 0.3, seed=4)
+    h_out, x_out = oracle.boundary(m, h, gp, gq, eps, 1)
+    rms = torch.nn.functional.rms_norm
+    ref_h = rms(torch.from_numpy(_bf16_value(m)), (d,), torch.from_numpy(_bf16_value(gp)),
+                eps=eps).numpy()
+    assert _within_half_step(h_out, ref_h)
+    ref_x = rms(torch.from_numpy(_bf16_value(h_out)), (d,), torch.from_numpy(_bf16_value(gq)),
+                eps=np.float32(eps).item()).numpy()
+    assert _within_half_step(x_out, ref_x)
+
+
+def test_boundary_residual_closed_forms():
+    T, d, eps = 4, 256, 1e-6
+    m = _rand_bf16((T, d), 1.0, seed=5)
+    h = _rand_bf16((T, d), 1.0, seed=6)
+    ones = inputs.bf16_bits(torch.ones(d, dtype=torch.bfloat16))
+    p, _ = oracle.boundary(m, h, ones, ones, eps, 1)          # p = RMSNorm(m)
+    # n = 4 with a zero stream: h' = p / 2 exactly (c_x = 1/2)
+    h4, _ = oracle.boundary(m, np.zeros_like(h), ones, ones, eps, 4)
+    assert np.array_equal(_bf16_value(h4), _bf16_value(p) / 2)
+    # a zero branch: h' = round(fp32(sqrt(3/4)) * h)
+    hz, _ = oracle.boundary(np.zeros_like(m), h, ones, ones, eps, 4)
+    assert _within_half_step(hz, float(np.float32(math.sqrt(0.75))) * _bf16_value(h))
+
+
+def test_boundary_is_odd():
+    T, d = 3, 256
+    m = _rand_bf16((T, d), 2.0, seed=7)
+    h = _rand_bf16((T, d), 1.0, seed=8)
+    g = _rand_bf16((d,), 0.5, seed=9)
+    a = oracle.boundary(m, h, g, g, 1e-6, 7)
+    b = oracle.boundary(m ^ np.uint16(0x8000), h ^ np.uint16(0x8000), g, g, 1e-6, 7)
+    for x, y in zip(a, b):
+        assert np.array_equal(x ^ np.uint16(0x8000), y)
+
+
+def test_depth_scaled_residual_keeps_unit_variance():
+    """The point of the depth scaling: unit-variance stream and branch give a
+    unit-variance stream at every depth."""
+    T, d = 64, 1024
+    h = _rand_bf16((T, d), 1.0, seed=10)
+    ones = inputs.bf16_bits(torch.ones(d, dtype=torch.bfloat16))
+    for n in (2, 10, 104):
+        m = _rand_bf16((T, d), 5.0, seed=11 + n)
+        h_out, _ = oracle.boundary(m, h, ones, ones, 1e-6, n)
+        assert abs(_bf16_value(h_out).var() - 1.0) < 0.03
