@@ -33,7 +33,8 @@ EXPORTS = ("beam_moe_workspace_size", "beam_moe_workspace_layout", "beam_moe_rou
            "beam_moe_forward_noalloc", "beam_moe_forward_nvfp4", "beam_moe_nvfp4_pack_scales",
            "beam_moe_check_status", "beam_moe_set_stage_events", "beam_moe_set_debug",
            "beam_moe_kernels_per_forward", "beam_status_string", "beam_moe_ep_dispatch",
-           "beam_moe_ep_workspace_size", "beam_moe_ep_experts", "beam_moe_ep_combine")
+           "beam_moe_ep_workspace_size", "beam_moe_ep_experts", "beam_moe_ep_combine",
+           "beam_moe_forward_boundary")
 
 
 class BeamError(RuntimeError):
@@ -46,6 +47,12 @@ class _Layout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in (
         "status", "logits", "topk_idx", "topk_w", "counts", "offsets", "perm_src", "pair_row",
         "perm_w", "x_perm", "h", "x_fp4", "x_sf", "h_fp4", "h_sf", "y", "total")]
+
+
+class _Boundary(ctypes.Structure):
+    _fields_ = [("residual", ctypes.c_void_p), ("post_norm_w", ctypes.c_void_p),
+                ("next_norm_w", ctypes.c_void_p), ("next_input", ctypes.c_void_p),
+                ("eps", ctypes.c_float), ("residual_index", ctypes.c_int32)]
 
 
 class _Fp4Weight(ctypes.Structure):
@@ -96,6 +103,9 @@ def lib():
         L.beam_moe_set_debug.restype = _ST
         L.beam_moe_kernels_per_forward.argtypes = [cfgp, _I64, ctypes.c_int32, ctypes.c_int32]
         L.beam_moe_kernels_per_forward.restype = ctypes.c_int32
+        L.beam_moe_forward_boundary.argtypes = [cfgp, _P, _P, _P, _P, _P, _P, _P, _I64,
+                                                ctypes.POINTER(_Boundary), _P, _SZ, _P]
+        L.beam_moe_forward_boundary.restype = _ST
         L.beam_moe_ep_dispatch.argtypes = [cfgp, _P, _P, _P, _I64, ctypes.c_int32, _P, _P, _P, _P,
                                            _P, _SZ, _P]
         L.beam_moe_ep_dispatch.restype = _ST
@@ -240,6 +250,34 @@ def forward(cfg, hidden, router_w, corr_bias, w_gate, w_up, w_down, out=None,
         out.copy_(o, non_blocking=True)
         return out
     return o
+
+
+def forward_boundary(cfg, hidden, router_w, corr_bias, w_gate, w_up, w_down, residual,
+                     post_norm_w, next_norm_w, eps: float, n: int, out=None, next_input=None,
+                     ws: Workspace | None = None, stream=None):
+    """The layer followed by the decoder's sublayer boundary (post-norm, n-th
+    depth-scaled residual add, next pre-norm) in its combine kernel.  Returns
+    (out, next_input); ``residual`` is overwritten with the new stream."""
+    T = hidden.shape[0]
+    dev = hidden.device
+    ws = _ws(cfg, T, ws, dev)
+    o = torch.empty(T, cfg.d, dtype=torch.bfloat16, device=dev) if out is None else out
+    nx = torch.empty(T, cfg.d, dtype=torch.bfloat16, device=dev) if next_input is None \
+        else next_input
+    b = _Boundary(_dev(residual, torch.bfloat16, "residual"),
+                  _dev(post_norm_w, torch.bfloat16, "post_norm_w"),
+                  _dev(next_norm_w, torch.bfloat16, "next_norm_w"),
+                  _dev(nx, torch.bfloat16, "next_input"), float(eps), int(n))
+    c = _cfg(cfg)
+    _check(lib().beam_moe_forward_boundary(ctypes.byref(c), _dev(hidden, torch.bfloat16, "hidden"),
+                                           _dev(router_w, torch.float32, "router_w"),
+                                           _dev(corr_bias, torch.float32, "corr_bias"),
+                                           _dev(w_gate, torch.bfloat16, "w_gate"),
+                                           _dev(w_up, torch.bfloat16, "w_up"),
+                                           _dev(w_down, torch.bfloat16, "w_down"), o.data_ptr(), T,
+                                           ctypes.byref(b), ws.ptr, ws.nbytes, _stream(stream)),
+           "beam_moe_forward_boundary")
+    return o, nx
 
 
 def forward_routed(cfg, hidden, topk_idx, topk_w, w_gate, w_up, w_down, out=None,

@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cmath>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -312,7 +313,8 @@ beam_status_t run_experts(const beam_moe_config_t& c, const void* hidden, const 
                           const float* w, const void* w_gate, const void* w_up,
                           const void* w_down, void* out, int64_t T, void* ws, const Layout& L,
                           const DevInfo& dev, cudaStream_t s, bool permuted = false,
-                          float* y_pairs = nullptr, int32_t id_base = 0) {
+                          float* y_pairs = nullptr, int32_t id_base = 0,
+                          const beam::BoundaryArgs* boundary = nullptr) {
   const int64_t TK = T * c.topk;
   const int64_t rows = std::max<int64_t>(TK, kMinRows);
   const int nt_gu = gateup_tile(c, TK);
@@ -390,7 +392,13 @@ beam_status_t run_experts(const beam_moe_config_t& c, const void* hidden, const 
   if (err != cudaSuccess) return BEAM_ERR_CUDA;
   record(6, s);
 
-  if (!y_pairs) beam::launch_combine(y, pa.pair_row, T, c.topk, c.d, static_cast<uint16_t*>(out), s);
+  if (boundary) {
+    if (beam::launch_combine_boundary(y, pa.pair_row, T, c.topk, c.d, static_cast<uint16_t*>(out),
+                                      *boundary, s) != cudaSuccess)
+      return BEAM_ERR_CUDA;
+  } else if (!y_pairs) {
+    beam::launch_combine(y, pa.pair_row, T, c.topk, c.d, static_cast<uint16_t*>(out), s);
+  }
   record(7, s);
   return cuda_status(cudaGetLastError());
 }
@@ -608,6 +616,47 @@ beam_status_t beam_moe_forward(const beam_moe_config_t* cfg, const void* hidden,
   if (st != BEAM_OK) return st;
   return run_experts(*cfg, hidden, idx, w, w_gate, w_up, w_down, out, T, workspace, L, dev, s,
                      permuted);
+}
+
+beam_status_t beam_moe_forward_boundary(const beam_moe_config_t* cfg, const void* hidden,
+                                        const float* router_w, const float* corr_bias,
+                                        const void* w_gate, const void* w_up, const void* w_down,
+                                        void* out, int64_t T, const beam_moe_boundary_t* bnd,
+                                        void* workspace, size_t ws_bytes, void* stream) {
+  Layout L;
+  DevInfo dev;
+  bool empty = false;
+  beam_status_t st = common_checks(cfg, T, workspace, ws_bytes, &L, &dev, &empty);
+  if (st != BEAM_OK) return st;
+  if (!bnd || bnd->residual_index < 1 || !(bnd->eps >= 0.f) ||
+      static_cast<int64_t>(cfg->d) * 4 > 200 * 1024)
+    return BEAM_ERR_INVALID_ARG;
+  if (empty) return BEAM_OK;
+  if (!aligned16(hidden) || !aligned16(router_w) || !aligned16(corr_bias) || !aligned16(w_gate) ||
+      !aligned16(w_up) || !aligned16(w_down) || !aligned16(out) || !aligned16(bnd->residual) ||
+      !aligned16(bnd->post_norm_w) || !aligned16(bnd->next_norm_w) ||
+      !aligned16(bnd->next_input))
+    return BEAM_ERR_INVALID_ARG;
+  if (!encoder()) return BEAM_ERR_CUDA;
+  beam::BoundaryArgs ba;
+  ba.g_post = static_cast<const uint16_t*>(bnd->post_norm_w);
+  ba.g_pre = static_cast<const uint16_t*>(bnd->next_norm_w);
+  ba.residual = static_cast<uint16_t*>(bnd->residual);
+  ba.next_x = static_cast<uint16_t*>(bnd->next_input);
+  ba.eps = bnd->eps;
+  const double n = bnd->residual_index;
+  ba.c_h = static_cast<float>(std::sqrt((n - 1.0) / n));
+  ba.c_x = static_cast<float>(1.0 / std::sqrt(n));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  record(0, s);
+  int32_t* idx = at<int32_t>(workspace, L.idx);
+  float* w = at<float>(workspace, L.w);
+  bool permuted = false;
+  st = run_route(*cfg, hidden, router_w, corr_bias, T, idx, w, at<float>(workspace, L.logits),
+                 workspace, L, dev, s, &permuted);
+  if (st != BEAM_OK) return st;
+  return run_experts(*cfg, hidden, idx, w, w_gate, w_up, w_down, out, T, workspace, L, dev, s,
+                     permuted, nullptr, 0, &ba);
 }
 
 beam_status_t beam_moe_forward_routed(const beam_moe_config_t* cfg, const void* hidden,

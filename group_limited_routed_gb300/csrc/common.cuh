@@ -67,6 +67,22 @@ void launch_gather(const uint16_t* x, const int32_t* perm_src, const int32_t* n_
 void launch_combine(const float* y, const int32_t* pair_row, int64_t T, int32_t k, int32_t d,
                     uint16_t* out, cudaStream_t s);
 
+// the decoder's sublayer boundary after the layer: post-norm, depth-scaled
+// residual add, next pre-norm
+struct BoundaryArgs {
+  const uint16_t* g_post;  // [d] BF16 RMSNorm weight of the layer's output
+  const uint16_t* g_pre;   // [d] BF16 RMSNorm weight of the next sublayer's input
+  uint16_t* residual;      // [T, d] BF16 residual stream, read and overwritten
+  uint16_t* next_x;        // [T, d] BF16 next sublayer's input
+  float eps;
+  float c_h, c_x;          // sqrt((n-1)/n), 1/sqrt(n) for the n-th residual add
+};
+// combine (as launch_combine, into out) fused with the boundary; d*4 bytes of
+// shared memory per block
+cudaError_t launch_combine_boundary(const float* y, const int32_t* pair_row, int64_t T, int32_t k,
+                                    int32_t d, uint16_t* out, const BoundaryArgs& b,
+                                    cudaStream_t s);
+
 // W_r [E, d] FP32 -> planes [E, 3d] BF16 (hi | mid | lo, W = hi + mid + lo to
 // within 2^-24 relative).
 void launch_router_split(const float* w, int32_t E, int32_t d, uint16_t* planes, cudaStream_t s);

@@ -451,6 +451,104 @@ __global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ 
   reinterpret_cast<uint4*>(out + t * d)[c8] = o;
 }
 
+// -------------------------------------------------- combine + boundary
+// One block per token, FP32 arithmetic, BF16 roundings where the decoder
+// keeps them: the combine exactly as combine_kernel (written to out); the
+// post-norm p = bf16(m * g_post / sqrt(mean(m^2) + eps)); the depth-scaled
+// residual add h' = bf16(bf16(c_h * h) + bf16(c_x * p)) (written over the
+// residual stream); the next pre-norm x = bf16(h' * g_pre / sqrt(mean(h'^2) +
+// eps)).  Sums of squares: per thread in chunk order, then a fixed-order
+// block reduction, so the result is deterministic.
+__device__ __forceinline__ float bf16r(float v) { return bf16_to_f32(f32_to_bf16(v)); }
+
+__device__ __forceinline__ float block_sum(float v, float* s_red) {
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+  const int warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  __syncthreads();  // s_red may still be read from the previous reduction
+  if ((threadIdx.x & 31) == 0) s_red[warp] = v;
+  __syncthreads();
+  float t = 0.f;
+  for (int w = 0; w < nw; ++w) t += s_red[w];
+  return t;
+}
+
+__global__ void __launch_bounds__(256) combine_boundary_kernel(const float* __restrict__ y,
+                                                               const int32_t* __restrict__ pair_row,
+                                                               int32_t k, int32_t d,
+                                                               uint16_t* __restrict__ out,
+                                                               BoundaryArgs b) {
+  extern __shared__ float s_v[];  // [d] the token's current values
+  __shared__ float s_red[32];
+  const int64_t t = blockIdx.x;
+  const int n8 = d / 8;
+  float ss = 0.f;
+  for (int c8 = threadIdx.x; c8 < n8; c8 += blockDim.x) {
+    float acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+    for (int sl = 0; sl < k; ++sl) {
+      const int row = pair_row[t * k + sl];
+      if (row < 0) continue;
+      const float4* src = reinterpret_cast<const float4*>(y + static_cast<int64_t>(row) * d) + 2 * c8;
+      const float4 a = src[0];
+      const float4 c = src[1];
+      acc[0] += a.x;
+      acc[1] += a.y;
+      acc[2] += a.z;
+      acc[3] += a.w;
+      acc[4] += c.x;
+      acc[5] += c.y;
+      acc[6] += c.z;
+      acc[7] += c.w;
+    }
+    uint4 o;
+    uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint16_t lo = f32_to_bf16(acc[2 * i]), hi = f32_to_bf16(acc[2 * i + 1]);
+      ow[i] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+      const float vl = bf16_to_f32(lo), vh = bf16_to_f32(hi);
+      s_v[c8 * 8 + 2 * i] = vl;
+      s_v[c8 * 8 + 2 * i + 1] = vh;
+      ss = fmaf(vl, vl, ss);
+      ss = fmaf(vh, vh, ss);
+    }
+    reinterpret_cast<uint4*>(out + t * d)[c8] = o;
+  }
+  const float r = 1.0f / sqrtf(block_sum(ss, s_red) / static_cast<float>(d) + b.eps);
+  float ss2 = 0.f;
+  for (int c8 = threadIdx.x; c8 < n8; c8 += blockDim.x) {
+    const uint4 hv = reinterpret_cast<const uint4*>(b.residual + t * d)[c8];
+    const uint4 gv = reinterpret_cast<const uint4*>(b.g_post)[c8];
+    const uint16_t* hs = reinterpret_cast<const uint16_t*>(&hv);
+    const uint16_t* gs = reinterpret_cast<const uint16_t*>(&gv);
+    uint4 o;
+    uint16_t* os = reinterpret_cast<uint16_t*>(&o);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float p = bf16r(s_v[c8 * 8 + i] * r * bf16_to_f32(gs[i]));
+      const float a = bf16r(b.c_h * bf16_to_f32(hs[i]));
+      const uint16_t hn = f32_to_bf16(a + bf16r(b.c_x * p));
+      os[i] = hn;
+      const float v = bf16_to_f32(hn);
+      s_v[c8 * 8 + i] = v;
+      ss2 = fmaf(v, v, ss2);
+    }
+    reinterpret_cast<uint4*>(b.residual + t * d)[c8] = o;
+  }
+  const float r2 = 1.0f / sqrtf(block_sum(ss2, s_red) / static_cast<float>(d) + b.eps);
+  for (int c8 = threadIdx.x; c8 < n8; c8 += blockDim.x) {
+    const uint4 gv = reinterpret_cast<const uint4*>(b.g_pre)[c8];
+    const uint16_t* gs = reinterpret_cast<const uint16_t*>(&gv);
+    uint4 o;
+    uint16_t* os = reinterpret_cast<uint16_t*>(&o);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) os[i] = f32_to_bf16(s_v[c8 * 8 + i] * r2 * bf16_to_f32(gs[i]));
+    reinterpret_cast<uint4*>(b.next_x + t * d)[c8] = o;
+  }
+}
+
 // ------------------------------------------------------- expert-parallel pack
 // Packed row r (expert order, hence grouped by owning rank) carries its
 // expert and its routing weight; block 0 also counts the rows per owner.
@@ -544,6 +642,19 @@ cudaError_t launch_fused_route(const RouterArgs& ra, int ksplit, const SelectArg
   void* args[] = {&a0, &ksplit, &a1, &a2};
   return cudaLaunchCooperativeKernel(reinterpret_cast<void*>(fused_route_kernel), dim3(grid),
                                      dim3(256), args, 0, s);
+}
+
+cudaError_t launch_combine_boundary(const float* y, const int32_t* pair_row, int64_t T, int32_t k,
+                                    int32_t d, uint16_t* out, const BoundaryArgs& b,
+                                    cudaStream_t s) {
+  const size_t smem = static_cast<size_t>(d) * sizeof(float);
+  if (smem > 48 * 1024) {
+    const cudaError_t e = cudaFuncSetAttribute(
+        combine_boundary_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+  }
+  combine_boundary_kernel<<<static_cast<unsigned>(T), 256, smem, s>>>(y, pair_row, k, d, out, b);
+  return cudaGetLastError();
 }
 
 void launch_ep_pack(const int32_t* idx, const int32_t* perm_src, const float* perm_w,

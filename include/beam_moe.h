@@ -154,6 +154,37 @@ beam_status_t beam_moe_forward_routed(const beam_moe_config_t *cfg, const void *
                                       const void *w_down, void *out, int64_t T,
                                       void *workspace, size_t ws_bytes, void *stream);
 
+/* The decoder's sublayer boundary after this layer ("vLLM 实现 Reflection Beam
+ * 501B MoE 模型 Day 0 支持", section "MoE and residual stream": sandwich norm and
+ * depth-scaled residuals; section "Agent-driven optimization", items 1 and 3:
+ * post-norm, scaled residual add and next pre-norm as one kernel that also
+ * combines the top-8 expert outputs; "SGLang 原生支持 Reflection 的 Beam 并驱动其
+ * 生产 API", section "Sandwich Normalization and Depth-Scaled Residuals": both
+ * scaled operands are rounded to BF16 before the addition).  All device
+ * pointers, BF16, 16-byte aligned, caller-owned. */
+typedef struct {
+  void *residual;          /* [T, d] the residual stream h; overwritten with h'     */
+  const void *post_norm_w; /* [d] RMSNorm weight after the MoE sublayer           */
+  const void *next_norm_w; /* [d] RMSNorm weight before the next sublayer         */
+  void *next_input;        /* [T, d] out: the next sublayer's normalised input    */
+  float eps;               /* RMSNorm epsilon (>= 0)                              */
+  int32_t residual_index;  /* n >= 1: this is the decoder's n-th residual add     */
+} beam_moe_boundary_t;
+
+/* beam_moe_forward (out = the layer's BF16 output m, as there) followed, in
+ * the combine kernel, by the boundary, per token in FP32 arithmetic:
+ *   p  = bf16(m * post_norm_w / sqrt(mean(m^2) + eps))
+ *   h' = bf16(bf16(c_h * h) + bf16(c_x * p)),  c_h = fp32(sqrt((n-1)/n)),
+ *                                                c_x = fp32(1/sqrt(n))
+ *   next_input = bf16(h' * next_norm_w / sqrt(mean(h'^2) + eps))
+ * Deterministic (fixed-order sums).  BEAM_ERR_INVALID_ARG for n < 1, eps < 0
+ * or d > 51200 (the token's values are staged in shared memory). */
+beam_status_t beam_moe_forward_boundary(const beam_moe_config_t *cfg, const void *hidden,
+                                        const float *router_w, const float *corr_bias,
+                                        const void *w_gate, const void *w_up, const void *w_down,
+                                        void *out, int64_t T, const beam_moe_boundary_t *boundary,
+                                        void *workspace, size_t ws_bytes, void *stream);
+
 /* beam_moe_forward without a caller workspace and without any allocation.
  * The pages have no counterpart: this entry point exists for callers that
  * cannot allocate device memory at all -- a plugin inside a host application
