@@ -245,6 +245,23 @@ beam::PermuteArgs permute_args(const beam_moe_config_t& c, const int32_t* idx, c
   return pa;
 }
 
+// From this many (token, slot) entries on, the permutation runs as a counting
+// sort (one cooperative launch) instead of one block per expert scanning all
+// entries; its chunk counts live in the router's partials buffer, which is
+// dead once the selection has run (it holds at least T * E floats).
+constexpr int64_t kSortMinEntries = 8192;
+
+beam_status_t launch_permutation(const beam::PermuteArgs& pa, void* ws, const Layout& L,
+                                 const DevInfo& dev, cudaStream_t s) {
+  if (pa.TK >= kSortMinEntries && pa.E <= 256) {
+    return beam::launch_permute_sort(pa, at<int32_t>(ws, L.part), dev.sms, s) == cudaSuccess
+               ? BEAM_OK
+               : BEAM_ERR_CUDA;
+  }
+  beam::launch_permute(pa, s);
+  return BEAM_OK;
+}
+
 // router + selection into idx/w (and logits).  With `permuted` given and a
 // decode-sized batch, the permutation runs in the same cooperative launch and
 // *permuted is set.
@@ -324,7 +341,7 @@ beam_status_t run_experts(const beam_moe_config_t& c, const void* hidden, const 
   beam::PermuteArgs pa = permute_args(c, idx, w, T, ws, L);
   pa.id_base = id_base;
   if (!permuted) {
-    beam::launch_permute(pa, s);
+    if (launch_permutation(pa, ws, L, dev, s) != BEAM_OK) return BEAM_ERR_CUDA;
     record(3, s);
   }
   // decode-sized batches: the gate/up GEMM gathers its token rows itself
@@ -415,7 +432,7 @@ beam_status_t run_experts_nvfp4(const beam_moe_config_t& c, const void* hidden, 
   uint32_t* status = at<uint32_t>(ws, L.status);
   const beam::PermuteArgs pa = permute_args(c, idx, w, T, ws, L);
   if (!permuted) {
-    beam::launch_permute(pa, s);
+    if (launch_permutation(pa, ws, L, dev, s) != BEAM_OK) return BEAM_ERR_CUDA;
     record(3, s);
   }
   uint8_t* xq = at<uint8_t>(ws, L.x_fp4);
@@ -783,7 +800,7 @@ beam_status_t beam_moe_ep_dispatch(const beam_moe_config_t* cfg, const void* hid
                  workspace, L, dev, s, &permuted);
   if (st != BEAM_OK) return st;
   const beam::PermuteArgs pa = permute_args(*cfg, idx, w, T, workspace, L);
-  if (!permuted) beam::launch_permute(pa, s);
+  if (!permuted && launch_permutation(pa, workspace, L, dev, s) != BEAM_OK) return BEAM_ERR_CUDA;
   record(3, s);
   const int64_t TK = T * cfg->topk;
   beam::launch_gather(static_cast<const uint16_t*>(hidden), pa.perm_src, pa.offsets + cfg->n_experts,

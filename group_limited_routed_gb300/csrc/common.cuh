@@ -54,6 +54,10 @@ struct PermuteArgs {
 void launch_router(const RouterArgs& a, int ksplit, cudaStream_t s);
 void launch_select(const SelectArgs& a, cudaStream_t s);
 void launch_permute(const PermuteArgs& a, cudaStream_t s);
+// the same permutation as a counting sort in one cooperative launch (large
+// batches); hist: int32 [ceil(TK / 1024), E] scratch
+cudaError_t launch_permute_sort(const PermuteArgs& a, int32_t* hist, int num_sms, cudaStream_t s);
+constexpr int64_t kPermuteSortChunk = 1024;
 // expert-parallel dispatch metadata: per packed row its expert and weight,
 // and the rows bound for each of n_ranks owners
 void launch_ep_pack(const int32_t* idx, const int32_t* perm_src, const float* perm_w,

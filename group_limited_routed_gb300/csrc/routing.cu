@@ -304,26 +304,35 @@ __device__ __forceinline__ void permute_expert(const PermuteArgs& a, int e) {
   __shared__ int s_tot[2];
   constexpr int64_t kStep = 256 * kPermPer;
 
+  // pass 1: this expert's entries and those of smaller experts; four steps'
+  // loads are issued together (the pass is bound by load latency)
+  constexpr int kAhead = 4;
   int cnt = 0, below = 0;
-  for (int64_t base = 0; base < a.TK; base += kStep) {
-    const int64_t i0 = base + static_cast<int64_t>(tid) * kPermPer;
-    if (i0 >= a.TK) continue;
-    int v[kPermPer];
-    load8(a.idx, i0, a.TK, v);
+  for (int64_t base = 0; base < a.TK; base += kAhead * kStep) {
+    int v[kAhead][kPermPer];
 #pragma unroll
-    for (int j = 0; j < kPermPer; ++j) v[j] -= a.id_base;
+    for (int q = 0; q < kAhead; ++q) {
+      const int64_t i0 = base + q * kStep + static_cast<int64_t>(tid) * kPermPer;
+      if (i0 < a.TK) load8(a.idx, i0, a.TK, v[q]);
+    }
 #pragma unroll
-    for (int j = 0; j < kPermPer; ++j) {
-      if (i0 + j >= a.TK) break;
-      if (static_cast<unsigned>(v[j]) >= static_cast<unsigned>(a.E)) {
-        if (e == 0) {
-          a.pair_row[i0 + j] = -1;
-          latch_status(a.status, kStatusDeviceCheck);
+    for (int q = 0; q < kAhead; ++q) {
+      const int64_t i0 = base + q * kStep + static_cast<int64_t>(tid) * kPermPer;
+      if (i0 >= a.TK) continue;
+#pragma unroll
+      for (int j = 0; j < kPermPer; ++j) {
+        if (i0 + j >= a.TK) break;
+        const int x = v[q][j] - a.id_base;
+        if (static_cast<unsigned>(x) >= static_cast<unsigned>(a.E)) {
+          if (e == 0) {
+            a.pair_row[i0 + j] = -1;
+            latch_status(a.status, kStatusDeviceCheck);
+          }
+          continue;
         }
-        continue;
+        cnt += (x == e);
+        below += (x < e);
       }
-      cnt += (v[j] == e);
-      below += (v[j] < e);
     }
   }
 #pragma unroll
@@ -351,10 +360,9 @@ __device__ __forceinline__ void permute_expert(const PermuteArgs& a, int e) {
   __syncthreads();
   const int total = s_tot[0];
   const int first = s_tot[1];
-  int running = 0;
-  for (int64_t base = 0; base < a.TK && running < total; base += kStep) {
-    const int64_t i0 = base + static_cast<int64_t>(tid) * kPermPer;
-    int v[kPermPer];
+  // pass 2: the entries in order; the next step's loads are issued before
+  // this step's scan
+  auto fetch = [&](int64_t i0, int (&v)[kPermPer]) {
     if (i0 < a.TK) {
       load8(a.idx, i0, a.TK, v);
 #pragma unroll
@@ -363,6 +371,16 @@ __device__ __forceinline__ void permute_expert(const PermuteArgs& a, int e) {
 #pragma unroll
       for (int j = 0; j < kPermPer; ++j) v[j] = -1;
     }
+  };
+  int running = 0;
+  int vn[kPermPer];
+  fetch(static_cast<int64_t>(tid) * kPermPer, vn);
+  for (int64_t base = 0; base < a.TK && running < total; base += kStep) {
+    const int64_t i0 = base + static_cast<int64_t>(tid) * kPermPer;
+    int v[kPermPer];
+#pragma unroll
+    for (int j = 0; j < kPermPer; ++j) v[j] = vn[j];
+    fetch(i0 + kStep, vn);
     unsigned mask = 0;
 #pragma unroll
     for (int j = 0; j < kPermPer; ++j) mask |= (v[j] == e ? 1u : 0u) << j;
@@ -399,6 +417,119 @@ __device__ __forceinline__ void permute_expert(const PermuteArgs& a, int e) {
   }
 }
 
+// ------------------------------------------------------ permute (large batches)
+// The same stable (expert, token, slot) order as permute_expert, as a
+// counting sort in one cooperative launch: (A) each block counts the experts
+// of a chunk of entries; (B) block 0 turns the chunk counts into each chunk's
+// first row per expert (per expert over chunks, then over experts); (C) each
+// block writes its chunk in order, 256 entries at a time: warp match-any
+// groups equal experts, their ranks by lane, per-warp counts in shared memory
+// order the warps.  Needs E <= 256 and chunk counts [ceil(TK/kSortChunk), E].
+constexpr int kSortChunk = 1024;
+
+__global__ void __launch_bounds__(256) permute_sort_kernel(PermuteArgs a, int32_t* hist) {
+  cg::grid_group grid = cg::this_grid();
+  __shared__ int s_h[256];
+  __shared__ int s_wc[8][256];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int E = a.E;
+  const int nc = static_cast<int>((a.TK + kSortChunk - 1) / kSortChunk);
+  for (int c = blockIdx.x; c < nc; c += gridDim.x) {  // (A)
+    for (int e = tid; e < E; e += 256) s_h[e] = 0;
+    __syncthreads();
+    const int64_t end = min(a.TK, static_cast<int64_t>(c + 1) * kSortChunk);
+    for (int64_t i = static_cast<int64_t>(c) * kSortChunk + tid; i < end; i += 256) {
+      const int v = a.idx[i] - a.id_base;
+      if (static_cast<unsigned>(v) < static_cast<unsigned>(E)) {
+        atomicAdd(&s_h[v], 1);
+      } else {
+        a.pair_row[i] = -1;
+        latch_status(a.status, kStatusDeviceCheck);
+      }
+    }
+    __syncthreads();
+    for (int e = tid; e < E; e += 256) hist[static_cast<int64_t>(c) * E + e] = s_h[e];
+    __syncthreads();
+  }
+  grid.sync();
+  if (blockIdx.x == 0) {  // (B)
+    int tot = 0;
+    if (tid < E) {
+      int c = 0;
+      for (; c + 8 <= nc; c += 8) {
+        int h[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) h[u] = hist[static_cast<int64_t>(c + u) * E + tid];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          hist[static_cast<int64_t>(c + u) * E + tid] = tot;
+          tot += h[u];
+        }
+      }
+      for (; c < nc; ++c) {
+        const int h = hist[static_cast<int64_t>(c) * E + tid];
+        hist[static_cast<int64_t>(c) * E + tid] = tot;
+        tot += h;
+      }
+    }
+    // exclusive scan of the totals over experts, in expert order
+    int incl = tot;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(kFull, incl, o);
+      if (lane >= o) incl += n;
+    }
+    if (lane == 31) s_wc[0][warp] = incl;
+    __syncthreads();
+    int woff = 0, all = 0;
+    for (int w = 0; w < 8; ++w) {
+      woff += w < warp ? s_wc[0][w] : 0;
+      all += s_wc[0][w];
+    }
+    const int off = woff + incl - tot;
+    if (tid < E) {
+      a.counts[tid] = tot;
+      a.offsets[tid] = off;
+      for (int c = 0; c < nc; ++c) hist[static_cast<int64_t>(c) * E + tid] += off;
+    }
+    if (tid == 0) a.offsets[E] = all;
+  }
+  grid.sync();
+  for (int e = tid; e < 256; e += 256)
+    for (int w = 0; w < 8; ++w) s_wc[w][e] = 0;
+  for (int c = blockIdx.x; c < nc; c += gridDim.x) {  // (C)
+    __syncthreads();
+    for (int e = tid; e < E; e += 256) s_h[e] = hist[static_cast<int64_t>(c) * E + e];
+    __syncthreads();
+    const int64_t end = min(a.TK, static_cast<int64_t>(c + 1) * kSortChunk);
+    for (int64_t sb = static_cast<int64_t>(c) * kSortChunk; sb < end; sb += 256) {
+      const int64_t i = sb + tid;
+      const int v = i < end ? a.idx[i] - a.id_base : -1;
+      const bool valid = static_cast<unsigned>(v) < static_cast<unsigned>(E);
+      const unsigned peers = __match_any_sync(kFull, valid ? v : (0x40000000 | lane));
+      const int rank = __popc(peers & ((1u << lane) - 1u));
+      if (valid && rank == 0) s_wc[warp][v] = __popc(peers);
+      __syncthreads();
+      int before = 0, total = 0;
+      if (valid) {
+        for (int w = 0; w < 8; ++w) {
+          const int x = s_wc[w][v];
+          before += w < warp ? x : 0;
+          total += x;
+        }
+        const int pos = s_h[v] + before + rank;
+        a.perm_src[pos] = static_cast<int>(i);
+        a.pair_row[i] = pos;
+        a.perm_w[pos] = a.w[i];
+      }
+      __syncthreads();
+      if (valid && before + rank + 1 == total) s_h[v] += total;
+      if (valid && rank == 0) s_wc[warp][v] = 0;
+      __syncthreads();
+    }
+  }
+}
+
 // ------------------------------------------------------------------ gather
 // x_perm[row] = x[token of row] for the larger token blocks; rows past the
 // last valid one are skipped.
@@ -412,7 +543,18 @@ __global__ void __launch_bounds__(128) gather_kernel(const uint16_t* __restrict_
   const int64_t t = perm_src[row] / k;
   const uint4* src = reinterpret_cast<const uint4*>(x + t * d);
   uint4* dst = reinterpret_cast<uint4*>(xp + row * d);
-  for (int i = threadIdx.x; i < d / 8; i += blockDim.x) dst[i] = src[i];
+  // all of a thread's loads are issued before its stores
+  constexpr int U = 8;
+  const int n8 = d / 8;
+  for (int base = threadIdx.x; base < n8; base += U * blockDim.x) {
+    uint4 r[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (base + u * blockDim.x < n8) r[u] = src[base + u * blockDim.x];
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (base + u * blockDim.x < n8) dst[base + u * blockDim.x] = r[u];
+  }
 }
 
 // ----------------------------------------------------------------- combine
@@ -663,6 +805,21 @@ void launch_ep_pack(const int32_t* idx, const int32_t* perm_src, const float* pe
   const int64_t blocks = TK > 0 ? (TK + 255) / 256 : 1;
   ep_pack_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
       idx, perm_src, perm_w, offsets, TK, E, n_ranks, send_expert, send_w, send_counts);
+}
+
+cudaError_t launch_permute_sort(const PermuteArgs& a, int32_t* hist, int num_sms, cudaStream_t s) {
+  static int per_sm = 0;
+  if (per_sm == 0 &&
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, permute_sort_kernel, 256, 0) !=
+          cudaSuccess)
+    return cudaErrorUnknown;
+  const int64_t nc = (a.TK + kSortChunk - 1) / kSortChunk;
+  const int64_t cap = static_cast<int64_t>(per_sm) * num_sms;
+  const int grid = static_cast<int>(nc < cap ? (nc > 0 ? nc : 1) : cap);
+  PermuteArgs a0 = a;
+  void* args[] = {&a0, &hist};
+  return cudaLaunchCooperativeKernel(reinterpret_cast<void*>(permute_sort_kernel), dim3(grid),
+                                     dim3(256), args, 0, s);
 }
 
 void launch_permute(const PermuteArgs& a, cudaStream_t s) {

@@ -76,6 +76,39 @@ def test_permutation_is_a_stable_counting_sort(tiny):
     assert np.array_equal(host(ws.view("perm_w", torch.float32, (TK,))), r["w"].reshape(-1)[order])
 
 
+@pytest.mark.parametrize("T,skew", [(1100, False), (2051, True)])
+def test_large_permutation_is_the_same_stable_sort(T, skew):
+    """From 8192 entries on the permutation is a counting sort over chunks of
+    1024 entries (ragged last chunk here); it must give the same stable
+    (expert, token, slot) order, also when a few experts take most rows."""
+    cfg = CFG.replace(T=T, seed=T)
+    t = inputs.generate(cfg, "cuda")
+    rng = np.random.default_rng(T)
+    E, k = cfg.n_experts, cfg.topk
+    p = rng.dirichlet(np.full(E, 0.05 if skew else 5.0))
+    idx = np.stack([rng.choice(E, k, replace=False, p=p) for _ in range(T)]).astype(np.int32)
+    w = rng.uniform(0.1, 0.5, (T, k)).astype(np.float32)
+    ws = pkg.Workspace(cfg, T)
+    out = pkg.forward_routed(cfg, t["hidden"], torch.from_numpy(idx).cuda(),
+                             torch.from_numpy(w).cuda(), t["w_gate"], t["w_up"], t["w_down"],
+                             ws=ws)
+    assert pkg.check_status(ws) == 0
+    TK = T * k
+    flat = idx.reshape(-1)
+    order = np.argsort(flat, kind="stable")
+    counts = np.bincount(flat, minlength=E)
+    assert np.array_equal(host(ws.view("counts", torch.int32, (E,))), counts)
+    assert np.array_equal(host(ws.view("offsets", torch.int32, (E + 1,))),
+                          np.concatenate([[0], np.cumsum(counts)]))
+    assert np.array_equal(host(ws.view("perm_src", torch.int32, (TK,))), order)
+    inv = np.empty(TK, np.int64)
+    inv[order] = np.arange(TK)
+    assert np.array_equal(host(ws.view("pair_row", torch.int32, (TK,))), inv)
+    assert np.array_equal(host(ws.view("perm_w", torch.float32, (TK,))), w.reshape(-1)[order])
+    rows = np.sort(rng.choice(T, 40, replace=False))
+    check_out(out, oracle_out(cfg, t, idx, w, tokens=rows), rows=rows)
+
+
 def test_deterministic_bitwise(tiny):
     t, _, _ = tiny
     args = (CFG, t["hidden"], t["router_w"], t["corr_bias"], t["w_gate"], t["w_up"], t["w_down"])
