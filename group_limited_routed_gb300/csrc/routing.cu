@@ -149,8 +149,11 @@ __device__ __forceinline__ void router_tile(const RouterArgs& a, int bx, int by,
 //     (score desc, group asc).
 //  4. expert e of a kept group takes slot r = the number of experts of kept
 //     groups that precede it in the order (c desc, expert asc); r < k selects
-//     it.  This ranking gives the same slots as k rounds of argmax.  The kept
-//     groups' scores are first packed into one array for vector loads.
+//     it.  This ranking gives the same slots as k rounds of argmax.  Only the
+//     top min(k, S) of each kept group (ranked inside the group by shuffles)
+//     can take a slot, and every expert preceding one of the k selected is
+//     itself selected, so ranking among those candidates gives the same
+//     slots; they are packed into one array for vector loads.
 //  5. weights: alpha * s / (sum of the k selected s in slot order), in FP64,
 //     rounded once to FP32.
 constexpr int kSelMaxG = 128;
@@ -210,21 +213,31 @@ __device__ __forceinline__ void select_token(const SelectArgs& a, int64_t t) {
     s_pos[e] = before < a.kg ? before : -1;
   }
   __syncthreads();
-  // the kept groups' choice scores, packed (any order: ties compare indices),
-  // padded to a multiple of four with entries that precede nothing
+  // expert rank inside its group, by shuffles over the group's S lanes
   const int pos = live ? s_pos[e / S] : -1;
-  const int n = a.kg * S;
+  const int seg = lane & ~(S - 1);
+  int lr = 0;
+  for (int j = 0; j < S; ++j) {
+    const float u = __shfl_sync(kFull, c, seg + j);
+    lr += (u > c || (u == c && seg + j < lane)) ? 1 : 0;
+  }
+  // the top min(k, S) of each kept group are the only candidates for the k
+  // slots, packed (any order: ties compare indices), padded to a multiple of
+  // four with entries that precede nothing
+  const int kk = a.k < S ? a.k : S;
+  const int n = a.kg * kk;
   const int n4 = (n + 3) & ~3;
-  if (pos >= 0) {
-    s_kc[pos * S + (e & (S - 1))] = c;
-    s_ke[pos * S + (e & (S - 1))] = e;
+  const bool cand = pos >= 0 && lr < kk;
+  if (cand) {
+    s_kc[pos * kk + lr] = c;
+    s_ke[pos * kk + lr] = e;
   }
   if (e >= n && e < n4) {
     s_kc[e] = -FLT_MAX;
     s_ke[e] = 1 << 30;
   }
   __syncthreads();
-  if (pos >= 0) {
+  if (cand) {
     int rank = 0;
     const float4* kc = reinterpret_cast<const float4*>(s_kc);
     const int4* ke = reinterpret_cast<const int4*>(s_ke);
