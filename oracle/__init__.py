@@ -65,6 +65,8 @@ def _load():
             getattr(lib, name).restype = ctypes.c_uint8
         lib.oracle_bf16_round.argtypes = [ctypes.c_float]
         lib.oracle_bf16_round.restype = ctypes.c_uint16
+        lib.oracle_f16_round.argtypes = [ctypes.c_double]
+        lib.oracle_f16_round.restype = ctypes.c_double
         lib.oracle_bf16_round_double.argtypes = [ctypes.c_double]
         lib.oracle_bf16_round_double.restype = ctypes.c_uint16
         lib.oracle_boundary.argtypes = [_P, _P, _P, _P, _I64, _I32, ctypes.c_double,
@@ -114,6 +116,11 @@ def e4m3_encode(v: float) -> int:
 
 def bf16_round(v: float) -> int:
     return int(_load().oracle_bf16_round(v))
+
+
+def f16_round(v: float) -> float:
+    """Nearest binary16 value (ties to even, subnormals, saturating at 65504)."""
+    return float(_load().oracle_f16_round(v))
 
 
 def bf16_round_double(v: float) -> int:
@@ -250,10 +257,18 @@ def experts_bf16(x_bf16, idx, w, wg, wu, wd, n_experts: int, tokens=None,
     return (out, ex) if exact else out
 
 
-def experts_nvfp4(x_bf16, idx, w, gate, up, down, n_experts: int, act_quant: bool = True,
+ACT_BF16, ACT_NVFP4, ACT_F16 = 0, 1, 2
+
+
+def experts_nvfp4(x_bf16, idx, w, gate, up, down, n_experts: int, act_quant=True,
                   tokens=None, out: np.ndarray | None = None, exact: bool = False):
     """NVFP4 experts.  gate/up/down are dicts with per-expert 'q' (packed
-    codes [N, K/2]), 'sf' (E4M3 codes [N, K/16]) and 'gs' (float32 [E])."""
+    codes [N, K/2]), 'sf' (E4M3 codes [N, K/16]) and 'gs' (float32 [E]).
+    act_quant: True / ACT_NVFP4 quantises both GEMM inputs to NVFP4, False /
+    ACT_BF16 keeps BF16 activations, ACT_F16 takes them in F16."""
+    mode = int(act_quant) if not isinstance(act_quant, bool) else int(act_quant)
+    if mode not in (ACT_BF16, ACT_NVFP4, ACT_F16):
+        raise ValueError(f"unknown activation mode {act_quant}")
     x = _c(x_bf16, np.uint16)
     T, d = x.shape
     idx = _c(idx, np.int32)
@@ -273,7 +288,7 @@ def experts_nvfp4(x_bf16, idx, w, gate, up, down, n_experts: int, act_quant: boo
     ex = np.zeros((T, d), np.float64) if exact else None
     tok = None if tokens is None else _c(tokens, np.int64)
     rc = _load().oracle_experts_nvfp4(_ptr(x), T, d, F, k, n_experts, _ptr(idx), _ptr(w),
-                                      *tabs, int(bool(act_quant)), _ptr(tok),
+                                      *tabs, mode, _ptr(tok),
                                       0 if tok is None else tok.size, _ptr(out), _ptr(ex))
     if rc:
         raise ValueError(f"oracle_experts_nvfp4 failed ({rc})")

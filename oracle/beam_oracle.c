@@ -62,6 +62,28 @@ static uint16_t bf16_round(float f) {
   return (uint16_t)keep;
 }
 
+/* Nearest IEEE binary16 value of a double, ties to even, with subnormals;
+ * magnitudes beyond the largest finite binary16 (65504) saturate to it.
+ * Written from the format: 11 significant bits, exponents -14..15, spacing
+ * 2^-24 below 2^-14. */
+static double f16_round_value(double v) {
+  if (v != v) return v;
+  const double a = fabs(v);
+  if (a >= 65504.0) return v < 0 ? -65504.0 : 65504.0;
+  if (a == 0.0) return v;
+  int e;
+  frexp(a, &e);                      /* a in [2^(e-1), 2^e) */
+  int q = e - 1 - 10;                /* spacing exponent for 11 significant bits */
+  if (q < -24) q = -24;              /* subnormal spacing */
+  const double step = ldexp(1.0, q);
+  double n = floor(a / step);        /* exact: a / step is a scaling by a power of two */
+  const double rest = a - n * step;
+  if (rest > step / 2 || (rest == step / 2 && fmod(n, 2.0) != 0.0)) n += 1.0;
+  double r = n * step;
+  if (r > 65504.0) r = 65504.0;
+  return v < 0 ? -r : r;
+}
+
 /* E2M1 (FP4): 1 sign bit, 2 exponent bits (bias 1), 1 mantissa bit.
  * Magnitudes of codes 0..7 written out from the format definition. */
 static double e2m1_value(uint8_t code) {
@@ -350,8 +372,11 @@ static int experts_impl(const uint16_t *x, int64_t T, int32_t d, int32_t F,
       for (int64_t i = 0; i < n; ++i) {
         int64_t t = tokens ? tokens[i] : i;
         const uint16_t *xr = x + t * (int64_t)d;
-        /* the expert input row (NVFP4 path may quantise it) */
-        if (W->fp4 && W->act_quant) {
+        /* the expert input row (NVFP4 path may quantise it, or take it in
+           F16 for the F16 tensor-core operands) */
+        if (W->fp4 && W->act_quant == 2) {
+          for (int32_t j = 0; j < d; ++j) xin[j] = f16_round_value(bf16_value(xr[j]));
+        } else if (W->fp4 && W->act_quant) {
           for (int32_t j = 0; j < d; ++j) tmp[j] = (float)bf16_value(xr[j]);
           for (int32_t j = 0; j < d; j += 16) nvfp4_block_roundtrip(tmp + j, xin + j);
         } else {
@@ -383,7 +408,9 @@ static int experts_impl(const uint16_t *x, int64_t T, int32_t d, int32_t F,
             hf[f] = (float)(silu * u);
           }
           /* the down GEMM's input */
-          if (W->fp4 && W->act_quant) {
+          if (W->fp4 && W->act_quant == 2) {
+            for (int32_t f = 0; f < F; ++f) hin[f] = f16_round_value((double)hf[f]);
+          } else if (W->fp4 && W->act_quant) {
             for (int32_t f = 0; f < F; f += 16) nvfp4_block_roundtrip(hf + f, hin + f);
           } else {
             for (int32_t f = 0; f < F; ++f) hin[f] = bf16_value(bf16_round(hf[f]));
@@ -434,7 +461,10 @@ int oracle_experts_bf16(const uint16_t *x, int64_t T, int32_t d, int32_t F,
  * quantises both GEMM inputs (x along d, the FP32 SwiGLU product along F) to
  * NVFP4 with the per-16 rule of nvfp4_block_roundtrip (the "quantization"
  * step of the NVFP4 MoE path, vLLM post, section "The fused graph");
- * act_quant = 0 keeps BF16 activations exactly as in the BF16 path. */
+ * act_quant = 0 keeps BF16 activations exactly as in the BF16 path;
+ * act_quant = 2 is the 16-bit-activation reading on F16 tensor-core operands
+ * [reading]: x rounded to F16 (exact inside F16's normal range) and the FP32
+ * SwiGLU product rounded to F16 instead of BF16, both saturating at 65504. */
 int oracle_experts_nvfp4(const uint16_t *x, int64_t T, int32_t d, int32_t F,
                          int32_t k, int32_t E, const int32_t *idx, const float *w,
                          const uint8_t *const *qg, const uint8_t *const *sfg, const float *gsg,
@@ -520,6 +550,7 @@ uint8_t oracle_e2m1_encode(float v) { return e2m1_encode(v); }
 uint8_t oracle_e4m3_encode(float v) { return e4m3_encode(v); }
 uint16_t oracle_bf16_round(float v) { return bf16_round(v); }
 uint16_t oracle_bf16_round_double(double v) { return bf16_round_double(v); }
+double oracle_f16_round(double v) { return f16_round_value(v); }
 
 /* NVFP4 activation quantiser on a row of n values (n % 16 == 0): packed codes
  * (low nibble = even index) and one E4M3 scale per 16. */

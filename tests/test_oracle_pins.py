@@ -450,3 +450,54 @@ def test_depth_scaled_residual_keeps_unit_variance():
         m = _rand_bf16((T, d), 5.0, seed=11 + n)
         h_out, _ = oracle.boundary(m, h, ones, ones, 1e-6, n)
         assert abs(_bf16_value(h_out).var() - 1.0) < 0.03
+
+
+# ------------------------------------------------ F16 activations (W4A16 path)
+def test_f16_round_matches_torch():
+    """binary32 values -> binary16 by torch (round to nearest even, with
+    subnormals) inside the finite range; beyond it the reading saturates."""
+    vals = np.concatenate([
+        RNG.standard_normal(20000).astype(np.float32) * np.float32(50.0),
+        RNG.standard_normal(3000).astype(np.float32) * np.float32(1e-6),   # subnormal range
+        # ties between neighbouring binary16 values at several exponents
+        (np.arange(1024, 1064, dtype=np.float32) + np.float32(0.5)) * np.float32(2.0 ** -10),
+        (np.arange(1, 40, dtype=np.float32) + np.float32(0.5)) * np.float32(2.0 ** -24),
+        np.array([0.0, -0.0, 65504.0, -65504.0, 65503.0, 6.1035156e-05], np.float32),
+    ])
+    got = np.array([oracle.f16_round(float(v)) for v in vals])
+    ref = torch.from_numpy(vals).to(torch.float16).double().numpy()
+    assert np.array_equal(got, ref)
+    for v, want in ((65519.0, 65504.0), (70000.0, 65504.0), (-1e9, -65504.0)):
+        assert oracle.f16_round(v) == want
+
+
+def test_f16_activation_experts_match_dense_torch():
+    """NVFP4 weights with F16 activations: the expert layer against a dense
+    torch FP64 restatement that rounds x and the SwiGLU product with torch's
+    own float16 casts."""
+    T, d, F, E = 5, 64, 32, 8
+    x = _bf16_matrix((T, d))
+    r = _route(RNG.standard_normal((T, E)), np.zeros(E), 4, 2, 3)
+    proj, deq = {}, {}
+    for name, (n, kk) in (("g", (F, d)), ("u", (F, d)), ("d", (d, F))):
+        q = RNG.integers(0, 256, (E, n, kk // 2), dtype=np.uint8)
+        sf = RNG.integers(0x20, 0x48, (E, n, kk // 16), dtype=np.uint8)
+        gs = (RNG.uniform(0.5, 2.0, E) * 2.0 ** -8).astype(np.float32)
+        proj[name] = dict(q=q, sf=sf, gs=gs)
+        codes = np.stack([q & 15, q >> 4], -1).reshape(E, n, kk)
+        deq[name] = torch.from_numpy(
+            np.vectorize(oracle.e2m1_value)(codes)
+            * np.repeat(np.vectorize(oracle.e4m3_value)(sf), 16, axis=2)
+            * gs.astype(np.float64)[:, None, None])
+    out, ex = oracle.experts_nvfp4(inputs.bf16_bits(x), r["idx"], r["w"], proj["g"], proj["u"],
+                                   proj["d"], E, act_quant=oracle.ACT_F16, exact=True)
+    x16 = x.to(torch.float16).double()
+    ref = torch.zeros(T, d, dtype=torch.float64)
+    for t in range(T):
+        for j in range(3):
+            e = int(r["idx"][t, j])
+            g = (x16[t] @ deq["g"][e].T).float().double()
+            u = (x16[t] @ deq["u"][e].T).float().double()
+            h = (g / (1 + torch.exp(-g)) * u).float().to(torch.float16).double()
+            ref[t] += float(r["w"][t, j]) * (h @ deq["d"][e].T)
+    assert np.allclose(ex, ref.numpy(), rtol=1e-12, atol=1e-12)
