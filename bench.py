@@ -154,7 +154,7 @@ def traffic_for(kernel: str, workload: str):
 
 
 # ------------------------------------------------------------------ CPU oracle
-def oracle_sample(cfg, t, n_tokens: int, seed: int = 0):
+def oracle_sample(cfg, t, n_tokens: int, seed: int = 0, a16: bool = False):
     """Runs the CPU oracle (router + selection for the whole batch, experts
     and combine for n_tokens sampled tokens); returns (seconds, sampled)."""
     import oracle
@@ -177,27 +177,28 @@ def oracle_sample(cfg, t, n_tokens: int, seed: int = 0):
     lg = oracle.router_logits(x[rows], wr)
     r = oracle.route(lg, b, cfg.n_groups, cfg.topk_groups, cfg.topk, cfg.routed_scale)
     if cfg.weight_fmt == "nvfp4":
-        oracle.experts_nvfp4(x[rows], r["idx"], r["w"], *proj, cfg.n_experts, act_quant=True)
+        oracle.experts_nvfp4(x[rows], r["idx"], r["w"], *proj, cfg.n_experts,
+                             act_quant=oracle.ACT_F16 if a16 else oracle.ACT_NVFP4)
     else:
         oracle.experts_bf16(x[rows], r["idx"], r["w"], *proj, cfg.n_experts)
     return time.perf_counter() - t0, len(rows)
 
 
-def cpu_baseline(cfg, t, budget_s: float = 12.0) -> dict:
+def cpu_baseline(cfg, t, budget_s: float = 12.0, a16: bool = False) -> dict:
     """The oracle on about budget_s seconds of the same workload: sampled
     tokens of the batch, or the whole batch repeated when it is quicker."""
     import oracle
-    sec1, n1 = oracle_sample(cfg, t, 1, seed=1)
+    sec1, n1 = oracle_sample(cfg, t, 1, seed=1, a16=a16)
     per_tok = sec1 / n1
     n = int(max(1, min(cfg.T, budget_s / max(per_tok, 1e-6))))
     reps = 1
     if n == cfg.T:
-        full, _ = oracle_sample(cfg, t, cfg.T, seed=2)
+        full, _ = oracle_sample(cfg, t, cfg.T, seed=2, a16=a16)
         reps = int(max(1, min(100, budget_s / max(full, 1e-6))))
     sec = 0.0
     toks = 0
     for r in range(reps):
-        s, m = oracle_sample(cfg, t, n, seed=2 + r)
+        s, m = oracle_sample(cfg, t, n, seed=2 + r, a16=a16)
         sec += s
         toks += m
     what = (f"the whole {cfg.T}-token {cfg.name} batch, {reps} times" if n == cfg.T
@@ -217,7 +218,7 @@ def run_reference(args, cfg):
     gen_cfg = cfg if dev.type == "cuda" else cfg.replace(cpu_generator=True)
     t = inputs.generate(gen_cfg, dev)
     # size each step so the whole run stays within about two minutes
-    sec1, _ = oracle_sample(cfg, t, 1, seed=1)
+    sec1, _ = oracle_sample(cfg, t, 1, seed=1, a16=a16)
     per_step_budget = 120.0 / max(1, args.steps + args.warmup)
     n = int(max(1, min(cfg.T, per_step_budget / max(sec1, 1e-6))))
     for i in range(args.warmup):
@@ -242,7 +243,7 @@ def run_reference(args, cfg):
     return 0
 
 
-def config_record(cfg, touched, routed=False):
+def config_record(cfg, touched, routed=False, a16=False):
     rec = {"workload": cfg.description, "T": cfg.T, "d": cfg.d, "n_experts": cfg.n_experts,
            "n_groups": cfg.n_groups, "topk_groups": cfg.topk_groups, "topk": cfg.topk,
            "d_ff": cfg.d_ff, "routed_scale": cfg.routed_scale, "weights": cfg.weight_fmt,
@@ -253,6 +254,8 @@ def config_record(cfg, touched, routed=False):
         rec["touched_experts"] = touched
     if routed:
         rec["routing"] = "replayed (recorded once; steps run experts + combine)"
+    if a16:
+        rec["activations"] = "f16 (not quantised): W4A16"
     return rec
 
 
@@ -266,15 +269,17 @@ def run_gpu(args, cfg):
         dist.init_process_group("nccl", device_id=dev)
     t = inputs.generate(cfg.replace(seed=cfg.seed + 1000 * rank) if rank else cfg, dev)
     fp4 = cfg.weight_fmt == "nvfp4"
-    ws = pkg.Workspace(cfg, cfg.T, dev, weight_fmt=pkg.NVFP4 if fp4 else 0)
+    a16 = fp4 and args.a16
+    fmt = (pkg.NVFP4_A16 if a16 else pkg.NVFP4) if fp4 else 0
+    ws = pkg.Workspace(cfg, cfg.T, dev, weight_fmt=fmt)
     stream = torch.cuda.current_stream()
     out = torch.empty(cfg.T, cfg.d, dtype=torch.bfloat16, device=dev)
     if fp4:
         wts = [pkg.Fp4Weight.of(t[n]) for n in ("w_gate", "w_up", "w_down")]
+        fwd = pkg.forward_nvfp4_a16 if a16 else pkg.forward_nvfp4
 
         def layer(x, o):
-            return pkg.forward_nvfp4(cfg, x, t["router_w"], t["corr_bias"], *wts, out=o, ws=ws,
-                                     stream=stream)
+            return fwd(cfg, x, t["router_w"], t["corr_bias"], *wts, out=o, ws=ws, stream=stream)
     elif args.routed:
         # routing replay: the routes are recorded once, the timed steps run
         # the experts and the combine on them
@@ -361,7 +366,7 @@ def run_gpu(args, cfg):
     pk = peaks()
     # weight bytes of one projection of one expert: BF16, or E2M1 + E4M3 per 16
     E_b = cfg.d * cfg.d_ff * 2 if not fp4 else cfg.d * cfg.d_ff // 2 + cfg.d * cfg.d_ff // 16
-    tok_b = 2 if not fp4 else 0.5625
+    tok_b = 2 if (not fp4 or a16) else 0.5625
     gu_bytes = touched * 2 * E_b + cfg.T * cfg.topk * (cfg.d + cfg.d_ff) * tok_b
     gu_gbs = gu_bytes / (stage_ms[4] / 1e3) / 1e9
     layer_bytes = touched * 3 * E_b + cfg.n_experts * cfg.d * 4 + cfg.n_experts * 4 \
@@ -372,8 +377,9 @@ def run_gpu(args, cfg):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": layer_ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
-        "dtype": "nvfp4 (e2m1 x e4m3 per 16)" if fp4 else "bf16", "data": "synthetic",
-        "config": config_record(cfg, touched, args.routed),
+        "dtype": ("nvfp4 weights x f16 activations" if a16 else "nvfp4 (e2m1 x e4m3 per 16)")
+        if fp4 else "bf16", "data": "synthetic",
+        "config": config_record(cfg, touched, args.routed, a16),
         "roofline": {"bound": "hbm", "kernel": DOMINANT, "achieved": gu_gbs,
                      "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": gu_gbs / pk["hbm_gbs"],
                      "peak_source": pk["source"],
@@ -388,11 +394,11 @@ def run_gpu(args, cfg):
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": cfg.T * cfg.d * 2,
                 "d2h_bytes_per_step": cfg.T * cfg.d * 2},
         "gpu_launches": args.steps * pkg.kernels_per_forward(
-            cfg, cfg.T, pkg.NVFP4 if fp4 else 0, args.routed),
+            cfg, cfg.T, fmt, args.routed),
         "clocks": clocks,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.routed:
-        line["cpu_baseline"] = cpu_baseline(cfg, t)
+        line["cpu_baseline"] = cpu_baseline(cfg, t, a16=a16)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if use_dist:
@@ -408,6 +414,8 @@ def main(argv=None):
     ap.add_argument("--config", default="decode", choices=sorted(inputs.CONFIGS))
     ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--a16", action="store_true",
+                    help="NVFP4 configs: 16-bit activations (beam_moe_forward_nvfp4_a16)")
     ap.add_argument("--routed", action="store_true",
                     help="time beam_moe_forward_routed on recorded routes (routing replay)")
     args = ap.parse_args(argv)

@@ -15,7 +15,8 @@ def __getattr__(name):
                 "check_status", "BeamError", "library_path", "lib", "set_stage_events",
                 "set_debug", "layout", "kernels_per_forward", "EXPORTS", "forward_noalloc",
                 "forward_nvfp4", "pack_scales", "Fp4Weight", "NVFP4", "ep_dispatch",
-                "ep_experts", "ep_combine", "EpWorkspace", "forward_boundary"):
+                "ep_experts", "ep_combine", "EpWorkspace", "forward_boundary",
+                "forward_nvfp4_a16", "NVFP4_A16"):
         from . import api
         return getattr(api, name)
     raise AttributeError(name)

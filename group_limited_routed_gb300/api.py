@@ -34,7 +34,7 @@ EXPORTS = ("beam_moe_workspace_size", "beam_moe_workspace_layout", "beam_moe_rou
            "beam_moe_check_status", "beam_moe_set_stage_events", "beam_moe_set_debug",
            "beam_moe_kernels_per_forward", "beam_status_string", "beam_moe_ep_dispatch",
            "beam_moe_ep_workspace_size", "beam_moe_ep_experts", "beam_moe_ep_combine",
-           "beam_moe_forward_boundary")
+           "beam_moe_forward_boundary", "beam_moe_forward_nvfp4_a16")
 
 
 class BeamError(RuntimeError):
@@ -93,6 +93,9 @@ def lib():
         L.beam_moe_forward_nvfp4.argtypes = [cfgp, _P, _P, _P, fp4p, fp4p, fp4p, _P, _I64, _P,
                                              _SZ, _P]
         L.beam_moe_forward_nvfp4.restype = _ST
+        L.beam_moe_forward_nvfp4_a16.argtypes = [cfgp, _P, _P, _P, fp4p, fp4p, fp4p, _P, _I64,
+                                                 _P, _SZ, _P]
+        L.beam_moe_forward_nvfp4_a16.restype = _ST
         L.beam_moe_nvfp4_pack_scales.argtypes = [_P, _I64, _I64, _P, _P]
         L.beam_moe_nvfp4_pack_scales.restype = _ST
         L.beam_moe_check_status.argtypes = [_P, _P]
@@ -318,6 +321,7 @@ def forward_noalloc(cfg, hidden, router_w, corr_bias, w_gate, w_up, w_down, out=
 
 
 NVFP4 = 1
+NVFP4_A16 = 2
 
 
 def pack_scales(sf: torch.Tensor, stream=None) -> torch.Tensor:
@@ -363,6 +367,24 @@ def forward_nvfp4(cfg, hidden, router_w, corr_bias, gate: Fp4Weight, up: Fp4Weig
                                         ctypes.byref(gate._c), ctypes.byref(up._c),
                                         ctypes.byref(down._c), o.data_ptr(), T, ws.ptr, ws.nbytes,
                                         _stream(stream)), "beam_moe_forward_nvfp4")
+    return o
+
+
+def forward_nvfp4_a16(cfg, hidden, router_w, corr_bias, gate: Fp4Weight, up: Fp4Weight,
+                      down: Fp4Weight, out=None, ws: Workspace | None = None, stream=None):
+    """The whole layer with NVFP4 expert weights and 16-bit (F16) activations."""
+    T = hidden.shape[0]
+    if ws is None:
+        ws = Workspace(cfg, max(int(T), 1), hidden.device, weight_fmt=NVFP4_A16)
+    o = torch.empty(T, cfg.d, dtype=torch.bfloat16, device=hidden.device) if out is None else out
+    c = _cfg(cfg)
+    _check(lib().beam_moe_forward_nvfp4_a16(ctypes.byref(c), _dev(hidden, torch.bfloat16, "hidden"),
+                                            _dev(router_w, torch.float32, "router_w"),
+                                            _dev(corr_bias, torch.float32, "corr_bias"),
+                                            ctypes.byref(gate._c), ctypes.byref(up._c),
+                                            ctypes.byref(down._c), o.data_ptr(), T, ws.ptr,
+                                            ws.nbytes, _stream(stream)),
+           "beam_moe_forward_nvfp4_a16")
     return o
 
 

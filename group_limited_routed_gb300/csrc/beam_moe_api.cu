@@ -161,6 +161,7 @@ int fp4_tile(const beam_moe_config_t& c, int64_t TK) { return small_batch(c, TK)
 
 Layout make_layout(const beam_moe_config_t& c, int64_t T_max, int32_t fmt = BEAM_WEIGHTS_BF16) {
   const bool fp4 = fmt == BEAM_WEIGHTS_NVFP4;
+  const bool a16 = fmt == BEAM_WEIGHTS_NVFP4_A16;  // F16 token rows gathered into x_perm
   const int64_t E = c.n_experts, k = c.topk;
   const int64_t TK = T_max * k;
   const int64_t rows = std::max<int64_t>(TK, kMinRows);
@@ -186,7 +187,7 @@ Layout make_layout(const beam_moe_config_t& c, int64_t T_max, int32_t fmt = BEAM
   L.perm_src = take(static_cast<size_t>(TK) * 4);
   L.pair_row = take(static_cast<size_t>(TK) * 4);
   L.perm_w = take(static_cast<size_t>(TK) * 4);
-  L.x_perm = take(fp4 || small_batch(c, TK) ? 0 : static_cast<size_t>(rows) * c.d * 2);
+  L.x_perm = take(!a16 && (fp4 || small_batch(c, TK)) ? 0 : static_cast<size_t>(rows) * c.d * 2);
   L.h = take(fp4 ? 0 : static_cast<size_t>(rows) * c.d_ff * 2);
   L.y = take(static_cast<size_t>(rows) * c.d * 4);
   L.router_planes = take(T_max >= kTensorRouterMinT ? static_cast<size_t>(E) * 3 * c.d * 2 : 0);
@@ -217,7 +218,8 @@ beam_status_t common_checks(const beam_moe_config_t* cfg, int64_t T, void* ws, s
                             Layout* L, DevInfo* dev, bool* empty,
                             int32_t fmt = BEAM_WEIGHTS_BF16) {
   if (!valid_cfg(cfg) || T < 0 || T > (int64_t(1) << 31) / 64) return BEAM_ERR_INVALID_ARG;
-  if (fmt == BEAM_WEIGHTS_NVFP4 && (cfg->d % 256 || cfg->d_ff % 256)) return BEAM_ERR_INVALID_ARG;
+  if ((fmt == BEAM_WEIGHTS_NVFP4 || fmt == BEAM_WEIGHTS_NVFP4_A16) && (cfg->d % 256 || cfg->d_ff % 256))
+    return BEAM_ERR_INVALID_ARG;
   *empty = (T == 0);
   if (*empty) return BEAM_OK;
   if (!aligned16(ws)) return BEAM_ERR_INVALID_ARG;
@@ -501,6 +503,80 @@ beam_status_t run_experts_nvfp4(const beam_moe_config_t& c, const void* hidden, 
   return cuda_status(cudaGetLastError());
 }
 
+// permute + F16 token rows + W4A16 gate/up (F16 h) + W4A16 down + combine
+beam_status_t run_experts_w4a16(const beam_moe_config_t& c, const void* hidden, const int32_t* idx,
+                                const float* w, const beam_fp4_weight_t& gate,
+                                const beam_fp4_weight_t& up, const beam_fp4_weight_t& down,
+                                void* out, int64_t T, void* ws, const Layout& L,
+                                const DevInfo& dev, cudaStream_t s, bool permuted = false) {
+  const int64_t TK = T * c.topk;
+  const int64_t rows = std::max<int64_t>(TK, kMinRows);
+  const int nt = fp4_tile(c, TK);
+  const beam::PermuteArgs pa = permute_args(c, idx, w, T, ws, L);
+  if (!permuted) {
+    if (launch_permutation(pa, ws, L, dev, s) != BEAM_OK) return BEAM_ERR_CUDA;
+    record(3, s);
+  }
+  uint16_t* x16 = at<uint16_t>(ws, L.x_perm);
+  uint16_t* h16 = at<uint16_t>(ws, L.h);
+  float* y = at<float>(ws, L.y);
+  beam::launch_gather_f16(static_cast<const uint16_t*>(hidden), pa.perm_src,
+                          pa.offsets + c.n_experts, TK, c.topk, c.d, x16, s);
+  record(4, s);
+  if (cudaGetLastError() != cudaSuccess) return BEAM_ERR_CUDA;
+
+  const int64_t EF = static_cast<int64_t>(c.n_experts) * c.d_ff;
+  const int64_t ED = static_cast<int64_t>(c.n_experts) * c.d;
+  CUtensorMap tm_g, tm_u, tm_d, tm_x, tm_h;
+  if (!tmap_u8(&tm_g, gate.q, EF, c.d / 2, 128, 128) ||
+      !tmap_u8(&tm_u, up.q, EF, c.d / 2, 128, 128) ||
+      !tmap_u8(&tm_d, down.q, ED, c.d_ff / 2, 128, 128) || !tmap_bf16(&tm_x, x16, rows, c.d, nt) ||
+      !tmap_bf16(&tm_h, h16, rows, c.d_ff, nt))
+    return BEAM_ERR_CUDA;
+  beam::W4a16GemmArgs ga{};
+  ga.counts = pa.counts;
+  ga.offsets = pa.offsets;
+  ga.perm_w = pa.perm_w;
+  ga.E = c.n_experts;
+  ga.status = at<uint32_t>(ws, L.status);
+  ga.wait_limit_ns = g_wait_ns;
+  ga.weight_evict_first = small_batch(c, TK) ? 1 : 0;
+  auto grid_for = [&](int m_blocks) {
+    const int64_t tiles = static_cast<int64_t>(m_blocks) * (c.n_experts + (TK + nt - 1) / nt);
+    return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(dev.sms, tiles)));
+  };
+  ga.sfa0 = gate.sf;
+  ga.sfa1 = up.sf;
+  ga.gs0 = gate.global_scale;
+  ga.gs1 = up.global_scale;
+  ga.h_out = h16;
+  ga.out_ld = c.d_ff;
+  ga.rows_per_expert = c.d_ff;
+  ga.m_blocks = c.d_ff / 128;
+  ga.k_blocks = c.d / 256;
+  if (beam::launch_w4a16_gemm(true, nt, tm_g, tm_u, tm_x, ga, grid_for(ga.m_blocks), s) !=
+      cudaSuccess)
+    return BEAM_ERR_CUDA;
+  record(5, s);
+  ga.sfa0 = down.sf;
+  ga.sfa1 = nullptr;
+  ga.gs0 = down.global_scale;
+  ga.gs1 = nullptr;
+  ga.h_out = nullptr;
+  ga.y_out = y;
+  ga.out_ld = c.d;
+  ga.rows_per_expert = c.d;
+  ga.m_blocks = c.d / 128;
+  ga.k_blocks = c.d_ff / 256;
+  if (beam::launch_w4a16_gemm(false, nt, tm_d, tm_d, tm_h, ga, grid_for(ga.m_blocks), s) !=
+      cudaSuccess)
+    return BEAM_ERR_CUDA;
+  record(6, s);
+  beam::launch_combine(y, pa.pair_row, T, c.topk, c.d, static_cast<uint16_t*>(out), s);
+  record(7, s);
+  return cuda_status(cudaGetLastError());
+}
+
 bool valid_fp4_weight(const beam_fp4_weight_t* w) {
   return w && aligned16(w->q) && aligned16(w->sf) && aligned16(w->global_scale);
 }
@@ -535,14 +611,17 @@ extern "C" {
 
 size_t beam_moe_workspace_size(const beam_moe_config_t* cfg, int64_t T_max, int32_t weight_fmt) {
   if (!valid_cfg(cfg) || T_max < 0) return 0;
-  if (weight_fmt != BEAM_WEIGHTS_BF16 && weight_fmt != BEAM_WEIGHTS_NVFP4) return 0;
+  if (weight_fmt != BEAM_WEIGHTS_BF16 && weight_fmt != BEAM_WEIGHTS_NVFP4 &&
+      weight_fmt != BEAM_WEIGHTS_NVFP4_A16)
+    return 0;
   return make_layout(*cfg, T_max, weight_fmt).total;
 }
 
 beam_status_t beam_moe_workspace_layout(const beam_moe_config_t* cfg, int64_t T_max,
                                         int32_t weight_fmt, beam_moe_ws_layout_t* out) {
   if (!out || !valid_cfg(cfg) || T_max < 0 ||
-      (weight_fmt != BEAM_WEIGHTS_BF16 && weight_fmt != BEAM_WEIGHTS_NVFP4))
+      (weight_fmt != BEAM_WEIGHTS_BF16 && weight_fmt != BEAM_WEIGHTS_NVFP4 &&
+       weight_fmt != BEAM_WEIGHTS_NVFP4_A16))
     return BEAM_ERR_INVALID_ARG;
   const Layout L = make_layout(*cfg, T_max, weight_fmt);
   out->status = L.status;
@@ -754,6 +833,34 @@ beam_status_t beam_moe_forward_nvfp4(const beam_moe_config_t* cfg, const void* h
                            permuted);
 }
 
+beam_status_t beam_moe_forward_nvfp4_a16(const beam_moe_config_t* cfg, const void* hidden,
+                                         const float* router_w, const float* corr_bias,
+                                         const beam_fp4_weight_t* gate, const beam_fp4_weight_t* up,
+                                         const beam_fp4_weight_t* down, void* out, int64_t T,
+                                         void* workspace, size_t ws_bytes, void* stream) {
+  Layout L;
+  DevInfo dev;
+  bool empty = false;
+  beam_status_t st = common_checks(cfg, T, workspace, ws_bytes, &L, &dev, &empty,
+                                   BEAM_WEIGHTS_NVFP4_A16);
+  if (st != BEAM_OK || empty) return st;
+  if (!aligned16(hidden) || !aligned16(router_w) || !aligned16(corr_bias) ||
+      !valid_fp4_weight(gate) || !valid_fp4_weight(up) || !valid_fp4_weight(down) ||
+      !aligned16(out))
+    return BEAM_ERR_INVALID_ARG;
+  if (!encoder()) return BEAM_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  record(0, s);
+  int32_t* idx = at<int32_t>(workspace, L.idx);
+  float* w = at<float>(workspace, L.w);
+  bool permuted = false;
+  st = run_route(*cfg, hidden, router_w, corr_bias, T, idx, w, at<float>(workspace, L.logits),
+                 workspace, L, dev, s, &permuted);
+  if (st != BEAM_OK) return st;
+  return run_experts_w4a16(*cfg, hidden, idx, w, *gate, *up, *down, out, T, workspace, L, dev, s,
+                           permuted);
+}
+
 // ------------------------------------------------------- expert parallelism
 namespace {
 
@@ -894,12 +1001,14 @@ beam_status_t beam_moe_set_debug(uint32_t wait_limit_us, int32_t withhold_first_
 int32_t beam_moe_kernels_per_forward(const beam_moe_config_t* cfg, int64_t T, int32_t weight_fmt,
                                      int32_t routed) {
   if (!valid_cfg(cfg) || T <= 0) return 0;
-  if (weight_fmt != BEAM_WEIGHTS_BF16 && weight_fmt != BEAM_WEIGHTS_NVFP4) return 0;
+  if (weight_fmt != BEAM_WEIGHTS_BF16 && weight_fmt != BEAM_WEIGHTS_NVFP4 &&
+      weight_fmt != BEAM_WEIGHTS_NVFP4_A16)
+    return 0;
   if (routed && weight_fmt != BEAM_WEIGHTS_BF16) return 0;
   // experts: permute, gather (BF16, larger batches) or row quantisation
   // (NVFP4), gate/up, down, combine
   const bool small = small_batch(*cfg, T * cfg->topk);
-  const int experts = weight_fmt == BEAM_WEIGHTS_NVFP4 ? 5 : 4 + (small ? 0 : 1);
+  const int experts = weight_fmt != BEAM_WEIGHTS_BF16 ? 5 : 4 + (small ? 0 : 1);
   if (routed) return experts;
   // routing: router (+ plane split), select; decode-sized batches run router,
   // select and permute as one launch

@@ -119,6 +119,35 @@ struct Fp4GemmArgs {
   uint64_t wait_limit_ns;
 };
 
+// ---------------------------------------------------------------- W4A16
+struct W4a16GemmArgs {
+  const int32_t* counts;
+  const int32_t* offsets;
+  const float* perm_w;     // [rows] routing weight (down)
+  const uint8_t* sfa0;     // blocked E4M3 weight scales (gate or down)
+  const uint8_t* sfa1;     // blocked E4M3 weight scales (up)
+  const float* gs0;        // [E] FP32 scale (gate or down)
+  const float* gs1;        // [E] FP32 scale (up)
+  uint16_t* h_out;         // gate/up out: h [rows, F] F16
+  float* y_out;            // down out: [rows, d] FP32
+  int32_t out_ld;          // elements per output row
+  int32_t E;
+  int32_t rows_per_expert;
+  int32_t m_blocks;
+  int32_t k_blocks;        // K / 256
+  int32_t weight_evict_first;
+  uint32_t* status;
+  uint64_t wait_limit_ns;
+};
+// permuted token rows -> F16 [rows, d] (saturating at 65504)
+void launch_gather_f16(const uint16_t* x, const int32_t* perm_src, const int32_t* n_valid,
+                       int64_t TK, int32_t k, int32_t d, uint16_t* x16, cudaStream_t s);
+// NVFP4 weights x F16 activations grouped GEMM, nt = 16 | 32; b maps F16 rows
+// (box 64 x nt, 128-byte swizzle)
+cudaError_t launch_w4a16_gemm(bool gateup, int nt, const CUtensorMap& a0, const CUtensorMap& a1,
+                              const CUtensorMap& b, const W4a16GemmArgs& p, int grid,
+                              cudaStream_t s);
+
 // [rows, S] row-major E4M3 scales -> 128-row x 4-scale blocks (see nvfp4.cu)
 void launch_pack_scales(const uint8_t* src, int64_t rows, int64_t S, uint8_t* dst, cudaStream_t s);
 // permuted token rows -> NVFP4 codes [rows, d/2] and scales [rows, d/4]

@@ -87,6 +87,7 @@ typedef struct {
 /* Weight formats for beam_moe_workspace_size. */
 #define BEAM_WEIGHTS_BF16 0
 #define BEAM_WEIGHTS_NVFP4 1
+#define BEAM_WEIGHTS_NVFP4_A16 2 /* NVFP4 weights, 16-bit activations */
 
 /* Bytes of device workspace a call with up to T_max tokens needs (256-byte
  * aligned).  Returns 0 for an invalid configuration. */
@@ -249,6 +250,21 @@ beam_status_t beam_moe_forward_nvfp4(const beam_moe_config_t *cfg, const void *h
                                      const beam_fp4_weight_t *down, void *out, int64_t T,
                                      void *workspace, size_t ws_bytes, void *stream);
 
+/* The whole layer with the same NVFP4 expert weights and unquantised 16-bit
+ * activations (W4A16).  The tensor cores take F16 operands: each weight is
+ * E2M1 code x E4M3 scale, exact in F16 (expanded in registers and stored into
+ * tensor memory), times the FP32 expert scale in the epilogue; the token
+ * rows are converted from BF16 to F16 (exact inside F16's normal range), and
+ * the FP32 SwiGLU product is rounded to F16 for the down GEMM; magnitudes
+ * beyond 65504 saturate.  Otherwise as beam_moe_forward_nvfp4 (d % 256 == 0,
+ * d_ff % 256 == 0).  Workspace: beam_moe_workspace_size(cfg, T,
+ * BEAM_WEIGHTS_NVFP4_A16). */
+beam_status_t beam_moe_forward_nvfp4_a16(const beam_moe_config_t *cfg, const void *hidden,
+                                         const float *router_w, const float *corr_bias,
+                                         const beam_fp4_weight_t *gate, const beam_fp4_weight_t *up,
+                                         const beam_fp4_weight_t *down, void *out, int64_t T,
+                                         void *workspace, size_t ws_bytes, void *stream);
+
 /* ---------------------------------------------------- expert parallelism
  * Expert parallelism over n_ranks ranks ("SGLang 原生支持 Reflection 的 Beam
  * 并驱动其生产 API", section "Fusion Optimizations", the MegaMoE item and the
@@ -333,7 +349,8 @@ beam_status_t beam_moe_set_debug(uint32_t wait_limit_us, int32_t withhold_first_
 
 /* Number of kernels one call of T tokens launches (for accounting):
  * beam_moe_forward (and beam_moe_forward_noalloc) for weight_fmt
- * BEAM_WEIGHTS_BF16, beam_moe_forward_nvfp4 for BEAM_WEIGHTS_NVFP4, and with
+ * BEAM_WEIGHTS_BF16, beam_moe_forward_nvfp4 for BEAM_WEIGHTS_NVFP4,
+ * beam_moe_forward_nvfp4_a16 for BEAM_WEIGHTS_NVFP4_A16, and with
  * routed != 0 beam_moe_forward_routed (BF16 only).  Returns 0 for an invalid
  * configuration, T <= 0 or an unknown combination.  Host-only. */
 int32_t beam_moe_kernels_per_forward(const beam_moe_config_t *cfg, int64_t T, int32_t weight_fmt,

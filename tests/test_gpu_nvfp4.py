@@ -123,3 +123,51 @@ def test_nvfp4_beam_workload():
     rows = rows[~exempt_tokens(r)[rows]]
     err, rms, same = check_out(out, _oracle_fp4(cfg, t, r, tokens=rows), rows=rows, tol=FP4_TOL)
     print(f"nvfp4 beam: {len(rows)} tokens, max|err| {err:.3e}, RMS {rms:.3e}")
+
+
+# ----------------------------------------------- W4A16 (NVFP4 weights, F16 activations)
+A16_TOL = 1e-2
+
+
+def _oracle_a16(cfg, t, r, tokens=None):
+    rows = np.arange(cfg.T) if tokens is None else np.asarray(tokens)
+    need = sorted({int(e) for e in r["idx"][rows].reshape(-1)})
+    proj = {}
+    for n in ("w_gate", "w_up", "w_down"):
+        proj[n] = {"q": {e: host(t[n]["q"][e]) for e in need},
+                   "sf": {e: host(t[n]["sf"][e]) for e in need},
+                   "gs": host(t[n]["gs"])}
+    return oracle.experts_nvfp4(host(t["hidden"]), r["idx"], r["w"], proj["w_gate"], proj["w_up"],
+                                proj["w_down"], cfg.n_experts, act_quant=oracle.ACT_F16,
+                                tokens=None if tokens is None else rows, exact=True)
+
+
+@pytest.mark.parametrize("T", [64, 1, 37, 300])
+def test_w4a16_forward_matches_oracle(T):
+    """16 and 32-row token blocks (300 tokens); the BF16 output tolerance:
+    activations are not quantised."""
+    cfg = TINY.replace(T=T, seed=80 + T)
+    t = _to(inputs.generate(cfg.replace(cpu_generator=True), "cpu"), "cuda")
+    lg, r = oracle_route(cfg, t)
+    ws = pkg.Workspace(cfg, cfg.T, weight_fmt=pkg.NVFP4_A16)
+    out = pkg.forward_nvfp4_a16(cfg, t["hidden"], t["router_w"], t["corr_bias"], *_weights(t),
+                                ws=ws)
+    assert pkg.check_status(ws) == 0
+    rows = np.nonzero(~exempt_tokens(r))[0][:64]
+    err, rms, same = check_out(out, _oracle_a16(cfg, t, r, tokens=rows), rows=rows, tol=A16_TOL)
+    print(f"w4a16 T={T}: max|err| {err:.3e}, RMS {rms:.3e}, identical {same:.3f}")
+
+
+def test_w4a16_beam_workload():
+    cfg = inputs.CONFIGS["nvfp4"]
+    t = inputs.generate(cfg, "cuda")
+    lg, r = oracle_route(cfg, t)
+    ws = pkg.Workspace(cfg, cfg.T, weight_fmt=pkg.NVFP4_A16)
+    out = pkg.forward_nvfp4_a16(cfg, t["hidden"], t["router_w"], t["corr_bias"], *_weights(t),
+                                ws=ws)
+    assert pkg.check_status(ws) == 0
+    rng = np.random.default_rng(11)
+    rows = np.sort(rng.choice(cfg.T, 12, replace=False))
+    rows = rows[~exempt_tokens(r)[rows]]
+    err, rms, same = check_out(out, _oracle_a16(cfg, t, r, tokens=rows), rows=rows, tol=A16_TOL)
+    print(f"w4a16 beam: {len(rows)} tokens, max|err| {err:.3e}, RMS {rms:.3e}")
