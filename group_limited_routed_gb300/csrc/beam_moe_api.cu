@@ -492,7 +492,7 @@ beam_status_t run_experts_nvfp4(const beam_moe_config_t& c, const void* hidden, 
   fa.y = y;
   fa.out_ld = c.d;
   fa.rows_per_expert = c.d;
-  fa.m_blocks = c.d / 128;
+  fa.m_blocks = c.d / 256;  // pairs of 128-row weight blocks
   fa.k_blocks = c.d_ff / 256;
   if (beam::launch_fp4_gemm(false, nt, tm_d, tm_d, tm_h, tm_hsf, fa, grid_for(fa.m_blocks), s) !=
       cudaSuccess)

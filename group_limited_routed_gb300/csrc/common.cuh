@@ -155,7 +155,8 @@ void launch_pack_scales(const uint8_t* src, int64_t rows, int64_t S, uint8_t* ds
 void launch_quantize_rows(const uint16_t* x, const int32_t* perm_src, const int32_t* n_valid,
                           int64_t TK, int32_t k, int32_t d, uint8_t* xq, uint8_t* xsf,
                           cudaStream_t s);
-// block-scaled FP4 grouped GEMM, nt = 16 | 32; sfb maps the token scales
+// block-scaled FP4 grouped GEMM, nt = 16 | 32; sfb maps the token scales; the
+// down GEMM works on pairs of adjacent 128-row weight blocks (m_blocks = d / 256)
 cudaError_t launch_fp4_gemm(bool gateup, int nt, const CUtensorMap& a0, const CUtensorMap& a1,
                             const CUtensorMap& b, const CUtensorMap& sfb, const Fp4GemmArgs& p,
                             int grid, cudaStream_t s);

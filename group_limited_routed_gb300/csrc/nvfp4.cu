@@ -127,9 +127,18 @@ __global__ void __launch_bounds__(128) quantize_rows_kernel(const uint16_t* __re
 }
 
 // --------------------------------------------------------------- FP4 GEMM
-template <int NT, bool GATEUP>
+// Kinds: the gate/up GEMM (gate and up weight tiles of the same rows, one
+// token tile), the down GEMM (one weight tile), and the down GEMM over pairs
+// of adjacent 128-row weight blocks sharing one token tile (twice the weight
+// bytes per stage for the same per-stage copies and barriers).
+constexpr int kKindDown = 0;
+constexpr int kKindGateUp = 1;
+constexpr int kKindDownPair = 2;
+
+template <int NT, int KIND>
 struct Cfg {
-  static constexpr int NUM_A = GATEUP ? 2 : 1;
+  static constexpr bool GATEUP = KIND == kKindGateUp;
+  static constexpr int NUM_A = KIND == kKindDown ? 1 : 2;
   static constexpr uint32_t A_BYTES = BM * BK_BYTES;           // 16 KB
   static constexpr uint32_t B_BYTES = NT * BK_BYTES;
   static constexpr uint32_t SFA_BYTES = 2048;                  // 128 rows x 16 scales
@@ -154,13 +163,15 @@ struct Cfg {
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 };
 
-template <int NT, bool GATEUP>
+template <int NT, int KIND>
 __global__ void __launch_bounds__(kThreads, 1)
     fp4_gemm_kernel(const __grid_constant__ CUtensorMap tm_a0,
                     const __grid_constant__ CUtensorMap tm_a1,
                     const __grid_constant__ CUtensorMap tm_b,
                     const __grid_constant__ CUtensorMap tm_sfb, const Fp4GemmArgs p) {
-  using C = Cfg<NT, GATEUP>;
+  using C = Cfg<NT, KIND>;
+  constexpr bool GATEUP = C::GATEUP;
+  constexpr bool PAIR = KIND == kKindDownPair;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = ptx::smem_addr(smem_raw);
   const uint32_t pad = (1024u - (raw_addr & 1023u)) & 1023u;
@@ -252,7 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
         const TileInfo ti = decode_tile<NT>(tile, s_start, s_cnt, s_off, E);
         if (ti.nvalid <= 0) continue;
-        const int a_row = ti.expert * p.rows_per_expert + ti.mblock * BM;
+        const int a_row = ti.expert * p.rows_per_expert + ti.mblock * (PAIR ? 2 * BM : BM);
         const int64_t sf_row_tile = a_row / BM;
         for (int kb = 0; kb < p.k_blocks; ++kb) {
           if (!W.wait(empty_bar(stage), phase ^ 1u)) {
@@ -268,6 +279,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (GATEUP) {
             ptx::tma_load_2d(st + C::A_BYTES, &tm_a1, fb, kb * BK_BYTES, a_row, pol_w);
             ptx::bulk_load(st + C::OFF_SFA + C::SFA_BYTES, p.sfa1 + sf_off, C::SFA_BYTES, fb);
+          }
+          if (PAIR) {  // the next 128 rows of the same projection
+            ptx::tma_load_2d(st + C::A_BYTES, &tm_a0, fb, kb * BK_BYTES, a_row + BM, pol_w);
+            ptx::bulk_load(st + C::OFF_SFA + C::SFA_BYTES,
+                           p.sfa0 + sf_off + sf_blocks_per_row_tile * 512, C::SFA_BYTES, fb);
           }
           ptx::tma_load_2d(st + C::OFF_B, &tm_b, fb, kb * BK_BYTES, ti.row0, pol_b);
 #pragma unroll
@@ -326,7 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t bd = ptx::sdesc_sw128(st + C::OFF_B + 32 * c);
             ptx::mma_fp4(d0, ptx::sdesc_sw128(st + 32 * c), bd, idesc, sf_col + 4 * c,
                          sfb_col + 4 * c, accum);
-            if (GATEUP)
+            if (C::NUM_A == 2)
               ptx::mma_fp4(d0 + NT, ptx::sdesc_sw128(st + C::A_BYTES + 32 * c), bd, idesc,
                            sf_col + 16 + 4 * c, sfb_col + 4 * c, accum);
           }
@@ -389,6 +405,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 p.hsf[row * (p.out_ld / 4) + (col / 64) * 16 + (col / 16) % 4] = sfc;
             }
           }
+        } else if constexpr (PAIR) {
+          uint32_t rb[16];
+          ptx::tmem_ld16(tq + NT + c0, rb);
+          ptx::tmem_wait_ld();
+          // this pair's first 128 rows are output columns col, the next col + 128
+          const int pcol = ti.mblock * 2 * BM + m;
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            if (c0 + j < ti.nvalid) {
+              const int row = ti.row0 + c0 + j;
+              const float wr = gs0 * p.perm_w[row];
+              p.y[static_cast<int64_t>(row) * p.out_ld + pcol] = __uint_as_float(ra[j]) * wr;
+              p.y[static_cast<int64_t>(row) * p.out_ld + pcol + BM] = __uint_as_float(rb[j]) * wr;
+            }
+          }
         } else {
           ptx::tmem_wait_ld();
 #pragma unroll
@@ -416,12 +447,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int NT, bool GATEUP>
+template <int NT, int KIND>
 cudaError_t launch_fp4_impl(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b,
                             const CUtensorMap& sfb, const Fp4GemmArgs& p, int grid,
                             cudaStream_t s) {
-  using C = Cfg<NT, GATEUP>;
-  auto kern = fp4_gemm_kernel<NT, GATEUP>;
+  using C = Cfg<NT, KIND>;
+  auto kern = fp4_gemm_kernel<NT, KIND>;
   cudaError_t err =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (err != cudaSuccess) return err;
@@ -448,12 +479,14 @@ void launch_quantize_rows(const uint16_t* x, const int32_t* perm_src, const int3
 cudaError_t launch_fp4_gemm(bool gateup, int nt, const CUtensorMap& a0, const CUtensorMap& a1,
                             const CUtensorMap& b, const CUtensorMap& sfb, const Fp4GemmArgs& p,
                             int grid, cudaStream_t s) {
+  // the down GEMM takes weight rows in pairs of 128-row blocks (m_blocks
+  // counts pairs)
   if (gateup) {
-    if (nt == 16) return launch_fp4_impl<16, true>(a0, a1, b, sfb, p, grid, s);
-    if (nt == 32) return launch_fp4_impl<32, true>(a0, a1, b, sfb, p, grid, s);
+    if (nt == 16) return launch_fp4_impl<16, kKindGateUp>(a0, a1, b, sfb, p, grid, s);
+    if (nt == 32) return launch_fp4_impl<32, kKindGateUp>(a0, a1, b, sfb, p, grid, s);
   } else {
-    if (nt == 16) return launch_fp4_impl<16, false>(a0, a0, b, sfb, p, grid, s);
-    if (nt == 32) return launch_fp4_impl<32, false>(a0, a0, b, sfb, p, grid, s);
+    if (nt == 16) return launch_fp4_impl<16, kKindDownPair>(a0, a0, b, sfb, p, grid, s);
+    if (nt == 32) return launch_fp4_impl<32, kKindDownPair>(a0, a0, b, sfb, p, grid, s);
   }
   return cudaErrorInvalidValue;
 }
