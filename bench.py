@@ -22,6 +22,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import re
 import os
 import statistics
 import subprocess
@@ -133,10 +134,15 @@ def touched_experts(ws, cfg) -> int:
 
 
 def file_sha(paths) -> str:
+    """Hash of the sources' code: comments and whitespace do not count, so
+    a comment edit keeps a capture valid; any code change invalidates it."""
     h = hashlib.sha256()
     for p in paths:
-        with open(p, "rb") as f:
-            h.update(f.read())
+        with open(p, encoding="utf-8") as f:
+            src = f.read()
+        src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", " ", src)
+        h.update("".join(src.split()).encode())
     return h.hexdigest()[:16]
 
 

@@ -31,11 +31,12 @@
 // ordered so the token blocks of one weight block run on neighbouring CTAs at
 // the same time (their weight tiles are then read from HBM once and from L2
 // after).  Warp roles: warp 0 streams weight tiles and warp 2 token tiles,
-// each into its own ring, warp 1
-// owns TMEM and issues tcgen05.mma from one thread, the remaining warps (4,
-// or 8 for 256-row token blocks: two per TMEM lane quarter, each draining half
-// of the columns) drain the accumulators, double-buffered when two fit in
-// TMEM's 512 columns.  Every
+// each into its own ring, warp 1 owns TMEM and issues tcgen05.mma from one
+// thread, the remaining warps drain the accumulators: 4, or for 256-row token
+// blocks 8 (down) or 16 (gate/up, whose two accumulators fill TMEM, so the
+// MMA waits for this epilogue), several per TMEM lane quarter, each draining
+// its share of the columns.  Accumulators are double-buffered when two fit
+// in TMEM's 512 columns.  Every
 // mbarrier wait is bounded: when one runs out the CTA latches
 // BEAM_ERR_TIMEOUT, stops, lets its copies in flight land, frees its TMEM and
 // returns.
