@@ -403,11 +403,14 @@ beam_status_t run_experts(const beam_moe_config_t& c, const void* hidden, const 
   ga.out_rows = y_pairs ? pa.perm_src : nullptr;
   ga.out_ld = c.d;
   ga.rows_per_expert = c.d;
-  ga.m_blocks = c.d / 128;
+  // 256-token blocks: pairs of adjacent 128-row W_d blocks share one token
+  // tile (half the token-tile reads per flop); decode-sized blocks stay single
+  const bool pair = c.d % 256 == 0 && nt_dn == 256;
+  ga.m_blocks = pair ? c.d / 256 : c.d / 128;
   ga.k_blocks = c.d_ff / 64;
   ga.b_k_blocks = ga.k_blocks;
-  err = beam::launch_grouped_gemm(beam::kModeDown, nt_dn, tm_wd, tm_wd, tm_h, ga,
-                                  grid_for(ga.m_blocks, nt_dn), s);
+  err = beam::launch_grouped_gemm(pair ? beam::kModeDownPair : beam::kModeDown, nt_dn, tm_wd, tm_wd,
+                                  tm_h, ga, grid_for(ga.m_blocks, nt_dn), s);
   if (err != cudaSuccess) return BEAM_ERR_CUDA;
   record(6, s);
 

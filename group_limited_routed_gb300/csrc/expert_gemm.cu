@@ -68,7 +68,7 @@ constexpr int UMMA_K = 16;
 // (four per TMEM lane quarter for the single-buffered 256-token gate/up tile,
 // whose epilogue the MMA waits for)
 constexpr int epi_warps_for(int nt, int mode) {
-  return nt >= 256 ? (mode == kModeGateUp ? 16 : 8) : 4;
+  return nt >= 256 ? (mode == kModeDown ? 8 : 16) : 4;
 }
 constexpr int threads_for(int nt, int mode) { return 96 + 32 * epi_warps_for(nt, mode); }
 constexpr int kMaxE = 256;
@@ -85,7 +85,9 @@ constexpr uint32_t pow2_at_least(uint32_t v) {
 // than L2), as many stages as fit.
 template <int NT, int MODE>
 struct Cfg {
-  static constexpr int NUM_A = MODE == kModeGateUp ? 2 : 1;
+  // gate/up: gate and up tiles of the same rows; down pair: two adjacent
+  // 128-row blocks of W_d; both share the token tile
+  static constexpr int NUM_A = MODE == kModeDown ? 1 : 2;
   static constexpr uint32_t A_BYTES = BM * BK * 2;
   static constexpr uint32_t A_STAGE = NUM_A * A_BYTES;
   static constexpr uint32_t B_STAGE = NT * BK * 2;
@@ -121,6 +123,7 @@ __global__ void __launch_bounds__(threads_for(NT, MODE), 1)
                        const __grid_constant__ CUtensorMap tm_b, const GemmArgs p) {
   using C = Cfg<NT, MODE>;
   constexpr bool GATEUP = MODE == kModeGateUp;
+  constexpr bool PAIR = MODE == kModeDownPair;
   // decode-sized token blocks gather their rows from the hidden states with
   // per-row TMA loads; larger blocks load whole tiles of a gathered copy
   constexpr bool ROW_GATHER = GATEUP && NT <= 32;
@@ -220,7 +223,7 @@ __global__ void __launch_bounds__(threads_for(NT, MODE), 1)
       for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
         const TileInfo ti = decode_tile<NT>(tile, s_start, s_cnt, s_off, E);
         if (ti.nvalid <= 0) continue;
-        const int a_row = ti.expert * p.rows_per_expert + ti.mblock * BM;
+        const int a_row = ti.expert * p.rows_per_expert + ti.mblock * (PAIR ? 2 * BM : BM);
         for (int kb = 0; kb < p.k_blocks; ++kb) {
           if (!W.wait(emptyA(stage), phase ^ 1u)) {
             ok = false;
@@ -234,6 +237,8 @@ __global__ void __launch_bounds__(threads_for(NT, MODE), 1)
             ptx::tma_load_2d(st, &tm_a0, fullA(stage), kb * BK, a_row, pol_w);
             if (GATEUP)
               ptx::tma_load_2d(st + C::A_BYTES, &tm_a1, fullA(stage), kb * BK, a_row, pol_w);
+            if (PAIR)
+              ptx::tma_load_2d(st + C::A_BYTES, &tm_a0, fullA(stage), kb * BK, a_row + BM, pol_w);
             last_parity[stage] = static_cast<int>(phase);
           }
           if (++stage == C::SA) {
@@ -338,7 +343,7 @@ __global__ void __launch_bounds__(threads_for(NT, MODE), 1)
             const uint32_t accum = (kb | kk) ? 1u : 0u;
             const uint64_t bd = ptx::sdesc_sw128(bt + kk * 32);
             ptx::mma_bf16(d0, ptx::sdesc_sw128(st + kk * 32), bd, idesc, accum);
-            if (GATEUP)
+            if (C::NUM_A == 2)
               ptx::mma_bf16(d0 + NT, ptx::sdesc_sw128(st + C::A_BYTES + kk * 32), bd, idesc, accum);
           }
           // free both stages once these MMAs have read them
@@ -401,6 +406,23 @@ __global__ void __launch_bounds__(threads_for(NT, MODE), 1)
               p.h_out[static_cast<int64_t>(ti.row0 + c0 + j) * p.out_ld + col] = f32_to_bf16(h);
             }
           }
+        } else if constexpr (PAIR) {
+          uint32_t rb[16];
+          ptx::tmem_ld16(tq + NT + c0, rb);
+          ptx::tmem_wait_ld();
+          // the pair's first 128 rows are output columns pcol, the next pcol + 128
+          const int pcol = ti.mblock * 2 * BM + m;
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            if (c0 + j < ti.nvalid) {
+              const int row = ti.row0 + c0 + j;
+              const int orow = p.out_rows ? p.out_rows[row] : row;
+              const float w = p.perm_w[row];
+              float* dst = p.f32_out + static_cast<int64_t>(orow) * p.out_ld + pcol;
+              dst[0] = __uint_as_float(ra[j]) * w;
+              dst[BM] = __uint_as_float(rb[j]) * w;
+            }
+          }
         } else {
           ptx::tmem_wait_ld();
 #pragma unroll
@@ -457,6 +479,10 @@ cudaError_t launch_grouped_gemm(int mode, int nt, const CUtensorMap& a0, const C
     case kModeDown:
       if (nt == 16) return launch_impl<16, kModeDown>(a0, a0, b, a, grid, s);
       if (nt == 256) return launch_impl<256, kModeDown>(a0, a0, b, a, grid, s);
+      break;
+    case kModeDownPair:
+      if (nt == 16) return launch_impl<16, kModeDownPair>(a0, a0, b, a, grid, s);
+      if (nt == 256) return launch_impl<256, kModeDownPair>(a0, a0, b, a, grid, s);
       break;
   }
   return cudaErrorInvalidValue;

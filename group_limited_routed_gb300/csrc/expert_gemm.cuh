@@ -9,6 +9,8 @@ namespace beam {
 
 constexpr int kModeDown = 0;    // y = w * (h W_d^T), FP32 out
 constexpr int kModeGateUp = 1;  // h = bf16(silu(x W_g^T) * (x W_u^T))
+constexpr int kModeDownPair = 2;  // as kModeDown over pairs of 128-row W_d blocks
+                                  // (m_blocks = d / 256)
 
 struct GemmArgs {
   const int32_t* counts;   // [E] rows per expert

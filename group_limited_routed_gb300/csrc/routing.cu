@@ -779,11 +779,15 @@ void launch_router_split(const float* w, int32_t E, int32_t d, uint16_t* planes,
 
 cudaError_t launch_fused_route(const RouterArgs& ra, int ksplit, const SelectArgs& sa,
                                const PermuteArgs& pa, int num_sms, cudaStream_t s) {
-  static int per_sm = 0;
-  if (per_sm == 0 &&
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fused_route_kernel, 256, 0) !=
-          cudaSuccess)
-    return cudaErrorUnknown;
+  // resident blocks per SM, queried once (thread-safe static initialisation)
+  static const int per_sm = [] {
+    int v = 0;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, fused_route_kernel, 256, 0) ==
+                   cudaSuccess
+               ? v
+               : 0;
+  }();
+  if (per_sm <= 0) return cudaErrorUnknown;
   const int64_t tiles = static_cast<int64_t>((ra.E + kRtExp - 1) / kRtExp) *
                         ((ra.T + kRtTok - 1) / kRtTok) * ksplit;
   int64_t want = tiles;
@@ -821,11 +825,14 @@ void launch_ep_pack(const int32_t* idx, const int32_t* perm_src, const float* pe
 }
 
 cudaError_t launch_permute_sort(const PermuteArgs& a, int32_t* hist, int num_sms, cudaStream_t s) {
-  static int per_sm = 0;
-  if (per_sm == 0 &&
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, permute_sort_kernel, 256, 0) !=
-          cudaSuccess)
-    return cudaErrorUnknown;
+  static const int per_sm = [] {
+    int v = 0;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, permute_sort_kernel, 256, 0) ==
+                   cudaSuccess
+               ? v
+               : 0;
+  }();
+  if (per_sm <= 0) return cudaErrorUnknown;
   const int64_t nc = (a.TK + kSortChunk - 1) / kSortChunk;
   const int64_t cap = static_cast<int64_t>(per_sm) * num_sms;
   const int grid = static_cast<int>(nc < cap ? (nc > 0 ? nc : 1) : cap);
