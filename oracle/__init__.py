@@ -65,6 +65,7 @@ def _load():
             getattr(lib, name).restype = ctypes.c_uint8
         lib.oracle_bf16_round.argtypes = [ctypes.c_float]
         lib.oracle_bf16_round.restype = ctypes.c_uint16
+        lib.oracle_swiglu_bf16.argtypes = [_P, _I64, _I32, _I32, _P, _P, _P]
         lib.oracle_f16_round.argtypes = [ctypes.c_double]
         lib.oracle_f16_round.restype = ctypes.c_double
         lib.oracle_bf16_round_double.argtypes = [ctypes.c_double]
@@ -116,6 +117,22 @@ def e4m3_encode(v: float) -> int:
 
 def bf16_round(v: float) -> int:
     return int(_load().oracle_bf16_round(v))
+
+
+def swiglu_bf16(x_bf16, wg, wu) -> np.ndarray:
+    """One expert's h = bf16(silu(x W_g^T) * (x W_u^T)) for rows x [n, d];
+    wg / wu [F, d]; BF16 bit patterns in and out."""
+    x = _c(x_bf16, np.uint16)
+    wg = _c(wg, np.uint16)
+    wu = _c(wu, np.uint16)
+    n, d = x.shape
+    F = wg.shape[0]
+    assert wg.shape == (F, d) and wu.shape == (F, d)
+    h = np.zeros((n, F), np.uint16)
+    rc = _load().oracle_swiglu_bf16(_ptr(x), n, d, F, _ptr(wg), _ptr(wu), _ptr(h))
+    if rc:
+        raise ValueError(f"oracle_swiglu_bf16 failed ({rc})")
+    return h
 
 
 def f16_round(v: float) -> float:

@@ -442,6 +442,35 @@ static int experts_impl(const uint16_t *x, int64_t T, int32_t d, int32_t F,
   return err;
 }
 
+/* The gate/up step of one expert on n rows alone, as the expert layer takes
+ * it ([SGL] "BF16 MoE Kernel Optimization"; [HF] "残差流": the SwiGLU product
+ * is computed in FP32 and h keeps its BF16 rounding): g and u accumulate in
+ * double and round to FP32, silu(g) = g / (1 + e^-g) in double, the product
+ * rounds to FP32 and then to BF16.  x [n, d], wg / wu [F, d] BF16 bits,
+ * h [n, F] BF16 bits. */
+int oracle_swiglu_bf16(const uint16_t *x, int64_t n, int32_t d, int32_t F, const uint16_t *wg,
+                       const uint16_t *wu, uint16_t *h) {
+  if (n < 0 || d <= 0 || F <= 0) return -1;
+#pragma omp parallel for schedule(static)
+  for (int64_t i = 0; i < n; ++i) {
+    const uint16_t *xr = x + i * d;
+    for (int32_t f = 0; f < F; ++f) {
+      double ga = 0.0, ua = 0.0;
+      const uint16_t *gr = wg + (int64_t)f * d;
+      const uint16_t *ur = wu + (int64_t)f * d;
+      for (int32_t j = 0; j < d; ++j) {
+        ga += bf16_value(xr[j]) * bf16_value(gr[j]);
+        ua += bf16_value(xr[j]) * bf16_value(ur[j]);
+      }
+      const double g = (double)(float)ga;
+      const double u = (double)(float)ua;
+      const double silu = g / (1.0 + exp(-g));
+      h[i * F + f] = bf16_round((float)(silu * u));
+    }
+  }
+  return 0;
+}
+
 int oracle_experts_bf16(const uint16_t *x, int64_t T, int32_t d, int32_t F,
                         int32_t k, int32_t E, const int32_t *idx, const float *w,
                         const uint16_t *const *wg, const uint16_t *const *wu,

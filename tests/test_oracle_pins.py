@@ -501,3 +501,21 @@ def test_f16_activation_experts_match_dense_torch():
             h = (g / (1 + torch.exp(-g)) * u).float().to(torch.float16).double()
             ref[t] += float(r["w"][t, j]) * (h @ deq["d"][e].T)
     assert np.allclose(ex, ref.numpy(), rtol=1e-12, atol=1e-12)
+
+
+def test_swiglu_rows_through_the_expert_layer():
+    """One expert, weight 1 and an identity down projection: the expert
+    layer's output is h itself (h is BF16, the identity sum is exact), so the
+    standalone gate/up oracle must match the layer oracle bit for bit."""
+    T, F = 9, 64
+    d = F
+    x = _bf16_matrix((T, d))
+    wg = _bf16_matrix((1, F, d), 0.3)
+    wu = _bf16_matrix((1, F, d), 0.3)
+    eye = torch.eye(d, dtype=torch.bfloat16).reshape(1, d, F)
+    idx = np.zeros((T, 1), np.int32)
+    w = np.ones((T, 1), np.float32)
+    layer = oracle.experts_bf16(inputs.bf16_bits(x), idx, w, inputs.bf16_bits(wg),
+                                inputs.bf16_bits(wu), inputs.bf16_bits(eye), 1)
+    h = oracle.swiglu_bf16(inputs.bf16_bits(x), inputs.bf16_bits(wg[0]), inputs.bf16_bits(wu[0]))
+    assert np.array_equal(layer, h)
