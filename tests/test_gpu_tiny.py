@@ -239,3 +239,44 @@ def test_group_shapes(E, G, kg, k):
     assert pkg.check_status(ws) == 0
     check_routing(cfg, host(ws.view("topk_idx", torch.int32, (cfg.T, k))),
                   host(ws.view("topk_w", torch.float32, (cfg.T, k))), r)
+
+
+@pytest.mark.parametrize("T", [32, 300])
+def test_expert_gemms_alone(T):
+    """Each expert GEMM from its own inputs: h of the gate/up GEMM against the
+    oracle's SwiGLU rows (one BF16 step apart at most, where the fast exp
+    lands a product on the other side of a rounding boundary), and y of the
+    down GEMM against an FP64 matmul of the GPU's own h times the routing
+    weight.  T = 32 takes the 16-row blocks, T = 300 the 256-row blocks and
+    the paired down GEMM."""
+    cfg = CFG.replace(T=T, seed=200 + T)
+    t = inputs.generate(cfg, "cuda")
+    lg, r = oracle_route(cfg, t)
+    ws = pkg.Workspace(cfg, T)
+    pkg.forward_routed(cfg, t["hidden"], torch.from_numpy(r["idx"]).cuda(),
+                       torch.from_numpy(r["w"]).cuda(), t["w_gate"], t["w_up"], t["w_down"],
+                       ws=ws)
+    assert pkg.check_status(ws) == 0
+    TK, F, d, k = T * cfg.topk, cfg.d_ff, cfg.d, cfg.topk
+    perm = host(ws.view("perm_src", torch.int32, (TK,)))
+    h = host(ws.view("h", torch.bfloat16, (TK, F)))
+    y = ws.view("y", torch.float32, (TK, d)).cpu().double().numpy()
+    x = host(t["hidden"])
+    rows = np.random.default_rng(T).choice(TK, 48, replace=False)
+    flat = r["idx"].reshape(-1)
+    wflat = r["w"].reshape(-1)
+    for row in rows:
+        e, tok = int(flat[perm[row]]), int(perm[row] // k)
+        ref = oracle.swiglu_bf16(x[tok:tok + 1], host(t["w_gate"][e]), host(t["w_up"][e]))[0]
+        a = h[row].astype(np.int32)
+        b = ref.astype(np.int32)
+        a = np.where(a & 0x8000, 0x8000 - a, a)
+        b = np.where(b & 0x8000, 0x8000 - b, b)
+        assert np.abs(a - b).max() <= 1, row
+        assert (a != b).mean() < 0.02, row
+        hv = torch.from_numpy(h[row].view(np.int16)).view(torch.bfloat16).double()
+        wd = t["w_down"][e].cpu().double()
+        prod = wd * hv[None, :]
+        yref = float(wflat[perm[row]]) * prod.sum(1).numpy()
+        bound = 1e-4 * abs(float(wflat[perm[row]])) * prod.abs().sum(1).numpy() + 1e-30
+        assert np.all(np.abs(y[row] - yref) <= bound), row
