@@ -35,30 +35,32 @@ __device__ __forceinline__ uint16_t f32_to_bf16(float v) {
 }
 
 // ------------------------------------------------------------------ router
-// Block: 32 tokens x 64 experts over one K range; 256 threads, each 2 tokens
-// x 4 experts, FP32 FMA in ascending K order, summed per 32-wide slice first
-// (blocked summation keeps the rounding error of the 5120-term sum near
-// 1e-7); fixed order => deterministic.
+// Block: 32 tokens x 64 experts over one K range; 256 threads, each 4 tokens
+// x 2 experts (a warp covers the 32 tokens and 8 experts, so a K step reads
+// one 16-byte and one 8-byte shared-memory word per 8 FMAs), FP32 FMA in
+// ascending K order, summed per 32-wide slice first (blocked summation keeps
+// the rounding error of the 5120-term sum near 1e-7); fixed order =>
+// deterministic.
 constexpr int kRtTok = 32;
 constexpr int kRtExp = 64;
 constexpr int kRtK = 32;
 constexpr int kRtDepth = 4;  // K slices whose loads are in flight together
 
 __device__ __forceinline__ void router_tile(const RouterArgs& a, int bx, int by, int bz) {
-  __shared__ float xs[kRtK][kRtTok + 1];
+  __shared__ __align__(16) float xs[kRtK][kRtTok + 4];
   __shared__ __align__(16) float ws[kRtK][kRtExp + 4];
   const int e0 = bx * kRtExp;
   const int64_t t0 = static_cast<int64_t>(by) * kRtTok;
   const int k_begin = bz * a.k_chunk;
   const int k_end = min(a.d, k_begin + a.k_chunk);
   const int tid = threadIdx.x;
-  const int tx = tid & 15;
-  const int ty = tid >> 4;
-  float acc[2][4];
+  const int tg = tid & 7;                              // tokens 4 tg .. 4 tg + 3
+  const int eg = ((tid & 31) >> 3) + 4 * (tid >> 5);   // experts 2 eg, 2 eg + 1
+  float acc[4][2];
 #pragma unroll
-  for (int i = 0; i < 2; ++i)
+  for (int i = 0; i < 4; ++i)
 #pragma unroll
-    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+    for (int j = 0; j < 2; ++j) acc[i][j] = 0.f;
 
   // the loads of up to four 32-wide K slices are issued together, so a
   // decode-sized K range (128) costs one memory round trip
@@ -105,35 +107,32 @@ __device__ __forceinline__ void router_tile(const RouterArgs& a, int bx, int by,
       }
       __syncthreads();
       // blocked summation: each 32-wide slice is summed on its own, then added
-      float sl[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      float sl[4][2] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
 #pragma unroll
       for (int kk = 0; kk < kRtK; ++kk) {
-        const float x0 = xs[kk][ty * 2];
-        const float x1 = xs[kk][ty * 2 + 1];
-        const float4 wv = *reinterpret_cast<const float4*>(&ws[kk][tx * 4]);
-        sl[0][0] = fmaf(x0, wv.x, sl[0][0]);
-        sl[0][1] = fmaf(x0, wv.y, sl[0][1]);
-        sl[0][2] = fmaf(x0, wv.z, sl[0][2]);
-        sl[0][3] = fmaf(x0, wv.w, sl[0][3]);
-        sl[1][0] = fmaf(x1, wv.x, sl[1][0]);
-        sl[1][1] = fmaf(x1, wv.y, sl[1][1]);
-        sl[1][2] = fmaf(x1, wv.z, sl[1][2]);
-        sl[1][3] = fmaf(x1, wv.w, sl[1][3]);
+        const float4 xv = *reinterpret_cast<const float4*>(&xs[kk][tg * 4]);
+        const float2 wv = *reinterpret_cast<const float2*>(&ws[kk][eg * 2]);
+        const float xa[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          sl[i][0] = fmaf(xa[i], wv.x, sl[i][0]);
+          sl[i][1] = fmaf(xa[i], wv.y, sl[i][1]);
+        }
       }
 #pragma unroll
-      for (int i = 0; i < 2; ++i)
+      for (int i = 0; i < 4; ++i)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] += sl[i][j];
+        for (int j = 0; j < 2; ++j) acc[i][j] += sl[i][j];
       __syncthreads();
     }
   }
 #pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const int64_t t = t0 + ty * 2 + i;
-    const int e = e0 + tx * 4;
+  for (int i = 0; i < 4; ++i) {
+    const int64_t t = t0 + tg * 4 + i;
+    const int e = e0 + eg * 2;
     if (t < a.T && e < a.E) {
       float* dst = a.part + (static_cast<int64_t>(bz) * a.T + t) * a.E + e;
-      *reinterpret_cast<float4*>(dst) = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+      *reinterpret_cast<float2*>(dst) = make_float2(acc[i][0], acc[i][1]);
     }
   }
 }
