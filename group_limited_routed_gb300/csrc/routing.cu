@@ -581,20 +581,35 @@ __global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ 
   float acc[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-  for (int sl = 0; sl < k; ++sl) {
-    const int row = pair_row[t * k + sl];
-    if (row < 0) continue;
-    const float4* src = reinterpret_cast<const float4*>(y + static_cast<int64_t>(row) * d) + 2 * c8;
-    const float4 a = src[0];
-    const float4 b = src[1];
-    acc[0] += a.x;
-    acc[1] += a.y;
-    acc[2] += a.z;
-    acc[3] += a.w;
-    acc[4] += b.x;
-    acc[5] += b.y;
-    acc[6] += b.z;
-    acc[7] += b.w;
+  // up to 8 slots at a time: their rows, then their loads, then the sums in
+  // slot order
+  constexpr int kAhead = 8;
+  for (int s0 = 0; s0 < k; s0 += kAhead) {
+    int row[kAhead];
+#pragma unroll
+    for (int j = 0; j < kAhead; ++j) row[j] = s0 + j < k ? pair_row[t * k + s0 + j] : -1;
+    float4 a[kAhead], b[kAhead];
+#pragma unroll
+    for (int j = 0; j < kAhead; ++j) {
+      if (row[j] >= 0) {
+        const float4* src =
+            reinterpret_cast<const float4*>(y + static_cast<int64_t>(row[j]) * d) + 2 * c8;
+        a[j] = src[0];
+        b[j] = src[1];
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kAhead; ++j) {
+      if (row[j] < 0) continue;
+      acc[0] += a[j].x;
+      acc[1] += a[j].y;
+      acc[2] += a[j].z;
+      acc[3] += a[j].w;
+      acc[4] += b[j].x;
+      acc[5] += b[j].y;
+      acc[6] += b[j].z;
+      acc[7] += b[j].w;
+    }
   }
   uint4 o;
   uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
