@@ -34,7 +34,8 @@ EXPORTS = ("beam_moe_workspace_size", "beam_moe_workspace_layout", "beam_moe_rou
            "beam_moe_check_status", "beam_moe_set_stage_events", "beam_moe_set_debug",
            "beam_moe_kernels_per_forward", "beam_status_string", "beam_moe_ep_dispatch",
            "beam_moe_ep_workspace_size", "beam_moe_ep_experts", "beam_moe_ep_combine",
-           "beam_moe_forward_boundary", "beam_moe_forward_nvfp4_a16")
+           "beam_moe_forward_boundary", "beam_moe_forward_nvfp4_a16",
+           "beam_moe_ep_experts_nvfp4")
 
 
 class BeamError(RuntimeError):
@@ -112,11 +113,14 @@ def lib():
         L.beam_moe_ep_dispatch.argtypes = [cfgp, _P, _P, _P, _I64, ctypes.c_int32, _P, _P, _P, _P,
                                            _P, _SZ, _P]
         L.beam_moe_ep_dispatch.restype = _ST
-        L.beam_moe_ep_workspace_size.argtypes = [cfgp, ctypes.c_int32, _I64]
+        L.beam_moe_ep_workspace_size.argtypes = [cfgp, ctypes.c_int32, _I64, ctypes.c_int32]
         L.beam_moe_ep_workspace_size.restype = _SZ
         L.beam_moe_ep_experts.argtypes = [cfgp, ctypes.c_int32, ctypes.c_int32, _P, _P, _P, _P, _P,
                                           _P, _P, _I64, _P, _SZ, _P]
         L.beam_moe_ep_experts.restype = _ST
+        L.beam_moe_ep_experts_nvfp4.argtypes = [cfgp, ctypes.c_int32, ctypes.c_int32, _P, _P, _P,
+                                                fp4p, fp4p, fp4p, _P, _I64, _P, _SZ, _P]
+        L.beam_moe_ep_experts_nvfp4.restype = _ST
         L.beam_moe_ep_combine.argtypes = [cfgp, _P, _I64, _P, _P, _SZ, _P]
         L.beam_moe_ep_combine.restype = _ST
         L.beam_status_string.argtypes = [_ST]
@@ -442,10 +446,11 @@ def ep_dispatch(cfg, hidden, router_w, corr_bias, n_ranks: int, ws: Workspace | 
 class EpWorkspace:
     """Device workspace of :func:`ep_experts` for up to M_max received rows."""
 
-    def __init__(self, cfg, n_ranks: int, M_max: int, device=None):
+    def __init__(self, cfg, n_ranks: int, M_max: int, device=None, weight_fmt: int = 0):
         c = _cfg(cfg)
         self.nbytes = int(lib().beam_moe_ep_workspace_size(ctypes.byref(c), int(n_ranks),
-                                                           int(M_max)))
+                                                           int(M_max), int(weight_fmt)))
+        self.weight_fmt = int(weight_fmt)
         if self.nbytes == 0:
             raise BeamError(1, "beam_moe_ep_workspace_size")
         self.M_max = int(M_max)
@@ -477,6 +482,30 @@ def ep_experts(cfg, n_ranks: int, rank: int, x_recv, expert_recv, w_recv, w_gate
                                      _dev(w_down, torch.bfloat16, "w_down"),
                                      _dev(y, torch.float32, "y_recv"), M, ws.ptr, ws.nbytes,
                                      _stream(stream)), "beam_moe_ep_experts")
+    return y
+
+
+def ep_experts_nvfp4(cfg, n_ranks: int, rank: int, x_recv, expert_recv, w_recv, gate: Fp4Weight,
+                     up: Fp4Weight, down: Fp4Weight, ws: EpWorkspace | None = None, out=None,
+                     stream=None):
+    """This rank's NVFP4 experts on its received rows -> y_recv [M, d] f32."""
+    M = x_recv.shape[0]
+    dev = x_recv.device
+    if ws is None or ws.M_max < M or ws.weight_fmt != NVFP4:
+        ws = EpWorkspace(cfg, n_ranks, max(M, 1), dev, weight_fmt=NVFP4)
+    y = torch.empty(M, cfg.d, dtype=torch.float32, device=dev) if out is None else out
+    if M == 0:
+        return y
+    c = _cfg(cfg)
+    _check(lib().beam_moe_ep_experts_nvfp4(ctypes.byref(c), int(n_ranks), int(rank),
+                                           _dev(x_recv, torch.bfloat16, "x_recv"),
+                                           _dev(expert_recv, torch.int32, "expert_recv"),
+                                           _dev(w_recv, torch.float32, "w_recv"),
+                                           ctypes.byref(gate._c), ctypes.byref(up._c),
+                                           ctypes.byref(down._c),
+                                           _dev(y, torch.float32, "y_recv"), M, ws.ptr,
+                                           ws.nbytes, _stream(stream)),
+           "beam_moe_ep_experts_nvfp4")
     return y
 
 

@@ -109,6 +109,7 @@ struct Fp4GemmArgs {
   uint8_t* hq;             // gate/up out: h codes [rows, F/2]
   uint8_t* hsf;            // gate/up out: h scales [rows, F/4] (16-byte slot per 64)
   float* y;                // down out: [rows, d]
+  const int32_t* out_rows; // down: output row of each permuted row (nullptr: the same row)
   int32_t out_ld;          // F (gate/up) or d (down), in elements
   int32_t E;
   int32_t rows_per_expert;

@@ -415,9 +415,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < 16; ++j) {
             if (c0 + j < ti.nvalid) {
               const int row = ti.row0 + c0 + j;
+              const int orow = p.out_rows ? p.out_rows[row] : row;
               const float wr = gs0 * p.perm_w[row];
-              p.y[static_cast<int64_t>(row) * p.out_ld + pcol] = __uint_as_float(ra[j]) * wr;
-              p.y[static_cast<int64_t>(row) * p.out_ld + pcol + BM] = __uint_as_float(rb[j]) * wr;
+              p.y[static_cast<int64_t>(orow) * p.out_ld + pcol] = __uint_as_float(ra[j]) * wr;
+              p.y[static_cast<int64_t>(orow) * p.out_ld + pcol + BM] = __uint_as_float(rb[j]) * wr;
             }
           }
         } else {

@@ -301,9 +301,11 @@ beam_status_t beam_moe_ep_dispatch(const beam_moe_config_t *cfg, const void *hid
                                    float *send_w, int32_t *send_counts, void *workspace,
                                    size_t ws_bytes, void *stream);
 
-/* Workspace bytes of beam_moe_ep_experts for up to M_max received rows;
- * 0 for an invalid configuration. */
-size_t beam_moe_ep_workspace_size(const beam_moe_config_t *cfg, int32_t n_ranks, int64_t M_max);
+/* Workspace bytes of beam_moe_ep_experts (weight_fmt BEAM_WEIGHTS_BF16) or
+ * beam_moe_ep_experts_nvfp4 (BEAM_WEIGHTS_NVFP4) for up to M_max received
+ * rows; 0 for an invalid configuration or format. */
+size_t beam_moe_ep_workspace_size(const beam_moe_config_t *cfg, int32_t n_ranks, int64_t M_max,
+                                  int32_t weight_fmt);
 
 /* Steps 3-4 of the layer on rank `rank` for M received rows:
  *   y_recv[i] = w_recv[i] * down(h), h = bf16(silu(x W_g^T) * (x W_u^T)),
@@ -317,6 +319,19 @@ beam_status_t beam_moe_ep_experts(const beam_moe_config_t *cfg, int32_t n_ranks,
                                   const float *w_recv, const void *w_gate, const void *w_up,
                                   const void *w_down, float *y_recv, int64_t M, void *workspace,
                                   size_t ws_bytes, void *stream);
+
+/* beam_moe_ep_experts with NVFP4 expert weights (the pages' MegaMoE path
+ * runs Beam's NVFP4 experts): the rank's received rows are quantised to
+ * NVFP4 and go through the block-scaled FP4 GEMMs of beam_moe_forward_nvfp4;
+ * gate / up / down describe this rank's E/n_ranks experts (codes
+ * [E/n_ranks, N, K/2], their blocked scales, global scales [E/n_ranks]).
+ * Extra shape rules: d % 256 == 0, d_ff % 256 == 0. */
+beam_status_t beam_moe_ep_experts_nvfp4(const beam_moe_config_t *cfg, int32_t n_ranks,
+                                        int32_t rank, const void *x_recv,
+                                        const int32_t *expert_recv, const float *w_recv,
+                                        const beam_fp4_weight_t *gate, const beam_fp4_weight_t *up,
+                                        const beam_fp4_weight_t *down, float *y_recv, int64_t M,
+                                        void *workspace, size_t ws_bytes, void *stream);
 
 /* The owner's combine: out[t] = bf16(sum over slots, in slot order, of the
  * returned FP32 rows), y_back [T*topk, d] in the order beam_moe_ep_dispatch

@@ -70,8 +70,11 @@ def test_ep_workspace_query(lib):
     c = api.CConfig.of(beam)
     size = lib.beam_moe_ep_workspace_size
     size.restype = ctypes.c_size_t
-    size.argtypes = [ctypes.POINTER(api.CConfig), ctypes.c_int32, ctypes.c_int64]
-    assert size(ctypes.byref(c), 8, 256) % 256 == 0 and size(ctypes.byref(c), 8, 256) > 0
-    assert size(ctypes.byref(c), 8, 1024) >= size(ctypes.byref(c), 8, 256)
-    assert size(ctypes.byref(c), 3, 256) == 0        # 3 does not divide 256 experts
-    assert size(ctypes.byref(c), 512, 256) == 0      # more ranks than experts
+    size.argtypes = [ctypes.POINTER(api.CConfig), ctypes.c_int32, ctypes.c_int64,
+                     ctypes.c_int32]
+    assert size(ctypes.byref(c), 8, 256, 0) % 256 == 0 and size(ctypes.byref(c), 8, 256, 0) > 0
+    assert size(ctypes.byref(c), 8, 1024, 0) >= size(ctypes.byref(c), 8, 256, 0)
+    assert size(ctypes.byref(c), 8, 256, 1) > 0       # NVFP4 experts
+    assert size(ctypes.byref(c), 3, 256, 0) == 0      # 3 does not divide 256 experts
+    assert size(ctypes.byref(c), 512, 256, 0) == 0    # more ranks than experts
+    assert size(ctypes.byref(c), 8, 256, 2) == 0      # no W4A16 expert-parallel path

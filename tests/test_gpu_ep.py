@@ -16,8 +16,16 @@ from _parity import check_out, exempt_tokens, oracle_out, oracle_route
 pytestmark = pytest.mark.gpu
 
 
-def _emulate(cfg, t, Ts):
+def _bf16_experts(cfg, t):
+    def run(R, q, x, e, w):
+        sl = ep.expert_slice(cfg, R, q)
+        return pkg.ep_experts(cfg, R, q, x, e, w, t["w_gate"][sl], t["w_up"][sl], t["w_down"][sl])
+    return run
+
+
+def _emulate(cfg, t, Ts, experts=None):
     """Every rank's output of the expert-parallel layer, ranks in sequence."""
+    experts = _bf16_experts(cfg, t) if experts is None else experts
     R = len(Ts)
     starts = np.concatenate([[0], np.cumsum(Ts)])
     hid = [t["hidden"][starts[r]:starts[r + 1]] for r in range(R)]
@@ -31,9 +39,7 @@ def _emulate(cfg, t, Ts):
         x = torch.cat([p[0] for p in parts]).contiguous()
         e = torch.cat([p[1] for p in parts]).contiguous()
         w = torch.cat([p[2] for p in parts]).contiguous()
-        sl = ep.expert_slice(cfg, R, q)
-        y_recv.append(pkg.ep_experts(cfg, R, q, x, e, w, t["w_gate"][sl], t["w_up"][sl],
-                                     t["w_down"][sl]))
+        y_recv.append(experts(R, q, x, e, w))
     outs = []
     for r in range(R):
         # rows come back per destination rank, in the order they were sent
@@ -87,3 +93,32 @@ def test_foreign_expert_latches_device_check():
     ws = pkg.EpWorkspace(cfg, R, 8)
     pkg.ep_experts(cfg, R, q, x, e, w, t["w_gate"][sl], t["w_up"][sl], t["w_down"][sl], ws=ws)
     assert pkg.check_status(ws) == 6
+
+
+@pytest.mark.parametrize("Ts", [[40, 24], [16, 0, 33, 5]])
+def test_emulated_ranks_nvfp4_experts(Ts):
+    """NVFP4 experts on each rank (the pages' MegaMoE path runs Beam's NVFP4
+    experts): every rank's output equals beam_moe_forward_nvfp4 on its tokens
+    bit for bit."""
+    cfg = inputs.CONFIGS["tiny"].replace(weight_fmt="nvfp4", seed=90 + len(Ts),
+                                         cpu_generator=True)
+    t = inputs.generate(cfg, "cpu", T=sum(Ts))
+    t = {k: ({kk: vv.cuda() for kk, vv in v.items()} if isinstance(v, dict)
+             else v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in t.items()}
+    full = [pkg.Fp4Weight.of(t[n]) for n in ("w_gate", "w_up", "w_down")]
+    R = len(Ts)
+    local = []
+    for q in range(R):
+        sl = ep.expert_slice(cfg, R, q)
+        local.append([pkg.Fp4Weight.of({k: v[sl] for k, v in t[n].items()})
+                      for n in ("w_gate", "w_up", "w_down")])
+
+    def run(R_, q, x, e, w):
+        return pkg.ep_experts_nvfp4(cfg, R_, q, x, e, w, *local[q])
+
+    hid, outs = _emulate(cfg, t, Ts, experts=run)
+    for h, o in zip(hid, outs):
+        if h.shape[0] == 0:
+            continue
+        ref = pkg.forward_nvfp4(cfg, h.contiguous(), t["router_w"], t["corr_bias"], *full)
+        assert torch.equal(o.view(torch.int16), ref.view(torch.int16))
