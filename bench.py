@@ -249,7 +249,7 @@ def run_reference(args, cfg):
     return 0
 
 
-def config_record(cfg, touched, routed=False, a16=False):
+def config_record(cfg, touched, routed=False, a16=False, graph=False):
     rec = {"workload": cfg.description, "T": cfg.T, "d": cfg.d, "n_experts": cfg.n_experts,
            "n_groups": cfg.n_groups, "topk_groups": cfg.topk_groups, "topk": cfg.topk,
            "d_ff": cfg.d_ff, "routed_scale": cfg.routed_scale, "weights": cfg.weight_fmt,
@@ -262,6 +262,8 @@ def config_record(cfg, touched, routed=False, a16=False):
         rec["routing"] = "replayed (recorded once; steps run experts + combine)"
     if a16:
         rec["activations"] = "f16 (not quantised): W4A16"
+    if graph:
+        rec["launch"] = "one layer call captured in a CUDA graph, replayed each step"
     return rec
 
 
@@ -285,7 +287,7 @@ def run_gpu(args, cfg):
         fwd = pkg.forward_nvfp4_a16 if a16 else pkg.forward_nvfp4
 
         def layer(x, o):
-            return fwd(cfg, x, t["router_w"], t["corr_bias"], *wts, out=o, ws=ws, stream=stream)
+            return fwd(cfg, x, t["router_w"], t["corr_bias"], *wts, out=o, ws=ws, stream=torch.cuda.current_stream())
     elif args.routed:
         # routing replay: the routes are recorded once, the timed steps run
         # the experts and the combine on them
@@ -293,11 +295,11 @@ def run_gpu(args, cfg):
 
         def layer(x, o):
             return pkg.forward_routed(cfg, x, ridx, rw, t["w_gate"], t["w_up"], t["w_down"],
-                                      out=o, ws=ws, stream=stream)
+                                      out=o, ws=ws, stream=torch.cuda.current_stream())
     else:
         def layer(x, o):
             return pkg.forward(cfg, x, t["router_w"], t["corr_bias"], t["w_gate"], t["w_up"],
-                               t["w_down"], out=o, ws=ws, stream=stream)
+                               t["w_down"], out=o, ws=ws, stream=torch.cuda.current_stream())
 
     def step(o=out):
         return layer(t["hidden"], o)
@@ -326,10 +328,28 @@ def run_gpu(args, cfg):
     if use_dist:
         dist.barrier()
     torch.cuda.synchronize()
+    graph = None
+    if args.graph:
+        # one layer call captured with its stage events (event-record nodes);
+        # each replay records them again, so they hold the last replay's times
+        gevs = [torch.cuda.Event(enable_timing=True) for _ in range(8)]
+        for e in gevs:
+            e.record(stream)  # creates the handles
+        graph = torch.cuda.CUDAGraph()
+        pkg.set_stage_events(gevs)
+        with torch.cuda.graph(graph):
+            step()
+        pkg.set_stage_events(None)
+        for _ in range(3):
+            graph.replay()
+        torch.cuda.synchronize()
     t_start.record(stream)
     for i in range(args.steps):
-        pkg.set_stage_events(evs[i])
-        step()
+        if graph is not None:
+            graph.replay()
+        else:
+            pkg.set_stage_events(evs[i])
+            step()
     t_end.record(stream)
     torch.cuda.synchronize()
     if use_dist:
@@ -337,8 +357,11 @@ def run_gpu(args, cfg):
     pkg.set_stage_events(None)
     clocks = sampler.stop()
     ms = t_start.elapsed_time(t_end)
-    stage_ms = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(7)]
-                         for i in range(args.steps)]).mean(axis=0)
+    if graph is not None:
+        stage_ms = np.array([gevs[j].elapsed_time(gevs[j + 1]) for j in range(7)])
+    else:
+        stage_ms = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(7)]
+                             for i in range(args.steps)]).mean(axis=0)
     if pkg.check_status(ws) != 0:
         raise RuntimeError("device status after the timed region")
 
@@ -407,7 +430,7 @@ def run_gpu(args, cfg):
         "scaling": "weak", "vs_baseline": None,
         "dtype": ("nvfp4 weights x f16 activations" if a16 else "nvfp4 (e2m1 x e4m3 per 16)")
         if fp4 else "bf16", "data": "synthetic",
-        "config": config_record(cfg, touched, args.routed, a16),
+        "config": config_record(cfg, touched, args.routed, a16, args.graph),
         "roofline": roofline,
         "layer_roofline": {"bound": "hbm", "algorithmic_bytes": layer_bytes,
                            "achieved": layer_bytes / (layer_ms / 1e3) / 1e9,
@@ -442,6 +465,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--a16", action="store_true",
                     help="NVFP4 configs: 16-bit activations (beam_moe_forward_nvfp4_a16)")
+    ap.add_argument("--graph", action="store_true",
+                    help="replay the layer call from a CUDA graph (stage times of the last replay)")
     ap.add_argument("--routed", action="store_true",
                     help="time beam_moe_forward_routed on recorded routes (routing replay)")
     args = ap.parse_args(argv)

@@ -206,8 +206,16 @@ T* at(void* ws, size_t off) {
   return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
 }
 
+// Inside a stream capture a plain record only orders streams; the external
+// flag makes it an event-record node that timestamps every graph replay.
 void record(int i, cudaStream_t s) {
-  if (g_num_events >= 8) cudaEventRecord(g_events[i], s);
+  if (g_num_events < 8) return;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  cudaStreamIsCapturing(s, &cap);
+  if (cap == cudaStreamCaptureStatusActive)
+    cudaEventRecordWithFlags(g_events[i], s, cudaEventRecordExternal);
+  else
+    cudaEventRecord(g_events[i], s);
 }
 
 beam_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? BEAM_OK : BEAM_ERR_CUDA; }

@@ -821,11 +821,10 @@ cudaError_t launch_combine_boundary(const float* y, const int32_t* pair_row, int
                                     int32_t d, uint16_t* out, const BoundaryArgs& b,
                                     cudaStream_t s) {
   const size_t smem = static_cast<size_t>(d) * sizeof(float);
-  if (smem > 48 * 1024) {
-    const cudaError_t e = cudaFuncSetAttribute(
-        combine_boundary_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-  }
+  // once: the largest row the entry point accepts (d <= 51200)
+  static const cudaError_t e = cudaFuncSetAttribute(
+      combine_boundary_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+  if (e != cudaSuccess) return e;
   combine_boundary_kernel<<<static_cast<unsigned>(T), 256, smem, s>>>(y, pair_row, k, d, out, b);
   return cudaGetLastError();
 }

@@ -351,7 +351,9 @@ beam_status_t beam_moe_check_status(void *workspace, void *stream);
  * step).  Steps a call does not run record at the same point as the previous
  * one.  Below 256 tokens (at most 256 experts) the router, the selection and
  * the permutation are one cooperative launch: [1], [2] and [3] are all
- * recorded after it.  n == 0 switches it off.  Process-wide; not
+ * recorded after it.  While `stream` is being captured into a CUDA graph
+ * the records become event-record nodes (cudaEventRecordExternal), so each
+ * replay timestamps them again.  n == 0 switches it off.  Process-wide; not
  * thread-safe. */
 beam_status_t beam_moe_set_stage_events(void *const *events, int32_t n);
 
