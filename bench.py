@@ -42,9 +42,16 @@ from group_limited_routed_gb300 import inputs  # noqa: E402
 METRIC = "Beam MoE-layer tokens/s"
 UNIT = "tokens/s"
 STAGES = ["router", "select", "permute", "gather", "gate_up", "down", "combine"]
-DOMINANT = "gate_up"
-DOMINANT_SRC = [os.path.join(ROOT, "group_limited_routed_gb300", "csrc", f)
-                for f in ("expert_gemm.cu", "expert_gemm.cuh", "gemm_common.cuh", "ptx.cuh")]
+# the dominant kernel of each expert format (its gate/up GEMM) and the source
+# files that define it; a stored traffic counter holds while they are unchanged
+DOMINANT = {"bf16": "gate_up", "nvfp4": "fp4_gate_up", "a16": "w4a16_gate_up"}
+DOMINANT_SRC = {k: [os.path.join(ROOT, "group_limited_routed_gb300", "csrc", f) for f in v]
+                for k, v in {
+                    "gate_up": ("expert_gemm.cu", "expert_gemm.cuh", "gemm_common.cuh",
+                                "common.cuh", "ptx.cuh"),
+                    "fp4_gate_up": ("nvfp4.cu", "gemm_common.cuh", "common.cuh", "ptx.cuh"),
+                    "w4a16_gate_up": ("w4a16.cu", "gemm_common.cuh", "common.cuh", "ptx.cuh"),
+                }.items()}
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 
 
@@ -154,7 +161,7 @@ def traffic_for(kernel: str, workload: str):
     with open(TRAFFIC_FILE) as f:
         j = json.load(f)
     ent = j.get(kernel, {}).get(workload)
-    if not ent or ent.get("source_sha") != file_sha(DOMINANT_SRC):
+    if not ent or ent.get("source_sha") != file_sha(DOMINANT_SRC[kernel]):
         return None
     return ent.get("bytes_per_launch")
 
@@ -409,20 +416,21 @@ def run_gpu(args, cfg):
     gu_flops = 4 * cfg.T * cfg.topk * cfg.d * cfg.d_ff
     ridge = pk["bf16_tflops_sustained"] * 1e12 / (pk["hbm_gbs"] * 1e9)
     tensor_bound = not fp4 and gu_flops / gu_bytes > ridge
+    dom = DOMINANT["a16" if a16 else "nvfp4" if fp4 else "bf16"]
     gu_tflops = gu_flops / (stage_ms[4] / 1e3) / 1e12
     if tensor_bound:
-        roofline = {"bound": "tensor", "kernel": DOMINANT, "achieved": gu_tflops,
+        roofline = {"bound": "tensor", "kernel": dom, "achieved": gu_tflops,
                     "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
                     "frac": gu_tflops / pk["bf16_tflops_sustained"],
                     "peak_source": pk["source"] + " (sustained bf16)",
-                    "traffic": traffic_for(DOMINANT, cfg.name),
+                    "traffic": traffic_for(dom, cfg.name),
                     "algorithmic_flops_per_launch": gu_flops,
                     "algorithmic_bytes_per_launch": gu_bytes}
     else:
-        roofline = {"bound": "hbm", "kernel": DOMINANT, "achieved": gu_gbs,
+        roofline = {"bound": "hbm", "kernel": dom, "achieved": gu_gbs,
                     "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": gu_gbs / pk["hbm_gbs"],
                     "peak_source": pk["source"],
-                    "traffic": traffic_for(DOMINANT, cfg.name),
+                    "traffic": traffic_for(dom, cfg.name),
                     "algorithmic_bytes_per_launch": gu_bytes}
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
