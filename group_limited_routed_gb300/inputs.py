@@ -8,7 +8,9 @@ and residual stream": hidden 5120, 256 experts in 8 groups, best 4 groups,
 top 8, d_ff 2560, scale 2.5; HF release post, section "专家混合": 32 experts per
 group).  Distributions: hidden ~ N(0, 1) in BF16; router W_r ~ N(0, 1/d) in
 FP32 stored [E, d]; correction bias ~ U(-0.05, 0.05) in FP32; expert weights
-~ N(0, 0.02^2) in BF16 stored W_gate/W_up [E, F, d] and W_down [E, d, F].
+~ N(0, 0.02^2) in BF16 stored W_gate/W_up [E, F, d] and W_down [E, d, F]
+(NVFP4 and FP8 expert weights are those draws quantised once, here: they are
+the checkpoint both sides read).
 Draw order: hidden, router_w, corr_bias, [skewed experts], w_gate, w_up,
 w_down, one torch.Generator seeded per configuration.  The small configuration
 is drawn on the CPU generator (so any machine reproduces it); the Beam-sized
@@ -34,7 +36,7 @@ class MoEConfig:
     d_ff: int
     routed_scale: float = 2.5
     seed: int = 0
-    weight_fmt: str = "bf16"          # "bf16" or "nvfp4"
+    weight_fmt: str = "bf16"          # "bf16", "nvfp4" or "fp8"
     skew_experts: int = 0             # experts that get +skew_bias
     skew_bias: float = 0.0
     cpu_generator: bool = False       # draw on the CPU generator
@@ -82,6 +84,18 @@ CONFIGS = {
     "nvfp4": MoEConfig(name="nvfp4", T=128, seed=4, weight_fmt="nvfp4", **_BEAM,
                        description="Beam MoE layer NVFP4 experts T=128 (E2M1 + E4M3 per "
                                    "16 along K + FP32 per-tensor scale)"),
+    "fp8": MoEConfig(name="fp8", T=32, seed=9, weight_fmt="fp8", **_BEAM,
+                     description="Beam MoE layer decode batch T=32, dynamic FP8 experts "
+                                 "(E4M3 weights with one FP32 scale per output row; "
+                                 "activations quantised per row at run time)"),
+    "fp8_prefill": MoEConfig(name="fp8_prefill", T=8192, seed=10, weight_fmt="fp8", **_BEAM,
+                             description="Beam MoE layer prefill chunk T=8192, dynamic FP8 "
+                                         "experts"),
+    # profiling case for the FP8 kernels: 32 experts, decode-sized batch
+    "profile_fp8": MoEConfig(name="profile_fp8", T=8, d=5120, n_experts=32, n_groups=8,
+                             topk_groups=4, topk=8, d_ff=2560, seed=11, weight_fmt="fp8",
+                             description="Beam expert shapes, 32 FP8 experts (8x4), T=8 "
+                                         "(profiling case)"),
 }
 
 
@@ -128,13 +142,26 @@ def quantize_nvfp4_weight(w: torch.Tensor):
     return packed, sf8.view(torch.uint8).contiguous(), gs.reshape(1)
 
 
+def quantize_fp8_weight(w: torch.Tensor):
+    """One expert projection [N, K] (float32) -> (E4M3 codes uint8 [N, K], FP32
+    scale per row [N]).  Each output row (channel) maps its amax onto 448, the
+    largest finite E4M3 value; codes round to nearest, ties to even (torch's
+    float8_e4m3fn cast).  Checkpoint-format preparation (per-channel FP8
+    weights of the dynamic FP8 scheme)."""
+    amax = w.abs().amax(dim=1).float()
+    scale = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax))
+    q = (w / scale.unsqueeze(1)).clamp(-448.0, 448.0).to(torch.float8_e4m3fn)
+    return q.view(torch.uint8).contiguous(), scale.contiguous()
+
+
 def generate(cfg: MoEConfig, device="cuda", T: int | None = None,
              weights: bool = True) -> dict:
     """Draw one configuration's tensors on ``device``.
 
     Returns hidden [T,d] bf16, router_w [E,d] f32, corr_bias [E] f32 and, with
     ``weights``, w_gate/w_up [E,F,d] and w_down [E,d,F] in BF16 or, for the
-    NVFP4 format, dicts {'q','sf','gs'} per projection.
+    NVFP4 format, dicts {'q','sf','gs'} per projection, for the FP8 format
+    dicts {'q' uint8 [E,N,K], 's' float32 [E,N]}.
     """
     T = cfg.T if T is None else T
     g, gdev = _gen(cfg, device)
@@ -167,6 +194,13 @@ def generate(cfg: MoEConfig, device="cuda", T: int | None = None,
                     torch.randn(n, k, generator=g, device=gdev) * 0.02)
                 q[e], sf[e], gs[e:e + 1] = wq, wsf, wgs
             res[name] = {"q": q, "sf": sf, "gs": gs}
+        elif cfg.weight_fmt == "fp8":
+            q = torch.empty(E, n, k, dtype=torch.uint8, device=out_dev)
+            sc = torch.empty(E, n, dtype=torch.float32, device=out_dev)
+            for e in range(E):
+                q[e], sc[e] = quantize_fp8_weight(
+                    torch.randn(n, k, generator=g, device=gdev) * 0.02)
+            res[name] = {"q": q, "s": sc}
         else:
             raise ValueError(cfg.weight_fmt)
     return res

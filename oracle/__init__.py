@@ -73,6 +73,10 @@ def _load():
         lib.oracle_boundary.argtypes = [_P, _P, _P, _P, _I64, _I32, ctypes.c_double,
                                         ctypes.c_float, ctypes.c_float, _P, _P]
         lib.oracle_nvfp4_quantize.argtypes = [_P, _I64, _P, _P]
+        lib.oracle_experts_fp8.argtypes = [_P, _I64, _I32, _I32, _I32, _I32, _P, _P,
+                                           _P, _P, _P, _P, _P, _P,
+                                           _I32, _P, _I64, _P, _P]
+        lib.oracle_fp8_quantize_rows.argtypes = [_P, _I64, _I32, _P, _P]
         lib.oracle_num_threads.restype = ctypes.c_int
         lib.oracle_set_threads.argtypes = [ctypes.c_int]
         _lib = lib
@@ -310,6 +314,57 @@ def experts_nvfp4(x_bf16, idx, w, gate, up, down, n_experts: int, act_quant=True
     if rc:
         raise ValueError(f"oracle_experts_nvfp4 failed ({rc})")
     return (out, ex) if exact else out
+
+
+ACT_FP8 = 3
+
+
+def experts_fp8(x_bf16, idx, w, gate, up, down, n_experts: int, act_quant=True,
+                tokens=None, out: np.ndarray | None = None, exact: bool = False):
+    """Dynamic FP8 experts.  gate/up/down are dicts with per-expert 'q' (E4M3
+    codes [N, K]) and 's' (FP32 scale per output row [N]).  act_quant: True /
+    ACT_FP8 quantises both GEMM inputs per row to E4M3 (x per token, h per
+    (token, expert) row after its BF16 rounding); False / ACT_BF16 keeps BF16
+    activations."""
+    mode = int(act_quant)
+    if mode not in (ACT_BF16, 1, ACT_FP8):
+        raise ValueError(f"unknown activation mode {act_quant}")
+    x = _c(x_bf16, np.uint16)
+    T, d = x.shape
+    idx = _c(idx, np.int32)
+    w = _c(w, np.float32)
+    k = idx.shape[1]
+    keep = []
+    tabs = []
+    for p in (gate, up, down):
+        q, kq = _expert_ptrs(p["q"], n_experts)
+        sc, ks = _expert_ptrs(p["s"], n_experts)
+        keep += kq + ks
+        tabs += [ctypes.cast(q, _P), ctypes.cast(sc, _P)]
+    F = _infer_F(gate["q"], d)
+    if out is None:
+        out = np.zeros((T, d), np.uint16)
+    ex = np.zeros((T, d), np.float64) if exact else None
+    tok = None if tokens is None else _c(tokens, np.int64)
+    rc = _load().oracle_experts_fp8(_ptr(x), T, d, F, k, n_experts, _ptr(idx), _ptr(w),
+                                    *tabs, 1 if mode else 0, _ptr(tok),
+                                    0 if tok is None else tok.size, _ptr(out), _ptr(ex))
+    if rc:
+        raise ValueError(f"oracle_experts_fp8 failed ({rc})")
+    return (out, ex) if exact else out
+
+
+def fp8_quantize_rows(x_bf16):
+    """The FP8 path's activation rule on BF16 rows [n, cols]: returns (E4M3
+    codes uint8 [n, cols], FP32 scale per row [n])."""
+    x = _c(x_bf16, np.uint16)
+    n, cols = x.shape
+    q = np.zeros((n, cols), np.uint8)
+    sc = np.zeros(n, np.float32)
+    rc = _load().oracle_fp8_quantize_rows(_ptr(x), n, cols, _ptr(q), _ptr(sc))
+    if rc:
+        raise ValueError(f"oracle_fp8_quantize_rows failed ({rc})")
+    return q, sc
 
 
 def _infer_F(ws, inner: int) -> int:

@@ -306,9 +306,53 @@ typedef struct {
   const uint8_t *const *qg, *const *qu, *const *qd;
   const uint8_t *const *sfg, *const *sfu, *const *sfd;
   const float *gsg, *gsu, *gsd;
+  /* FP8 weights: E4M3 codes [N, K], one FP32 scale per output row [N]. */
+  const uint8_t *const *eg, *const *eu, *const *ed;
+  const float *const *seg, *const *seu, *const *sed;
   int fp4;
+  int fp8;
   int act_quant;
 } weights_t;
+
+/* One row of the dynamic FP8 scheme's activation rule (per token, or per
+ * (token, expert) row of the down GEMM's input): scale = amax / 448 in FP32
+ * (1 for an all-zero row), code_i = E4M3(v_i / scale) with FP32 divisions,
+ * round to nearest even, saturating at 448.  The E4M3 magnitudes are tabled
+ * from the format definition once per row; the search over them is the same
+ * exhaustive nearest-even rule as e4m3_encode.  Writes codes and scale when
+ * asked, and the dequantised values code * scale when out is given. */
+static void fp8_row_quantize(const float *v, int64_t n, uint8_t *q, float *scale_out,
+                             double *out) {
+  double mag[127];
+  for (int c = 0; c < 127; ++c) mag[c] = e4m3_value((uint8_t)c);
+  float amax = 0.0f;
+  for (int64_t i = 0; i < n; ++i) {
+    float a = fabsf(v[i]);
+    if (a > amax) amax = a;
+  }
+  const float scale = amax > 0.0f ? amax / 448.0f : 1.0f;
+  for (int64_t i = 0; i < n; ++i) {
+    const float r = v[i] / scale;
+    const double a = fabs((double)r);
+    int best = 0;
+    double best_err = fabs(a - mag[0]);
+    for (int c = 1; c < 127; ++c) {
+      double err = fabs(a - mag[c]);
+      if (err < best_err || (err == best_err && (best & 1) && !(c & 1))) {
+        best = c;
+        best_err = err;
+      }
+    }
+    const uint8_t code = (uint8_t)(signbit(r) ? (best | 0x80) : best);
+    if (q) q[i] = code;
+    if (out) out[i] = e4m3_value(code) * (double)scale;
+  }
+  if (scale_out) *scale_out = scale;
+}
+
+static double fp8_weight(const uint8_t *q, const float *s, int64_t row, int64_t col, int64_t K) {
+  return e4m3_value(q[row * K + col]) * (double)s[row];
+}
 
 /* One NVFP4 block of 16: the activation rule used on both GEMM inputs of the
  * NVFP4 path (global scale 1): scale = E4M3(amax / 6), code_i =
@@ -350,7 +394,9 @@ static int experts_impl(const uint16_t *x, int64_t T, int32_t d, int32_t F,
     for (int32_t j = 0; j < k; ++j) {
       int32_t e = idx[t * k + j];
       if (e < 0 || e >= E) { err = -1; break; }
-      if (W->fp4 ? (!W->qg[e] || !W->qu[e] || !W->qd[e]) : (!W->wg[e] || !W->wu[e] || !W->wd[e])) {
+      if (W->fp4   ? (!W->qg[e] || !W->qu[e] || !W->qd[e])
+          : W->fp8 ? (!W->eg[e] || !W->eu[e] || !W->ed[e])
+                   : (!W->wg[e] || !W->wu[e] || !W->wd[e])) {
         err = -2;
         break;
       }
@@ -374,7 +420,10 @@ static int experts_impl(const uint16_t *x, int64_t T, int32_t d, int32_t F,
         const uint16_t *xr = x + t * (int64_t)d;
         /* the expert input row (NVFP4 path may quantise it, or take it in
            F16 for the F16 tensor-core operands) */
-        if (W->fp4 && W->act_quant == 2) {
+        if (W->fp8 && W->act_quant) {
+          for (int32_t j = 0; j < d; ++j) tmp[j] = (float)bf16_value(xr[j]);
+          fp8_row_quantize(tmp, d, NULL, NULL, xin);
+        } else if (W->fp4 && W->act_quant == 2) {
           for (int32_t j = 0; j < d; ++j) xin[j] = f16_round_value(bf16_value(xr[j]));
         } else if (W->fp4 && W->act_quant) {
           for (int32_t j = 0; j < d; ++j) tmp[j] = (float)bf16_value(xr[j]);
@@ -394,6 +443,11 @@ static int experts_impl(const uint16_t *x, int64_t T, int32_t d, int32_t F,
                 ga += xin[j] * fp4_weight(W->qg[e], W->sfg[e], W->gsg[e], f, j, d);
                 ua += xin[j] * fp4_weight(W->qu[e], W->sfu[e], W->gsu[e], f, j, d);
               }
+            } else if (W->fp8) {
+              for (int32_t j = 0; j < d; ++j) {
+                ga += xin[j] * fp8_weight(W->eg[e], W->seg[e], f, j, d);
+                ua += xin[j] * fp8_weight(W->eu[e], W->seu[e], f, j, d);
+              }
             } else {
               const uint16_t *gr = W->wg[e] + (int64_t)f * d;
               const uint16_t *ur = W->wu[e] + (int64_t)f * d;
@@ -408,7 +462,11 @@ static int experts_impl(const uint16_t *x, int64_t T, int32_t d, int32_t F,
             hf[f] = (float)(silu * u);
           }
           /* the down GEMM's input */
-          if (W->fp4 && W->act_quant == 2) {
+          if (W->fp8 && W->act_quant) {
+            /* h keeps its BF16 rounding, then the row is quantised */
+            for (int32_t f = 0; f < F; ++f) tmp[f] = (float)bf16_value(bf16_round(hf[f]));
+            fp8_row_quantize(tmp, F, NULL, NULL, hin);
+          } else if (W->fp4 && W->act_quant == 2) {
             for (int32_t f = 0; f < F; ++f) hin[f] = f16_round_value((double)hf[f]);
           } else if (W->fp4 && W->act_quant) {
             for (int32_t f = 0; f < F; f += 16) nvfp4_block_roundtrip(hf + f, hin + f);
@@ -421,6 +479,9 @@ static int experts_impl(const uint16_t *x, int64_t T, int32_t d, int32_t F,
             if (W->fp4) {
               for (int32_t f = 0; f < F; ++f)
                 ya += hin[f] * fp4_weight(W->qd[e], W->sfd[e], W->gsd[e], r, f, F);
+            } else if (W->fp8) {
+              for (int32_t f = 0; f < F; ++f)
+                ya += hin[f] * fp8_weight(W->ed[e], W->sed[e], r, f, F);
             } else {
               const uint16_t *dr = W->wd[e] + (int64_t)r * F;
               for (int32_t f = 0; f < F; ++f) ya += hin[f] * bf16_value(dr[f]);
@@ -509,6 +570,49 @@ int oracle_experts_nvfp4(const uint16_t *x, int64_t T, int32_t d, int32_t F,
   W.fp4 = 1;
   W.act_quant = act_quant;
   return experts_impl(x, T, d, F, k, E, idx, w, &W, tokens, n_tokens, out, out_exact);
+}
+
+/* Dynamic FP8 experts (the pages list a compressed-tensors dynamic FP8
+ * checkpoint beside the BF16 and NVFP4 ones: SGLang post, sections
+ * "Highlights" and "BF16, NVFP4 and FP8 Model Support"; HF release post,
+ * sections "专家混合" and "硬件要求").  [reading] The FP8 scheme is the usual dynamic one:
+ * E4M3 weights with one FP32 scale per output row (each weight is exactly
+ * code x scale); with act_quant != 0 both GEMM inputs are quantised per row
+ * at run time with fp8_row_quantize -- x per token along d, and h per
+ * (token, expert) row along F after its BF16 rounding (h is BF16 between
+ * the GEMMs in every path).  act_quant = 0 keeps BF16 activations exactly as
+ * in the BF16 path.  Everything else (FP32 accumulators and SwiGLU product,
+ * weighted FP64 sum, one BF16 rounding) is the BF16 path's. */
+int oracle_experts_fp8(const uint16_t *x, int64_t T, int32_t d, int32_t F,
+                       int32_t k, int32_t E, const int32_t *idx, const float *w,
+                       const uint8_t *const *qg, const float *const *sg,
+                       const uint8_t *const *qu, const float *const *su,
+                       const uint8_t *const *qd, const float *const *sd,
+                       int32_t act_quant, const int64_t *tokens, int64_t n_tokens,
+                       uint16_t *out, double *out_exact) {
+  weights_t W;
+  memset(&W, 0, sizeof W);
+  W.eg = qg; W.seg = sg;
+  W.eu = qu; W.seu = su;
+  W.ed = qd; W.sed = sd;
+  W.fp8 = 1;
+  W.act_quant = act_quant;
+  return experts_impl(x, T, d, F, k, E, idx, w, &W, tokens, n_tokens, out, out_exact);
+}
+
+/* The activation rule of the FP8 path on n rows of `cols` BF16 values:
+ * codes [n, cols] and one FP32 scale per row. */
+int oracle_fp8_quantize_rows(const uint16_t *x, int64_t n, int32_t cols, uint8_t *q,
+                             float *scale) {
+  if (n < 0 || cols <= 0) return -1;
+  float *tmp = (float *)malloc(sizeof(float) * (size_t)cols);
+  if (!tmp) return -3;
+  for (int64_t i = 0; i < n; ++i) {
+    for (int32_t j = 0; j < cols; ++j) tmp[j] = (float)bf16_value(x[i * cols + j]);
+    fp8_row_quantize(tmp, cols, q + i * cols, scale + i, NULL);
+  }
+  free(tmp);
+  return 0;
 }
 
 /* ------------------------------------------------------------------------ */

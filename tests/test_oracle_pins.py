@@ -519,3 +519,106 @@ def test_swiglu_rows_through_the_expert_layer():
                                 inputs.bf16_bits(wu), inputs.bf16_bits(eye), 1)
     h = oracle.swiglu_bf16(inputs.bf16_bits(x), inputs.bf16_bits(wg[0]), inputs.bf16_bits(wu[0]))
     assert np.array_equal(layer, h)
+
+
+# ------------------------------------------------------------ dynamic FP8
+def _fp8_torch_rows(x):
+    """Per-row FP8 quantisation written with torch's own float8_e4m3fn cast
+    (round to nearest even) for the rounding step."""
+    xf = x.float()
+    amax = xf.abs().amax(dim=1)
+    scale = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax))
+    q = (xf / scale.unsqueeze(1)).to(torch.float8_e4m3fn)
+    return q, scale
+
+
+def test_fp8_row_quantizer_vs_torch():
+    n, cols = 40, 96
+    mag = np.exp(RNG.uniform(-12, 6, n))[:, None]
+    x = torch.from_numpy((RNG.standard_normal((n, cols)) * mag).astype(np.float32))
+    x[3] = 0.0                                    # an all-zero row: scale 1, codes 0
+    x[4, :] = 1.0
+    x[4, 0] = -2.0                                # exact grid values, amax -> -448
+    x = x.to(torch.bfloat16)
+    q, sc = oracle.fp8_quantize_rows(inputs.bf16_bits(x))
+    q_ref, sc_ref = _fp8_torch_rows(x)
+    assert np.array_equal(sc, sc_ref.numpy())
+    assert np.array_equal(q, q_ref.view(torch.uint8).numpy())
+    assert sc[3] == 1.0 and not q[3].any()
+    assert q[4, 0] == 0xFE and np.all(q[4, 1:] == 0x76)         # -448 and 224
+    # the element of largest magnitude always lands on +-448
+    big = np.abs(x.float().numpy()).argmax(axis=1)
+    for i in range(n):
+        if i != 3:
+            assert q[i, big[i]] & 0x7F == 0x7E
+
+
+def test_fp8_generator_weights_round_trip_grid_values():
+    """Rows already on an E4M3 grid (one power-of-two scale per row, each row
+    reaching 448) come back unchanged from the checkpoint quantiser."""
+    n, kk = 8, 64
+    codes = RNG.integers(0, 127, (n, kk)) | (RNG.integers(0, 2, (n, kk)) << 7)
+    vals = np.vectorize(oracle.e4m3_value)(codes)
+    vals[:, 0] = 448.0
+    w = torch.from_numpy(vals * (2.0 ** RNG.integers(-12, -4, n))[:, None]).float()
+    q, s = inputs.quantize_fp8_weight(w)
+    back = np.vectorize(oracle.e4m3_value)(q.numpy()) * s.double().numpy()[:, None]
+    assert np.array_equal(back, w.double().numpy())
+
+
+def _fp8_weights(E, n, kk, pow2_scales):
+    codes = (RNG.integers(0, 127, (E, n, kk)) | (RNG.integers(0, 2, (E, n, kk)) << 7))
+    codes = codes.astype(np.uint8)
+    if pow2_scales:
+        s = (2.0 ** RNG.integers(-12, -6, (E, n))).astype(np.float32)
+    else:
+        s = (RNG.uniform(0.5, 2.0, (E, n)) * 2.0 ** -10).astype(np.float32)
+    deq = np.vectorize(oracle.e4m3_value)(codes) * s.astype(np.float64)[:, :, None]
+    return {"q": codes, "s": s}, torch.from_numpy(deq)
+
+
+def test_fp8_weights_equal_bf16_when_exactly_representable():
+    """An E4M3 value (4 significant bits) times a power of two is a BF16
+    value, so with BF16 activations the FP8 and BF16 oracle paths agree bit
+    for bit: this pins the weight decoding (codes and row scales)."""
+    T, d, F, E = 6, 64, 32, 8
+    x = _bf16_matrix((T, d))
+    r = _route(RNG.standard_normal((T, E)), np.zeros(E), 4, 2, 3)
+    proj, deq = {}, {}
+    for name, (n, kk) in (("g", (F, d)), ("u", (F, d)), ("d", (d, F))):
+        proj[name], full = _fp8_weights(E, n, kk, pow2_scales=True)
+        t = full.to(torch.bfloat16)
+        assert torch.equal(t.double(), full)
+        deq[name] = inputs.bf16_bits(t)
+    a = oracle.experts_fp8(inputs.bf16_bits(x), r["idx"], r["w"], proj["g"], proj["u"], proj["d"],
+                           E, act_quant=False)
+    b = oracle.experts_bf16(inputs.bf16_bits(x), r["idx"], r["w"], deq["g"], deq["u"], deq["d"], E)
+    assert np.array_equal(a, b)
+
+
+def test_fp8_activation_experts_match_dense_torch():
+    """FP8 weights and per-row FP8 activations: the expert layer against a
+    dense torch FP64 restatement that quantises x and the BF16 h rows with
+    torch's float8_e4m3fn cast."""
+    T, d, F, E = 5, 64, 32, 8
+    x = _bf16_matrix((T, d))
+    r = _route(RNG.standard_normal((T, E)), np.zeros(E), 4, 2, 3)
+    proj, deq = {}, {}
+    for name, (n, kk) in (("g", (F, d)), ("u", (F, d)), ("d", (d, F))):
+        proj[name], deq[name] = _fp8_weights(E, n, kk, pow2_scales=False)
+    out, ex = oracle.experts_fp8(inputs.bf16_bits(x), r["idx"], r["w"], proj["g"], proj["u"],
+                                 proj["d"], E, act_quant=True, exact=True)
+    qx, sx = _fp8_torch_rows(x)
+    xh = qx.double() * sx.double().unsqueeze(1)
+    ref = torch.zeros(T, d, dtype=torch.float64)
+    for t in range(T):
+        for j in range(3):
+            e = int(r["idx"][t, j])
+            g = (xh[t] @ deq["g"][e].T).float().double()
+            u = (xh[t] @ deq["u"][e].T).float().double()
+            h = (g / (1 + torch.exp(-g)) * u).float().to(torch.bfloat16)
+            qh, sh = _fp8_torch_rows(h.unsqueeze(0))
+            hh = qh.double()[0] * float(sh[0])
+            ref[t] += float(r["w"][t, j]) * (hh @ deq["d"][e].T)
+    assert np.allclose(ex, ref.numpy(), rtol=1e-12, atol=1e-12)
+    assert np.array_equal(out, inputs.bf16_bits(ref.float().to(torch.bfloat16)))
