@@ -230,23 +230,24 @@ def run_reference(args, cfg):
     dev = torch.device("cuda", local) if torch.cuda.is_available() else torch.device("cpu")
     gen_cfg = cfg if dev.type == "cuda" else cfg.replace(cpu_generator=True)
     t = inputs.generate(gen_cfg, dev)
+    a16 = cfg.weight_fmt == "nvfp4" and args.a16
     # size each step so the whole run stays within about two minutes
     sec1, _ = oracle_sample(cfg, t, 1, seed=1, a16=a16)
     per_step_budget = 120.0 / max(1, args.steps + args.warmup)
     n = int(max(1, min(cfg.T, per_step_budget / max(sec1, 1e-6))))
     for i in range(args.warmup):
-        oracle_sample(cfg, t, n, seed=100 + i)
+        oracle_sample(cfg, t, n, seed=100 + i, a16=a16)
     secs = 0.0
     toks = 0
     for i in range(args.steps):
-        s, m = oracle_sample(cfg, t, n, seed=1000 + i)
+        s, m = oracle_sample(cfg, t, n, seed=1000 + i, a16=a16)
         secs += s
         toks += m
     value = toks / secs
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": config_record(cfg, None),
+            "data": "synthetic", "config": config_record(cfg, None, a16=a16),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(),
                              "kind": "oracle",
                              "sample": f"{n} sampled tokens of the {cfg.T}-token batch per step"},

@@ -52,3 +52,23 @@ def test_reference_arm_runs_on_rank_zero_only(monkeypatch):
     monkeypatch.setenv("WORLD_SIZE", "2")
     args = bench.main.__globals__["argparse"].Namespace(steps=3, warmup=3)
     assert bench.run_reference(args, bench.inputs.CONFIGS["decode"]) == 0
+
+
+def test_reference_arm_prints_its_line_on_cpu():
+    """The whole reference arm (the oracle, timed) on the small configuration,
+    run as the driver runs it; the JSON line carries the contract's keys."""
+    import json
+    import subprocess
+    import sys
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="")
+    env.pop("RANK", None)
+    env.pop("WORLD_SIZE", None)
+    r = subprocess.run([sys.executable, bench.__file__, "--impl", "reference", "--config", "tiny",
+                        "--steps", "2", "--warmup", "1"], capture_output=True, text=True,
+                       env=env, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    line = json.loads([x for x in r.stdout.splitlines() if x.startswith("{")][-1])
+    assert line["impl"] == "reference" and line["value"] > 0 and line["steps"] == 2
+    for k in ("metric", "unit", "higher_is_better", "config", "cpu_baseline", "e2e"):
+        assert k in line, k
+    assert line["cpu_baseline"]["kind"] == "oracle"
