@@ -44,13 +44,16 @@ UNIT = "tokens/s"
 STAGES = ["router", "select", "permute", "gather", "gate_up", "down", "combine"]
 # the dominant kernel of each expert format (its gate/up GEMM) and the source
 # files that define it; a stored traffic counter holds while they are unchanged
-DOMINANT = {"bf16": "gate_up", "nvfp4": "fp4_gate_up", "a16": "w4a16_gate_up"}
+DOMINANT = {"bf16": "gate_up", "nvfp4": "fp4_gate_up", "a16": "w4a16_gate_up",
+            "fp8": "fp8_gate_up"}
 DOMINANT_SRC = {k: [os.path.join(ROOT, "group_limited_routed_gb300", "csrc", f) for f in v]
                 for k, v in {
                     "gate_up": ("expert_gemm.cu", "expert_gemm.cuh", "gemm_common.cuh",
                                 "common.cuh", "ptx.cuh"),
                     "fp4_gate_up": ("nvfp4.cu", "gemm_common.cuh", "common.cuh", "ptx.cuh"),
                     "w4a16_gate_up": ("w4a16.cu", "gemm_common.cuh", "common.cuh", "ptx.cuh"),
+                    "fp8_gate_up": ("expert_gemm.cu", "expert_gemm.cuh", "gemm_common.cuh",
+                                    "common.cuh", "ptx.cuh"),
                 }.items()}
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 
@@ -184,6 +187,10 @@ def oracle_sample(cfg, t, n_tokens: int, seed: int = 0, a16: bool = False):
         proj = [{"q": {e: p["q"][e].cpu().numpy() for e in need},
                  "sf": {e: p["sf"][e].cpu().numpy() for e in need},
                  "gs": p["gs"].cpu().numpy()} for p in (t["w_gate"], t["w_up"], t["w_down"])]
+    elif cfg.weight_fmt == "fp8":
+        proj = [{"q": {e: p["q"][e].cpu().numpy() for e in need},
+                 "s": {e: p["s"][e].cpu().numpy() for e in need}}
+                for p in (t["w_gate"], t["w_up"], t["w_down"])]
     else:
         proj = [{e: inputs.bf16_bits(t[n][e]) for e in need} for n in ("w_gate", "w_up", "w_down")]
     t0 = time.perf_counter()
@@ -192,6 +199,8 @@ def oracle_sample(cfg, t, n_tokens: int, seed: int = 0, a16: bool = False):
     if cfg.weight_fmt == "nvfp4":
         oracle.experts_nvfp4(x[rows], r["idx"], r["w"], *proj, cfg.n_experts,
                              act_quant=oracle.ACT_F16 if a16 else oracle.ACT_NVFP4)
+    elif cfg.weight_fmt == "fp8":
+        oracle.experts_fp8(x[rows], r["idx"], r["w"], *proj, cfg.n_experts, act_quant=True)
     else:
         oracle.experts_bf16(x[rows], r["idx"], r["w"], *proj, cfg.n_experts)
     return time.perf_counter() - t0, len(rows)
@@ -285,8 +294,9 @@ def run_gpu(args, cfg):
         dist.init_process_group("nccl", device_id=dev)
     t = inputs.generate(cfg.replace(seed=cfg.seed + 1000 * rank) if rank else cfg, dev)
     fp4 = cfg.weight_fmt == "nvfp4"
+    fp8 = cfg.weight_fmt == "fp8"
     a16 = fp4 and args.a16
-    fmt = (pkg.NVFP4_A16 if a16 else pkg.NVFP4) if fp4 else 0
+    fmt = (pkg.NVFP4_A16 if a16 else pkg.NVFP4) if fp4 else pkg.FP8 if fp8 else 0
     ws = pkg.Workspace(cfg, cfg.T, dev, weight_fmt=fmt)
     stream = torch.cuda.current_stream()
     out = torch.empty(cfg.T, cfg.d, dtype=torch.bfloat16, device=dev)
@@ -296,6 +306,12 @@ def run_gpu(args, cfg):
 
         def layer(x, o):
             return fwd(cfg, x, t["router_w"], t["corr_bias"], *wts, out=o, ws=ws, stream=torch.cuda.current_stream())
+    elif fp8:
+        wts = [pkg.Fp8Weight.of(t[n]) for n in ("w_gate", "w_up", "w_down")]
+
+        def layer(x, o):
+            return pkg.forward_fp8(cfg, x, t["router_w"], t["corr_bias"], *wts, out=o, ws=ws,
+                                   stream=torch.cuda.current_stream())
     elif args.routed:
         # routing replay: the routes are recorded once, the timed steps run
         # the experts and the combine on them
@@ -401,29 +417,42 @@ def run_gpu(args, cfg):
     e2e_value = job_throughput(world, cfg.T, e2e_steps, e2e_ms)
 
     pk = peaks()
-    # weight bytes of one projection of one expert: BF16, or E2M1 + E4M3 per 16
-    E_b = cfg.d * cfg.d_ff * 2 if not fp4 else cfg.d * cfg.d_ff // 2 + cfg.d * cfg.d_ff // 16
-    tok_b = 2 if (not fp4 or a16) else 0.5625
-    gu_bytes = touched * 2 * E_b + cfg.T * cfg.topk * (cfg.d + cfg.d_ff) * tok_b
+    # weight bytes of one projection of one expert: BF16, E2M1 + E4M3 per 16,
+    # or E4M3 + one FP32 scale per row (d_ff rows for gate/up, d for down)
+    E_b = (cfg.d * cfg.d_ff // 2 + cfg.d * cfg.d_ff // 16 if fp4
+           else cfg.d * cfg.d_ff if fp8 else cfg.d * cfg.d_ff * 2)
+    sc_b = 4 if fp8 else 0
+    # gate/up token bytes per (token, expert) row: its input row and its h
+    # row (E4M3 in, BF16 out for FP8)
+    TK = cfg.T * cfg.topk
+    if fp8:
+        tok_rows = TK * (cfg.d + 2 * cfg.d_ff + 4)
+    else:
+        tok_rows = TK * (cfg.d + cfg.d_ff) * (2 if (not fp4 or a16) else 0.5625)
+    gu_bytes = touched * 2 * (E_b + sc_b * cfg.d_ff) + tok_rows
     gu_gbs = gu_bytes / (stage_ms[4] / 1e3) / 1e9
-    layer_bytes = touched * 3 * E_b + cfg.n_experts * cfg.d * 4 + cfg.n_experts * 4 \
-        + 2 * cfg.T * cfg.d * 2
+    layer_bytes = touched * (3 * E_b + sc_b * (2 * cfg.d_ff + cfg.d)) + cfg.n_experts * cfg.d * 4 \
+        + cfg.n_experts * 4 + 2 * cfg.T * cfg.d * 2
     layer_ms = ms / args.steps
     layer_flops = 2 * cfg.T * cfg.d * cfg.n_experts + 6 * cfg.T * cfg.topk * cfg.d * cfg.d_ff
     # The dominant kernel's bound: tensor when its flops per algorithmic byte
-    # exceed the measured ridge (sustained BF16 peak / copy bandwidth), else
-    # HBM.  It is timed inside the step, so the tensor peak is the sustained
-    # one.  (NVFP4 batches here are far below any ridge.)
+    # exceed the measured ridge (sustained tensor peak of its dtype / copy
+    # bandwidth), else HBM.  It is timed inside the step, so the tensor peak
+    # is the sustained one; FP8 takes the measured BF16 peak times the
+    # nominal FP8 / BF16 ratio (4.5 / 2.25).  (NVFP4 batches here are far
+    # below any ridge.)
     gu_flops = 4 * cfg.T * cfg.topk * cfg.d * cfg.d_ff
-    ridge = pk["bf16_tflops_sustained"] * 1e12 / (pk["hbm_gbs"] * 1e9)
+    tc_peak = pk["bf16_tflops_sustained"] * (2.0 if fp8 else 1.0)
+    ridge = tc_peak * 1e12 / (pk["hbm_gbs"] * 1e9)
     tensor_bound = not fp4 and gu_flops / gu_bytes > ridge
-    dom = DOMINANT["a16" if a16 else "nvfp4" if fp4 else "bf16"]
+    dom = DOMINANT["a16" if a16 else "nvfp4" if fp4 else "fp8" if fp8 else "bf16"]
     gu_tflops = gu_flops / (stage_ms[4] / 1e3) / 1e12
     if tensor_bound:
         roofline = {"bound": "tensor", "kernel": dom, "achieved": gu_tflops,
-                    "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
-                    "frac": gu_tflops / pk["bf16_tflops_sustained"],
-                    "peak_source": pk["source"] + " (sustained bf16)",
+                    "peak": tc_peak, "unit": "TFLOP/s",
+                    "frac": gu_tflops / tc_peak,
+                    "peak_source": pk["source"] + (" (sustained bf16 x 2, the nominal fp8 ratio)"
+                                                   if fp8 else " (sustained bf16)"),
                     "traffic": traffic_for(dom, cfg.name),
                     "algorithmic_flops_per_launch": gu_flops,
                     "algorithmic_bytes_per_launch": gu_bytes}
@@ -438,7 +467,7 @@ def run_gpu(args, cfg):
         "warmup": args.warmup, "ms_per_step": layer_ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
         "dtype": ("nvfp4 weights x f16 activations" if a16 else "nvfp4 (e2m1 x e4m3 per 16)")
-        if fp4 else "bf16", "data": "synthetic",
+        if fp4 else "fp8 (e4m3, fp32 scale per row)" if fp8 else "bf16", "data": "synthetic",
         "config": config_record(cfg, touched, args.routed, a16, args.graph),
         "roofline": roofline,
         "layer_roofline": {"bound": "hbm", "algorithmic_bytes": layer_bytes,
@@ -446,8 +475,9 @@ def run_gpu(args, cfg):
                            "peak": pk["hbm_gbs"], "unit": "GB/s",
                            "frac": layer_bytes / (layer_ms / 1e3) / 1e9 / pk["hbm_gbs"],
                            "tflops": layer_flops / (layer_ms / 1e3) / 1e12,
+                           "tflops_peak_sustained": tc_peak,
                            "tflops_frac_sustained":
-                               layer_flops / (layer_ms / 1e3) / 1e12 / pk["bf16_tflops_sustained"]},
+                               layer_flops / (layer_ms / 1e3) / 1e12 / tc_peak},
         "stage_us": {n: round(float(v) * 1e3, 1) for n, v in zip(STAGES, stage_ms)},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": cfg.T * cfg.d * 2,
                 "d2h_bytes_per_step": cfg.T * cfg.d * 2},

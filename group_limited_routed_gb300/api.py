@@ -35,7 +35,7 @@ EXPORTS = ("beam_moe_workspace_size", "beam_moe_workspace_layout", "beam_moe_rou
            "beam_moe_kernels_per_forward", "beam_status_string", "beam_moe_ep_dispatch",
            "beam_moe_ep_workspace_size", "beam_moe_ep_experts", "beam_moe_ep_combine",
            "beam_moe_forward_boundary", "beam_moe_forward_nvfp4_a16",
-           "beam_moe_ep_experts_nvfp4")
+           "beam_moe_ep_experts_nvfp4", "beam_moe_forward_fp8", "beam_moe_fp8_quantize_rows")
 
 
 class BeamError(RuntimeError):
@@ -47,7 +47,8 @@ class BeamError(RuntimeError):
 class _Layout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in (
         "status", "logits", "topk_idx", "topk_w", "counts", "offsets", "perm_src", "pair_row",
-        "perm_w", "x_perm", "h", "x_fp4", "x_sf", "h_fp4", "h_sf", "y", "total")]
+        "perm_w", "x_perm", "h", "x_fp4", "x_sf", "h_fp4", "h_sf", "y", "x_fp8", "x_scale",
+        "h_fp8", "h_scale", "total")]
 
 
 class _Boundary(ctypes.Structure):
@@ -58,6 +59,10 @@ class _Boundary(ctypes.Structure):
 
 class _Fp4Weight(ctypes.Structure):
     _fields_ = [("q", ctypes.c_void_p), ("sf", ctypes.c_void_p), ("global_scale", ctypes.c_void_p)]
+
+
+class _Fp8Weight(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("scale", ctypes.c_void_p)]
 
 
 def library_path() -> str:
@@ -97,6 +102,12 @@ def lib():
         L.beam_moe_forward_nvfp4_a16.argtypes = [cfgp, _P, _P, _P, fp4p, fp4p, fp4p, _P, _I64,
                                                  _P, _SZ, _P]
         L.beam_moe_forward_nvfp4_a16.restype = _ST
+        fp8p = ctypes.POINTER(_Fp8Weight)
+        L.beam_moe_forward_fp8.argtypes = [cfgp, _P, _P, _P, fp8p, fp8p, fp8p, _P, _I64, _P,
+                                           _SZ, _P]
+        L.beam_moe_forward_fp8.restype = _ST
+        L.beam_moe_fp8_quantize_rows.argtypes = [_P, _I64, ctypes.c_int32, _P, _P, _P]
+        L.beam_moe_fp8_quantize_rows.restype = _ST
         L.beam_moe_nvfp4_pack_scales.argtypes = [_P, _I64, _I64, _P, _P]
         L.beam_moe_nvfp4_pack_scales.restype = _ST
         L.beam_moe_check_status.argtypes = [_P, _P]
@@ -390,6 +401,54 @@ def forward_nvfp4_a16(cfg, hidden, router_w, corr_bias, gate: Fp4Weight, up: Fp4
                                             ws.nbytes, _stream(stream)),
            "beam_moe_forward_nvfp4_a16")
     return o
+
+
+FP8 = 3
+
+
+class Fp8Weight:
+    """One dynamic-FP8 projection: E4M3 codes q [E, N, K] (uint8) and one
+    FP32 scale per output row [E, N]."""
+
+    def __init__(self, q: torch.Tensor, scale: torch.Tensor):
+        self.q = q.contiguous()
+        self.scale = scale.contiguous()
+        self._c = _Fp8Weight(_dev(self.q, torch.uint8, "q"),
+                             _dev(self.scale, torch.float32, "scale"))
+
+    @classmethod
+    def of(cls, d: dict) -> "Fp8Weight":
+        return cls(d["q"], d["s"])
+
+
+def forward_fp8(cfg, hidden, router_w, corr_bias, gate: Fp8Weight, up: Fp8Weight,
+                down: Fp8Weight, out=None, ws: Workspace | None = None, stream=None):
+    """The whole layer with dynamic FP8 experts (E4M3 weights with per-row
+    scales; token rows and h quantised per row at run time)."""
+    T = hidden.shape[0]
+    if ws is None:
+        ws = Workspace(cfg, max(int(T), 1), hidden.device, weight_fmt=FP8)
+    o = torch.empty(T, cfg.d, dtype=torch.bfloat16, device=hidden.device) if out is None else out
+    c = _cfg(cfg)
+    _check(lib().beam_moe_forward_fp8(ctypes.byref(c), _dev(hidden, torch.bfloat16, "hidden"),
+                                      _dev(router_w, torch.float32, "router_w"),
+                                      _dev(corr_bias, torch.float32, "corr_bias"),
+                                      ctypes.byref(gate._c), ctypes.byref(up._c),
+                                      ctypes.byref(down._c), o.data_ptr(), T, ws.ptr, ws.nbytes,
+                                      _stream(stream)), "beam_moe_forward_fp8")
+    return o
+
+
+def fp8_quantize_rows(x: torch.Tensor, stream=None):
+    """BF16 rows [n, cols] -> (E4M3 codes uint8 [n, cols], FP32 scales [n]),
+    the FP8 path's activation rule (beam_moe_fp8_quantize_rows)."""
+    n, cols = x.shape
+    q = torch.empty(n, cols, dtype=torch.uint8, device=x.device)
+    sc = torch.empty(n, dtype=torch.float32, device=x.device)
+    _check(lib().beam_moe_fp8_quantize_rows(_dev(x, torch.bfloat16, "x"), n, cols, q.data_ptr(),
+                                            sc.data_ptr(), _stream(stream)),
+           "beam_moe_fp8_quantize_rows")
+    return q, sc
 
 
 def check_status(ws: Workspace, stream=None) -> int:

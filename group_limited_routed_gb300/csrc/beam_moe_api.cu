@@ -153,8 +153,13 @@ bool fused_routing(const beam_moe_config_t& c, int64_t T) {
 
 struct Layout {
   size_t status, part, logits, idx, w, counts, offsets, perm_src, pair_row, perm_w, x_perm, h, y,
-      router_planes, x_fp4, x_sf, h_fp4, h_sf, total;
+      router_planes, x_fp4, x_sf, h_fp4, h_sf, x_fp8, x_scale, h_fp8, h_scale, total;
 };
+
+bool known_fmt(int32_t fmt) {
+  return fmt == BEAM_WEIGHTS_BF16 || fmt == BEAM_WEIGHTS_NVFP4 || fmt == BEAM_WEIGHTS_NVFP4_A16 ||
+         fmt == BEAM_WEIGHTS_FP8;
+}
 
 // NVFP4 token-block width: the token scales are read row-major, 32 rows at most
 int fp4_tile(const beam_moe_config_t& c, int64_t TK) { return small_batch(c, TK) ? 16 : 32; }
@@ -162,6 +167,7 @@ int fp4_tile(const beam_moe_config_t& c, int64_t TK) { return small_batch(c, TK)
 Layout make_layout(const beam_moe_config_t& c, int64_t T_max, int32_t fmt = BEAM_WEIGHTS_BF16) {
   const bool fp4 = fmt == BEAM_WEIGHTS_NVFP4;
   const bool a16 = fmt == BEAM_WEIGHTS_NVFP4_A16;  // F16 token rows gathered into x_perm
+  const bool fp8 = fmt == BEAM_WEIGHTS_FP8;         // E4M3 token rows (gathered when large)
   const int64_t E = c.n_experts, k = c.topk;
   const int64_t TK = T_max * k;
   const int64_t rows = std::max<int64_t>(TK, kMinRows);
@@ -187,7 +193,10 @@ Layout make_layout(const beam_moe_config_t& c, int64_t T_max, int32_t fmt = BEAM
   L.perm_src = take(static_cast<size_t>(TK) * 4);
   L.pair_row = take(static_cast<size_t>(TK) * 4);
   L.perm_w = take(static_cast<size_t>(TK) * 4);
-  L.x_perm = take(!a16 && (fp4 || small_batch(c, TK)) ? 0 : static_cast<size_t>(rows) * c.d * 2);
+  // gathered token rows: F16 (W4A16), E4M3 (FP8) or BF16, the last two only
+  // for batches that do not gather inside the gate/up GEMM
+  const size_t xrow = static_cast<size_t>(rows) * c.d;
+  L.x_perm = take(a16 ? xrow * 2 : fp4 || small_batch(c, TK) ? 0 : fp8 ? xrow : xrow * 2);
   L.h = take(fp4 ? 0 : static_cast<size_t>(rows) * c.d_ff * 2);
   L.y = take(static_cast<size_t>(rows) * c.d * 4);
   L.router_planes = take(T_max >= kTensorRouterMinT ? static_cast<size_t>(E) * 3 * c.d * 2 : 0);
@@ -195,6 +204,10 @@ Layout make_layout(const beam_moe_config_t& c, int64_t T_max, int32_t fmt = BEAM
   L.x_sf = take(fp4 ? static_cast<size_t>(rows) * c.d / 4 : 0);
   L.h_fp4 = take(fp4 ? static_cast<size_t>(rows) * c.d_ff / 2 : 0);
   L.h_sf = take(fp4 ? static_cast<size_t>(rows) * c.d_ff / 4 : 0);
+  L.x_fp8 = take(fp8 ? static_cast<size_t>(T_max) * c.d : 0);
+  L.x_scale = take(fp8 ? static_cast<size_t>(T_max) * 4 : 0);
+  L.h_fp8 = take(fp8 ? static_cast<size_t>(rows) * c.d_ff : 0);
+  L.h_scale = take(fp8 ? static_cast<size_t>(rows) * 4 : 0);
   L.total = off;
   return L;
 }
@@ -519,6 +532,103 @@ beam_status_t run_experts_nvfp4(const beam_moe_config_t& c, const void* hidden, 
   return cuda_status(cudaGetLastError());
 }
 
+// permute + E4M3 token rows (+ gather) + FP8 gate/up (BF16 h) + E4M3 h rows
+// + FP8 down + combine
+beam_status_t run_experts_fp8(const beam_moe_config_t& c, const void* hidden, const int32_t* idx,
+                              const float* w, const beam_fp8_weight_t& gate,
+                              const beam_fp8_weight_t& up, const beam_fp8_weight_t& down,
+                              void* out, int64_t T, void* ws, const Layout& L, const DevInfo& dev,
+                              cudaStream_t s, bool permuted = false) {
+  const int64_t TK = T * c.topk;
+  const int64_t rows = std::max<int64_t>(TK, kMinRows);
+  const int nt_gu = gateup_tile(c, TK);
+  const int nt_dn = down_tile(c, TK);
+  const beam::PermuteArgs pa = permute_args(c, idx, w, T, ws, L);
+  if (!permuted) {
+    if (launch_permutation(pa, ws, L, dev, s) != BEAM_OK) return BEAM_ERR_CUDA;
+    record(3, s);
+  }
+  // the token rows are quantised once per token; decode-sized batches gather
+  // them inside the gate/up GEMM, larger ones into expert order first (byte
+  // rows, copied as d/2 16-bit words)
+  uint8_t* xq = at<uint8_t>(ws, L.x_fp8);
+  float* xs = at<float>(ws, L.x_scale);
+  beam::launch_quantize_e4m3_rows(static_cast<const uint16_t*>(hidden), nullptr, T, c.d, xq, xs,
+                                  s);
+  const bool row_gather = small_batch(c, TK);
+  uint8_t* xp = at<uint8_t>(ws, L.x_perm);
+  if (!row_gather)
+    beam::launch_gather(reinterpret_cast<const uint16_t*>(xq), pa.perm_src,
+                        pa.offsets + c.n_experts, TK, c.topk, c.d / 2,
+                        reinterpret_cast<uint16_t*>(xp), s);
+  record(4, s);
+  if (cudaGetLastError() != cudaSuccess) return BEAM_ERR_CUDA;
+
+  const int64_t EF = static_cast<int64_t>(c.n_experts) * c.d_ff;
+  const int64_t ED = static_cast<int64_t>(c.n_experts) * c.d;
+  uint16_t* h = at<uint16_t>(ws, L.h);
+  uint8_t* hq = at<uint8_t>(ws, L.h_fp8);
+  float* hs = at<float>(ws, L.h_scale);
+  float* y = at<float>(ws, L.y);
+  CUtensorMap tm_g, tm_u, tm_d, tm_x, tm_h;
+  if (!tmap_u8(&tm_g, gate.q, EF, c.d, 128, 128) || !tmap_u8(&tm_u, up.q, EF, c.d, 128, 128) ||
+      !tmap_u8(&tm_d, down.q, ED, c.d_ff, 128, 128) ||
+      !(row_gather ? tmap_u8(&tm_x, xq, T, c.d, 128, 1) : tmap_u8(&tm_x, xp, rows, c.d, 128, nt_gu)) ||
+      !tmap_u8(&tm_h, hq, rows, c.d_ff, 128, nt_dn))
+    return BEAM_ERR_CUDA;
+
+  GemmArgs ga{};
+  ga.counts = pa.counts;
+  ga.perm_src = pa.perm_src;
+  ga.topk = c.topk;
+  ga.offsets = pa.offsets;
+  ga.perm_w = pa.perm_w;
+  ga.E = c.n_experts;
+  ga.status = at<uint32_t>(ws, L.status);
+  ga.wait_limit_ns = g_wait_ns;
+  ga.withhold_first_load = 0;
+  ga.weight_evict_first = small_batch(c, TK) ? 1 : 0;
+  auto grid_for = [&](int m_blocks, int nt) {
+    const int64_t tiles = static_cast<int64_t>(m_blocks) * (c.n_experts + (TK + nt - 1) / nt);
+    return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(dev.sms, tiles)));
+  };
+
+  ga.h_out = h;
+  ga.out_ld = c.d_ff;
+  ga.rows_per_expert = c.d_ff;
+  ga.m_blocks = c.d_ff / 128;
+  ga.k_blocks = c.d / 128;
+  ga.b_k_blocks = ga.k_blocks;
+  ga.a0_scale = gate.scale;
+  ga.a1_scale = up.scale;
+  ga.b_scale = xs;  // per token
+  if (beam::launch_grouped_gemm(beam::kModeGateUp, nt_gu, tm_g, tm_u, tm_x, ga,
+                                grid_for(ga.m_blocks, nt_gu), s, true) != cudaSuccess)
+    return BEAM_ERR_CUDA;
+  record(5, s);
+
+  beam::launch_quantize_e4m3_rows(h, pa.offsets + c.n_experts, TK, c.d_ff, hq, hs, s);
+  ga.h_out = nullptr;
+  ga.f32_out = y;
+  ga.out_rows = nullptr;
+  ga.out_ld = c.d;
+  ga.rows_per_expert = c.d;
+  const bool pair = c.d % 256 == 0 && nt_dn == 256;
+  ga.m_blocks = pair ? c.d / 256 : c.d / 128;
+  ga.k_blocks = c.d_ff / 128;
+  ga.b_k_blocks = ga.k_blocks;
+  ga.a0_scale = down.scale;
+  ga.a1_scale = nullptr;
+  ga.b_scale = hs;  // per permuted row
+  if (beam::launch_grouped_gemm(pair ? beam::kModeDownPair : beam::kModeDown, nt_dn, tm_d, tm_d,
+                                tm_h, ga, grid_for(ga.m_blocks, nt_dn), s, true) != cudaSuccess)
+    return BEAM_ERR_CUDA;
+  record(6, s);
+  beam::launch_combine(y, pa.pair_row, T, c.topk, c.d, static_cast<uint16_t*>(out), s);
+  record(7, s);
+  return cuda_status(cudaGetLastError());
+}
+
 // permute + F16 token rows + W4A16 gate/up (F16 h) + W4A16 down + combine
 beam_status_t run_experts_w4a16(const beam_moe_config_t& c, const void* hidden, const int32_t* idx,
                                 const float* w, const beam_fp4_weight_t& gate,
@@ -597,6 +707,10 @@ bool valid_fp4_weight(const beam_fp4_weight_t* w) {
   return w && aligned16(w->q) && aligned16(w->sf) && aligned16(w->global_scale);
 }
 
+bool valid_fp8_weight(const beam_fp8_weight_t* w) {
+  return w && aligned16(w->q) && aligned16(w->scale);
+}
+
 // ---------------------------------------------------------------- no-allocation scratch
 // Scratch for beam_moe_forward_noalloc, which serves callers that cannot
 // allocate device memory.  A fixed-size device array takes the place of the
@@ -626,19 +740,13 @@ void* noalloc_scratch_address() {
 extern "C" {
 
 size_t beam_moe_workspace_size(const beam_moe_config_t* cfg, int64_t T_max, int32_t weight_fmt) {
-  if (!valid_cfg(cfg) || T_max < 0) return 0;
-  if (weight_fmt != BEAM_WEIGHTS_BF16 && weight_fmt != BEAM_WEIGHTS_NVFP4 &&
-      weight_fmt != BEAM_WEIGHTS_NVFP4_A16)
-    return 0;
+  if (!valid_cfg(cfg) || T_max < 0 || !known_fmt(weight_fmt)) return 0;
   return make_layout(*cfg, T_max, weight_fmt).total;
 }
 
 beam_status_t beam_moe_workspace_layout(const beam_moe_config_t* cfg, int64_t T_max,
                                         int32_t weight_fmt, beam_moe_ws_layout_t* out) {
-  if (!out || !valid_cfg(cfg) || T_max < 0 ||
-      (weight_fmt != BEAM_WEIGHTS_BF16 && weight_fmt != BEAM_WEIGHTS_NVFP4 &&
-       weight_fmt != BEAM_WEIGHTS_NVFP4_A16))
-    return BEAM_ERR_INVALID_ARG;
+  if (!out || !valid_cfg(cfg) || T_max < 0 || !known_fmt(weight_fmt)) return BEAM_ERR_INVALID_ARG;
   const Layout L = make_layout(*cfg, T_max, weight_fmt);
   out->status = L.status;
   out->logits = L.logits;
@@ -656,6 +764,10 @@ beam_status_t beam_moe_workspace_layout(const beam_moe_config_t* cfg, int64_t T_
   out->h_fp4 = L.h_fp4;
   out->h_sf = L.h_sf;
   out->y = L.y;
+  out->x_fp8 = L.x_fp8;
+  out->x_scale = L.x_scale;
+  out->h_fp8 = L.h_fp8;
+  out->h_scale = L.h_scale;
   out->total = L.total;
   return BEAM_OK;
 }
@@ -847,6 +959,44 @@ beam_status_t beam_moe_forward_nvfp4(const beam_moe_config_t* cfg, const void* h
   if (st != BEAM_OK) return st;
   return run_experts_nvfp4(*cfg, hidden, idx, w, *gate, *up, *down, out, T, workspace, L, dev, s,
                            permuted);
+}
+
+beam_status_t beam_moe_forward_fp8(const beam_moe_config_t* cfg, const void* hidden,
+                                   const float* router_w, const float* corr_bias,
+                                   const beam_fp8_weight_t* gate, const beam_fp8_weight_t* up,
+                                   const beam_fp8_weight_t* down, void* out, int64_t T,
+                                   void* workspace, size_t ws_bytes, void* stream) {
+  Layout L;
+  DevInfo dev;
+  bool empty = false;
+  beam_status_t st = common_checks(cfg, T, workspace, ws_bytes, &L, &dev, &empty,
+                                   BEAM_WEIGHTS_FP8);
+  if (st != BEAM_OK || empty) return st;
+  if (!aligned16(hidden) || !aligned16(router_w) || !aligned16(corr_bias) ||
+      !valid_fp8_weight(gate) || !valid_fp8_weight(up) || !valid_fp8_weight(down) ||
+      !aligned16(out))
+    return BEAM_ERR_INVALID_ARG;
+  if (!encoder()) return BEAM_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  record(0, s);
+  int32_t* idx = at<int32_t>(workspace, L.idx);
+  float* w = at<float>(workspace, L.w);
+  bool permuted = false;
+  st = run_route(*cfg, hidden, router_w, corr_bias, T, idx, w, at<float>(workspace, L.logits),
+                 workspace, L, dev, s, &permuted);
+  if (st != BEAM_OK) return st;
+  return run_experts_fp8(*cfg, hidden, idx, w, *gate, *up, *down, out, T, workspace, L, dev, s,
+                         permuted);
+}
+
+beam_status_t beam_moe_fp8_quantize_rows(const void* x, int64_t n, int32_t cols, uint8_t* q,
+                                         float* scale, void* stream) {
+  if (n < 0 || n > INT32_MAX || cols <= 0 || cols % 8) return BEAM_ERR_INVALID_ARG;
+  if (n == 0) return BEAM_OK;
+  if (!aligned16(x) || !aligned16(q) || !aligned16(scale)) return BEAM_ERR_INVALID_ARG;
+  beam::launch_quantize_e4m3_rows(static_cast<const uint16_t*>(x), nullptr, n, cols, q, scale,
+                                  static_cast<cudaStream_t>(stream));
+  return cuda_status(cudaGetLastError());
 }
 
 beam_status_t beam_moe_forward_nvfp4_a16(const beam_moe_config_t* cfg, const void* hidden,
@@ -1048,15 +1198,15 @@ beam_status_t beam_moe_set_debug(uint32_t wait_limit_us, int32_t withhold_first_
 
 int32_t beam_moe_kernels_per_forward(const beam_moe_config_t* cfg, int64_t T, int32_t weight_fmt,
                                      int32_t routed) {
-  if (!valid_cfg(cfg) || T <= 0) return 0;
-  if (weight_fmt != BEAM_WEIGHTS_BF16 && weight_fmt != BEAM_WEIGHTS_NVFP4 &&
-      weight_fmt != BEAM_WEIGHTS_NVFP4_A16)
-    return 0;
+  if (!valid_cfg(cfg) || T <= 0 || !known_fmt(weight_fmt)) return 0;
   if (routed && weight_fmt != BEAM_WEIGHTS_BF16) return 0;
   // experts: permute, gather (BF16, larger batches) or row quantisation
-  // (NVFP4), gate/up, down, combine
+  // (NVFP4) or F16 gather (W4A16), gate/up, down, combine; FP8 quantises the
+  // token rows and h (and gathers the token codes for larger batches)
   const bool small = small_batch(*cfg, T * cfg->topk);
-  const int experts = weight_fmt != BEAM_WEIGHTS_BF16 ? 5 : 4 + (small ? 0 : 1);
+  const int experts = weight_fmt == BEAM_WEIGHTS_FP8    ? 6 + (small ? 0 : 1)
+                      : weight_fmt != BEAM_WEIGHTS_BF16 ? 5
+                                                        : 4 + (small ? 0 : 1);
   if (routed) return experts;
   // routing: router (+ plane split), select; decode-sized batches run router,
   // select and permute as one launch

@@ -151,6 +151,10 @@ cudaError_t launch_w4a16_gemm(bool gateup, int nt, const CUtensorMap& a0, const 
 
 // [rows, S] row-major E4M3 scales -> 128-row x 4-scale blocks (see nvfp4.cu)
 void launch_pack_scales(const uint8_t* src, int64_t rows, int64_t S, uint8_t* dst, cudaStream_t s);
+// BF16 rows [rows, cols] -> E4M3 codes [rows, cols] and one FP32 scale per
+// row (amax / 448); rows at or past *n_valid, when given, are skipped
+void launch_quantize_e4m3_rows(const uint16_t* x, const int32_t* n_valid, int64_t rows,
+                               int32_t cols, uint8_t* q, float* scale, cudaStream_t s);
 // permuted token rows -> NVFP4 codes [rows, d/2] and scales [rows, d/4]
 // (one 16-byte slot, 4 scales + padding, per 64 elements)
 void launch_quantize_rows(const uint16_t* x, const int32_t* perm_src, const int32_t* n_valid,

@@ -15,8 +15,10 @@
 //
 // Tiling ("swap AB"): the MMA's M side is 128 weight rows, its N side a block
 // of the expert's permuted token rows (up to NT; the MMA's N is the block's
-// row count rounded up to 16), K steps of 64 (one 128-byte swizzle row of
-// BF16).  gate/up issue two MMAs per K step into two TMEM accumulators (gate,
+// row count rounded up to 16), K steps of one 128-byte swizzle row: 64 BF16
+// values, or 128 E4M3 values for the FP8 experts (kind::f8f6f4 MMAs; the
+// epilogue then multiplies each accumulator by its weight row's and its
+// token row's FP32 scales).  gate/up issue two MMAs per K step into two TMEM accumulators (gate,
 // up) that share the token operand, so one thread holds g and u of the same
 // (f, token) and the SwiGLU epilogue is local.  An expert's rows are split
 // into ceil(rows / NT) blocks of nearly equal size.  With 16-row token
@@ -62,8 +64,8 @@ using gemm::token_blocks;
 
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int BM = 128;
-constexpr int BK = 64;
-constexpr int UMMA_K = 16;
+constexpr int kRowBytes = 128;     // one K block of one operand row: a 128-byte swizzle row
+constexpr int kMmaKBytes = 32;     // K bytes per MMA instruction (16 BF16 or 32 E4M3)
 // warps: weight producer, MMA issuer, token producer, then the epilogue warps
 // (four per TMEM lane quarter for the single-buffered 256-token gate/up tile,
 // whose epilogue the MMA waits for)
@@ -88,9 +90,9 @@ struct Cfg {
   // gate/up: gate and up tiles of the same rows; down pair: two adjacent
   // 128-row blocks of W_d; both share the token tile
   static constexpr int NUM_A = MODE == kModeDown ? 1 : 2;
-  static constexpr uint32_t A_BYTES = BM * BK * 2;
+  static constexpr uint32_t A_BYTES = BM * kRowBytes;
   static constexpr uint32_t A_STAGE = NUM_A * A_BYTES;
-  static constexpr uint32_t B_STAGE = NT * BK * 2;
+  static constexpr uint32_t B_STAGE = NT * kRowBytes;
   static constexpr int SA_RAW = static_cast<int>(kTileBudget / (A_STAGE + B_STAGE));
   static constexpr int SA = SA_RAW > 16 ? 16 : SA_RAW;
   static constexpr int SB = SA;
@@ -116,7 +118,7 @@ __device__ __forceinline__ uint16_t f32_to_bf16(float v) {
   return *reinterpret_cast<uint16_t*>(&b);
 }
 
-template <int NT, int MODE>
+template <int NT, int MODE, bool F8>
 __global__ void __launch_bounds__(threads_for(NT, MODE), 1)
     expert_gemm_kernel(const __grid_constant__ CUtensorMap tm_a0,
                        const __grid_constant__ CUtensorMap tm_a1,
@@ -127,6 +129,7 @@ __global__ void __launch_bounds__(threads_for(NT, MODE), 1)
   // decode-sized token blocks gather their rows from the hidden states with
   // per-row TMA loads; larger blocks load whole tiles of a gathered copy
   constexpr bool ROW_GATHER = GATEUP && NT <= 32;
+  constexpr int KE = F8 ? kRowBytes : kRowBytes / 2;  // K elements per K block
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = ptx::smem_addr(smem_raw);
   const uint32_t pad = (1024u - (raw_addr & 1023u)) & 1023u;
@@ -234,11 +237,11 @@ __global__ void __launch_bounds__(threads_for(NT, MODE), 1)
           } else {
             const uint32_t st = a_ring + stage * C::A_STAGE;
             ptx::mbar_arrive_expect_tx(fullA(stage), C::A_STAGE);
-            ptx::tma_load_2d(st, &tm_a0, fullA(stage), kb * BK, a_row, pol_w);
+            ptx::tma_load_2d(st, &tm_a0, fullA(stage), kb * KE, a_row, pol_w);
             if (GATEUP)
-              ptx::tma_load_2d(st + C::A_BYTES, &tm_a1, fullA(stage), kb * BK, a_row, pol_w);
+              ptx::tma_load_2d(st + C::A_BYTES, &tm_a1, fullA(stage), kb * KE, a_row, pol_w);
             if (PAIR)
-              ptx::tma_load_2d(st + C::A_BYTES, &tm_a0, fullA(stage), kb * BK, a_row + BM, pol_w);
+              ptx::tma_load_2d(st + C::A_BYTES, &tm_a0, fullA(stage), kb * KE, a_row + BM, pol_w);
             last_parity[stage] = static_cast<int>(phase);
           }
           if (++stage == C::SA) {
@@ -256,7 +259,7 @@ __global__ void __launch_bounds__(threads_for(NT, MODE), 1)
   } else if (warp == 2) {
     // ------------------------------------------------------- token producer
     // With ROW_GATHER every lane issues one 128-byte row load per token it
-    // owns (box 64 x 1; the row lands at its swizzled place in the tile);
+    // owns (box of one row; the row lands at its swizzled place in the tile);
     // otherwise lane 0 loads the whole token tile (x gathered into expert
     // order, or h).
     constexpr int RPL = (NT + 31) / 32;  // token rows per lane
@@ -279,7 +282,7 @@ __global__ void __launch_bounds__(threads_for(NT, MODE), 1)
         }
       }
       const uint32_t tx_bytes =
-          ROW_GATHER ? static_cast<uint32_t>(ti.nvalid) * BK * 2 : C::B_STAGE;
+          ROW_GATHER ? static_cast<uint32_t>(ti.nvalid) * kRowBytes : C::B_STAGE;
       for (int kb = 0; kb < p.k_blocks; ++kb) {
         int okw = 1;
         if (lane == 0) okw = W.wait(emptyB(stage), phase ^ 1u) ? 1 : 0;
@@ -291,14 +294,14 @@ __global__ void __launch_bounds__(threads_for(NT, MODE), 1)
         const uint32_t st = b_ring + stage * C::B_STAGE;
         if (lane == 0) {
           ptx::mbar_arrive_expect_tx(fullB(stage), tx_bytes);
-          if (!ROW_GATHER) ptx::tma_load_2d(st, &tm_b, fullB(stage), kb * BK, ti.row0, pol_b);
+          if (!ROW_GATHER) ptx::tma_load_2d(st, &tm_b, fullB(stage), kb * KE, ti.row0, pol_b);
         }
         if constexpr (ROW_GATHER) {
           __syncwarp();
 #pragma unroll
           for (int j = 0; j < RPL; ++j)
             if (tok[j] >= 0)
-              ptx::tma_load_2d(st + (lane + 32 * j) * (BK * 2), &tm_b, fullB(stage), kb * BK,
+              ptx::tma_load_2d(st + (lane + 32 * j) * kRowBytes, &tm_b, fullB(stage), kb * KE,
                                tok[j], pol_b);
         }
         last_parity[stage] = static_cast<int>(phase);
@@ -317,7 +320,7 @@ __global__ void __launch_bounds__(threads_for(NT, MODE), 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc_m = ptx::idesc_bf16_f32(BM, 0);
+      constexpr uint32_t idesc_m = F8 ? ptx::idesc_e4m3_f32(BM, 0) : ptx::idesc_bf16_f32(BM, 0);
       int sa = 0, sb = 0;
       uint32_t pa = 0, pb = 0;
       int acc = 0;
@@ -339,12 +342,19 @@ __global__ void __launch_bounds__(threads_for(NT, MODE), 1)
           const uint32_t st = a_ring + sa * C::A_STAGE;
           const uint32_t bt = b_ring + sb * C::B_STAGE;
 #pragma unroll
-          for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+          for (int kk = 0; kk < kRowBytes / kMmaKBytes; ++kk) {
             const uint32_t accum = (kb | kk) ? 1u : 0u;
-            const uint64_t bd = ptx::sdesc_sw128(bt + kk * 32);
-            ptx::mma_bf16(d0, ptx::sdesc_sw128(st + kk * 32), bd, idesc, accum);
-            if (C::NUM_A == 2)
-              ptx::mma_bf16(d0 + NT, ptx::sdesc_sw128(st + C::A_BYTES + kk * 32), bd, idesc, accum);
+            const uint32_t ko = kk * kMmaKBytes;
+            const uint64_t bd = ptx::sdesc_sw128(bt + ko);
+            if constexpr (F8) {
+              ptx::mma_f8(d0, ptx::sdesc_sw128(st + ko), bd, idesc, accum);
+              if (C::NUM_A == 2)
+                ptx::mma_f8(d0 + NT, ptx::sdesc_sw128(st + C::A_BYTES + ko), bd, idesc, accum);
+            } else {
+              ptx::mma_bf16(d0, ptx::sdesc_sw128(st + ko), bd, idesc, accum);
+              if (C::NUM_A == 2)
+                ptx::mma_bf16(d0 + NT, ptx::sdesc_sw128(st + C::A_BYTES + ko), bd, idesc, accum);
+            }
           }
           // free both stages once these MMAs have read them
           ptx::mma_commit(emptyA(sa));
@@ -387,6 +397,15 @@ __global__ void __launch_bounds__(threads_for(NT, MODE), 1)
       ptx::tc_fence_after();
       const uint32_t tq = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * C::ACC_COLS;
       const int col = ti.mblock * BM + m;
+      // E4M3 operands: the scales of this thread's weight row(s)
+      float sw0 = 1.f, sw1 = 1.f;
+      if constexpr (F8) {
+        const int64_t wrow = static_cast<int64_t>(ti.expert) * p.rows_per_expert +
+                             (PAIR ? ti.mblock * 2 * BM + m : col);
+        sw0 = p.a0_scale[wrow];
+        if constexpr (GATEUP) sw1 = p.a1_scale[wrow];
+        if constexpr (PAIR) sw1 = p.a0_scale[wrow + BM];
+      }
 #pragma unroll 1
       for (int c0 = col_begin; c0 < min(ti.nvalid, col_begin + COLS_PER_WARP); c0 += 16) {
         uint32_t ra[16];
@@ -398,8 +417,13 @@ __global__ void __launch_bounds__(threads_for(NT, MODE), 1)
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             if (c0 + j < ti.nvalid) {
-              const float g = __uint_as_float(ra[j]);
-              const float u = __uint_as_float(rb[j]);
+              float g = __uint_as_float(ra[j]);
+              float u = __uint_as_float(rb[j]);
+              if constexpr (F8) {
+                const float sx = p.b_scale[p.perm_src[ti.row0 + c0 + j] / p.topk];
+                g *= sw0 * sx;
+                u *= sw1 * sx;
+              }
               // fast exp and divide: relative error near 1e-6, far below the
               // BF16 rounding of h that follows
               const float h = __fdividef(g, 1.0f + __expf(-g)) * u;
@@ -417,10 +441,10 @@ __global__ void __launch_bounds__(threads_for(NT, MODE), 1)
             if (c0 + j < ti.nvalid) {
               const int row = ti.row0 + c0 + j;
               const int orow = p.out_rows ? p.out_rows[row] : row;
-              const float w = p.perm_w[row];
+              const float w = F8 ? p.b_scale[row] * p.perm_w[row] : p.perm_w[row];
               float* dst = p.f32_out + static_cast<int64_t>(orow) * p.out_ld + pcol;
-              dst[0] = __uint_as_float(ra[j]) * w;
-              dst[BM] = __uint_as_float(rb[j]) * w;
+              dst[0] = F8 ? __uint_as_float(ra[j]) * sw0 * w : __uint_as_float(ra[j]) * w;
+              dst[BM] = F8 ? __uint_as_float(rb[j]) * sw1 * w : __uint_as_float(rb[j]) * w;
             }
           }
         } else {
@@ -431,7 +455,8 @@ __global__ void __launch_bounds__(threads_for(NT, MODE), 1)
               const int row = ti.row0 + c0 + j;
               const int orow = p.out_rows ? p.out_rows[row] : row;
               p.f32_out[static_cast<int64_t>(orow) * p.out_ld + col] =
-                  __uint_as_float(ra[j]) * p.perm_w[row];
+                  F8 ? __uint_as_float(ra[j]) * sw0 * (p.b_scale[row] * p.perm_w[row])
+                     : __uint_as_float(ra[j]) * p.perm_w[row];
             }
           }
         }
@@ -453,11 +478,11 @@ __global__ void __launch_bounds__(threads_for(NT, MODE), 1)
   }
 }
 
-template <int NT, int MODE>
+template <int NT, int MODE, bool F8>
 cudaError_t launch_impl(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b,
                         const GemmArgs& p, int grid, cudaStream_t s) {
   using C = Cfg<NT, MODE>;
-  auto kern = expert_gemm_kernel<NT, MODE>;
+  auto kern = expert_gemm_kernel<NT, MODE, F8>;
   // set once per instantiation (thread-safe static initialisation), so a
   // call can also be captured into a CUDA graph
   static const cudaError_t err =
@@ -471,20 +496,37 @@ cudaError_t launch_impl(const CUtensorMap& a0, const CUtensorMap& a1, const CUte
 
 cudaError_t launch_grouped_gemm(int mode, int nt, const CUtensorMap& a0, const CUtensorMap& a1,
                                 const CUtensorMap& b, const GemmArgs& a, int grid,
-                                cudaStream_t s) {
+                                cudaStream_t s, bool f8) {
+  if (f8) {
+    switch (mode) {
+      case kModeGateUp:
+        if (nt == 16) return launch_impl<16, kModeGateUp, true>(a0, a1, b, a, grid, s);
+        if (nt == 256) return launch_impl<256, kModeGateUp, true>(a0, a1, b, a, grid, s);
+        break;
+      case kModeDown:
+        if (nt == 16) return launch_impl<16, kModeDown, true>(a0, a0, b, a, grid, s);
+        if (nt == 256) return launch_impl<256, kModeDown, true>(a0, a0, b, a, grid, s);
+        break;
+      case kModeDownPair:
+        if (nt == 16) return launch_impl<16, kModeDownPair, true>(a0, a0, b, a, grid, s);
+        if (nt == 256) return launch_impl<256, kModeDownPair, true>(a0, a0, b, a, grid, s);
+        break;
+    }
+    return cudaErrorInvalidValue;
+  }
   switch (mode) {
     case kModeGateUp:
-      if (nt == 16) return launch_impl<16, kModeGateUp>(a0, a1, b, a, grid, s);
-      if (nt == 128) return launch_impl<128, kModeGateUp>(a0, a1, b, a, grid, s);
-      if (nt == 256) return launch_impl<256, kModeGateUp>(a0, a1, b, a, grid, s);
+      if (nt == 16) return launch_impl<16, kModeGateUp, false>(a0, a1, b, a, grid, s);
+      if (nt == 128) return launch_impl<128, kModeGateUp, false>(a0, a1, b, a, grid, s);
+      if (nt == 256) return launch_impl<256, kModeGateUp, false>(a0, a1, b, a, grid, s);
       break;
     case kModeDown:
-      if (nt == 16) return launch_impl<16, kModeDown>(a0, a0, b, a, grid, s);
-      if (nt == 256) return launch_impl<256, kModeDown>(a0, a0, b, a, grid, s);
+      if (nt == 16) return launch_impl<16, kModeDown, false>(a0, a0, b, a, grid, s);
+      if (nt == 256) return launch_impl<256, kModeDown, false>(a0, a0, b, a, grid, s);
       break;
     case kModeDownPair:
-      if (nt == 16) return launch_impl<16, kModeDownPair>(a0, a0, b, a, grid, s);
-      if (nt == 256) return launch_impl<256, kModeDownPair>(a0, a0, b, a, grid, s);
+      if (nt == 16) return launch_impl<16, kModeDownPair, false>(a0, a0, b, a, grid, s);
+      if (nt == 256) return launch_impl<256, kModeDownPair, false>(a0, a0, b, a, grid, s);
       break;
   }
   return cudaErrorInvalidValue;

@@ -25,18 +25,27 @@ struct GemmArgs {
   int32_t E;               // experts in the tile list
   int32_t rows_per_expert; // weight rows of one expert (A operand)
   int32_t m_blocks;        // rows_per_expert / 128
-  int32_t k_blocks;        // A's K / 64
-  int32_t b_k_blocks;      // token operand's K / 64 (== k_blocks)
+  int32_t k_blocks;        // A's K / 64 (BF16) or / 128 (E4M3): 128-byte K blocks
+  int32_t b_k_blocks;      // the token operand's, == k_blocks
   int32_t weight_evict_first;
   uint32_t* status;
   uint64_t wait_limit_ns;
   int32_t withhold_first_load;
+  // E4M3 operands only: FP32 scale of every weight row ([E * rows_per_expert];
+  // a0's rows, and a1's for gate/up) and of every token operand row: per
+  // token for gate/up ([T], looked up through perm_src), per permuted row
+  // for down ([rows]).  The accumulators are multiplied by both.
+  const float* a0_scale;
+  const float* a1_scale;
+  const float* b_scale;
 };
 
 // Persistent grouped GEMM; `nt` is the token-block width (gate/up 16 | 128,
-// down 16 | 256).  Tensor maps are encoded by the caller.
+// down 16 | 256).  `f8`: both operands are E4M3 (K blocks of 128 elements)
+// instead of BF16 (K blocks of 64); the only other difference is the
+// scaling in the epilogue.  Tensor maps are encoded by the caller.
 cudaError_t launch_grouped_gemm(int mode, int nt, const CUtensorMap& a0, const CUtensorMap& a1,
                                 const CUtensorMap& b, const GemmArgs& a, int grid,
-                                cudaStream_t s);
+                                cudaStream_t s, bool f8 = false);
 
 }  // namespace beam

@@ -121,6 +121,19 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint6
       : "memory");
 }
 
+// D[tmem] (+)= A[smem] * B[smem]^T, kind::f8f6f4 with 8-bit A and B (the
+// formats come from the instruction descriptor), FP32 accumulate; K = 32 per
+// instruction (32 bytes of each operand row).
+__device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                       uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // D[tmem] (+)= (A * SFA)[smem] * (B * SFB)[smem]^T, kind::mxf4nvf4: packed E2M1
 // A and B (two per byte, K-major), one UE4M3 scale per 16 elements along K
 // (scale_vec::4X), FP32 D.  K per instruction = 64.  For M = 128 (or N <= 128
@@ -213,6 +226,12 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
 //   bits 17-22 N >> 3              bits 24-28 M >> 4
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+
+// Instruction descriptor, kind::f8f6f4: E4M3 A and B (format code 0 in bits
+// 7-9 and 10-12, both K-major), FP32 D (bits 4-5 = 1).
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(uint32_t M, uint32_t N) {
+  return (1u << 4) | ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 
 // Instruction descriptor, kind::mxf4nvf4: E2M1 A and B (format code 1, both

@@ -88,6 +88,7 @@ typedef struct {
 #define BEAM_WEIGHTS_BF16 0
 #define BEAM_WEIGHTS_NVFP4 1
 #define BEAM_WEIGHTS_NVFP4_A16 2 /* NVFP4 weights, 16-bit activations */
+#define BEAM_WEIGHTS_FP8 3       /* dynamic FP8: E4M3 weights and activations */
 
 /* Bytes of device workspace a call with up to T_max tokens needs (256-byte
  * aligned).  Returns 0 for an invalid configuration. */
@@ -117,6 +118,12 @@ typedef struct {
   size_t h_fp4;         /*   SwiGLU activations [T*topk, F/2]                  */
   size_t h_sf;          /*   and their scales [T*topk, F/4], same slots        */
   size_t y;             /* FP32 [T*topk, d] weighted expert outputs           */
+  size_t x_fp8;         /* FP8 path: token rows, E4M3 codes [T, d]            */
+  size_t x_scale;       /*   their FP32 scales [T]                            */
+  size_t h_fp8;         /*   SwiGLU activations, E4M3 codes [T*topk, F] (x_perm
+                             holds the gathered token codes [T*topk, d] when
+                             T*topk > 4*E)                                   */
+  size_t h_scale;       /*   their FP32 scales [T*topk]                       */
   size_t total;         /* == beam_moe_workspace_size                         */
 } beam_moe_ws_layout_t;
 
@@ -265,6 +272,40 @@ beam_status_t beam_moe_forward_nvfp4_a16(const beam_moe_config_t *cfg, const voi
                                          const beam_fp4_weight_t *down, void *out, int64_t T,
                                          void *workspace, size_t ws_bytes, void *stream);
 
+/* Dynamic FP8 expert weights (one projection of all experts): E4M3 codes
+ * q [E, N, K] (K contiguous; N = d_ff for gate/up, d for down) and one FP32
+ * scale per output row, scale [E, N]: the weight is code x scale (the
+ * per-channel FP8 weights of a compressed-tensors dynamic FP8 checkpoint;
+ * SGLang post, sections "Highlights" and "BF16, NVFP4 and FP8 Model
+ * Support"). */
+typedef struct {
+  const uint8_t *q;     /* E4M3 [E, N, K]                                      */
+  const float *scale;   /* FP32 [E, N]                                         */
+} beam_fp8_weight_t;
+
+/* The whole layer with dynamic FP8 experts.  Router and selection as in
+ * beam_moe_forward.  Both expert GEMM inputs are quantised per row at run
+ * time: x per token along d, and h (the FP32 SwiGLU product rounded to BF16,
+ * as in beam_moe_forward) per (token, expert) row along d_ff.  The rule:
+ * scale = amax / 448 in FP32 (1 for an all-zero row), code = E4M3(value /
+ * scale) with an FP32 division, round to nearest even, saturating at 448.
+ * The GEMMs run as E4M3 x E4M3 tensor-core MMAs with FP32 accumulation; the
+ * weight row's and the token row's scales multiply each accumulator; the
+ * rest (FP32 routing weights, FP32 combine in slot order, one BF16 rounding)
+ * is beam_moe_forward's.  Workspace: beam_moe_workspace_size(cfg, T,
+ * BEAM_WEIGHTS_FP8). */
+beam_status_t beam_moe_forward_fp8(const beam_moe_config_t *cfg, const void *hidden,
+                                   const float *router_w, const float *corr_bias,
+                                   const beam_fp8_weight_t *gate, const beam_fp8_weight_t *up,
+                                   const beam_fp8_weight_t *down, void *out, int64_t T,
+                                   void *workspace, size_t ws_bytes, void *stream);
+
+/* The FP8 path's activation rule on its own: BF16 rows x [n, cols] ->
+ * E4M3 codes q [n, cols] and FP32 scales [n] (cols % 8 == 0; all pointers
+ * 16-byte aligned device memory).  n == 0 launches nothing. */
+beam_status_t beam_moe_fp8_quantize_rows(const void *x, int64_t n, int32_t cols, uint8_t *q,
+                                         float *scale, void *stream);
+
 /* ---------------------------------------------------- expert parallelism
  * Expert parallelism over n_ranks ranks ("SGLang 原生支持 Reflection 的 Beam
  * 并驱动其生产 API", section "Fusion Optimizations", the MegaMoE item and the
@@ -367,7 +408,8 @@ beam_status_t beam_moe_set_debug(uint32_t wait_limit_us, int32_t withhold_first_
 /* Number of kernels one call of T tokens launches (for accounting):
  * beam_moe_forward (and beam_moe_forward_noalloc) for weight_fmt
  * BEAM_WEIGHTS_BF16, beam_moe_forward_nvfp4 for BEAM_WEIGHTS_NVFP4,
- * beam_moe_forward_nvfp4_a16 for BEAM_WEIGHTS_NVFP4_A16, and with
+ * beam_moe_forward_nvfp4_a16 for BEAM_WEIGHTS_NVFP4_A16,
+ * beam_moe_forward_fp8 for BEAM_WEIGHTS_FP8, and with
  * routed != 0 beam_moe_forward_routed (BF16 only).  Returns 0 for an invalid
  * configuration, T <= 0 or an unknown combination.  Host-only. */
 int32_t beam_moe_kernels_per_forward(const beam_moe_config_t *cfg, int64_t T, int32_t weight_fmt,

@@ -57,6 +57,13 @@ def test_host_only_queries(lib):
     assert api.kernels_per_forward(beam, 128, weight_fmt=api.NVFP4) == 5
     assert api.kernels_per_forward(beam, 4096, weight_fmt=api.NVFP4) == 8
     assert api.kernels_per_forward(beam, 32, weight_fmt=api.NVFP4, routed=True) == 0
+    # FP8: routing+permute, x quantisation, gate/up, h quantisation, down, combine
+    assert api.kernels_per_forward(beam, 32, weight_fmt=api.FP8) == 6
+    # ... plus plane split, tensor router, select and the gather of the token codes
+    assert api.kernels_per_forward(beam, 8192, weight_fmt=api.FP8) == 10
+    f8 = api.layout(beam, 32, weight_fmt=api.FP8)
+    assert f8["x_fp8"] > 0 and f8["h_scale"] > f8["h_fp8"] > f8["x_scale"] > f8["x_fp8"]
+    assert f8["total"] == api.workspace_size(beam, 32, weight_fmt=api.FP8)
     with pytest.raises(api.BeamError):
         api.workspace_size(beam.replace(n_groups=7), 32)
     lib.beam_status_string.restype = ctypes.c_char_p
@@ -78,3 +85,4 @@ def test_ep_workspace_query(lib):
     assert size(ctypes.byref(c), 3, 256, 0) == 0      # 3 does not divide 256 experts
     assert size(ctypes.byref(c), 512, 256, 0) == 0    # more ranks than experts
     assert size(ctypes.byref(c), 8, 256, 2) == 0      # no W4A16 expert-parallel path
+    assert size(ctypes.byref(c), 8, 256, 3) == 0      # nor an FP8 one

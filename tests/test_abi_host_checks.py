@@ -35,7 +35,7 @@ def test_invalid_shapes_are_rejected_before_any_launch(lib, shape):
     cfg = _cfg(**shape)
     for name in ("beam_moe_forward", "beam_moe_forward_routed"):
         assert _forward_like(getattr(lib, name), cfg, 4) == INVALID, (name, shape)
-    for name in ("beam_moe_forward_nvfp4", "beam_moe_forward_nvfp4_a16"):
+    for name in ("beam_moe_forward_nvfp4", "beam_moe_forward_nvfp4_a16", "beam_moe_forward_fp8"):
         fn = getattr(lib, name)
         fn.restype = ctypes.c_int
         assert fn(cfg, None, None, None, None, None, None, None, ctypes.c_int64(4), None,
@@ -80,3 +80,21 @@ def test_boundary_and_expert_parallel_checks(lib):
                                    ctypes.c_int64(0), None, ctypes.c_size_t(0), None) == OK
     lib.beam_moe_kernels_per_forward.restype = ctypes.c_int32
     assert lib.beam_moe_kernels_per_forward(_cfg(n_groups=7), ctypes.c_int64(32), 0, 0) == 0
+
+
+def test_fp8_entry_points(lib):
+    fwd = lib.beam_moe_forward_fp8
+    fwd.restype = ctypes.c_int
+    assert fwd(_cfg(), None, None, None, None, None, None, None, ctypes.c_int64(0), None,
+               ctypes.c_size_t(0), None) == OK                        # nothing to do
+    assert fwd(_cfg(), None, None, None, None, None, None, None, ctypes.c_int64(-3), None,
+               ctypes.c_size_t(0), None) == INVALID
+    q = lib.beam_moe_fp8_quantize_rows
+    q.restype = ctypes.c_int
+    q.argtypes = [P, ctypes.c_int64, ctypes.c_int32, P, P, P]
+    assert q(None, 0, 128, None, None, None) == OK                     # no rows, no launch
+    assert q(None, -1, 128, None, None, None) == INVALID
+    assert q(None, 4, 100, None, None, None) == INVALID                 # cols % 8 != 0
+    assert q(None, 4, 128, None, None, None) == INVALID                 # null pointers
+    lib.beam_moe_workspace_size.restype = ctypes.c_size_t
+    assert lib.beam_moe_workspace_size(_cfg(), ctypes.c_int64(32), 3) > 0
