@@ -410,17 +410,35 @@ __global__ void __launch_bounds__(threads_for(NT, MODE), 1)
       for (int c0 = col_begin; c0 < min(ti.nvalid, col_begin + COLS_PER_WARP); c0 += 16) {
         uint32_t ra[16];
         ptx::tmem_ld16(tq + c0, ra);
+        // per-token factors of the chunk's 16 columns, one column per lane
+        // (lanes 16-31 repeat 0-15), loaded while the TMEM load is in flight
+        // and handed out by shuffles: gate/up's E4M3 token scale, or down's
+        // routing weight (times the E4M3 row scale) and output row
+        const int lrow = ti.row0 + c0 + (lane & 15);
+        const bool lvalid = c0 + (lane & 15) < ti.nvalid;
+        float lfac = 1.f;
+        int lorow = lrow;
+        if constexpr (GATEUP) {
+          if constexpr (F8)
+            if (lvalid) lfac = p.b_scale[p.perm_src[lrow] / p.topk];
+        } else {
+          if (lvalid) {
+            lfac = F8 ? p.b_scale[lrow] * p.perm_w[lrow] : p.perm_w[lrow];
+            if (p.out_rows) lorow = p.out_rows[lrow];
+          }
+        }
         if constexpr (GATEUP) {
           uint32_t rb[16];
           ptx::tmem_ld16(tq + NT + c0, rb);
           ptx::tmem_wait_ld();
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
+            // c0 + j < ti.nvalid is the same on every lane of the warp
             if (c0 + j < ti.nvalid) {
               float g = __uint_as_float(ra[j]);
               float u = __uint_as_float(rb[j]);
               if constexpr (F8) {
-                const float sx = p.b_scale[p.perm_src[ti.row0 + c0 + j] / p.topk];
+                const float sx = __shfl_sync(kFull, lfac, j);
                 g *= sw0 * sx;
                 u *= sw1 * sx;
               }
@@ -439,9 +457,8 @@ __global__ void __launch_bounds__(threads_for(NT, MODE), 1)
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             if (c0 + j < ti.nvalid) {
-              const int row = ti.row0 + c0 + j;
-              const int orow = p.out_rows ? p.out_rows[row] : row;
-              const float w = F8 ? p.b_scale[row] * p.perm_w[row] : p.perm_w[row];
+              const float w = __shfl_sync(kFull, lfac, j);
+              const int orow = __shfl_sync(kFull, lorow, j);
               float* dst = p.f32_out + static_cast<int64_t>(orow) * p.out_ld + pcol;
               dst[0] = F8 ? __uint_as_float(ra[j]) * sw0 * w : __uint_as_float(ra[j]) * w;
               dst[BM] = F8 ? __uint_as_float(rb[j]) * sw1 * w : __uint_as_float(rb[j]) * w;
@@ -452,11 +469,10 @@ __global__ void __launch_bounds__(threads_for(NT, MODE), 1)
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             if (c0 + j < ti.nvalid) {
-              const int row = ti.row0 + c0 + j;
-              const int orow = p.out_rows ? p.out_rows[row] : row;
+              const float w = __shfl_sync(kFull, lfac, j);
+              const int orow = __shfl_sync(kFull, lorow, j);
               p.f32_out[static_cast<int64_t>(orow) * p.out_ld + col] =
-                  F8 ? __uint_as_float(ra[j]) * sw0 * (p.b_scale[row] * p.perm_w[row])
-                     : __uint_as_float(ra[j]) * p.perm_w[row];
+                  F8 ? __uint_as_float(ra[j]) * sw0 * w : __uint_as_float(ra[j]) * w;
             }
           }
         }

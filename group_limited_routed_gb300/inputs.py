@@ -91,6 +91,13 @@ CONFIGS = {
     "fp8_prefill": MoEConfig(name="fp8_prefill", T=8192, seed=10, weight_fmt="fp8", **_BEAM,
                              description="Beam MoE layer prefill chunk T=8192, dynamic FP8 "
                                          "experts"),
+    # profiling case for the FP8 kernels in the prefill regime: 32 experts,
+    # 256 rows each on average
+    "profile_fp8_prefill": MoEConfig(name="profile_fp8_prefill", T=1024, d=5120, n_experts=32,
+                                     n_groups=8, topk_groups=4, topk=8, d_ff=2560, seed=12,
+                                     weight_fmt="fp8",
+                                     description="Beam expert shapes, 32 FP8 experts (8x4), "
+                                                 "T=1024 (profiling case, prefill regime)"),
     # profiling case for the FP8 kernels: 32 experts, decode-sized batch
     "profile_fp8": MoEConfig(name="profile_fp8", T=8, d=5120, n_experts=32, n_groups=8,
                              topk_groups=4, topk=8, d_ff=2560, seed=11, weight_fmt="fp8",
