@@ -93,3 +93,21 @@ def test_nvfp4_and_boundary_replays_match_eager():
                                          gam, 1e-6, 5)
     for a, b in ((o2, o_ref), (res, res_ref), (nx, nx_ref)):
         assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_fp8_replays_match_eager():
+    """Both token-block widths: 64 tokens (16-row blocks) and 300 (256-row
+    blocks with the gathered token codes)."""
+    for T in (64, 300):
+        cfg = inputs.CONFIGS["tiny"].replace(weight_fmt="fp8", T=T, seed=40 + T)
+        t = inputs.generate(cfg, "cuda")
+        wts = [pkg.Fp8Weight.of(t[n]) for n in ("w_gate", "w_up", "w_down")]
+        ws = pkg.Workspace(cfg, T, weight_fmt=pkg.FP8)
+        out = torch.empty(T, cfg.d, dtype=torch.bfloat16, device="cuda")
+        g = _capture(lambda: pkg.forward_fp8(cfg, t["hidden"], t["router_w"], t["corr_bias"], *wts,
+                                             out=out, ws=ws, stream=torch.cuda.current_stream()))
+        g.replay()
+        torch.cuda.synchronize()
+        ref = pkg.forward_fp8(cfg, t["hidden"], t["router_w"], t["corr_bias"], *wts)
+        assert torch.equal(out.view(torch.int16), ref.view(torch.int16)), T
+        assert pkg.check_status(ws) == 0
