@@ -53,3 +53,30 @@ def test_beam_config_parity(name, n_sample):
         del t
         gc.collect()
         torch.cuda.empty_cache()
+
+
+def test_beam_largest_batch():
+    """65536 tokens (524288 token rows, 2048 per expert): row offsets past
+    2^31 elements in the FP32 expert outputs, the counting sort over 512
+    chunks, 40960 GEMM tiles.  Routing on every token, outputs on a sample
+    that includes the first and last tokens."""
+    cfg = inputs.CONFIGS["prefill"].replace(T=65536, seed=21)
+    t = inputs.generate(cfg, "cuda")
+    try:
+        lg, r = oracle_route(cfg, t)
+        ws = pkg.Workspace(cfg, cfg.T)
+        out = pkg.forward(cfg, t["hidden"], t["router_w"], t["corr_bias"], t["w_gate"],
+                          t["w_up"], t["w_down"], ws=ws)
+        assert pkg.check_status(ws) == 0
+        idx = host(ws.view("topk_idx", torch.int32, (cfg.T, cfg.topk)))
+        w = host(ws.view("topk_w", torch.float32, (cfg.T, cfg.topk)))
+        check_routing(cfg, idx, w, r)
+        rows = _sample(cfg.T, 8, seed=3)
+        rows = rows[~exempt_tokens(r)[rows]]
+        err, rms, same = check_out(out, oracle_out(cfg, t, r["idx"], r["w"], tokens=rows),
+                                   rows=rows)
+        print(f"T=65536: {len(rows)} tokens, max|err| {err:.3e}, RMS {rms:.3e}")
+    finally:
+        del t
+        gc.collect()
+        torch.cuda.empty_cache()
