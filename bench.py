@@ -240,10 +240,13 @@ def run_reference(args, cfg):
     gen_cfg = cfg if dev.type == "cuda" else cfg.replace(cpu_generator=True)
     t = inputs.generate(gen_cfg, dev)
     a16 = cfg.weight_fmt == "nvfp4" and args.a16
-    # size each step so the whole run stays within about two minutes
+    # size each step so the whole run stays within about two minutes; the
+    # oracle spreads tokens over its threads, so a step samples at least one
+    # token per thread when that fits (one token alone would use one core)
+    cores = oracle.num_threads()
     sec1, _ = oracle_sample(cfg, t, 1, seed=1, a16=a16)
     per_step_budget = 120.0 / max(1, args.steps + args.warmup)
-    n = int(max(1, min(cfg.T, per_step_budget / max(sec1, 1e-6))))
+    n = int(max(1, min(cfg.T, cores * per_step_budget / max(sec1, 1e-6))))
     for i in range(args.warmup):
         oracle_sample(cfg, t, n, seed=100 + i, a16=a16)
     secs = 0.0
@@ -257,7 +260,7 @@ def run_reference(args, cfg):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": config_record(cfg, None, a16=a16),
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores,
                              "kind": "oracle",
                              "sample": f"{n} sampled tokens of the {cfg.T}-token batch per step"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
