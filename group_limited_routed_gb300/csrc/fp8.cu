@@ -73,11 +73,75 @@ __global__ void __launch_bounds__(kThreads) quantize_e4m3_rows_kernel(
   if (threadIdx.x == 0) scale[row] = s;
 }
 
+// The same rule with one warp per row and the row held in registers (V
+// 16-byte words per lane: cols <= 256 V): one read of the row, the amax by
+// shuffles, no shared memory.  Four rows per 128-thread block.
+template <int V>
+__global__ void __launch_bounds__(kThreads) quantize_e4m3_rows_warp_kernel(
+    const uint16_t* __restrict__ x, const int32_t* __restrict__ n_valid, int64_t rows,
+    int32_t cols, uint8_t* __restrict__ q, float* __restrict__ scale) {
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * (kThreads / 32) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  // row is the same on every lane of the warp: whole warps leave together
+  if (row >= rows || (n_valid && row >= *n_valid)) return;
+  const uint4* in = reinterpret_cast<const uint4*>(x + row * cols);
+  const int n8 = cols / 8;
+  uint4 v[V];
+  float amax = 0.f;
+#pragma unroll
+  for (int j = 0; j < V; ++j) {
+    const int i = lane + 32 * j;
+    if (i < n8) {
+      v[j] = in[i];
+      const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w[k])), fabsf(bf16_hi(w[k]))));
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  const float s = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
+  uint2* out = reinterpret_cast<uint2*>(q + row * cols);
+#pragma unroll
+  for (int j = 0; j < V; ++j) {
+    const int i = lane + 32 * j;
+    if (i < n8) {
+      const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+      uint32_t c[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        c[k] = e4m3x2(__fdiv_rn(bf16_lo(w[k]), s), __fdiv_rn(bf16_hi(w[k]), s));
+      out[i] = make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+    }
+  }
+  if (lane == 0) scale[row] = s;
+}
+
+template <int V>
+void launch_warp(const uint16_t* x, const int32_t* n_valid, int64_t rows, int32_t cols,
+                 uint8_t* q, float* scale, cudaStream_t s) {
+  const int64_t blocks = (rows + kThreads / 32 - 1) / (kThreads / 32);
+  quantize_e4m3_rows_warp_kernel<V>
+      <<<static_cast<unsigned>(blocks), kThreads, 0, s>>>(x, n_valid, rows, cols, q, scale);
+}
+
 }  // namespace
 
 void launch_quantize_e4m3_rows(const uint16_t* x, const int32_t* n_valid, int64_t rows,
                                int32_t cols, uint8_t* q, float* scale, cudaStream_t s) {
   if (rows <= 0) return;
+  // Many short rows (the h rows of a large batch): one warp per row from
+  // registers, 124 -> 102 us on 65536 rows of 2560.  Few rows or long rows
+  // (the token rows, decode batches): one block per row, which keeps more
+  // loads and divisions in flight per row (5120-wide rows: 28 us against 35
+  // with a warp per row; 32 rows: 7 us against 12).
+  const int v = (cols / 8 + 31) / 32;  // 16-byte words per lane
+  if (rows >= 2048 && v <= 12) {
+    if (v <= 4) return launch_warp<4>(x, n_valid, rows, cols, q, scale, s);
+    if (v <= 8) return launch_warp<8>(x, n_valid, rows, cols, q, scale, s);
+    return launch_warp<12>(x, n_valid, rows, cols, q, scale, s);
+  }
   quantize_e4m3_rows_kernel<<<static_cast<unsigned>(rows), kThreads, 0, s>>>(x, n_valid, cols, q,
                                                                             scale);
 }

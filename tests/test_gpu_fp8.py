@@ -72,9 +72,12 @@ def _oracle_fp8(cfg, t, r, tokens=None):
                               tokens=None if tokens is None else rows, exact=True)
 
 
-def test_row_quantiser_is_bit_exact():
+@pytest.mark.parametrize("n,cols", [(67, 8), (67, 2560), (67, 5120), (2051, 40), (2051, 2560),
+                                    (2051, 3072)])
+def test_row_quantiser_is_bit_exact(n, cols):
+    """One block per row (67 rows, or rows longer than 3072 values) and one
+    warp per row (2051 rows of up to 3072: a ragged last block of four)."""
     g = torch.Generator().manual_seed(5)
-    n, cols = 67, 2560
     mag = torch.exp(torch.empty(n, 1).uniform_(-14, 8, generator=g))
     x = (torch.randn(n, cols, generator=g) * mag)
     x[5] = 0.0                                     # scale 1, all codes 0
