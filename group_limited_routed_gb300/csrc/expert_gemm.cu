@@ -499,10 +499,7 @@ cudaError_t launch_impl(const CUtensorMap& a0, const CUtensorMap& a1, const CUte
                         const GemmArgs& p, int grid, cudaStream_t s) {
   using C = Cfg<NT, MODE>;
   auto kern = expert_gemm_kernel<NT, MODE, F8>;
-  // set once per instantiation (thread-safe static initialisation), so a
-  // call can also be captured into a CUDA graph
-  static const cudaError_t err =
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  const cudaError_t err = smem_limit_once<expert_gemm_kernel<NT, MODE, F8>>(C::SMEM_BYTES);
   if (err != cudaSuccess) return err;
   kern<<<grid, C::THREADS, C::SMEM_BYTES, s>>>(a0, a1, b, p);
   return cudaGetLastError();

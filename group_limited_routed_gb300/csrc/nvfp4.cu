@@ -454,8 +454,7 @@ cudaError_t launch_fp4_impl(const CUtensorMap& a0, const CUtensorMap& a1, const 
                             cudaStream_t s) {
   using C = Cfg<NT, KIND>;
   auto kern = fp4_gemm_kernel<NT, KIND>;
-  static const cudaError_t err =  // once per instantiation
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  const cudaError_t err = smem_limit_once<fp4_gemm_kernel<NT, KIND>>(C::SMEM_BYTES);
   if (err != cudaSuccess) return err;
   kern<<<grid, kThreads, C::SMEM_BYTES, s>>>(a0, a1, b, sfb, p);
   return cudaGetLastError();

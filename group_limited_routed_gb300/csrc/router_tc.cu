@@ -280,8 +280,7 @@ cudaError_t launch_router_tc(const CUtensorMap& w_planes, const CUtensorMap& x, 
   const int64_t tiles = static_cast<int64_t>(E / BM) * ((T + BN - 1) / BN);
   const int grid = static_cast<int>(tiles < num_sms ? tiles : num_sms);
   if (grid <= 0) return cudaSuccess;
-  static const cudaError_t err = cudaFuncSetAttribute(  // once
-      router_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  const cudaError_t err = smem_limit_once<router_tc_kernel>(SMEM_BYTES);
   if (err != cudaSuccess) return err;
   router_tc_kernel<<<grid, kThreads, SMEM_BYTES, s>>>(w_planes, x, logits, T, E, d, status,
                                                       wait_limit_ns);

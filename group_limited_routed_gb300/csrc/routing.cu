@@ -793,14 +793,8 @@ void launch_router_split(const float* w, int32_t E, int32_t d, uint16_t* planes,
 
 cudaError_t launch_fused_route(const RouterArgs& ra, int ksplit, const SelectArgs& sa,
                                const PermuteArgs& pa, int num_sms, cudaStream_t s) {
-  // resident blocks per SM, queried once (thread-safe static initialisation)
-  static const int per_sm = [] {
-    int v = 0;
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, fused_route_kernel, 256, 0) ==
-                   cudaSuccess
-               ? v
-               : 0;
-  }();
+  // all blocks of a cooperative launch are resident at once
+  const int per_sm = blocks_per_sm_once<fused_route_kernel>(256);
   if (per_sm <= 0) return cudaErrorUnknown;
   const int64_t tiles = static_cast<int64_t>((ra.E + kRtExp - 1) / kRtExp) *
                         ((ra.T + kRtTok - 1) / kRtTok) * ksplit;
@@ -821,9 +815,8 @@ cudaError_t launch_combine_boundary(const float* y, const int32_t* pair_row, int
                                     int32_t d, uint16_t* out, const BoundaryArgs& b,
                                     cudaStream_t s) {
   const size_t smem = static_cast<size_t>(d) * sizeof(float);
-  // once: the largest row the entry point accepts (d <= 51200)
-  static const cudaError_t e = cudaFuncSetAttribute(
-      combine_boundary_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+  // the largest row the entry point accepts (d <= 51200)
+  const cudaError_t e = smem_limit_once<combine_boundary_kernel>(200 * 1024);
   if (e != cudaSuccess) return e;
   combine_boundary_kernel<<<static_cast<unsigned>(T), 256, smem, s>>>(y, pair_row, k, d, out, b);
   return cudaGetLastError();
@@ -838,13 +831,7 @@ void launch_ep_pack(const int32_t* idx, const int32_t* perm_src, const float* pe
 }
 
 cudaError_t launch_permute_sort(const PermuteArgs& a, int32_t* hist, int num_sms, cudaStream_t s) {
-  static const int per_sm = [] {
-    int v = 0;
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, permute_sort_kernel, 256, 0) ==
-                   cudaSuccess
-               ? v
-               : 0;
-  }();
+  const int per_sm = blocks_per_sm_once<permute_sort_kernel>(256);
   if (per_sm <= 0) return cudaErrorUnknown;
   const int64_t nc = (a.TK + kSortChunk - 1) / kSortChunk;
   const int64_t cap = static_cast<int64_t>(per_sm) * num_sms;

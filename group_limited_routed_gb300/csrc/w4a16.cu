@@ -492,8 +492,7 @@ cudaError_t launch_impl(const CUtensorMap& a0, const CUtensorMap& a1, const CUte
                         const W4a16GemmArgs& p, int grid, cudaStream_t s) {
   using C = Cfg<NT, GATEUP>;
   auto kern = w4a16_gemm_kernel<NT, GATEUP>;
-  static const cudaError_t err =  // once per instantiation
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  const cudaError_t err = smem_limit_once<w4a16_gemm_kernel<NT, GATEUP>>(C::SMEM_BYTES);
   if (err != cudaSuccess) return err;
   kern<<<grid, kThreads, C::SMEM_BYTES, s>>>(a0, a1, b, p);
   return cudaGetLastError();
