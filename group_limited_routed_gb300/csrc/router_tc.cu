@@ -23,6 +23,7 @@
 #include <cstdint>
 
 #include "common.cuh"
+#include "launch_once.cuh"
 #include "ptx.cuh"
 
 namespace beam {

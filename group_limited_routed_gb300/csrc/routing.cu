@@ -18,6 +18,7 @@
 #include <cstdint>
 
 #include "common.cuh"
+#include "launch_once.cuh"
 
 namespace beam {
 namespace {

@@ -28,6 +28,7 @@
 #include <cstdint>
 
 #include "common.cuh"
+#include "launch_once.cuh"
 #include "gemm_common.cuh"
 #include "ptx.cuh"
 
