@@ -355,36 +355,51 @@ def run_gpu(args, cfg):
     if use_dist:
         dist.barrier()
     torch.cuda.synchronize()
-    graph = None
+    graphs = None
     if args.graph:
-        # one layer call captured with its stage events (event-record nodes);
-        # each replay records them again, so they hold the last replay's times
+        # one layer call captured twice: plain, and with its stage events
+        # (event-record nodes; each replay records them again, so they hold
+        # the last replay's times)
         gevs = [torch.cuda.Event(enable_timing=True) for _ in range(8)]
         for e in gevs:
             e.record(stream)  # creates the handles
-        graph = torch.cuda.CUDAGraph()
+        graphs = [torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()]
+        with torch.cuda.graph(graphs[0]):
+            step()
         pkg.set_stage_events(gevs)
-        with torch.cuda.graph(graph):
+        with torch.cuda.graph(graphs[1]):
             step()
         pkg.set_stage_events(None)
-        for _ in range(3):
-            graph.replay()
+        for g in graphs:
+            for _ in range(3):
+                g.replay()
         torch.cuda.synchronize()
-    t_start.record(stream)
-    for i in range(args.steps):
-        if graph is not None:
-            graph.replay()
-        else:
-            pkg.set_stage_events(evs[i])
-            step()
-    t_end.record(stream)
-    torch.cuda.synchronize()
-    if use_dist:
-        dist.barrier()
-    pkg.set_stage_events(None)
+
+    def timed_loop(with_events: bool) -> float:
+        """K steps between a barrier and a synchronize on both sides; with
+        stage events the library records each step's stage boundaries (they
+        cost GPU time of their own, so the headline loop runs without)."""
+        if use_dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+        t_start.record(stream)
+        for i in range(args.steps):
+            if graphs is not None:
+                graphs[1 if with_events else 0].replay()
+            else:
+                pkg.set_stage_events(evs[i] if with_events else None)
+                step()
+        t_end.record(stream)
+        torch.cuda.synchronize()
+        if use_dist:
+            dist.barrier()
+        pkg.set_stage_events(None)
+        return t_start.elapsed_time(t_end)
+
+    ms = timed_loop(False)          # the layer as a caller runs it
+    ms_events = timed_loop(True)    # the same steps with stage events: per-kernel times
     clocks = sampler.stop()
-    ms = t_start.elapsed_time(t_end)
-    if graph is not None:
+    if graphs is not None:
         stage_ms = np.array([gevs[j].elapsed_time(gevs[j + 1]) for j in range(7)])
     else:
         stage_ms = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(7)]
@@ -482,6 +497,9 @@ def run_gpu(args, cfg):
                            "tflops_frac_sustained":
                                layer_flops / (layer_ms / 1e3) / 1e12 / tc_peak},
         "stage_us": {n: round(float(v) * 1e3, 1) for n, v in zip(STAGES, stage_ms)},
+        # the per-stage times (and the roofline's kernel time) come from a
+        # second timed loop of the same steps with stage events recorded
+        "stage_events_ms_per_step": ms_events / args.steps,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": cfg.T * cfg.d * 2,
                 "d2h_bytes_per_step": cfg.T * cfg.d * 2},
         "gpu_launches": args.steps * pkg.kernels_per_forward(
