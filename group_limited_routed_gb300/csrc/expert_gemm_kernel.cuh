@@ -465,8 +465,10 @@ __global__ void __launch_bounds__(threads_for(NT, MODE), 1)
               const float w = __shfl_sync(kFull, lfac, j);
               const int orow = __shfl_sync(kFull, lorow, j);
               float* dst = p.f32_out + static_cast<int64_t>(orow) * p.out_ld + pcol;
-              dst[0] = F8 ? __uint_as_float(ra[j]) * sw0 * w : __uint_as_float(ra[j]) * w;
-              dst[BM] = F8 ? __uint_as_float(rb[j]) * sw1 * w : __uint_as_float(rb[j]) * w;
+              // streaming stores: the FP32 rows are read once, by the
+              // combine, and would otherwise push tiles out of L2
+              __stcs(dst, F8 ? __uint_as_float(ra[j]) * sw0 * w : __uint_as_float(ra[j]) * w);
+              __stcs(dst + BM, F8 ? __uint_as_float(rb[j]) * sw1 * w : __uint_as_float(rb[j]) * w);
             }
           }
         } else {
@@ -476,8 +478,8 @@ __global__ void __launch_bounds__(threads_for(NT, MODE), 1)
             if (c0 + j < ti.nvalid) {
               const float w = __shfl_sync(kFull, lfac, j);
               const int orow = __shfl_sync(kFull, lorow, j);
-              p.f32_out[static_cast<int64_t>(orow) * p.out_ld + col] =
-                  F8 ? __uint_as_float(ra[j]) * sw0 * w : __uint_as_float(ra[j]) * w;
+              __stcs(p.f32_out + static_cast<int64_t>(orow) * p.out_ld + col,
+                     F8 ? __uint_as_float(ra[j]) * sw0 * w : __uint_as_float(ra[j]) * w);
             }
           }
         }
