@@ -87,3 +87,26 @@ def test_smallest_shapes(fmt, T):
         if g.size:
             inside = np.abs(g - exact) <= tol * rms + half_ulp_bf16(exact)
             assert inside.mean() >= 0.99
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "fp8", "nvfp4", "a16"])
+def test_repeated_calls_are_bit_identical(fmt):
+    """Every reduction runs in a fixed order: two calls on the same inputs
+    give the same bits, at both token-block widths (the W4A16 partial sums of
+    its four MMA issuers included)."""
+    for T in (20, 70):
+        d = 256 if fmt in ("nvfp4", "a16") else 128
+        cfg = _cfg(fmt, T, d, seed=3 * T + len(fmt))
+        t = _to(inputs.generate(cfg, "cpu"), "cuda")
+        args = (cfg, t["hidden"], t["router_w"], t["corr_bias"])
+        if fmt == "bf16":
+            run = lambda: pkg.forward(*args, t["w_gate"], t["w_up"], t["w_down"])
+        elif fmt == "fp8":
+            wts = [pkg.Fp8Weight.of(t[n]) for n in ("w_gate", "w_up", "w_down")]
+            run = lambda: pkg.forward_fp8(*args, *wts)
+        else:
+            wts = [pkg.Fp4Weight.of(t[n]) for n in ("w_gate", "w_up", "w_down")]
+            fwd = pkg.forward_nvfp4_a16 if fmt == "a16" else pkg.forward_nvfp4
+            run = lambda: fwd(*args, *wts)
+        a, b = run(), run()
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16)), (fmt, T)
