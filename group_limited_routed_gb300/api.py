@@ -35,7 +35,8 @@ EXPORTS = ("beam_moe_workspace_size", "beam_moe_workspace_layout", "beam_moe_rou
            "beam_moe_kernels_per_forward", "beam_status_string", "beam_moe_ep_dispatch",
            "beam_moe_ep_workspace_size", "beam_moe_ep_experts", "beam_moe_ep_combine",
            "beam_moe_forward_boundary", "beam_moe_forward_nvfp4_a16",
-           "beam_moe_ep_experts_nvfp4", "beam_moe_forward_fp8", "beam_moe_fp8_quantize_rows")
+           "beam_moe_ep_experts_nvfp4", "beam_moe_forward_fp8", "beam_moe_fp8_quantize_rows",
+           "beam_moe_ep_experts_fp8")
 
 
 class BeamError(RuntimeError):
@@ -107,6 +108,9 @@ def lib():
                                            _SZ, _P]
         L.beam_moe_forward_fp8.restype = _ST
         L.beam_moe_fp8_quantize_rows.argtypes = [_P, _I64, ctypes.c_int32, _P, _P, _P]
+        L.beam_moe_ep_experts_fp8.argtypes = [cfgp, ctypes.c_int32, ctypes.c_int32, _P, _P, _P,
+                                              fp8p, fp8p, fp8p, _P, _I64, _P, _SZ, _P]
+        L.beam_moe_ep_experts_fp8.restype = _ST
         L.beam_moe_fp8_quantize_rows.restype = _ST
         L.beam_moe_nvfp4_pack_scales.argtypes = [_P, _I64, _I64, _P, _P]
         L.beam_moe_nvfp4_pack_scales.restype = _ST
@@ -565,6 +569,30 @@ def ep_experts_nvfp4(cfg, n_ranks: int, rank: int, x_recv, expert_recv, w_recv, 
                                            _dev(y, torch.float32, "y_recv"), M, ws.ptr,
                                            ws.nbytes, _stream(stream)),
            "beam_moe_ep_experts_nvfp4")
+    return y
+
+
+def ep_experts_fp8(cfg, n_ranks: int, rank: int, x_recv, expert_recv, w_recv, gate: Fp8Weight,
+                   up: Fp8Weight, down: Fp8Weight, ws: EpWorkspace | None = None, out=None,
+                   stream=None):
+    """This rank's dynamic-FP8 experts on its received rows -> y_recv [M, d] f32."""
+    M = x_recv.shape[0]
+    dev = x_recv.device
+    if ws is None or ws.M_max < M or ws.weight_fmt != FP8:
+        ws = EpWorkspace(cfg, n_ranks, max(M, 1), dev, weight_fmt=FP8)
+    y = torch.empty(M, cfg.d, dtype=torch.float32, device=dev) if out is None else out
+    if M == 0:
+        return y
+    c = _cfg(cfg)
+    _check(lib().beam_moe_ep_experts_fp8(ctypes.byref(c), int(n_ranks), int(rank),
+                                         _dev(x_recv, torch.bfloat16, "x_recv"),
+                                         _dev(expert_recv, torch.int32, "expert_recv"),
+                                         _dev(w_recv, torch.float32, "w_recv"),
+                                         ctypes.byref(gate._c), ctypes.byref(up._c),
+                                         ctypes.byref(down._c),
+                                         _dev(y, torch.float32, "y_recv"), M, ws.ptr,
+                                         ws.nbytes, _stream(stream)),
+           "beam_moe_ep_experts_fp8")
     return y
 
 

@@ -533,17 +533,21 @@ beam_status_t run_experts_nvfp4(const beam_moe_config_t& c, const void* hidden, 
 }
 
 // permute + E4M3 token rows (+ gather) + FP8 gate/up (BF16 h) + E4M3 h rows
-// + FP8 down + combine
+// + FP8 down + combine.  With y_pairs given, the down GEMM writes each
+// pair's weighted FP32 row there (pair order) and there is no combine; idx
+// then holds ids from id_base on.
 beam_status_t run_experts_fp8(const beam_moe_config_t& c, const void* hidden, const int32_t* idx,
                               const float* w, const beam_fp8_weight_t& gate,
                               const beam_fp8_weight_t& up, const beam_fp8_weight_t& down,
                               void* out, int64_t T, void* ws, const Layout& L, const DevInfo& dev,
-                              cudaStream_t s, bool permuted = false) {
+                              cudaStream_t s, bool permuted = false, float* y_pairs = nullptr,
+                              int32_t id_base = 0) {
   const int64_t TK = T * c.topk;
   const int64_t rows = std::max<int64_t>(TK, kMinRows);
   const int nt_gu = gateup_tile(c, TK);
   const int nt_dn = down_tile(c, TK);
-  const beam::PermuteArgs pa = permute_args(c, idx, w, T, ws, L);
+  beam::PermuteArgs pa = permute_args(c, idx, w, T, ws, L);
+  pa.id_base = id_base;
   if (!permuted) {
     if (launch_permutation(pa, ws, L, dev, s) != BEAM_OK) return BEAM_ERR_CUDA;
     record(3, s);
@@ -609,8 +613,8 @@ beam_status_t run_experts_fp8(const beam_moe_config_t& c, const void* hidden, co
 
   beam::launch_quantize_e4m3_rows(h, pa.offsets + c.n_experts, TK, c.d_ff, hq, hs, s);
   ga.h_out = nullptr;
-  ga.f32_out = y;
-  ga.out_rows = nullptr;
+  ga.f32_out = y_pairs ? y_pairs : y;
+  ga.out_rows = y_pairs ? pa.perm_src : nullptr;
   ga.out_ld = c.d;
   ga.rows_per_expert = c.d;
   const bool pair = c.d % 256 == 0 && nt_dn == 256;
@@ -624,7 +628,7 @@ beam_status_t run_experts_fp8(const beam_moe_config_t& c, const void* hidden, co
                                 tm_h, ga, grid_for(ga.m_blocks, nt_dn), s, true) != cudaSuccess)
     return BEAM_ERR_CUDA;
   record(6, s);
-  beam::launch_combine(y, pa.pair_row, T, c.topk, c.d, static_cast<uint16_t*>(out), s);
+  if (!y_pairs) beam::launch_combine(y, pa.pair_row, T, c.topk, c.d, static_cast<uint16_t*>(out), s);
   record(7, s);
   return cuda_status(cudaGetLastError());
 }
@@ -1087,7 +1091,9 @@ beam_status_t beam_moe_ep_dispatch(const beam_moe_config_t* cfg, const void* hid
 size_t beam_moe_ep_workspace_size(const beam_moe_config_t* cfg, int32_t n_ranks, int64_t M_max,
                                   int32_t weight_fmt) {
   if (!valid_ep(cfg, n_ranks) || M_max < 0 || M_max > (int64_t(1) << 31) / 64) return 0;
-  if (weight_fmt != BEAM_WEIGHTS_BF16 && weight_fmt != BEAM_WEIGHTS_NVFP4) return 0;
+  if (weight_fmt != BEAM_WEIGHTS_BF16 && weight_fmt != BEAM_WEIGHTS_NVFP4 &&
+      weight_fmt != BEAM_WEIGHTS_FP8)
+    return 0;
   if (weight_fmt == BEAM_WEIGHTS_NVFP4 && (cfg->d % 256 || cfg->d_ff % 256)) return 0;
   return make_layout(local_cfg(*cfg, n_ranks), std::max<int64_t>(M_max, 1), weight_fmt).total;
 }
@@ -1147,6 +1153,37 @@ beam_status_t beam_moe_ep_experts_nvfp4(const beam_moe_config_t* cfg, int32_t n_
   record(2, s);
   return run_experts_nvfp4(lc, x_recv, expert_recv, w_recv, *gate, *up, *down, nullptr, M,
                            workspace, L, dev, s, false, y_recv, rank * lc.n_experts);
+}
+
+beam_status_t beam_moe_ep_experts_fp8(const beam_moe_config_t* cfg, int32_t n_ranks, int32_t rank,
+                                      const void* x_recv, const int32_t* expert_recv,
+                                      const float* w_recv, const beam_fp8_weight_t* gate,
+                                      const beam_fp8_weight_t* up, const beam_fp8_weight_t* down,
+                                      float* y_recv, int64_t M, void* workspace, size_t ws_bytes,
+                                      void* stream) {
+  if (!valid_ep(cfg, n_ranks) || rank < 0 || rank >= n_ranks || M < 0 ||
+      M > (int64_t(1) << 31) / 64)
+    return BEAM_ERR_INVALID_ARG;
+  if (M == 0) return BEAM_OK;
+  const beam_moe_config_t lc = local_cfg(*cfg, n_ranks);
+  if (!aligned16(workspace) || !aligned16(x_recv) || !aligned16(expert_recv) ||
+      !aligned16(w_recv) || !valid_fp8_weight(gate) || !valid_fp8_weight(up) ||
+      !valid_fp8_weight(down) || !aligned16(y_recv))
+    return BEAM_ERR_INVALID_ARG;
+  const Layout L = make_layout(lc, M, BEAM_WEIGHTS_FP8);
+  if (ws_bytes < L.total) return BEAM_ERR_WORKSPACE;
+  DevInfo dev;
+  if (!device_info(&dev)) return BEAM_ERR_CUDA;
+  if (!dev.supported) return BEAM_ERR_UNSUPPORTED;
+  if (!encoder()) return BEAM_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  record(0, s);
+  record(1, s);
+  record(2, s);
+  // one received row per (token, slot): the rows are quantised per row, which
+  // gives each the codes and scale of its token
+  return run_experts_fp8(lc, x_recv, expert_recv, w_recv, *gate, *up, *down, nullptr, M,
+                         workspace, L, dev, s, false, y_recv, rank * lc.n_experts);
 }
 
 beam_status_t beam_moe_ep_combine(const beam_moe_config_t* cfg, const float* y_back, int64_t T,

@@ -26,9 +26,10 @@ def forward_ep(cfg, hidden, router_w, corr_bias, w_gate, w_up, w_down, group=Non
     """This rank's tokens through the expert-parallel layer -> out [T, d] bf16.
 
     ``w_gate`` / ``w_up`` [E/R, d_ff, d] and ``w_down`` [E/R, d, d_ff] hold
-    this rank's experts, BF16 tensors or ``api.Fp4Weight`` (NVFP4, as the
-    pages' MegaMoE path).  ``ops`` supplies ``ep_dispatch``, ``ep_experts``,
-    ``ep_experts_nvfp4`` and ``ep_combine`` (default: the CUDA library)."""
+    this rank's experts, BF16 tensors, ``api.Fp4Weight`` (NVFP4, as the
+    pages' MegaMoE path) or ``api.Fp8Weight`` (dynamic FP8).  ``ops``
+    supplies ``ep_dispatch``, ``ep_experts``, ``ep_experts_nvfp4``,
+    ``ep_experts_fp8`` and ``ep_combine`` (default: the CUDA library)."""
     ops = api if ops is None else ops
     R = dist.get_world_size(group)
     r = dist.get_rank(group)
@@ -50,7 +51,8 @@ def forward_ep(cfg, hidden, router_w, corr_bias, w_gate, w_up, w_down, group=Non
     dist.all_to_all_single(recv_e, send_e, recv_split, send_split, group=group)
     dist.all_to_all_single(recv_w, send_w, recv_split, send_split, group=group)
 
-    experts = ops.ep_experts_nvfp4 if isinstance(w_gate, api.Fp4Weight) else ops.ep_experts
+    experts = (ops.ep_experts_nvfp4 if isinstance(w_gate, api.Fp4Weight)
+               else ops.ep_experts_fp8 if isinstance(w_gate, api.Fp8Weight) else ops.ep_experts)
     y_recv = experts(cfg, R, r, recv_x, recv_e, recv_w, w_gate, w_up, w_down)
 
     y_back = y_recv.new_empty(T * cfg.topk, cfg.d)

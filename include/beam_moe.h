@@ -342,9 +342,10 @@ beam_status_t beam_moe_ep_dispatch(const beam_moe_config_t *cfg, const void *hid
                                    float *send_w, int32_t *send_counts, void *workspace,
                                    size_t ws_bytes, void *stream);
 
-/* Workspace bytes of beam_moe_ep_experts (weight_fmt BEAM_WEIGHTS_BF16) or
- * beam_moe_ep_experts_nvfp4 (BEAM_WEIGHTS_NVFP4) for up to M_max received
- * rows; 0 for an invalid configuration or format. */
+/* Workspace bytes of beam_moe_ep_experts (weight_fmt BEAM_WEIGHTS_BF16),
+ * beam_moe_ep_experts_nvfp4 (BEAM_WEIGHTS_NVFP4) or beam_moe_ep_experts_fp8
+ * (BEAM_WEIGHTS_FP8) for up to M_max received rows; 0 for an invalid
+ * configuration or format. */
 size_t beam_moe_ep_workspace_size(const beam_moe_config_t *cfg, int32_t n_ranks, int64_t M_max,
                                   int32_t weight_fmt);
 
@@ -373,6 +374,19 @@ beam_status_t beam_moe_ep_experts_nvfp4(const beam_moe_config_t *cfg, int32_t n_
                                         const beam_fp4_weight_t *gate, const beam_fp4_weight_t *up,
                                         const beam_fp4_weight_t *down, float *y_recv, int64_t M,
                                         void *workspace, size_t ws_bytes, void *stream);
+
+/* beam_moe_ep_experts with dynamic FP8 expert weights (beyond the pages,
+ * whose expert-parallel MegaMoE path leaves dynamic FP8 out): each received
+ * row is quantised to E4M3 with its own scale (a row per token and slot, so
+ * the token's codes and scale) and goes through the FP8 GEMMs of
+ * beam_moe_forward_fp8; gate / up / down describe this rank's E/n_ranks
+ * experts (codes [E/n_ranks, N, K], row scales [E/n_ranks, N]). */
+beam_status_t beam_moe_ep_experts_fp8(const beam_moe_config_t *cfg, int32_t n_ranks,
+                                      int32_t rank, const void *x_recv,
+                                      const int32_t *expert_recv, const float *w_recv,
+                                      const beam_fp8_weight_t *gate, const beam_fp8_weight_t *up,
+                                      const beam_fp8_weight_t *down, float *y_recv, int64_t M,
+                                      void *workspace, size_t ws_bytes, void *stream);
 
 /* The owner's combine: out[t] = bf16(sum over slots, in slot order, of the
  * returned FP32 rows), y_back [T*topk, d] in the order beam_moe_ep_dispatch

@@ -78,6 +78,14 @@ def test_boundary_and_expert_parallel_checks(lib):
     # a rank that received nothing launches nothing
     assert lib.beam_moe_ep_experts(cfg, 8, 3, None, None, None, None, None, None, None,
                                    ctypes.c_int64(0), None, ctypes.c_size_t(0), None) == OK
+    for name in ("beam_moe_ep_experts_nvfp4", "beam_moe_ep_experts_fp8"):
+        fn = getattr(lib, name)
+        fn.restype = ctypes.c_int
+        for n_ranks, rank in ((3, 0), (8, 8), (8, -1)):
+            assert fn(cfg, n_ranks, rank, None, None, None, None, None, None, None,
+                      ctypes.c_int64(4), None, ctypes.c_size_t(0), None) == INVALID, (name, rank)
+        assert fn(cfg, 8, 3, None, None, None, None, None, None, None, ctypes.c_int64(0), None,
+                  ctypes.c_size_t(0), None) == OK
     lib.beam_moe_kernels_per_forward.restype = ctypes.c_int32
     assert lib.beam_moe_kernels_per_forward(_cfg(n_groups=7), ctypes.c_int64(32), 0, 0) == 0
 

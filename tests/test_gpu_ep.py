@@ -122,3 +122,31 @@ def test_emulated_ranks_nvfp4_experts(Ts):
             continue
         ref = pkg.forward_nvfp4(cfg, h.contiguous(), t["router_w"], t["corr_bias"], *full)
         assert torch.equal(o.view(torch.int16), ref.view(torch.int16))
+
+
+@pytest.mark.parametrize("Ts", [[40, 24], [16, 0, 33, 5]])
+def test_emulated_ranks_fp8_experts(Ts):
+    """Dynamic FP8 experts on each rank: every received row is quantised with
+    its own scale, which is its token's, so every rank's output equals
+    beam_moe_forward_fp8 on its tokens bit for bit."""
+    cfg = inputs.CONFIGS["tiny"].replace(weight_fmt="fp8", seed=95 + len(Ts), cpu_generator=True)
+    t = inputs.generate(cfg, "cpu", T=sum(Ts))
+    t = {k: ({kk: vv.cuda() for kk, vv in v.items()} if isinstance(v, dict)
+             else v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in t.items()}
+    full = [pkg.Fp8Weight.of(t[n]) for n in ("w_gate", "w_up", "w_down")]
+    R = len(Ts)
+    local = []
+    for q in range(R):
+        sl = ep.expert_slice(cfg, R, q)
+        local.append([pkg.Fp8Weight(t[n]["q"][sl], t[n]["s"][sl])
+                      for n in ("w_gate", "w_up", "w_down")])
+
+    def run(R_, q, x, e, w):
+        return pkg.ep_experts_fp8(cfg, R_, q, x, e, w, *local[q])
+
+    hid, outs = _emulate(cfg, t, Ts, experts=run)
+    for h, o in zip(hid, outs):
+        if h.shape[0] == 0:
+            continue
+        ref = pkg.forward_fp8(cfg, h.contiguous(), t["router_w"], t["corr_bias"], *full)
+        assert torch.equal(o.view(torch.int16), ref.view(torch.int16))
