@@ -36,7 +36,8 @@ EXPORTS = ("beam_moe_workspace_size", "beam_moe_workspace_layout", "beam_moe_rou
            "beam_moe_ep_workspace_size", "beam_moe_ep_experts", "beam_moe_ep_combine",
            "beam_moe_forward_boundary", "beam_moe_forward_nvfp4_a16",
            "beam_moe_ep_experts_nvfp4", "beam_moe_forward_fp8", "beam_moe_fp8_quantize_rows",
-           "beam_moe_ep_experts_fp8")
+           "beam_moe_ep_experts_fp8", "beam_moe_forward_nvfp4_boundary",
+           "beam_moe_forward_nvfp4_a16_boundary", "beam_moe_forward_fp8_boundary")
 
 
 class BeamError(RuntimeError):
@@ -125,6 +126,13 @@ def lib():
         L.beam_moe_forward_boundary.argtypes = [cfgp, _P, _P, _P, _P, _P, _P, _P, _I64,
                                                 ctypes.POINTER(_Boundary), _P, _SZ, _P]
         L.beam_moe_forward_boundary.restype = _ST
+        for name, wp in (("beam_moe_forward_nvfp4_boundary", fp4p),
+                         ("beam_moe_forward_nvfp4_a16_boundary", fp4p),
+                         ("beam_moe_forward_fp8_boundary", fp8p)):
+            f = getattr(L, name)
+            f.argtypes = [cfgp, _P, _P, _P, wp, wp, wp, _P, _I64, ctypes.POINTER(_Boundary), _P,
+                          _SZ, _P]
+            f.restype = _ST
         L.beam_moe_ep_dispatch.argtypes = [cfgp, _P, _P, _P, _I64, ctypes.c_int32, _P, _P, _P, _P,
                                            _P, _SZ, _P]
         L.beam_moe_ep_dispatch.restype = _ST
@@ -276,13 +284,28 @@ def forward(cfg, hidden, router_w, corr_bias, w_gate, w_up, w_down, out=None,
 
 def forward_boundary(cfg, hidden, router_w, corr_bias, w_gate, w_up, w_down, residual,
                      post_norm_w, next_norm_w, eps: float, n: int, out=None, next_input=None,
-                     ws: Workspace | None = None, stream=None):
+                     ws: Workspace | None = None, stream=None, a16: bool = False):
     """The layer followed by the decoder's sublayer boundary (post-norm, n-th
     depth-scaled residual add, next pre-norm) in its combine kernel.  Returns
-    (out, next_input); ``residual`` is overwritten with the new stream."""
+    (out, next_input); ``residual`` is overwritten with the new stream.
+
+    The expert format follows the weights: BF16 tensors, ``Fp4Weight`` (NVFP4
+    activations, or F16 ones with ``a16=True``) or ``Fp8Weight``."""
     T = hidden.shape[0]
     dev = hidden.device
-    ws = _ws(cfg, T, ws, dev)
+    if isinstance(w_gate, Fp4Weight):
+        fmt, name = (NVFP4_A16, "beam_moe_forward_nvfp4_a16_boundary") if a16 else \
+            (NVFP4, "beam_moe_forward_nvfp4_boundary")
+        wts = tuple(ctypes.byref(x._c) for x in (w_gate, w_up, w_down))
+    elif isinstance(w_gate, Fp8Weight):
+        fmt, name = FP8, "beam_moe_forward_fp8_boundary"
+        wts = tuple(ctypes.byref(x._c) for x in (w_gate, w_up, w_down))
+    else:
+        fmt, name = BF16, "beam_moe_forward_boundary"
+        wts = (_dev(w_gate, torch.bfloat16, "w_gate"), _dev(w_up, torch.bfloat16, "w_up"),
+               _dev(w_down, torch.bfloat16, "w_down"))
+    if ws is None:
+        ws = Workspace(cfg, max(int(T), 1), dev, weight_fmt=fmt)
     o = torch.empty(T, cfg.d, dtype=torch.bfloat16, device=dev) if out is None else out
     nx = torch.empty(T, cfg.d, dtype=torch.bfloat16, device=dev) if next_input is None \
         else next_input
@@ -291,14 +314,10 @@ def forward_boundary(cfg, hidden, router_w, corr_bias, w_gate, w_up, w_down, res
                   _dev(next_norm_w, torch.bfloat16, "next_norm_w"),
                   _dev(nx, torch.bfloat16, "next_input"), float(eps), int(n))
     c = _cfg(cfg)
-    _check(lib().beam_moe_forward_boundary(ctypes.byref(c), _dev(hidden, torch.bfloat16, "hidden"),
-                                           _dev(router_w, torch.float32, "router_w"),
-                                           _dev(corr_bias, torch.float32, "corr_bias"),
-                                           _dev(w_gate, torch.bfloat16, "w_gate"),
-                                           _dev(w_up, torch.bfloat16, "w_up"),
-                                           _dev(w_down, torch.bfloat16, "w_down"), o.data_ptr(), T,
-                                           ctypes.byref(b), ws.ptr, ws.nbytes, _stream(stream)),
-           "beam_moe_forward_boundary")
+    _check(getattr(lib(), name)(ctypes.byref(c), _dev(hidden, torch.bfloat16, "hidden"),
+                                _dev(router_w, torch.float32, "router_w"),
+                                _dev(corr_bias, torch.float32, "corr_bias"), *wts, o.data_ptr(),
+                                T, ctypes.byref(b), ws.ptr, ws.nbytes, _stream(stream)), name)
     return o, nx
 
 
@@ -339,6 +358,7 @@ def forward_noalloc(cfg, hidden, router_w, corr_bias, w_gate, w_up, w_down, out=
     return o
 
 
+BF16 = 0
 NVFP4 = 1
 NVFP4_A16 = 2
 
@@ -592,7 +612,8 @@ def ep_experts_fp8(cfg, n_ranks: int, rank: int, x_recv, expert_recv, w_recv, ga
                                          ctypes.byref(down._c),
                                          _dev(y, torch.float32, "y_recv"), M, ws.ptr,
                                          ws.nbytes, _stream(stream)),
-           "beam_moe_ep_experts_fp8")
+           "beam_moe_ep_experts_fp8", "beam_moe_forward_nvfp4_boundary",
+           "beam_moe_forward_nvfp4_a16_boundary", "beam_moe_forward_fp8_boundary")
     return y
 
 

@@ -346,6 +346,21 @@ beam_status_t run_route(const beam_moe_config_t& c, const void* hidden, const fl
   return cuda_status(cudaGetLastError());
 }
 
+// The layer's last kernel: the weighted combine of the FP32 expert rows y
+// into BF16 out, or that combine followed by the sublayer boundary when one
+// is given (every expert format ends in the same y rows).  With y_pairs
+// given (expert parallelism) there is no combine here.
+cudaError_t finish_combine(const beam_moe_config_t& c, const float* y, const int32_t* pair_row,
+                           int64_t T, void* out, const float* y_pairs,
+                           const beam::BoundaryArgs* boundary, cudaStream_t s) {
+  if (y_pairs) return cudaSuccess;
+  if (boundary)
+    return beam::launch_combine_boundary(y, pair_row, T, c.topk, c.d,
+                                         static_cast<uint16_t*>(out), *boundary, s);
+  beam::launch_combine(y, pair_row, T, c.topk, c.d, static_cast<uint16_t*>(out), s);
+  return cudaGetLastError();
+}
+
 // permute + gather + expert GEMMs + combine.  With y_pairs given, the down
 // GEMM writes each pair's weighted FP32 row there (pair order) and there is
 // no combine; idx then holds ids from id_base on.
@@ -435,13 +450,8 @@ beam_status_t run_experts(const beam_moe_config_t& c, const void* hidden, const 
   if (err != cudaSuccess) return BEAM_ERR_CUDA;
   record(6, s);
 
-  if (boundary) {
-    if (beam::launch_combine_boundary(y, pa.pair_row, T, c.topk, c.d, static_cast<uint16_t*>(out),
-                                      *boundary, s) != cudaSuccess)
-      return BEAM_ERR_CUDA;
-  } else if (!y_pairs) {
-    beam::launch_combine(y, pa.pair_row, T, c.topk, c.d, static_cast<uint16_t*>(out), s);
-  }
+  if (finish_combine(c, y, pa.pair_row, T, out, y_pairs, boundary, s) != cudaSuccess)
+    return BEAM_ERR_CUDA;
   record(7, s);
   return cuda_status(cudaGetLastError());
 }
@@ -454,7 +464,8 @@ beam_status_t run_experts_nvfp4(const beam_moe_config_t& c, const void* hidden, 
                                 const beam_fp4_weight_t& up, const beam_fp4_weight_t& down,
                                 void* out, int64_t T, void* ws, const Layout& L,
                                 const DevInfo& dev, cudaStream_t s, bool permuted = false,
-                                float* y_pairs = nullptr, int32_t id_base = 0) {
+                                float* y_pairs = nullptr, int32_t id_base = 0,
+                                const beam::BoundaryArgs* boundary = nullptr) {
   const int64_t TK = T * c.topk;
   const int64_t rows = std::max<int64_t>(TK, kMinRows);
   const int nt = fp4_tile(c, TK);
@@ -527,7 +538,8 @@ beam_status_t run_experts_nvfp4(const beam_moe_config_t& c, const void* hidden, 
       cudaSuccess)
     return BEAM_ERR_CUDA;
   record(6, s);
-  if (!y_pairs) beam::launch_combine(y, pa.pair_row, T, c.topk, c.d, static_cast<uint16_t*>(out), s);
+  if (finish_combine(c, y, pa.pair_row, T, out, y_pairs, boundary, s) != cudaSuccess)
+    return BEAM_ERR_CUDA;
   record(7, s);
   return cuda_status(cudaGetLastError());
 }
@@ -541,7 +553,7 @@ beam_status_t run_experts_fp8(const beam_moe_config_t& c, const void* hidden, co
                               const beam_fp8_weight_t& up, const beam_fp8_weight_t& down,
                               void* out, int64_t T, void* ws, const Layout& L, const DevInfo& dev,
                               cudaStream_t s, bool permuted = false, float* y_pairs = nullptr,
-                              int32_t id_base = 0) {
+                              int32_t id_base = 0, const beam::BoundaryArgs* boundary = nullptr) {
   const int64_t TK = T * c.topk;
   const int64_t rows = std::max<int64_t>(TK, kMinRows);
   const int nt_gu = gateup_tile(c, TK);
@@ -628,7 +640,8 @@ beam_status_t run_experts_fp8(const beam_moe_config_t& c, const void* hidden, co
                                 tm_h, ga, grid_for(ga.m_blocks, nt_dn), s, true) != cudaSuccess)
     return BEAM_ERR_CUDA;
   record(6, s);
-  if (!y_pairs) beam::launch_combine(y, pa.pair_row, T, c.topk, c.d, static_cast<uint16_t*>(out), s);
+  if (finish_combine(c, y, pa.pair_row, T, out, y_pairs, boundary, s) != cudaSuccess)
+    return BEAM_ERR_CUDA;
   record(7, s);
   return cuda_status(cudaGetLastError());
 }
@@ -638,7 +651,8 @@ beam_status_t run_experts_w4a16(const beam_moe_config_t& c, const void* hidden, 
                                 const float* w, const beam_fp4_weight_t& gate,
                                 const beam_fp4_weight_t& up, const beam_fp4_weight_t& down,
                                 void* out, int64_t T, void* ws, const Layout& L,
-                                const DevInfo& dev, cudaStream_t s, bool permuted = false) {
+                                const DevInfo& dev, cudaStream_t s, bool permuted = false,
+                                const beam::BoundaryArgs* boundary = nullptr) {
   const int64_t TK = T * c.topk;
   const int64_t rows = std::max<int64_t>(TK, kMinRows);
   const int nt = fp4_tile(c, TK);
@@ -702,7 +716,8 @@ beam_status_t run_experts_w4a16(const beam_moe_config_t& c, const void* hidden, 
       cudaSuccess)
     return BEAM_ERR_CUDA;
   record(6, s);
-  beam::launch_combine(y, pa.pair_row, T, c.topk, c.d, static_cast<uint16_t*>(out), s);
+  if (finish_combine(c, y, pa.pair_row, T, out, nullptr, boundary, s) != cudaSuccess)
+    return BEAM_ERR_CUDA;
   record(7, s);
   return cuda_status(cudaGetLastError());
 }
@@ -713,6 +728,65 @@ bool valid_fp4_weight(const beam_fp4_weight_t* w) {
 
 bool valid_fp8_weight(const beam_fp8_weight_t* w) {
   return w && aligned16(w->q) && aligned16(w->scale);
+}
+
+// The boundary's own argument checks that need no pointer (they come before
+// the empty-batch return, so a bad description fails at T = 0 too): n >= 1,
+// eps >= 0, and a token's FP32 values fit the combine kernel's shared memory.
+bool boundary_shape_ok(const beam_moe_config_t* cfg, const beam_moe_boundary_t* b) {
+  return b && b->residual_index >= 1 && b->eps >= 0.f &&
+         static_cast<int64_t>(cfg->d) * 4 <= 200 * 1024;
+}
+
+// The combine kernel's boundary arguments: c_h = sqrt((n-1)/n) and
+// c_x = 1/sqrt(n) in double, rounded once to FP32.  False for an unaligned
+// buffer.
+bool boundary_args(const beam_moe_boundary_t* b, beam::BoundaryArgs* ba) {
+  if (!aligned16(b->residual) || !aligned16(b->post_norm_w) || !aligned16(b->next_norm_w) ||
+      !aligned16(b->next_input))
+    return false;
+  ba->g_post = static_cast<const uint16_t*>(b->post_norm_w);
+  ba->g_pre = static_cast<const uint16_t*>(b->next_norm_w);
+  ba->residual = static_cast<uint16_t*>(b->residual);
+  ba->next_x = static_cast<uint16_t*>(b->next_input);
+  ba->eps = b->eps;
+  const double n = b->residual_index;
+  ba->c_h = static_cast<float>(std::sqrt((n - 1.0) / n));
+  ba->c_x = static_cast<float>(1.0 / std::sqrt(n));
+  return true;
+}
+
+// The body every quantised-expert layer call shares: checks, routing, then
+// run(idx, w, layout, dev, stream, permuted, boundary) for the format's
+// expert kernels.  bnd == nullptr: the plain layer.
+template <class W, class Valid, class Run>
+beam_status_t forward_quantised(const beam_moe_config_t* cfg, int32_t fmt, const void* hidden,
+                                const float* router_w, const float* corr_bias, const W* gate,
+                                const W* up, const W* down, void* out, int64_t T,
+                                const beam_moe_boundary_t* bnd, void* workspace, size_t ws_bytes,
+                                void* stream, Valid valid, Run run) {
+  Layout L;
+  DevInfo dev;
+  bool empty = false;
+  beam_status_t st = common_checks(cfg, T, workspace, ws_bytes, &L, &dev, &empty, fmt);
+  if (st != BEAM_OK) return st;
+  if (bnd && !boundary_shape_ok(cfg, bnd)) return BEAM_ERR_INVALID_ARG;
+  if (empty) return BEAM_OK;
+  if (!aligned16(hidden) || !aligned16(router_w) || !aligned16(corr_bias) || !valid(gate) ||
+      !valid(up) || !valid(down) || !aligned16(out))
+    return BEAM_ERR_INVALID_ARG;
+  beam::BoundaryArgs ba;
+  if (bnd && !boundary_args(bnd, &ba)) return BEAM_ERR_INVALID_ARG;
+  if (!encoder()) return BEAM_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  record(0, s);
+  int32_t* idx = at<int32_t>(workspace, L.idx);
+  float* w = at<float>(workspace, L.w);
+  bool permuted = false;
+  st = run_route(*cfg, hidden, router_w, corr_bias, T, idx, w, at<float>(workspace, L.logits),
+                 workspace, L, dev, s, &permuted);
+  if (st != BEAM_OK) return st;
+  return run(idx, w, L, dev, s, permuted, bnd ? &ba : nullptr);
 }
 
 // ---------------------------------------------------------------- no-allocation scratch
@@ -856,25 +930,13 @@ beam_status_t beam_moe_forward_boundary(const beam_moe_config_t* cfg, const void
   bool empty = false;
   beam_status_t st = common_checks(cfg, T, workspace, ws_bytes, &L, &dev, &empty);
   if (st != BEAM_OK) return st;
-  if (!bnd || bnd->residual_index < 1 || !(bnd->eps >= 0.f) ||
-      static_cast<int64_t>(cfg->d) * 4 > 200 * 1024)
-    return BEAM_ERR_INVALID_ARG;
+  if (!boundary_shape_ok(cfg, bnd)) return BEAM_ERR_INVALID_ARG;
   if (empty) return BEAM_OK;
+  beam::BoundaryArgs ba;
   if (!aligned16(hidden) || !aligned16(router_w) || !aligned16(corr_bias) || !aligned16(w_gate) ||
-      !aligned16(w_up) || !aligned16(w_down) || !aligned16(out) || !aligned16(bnd->residual) ||
-      !aligned16(bnd->post_norm_w) || !aligned16(bnd->next_norm_w) ||
-      !aligned16(bnd->next_input))
+      !aligned16(w_up) || !aligned16(w_down) || !aligned16(out) || !boundary_args(bnd, &ba))
     return BEAM_ERR_INVALID_ARG;
   if (!encoder()) return BEAM_ERR_CUDA;
-  beam::BoundaryArgs ba;
-  ba.g_post = static_cast<const uint16_t*>(bnd->post_norm_w);
-  ba.g_pre = static_cast<const uint16_t*>(bnd->next_norm_w);
-  ba.residual = static_cast<uint16_t*>(bnd->residual);
-  ba.next_x = static_cast<uint16_t*>(bnd->next_input);
-  ba.eps = bnd->eps;
-  const double n = bnd->residual_index;
-  ba.c_h = static_cast<float>(std::sqrt((n - 1.0) / n));
-  ba.c_x = static_cast<float>(1.0 / std::sqrt(n));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   record(0, s);
   int32_t* idx = at<int32_t>(workspace, L.idx);
@@ -942,27 +1004,25 @@ beam_status_t beam_moe_forward_nvfp4(const beam_moe_config_t* cfg, const void* h
                                      const beam_fp4_weight_t* gate, const beam_fp4_weight_t* up,
                                      const beam_fp4_weight_t* down, void* out, int64_t T,
                                      void* workspace, size_t ws_bytes, void* stream) {
-  Layout L;
-  DevInfo dev;
-  bool empty = false;
-  beam_status_t st = common_checks(cfg, T, workspace, ws_bytes, &L, &dev, &empty,
-                                   BEAM_WEIGHTS_NVFP4);
-  if (st != BEAM_OK || empty) return st;
-  if (!aligned16(hidden) || !aligned16(router_w) || !aligned16(corr_bias) ||
-      !valid_fp4_weight(gate) || !valid_fp4_weight(up) || !valid_fp4_weight(down) ||
-      !aligned16(out))
-    return BEAM_ERR_INVALID_ARG;
-  if (!encoder()) return BEAM_ERR_CUDA;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  record(0, s);
-  int32_t* idx = at<int32_t>(workspace, L.idx);
-  float* w = at<float>(workspace, L.w);
-  bool permuted = false;
-  st = run_route(*cfg, hidden, router_w, corr_bias, T, idx, w, at<float>(workspace, L.logits),
-                 workspace, L, dev, s, &permuted);
-  if (st != BEAM_OK) return st;
-  return run_experts_nvfp4(*cfg, hidden, idx, w, *gate, *up, *down, out, T, workspace, L, dev, s,
-                           permuted);
+  return beam_moe_forward_nvfp4_boundary(cfg, hidden, router_w, corr_bias, gate, up, down, out, T,
+                                         nullptr, workspace, ws_bytes, stream);
+}
+
+beam_status_t beam_moe_forward_nvfp4_boundary(const beam_moe_config_t* cfg, const void* hidden,
+                                              const float* router_w, const float* corr_bias,
+                                              const beam_fp4_weight_t* gate,
+                                              const beam_fp4_weight_t* up,
+                                              const beam_fp4_weight_t* down, void* out, int64_t T,
+                                              const beam_moe_boundary_t* boundary,
+                                              void* workspace, size_t ws_bytes, void* stream) {
+  return forward_quantised(
+      cfg, BEAM_WEIGHTS_NVFP4, hidden, router_w, corr_bias, gate, up, down, out, T, boundary,
+      workspace, ws_bytes, stream, valid_fp4_weight,
+      [&](const int32_t* idx, const float* w, const Layout& L, const DevInfo& dev,
+          cudaStream_t s, bool permuted, const beam::BoundaryArgs* ba) {
+        return run_experts_nvfp4(*cfg, hidden, idx, w, *gate, *up, *down, out, T, workspace, L,
+                                 dev, s, permuted, nullptr, 0, ba);
+      });
 }
 
 beam_status_t beam_moe_forward_fp8(const beam_moe_config_t* cfg, const void* hidden,
@@ -970,27 +1030,25 @@ beam_status_t beam_moe_forward_fp8(const beam_moe_config_t* cfg, const void* hid
                                    const beam_fp8_weight_t* gate, const beam_fp8_weight_t* up,
                                    const beam_fp8_weight_t* down, void* out, int64_t T,
                                    void* workspace, size_t ws_bytes, void* stream) {
-  Layout L;
-  DevInfo dev;
-  bool empty = false;
-  beam_status_t st = common_checks(cfg, T, workspace, ws_bytes, &L, &dev, &empty,
-                                   BEAM_WEIGHTS_FP8);
-  if (st != BEAM_OK || empty) return st;
-  if (!aligned16(hidden) || !aligned16(router_w) || !aligned16(corr_bias) ||
-      !valid_fp8_weight(gate) || !valid_fp8_weight(up) || !valid_fp8_weight(down) ||
-      !aligned16(out))
-    return BEAM_ERR_INVALID_ARG;
-  if (!encoder()) return BEAM_ERR_CUDA;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  record(0, s);
-  int32_t* idx = at<int32_t>(workspace, L.idx);
-  float* w = at<float>(workspace, L.w);
-  bool permuted = false;
-  st = run_route(*cfg, hidden, router_w, corr_bias, T, idx, w, at<float>(workspace, L.logits),
-                 workspace, L, dev, s, &permuted);
-  if (st != BEAM_OK) return st;
-  return run_experts_fp8(*cfg, hidden, idx, w, *gate, *up, *down, out, T, workspace, L, dev, s,
-                         permuted);
+  return beam_moe_forward_fp8_boundary(cfg, hidden, router_w, corr_bias, gate, up, down, out, T,
+                                       nullptr, workspace, ws_bytes, stream);
+}
+
+beam_status_t beam_moe_forward_fp8_boundary(const beam_moe_config_t* cfg, const void* hidden,
+                                            const float* router_w, const float* corr_bias,
+                                            const beam_fp8_weight_t* gate,
+                                            const beam_fp8_weight_t* up,
+                                            const beam_fp8_weight_t* down, void* out, int64_t T,
+                                            const beam_moe_boundary_t* boundary, void* workspace,
+                                            size_t ws_bytes, void* stream) {
+  return forward_quantised(
+      cfg, BEAM_WEIGHTS_FP8, hidden, router_w, corr_bias, gate, up, down, out, T, boundary,
+      workspace, ws_bytes, stream, valid_fp8_weight,
+      [&](const int32_t* idx, const float* w, const Layout& L, const DevInfo& dev,
+          cudaStream_t s, bool permuted, const beam::BoundaryArgs* ba) {
+        return run_experts_fp8(*cfg, hidden, idx, w, *gate, *up, *down, out, T, workspace, L, dev,
+                               s, permuted, nullptr, 0, ba);
+      });
 }
 
 beam_status_t beam_moe_fp8_quantize_rows(const void* x, int64_t n, int32_t cols, uint8_t* q,
@@ -1008,27 +1066,26 @@ beam_status_t beam_moe_forward_nvfp4_a16(const beam_moe_config_t* cfg, const voi
                                          const beam_fp4_weight_t* gate, const beam_fp4_weight_t* up,
                                          const beam_fp4_weight_t* down, void* out, int64_t T,
                                          void* workspace, size_t ws_bytes, void* stream) {
-  Layout L;
-  DevInfo dev;
-  bool empty = false;
-  beam_status_t st = common_checks(cfg, T, workspace, ws_bytes, &L, &dev, &empty,
-                                   BEAM_WEIGHTS_NVFP4_A16);
-  if (st != BEAM_OK || empty) return st;
-  if (!aligned16(hidden) || !aligned16(router_w) || !aligned16(corr_bias) ||
-      !valid_fp4_weight(gate) || !valid_fp4_weight(up) || !valid_fp4_weight(down) ||
-      !aligned16(out))
-    return BEAM_ERR_INVALID_ARG;
-  if (!encoder()) return BEAM_ERR_CUDA;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  record(0, s);
-  int32_t* idx = at<int32_t>(workspace, L.idx);
-  float* w = at<float>(workspace, L.w);
-  bool permuted = false;
-  st = run_route(*cfg, hidden, router_w, corr_bias, T, idx, w, at<float>(workspace, L.logits),
-                 workspace, L, dev, s, &permuted);
-  if (st != BEAM_OK) return st;
-  return run_experts_w4a16(*cfg, hidden, idx, w, *gate, *up, *down, out, T, workspace, L, dev, s,
-                           permuted);
+  return beam_moe_forward_nvfp4_a16_boundary(cfg, hidden, router_w, corr_bias, gate, up, down,
+                                             out, T, nullptr, workspace, ws_bytes, stream);
+}
+
+beam_status_t beam_moe_forward_nvfp4_a16_boundary(const beam_moe_config_t* cfg,
+                                                  const void* hidden, const float* router_w,
+                                                  const float* corr_bias,
+                                                  const beam_fp4_weight_t* gate,
+                                                  const beam_fp4_weight_t* up,
+                                                  const beam_fp4_weight_t* down, void* out,
+                                                  int64_t T, const beam_moe_boundary_t* boundary,
+                                                  void* workspace, size_t ws_bytes, void* stream) {
+  return forward_quantised(
+      cfg, BEAM_WEIGHTS_NVFP4_A16, hidden, router_w, corr_bias, gate, up, down, out, T, boundary,
+      workspace, ws_bytes, stream, valid_fp4_weight,
+      [&](const int32_t* idx, const float* w, const Layout& L, const DevInfo& dev,
+          cudaStream_t s, bool permuted, const beam::BoundaryArgs* ba) {
+        return run_experts_w4a16(*cfg, hidden, idx, w, *gate, *up, *down, out, T, workspace, L,
+                                 dev, s, permuted, ba);
+      });
 }
 
 // ------------------------------------------------------- expert parallelism

@@ -306,6 +306,37 @@ beam_status_t beam_moe_forward_fp8(const beam_moe_config_t *cfg, const void *hid
 beam_status_t beam_moe_fp8_quantize_rows(const void *x, int64_t n, int32_t cols, uint8_t *q,
                                          float *scale, void *stream);
 
+/* The quantised-expert layers followed by the decoder's sublayer boundary,
+ * as beam_moe_forward_boundary is beam_moe_forward followed by it: the
+ * boundary runs in the combine kernel on the layer's FP32 expert rows,
+ * whatever format produced them, with the same arithmetic and the same
+ * argument rules (boundary == NULL is the plain layer call).  The SGLang
+ * post extends the fused norm / scaled-residual boundary to NVFP4 layers
+ * (section "Fusion Optimizations", the kernel-fusion item).  Workspace and
+ * weight rules as for the layer call of the same format. */
+beam_status_t beam_moe_forward_nvfp4_boundary(const beam_moe_config_t *cfg, const void *hidden,
+                                              const float *router_w, const float *corr_bias,
+                                              const beam_fp4_weight_t *gate,
+                                              const beam_fp4_weight_t *up,
+                                              const beam_fp4_weight_t *down, void *out, int64_t T,
+                                              const beam_moe_boundary_t *boundary,
+                                              void *workspace, size_t ws_bytes, void *stream);
+beam_status_t beam_moe_forward_nvfp4_a16_boundary(const beam_moe_config_t *cfg,
+                                                  const void *hidden, const float *router_w,
+                                                  const float *corr_bias,
+                                                  const beam_fp4_weight_t *gate,
+                                                  const beam_fp4_weight_t *up,
+                                                  const beam_fp4_weight_t *down, void *out,
+                                                  int64_t T, const beam_moe_boundary_t *boundary,
+                                                  void *workspace, size_t ws_bytes, void *stream);
+beam_status_t beam_moe_forward_fp8_boundary(const beam_moe_config_t *cfg, const void *hidden,
+                                            const float *router_w, const float *corr_bias,
+                                            const beam_fp8_weight_t *gate,
+                                            const beam_fp8_weight_t *up,
+                                            const beam_fp8_weight_t *down, void *out, int64_t T,
+                                            const beam_moe_boundary_t *boundary, void *workspace,
+                                            size_t ws_bytes, void *stream);
+
 /* ---------------------------------------------------- expert parallelism
  * Expert parallelism over n_ranks ranks ("SGLang 原生支持 Reflection 的 Beam
  * 并驱动其生产 API", section "Fusion Optimizations", the MegaMoE item and the

@@ -106,3 +106,30 @@ def test_fp8_entry_points(lib):
     assert q(None, 4, 128, None, None, None) == INVALID                 # null pointers
     lib.beam_moe_workspace_size.restype = ctypes.c_size_t
     assert lib.beam_moe_workspace_size(_cfg(), ctypes.c_int64(32), 3) > 0
+
+
+def test_quantised_boundary_entry_points(lib):
+    """The boundary description is checked before the zero-token return; a
+    NULL description is the plain layer call."""
+    bad_n = api._Boundary(None, None, None, None, 1e-6, 0)
+    bad_eps = api._Boundary(None, None, None, None, -1.0, 2)
+    good = api._Boundary(None, None, None, None, 1e-6, 2)
+    for name in ("beam_moe_forward_nvfp4_boundary", "beam_moe_forward_nvfp4_a16_boundary",
+                 "beam_moe_forward_fp8_boundary"):
+        fn = getattr(lib, name)
+        fn.restype = ctypes.c_int
+
+        def call(b, T, **kw):
+            return fn(_cfg(**kw), None, None, None, None, None, None, None, ctypes.c_int64(T),
+                      None if b is None else ctypes.byref(b), None, ctypes.c_size_t(0), None)
+
+        assert call(None, 0) == OK, name
+        assert call(good, 0) == OK, name
+        assert call(bad_n, 0) == INVALID, name
+        assert call(bad_eps, 0) == INVALID, name
+        assert call(good, -1) == INVALID, name
+        assert call(good, 4, n_groups=7) == INVALID, name
+        assert call(good, 4) == INVALID, name                  # null pointers
+    fn = lib.beam_moe_forward_nvfp4_boundary
+    assert fn(_cfg(d=5120 + 128), None, None, None, None, None, None, None, ctypes.c_int64(4),
+              ctypes.byref(good), None, ctypes.c_size_t(0), None) == INVALID

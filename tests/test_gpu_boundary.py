@@ -41,17 +41,35 @@ def _steps_apart(a, b):
     return np.abs(ia - ib)
 
 
-def _check(cfg, t, n, seed):
+def _weights(t, fmt):
+    names = ("w_gate", "w_up", "w_down")
+    if fmt == "bf16":
+        return [t[n] for n in names]
+    if fmt == "fp8":
+        return [pkg.Fp8Weight.of(t[n]) for n in names]
+    return [pkg.Fp4Weight.of(t[n]) for n in names]
+
+
+def _plain(cfg, t, fmt, wts):
+    args = (cfg, t["hidden"], t["router_w"], t["corr_bias"], *wts)
+    return {"bf16": pkg.forward, "fp8": pkg.forward_fp8, "nvfp4": pkg.forward_nvfp4,
+            "a16": pkg.forward_nvfp4_a16}[fmt](*args)
+
+
+def _check(cfg, t, n, seed, fmt="bf16"):
+    """The boundary call's m is the plain layer call's, bit for bit (the same
+    expert kernels and combine order, whatever the expert format); h' and the
+    next input are checked from the GPU's m against the oracle."""
     T, d = t["hidden"].shape
     g = torch.Generator(device="cuda").manual_seed(seed)
     h0 = torch.randn(T, d, generator=g, device="cuda").to(torch.bfloat16)
     gp = (1 + 0.1 * torch.randn(d, generator=g, device="cuda")).to(torch.bfloat16)
     gq = (1 + 0.1 * torch.randn(d, generator=g, device="cuda")).to(torch.bfloat16)
     res = h0.clone()
-    out, nx = pkg.forward_boundary(cfg, t["hidden"], t["router_w"], t["corr_bias"], t["w_gate"],
-                                   t["w_up"], t["w_down"], res, gp, gq, EPS, n)
-    ref_out = pkg.forward(cfg, t["hidden"], t["router_w"], t["corr_bias"], t["w_gate"], t["w_up"],
-                          t["w_down"])
+    wts = _weights(t, fmt)
+    out, nx = pkg.forward_boundary(cfg, t["hidden"], t["router_w"], t["corr_bias"], *wts, res, gp,
+                                   gq, EPS, n, a16=fmt == "a16")
+    ref_out = _plain(cfg, t, fmt, wts)
     assert torch.equal(out.view(torch.int16), ref_out.view(torch.int16))   # the same combine
     # new residual from the GPU's m and the old stream
     h_ref, _ = oracle.boundary(_bits(out), _bits(h0), _bits(gp), _bits(gq), EPS, n)
@@ -89,6 +107,29 @@ def test_boundary_beam_decode():
     cfg = inputs.CONFIGS["decode"]
     t = inputs.generate(cfg, "cuda")
     _check(cfg, t, 40, seed=3)
+
+
+@pytest.mark.parametrize("fmt", ["fp8", "nvfp4", "a16"])
+@pytest.mark.parametrize("T,n", [(20, 2), (70, 33)])
+def test_boundary_after_quantised_experts(fmt, T, n):
+    """The NVFP4, W4A16 and FP8 layers end in the same FP32 expert rows and
+    the same combine kernel: T = 20 takes the 16-row token blocks, T = 70
+    the 256-row ones (T * topk > 4 * E)."""
+    d = 256 if fmt in ("nvfp4", "a16") else 128
+    cfg = inputs.MoEConfig(name=f"bnd_{fmt}", T=T, d=d, d_ff=d, seed=40 + T,
+                           weight_fmt="nvfp4" if fmt == "a16" else fmt, n_experts=32, n_groups=4,
+                           topk_groups=2, topk=4, routed_scale=2.5)
+    t = inputs.generate(cfg, "cuda")
+    _check(cfg, t, n, seed=T + n, fmt=fmt)
+
+
+@pytest.mark.parametrize("fmt", ["fp8", "nvfp4"])
+def test_boundary_quantised_beam_shapes(fmt):
+    """Beam expert shapes with the decode batches of the two quantised
+    checkpoint formats."""
+    cfg = inputs.CONFIGS[fmt]
+    t = inputs.generate(cfg, "cuda")
+    _check(cfg, t, 12, seed=5, fmt=fmt)
 
 
 def test_boundary_rejects_bad_arguments():
