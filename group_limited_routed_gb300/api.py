@@ -612,8 +612,7 @@ def ep_experts_fp8(cfg, n_ranks: int, rank: int, x_recv, expert_recv, w_recv, ga
                                          ctypes.byref(down._c),
                                          _dev(y, torch.float32, "y_recv"), M, ws.ptr,
                                          ws.nbytes, _stream(stream)),
-           "beam_moe_ep_experts_fp8", "beam_moe_forward_nvfp4_boundary",
-           "beam_moe_forward_nvfp4_a16_boundary", "beam_moe_forward_fp8_boundary")
+           "beam_moe_ep_experts_fp8")
     return y
 
 

@@ -86,3 +86,30 @@ def test_ep_workspace_query(lib):
     assert size(ctypes.byref(c), 512, 256, 0) == 0    # more ranks than experts
     assert size(ctypes.byref(c), 8, 256, 2) == 0      # no W4A16 expert-parallel path
     assert size(ctypes.byref(c), 8, 256, 3) > 0       # FP8 experts
+
+
+def _calls_of(tree, name):
+    import ast
+    return [n for n in ast.walk(tree) if isinstance(n, ast.Call) and
+            isinstance(n.func, ast.Name) and n.func.id == name]
+
+
+def test_every_binding_checks_the_status_of_the_function_it_calls():
+    """Each `_check(status, name)` in the binding names the library function
+    whose status it checks, and that function is declared and exported (a
+    wrapper only reaches the library on a GPU, so this is its CPU check)."""
+    import ast
+    from group_limited_routed_gb300 import api
+    tree = ast.parse(open(api.__file__).read())
+    declared = set(_declared())
+    checks = _calls_of(tree, "_check")
+    assert len(checks) >= 15
+    for c in checks:
+        assert len(c.args) == 2 and not c.keywords, ast.unparse(c)[:80]
+        call, name = c.args
+        assert isinstance(call, ast.Call), ast.unparse(c)[:80]
+        if isinstance(name, ast.Constant):
+            f = call.func
+            assert isinstance(f, ast.Attribute) and f.attr == name.value, ast.unparse(c)[:80]
+            assert name.value in declared and name.value in api.EXPORTS, name.value
+    assert set(api.EXPORTS) <= declared
