@@ -32,7 +32,6 @@ cudaError_t launch_grouped_gemm(int mode, int nt, const CUtensorMap& a0, const C
         if (nt == 256) return launch_impl<256, kModeDown, true>(a0, a0, b, a, grid, s);
         break;
       case kModeDownPair:
-        if (nt == 16) return launch_impl<16, kModeDownPair, true>(a0, a0, b, a, grid, s);
         if (nt == 256) return launch_impl<256, kModeDownPair, true>(a0, a0, b, a, grid, s);
         break;
     }
@@ -41,7 +40,6 @@ cudaError_t launch_grouped_gemm(int mode, int nt, const CUtensorMap& a0, const C
   switch (mode) {
     case kModeGateUp:
       if (nt == 16) return launch_impl<16, kModeGateUp, false>(a0, a1, b, a, grid, s);
-      if (nt == 128) return launch_impl<128, kModeGateUp, false>(a0, a1, b, a, grid, s);
       if (nt == 256) return launch_impl<256, kModeGateUp, false>(a0, a1, b, a, grid, s);
       break;
     case kModeDown:
@@ -49,7 +47,6 @@ cudaError_t launch_grouped_gemm(int mode, int nt, const CUtensorMap& a0, const C
       if (nt == 256) return launch_impl<256, kModeDown, false>(a0, a0, b, a, grid, s);
       break;
     case kModeDownPair:
-      if (nt == 16) return launch_impl<16, kModeDownPair, false>(a0, a0, b, a, grid, s);
       if (nt == 256) return launch_impl<256, kModeDownPair, false>(a0, a0, b, a, grid, s);
       break;
   }

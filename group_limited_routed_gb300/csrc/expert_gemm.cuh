@@ -40,8 +40,8 @@ struct GemmArgs {
   const float* b_scale;
 };
 
-// Persistent grouped GEMM; `nt` is the token-block width (gate/up 16 | 128,
-// down 16 | 256).  `f8`: both operands are E4M3 (K blocks of 128 elements)
+// Persistent grouped GEMM; `nt` is the token-block width, 16 or 256 (the
+// paired down mode takes 256 only).  `f8`: both operands are E4M3 (K blocks of 128 elements)
 // instead of BF16 (K blocks of 64); the only other difference is the
 // scaling in the epilogue.  Tensor maps are encoded by the caller.
 cudaError_t launch_grouped_gemm(int mode, int nt, const CUtensorMap& a0, const CUtensorMap& a1,
