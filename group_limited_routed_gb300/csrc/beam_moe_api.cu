@@ -22,6 +22,9 @@ using beam::GemmArgs;
 constexpr size_t kAlign = 256;
 constexpr int kMinRows = 256;  // token-operand buffers hold at least one full tile
 constexpr int64_t kTensorRouterMinT = 256;  // from here on the router runs on tensor cores
+// SM count the router's split-K partials are sized for (a workspace is sized
+// without a device); a call on a larger GPU splits no further than that room
+constexpr int kSizingSms = 160;
 constexpr uint64_t kDefaultWaitNs = 2000000000ull;
 
 size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
@@ -174,7 +177,10 @@ Layout make_layout(const beam_moe_config_t& c, int64_t T_max, int32_t fmt = BEAM
   int64_t part_rows = 0;  // max over T <= T_max of ksplit(T) * T
   for (int64_t nb = 1; nb <= (T_max + 31) / 32; ++nb) {
     const int64_t Tn = std::min<int64_t>(T_max, nb * 32);
-    part_rows = std::max<int64_t>(part_rows, router_ksplit(c, Tn) * Tn);
+    const int64_t ks = tensor_router(c, Tn)
+                           ? beam::router_tc_ksplit(Tn, c.n_experts, c.d, kSizingSms)
+                           : router_ksplit(c, Tn);
+    part_rows = std::max<int64_t>(part_rows, ks * Tn);
   }
   Layout L;
   size_t off = 0;
@@ -304,8 +310,12 @@ beam_status_t run_route(const beam_moe_config_t& c, const void* hidden, const fl
     if (!tmap_bf16(&tm_w, planes, c.n_experts, 3LL * c.d, 128) ||
         !tmap_bf16(&tm_x, hidden, T, c.d, 128))
       return BEAM_ERR_CUDA;
-    if (beam::launch_router_tc(tm_w, tm_x, part, T, c.n_experts, c.d, at<uint32_t>(ws, L.status),
-                               g_wait_ns, dev.sms, s) != cudaSuccess)
+    // splits the workspace's partials buffer has room for
+    const int64_t room = static_cast<int64_t>((L.logits - L.part) / (4 * c.n_experts)) / T;
+    ks = static_cast<int>(std::max<int64_t>(
+        1, std::min<int64_t>(beam::router_tc_ksplit(T, c.n_experts, c.d, dev.sms), room)));
+    if (beam::launch_router_tc(tm_w, tm_x, part, T, c.n_experts, c.d, ks,
+                               at<uint32_t>(ws, L.status), g_wait_ns, dev.sms, s) != cudaSuccess)
       return BEAM_ERR_CUDA;
   } else {
     ks = router_ksplit(c, T);

@@ -92,10 +92,14 @@ cudaError_t launch_combine_boundary(const float* y, const int32_t* pair_row, int
 void launch_router_split(const float* w, int32_t E, int32_t d, uint16_t* planes, cudaStream_t s);
 
 // logits [T, E] = x [T, d] (BF16) * planes^T on the tensor cores, K-groups
-// summed in FP32 (E % 128 == 0, d % 128 == 0).
+// summed in FP32 (E % 128 == 0, d % 128 == 0).  With ksplit > 1, split c of
+// the K ranges writes its partial logits to logits + c * T * E (the caller
+// adds the ksplit partials in order).
 cudaError_t launch_router_tc(const CUtensorMap& w_planes, const CUtensorMap& x, float* logits,
-                             int64_t T, int32_t E, int32_t d, uint32_t* status,
+                             int64_t T, int32_t E, int32_t d, int32_t ksplit, uint32_t* status,
                              uint64_t wait_limit_ns, int num_sms, cudaStream_t s);
+// The K split launch_router_tc uses for T tokens on num_sms SMs (>= 1).
+int router_tc_ksplit(int64_t T, int32_t E, int32_t d, int num_sms);
 
 // ---------------------------------------------------------------- NVFP4
 struct Fp4GemmArgs {

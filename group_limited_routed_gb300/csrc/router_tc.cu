@@ -13,13 +13,19 @@
 // K order (deterministic).
 //
 // Tile: 128 experts (MMA M) x up to 128 tokens (MMA N), A = planes [E, 3d]
-// (hi | mid | lo side by side), B = hidden rows [T, d] re-read for each plane.
-// Warp 0: TMA producer; warp 1: TMEM owner and MMA issuer; warps 2-9: two
-// warps per TMEM lane quarter, each draining half of the token columns.
+// (per 64-wide K range: hi | mid | lo side by side), B = hidden rows [T, d].
+// One pipeline stage holds a K range's three weight blocks and its token
+// block, so each token block is loaded once for the three planes.  When the
+// tiles do not fill the GPU, K is split over `ksplit` CTAs per tile: split c
+// writes its partial logits to logits + c * T * E and the selection adds the
+// partials in split order.
+// Warp 0: TMA producer; warp 1: TMEM owner and MMA issuer; warps 2-17: four
+// warps per TMEM lane quarter, each draining a quarter of the token columns.
 // Waits are bounded as in the expert GEMMs.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdint>
 
 #include "common.cuh"
@@ -33,15 +39,15 @@ constexpr int BM = 128;
 constexpr int BN = 128;
 constexpr int BK = 64;
 constexpr int UMMA_K = 16;
-constexpr int KB_PER_GROUP = 3;   // the three planes of one K range
+constexpr int PLANES = 3;         // hi, mid, lo: the three BF16 planes of W_r
 constexpr int kSumGroup = 8;      // K ranges per first-level partial sum
 constexpr int kEpiWarps = 16;
 constexpr int kEpiCols = BN / (kEpiWarps / 4);
 constexpr int kThreads = 32 * (2 + kEpiWarps);
 constexpr uint32_t A_BYTES = BM * BK * 2;
 constexpr uint32_t B_BYTES = BN * BK * 2;
-constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int STAGES = 6;
+constexpr uint32_t STAGE_BYTES = PLANES * A_BYTES + B_BYTES;  // one K range
+constexpr int STAGES = 3;
 constexpr uint32_t ACC_COLS = BN;
 constexpr uint32_t TMEM_COLS = 2 * ACC_COLS;
 constexpr uint32_t NUM_BARS = 2 * STAGES + 4 + 1;
@@ -80,7 +86,7 @@ struct Waiter {
 
 __global__ void __launch_bounds__(kThreads, 1)
     router_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
-                     float* __restrict__ logits, int64_t T, int32_t E, int32_t d,
+                     float* __restrict__ logits, int64_t T, int32_t E, int32_t d, int32_t ksplit,
                      uint32_t* status, uint64_t wait_limit_ns) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = ptx::smem_addr(smem_raw);
@@ -104,8 +110,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int m_blocks = E / BM;
   const int t_blocks = static_cast<int>((T + BN - 1) / BN);
   const int num_tiles = m_blocks * t_blocks;
-  const int k_blocks = 3 * d / BK;       // A blocks: (K range, plane)
-  const int groups = k_blocks / KB_PER_GROUP;  // K ranges
+  const int num_items = num_tiles * ksplit;  // (tile, K split)
+  const int groups = d / BK;                 // K ranges
+  // item -> tile, split and its K ranges [g0, g1); consecutive items share
+  // the split (the same K range of W_r) and differ in the tile
+  auto item_of = [&](int item, int& mb, int& tb, int& kc, int& g0, int& g1) {
+    const int tile = item % num_tiles;
+    kc = item / num_tiles;
+    mb = tile % m_blocks;
+    tb = tile / m_blocks;
+    g0 = kc * groups / ksplit;
+    g1 = (kc + 1) * groups / ksplit;
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -143,18 +159,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-        const int mb = tile % m_blocks, tb = tile / m_blocks;
-        for (int kb = 0; kb < k_blocks; ++kb) {
+      for (int item = blockIdx.x; ok && item < num_items; item += gridDim.x) {
+        int mb, tb, kc, g0, g1;
+        item_of(item, mb, tb, kc, g0, g1);
+        for (int g = g0; g < g1; ++g) {
           if (!W.wait(empty_bar(stage), phase ^ 1u)) {
             ok = false;
             break;
           }
           const uint32_t st = tiles + stage * STAGE_BYTES;
           ptx::mbar_arrive_expect_tx(full_bar(stage), STAGE_BYTES);
-          ptx::tma_load_2d(st, &tm_w, full_bar(stage), kb * BK, mb * BM, pol);
-          ptx::tma_load_2d(st + A_BYTES, &tm_x, full_bar(stage), (kb / KB_PER_GROUP) * BK, tb * BN,
-                           pol);
+#pragma unroll
+          for (int pl = 0; pl < PLANES; ++pl)
+            ptx::tma_load_2d(st + pl * A_BYTES, &tm_w, full_bar(stage), (PLANES * g + pl) * BK,
+                             mb * BM, pol);
+          ptx::tma_load_2d(st + PLANES * A_BYTES, &tm_x, full_bar(stage), g * BK, tb * BN, pol);
           last_parity[stage] = static_cast<int>(phase);
           if (++stage == STAGES) {
             stage = 0;
@@ -174,35 +193,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-        const int tb = tile / m_blocks;
+      for (int item = blockIdx.x; ok && item < num_items; item += gridDim.x) {
+        int mb, tb, kc, g0, g1;
+        item_of(item, mb, tb, kc, g0, g1);
         const int nvalid = static_cast<int>(T - static_cast<int64_t>(tb) * BN < BN ? T - static_cast<int64_t>(tb) * BN : BN);
         const uint32_t idesc = ptx::idesc_bf16_f32(BM, (nvalid + 15) & ~15);
-        for (int g = 0; ok && g < groups; ++g) {
-          if (!W.wait(tempty_bar(acc), acc_phase ^ 1u)) {
+        for (int g = g0; ok && g < g1; ++g) {
+          // each K range into a fresh accumulator: its three planes, four
+          // MMAs each, all reading the stage's one token block
+          if (!W.wait(tempty_bar(acc), acc_phase ^ 1u) || !W.wait(full_bar(stage), phase)) {
             ok = false;
             break;
           }
           ptx::tc_fence_after();
           const uint32_t d0 = tmem_base + acc * ACC_COLS;
-          for (int j = 0; j < KB_PER_GROUP; ++j) {
-            if (!W.wait(full_bar(stage), phase)) {
-              ok = false;
-              break;
-            }
-            ptx::tc_fence_after();
-            const uint32_t st = tiles + stage * STAGE_BYTES;
+          const uint32_t st = tiles + stage * STAGE_BYTES;
+#pragma unroll
+          for (int pl = 0; pl < PLANES; ++pl)
 #pragma unroll
             for (int kk = 0; kk < BK / UMMA_K; ++kk)
-              ptx::mma_bf16(d0, ptx::sdesc_sw128(st + kk * 32),
-                            ptx::sdesc_sw128(st + A_BYTES + kk * 32), idesc, (j | kk) ? 1u : 0u);
-            ptx::mma_commit(empty_bar(stage));
-            if (++stage == STAGES) {
-              stage = 0;
-              phase ^= 1u;
-            }
+              ptx::mma_bf16(d0, ptx::sdesc_sw128(st + pl * A_BYTES + kk * 32),
+                            ptx::sdesc_sw128(st + PLANES * A_BYTES + kk * 32), idesc,
+                            (pl | kk) ? 1u : 0u);
+          ptx::mma_commit(empty_bar(stage));
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
           }
-          if (!ok) break;
           ptx::mma_commit(tfull_bar(acc));
           acc ^= 1;
           if (acc == 0) acc_phase ^= 1u;
@@ -220,14 +237,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-      const int mb = tile % m_blocks, tb = tile / m_blocks;
+    for (int item = blockIdx.x; ok && item < num_items; item += gridDim.x) {
+      int mb, tb, kc, g0, g1;
+      item_of(item, mb, tb, kc, g0, g1);
       const int nvalid = static_cast<int>(
           T - static_cast<int64_t>(tb) * BN < BN ? T - static_cast<int64_t>(tb) * BN : BN);
       float sum[kEpiCols], grp[kEpiCols];
 #pragma unroll
       for (int i = 0; i < kEpiCols; ++i) sum[i] = grp[i] = 0.f;
-      for (int g = 0; g < groups; ++g) {
+      for (int g = 0; g < g1 - g0; ++g) {
         if (!W.wait(tfull_bar(acc), acc_phase)) {
           ok = false;
           break;
@@ -247,7 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mbar_arrive(tempty_bar(acc));
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1u;
-        if ((g + 1) % kSumGroup == 0 || g + 1 == groups) {
+        if ((g + 1) % kSumGroup == 0 || g + 1 == g1 - g0) {
 #pragma unroll
           for (int i = 0; i < kEpiCols; ++i) {
             sum[i] += grp[i];
@@ -257,10 +275,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
       const int e = mb * BM + e_row;
+      float* out = logits + static_cast<int64_t>(kc) * T * E;
 #pragma unroll
       for (int i = 0; i < kEpiCols; ++i) {
         const int col = part * kEpiCols + i;
-        if (col < nvalid) logits[(static_cast<int64_t>(tb) * BN + col) * E + e] = sum[i];
+        if (col < nvalid) out[(static_cast<int64_t>(tb) * BN + col) * E + e] = sum[i];
       }
     }
   }
@@ -275,16 +294,26 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-cudaError_t launch_router_tc(const CUtensorMap& w_planes, const CUtensorMap& x, float* logits,
-                             int64_t T, int32_t E, int32_t d, uint32_t* status,
-                             uint64_t wait_limit_ns, int num_sms, cudaStream_t s) {
+int router_tc_ksplit(int64_t T, int32_t E, int32_t d, int num_sms) {
   const int64_t tiles = static_cast<int64_t>(E / BM) * ((T + BN - 1) / BN);
-  const int grid = static_cast<int>(tiles < num_sms ? tiles : num_sms);
+  if (tiles <= 0) return 1;
+  // as many splits as whole waves of (tile, split) items fill the SMs, at
+  // most one per 8 K ranges and 16 in all
+  int64_t ks = num_sms / tiles;
+  const int64_t cap = std::min<int64_t>(16, std::max<int64_t>(1, (d / BK) / kSumGroup));
+  return static_cast<int>(std::max<int64_t>(1, std::min(ks, cap)));
+}
+
+cudaError_t launch_router_tc(const CUtensorMap& w_planes, const CUtensorMap& x, float* logits,
+                             int64_t T, int32_t E, int32_t d, int32_t ksplit, uint32_t* status,
+                             uint64_t wait_limit_ns, int num_sms, cudaStream_t s) {
+  const int64_t items = static_cast<int64_t>(E / BM) * ((T + BN - 1) / BN) * ksplit;
+  const int grid = static_cast<int>(items < num_sms ? items : num_sms);
   if (grid <= 0) return cudaSuccess;
   const cudaError_t err = smem_limit_once<router_tc_kernel>(SMEM_BYTES);
   if (err != cudaSuccess) return err;
-  router_tc_kernel<<<grid, kThreads, SMEM_BYTES, s>>>(w_planes, x, logits, T, E, d, status,
-                                                      wait_limit_ns);
+  router_tc_kernel<<<grid, kThreads, SMEM_BYTES, s>>>(w_planes, x, logits, T, E, d, ksplit,
+                                                      status, wait_limit_ns);
   return cudaGetLastError();
 }
 
