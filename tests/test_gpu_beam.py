@@ -80,3 +80,17 @@ def test_beam_largest_batch():
         del t
         gc.collect()
         torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("T", [256, 640, 1500, 2051])
+def test_router_k_splits_at_beam_shapes(T):
+    """Batches whose router tiles leave SMs idle split K over CTAs (256 tokens:
+    4 tiles, 10 splits of 8 K ranges; 2051: 34 tiles, 4 splits, a ragged last
+    tile) and the selection adds the partials: logits and routing still meet
+    the FP32 bounds on every token."""
+    cfg = inputs.CONFIGS["prefill"].replace(T=T, seed=300 + T)
+    t = inputs.generate(cfg, "cuda", weights=False)
+    lg, r = oracle_route(cfg, t)
+    idx, w, logits = pkg.route(cfg, t["hidden"], t["router_w"], t["corr_bias"], want_logits=True)
+    check_logits(host(logits), lg)
+    check_routing(cfg, host(idx), host(w), r)
