@@ -265,6 +265,117 @@ __device__ __forceinline__ void select_token(const SelectArgs& a, int64_t t) {
   }
 }
 
+// ------------------------------------------------- selection, warp per token
+// The same rule as select_token with one warp per token, for batches large
+// enough that a block per token would run many waves of short blocks.  Lane
+// l holds experts l, l + 32, ... (E % 32 == 0, so every lane is live).
+//  1.-2. logits, scores and group scores exactly as in select_token (the
+//     same FP32 operations in the same order; groups are aligned segments of
+//     S lanes inside one row of 32 experts).
+//  3. group g is kept when fewer than kg groups precede it (score desc,
+//     group asc), ranked from the warp's copy of the group scores.
+//  4. slot r takes the r-th expert of the kept groups in the order (c desc,
+//     expert asc): k rounds of a warp argmax, the same slots as the ranking.
+//  5. weights as in select_token: FP64 sum of the k scores in slot order.
+constexpr int kSelWarps = 8;  // tokens per 256-thread block
+
+__global__ void __launch_bounds__(32 * kSelWarps) select_warp_kernel(SelectArgs a) {
+  __shared__ float s_gs[kSelWarps][kSelMaxG];
+  __shared__ int s_keep[kSelWarps][kSelMaxG];
+  __shared__ int s_slot_e[kSelWarps][32];
+  __shared__ float s_slot_s[kSelWarps][32];
+  const int wi = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * kSelWarps + wi;
+  if (t >= a.T) return;  // whole warps leave together
+  const int E = a.E;
+  const int J = E / 32;
+  const int S = E / a.G;
+  float sc[8], c[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    sc[j] = 0.f;
+    c[j] = -FLT_MAX;
+    if (j < J) {
+      const int e = 32 * j + lane;
+      const float* src = a.part + t * E + e;
+      const int64_t stride = a.T * E;
+      float lg = src[0];
+      for (int sp = 1; sp < a.ksplit; ++sp) lg += src[sp * stride];
+      if (a.logits) a.logits[t * E + e] = lg;
+      sc[j] = 1.0f / (1.0f + expf(-lg));
+      c[j] = sc[j] + a.bias[e];
+      // top-1 + top-2 of the S-lane segment (a group)
+      float m1 = c[j], m2 = -FLT_MAX;
+      for (int o = S >> 1; o >= 1; o >>= 1) {
+        const float b1 = __shfl_xor_sync(kFull, m1, o);
+        const float b2 = __shfl_xor_sync(kFull, m2, o);
+        const float n1 = fmaxf(m1, b1);
+        const float n2 = fmaxf(fminf(m1, b1), fmaxf(m2, b2));
+        m1 = n1;
+        m2 = n2;
+      }
+      if ((lane & (S - 1)) == 0) s_gs[wi][e / S] = m1 + m2;
+    }
+  }
+  __syncwarp();
+  for (int g = lane; g < a.G; g += 32) {
+    const float v = s_gs[wi][g];
+    int before = 0;
+    for (int h = 0; h < a.G; ++h) {
+      const float u = s_gs[wi][h];
+      before += (u > v || (u == v && h < g)) ? 1 : 0;
+    }
+    s_keep[wi][g] = before < a.kg ? 1 : 0;
+  }
+  __syncwarp();
+  // experts outside the kept groups never win a round
+  unsigned live = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+    if (j < J && s_keep[wi][(32 * j + lane) / S]) live |= 1u << j;
+  for (int r = 0; r < a.k; ++r) {
+    float bv = -FLT_MAX;
+    int be = 0x7fffffff;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int e = 32 * j + lane;
+      if (((live >> j) & 1u) && (be == 0x7fffffff || c[j] > bv)) {
+        bv = c[j];
+        be = e;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+      const float ov = __shfl_xor_sync(kFull, bv, o);
+      const int oe = __shfl_xor_sync(kFull, be, o);
+      if (oe != 0x7fffffff && (be == 0x7fffffff || ov > bv || (ov == bv && oe < be))) {
+        bv = ov;
+        be = oe;
+      }
+    }
+    // be is the same on every lane: its owner records it and drops it
+    if ((be & 31) == lane) {
+      const int jw = be >> 5;
+      float sw = 0.f;
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (j == jw) sw = sc[j];
+      live &= ~(1u << jw);
+      s_slot_e[wi][r] = be;
+      s_slot_s[wi][r] = sw;
+    }
+  }
+  __syncwarp();
+  if (lane < a.k) {
+    double ssum = 0.0;
+    for (int r = 0; r < a.k; ++r) ssum += static_cast<double>(s_slot_s[wi][r]);
+    a.idx[t * a.k + lane] = s_slot_e[wi][lane];
+    a.w[t * a.k + lane] = static_cast<float>(static_cast<double>(a.alpha) *
+                                             static_cast<double>(s_slot_s[wi][lane]) / ssum);
+  }
+}
+
 // ------------------------------------------------------------ router split
 // planes[e] = for each 64-wide K range r: [hi | mid | lo] of that range, with
 // hi = bf16(w), mid = bf16(w - hi), lo = bf16(w - hi - mid): each product with
@@ -785,7 +896,14 @@ void launch_router(const RouterArgs& a, int ksplit, cudaStream_t s) {
 }
 
 void launch_select(const SelectArgs& a, cudaStream_t s) {
-  select_kernel<<<static_cast<unsigned>(a.T), 256, 0, s>>>(a);
+  // a block per token for small batches (more threads per token, one wave),
+  // a warp per token from 256 tokens on
+  if (a.T < 256) {
+    select_kernel<<<static_cast<unsigned>(a.T), 256, 0, s>>>(a);
+    return;
+  }
+  const int64_t blocks = (a.T + kSelWarps - 1) / kSelWarps;
+  select_warp_kernel<<<static_cast<unsigned>(blocks), 32 * kSelWarps, 0, s>>>(a);
 }
 
 void launch_router_split(const float* w, int32_t E, int32_t d, uint16_t* planes, cudaStream_t s) {
