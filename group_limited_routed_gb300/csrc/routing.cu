@@ -381,22 +381,34 @@ __global__ void __launch_bounds__(32 * kSelWarps) select_warp_kernel(SelectArgs 
 // hi = bf16(w), mid = bf16(w - hi), lo = bf16(w - hi - mid): each product with
 // a BF16 x is exact in FP32, and hi + mid + lo equals w to within 2^-24
 // relative.
+// Four consecutive weights per thread (d % 64 == 0, so they share a 64-wide
+// range): one 16-byte load, three 8-byte stores.
 __global__ void __launch_bounds__(256) router_split_kernel(const float* __restrict__ w, int32_t E,
                                                            int32_t d, uint16_t* __restrict__ planes) {
-  const int64_t n = static_cast<int64_t>(E) * d;
-  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+  const int64_t n4 = static_cast<int64_t>(E) * d / 4;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n4;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int64_t e = i / d, j = i % d;
-    const float v = w[i];
-    const __nv_bfloat16 hi = __float2bfloat16_rn(v);
-    const float r1 = v - __bfloat162float(hi);
-    const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
-    const float r2 = r1 - __bfloat162float(mid);
-    const __nv_bfloat16 lo = __float2bfloat16_rn(r2);
+    const int64_t e = (4 * i) / d, j = (4 * i) % d;
+    const float4 v4 = reinterpret_cast<const float4*>(w)[i];
+    const float v[4] = {v4.x, v4.y, v4.z, v4.w};
+    uint16_t p[3][4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const __nv_bfloat16 hi = __float2bfloat16_rn(v[q]);
+      const float r1 = v[q] - __bfloat162float(hi);
+      const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+      const float r2 = r1 - __bfloat162float(mid);
+      const __nv_bfloat16 lo = __float2bfloat16_rn(r2);
+      p[0][q] = *reinterpret_cast<const uint16_t*>(&hi);
+      p[1][q] = *reinterpret_cast<const uint16_t*>(&mid);
+      p[2][q] = *reinterpret_cast<const uint16_t*>(&lo);
+    }
     uint16_t* blk = planes + e * 3 * d + (j / 64) * 192 + (j % 64);
-    blk[0] = *reinterpret_cast<const uint16_t*>(&hi);
-    blk[64] = *reinterpret_cast<const uint16_t*>(&mid);
-    blk[128] = *reinterpret_cast<const uint16_t*>(&lo);
+#pragma unroll
+    for (int pl = 0; pl < 3; ++pl)
+      *reinterpret_cast<uint2*>(blk + 64 * pl) =
+          make_uint2(p[pl][0] | (static_cast<uint32_t>(p[pl][1]) << 16),
+                     p[pl][2] | (static_cast<uint32_t>(p[pl][3]) << 16));
   }
 }
 
@@ -907,7 +919,7 @@ void launch_select(const SelectArgs& a, cudaStream_t s) {
 }
 
 void launch_router_split(const float* w, int32_t E, int32_t d, uint16_t* planes, cudaStream_t s) {
-  router_split_kernel<<<512, 256, 0, s>>>(w, E, d, planes);
+  router_split_kernel<<<2 * 152, 256, 0, s>>>(w, E, d, planes);
 }
 
 cudaError_t launch_fused_route(const RouterArgs& ra, int ksplit, const SelectArgs& sa,
