@@ -491,8 +491,8 @@ beam_status_t run_experts_nvfp4(const beam_moe_config_t& c, const void* hidden, 
   uint8_t* hq = at<uint8_t>(ws, L.h_fp4);
   uint8_t* hsf = at<uint8_t>(ws, L.h_sf);
   float* y = at<float>(ws, L.y);
-  beam::launch_quantize_rows(static_cast<const uint16_t*>(hidden), pa.perm_src,
-                             pa.offsets + c.n_experts, TK, c.topk, c.d, xq, xsf, s);
+  beam::launch_quantize_tokens(static_cast<const uint16_t*>(hidden), pa.pair_row, T, c.topk, c.d,
+                               xq, xsf, s);
   record(4, s);
   if (cudaGetLastError() != cudaSuccess) return BEAM_ERR_CUDA;
 

@@ -159,11 +159,11 @@ void launch_pack_scales(const uint8_t* src, int64_t rows, int64_t S, uint8_t* ds
 // row (amax / 448); rows at or past *n_valid, when given, are skipped
 void launch_quantize_e4m3_rows(const uint16_t* x, const int32_t* n_valid, int64_t rows,
                                int32_t cols, uint8_t* q, float* scale, cudaStream_t s);
-// permuted token rows -> NVFP4 codes [rows, d/2] and scales [rows, d/4]
-// (one 16-byte slot, 4 scales + padding, per 64 elements)
-void launch_quantize_rows(const uint16_t* x, const int32_t* perm_src, const int32_t* n_valid,
-                          int64_t TK, int32_t k, int32_t d, uint8_t* xq, uint8_t* xsf,
-                          cudaStream_t s);
+// token rows x [T, d] -> NVFP4 codes [rows, d/2] and scales [rows, d/4] (one
+// 16-byte slot, 4 scales + padding, per 64 elements) of each token's k
+// permuted rows pair_row[t * k + j]; each token is quantised once (k <= 32)
+void launch_quantize_tokens(const uint16_t* x, const int32_t* pair_row, int64_t T, int32_t k,
+                            int32_t d, uint8_t* xq, uint8_t* xsf, cudaStream_t s);
 // block-scaled FP4 grouped GEMM, nt = 16 | 32; sfb maps the token scales; the
 // down GEMM works on pairs of adjacent 128-row weight blocks (m_blocks = d / 256)
 cudaError_t launch_fp4_gemm(bool gateup, int nt, const CUtensorMap& a0, const CUtensorMap& a1,

@@ -87,18 +87,19 @@ __global__ void __launch_bounds__(256) pack_scales_kernel(const uint8_t* __restr
 }
 
 // ------------------------------------------------------ quantise token rows
-// Permuted row r: the hidden row of its token, quantised per 16 along d.
-// xq [rows, d/2] packed E2M1 (low nibble = even element); xsf [rows, d/4]:
-// per 64 elements a 16-byte slot holding their 4 scales (then padding).
-__global__ void __launch_bounds__(128) quantize_rows_kernel(const uint16_t* __restrict__ x,
-                                                            const int32_t* __restrict__ perm_src,
-                                                            const int32_t* __restrict__ n_valid,
-                                                            int32_t k, int32_t d,
-                                                            uint8_t* __restrict__ xq,
-                                                            uint8_t* __restrict__ xsf) {
-  const int64_t row = blockIdx.x;
-  if (row >= *n_valid) return;
-  const int64_t t = perm_src[row] / k;
+// Token t's hidden row, quantised per 16 along d once and written to each of
+// its k permuted rows (pair_row[t * k + j]).  xq [rows, d/2] packed E2M1 (low
+// nibble = even element); xsf [rows, d/4]: per 64 elements a 16-byte slot
+// holding their 4 scales (then padding).
+__global__ void __launch_bounds__(128) quantize_tokens_kernel(const uint16_t* __restrict__ x,
+                                                              const int32_t* __restrict__ pair_row,
+                                                              int32_t k, int32_t d,
+                                                              uint8_t* __restrict__ xq,
+                                                              uint8_t* __restrict__ xsf) {
+  const int64_t t = blockIdx.x;
+  __shared__ int64_t s_row[32];
+  if (threadIdx.x < k) s_row[threadIdx.x] = pair_row[t * k + threadIdx.x];
+  __syncthreads();
   const uint4* src = reinterpret_cast<const uint4*>(x + t * d);
   for (int blk = threadIdx.x; blk < d / 16; blk += blockDim.x) {
     const uint4 a = src[2 * blk], b = src[2 * blk + 1];
@@ -122,8 +123,11 @@ __global__ void __launch_bounds__(128) quantize_rows_kernel(const uint16_t* __re
       else
         hi |= c << (4 * (i - 8));
     }
-    *reinterpret_cast<uint2*>(xq + row * (d / 2) + blk * 8) = make_uint2(lo, hi);
-    xsf[row * (d / 4) + (blk / 4) * 16 + (blk % 4)] = sfc;
+    for (int j = 0; j < k; ++j) {
+      const int64_t row = s_row[j];
+      *reinterpret_cast<uint2*>(xq + row * (d / 2) + blk * 8) = make_uint2(lo, hi);
+      xsf[row * (d / 4) + (blk / 4) * 16 + (blk % 4)] = sfc;
+    }
   }
 }
 
@@ -470,11 +474,10 @@ void launch_pack_scales(const uint8_t* src, int64_t rows, int64_t S, uint8_t* ds
   pack_scales_kernel<<<grid > 0 ? grid : 1, 256, 0, s>>>(src, rows, S, dst);
 }
 
-void launch_quantize_rows(const uint16_t* x, const int32_t* perm_src, const int32_t* n_valid,
-                          int64_t TK, int32_t k, int32_t d, uint8_t* xq, uint8_t* xsf,
-                          cudaStream_t s) {
-  quantize_rows_kernel<<<static_cast<unsigned>(TK), 128, 0, s>>>(x, perm_src, n_valid, k, d, xq,
-                                                                  xsf);
+void launch_quantize_tokens(const uint16_t* x, const int32_t* pair_row, int64_t T, int32_t k,
+                            int32_t d, uint8_t* xq, uint8_t* xsf, cudaStream_t s) {
+  if (T <= 0) return;
+  quantize_tokens_kernel<<<static_cast<unsigned>(T), 128, 0, s>>>(x, pair_row, k, d, xq, xsf);
 }
 
 cudaError_t launch_fp4_gemm(bool gateup, int nt, const CUtensorMap& a0, const CUtensorMap& a1,
