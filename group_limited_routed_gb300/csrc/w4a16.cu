@@ -57,6 +57,13 @@ constexpr int kEpiWarp0 = 2 + kConvWarps;             // first of the 4 epilogue
 // pipe idle (four issuers: gate/up 1051 -> 748 us, down 760 -> 559 us on
 // the 128-token NVFP4 batch; eight gave no more).
 constexpr int kIssuers = 4;
+// gate/up: the two converter warps of a lane quarter take alternate 64-wide
+// slices whole (a warp's TMEM stores wait behind the queued MMAs, and the
+// other warp converts meanwhile: gate/up 747 -> 709 us on the 128-token
+// batch); down: both convert half of every slice (one projection per slice
+// leaves too little work to overlap: 557 -> 574 us when split by slices).
+template <bool GATEUP>
+constexpr bool kConvSplitSlices = GATEUP;
 constexpr int kIssuer1 = kEpiWarp0 + 4;  // warps of issuers 1..kIssuers-1
 constexpr int kThreads = 32 * (kIssuer1 + kIssuers - 1);
 constexpr uint32_t kTileBudget = 216 * 1024;
@@ -96,6 +103,8 @@ struct Cfg {
   static_assert(TMEM_COLS <= 512, "TMEM columns");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
   static_assert(STAGES >= 2, "two stages at least");
+  static_assert(!kConvSplitSlices<GATEUP> || RA % 2 == 0,
+                "slices alternate between two converter warps: an even ring");
 };
 
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
@@ -224,7 +233,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(empty_bar(s), NI + kConvWarps);  // the MMA commits and the converters
     }
     for (int a = 0; a < C::RA; ++a) {
-      ptx::mbar_init(afull_bar(a), kConvWarps);
+      ptx::mbar_init(afull_bar(a), kConvSplitSlices<GATEUP> ? kConvWarps / 2 : kConvWarps);
       ptx::mbar_init(aempty_bar(a), NI);
     }
     for (int a = 0; a < 2; ++a) {
@@ -395,11 +404,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     // swizzled row) and 2 scales (blocked order) -> 16 F16 pairs -> 16 TMEM
     // columns.
     const int q = warp & 3;
-    const int half = (warp - 2) >> 2;
+    const int grp = (warp - 2) >> 2;  // which of the two converter warps of lane quarter q
     const int m = q * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
-    int stage = 0, ra = 0;
-    uint32_t phase = 0, ra_phase = 0;
+    int stage = 0;
+    uint32_t phase = 0;
+    // global index of this warp's next slice: gate/up alternates the slices
+    // between the two warps of a lane quarter (each converts whole slices),
+    // down has both convert a half of every slice
+    uint32_t gs = kConvSplitSlices<GATEUP> ? static_cast<uint32_t>(grp) : 0u;
+    constexpr int JSTEP = kConvSplitSlices<GATEUP> ? 2 : 1;
     bool ok = true;
     for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
       const TileInfo ti = decode_tile<NT>(tile, s_start, s_cnt, s_off, E);
@@ -410,8 +424,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         const uint8_t* st = smem + stage * C::STAGE_BYTES;
-        for (int j = 0; j < 4; ++j) {
-          if (!W.wait(aempty_bar(ra), ra_phase ^ 1u)) {
+        for (int j = kConvSplitSlices<GATEUP> ? grp : 0; j < 4; j += JSTEP) {
+          const int slot = static_cast<int>(gs % C::RA);
+          const uint32_t sph = (gs / C::RA) & 1u;
+          if (!W.wait(aempty_bar(slot), sph ^ 1u)) {
             ok = false;
             break;
           }
@@ -419,28 +435,31 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int a = 0; a < C::NUM_A; ++a) {
             const uint8_t* row = st + a * C::A_BYTES + m * KS_BYTES;
-            const uint4 c = *reinterpret_cast<const uint4*>(row + (((2 * j + half) ^ (m & 7)) << 4));
-            const uint16_t sf = *reinterpret_cast<const uint16_t*>(
-                st + C::OFF_SFA + a * C::SFA_BYTES + j * 512 + (m & 31) * 16 + (m >> 5) * 4 +
-                2 * half);
-            const uint32_t s0 = scale_pair(static_cast<uint8_t>(sf));
-            const uint32_t s1 = scale_pair(static_cast<uint8_t>(sf >> 8));
-            uint32_t v[16];
-            dequant8(c.x, s0, v);
-            dequant8(c.y, s0, v + 4);
-            dequant8(c.z, s1, v + 8);
-            dequant8(c.w, s1, v + 12);
-            tmem_st16(tmem_base + lane_off + C::A_BASE + ra * C::A_COLS + a * (KSUB / 2) + 16 * half,
-                      v);
+            // the slice's four scales of row m (blocked order)
+            const uint32_t sf4 = *reinterpret_cast<const uint32_t*>(
+                st + C::OFF_SFA + a * C::SFA_BYTES + j * 512 + (m & 31) * 16 + (m >> 5) * 4);
+#pragma unroll
+            for (int hh = 0; hh < (kConvSplitSlices<GATEUP> ? 2 : 1); ++hh) {
+              const int half = kConvSplitSlices<GATEUP> ? hh : grp;
+              const uint4 c =
+                  *reinterpret_cast<const uint4*>(row + (((2 * j + half) ^ (m & 7)) << 4));
+              const uint32_t s0 = scale_pair(static_cast<uint8_t>(sf4 >> (16 * half)));
+              const uint32_t s1 = scale_pair(static_cast<uint8_t>(sf4 >> (16 * half + 8)));
+              uint32_t v[16];
+              dequant8(c.x, s0, v);
+              dequant8(c.y, s0, v + 4);
+              dequant8(c.z, s1, v + 8);
+              dequant8(c.w, s1, v + 12);
+              tmem_st16(tmem_base + lane_off + C::A_BASE + slot * C::A_COLS + a * (KSUB / 2) +
+                            16 * half,
+                        v);
+            }
           }
           tmem_wait_st();
           ptx::tc_fence_before();
           __syncwarp();
-          if (lane == 0) ptx::mbar_arrive(afull_bar(ra));
-          if (++ra == C::RA) {
-            ra = 0;
-            ra_phase ^= 1u;
-          }
+          if (lane == 0) ptx::mbar_arrive(afull_bar(slot));
+          gs += JSTEP;
         }
         if (!ok) break;
         // this stage's codes and scales have been read
