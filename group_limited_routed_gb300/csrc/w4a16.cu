@@ -11,9 +11,10 @@
 //     (exact inside F16's normal range, saturating at 65504), and the SwiGLU
 //     product h is rounded to F16 for the down GEMM.
 // The weight tiles stay packed in shared memory (0.5 byte per weight); eight
-// converter warps (two per TMEM lane quarter, one half of the K slice each)
-// expand each row's 64-wide K slice to F16 pairs in registers and store it
-// into tensor memory, where the MMA reads its A operand.  So shared memory
+// converter warps (two per TMEM lane quarter: for gate/up each takes
+// alternate 64-wide K slices whole, for down each half of every slice)
+// expand each row's K slice to F16 pairs in registers and store it into
+// tensor memory, where the MMA reads its A operand.  So shared memory
 // carries only the packed codes and the token tiles.
 //
 // At decode-sized batches this path issues many tiny MMAs: an F16 MMA covers
