@@ -396,8 +396,8 @@ beam_status_t run_experts(const beam_moe_config_t& c, const void* hidden, const 
   const bool row_gather = small_batch(c, TK);
   uint16_t* xp = at<uint16_t>(ws, L.x_perm);
   if (!row_gather)
-    beam::launch_gather(static_cast<const uint16_t*>(hidden), pa.perm_src,
-                        pa.offsets + c.n_experts, TK, c.topk, c.d, xp, s);
+    beam::launch_scatter_tokens(static_cast<const uint16_t*>(hidden), pa.pair_row, T, c.topk, c.d,
+                                xp, s);
   record(4, s);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return BEAM_ERR_CUDA;
@@ -575,8 +575,8 @@ beam_status_t run_experts_fp8(const beam_moe_config_t& c, const void* hidden, co
     record(3, s);
   }
   // the token rows are quantised once per token; decode-sized batches gather
-  // them inside the gate/up GEMM, larger ones into expert order first (byte
-  // rows, copied as d/2 16-bit words)
+  // them inside the gate/up GEMM, larger ones are scattered into expert order
+  // first (byte rows, copied as d/2 16-bit words)
   uint8_t* xq = at<uint8_t>(ws, L.x_fp8);
   float* xs = at<float>(ws, L.x_scale);
   beam::launch_quantize_e4m3_rows(static_cast<const uint16_t*>(hidden), nullptr, T, c.d, xq, xs,
@@ -584,9 +584,8 @@ beam_status_t run_experts_fp8(const beam_moe_config_t& c, const void* hidden, co
   const bool row_gather = small_batch(c, TK);
   uint8_t* xp = at<uint8_t>(ws, L.x_perm);
   if (!row_gather)
-    beam::launch_gather(reinterpret_cast<const uint16_t*>(xq), pa.perm_src,
-                        pa.offsets + c.n_experts, TK, c.topk, c.d / 2,
-                        reinterpret_cast<uint16_t*>(xp), s);
+    beam::launch_scatter_tokens(reinterpret_cast<const uint16_t*>(xq), pa.pair_row, T, c.topk,
+                                c.d / 2, reinterpret_cast<uint16_t*>(xp), s);
   record(4, s);
   if (cudaGetLastError() != cudaSuccess) return BEAM_ERR_CUDA;
 

@@ -68,6 +68,10 @@ cudaError_t launch_fused_route(const RouterArgs& ra, int ksplit, const SelectArg
                                const PermuteArgs& pa, int num_sms, cudaStream_t s);
 void launch_gather(const uint16_t* x, const int32_t* perm_src, const int32_t* n_valid, int64_t TK,
                    int32_t k, int32_t d, uint16_t* x_perm, cudaStream_t s);
+// token rows x [T, n16 16-bit words] -> each token's k permuted rows
+// pair_row[t * k + j] of x_perm (each row read once; k <= 32)
+void launch_scatter_tokens(const uint16_t* x, const int32_t* pair_row, int64_t T, int32_t k,
+                           int32_t n16, uint16_t* x_perm, cudaStream_t s);
 void launch_combine(const float* y, const int32_t* pair_row, int64_t T, int32_t k, int32_t d,
                     uint16_t* out, cudaStream_t s);
 

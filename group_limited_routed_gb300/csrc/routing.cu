@@ -667,6 +667,34 @@ __global__ void __launch_bounds__(256) permute_sort_kernel(PermuteArgs a, int32_
 }
 
 // ------------------------------------------------------------------ gather
+// Block t: token t's row of x, read once, written to each of its k permuted
+// rows pair_row[t * k + j] (x_perm in expert order for the larger token
+// blocks).  n16 16-bit words per row, a multiple of 8.
+__global__ void __launch_bounds__(128) scatter_tokens_kernel(const uint16_t* __restrict__ x,
+                                                             const int32_t* __restrict__ pair_row,
+                                                             int32_t k, int32_t n16,
+                                                             uint16_t* __restrict__ xp) {
+  const int64_t t = blockIdx.x;
+  __shared__ int64_t s_row[32];
+  if (threadIdx.x < k) s_row[threadIdx.x] = pair_row[t * k + threadIdx.x];
+  __syncthreads();
+  const uint4* src = reinterpret_cast<const uint4*>(x + t * n16);
+  constexpr int U = 8;
+  const int n8 = n16 / 8;
+  for (int base = threadIdx.x; base < n8; base += U * blockDim.x) {
+    uint4 r[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (base + u * blockDim.x < n8) r[u] = src[base + u * blockDim.x];
+    for (int j = 0; j < k; ++j) {
+      uint4* dst = reinterpret_cast<uint4*>(xp + s_row[j] * n16);
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+        if (base + u * blockDim.x < n8) dst[base + u * blockDim.x] = r[u];
+    }
+  }
+}
+
 // x_perm[row] = x[token of row] for the larger token blocks; rows past the
 // last valid one are skipped.
 __global__ void __launch_bounds__(128) gather_kernel(const uint16_t* __restrict__ x,
@@ -980,6 +1008,12 @@ void launch_permute(const PermuteArgs& a, cudaStream_t s) {
 void launch_gather(const uint16_t* x, const int32_t* perm_src, const int32_t* n_valid, int64_t TK,
                    int32_t k, int32_t d, uint16_t* x_perm, cudaStream_t s) {
   gather_kernel<<<static_cast<unsigned>(TK), 128, 0, s>>>(x, perm_src, n_valid, k, d, x_perm);
+}
+
+void launch_scatter_tokens(const uint16_t* x, const int32_t* pair_row, int64_t T, int32_t k,
+                           int32_t n16, uint16_t* x_perm, cudaStream_t s) {
+  if (T <= 0) return;
+  scatter_tokens_kernel<<<static_cast<unsigned>(T), 128, 0, s>>>(x, pair_row, k, n16, x_perm);
 }
 
 void launch_combine(const float* y, const int32_t* pair_row, int64_t T, int32_t k, int32_t d,
