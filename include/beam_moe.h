@@ -432,9 +432,10 @@ beam_status_t beam_moe_check_status(void *workspace, void *stream);
 /* Profiling aid: when n >= 8 events (cudaEvent_t) are given, every later
  * beam_moe_forward / beam_moe_forward_routed records them on its stream at
  * the step boundaries: [0] start, [1] router, [2] selection, [3] permute,
- * [4] gather (only when T*topk > 4*E; smaller batches gather inside the
- * gate/up GEMM), [5] gate/up GEMM, [6] down GEMM, [7] combine (each after its
- * step).  Steps a call does not run record at the same point as the previous
+ * [4] token rows (BF16: their scatter into expert order when T*topk > 4*E,
+ * smaller batches gather inside the gate/up GEMM; NVFP4 and FP8: their
+ * quantisation, then for FP8 the scatter), [5] gate/up GEMM, [6] down GEMM,
+ * [7] combine (each after its step).  Steps a call does not run record at the same point as the previous
  * one.  Below 256 tokens (at most 256 experts) the router, the selection and
  * the permutation are one cooperative launch: [1], [2] and [3] are all
  * recorded after it.  While `stream` is being captured into a CUDA graph
