@@ -88,7 +88,8 @@ __global__ void __launch_bounds__(256) pack_scales_kernel(const uint8_t* __restr
 
 // ------------------------------------------------------ quantise token rows
 // Token t's hidden row, quantised per 16 along d once and written to each of
-// its k permuted rows (pair_row[t * k + j]).  xq [rows, d/2] packed E2M1 (low
+// its k permuted rows (pair_row[t * k + j]; -1 for an invalid routed index,
+// skipped).  xq [rows, d/2] packed E2M1 (low
 // nibble = even element); xsf [rows, d/4]: per 64 elements a 16-byte slot
 // holding their 4 scales (then padding).
 __global__ void __launch_bounds__(128) quantize_tokens_kernel(const uint16_t* __restrict__ x,
@@ -125,6 +126,7 @@ __global__ void __launch_bounds__(128) quantize_tokens_kernel(const uint16_t* __
     }
     for (int j = 0; j < k; ++j) {
       const int64_t row = s_row[j];
+      if (row < 0) continue;  // an invalid routed index has no permuted row
       *reinterpret_cast<uint2*>(xq + row * (d / 2) + blk * 8) = make_uint2(lo, hi);
       xsf[row * (d / 4) + (blk / 4) * 16 + (blk % 4)] = sfc;
     }

@@ -669,7 +669,8 @@ __global__ void __launch_bounds__(256) permute_sort_kernel(PermuteArgs a, int32_
 // ------------------------------------------------------------------ gather
 // Block t: token t's row of x, read once, written to each of its k permuted
 // rows pair_row[t * k + j] (x_perm in expert order for the larger token
-// blocks).  n16 16-bit words per row, a multiple of 8.
+// blocks); a slot whose pair_row is -1 (an out-of-range or foreign routed
+// index) is skipped.  n16 16-bit words per row, a multiple of 8.
 __global__ void __launch_bounds__(128) scatter_tokens_kernel(const uint16_t* __restrict__ x,
                                                              const int32_t* __restrict__ pair_row,
                                                              int32_t k, int32_t n16,
@@ -687,6 +688,7 @@ __global__ void __launch_bounds__(128) scatter_tokens_kernel(const uint16_t* __r
     for (int u = 0; u < U; ++u)
       if (base + u * blockDim.x < n8) r[u] = src[base + u * blockDim.x];
     for (int j = 0; j < k; ++j) {
+      if (s_row[j] < 0) continue;  // an invalid routed index has no permuted row
       uint4* dst = reinterpret_cast<uint4*>(xp + s_row[j] * n16);
 #pragma unroll
       for (int u = 0; u < U; ++u)
