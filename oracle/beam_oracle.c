@@ -62,6 +62,21 @@ static uint16_t bf16_round(float f) {
   return (uint16_t)keep;
 }
 
+/* Nearest BF16 of a double, ties to even, with one rounding: the double is
+ * first brought to binary32 by rounding to odd (truncate, then set the last
+ * bit when inexact), which keeps the later rounding to 8 bits correct. */
+static uint16_t bf16_round_double(double v) {
+  float f = (float)v;
+  if ((double)f != v) {
+    if (fabs((double)f) > fabs(v)) f = nextafterf(f, 0.0f);
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    u |= 1u;
+    memcpy(&f, &u, sizeof f);
+  }
+  return bf16_round(f);
+}
+
 /* Nearest IEEE binary16 value of a double, ties to even, with subnormals;
  * magnitudes beyond the largest finite binary16 (65504) saturate to it.
  * Written from the format: 11 significant bits, exponents -14..15, spacing
@@ -290,7 +305,7 @@ int oracle_route(const float *logits, const float *bias, int64_t T, int32_t E,
 /* g and u are the FP32-rounded accumulators (not rounded to BF16); the      */
 /* product is rounded to FP32 and then to BF16 (h, the down GEMM's input);   */
 /* the down accumulation, the weighting and the sum over the k slots stay in */
-/* double; the output is rounded to FP32 and then to BF16.                   */
+/* double; the output is that double sum rounded once to BF16.               */
 /* Weight layouts (nn.Linear): W_g, W_u [F, d] and W_d [d, F] per expert,    */
 /* passed as one pointer per expert (NULL for experts nobody uses).          */
 /* tokens: optional list of rows to compute (NULL = all T rows); rows not    */
@@ -489,7 +504,7 @@ static int experts_impl(const uint16_t *x, int64_t T, int32_t d, int32_t F,
             acc[r] += wt * ya;
           }
         }
-        for (int32_t r = 0; r < d; ++r) out[t * (int64_t)d + r] = bf16_round((float)acc[r]);
+        for (int32_t r = 0; r < d; ++r) out[t * (int64_t)d + r] = bf16_round_double(acc[r]);
         if (out_exact)
           for (int32_t r = 0; r < d; ++r) out_exact[t * (int64_t)d + r] = acc[r];
       }
@@ -618,21 +633,6 @@ int oracle_fp8_quantize_rows(const uint16_t *x, int64_t n, int32_t cols, uint8_t
 /* ------------------------------------------------------------------------ */
 /* The sublayer boundary after the MoE branch                                */
 /* ------------------------------------------------------------------------ */
-
-/* Nearest BF16 of a double, ties to even, with one rounding: the double is
- * first brought to binary32 by rounding to odd (truncate, then set the last
- * bit when inexact), which keeps the later rounding to 8 bits correct. */
-static uint16_t bf16_round_double(double v) {
-  float f = (float)v;
-  if ((double)f != v) {
-    if (fabs((double)f) > fabs(v)) f = nextafterf(f, 0.0f);
-    uint32_t u;
-    memcpy(&u, &f, sizeof u);
-    u |= 1u;
-    memcpy(&f, &u, sizeof f);
-  }
-  return bf16_round(f);
-}
 
 /* One token's boundary after the MoE branch, [VLLM] "MoE and residual
  * stream" (sandwich norm: an RMSNorm after every sublayer and one before the

@@ -21,6 +21,17 @@ def f32_ulp_close(a, b, ulps=1):
     return np.all(np.abs(a.astype(np.float64) - b.astype(np.float64)) <= ulps * sp)
 
 
+def bf16_nearest(v) -> np.ndarray:
+    """BF16 bits of the nearest BF16 value of each float64 in v, ties to even,
+    in one rounding.  Exact: |v| / spacing is a scaling by a power of two, and
+    numpy's rint rounds half to even (normal BF16 range)."""
+    v = np.asarray(v, np.float64)
+    _, e = np.frexp(np.abs(v))                 # |v| in [2^(e-1), 2^e)
+    step = np.ldexp(1.0, e - 8)                # 8 significant bits
+    r = np.where(v == 0, v, np.copysign(np.rint(np.abs(v) / step) * step, v))
+    return inputs.bf16_bits(torch.from_numpy(r).float().to(torch.bfloat16))
+
+
 # ---------------------------------------------------------------- formats
 def test_bf16_round_matches_torch():
     vals = np.concatenate([
@@ -272,7 +283,7 @@ def test_identical_experts_closed_form():
     out = oracle.experts_bf16(inputs.bf16_bits(x), r["idx"], r["w"], inputs.bf16_bits(wg),
                               inputs.bf16_bits(wu), inputs.bf16_bits(wd), E)
     y = _torch_expert(x, wg[0], wu[0], wd[0])
-    ref = (2.5 * y).float().to(torch.bfloat16)
+    ref = torch.from_numpy(bf16_nearest((2.5 * y).numpy()).view(np.int16)).view(torch.bfloat16)
     got = torch.from_numpy(out.view(np.int16)).view(torch.bfloat16)
     # the weights sum to 2.5 up to FP32 rounding: at most one BF16 step apart
     diff = (got.float() - ref.float()).abs()
@@ -290,18 +301,47 @@ def test_forced_routing_matches_dense_torch_experts():
     lg = oracle.router_logits(inputs.bf16_bits(x), (RNG.standard_normal((E, d)) / 12).astype(np.float32))
     r = _route(lg, bias, G, 4, 8)
     assert np.all(np.sort(r["idx"], 1) == chosen)
-    out = oracle.experts_bf16(inputs.bf16_bits(x), r["idx"], r["w"], inputs.bf16_bits(wg),
-                              inputs.bf16_bits(wu), inputs.bf16_bits(wd), E)
+    out, ex = oracle.experts_bf16(inputs.bf16_bits(x), r["idx"], r["w"], inputs.bf16_bits(wg),
+                                  inputs.bf16_bits(wu), inputs.bf16_bits(wd), E, exact=True)
     ref = torch.zeros(T, d, dtype=torch.float64)
     for t in range(T):
         for j in range(8):
             e = int(r["idx"][t, j])
             ref[t] += float(r["w"][t, j]) * _torch_expert(x[t:t + 1], wg[e], wu[e], wd[e])[0]
-    ref16 = ref.float().to(torch.bfloat16)
-    got = torch.from_numpy(out.view(np.int16)).view(torch.bfloat16)
-    diff = (got.float() - ref16.float()).abs()
-    assert torch.all(diff <= ref16.float().abs() * 2 ** -7 + 1e-6)
-    assert (got == ref16).float().mean() > 0.97
+    # the FP64 sums agree to rounding order; the output is their one BF16 rounding
+    assert np.allclose(ex, ref.numpy(), rtol=1e-12, atol=1e-15)
+    assert np.array_equal(out, bf16_nearest(ref.numpy()))
+
+
+def test_output_is_one_rounding_of_the_exact_sum():
+    """The layer output is the FP64 sum over the slots rounded once to BF16.
+    Built so that each expert's down row is exactly 1 (h = 1: silu(64) * 2^-6
+    rounds to 1 in FP32, and W_d picks h_0): the output is w_0 + w_1 exactly.
+    With w = (1 + 2^-8, 2^-30) that sum lies just above the BF16 tie
+    1 + 2^-8, so one rounding gives 1 + 2^-7; rounding to FP32 first would
+    land on the tie and give 1.0.  The second token mirrors it below zero,
+    the third is an exact tie (ties to even), the fourth needs no rounding."""
+    d = F = 16
+    E = 2
+    x = torch.zeros(4, d, dtype=torch.bfloat16)
+    x[:, 0] = 1.0
+    wg = torch.zeros(E, F, d, dtype=torch.bfloat16)
+    wu = torch.zeros(E, F, d, dtype=torch.bfloat16)
+    wd = torch.zeros(E, d, F, dtype=torch.bfloat16)
+    wg[:, :, 0] = 64.0
+    wu[:, :, 0] = 2.0 ** -6
+    wd[:, :, 0] = 1.0
+    idx = np.tile(np.array([[0, 1]], np.int32), (4, 1))
+    w = np.array([[1 + 2.0 ** -8, 2.0 ** -30], [-(1 + 2.0 ** -8), -(2.0 ** -30)],
+                  [1 + 2.0 ** -8, 0.0], [1.5, 0.25]], np.float32)
+    out, ex = oracle.experts_bf16(inputs.bf16_bits(x), idx, w, inputs.bf16_bits(wg),
+                                  inputs.bf16_bits(wu), inputs.bf16_bits(wd), E, exact=True)
+    assert np.array_equal(ex[:, 0], w.astype(np.float64).sum(1))
+    assert np.all(out == out[:, :1])
+    assert out[0, 0] == 0x3F81            # 1 + 2^-7
+    assert out[1, 0] == 0xBF81            # -(1 + 2^-7)
+    assert out[2, 0] == 0x3F80            # the tie 1 + 2^-8 goes to the even 1.0
+    assert out[3, 0] == 0x3FE0            # 1.75, exact
 
 
 def test_token_subset_matches_full_run():
@@ -503,6 +543,59 @@ def test_f16_activation_experts_match_dense_torch():
     assert np.allclose(ex, ref.numpy(), rtol=1e-12, atol=1e-12)
 
 
+def _nvfp4_torch_blocks(v: torch.Tensor) -> torch.Tensor:
+    """The NVFP4 activation rule restated with torch: per 16 consecutive
+    values, scale = float8_e4m3fn(amax / 6) (FP32 division, torch's
+    round-to-nearest-even cast), codes by the independent E2M1 rounding of
+    the generator on v / scale (FP32 division), zeros where the scale is 0;
+    returns the dequantised values code * scale in float64."""
+    vf = v.float().reshape(-1, 16)
+    scale = (vf.abs().amax(dim=1) / 6.0).to(torch.float8_e4m3fn).float().unsqueeze(1)
+    safe = torch.where(scale > 0, scale, torch.ones_like(scale))
+    codes = inputs._e2m1_codes(vf / safe)
+    mag = torch.tensor([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0], dtype=torch.float64)
+    val = mag[(codes & 7).long()] * torch.where(codes >= 8, -1.0, 1.0).double()
+    val = torch.where(scale > 0, val * scale.double(), torch.zeros_like(val))
+    return val.reshape(v.shape)
+
+
+def test_nvfp4_activation_experts_match_dense_torch():
+    """NVFP4 weights and NVFP4 activations (both GEMM inputs quantised per 16
+    with global scale 1): the expert layer against a dense torch FP64
+    restatement.  x is quantised along d from its BF16 values; the FP32
+    SwiGLU product is quantised along F as it is, with no BF16 rounding first.
+    Planting either plausible mistake in the oracle's block rule fails this
+    test: rounding h to BF16 before quantising it, or taking the scale from
+    amax / 4 instead of amax / 6."""
+    T, d, F, E = 6, 64, 48, 8
+    x = _bf16_matrix((T, d))
+    r = _route(RNG.standard_normal((T, E)), np.zeros(E), 4, 2, 3)
+    proj, deq = {}, {}
+    for name, (n, kk) in (("g", (F, d)), ("u", (F, d)), ("d", (d, F))):
+        q = RNG.integers(0, 256, (E, n, kk // 2), dtype=np.uint8)
+        sf = RNG.integers(0x20, 0x48, (E, n, kk // 16), dtype=np.uint8)
+        gs = (RNG.uniform(0.5, 2.0, E) * 2.0 ** -6).astype(np.float32)
+        proj[name] = dict(q=q, sf=sf, gs=gs)
+        codes = np.stack([q & 15, q >> 4], -1).reshape(E, n, kk)
+        deq[name] = torch.from_numpy(
+            np.vectorize(oracle.e2m1_value)(codes)
+            * np.repeat(np.vectorize(oracle.e4m3_value)(sf), 16, axis=2)
+            * gs.astype(np.float64)[:, None, None])
+    out, ex = oracle.experts_nvfp4(inputs.bf16_bits(x), r["idx"], r["w"], proj["g"], proj["u"],
+                                   proj["d"], E, act_quant=oracle.ACT_NVFP4, exact=True)
+    xq = _nvfp4_torch_blocks(x.float())
+    ref = torch.zeros(T, d, dtype=torch.float64)
+    for t in range(T):
+        for j in range(3):
+            e = int(r["idx"][t, j])
+            g = (xq[t] @ deq["g"][e].T).float().double()
+            u = (xq[t] @ deq["u"][e].T).float().double()
+            hq = _nvfp4_torch_blocks((g / (1 + torch.exp(-g)) * u).float())
+            ref[t] += float(r["w"][t, j]) * (hq @ deq["d"][e].T)
+    assert np.allclose(ex, ref.numpy(), rtol=1e-12, atol=1e-12)
+    assert np.array_equal(out, bf16_nearest(ref.numpy()))
+
+
 def test_swiglu_rows_through_the_expert_layer():
     """One expert, weight 1 and an identity down projection: the expert
     layer's output is h itself (h is BF16, the identity sum is exact), so the
@@ -621,4 +714,4 @@ def test_fp8_activation_experts_match_dense_torch():
             hh = qh.double()[0] * float(sh[0])
             ref[t] += float(r["w"][t, j]) * (hh @ deq["d"][e].T)
     assert np.allclose(ex, ref.numpy(), rtol=1e-12, atol=1e-12)
-    assert np.array_equal(out, inputs.bf16_bits(ref.float().to(torch.bfloat16)))
+    assert np.array_equal(out, bf16_nearest(ref.numpy()))
