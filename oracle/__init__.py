@@ -11,6 +11,7 @@ BF16 arrays cross this boundary as ``numpy.uint16`` bit patterns.
 from __future__ import annotations
 
 import ctypes
+import itertools
 import os
 import subprocess
 import threading
@@ -76,6 +77,9 @@ def _load():
         lib.oracle_experts_fp8.argtypes = [_P, _I64, _I32, _I32, _I32, _I32, _P, _P,
                                            _P, _P, _P, _P, _P, _P,
                                            _I32, _P, _I64, _P, _P]
+        lib.oracle_experts_fp8_ties.argtypes = [_P, _I64, _I32, _I32, _I32, _I32, _P, _P,
+                                                _P, _P, _P, _P, _P, _P,
+                                                ctypes.c_double, _P, _I64, _P, _P, _P, _P]
         lib.oracle_fp8_quantize_rows.argtypes = [_P, _I64, _I32, _P, _P]
         lib.oracle_num_threads.restype = ctypes.c_int
         lib.oracle_set_threads.argtypes = [ctypes.c_int]
@@ -230,6 +234,65 @@ def route(logits: np.ndarray, bias: np.ndarray, n_groups: int, topk_groups: int,
             "expert_margin": em, "group_margin": gm}
 
 
+def _tie_choices(order, score, n_take, tol):
+    """The ways to take the first n_take entries of `order` (sorted best
+    first by `score`) when scores closer than tol are read as tied: the
+    entries before the tie run that straddles the cut are always taken, and
+    any n_take minus that many of the run's members complete the choice."""
+    n = len(order)
+    if n_take >= n or score[order[n_take - 1]] - score[order[n_take]] >= tol:
+        return [tuple(order[:n_take])]
+    a = n_take - 1
+    while a > 0 and score[order[a - 1]] - score[order[a]] < tol:
+        a -= 1
+    b = n_take
+    while b + 1 < n and score[order[b]] - score[order[b + 1]] < tol:
+        b += 1
+    run = order[a:b + 1]
+    return [tuple(order[:a]) + tuple(pick)
+            for pick in itertools.combinations(run, n_take - a)]
+
+
+def route_alternatives(r: dict, t: int, n_groups: int, topk_groups: int, topk: int,
+                       routed_scale: float, tol: float, limit: int = 4096) -> list[dict]:
+    """Every routing of token t that the selection would give if the choice
+    scores it ranks (the group scores, then the experts' c) that lie closer
+    than tol were tied, from this oracle's own scores r["s"], r["c"] (the
+    output of route()).  Each entry: 'idx' (the experts, slot order by c
+    descending, expert ascending) and 'w' (FP32 weights 2.5 * s / sum s of
+    that set).  The first entry is the oracle's own choice when nothing is
+    near a tie.  Used to accept a near-tie token routed to another valid set
+    and to compute its output from that set."""
+    s = np.asarray(r["s"][t], np.float32)
+    c = np.asarray(r["c"][t], np.float32)
+    E = c.size
+    S = E // n_groups
+    gs = np.zeros(n_groups, np.float32)
+    for g in range(n_groups):
+        top = sorted(range(g * S, (g + 1) * S), key=lambda e: (-float(c[e]), e))[:2]
+        gs[g] = np.float32(c[top[0]]) + np.float32(c[top[1]])
+    g_order = sorted(range(n_groups), key=lambda g: (-float(gs[g]), g))
+    out, seen = [], set()
+    for groups in _tie_choices(g_order, gs.astype(np.float64), topk_groups, tol):
+        cand = sorted((e for g in groups for e in range(g * S, (g + 1) * S)),
+                      key=lambda e: (-float(c[e]), e))
+        for chosen in _tie_choices(cand, c.astype(np.float64), topk, tol):
+            key = frozenset(chosen)
+            if key in seen:
+                continue
+            seen.add(key)
+            idx = np.array(sorted(chosen, key=lambda e: (-float(c[e]), e)), np.int32)
+            ssum = 0.0
+            for e in idx:
+                ssum += float(s[e])
+            w = np.array([np.float32(routed_scale * float(s[e]) / ssum) for e in idx],
+                         np.float32)
+            out.append({"idx": idx, "w": w})
+            if len(out) > limit:
+                raise ValueError(f"token {t}: more than {limit} near-tie routings")
+    return out
+
+
 def _expert_ptrs(ws, E: int):
     """Per-expert pointer table from a 3-D array or a list/dict of 2-D arrays
     (None / missing entries for experts nobody uses)."""
@@ -319,16 +382,30 @@ def experts_nvfp4(x_bf16, idx, w, gate, up, down, n_experts: int, act_quant=True
 ACT_FP8 = 3
 
 
+FP8_TIE_REL = 2.0 ** -16
+
+
 def experts_fp8(x_bf16, idx, w, gate, up, down, n_experts: int, act_quant=True,
-                tokens=None, out: np.ndarray | None = None, exact: bool = False):
+                tokens=None, out: np.ndarray | None = None, exact: bool = False,
+                ties: bool = False, tie_rel: float = FP8_TIE_REL):
     """Dynamic FP8 experts.  gate/up/down are dicts with per-expert 'q' (E4M3
     codes [N, K]) and 's' (FP32 scale per output row [N]).  act_quant: True /
     ACT_FP8 quantises both GEMM inputs per row to E4M3 (x per token, h per
     (token, expert) row after its BF16 rounding); False / ACT_BF16 keeps BF16
-    activations."""
+    activations.
+
+    With ``ties`` (FP8 activations only) it also returns the near ties of the
+    h quantisation: elements whose FP32 value lies within ``tie_rel`` of a
+    BF16 rounding midpoint, where a computation that differs from this one by
+    less than that may take the other BF16 value and so another E4M3 code.
+    Returns (out, exact, slack [T, d], scale_tie [T] bool): slack bounds how far
+    each output moves under any such choices; scale_tie marks tokens whose
+    row scale itself could move."""
     mode = int(act_quant)
     if mode not in (ACT_BF16, 1, ACT_FP8):
         raise ValueError(f"unknown activation mode {act_quant}")
+    if ties and not mode:
+        raise ValueError("near ties exist only with FP8 activations")
     x = _c(x_bf16, np.uint16)
     T, d = x.shape
     idx = _c(idx, np.int32)
@@ -346,6 +423,17 @@ def experts_fp8(x_bf16, idx, w, gate, up, down, n_experts: int, act_quant=True,
         out = np.zeros((T, d), np.uint16)
     ex = np.zeros((T, d), np.float64) if exact else None
     tok = None if tokens is None else _c(tokens, np.int64)
+    if ties:
+        ex = np.zeros((T, d), np.float64) if ex is None else ex
+        slack = np.zeros((T, d), np.float64)
+        flag = np.zeros(T, np.uint8)
+        rc = _load().oracle_experts_fp8_ties(_ptr(x), T, d, F, k, n_experts, _ptr(idx), _ptr(w),
+                                             *tabs, float(tie_rel), _ptr(tok),
+                                             0 if tok is None else tok.size, _ptr(out), _ptr(ex),
+                                             _ptr(slack), _ptr(flag))
+        if rc:
+            raise ValueError(f"oracle_experts_fp8_ties failed ({rc})")
+        return out, ex, slack, flag.astype(bool)
     rc = _load().oracle_experts_fp8(_ptr(x), T, d, F, k, n_experts, _ptr(idx), _ptr(w),
                                     *tabs, 1 if mode else 0, _ptr(tok),
                                     0 if tok is None else tok.size, _ptr(out), _ptr(ex))

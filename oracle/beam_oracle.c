@@ -327,6 +327,12 @@ typedef struct {
   int fp4;
   int fp8;
   int act_quant;
+  /* FP8 near ties (optional): per token the summed effect on each output of
+   * the h codes that a rounding of h on the other side of a BF16 midpoint
+   * would move, and a flag for rows whose scale could move. */
+  double tie_rel;
+  double *tie_slack;   /* [T, d] */
+  uint8_t *scale_tie;  /* [T] */
 } weights_t;
 
 /* One row of the dynamic FP8 scheme's activation rule (per token, or per
@@ -365,8 +371,54 @@ static void fp8_row_quantize(const float *v, int64_t n, uint8_t *q, float *scale
   if (scale_out) *scale_out = scale;
 }
 
+/* The values of all 256 E4M3 and all 16 E2M1 codes, tabled from the
+ * decoders above (the weight loops look codes up here instead of decoding
+ * each one again).  Filled by experts_impl before its parallel region. */
+static double e4m3_tab[256];
+static double e2m1_tab[16];
+
+static void fill_format_tables(void) {
+  for (int c = 0; c < 256; ++c) e4m3_tab[c] = e4m3_value((uint8_t)c);
+  for (int c = 0; c < 16; ++c) e2m1_tab[c] = e2m1_value((uint8_t)c);
+}
+
 static double fp8_weight(const uint8_t *q, const float *s, int64_t row, int64_t col, int64_t K) {
-  return e4m3_value(q[row * K + col]) * (double)s[row];
+  return e4m3_tab[q[row * K + col]] * (double)s[row];
+}
+
+/* Near ties of the FP8 path's h quantisation.  hf holds one (token, expert)
+ * row of FP32 SwiGLU products and hb their BF16 roundings.  An element whose
+ * FP32 value lies within rel * |value| of the midpoint between its BF16
+ * value and the next BF16 value on its side could be rounded to that
+ * neighbour by an FP32 computation whose error is below that bound.  For
+ * such an element diff receives the change of its dequantised E4M3 value if
+ * the neighbour were taken (0 when both quantise alike); when the neighbour
+ * or the element itself decides the row's amax, the row's scale could move
+ * and *scale_flag is set instead. */
+static void fp8_h_ties(const float *hf, const float *hb, int64_t n, double rel, double *diff,
+                       int *scale_flag) {
+  float amax = 0.0f;
+  for (int64_t i = 0; i < n; ++i) {
+    float a = fabsf(hb[i]);
+    if (a > amax) amax = a;
+  }
+  const float scale = amax > 0.0f ? amax / 448.0f : 1.0f;
+  for (int64_t i = 0; i < n; ++i) {
+    diff[i] = 0.0;
+    const double v = (double)hf[i], b = (double)hb[i];
+    if (v == b || v != v) continue;
+    const uint16_t mag = (uint16_t)(bf16_round(hf[i]) & 0x7fffu);
+    const uint16_t nmag = fabs(v) > fabs(b) ? (uint16_t)(mag + 1u) : (uint16_t)(mag - 1u);
+    const double nb = bf16_value((uint16_t)((v < 0 ? 0x8000u : 0u) | nmag));
+    if (fabs(v - 0.5 * (b + nb)) > rel * fabs(v)) continue;
+    if (fabs(nb) >= (double)amax || fabs(b) == (double)amax) {
+      *scale_flag = 1;
+      continue;
+    }
+    const double qb = e4m3_value(e4m3_encode((float)b / scale)) * (double)scale;
+    const double qn = e4m3_value(e4m3_encode((float)nb / scale)) * (double)scale;
+    diff[i] = qn - qb;
+  }
 }
 
 /* One NVFP4 block of 16: the activation rule used on both GEMM inputs of the
@@ -392,7 +444,7 @@ static double fp4_weight(const uint8_t *q, const uint8_t *sf, float gs,
   int64_t flat = row * K + col;
   uint8_t byte = q[flat >> 1];
   uint8_t code = (flat & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 15u);
-  return e2m1_value(code) * e4m3_value(sf[row * (K / 16) + col / 16]) * (double)gs;
+  return e2m1_tab[code] * e4m3_tab[sf[row * (K / 16) + col / 16]] * (double)gs;
 }
 
 static int experts_impl(const uint16_t *x, int64_t T, int32_t d, int32_t F,
@@ -418,6 +470,7 @@ static int experts_impl(const uint16_t *x, int64_t T, int32_t d, int32_t F,
     }
   }
   if (err) return err;
+  fill_format_tables();
 #pragma omp parallel
   {
     double *xin = (double *)malloc(sizeof(double) * (size_t)d);
@@ -425,7 +478,11 @@ static int experts_impl(const uint16_t *x, int64_t T, int32_t d, int32_t F,
     double *hin = (double *)malloc(sizeof(double) * (size_t)F);
     double *acc = (double *)malloc(sizeof(double) * (size_t)d);
     float *tmp = (float *)malloc(sizeof(float) * (size_t)(d > F ? d : F));
-    if (!xin || !hf || !hin || !acc || !tmp) {
+    double *hdiff = W->tie_slack ? (double *)malloc(sizeof(double) * (size_t)F) : NULL;
+    double *slack = W->tie_slack ? (double *)malloc(sizeof(double) * (size_t)d) : NULL;
+    int32_t *tie_f = W->tie_slack ? (int32_t *)malloc(sizeof(int32_t) * (size_t)F) : NULL;
+    if (!xin || !hf || !hin || !acc || !tmp ||
+        (W->tie_slack && (!hdiff || !slack || !tie_f))) {
 #pragma omp atomic write
       err = -3;
     } else {
@@ -447,6 +504,9 @@ static int experts_impl(const uint16_t *x, int64_t T, int32_t d, int32_t F,
           for (int32_t j = 0; j < d; ++j) xin[j] = bf16_value(xr[j]);
         }
         for (int32_t j = 0; j < d; ++j) acc[j] = 0.0;
+        int scale_flag = 0;
+        if (slack)
+          for (int32_t j = 0; j < d; ++j) slack[j] = 0.0;
         for (int32_t slot = 0; slot < k; ++slot) {
           const int32_t e = idx[t * k + slot];
           const double wt = (double)w[t * k + slot];
@@ -481,6 +541,17 @@ static int experts_impl(const uint16_t *x, int64_t T, int32_t d, int32_t F,
             /* h keeps its BF16 rounding, then the row is quantised */
             for (int32_t f = 0; f < F; ++f) tmp[f] = (float)bf16_value(bf16_round(hf[f]));
             fp8_row_quantize(tmp, F, NULL, NULL, hin);
+            if (slack) {
+              int32_t n_tie = 0;
+              fp8_h_ties(hf, tmp, F, W->tie_rel, hdiff, &scale_flag);
+              for (int32_t f = 0; f < F; ++f)
+                if (hdiff[f] != 0.0) tie_f[n_tie++] = f;
+              /* each near tie's whole effect on every output of the token */
+              for (int32_t q = 0; q < n_tie; ++q)
+                for (int32_t r = 0; r < d; ++r)
+                  slack[r] += fabs(wt * hdiff[tie_f[q]] * fp8_weight(W->ed[e], W->sed[e], r,
+                                                                      tie_f[q], F));
+            }
           } else if (W->fp4 && W->act_quant == 2) {
             for (int32_t f = 0; f < F; ++f) hin[f] = f16_round_value((double)hf[f]);
           } else if (W->fp4 && W->act_quant) {
@@ -507,6 +578,10 @@ static int experts_impl(const uint16_t *x, int64_t T, int32_t d, int32_t F,
         for (int32_t r = 0; r < d; ++r) out[t * (int64_t)d + r] = bf16_round_double(acc[r]);
         if (out_exact)
           for (int32_t r = 0; r < d; ++r) out_exact[t * (int64_t)d + r] = acc[r];
+        if (slack) {
+          for (int32_t r = 0; r < d; ++r) W->tie_slack[t * (int64_t)d + r] = slack[r];
+          W->scale_tie[t] = (uint8_t)scale_flag;
+        }
       }
     }
     free(xin);
@@ -514,6 +589,9 @@ static int experts_impl(const uint16_t *x, int64_t T, int32_t d, int32_t F,
     free(hin);
     free(acc);
     free(tmp);
+    free(hdiff);
+    free(slack);
+    free(tie_f);
   }
   return err;
 }
@@ -612,6 +690,34 @@ int oracle_experts_fp8(const uint16_t *x, int64_t T, int32_t d, int32_t F,
   W.ed = qd; W.sed = sd;
   W.fp8 = 1;
   W.act_quant = act_quant;
+  return experts_impl(x, T, d, F, k, E, idx, w, &W, tokens, n_tokens, out, out_exact);
+}
+
+/* The same layer with FP8 activations, also reporting its near ties (see
+ * fp8_h_ties): tie_slack [T, d] receives, per output, the sum over the
+ * token's near-tie h codes of |w * (code change) * W_d[., f]|, which is how
+ * far that output moves if any subset of those codes takes the neighbouring
+ * BF16 value's code; scale_tie [T] flags tokens with a row whose amax
+ * element sits at such a midpoint. */
+int oracle_experts_fp8_ties(const uint16_t *x, int64_t T, int32_t d, int32_t F,
+                            int32_t k, int32_t E, const int32_t *idx, const float *w,
+                            const uint8_t *const *qg, const float *const *sg,
+                            const uint8_t *const *qu, const float *const *su,
+                            const uint8_t *const *qd, const float *const *sd,
+                            double tie_rel, const int64_t *tokens, int64_t n_tokens,
+                            uint16_t *out, double *out_exact, double *tie_slack,
+                            uint8_t *scale_tie) {
+  if (!tie_slack || !scale_tie || !(tie_rel >= 0.0)) return -1;
+  weights_t W;
+  memset(&W, 0, sizeof W);
+  W.eg = qg; W.seg = sg;
+  W.eu = qu; W.seu = su;
+  W.ed = qd; W.sed = sd;
+  W.fp8 = 1;
+  W.act_quant = 1;
+  W.tie_rel = tie_rel;
+  W.tie_slack = tie_slack;
+  W.scale_tie = scale_tie;
   return experts_impl(x, T, d, F, k, E, idx, w, &W, tokens, n_tokens, out, out_exact);
 }
 

@@ -11,7 +11,7 @@ import torch
 import group_limited_routed_gb300 as pkg
 from group_limited_routed_gb300 import ep, inputs
 
-from _parity import check_out, exempt_tokens, oracle_out, oracle_route
+from _parity import check_out, gpu_routing, oracle_out, oracle_route, output_routing
 
 pytestmark = pytest.mark.gpu
 
@@ -24,7 +24,9 @@ def _bf16_experts(cfg, t):
 
 
 def _emulate(cfg, t, Ts, experts=None):
-    """Every rank's output of the expert-parallel layer, ranks in sequence."""
+    """Every rank's input rows, its output of the expert-parallel layer (ranks
+    in sequence) and the expert indices the ranks' routing chose, in token
+    order."""
     experts = _bf16_experts(cfg, t) if experts is None else experts
     R = len(Ts)
     starts = np.concatenate([[0], np.cumsum(Ts)])
@@ -40,7 +42,7 @@ def _emulate(cfg, t, Ts, experts=None):
         e = torch.cat([p[1] for p in parts]).contiguous()
         w = torch.cat([p[2] for p in parts]).contiguous()
         y_recv.append(experts(R, q, x, e, w))
-    outs = []
+    outs, routing = [], []
     for r in range(R):
         # rows come back per destination rank, in the order they were sent
         back = []
@@ -51,14 +53,15 @@ def _emulate(cfg, t, Ts, experts=None):
         ws = disp[r][4]
         outs.append(pkg.ep_combine(cfg, y_back, Ts[r], ws))
         assert pkg.check_status(ws) == 0
-    return hid, outs
+        routing.append(gpu_routing(ws, cfg, Ts[r]))
+    return hid, outs, np.concatenate(routing)
 
 
 @pytest.mark.parametrize("Ts", [[40, 24], [16, 0, 33, 5], [9, 1, 0, 30, 7, 12, 3, 20]])
 def test_emulated_ranks_reproduce_the_layer(Ts):
     cfg = inputs.CONFIGS["tiny"].replace(seed=70 + len(Ts))
     t = inputs.generate(cfg, "cuda", T=sum(Ts))
-    hid, outs = _emulate(cfg, t, Ts)
+    hid, outs, gidx = _emulate(cfg, t, Ts)
     for h, o in zip(hid, outs):
         ref = pkg.forward(cfg, h, t["router_w"], t["corr_bias"], t["w_gate"], t["w_up"],
                           t["w_down"])
@@ -67,14 +70,14 @@ def test_emulated_ranks_reproduce_the_layer(Ts):
     full = torch.cat(outs)
     c2 = cfg.replace(T=sum(Ts))
     lg, r = oracle_route(c2, t)
-    check_out(full, oracle_out(c2, t, r["idx"], r["w"]), rows=~exempt_tokens(r))
+    check_out(full, oracle_out(c2, t, *output_routing(c2, r, gidx)))
 
 
 def test_emulated_ranks_beam_decode():
     """Beam shapes, eight ranks of 32 experts, 32 tokens per rank."""
     cfg = inputs.CONFIGS["decode"]
     t = inputs.generate(cfg, "cuda", T=8 * 32)
-    hid, outs = _emulate(cfg, t, [32] * 8)
+    hid, outs, _ = _emulate(cfg, t, [32] * 8)
     for h, o in zip(hid, outs):
         ref = pkg.forward(cfg, h, t["router_w"], t["corr_bias"], t["w_gate"], t["w_up"],
                           t["w_down"])
@@ -116,7 +119,7 @@ def test_emulated_ranks_nvfp4_experts(Ts):
     def run(R_, q, x, e, w):
         return pkg.ep_experts_nvfp4(cfg, R_, q, x, e, w, *local[q])
 
-    hid, outs = _emulate(cfg, t, Ts, experts=run)
+    hid, outs, _ = _emulate(cfg, t, Ts, experts=run)
     for h, o in zip(hid, outs):
         if h.shape[0] == 0:
             continue
@@ -144,7 +147,7 @@ def test_emulated_ranks_fp8_experts(Ts):
     def run(R_, q, x, e, w):
         return pkg.ep_experts_fp8(cfg, R_, q, x, e, w, *local[q])
 
-    hid, outs = _emulate(cfg, t, Ts, experts=run)
+    hid, outs, _ = _emulate(cfg, t, Ts, experts=run)
     for h, o in zip(hid, outs):
         if h.shape[0] == 0:
             continue

@@ -10,7 +10,7 @@ import torch
 import group_limited_routed_gb300 as pkg
 from group_limited_routed_gb300 import inputs
 
-from _parity import check_out, exempt_tokens, oracle_out, oracle_route
+from _parity import check_out, gpu_routing, oracle_out, oracle_route, output_routing
 
 pytestmark = pytest.mark.gpu
 
@@ -31,4 +31,4 @@ def test_bounded_wait_reports_timeout_and_the_context_recovers(T):
     out = pkg.forward(*args, ws=ws)
     assert pkg.check_status(ws) == 0
     lg, r = oracle_route(cfg, t)
-    check_out(out, oracle_out(cfg, t, r["idx"], r["w"]), rows=~exempt_tokens(r))
+    check_out(out, oracle_out(cfg, t, *output_routing(cfg, r, gpu_routing(ws, cfg, cfg.T))))

@@ -8,8 +8,8 @@ import oracle
 import group_limited_routed_gb300 as pkg
 from group_limited_routed_gb300 import inputs
 
-from _parity import (W_RTOL_SELECT, check_logits, check_out, check_routing, exempt_tokens, host,
-                     oracle_out, oracle_route)
+from _parity import (W_RTOL_SELECT, check_logits, check_out, check_routing, gpu_routing, host,
+                     oracle_out, oracle_route, output_routing)
 
 pytestmark = pytest.mark.gpu
 CFG = inputs.CONFIGS["tiny"]
@@ -50,9 +50,8 @@ def test_forward_matches_oracle(tiny):
     out = pkg.forward(CFG, t["hidden"], t["router_w"], t["corr_bias"], t["w_gate"], t["w_up"],
                       t["w_down"], ws=ws)
     assert pkg.check_status(ws) == 0
-    ref = oracle_out(CFG, t, r["idx"], r["w"])
-    keep = ~exempt_tokens(r)
-    check_out(out, ref, rows=keep)
+    ref = oracle_out(CFG, t, *output_routing(CFG, r, gpu_routing(ws, CFG, CFG.T)))
+    check_out(out, ref)
 
 
 def test_permutation_is_a_stable_counting_sort(tiny):
@@ -123,10 +122,11 @@ def test_ragged_token_counts(T):
     cfg = CFG.replace(T=T, seed=10 + T)
     t = inputs.generate(cfg, "cuda")
     lg, r = oracle_route(cfg, t)
+    ws = pkg.Workspace(cfg, T)
     out = pkg.forward(cfg, t["hidden"], t["router_w"], t["corr_bias"], t["w_gate"], t["w_up"],
-                      t["w_down"])
-    ref = oracle_out(cfg, t, r["idx"], r["w"])
-    check_out(out, ref, rows=~exempt_tokens(r))
+                      t["w_down"], ws=ws)
+    ref = oracle_out(cfg, t, *output_routing(cfg, r, gpu_routing(ws, cfg, T)))
+    check_out(out, ref)
     idx, w = pkg.route(cfg, t["hidden"], t["router_w"], t["corr_bias"])
     check_routing(cfg, host(idx), host(w), r)
 
@@ -150,10 +150,11 @@ def test_all_tokens_on_one_expert_and_idle_experts():
     t["corr_bias"] = b
     lg, r = oracle_route(cfg, t)
     assert np.all(np.sort(r["idx"], 1) == [3, 4, 9, 12, 17, 18, 25, 26])
+    ws = pkg.Workspace(cfg, cfg.T)
     out = pkg.forward(cfg, t["hidden"], t["router_w"], t["corr_bias"], t["w_gate"], t["w_up"],
-                      t["w_down"])
-    ref = oracle_out(cfg, t, r["idx"], r["w"])
-    check_out(out, ref, rows=~exempt_tokens(r))
+                      t["w_down"], ws=ws)
+    ref = oracle_out(cfg, t, *output_routing(cfg, r, gpu_routing(ws, cfg, cfg.T)))
+    check_out(out, ref)
 
 
 def test_all_equal_scores_follow_the_tie_rule():
@@ -215,10 +216,11 @@ def test_tensor_core_router_mid_sized_layer(T):
     idx, w, logits = pkg.route(cfg, t["hidden"], t["router_w"], t["corr_bias"], want_logits=True)
     check_logits(host(logits), lg)
     check_routing(cfg, host(idx), host(w), r)
+    ws = pkg.Workspace(cfg, T)
     out = pkg.forward(cfg, t["hidden"], t["router_w"], t["corr_bias"], t["w_gate"], t["w_up"],
-                      t["w_down"])
-    rows = np.nonzero(~exempt_tokens(r))[0][:64]
-    ref = oracle_out(cfg, t, r["idx"], r["w"], tokens=rows)
+                      t["w_down"], ws=ws)
+    rows = np.arange(min(T, 64))
+    ref = oracle_out(cfg, t, *output_routing(cfg, r, gpu_routing(ws, cfg, T), rows), tokens=rows)
     check_out(out, ref, rows=rows)
 
 

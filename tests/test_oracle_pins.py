@@ -715,3 +715,130 @@ def test_fp8_activation_experts_match_dense_torch():
             ref[t] += float(r["w"][t, j]) * (hh @ deq["d"][e].T)
     assert np.allclose(ex, ref.numpy(), rtol=1e-12, atol=1e-12)
     assert np.array_equal(out, bf16_nearest(ref.numpy()))
+
+
+# ------------------------------------------------- near-tie routings and h codes
+def _tie_heavy_scores(T, E, tol, seed):
+    """Logits and a bias that put every token's choice scores c = s + b on a
+    grid of spacing 0.3 tol in a narrow band (about an eighth of the levels
+    taken), so the group and expert cuts often fall inside short runs of
+    scores closer than tol."""
+    rng = np.random.default_rng(seed)
+    lg = rng.standard_normal((T, E)).astype(np.float32)
+    s = (1.0 / (1.0 + np.exp(-lg.astype(np.float64)))).astype(np.float32)
+    target = 0.5 + rng.integers(0, 8 * E, (T, E)) * (0.3 * tol)
+    return lg, s, target
+
+
+def test_route_alternatives_without_ties_is_the_routing():
+    """tol = 0: the oracle's own routing, weights bit for bit."""
+    T, E, G, kg, k = 40, 64, 8, 4, 8
+    lg = RNG.standard_normal((T, E)).astype(np.float32)
+    r = _route(lg, RNG.uniform(-0.05, 0.05, E).astype(np.float32), G, kg, k)
+    for t in range(T):
+        alts = oracle.route_alternatives(r, t, G, kg, k, 2.5, 0.0)
+        assert len(alts) == 1
+        assert np.array_equal(alts[0]["idx"], r["idx"][t])
+        assert np.array_equal(alts[0]["w"], r["w"][t])
+
+
+@pytest.mark.parametrize("E,G,kg,k", [(16, 4, 2, 3), (32, 8, 4, 5), (64, 8, 4, 8)])
+def test_route_alternatives_cover_perturbed_selections(E, G, kg, k):
+    """Perturbing every choice score by less than tol / 5 (through the bias)
+    can only reorder scores closer than tol: each routing the selection then
+    returns must be among the alternatives listed from the unperturbed
+    scores (same expert set, same weights per expert).  The list is the
+    oracle's own routing first; it may hold more than perturbations reach
+    (a run of scores each closer than tol to the next is taken whole)."""
+    tol = 3e-6
+    T = 12
+    lg, s, target = _tie_heavy_scores(T, E, tol, seed=E + k)
+    rng = np.random.default_rng(7)
+    moved = []
+    for t in range(T):
+        bias = (target[t] - s[t]).astype(np.float32)
+        r = _route(lg[t:t + 1], bias, G, kg, k)
+        alts = oracle.route_alternatives(r, 0, G, kg, k, 2.5, tol)
+        sets = [frozenset(a["idx"].tolist()) for a in alts]
+        assert len(set(sets)) == len(sets)
+        reached = set()
+        for _ in range(200):
+            pb = (bias + rng.uniform(-tol / 5, tol / 5, E)).astype(np.float32)
+            rp = _route(lg[t:t + 1], pb, G, kg, k)
+            key = frozenset(rp["idx"][0].tolist())
+            assert key in sets, (t, sorted(key))
+            a = alts[sets.index(key)]
+            wa = dict(zip(a["idx"].tolist(), a["w"].tolist()))
+            for e, wv in zip(rp["idx"][0].tolist(), rp["w"][0].tolist()):
+                assert abs(wa[e] - wv) <= 1e-6 * abs(wv)
+            reached.add(key)
+        assert sets[0] == frozenset(r["idx"][0].tolist())
+        assert np.array_equal(alts[0]["idx"], r["idx"][0]) and np.array_equal(alts[0]["w"], r["w"][0])
+        moved.append(len(reached))
+    assert max(moved) > 1                # the tie-heavy scores do move the selection
+
+
+def test_fp8_near_tie_slack_matches_torch_restatement():
+    """The near ties the FP8 oracle reports, restated with torch: per (token,
+    expert) row the FP32 h, its BF16 rounding, the next BF16 value on its
+    side and their midpoint; an element within rel * |h| of the midpoint
+    whose E4M3 code (row scale from the BF16 row) differs between the two
+    BF16 values adds |w * (code change) * W_d[., f]| to every output of its
+    token; one whose BF16 value or neighbour reaches the row's amax flags the
+    token instead.  A large rel gives many ties.  Forcing one tie to the
+    neighbour in the dense restatement moves the output by exactly that
+    element's share."""
+    T, d, F, E = 5, 64, 48, 8
+    rel = 2.0 ** -9
+    x = _bf16_matrix((T, d))
+    r = _route(RNG.standard_normal((T, E)), np.zeros(E), 4, 2, 3)
+    proj, deq = {}, {}
+    for name, (n, kk) in (("g", (F, d)), ("u", (F, d)), ("d", (d, F))):
+        proj[name], deq[name] = _fp8_weights(E, n, kk, pow2_scales=False)
+    out, ex, slack, flag = oracle.experts_fp8(inputs.bf16_bits(x), r["idx"], r["w"], proj["g"],
+                                              proj["u"], proj["d"], E, act_quant=True,
+                                              ties=True, tie_rel=rel)
+    qx, sx = _fp8_torch_rows(x)
+    xh = qx.double() * sx.double().unsqueeze(1)
+    want = torch.zeros(T, d, dtype=torch.float64)
+    want_flag = np.zeros(T, bool)
+    n_ties = 0
+    for t in range(T):
+        for j in range(3):
+            e = int(r["idx"][t, j])
+            wt = float(r["w"][t, j])
+            g = (xh[t] @ deq["g"][e].T).float().double()
+            u = (xh[t] @ deq["u"][e].T).float().double()
+            hf = (g / (1 + torch.exp(-g)) * u).float()
+            hb = hf.to(torch.bfloat16)
+            bits = hb.view(torch.int16).int() & 0x7FFF
+            up = hf.double().abs() > hb.double().abs()
+            nbits = torch.where(up, bits + 1, bits - 1) | torch.where(hf < 0, 0x8000, 0)
+            nb = nbits.to(torch.int16).view(torch.bfloat16)
+            near = ((hf.double() - (hb.double() + nb.double()) / 2).abs()
+                    <= rel * hf.double().abs()) & (hf.double() != hb.double())
+            amax = hb.float().abs().max()
+            scale = amax / 448.0 if amax > 0 else torch.tensor(1.0)
+            at_amax = near & ((nb.double().abs() >= float(amax)) |
+                              (hb.double().abs() == float(amax)))
+            if at_amax.any():
+                want_flag[t] = True
+            qb = (hb.float() / scale).to(torch.float8_e4m3fn).double() * float(scale)
+            qn = (nb.float() / scale).to(torch.float8_e4m3fn).double() * float(scale)
+            moves = near & ~at_amax & (qb != qn)
+            for f in torch.nonzero(moves).reshape(-1).tolist():
+                n_ties += 1
+                share = wt * float(qn[f] - qb[f]) * deq["d"][e][:, f]
+                want[t] += share.abs()
+                if n_ties == 1:        # force this one tie in the dense restatement
+                    h_alt = hb.clone()
+                    h_alt[f] = nb[f]
+                    qh, sh = _fp8_torch_rows(h_alt.unsqueeze(0))
+                    qh0, sh0 = _fp8_torch_rows(hb.unsqueeze(0))
+                    assert float(sh[0]) == float(sh0[0])
+                    moved = wt * ((qh.double()[0] * float(sh[0]) - qh0.double()[0] * float(sh0[0]))
+                                  @ deq["d"][e].T)
+                    assert torch.allclose(moved, share, rtol=1e-12, atol=1e-18)
+    assert n_ties > 0
+    assert np.array_equal(flag, want_flag)
+    assert np.allclose(slack, want.numpy(), rtol=1e-12, atol=1e-18)

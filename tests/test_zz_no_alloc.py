@@ -9,13 +9,14 @@ stop-at-first-failure run has already run every other test; it also passes
 on its own in a fresh process."""
 import ctypes
 
+import numpy as np
 import pytest
 import torch
 
 from group_limited_routed_gb300 import api, inputs
 from group_limited_routed_gb300.config import CConfig
 
-from _parity import check_out, exempt_tokens, oracle_out, oracle_route
+from _parity import check_out, oracle_out, oracle_route, output_routing
 
 pytestmark = pytest.mark.gpu
 
@@ -60,8 +61,10 @@ def test_noalloc_matches_forward_on_two_calls_in_a_row(name):
     sub = cfg.replace(T=batches[0].shape[0])
     tt = dict(t, hidden=batches[0])
     lg, r = oracle_route(sub, tt)
-    rows = (~exempt_tokens(r)).nonzero()[0][:8]
-    check_out(outs[0], oracle_out(sub, tt, r["idx"], r["w"], tokens=rows), rows=rows)
+    rows = np.arange(min(sub.T, 8))
+    gidx = api.route(sub, batches[0], t["router_w"], t["corr_bias"])[0].cpu().numpy()
+    check_out(outs[0], oracle_out(sub, tt, *output_routing(sub, r, gidx, rows), tokens=rows),
+              rows=rows)
 
 
 def test_noalloc_refuses_batches_beyond_its_array():
