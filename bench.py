@@ -6,7 +6,12 @@
 A step is one call of the whole layer (router, selection, permute, gather of
 the token rows (inside the gate/up GEMM for decode-sized batches), gate/up
 GEMM, down GEMM, combine) on one batch of the workload, with every
-input resident in device memory.  Metric: layer tokens/s.  The expert weights
+input resident in device memory.  Metric: layer tokens/s.  The headline is
+--config (the decode batch by default); the default run also measures the
+prefill chunk, the skewed routing, the NVFP4 batch (quantised and 16-bit
+activations) and the dynamic FP8 decode and prefill batches in the same
+process with the same steps, each as a record under "workloads" (a summary
+of each also under "roofline").  The expert weights
 a step touches (about 12 GB for the decode batch) are far larger than L2, so
 no flush is needed between steps.  Timing: CUDA events on the launching
 stream around the K timed steps, bracketed by a barrier and a device
@@ -244,6 +249,12 @@ def run_reference(args, cfg):
     # oracle spreads tokens over its threads, so a step samples at least one
     # token per thread when that fits (one token alone would use one core)
     cores = oracle.num_threads()
+    # the experts the whole batch touches, from the oracle's own routing
+    r = oracle.route(oracle.router_logits(inputs.bf16_bits(t["hidden"]),
+                                          t["router_w"].cpu().numpy()),
+                     t["corr_bias"].cpu().numpy(), cfg.n_groups, cfg.topk_groups, cfg.topk,
+                     cfg.routed_scale)
+    touched = int(np.unique(r["idx"]).size)
     sec1, _ = oracle_sample(cfg, t, 1, seed=1, a16=a16)
     per_step_budget = 120.0 / max(1, args.steps + args.warmup)
     n = int(max(1, min(cfg.T, cores * per_step_budget / max(sec1, 1e-6))))
@@ -259,7 +270,7 @@ def run_reference(args, cfg):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": config_record(cfg, None, a16=a16),
+            "data": "synthetic", "config": config_record(cfg, touched, a16=a16),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores,
                              "kind": "oracle",
                              "sample": f"{n} sampled tokens of the {cfg.T}-token batch per step"},
@@ -287,35 +298,77 @@ def config_record(cfg, touched, routed=False, a16=False, graph=False):
     return rec
 
 
-def run_gpu(args, cfg):
-    rank, local, world = dist_env()
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    use_dist = world > 1
-    if use_dist:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=dev)
+# Nominal dense tensor rate of each expert format relative to BF16 on GB300
+# (2.25 PFLOP/s BF16, 4.5 FP8, 13.5 FP4); W4A16 multiplies in F16.
+TC_RATIO = {"bf16": 1.0, "fp8": 2.0, "nvfp4": 6.0, "a16": 1.0}
+NOMINAL_HBM_GBS = 7900.0
+
+
+def kernel_roofline(kernel, bytes_alg, flops, us, fmt, pk, traffic=None, intermediates=None):
+    """One kernel's place against its bounds.  bytes_alg: the algorithmic
+    bytes it must move (the touched experts' weights of its projections, and
+    the layer's hidden input for gate/up); intermediates: the bytes of the
+    implementation's own buffers it reads and writes, reported apart.  Bound
+    "tensor" when its flops per algorithmic byte exceed the ridge of the
+    sustained tensor peak of its dtype over the copy bandwidth.  The copy
+    bandwidth moves as many bytes written as read, so a read-dominated kernel
+    can pass it: the fraction of the nominal HBM rate is reported beside."""
+    sec = us / 1e6
+    gbs = bytes_alg / sec / 1e9
+    tflops = flops / sec / 1e12
+    sus = pk["bf16_tflops_sustained"] * TC_RATIO[fmt]
+    burst = pk["bf16_tflops"] * TC_RATIO[fmt]
+    ridge = sus * 1e12 / (pk["hbm_gbs"] * 1e9)
+    tensor = flops / bytes_alg > ridge
+    rec = {"kernel": kernel, "us": round(us, 2), "algorithmic_bytes_per_launch": int(bytes_alg),
+           "algorithmic_flops_per_launch": int(flops),
+           "hbm": {"achieved": gbs, "peak": pk["hbm_gbs"], "frac": gbs / pk["hbm_gbs"],
+                   "frac_nominal": gbs / NOMINAL_HBM_GBS},
+           "tensor": {"achieved": tflops, "peak_sustained": sus, "frac_sustained": tflops / sus,
+                      "peak_burst": burst, "frac_burst": tflops / burst},
+           "roofline_frac": max(bytes_alg / (pk["hbm_gbs"] * 1e9), flops / (sus * 1e12)) / sec}
+    if tensor:
+        rec.update({"bound": "tensor", "achieved": tflops, "peak": sus, "unit": "TFLOP/s",
+                    "frac": tflops / sus})
+    else:
+        rec.update({"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                    "frac": gbs / pk["hbm_gbs"]})
+    rec["traffic"] = traffic
+    if intermediates:
+        rec["intermediate_bytes"] = {k: int(v) for k, v in intermediates.items()}
+    return rec
+
+
+def measure(cfg, args, dev, rank, world, use_dist, *, a16=False, routed=False, graph=False,
+            cpu=False):
+    """One workload: W warm-up steps, then the K timed steps of the layer as
+    a caller runs it, the same K steps again with the library's stage events
+    (per-kernel times), and K end-to-end steps from pinned host memory.
+    Returns its record (tokens/s over the slowest rank)."""
     t = inputs.generate(cfg.replace(seed=cfg.seed + 1000 * rank) if rank else cfg, dev)
     fp4 = cfg.weight_fmt == "nvfp4"
     fp8 = cfg.weight_fmt == "fp8"
-    a16 = fp4 and args.a16
+    a16 = fp4 and a16
+    fmt_name = ("a16" if a16 else "nvfp4") if fp4 else "fp8" if fp8 else "bf16"
     fmt = (pkg.NVFP4_A16 if a16 else pkg.NVFP4) if fp4 else pkg.FP8 if fp8 else 0
     ws = pkg.Workspace(cfg, cfg.T, dev, weight_fmt=fmt)
     stream = torch.cuda.current_stream()
     out = torch.empty(cfg.T, cfg.d, dtype=torch.bfloat16, device=dev)
+    ridx = None
     if fp4:
         wts = [pkg.Fp4Weight.of(t[n]) for n in ("w_gate", "w_up", "w_down")]
         fwd = pkg.forward_nvfp4_a16 if a16 else pkg.forward_nvfp4
 
         def layer(x, o):
-            return fwd(cfg, x, t["router_w"], t["corr_bias"], *wts, out=o, ws=ws, stream=torch.cuda.current_stream())
+            return fwd(cfg, x, t["router_w"], t["corr_bias"], *wts, out=o, ws=ws,
+                       stream=torch.cuda.current_stream())
     elif fp8:
         wts = [pkg.Fp8Weight.of(t[n]) for n in ("w_gate", "w_up", "w_down")]
 
         def layer(x, o):
             return pkg.forward_fp8(cfg, x, t["router_w"], t["corr_bias"], *wts, out=o, ws=ws,
                                    stream=torch.cuda.current_stream())
-    elif args.routed:
+    elif routed:
         # routing replay: the routes are recorded once, the timed steps run
         # the experts and the combine on them
         ridx, rw = pkg.route(cfg, t["hidden"], t["router_w"], t["corr_bias"], stream=stream)
@@ -335,11 +388,8 @@ def run_gpu(args, cfg):
         step()
     torch.cuda.synchronize()
     if pkg.check_status(ws) != 0:
-        raise RuntimeError("device status after warm-up")
-    if args.routed:
-        touched = int(torch.unique(ridx).numel())
-    else:
-        touched = touched_experts(ws, cfg)
+        raise RuntimeError(f"{cfg.name}: device status after warm-up")
+    touched = int(torch.unique(ridx).numel()) if routed else touched_experts(ws, cfg)
 
     # per-step stage events (created and recorded once so the handles exist)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(args.steps)]
@@ -348,15 +398,15 @@ def run_gpu(args, cfg):
             e.record(stream)
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
-    sampler = ClockSampler(local)
+    sampler = ClockSampler(torch.cuda.current_device())
     sampler.start()
     for _ in range(max(3, args.warmup)):
         step()
     if use_dist:
-        dist.barrier()
+        dist_barrier()
     torch.cuda.synchronize()
     graphs = None
-    if args.graph:
+    if graph:
         # one layer call captured twice: plain, and with its stage events
         # (event-record nodes; each replay records them again, so they hold
         # the last replay's times)
@@ -380,7 +430,7 @@ def run_gpu(args, cfg):
         stage events the library records each step's stage boundaries (they
         cost GPU time of their own, so the headline loop runs without)."""
         if use_dist:
-            dist.barrier()
+            dist_barrier()
         torch.cuda.synchronize()
         t_start.record(stream)
         for i in range(args.steps):
@@ -392,7 +442,7 @@ def run_gpu(args, cfg):
         t_end.record(stream)
         torch.cuda.synchronize()
         if use_dist:
-            dist.barrier()
+            dist_barrier()
         pkg.set_stage_events(None)
         return t_start.elapsed_time(t_end)
 
@@ -405,7 +455,7 @@ def run_gpu(args, cfg):
         stage_ms = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(7)]
                              for i in range(args.steps)]).mean(axis=0)
     if pkg.check_status(ws) != 0:
-        raise RuntimeError("device status after the timed region")
+        raise RuntimeError(f"{cfg.name}: device status after the timed region")
 
     # end to end through the public API: pinned host in, pinned host out
     x_host = t["hidden"].cpu().pin_memory()
@@ -435,79 +485,138 @@ def run_gpu(args, cfg):
     e2e_value = job_throughput(world, cfg.T, e2e_steps, e2e_ms)
 
     pk = peaks()
+    T, d, F, E, k = cfg.T, cfg.d, cfg.d_ff, cfg.n_experts, cfg.topk
+    TK = T * k
     # weight bytes of one projection of one expert: BF16, E2M1 + E4M3 per 16,
-    # or E4M3 + one FP32 scale per row (d_ff rows for gate/up, d for down)
-    E_b = (cfg.d * cfg.d_ff // 2 + cfg.d * cfg.d_ff // 16 if fp4
-           else cfg.d * cfg.d_ff if fp8 else cfg.d * cfg.d_ff * 2)
-    sc_b = 4 if fp8 else 0
-    # gate/up token bytes per (token, expert) row: its input row and its h
-    # row (E4M3 in, BF16 out for FP8)
-    TK = cfg.T * cfg.topk
+    # or E4M3 + one FP32 scale per output row
+    E_b = d * F // 2 + d * F // 16 if fp4 else d * F if fp8 else d * F * 2
+    gu_w = touched * 2 * (E_b + (4 * F if fp8 else 0))
+    dn_w = touched * (E_b + (4 * d if fp8 else 0))
+    hidden_b = T * d * 2
+    # the implementation's own buffers (not algorithmic bytes): token rows in
+    # expert order, h, the FP32 expert rows y
+    x_row = d * (0.5625 if fp4 and not a16 else 1 if fp8 else 2)
+    h_row = F * (0.5625 if fp4 and not a16 else 2)
+    small = TK <= 4 * E
+    gu_inter = {"token_rows_read": TK * x_row, "h_written": TK * h_row}
     if fp8:
-        tok_rows = TK * (cfg.d + 2 * cfg.d_ff + 4)
-    else:
-        tok_rows = TK * (cfg.d + cfg.d_ff) * (2 if (not fp4 or a16) else 0.5625)
-    gu_bytes = touched * 2 * (E_b + sc_b * cfg.d_ff) + tok_rows
-    gu_gbs = gu_bytes / (stage_ms[4] / 1e3) / 1e9
-    layer_bytes = touched * (3 * E_b + sc_b * (2 * cfg.d_ff + cfg.d)) + cfg.n_experts * cfg.d * 4 \
-        + cfg.n_experts * 4 + 2 * cfg.T * cfg.d * 2
+        gu_inter["h_bf16_written"] = TK * F * 2
+        gu_inter.pop("h_written")
+    dn_inter = {"h_read": TK * (F if fp8 else h_row), "y_written": TK * d * 4}
+    gu_flops = 4 * TK * d * F
+    dn_flops = 2 * TK * d * F
+    dom = DOMINANT[fmt_name]
+    kernels = {
+        "gate_up": kernel_roofline(dom, gu_w + hidden_b, gu_flops, stage_ms[4] * 1e3, fmt_name,
+                                   pk, traffic_for(dom, cfg.name), gu_inter),
+        "down": kernel_roofline(dom.replace("gate_up", "down"), dn_w, dn_flops,
+                                stage_ms[5] * 1e3, fmt_name, pk, None, dn_inter),
+    }
+    layer_bytes = touched * (3 * E_b + (4 * (2 * F + d) if fp8 else 0)) + E * d * 4 + E * 4 \
+        + 2 * T * d * 2
     layer_ms = ms / args.steps
-    layer_flops = 2 * cfg.T * cfg.d * cfg.n_experts + 6 * cfg.T * cfg.topk * cfg.d * cfg.d_ff
-    # The dominant kernel's bound: tensor when its flops per algorithmic byte
-    # exceed the measured ridge (sustained tensor peak of its dtype / copy
-    # bandwidth), else HBM.  It is timed inside the step, so the tensor peak
-    # is the sustained one; FP8 takes the measured BF16 peak times the
-    # nominal FP8 / BF16 ratio (4.5 / 2.25).  (NVFP4 batches here are far
-    # below any ridge.)
-    gu_flops = 4 * cfg.T * cfg.topk * cfg.d * cfg.d_ff
-    tc_peak = pk["bf16_tflops_sustained"] * (2.0 if fp8 else 1.0)
-    ridge = tc_peak * 1e12 / (pk["hbm_gbs"] * 1e9)
-    tensor_bound = not fp4 and gu_flops / gu_bytes > ridge
-    dom = DOMINANT["a16" if a16 else "nvfp4" if fp4 else "fp8" if fp8 else "bf16"]
-    gu_tflops = gu_flops / (stage_ms[4] / 1e3) / 1e12
-    if tensor_bound:
-        roofline = {"bound": "tensor", "kernel": dom, "achieved": gu_tflops,
-                    "peak": tc_peak, "unit": "TFLOP/s",
-                    "frac": gu_tflops / tc_peak,
-                    "peak_source": pk["source"] + (" (sustained bf16 x 2, the nominal fp8 ratio)"
-                                                   if fp8 else " (sustained bf16)"),
-                    "traffic": traffic_for(dom, cfg.name),
-                    "algorithmic_flops_per_launch": gu_flops,
-                    "algorithmic_bytes_per_launch": gu_bytes}
-    else:
-        roofline = {"bound": "hbm", "kernel": dom, "achieved": gu_gbs,
-                    "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": gu_gbs / pk["hbm_gbs"],
-                    "peak_source": pk["source"],
-                    "traffic": traffic_for(dom, cfg.name),
-                    "algorithmic_bytes_per_launch": gu_bytes}
-    line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": layer_ms, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None,
+    layer_flops = 2 * T * d * E + 6 * TK * d * F
+    sus = pk["bf16_tflops_sustained"] * TC_RATIO[fmt_name]
+    burst = pk["bf16_tflops"] * TC_RATIO[fmt_name]
+    lsec = layer_ms / 1e3
+    layer_roof = {
+        "algorithmic_bytes": int(layer_bytes), "algorithmic_flops": int(layer_flops),
+        "hbm": {"achieved": layer_bytes / lsec / 1e9, "peak": pk["hbm_gbs"],
+                "frac": layer_bytes / lsec / 1e9 / pk["hbm_gbs"],
+                "frac_nominal": layer_bytes / lsec / 1e9 / NOMINAL_HBM_GBS},
+        "tensor": {"achieved": layer_flops / lsec / 1e12, "peak_sustained": sus,
+                   "frac_sustained": layer_flops / lsec / 1e12 / sus, "peak_burst": burst,
+                   "frac_burst": layer_flops / lsec / 1e12 / burst},
+        # max(bytes / BW, flops / TC) / time, the sustained tensor peak
+        "roofline_frac": max(layer_bytes / (pk["hbm_gbs"] * 1e9),
+                             layer_flops / (sus * 1e12)) / lsec,
+        "intermediate_bytes": {
+            "scatter": 0 if small or fp4 else int(T * x_row + TK * x_row),
+            "gate_up": int(sum(gu_inter.values())), "down": int(sum(dn_inter.values())),
+            "combine": int(TK * d * 4 + T * d * 2)}}
+    gu = kernels["gate_up"]
+    roofline = {k: gu[k] for k in ("bound", "achieved", "peak", "unit", "frac", "traffic")}
+    roofline.update({"kernel": dom, "peak_source": pk["source"] + (
+        " (sustained bf16" + (f" x {TC_RATIO[fmt_name]:g}, the nominal ratio)" if
+                              TC_RATIO[fmt_name] != 1 else ")") if gu["bound"] == "tensor"
+        else " (copy bandwidth)"),
+        "algorithmic_bytes_per_launch": gu["algorithmic_bytes_per_launch"],
+        "algorithmic_flops_per_launch": gu["algorithmic_flops_per_launch"],
+        "frac_nominal_hbm": gu["hbm"]["frac_nominal"], "nominal_hbm_gbs": NOMINAL_HBM_GBS})
+    rec = {
+        "value": value, "unit": UNIT, "ms_per_step": layer_ms,
         "dtype": ("nvfp4 weights x f16 activations" if a16 else "nvfp4 (e2m1 x e4m3 per 16)")
-        if fp4 else "fp8 (e4m3, fp32 scale per row)" if fp8 else "bf16", "data": "synthetic",
-        "config": config_record(cfg, touched, args.routed, a16, args.graph),
-        "roofline": roofline,
-        "layer_roofline": {"bound": "hbm", "algorithmic_bytes": layer_bytes,
-                           "achieved": layer_bytes / (layer_ms / 1e3) / 1e9,
-                           "peak": pk["hbm_gbs"], "unit": "GB/s",
-                           "frac": layer_bytes / (layer_ms / 1e3) / 1e9 / pk["hbm_gbs"],
-                           "tflops": layer_flops / (layer_ms / 1e3) / 1e12,
-                           "tflops_peak_sustained": tc_peak,
-                           "tflops_frac_sustained":
-                               layer_flops / (layer_ms / 1e3) / 1e12 / tc_peak},
+        if fp4 else "fp8 (e4m3, fp32 scale per row)" if fp8 else "bf16",
+        "config": config_record(cfg, touched, routed, a16, graph),
+        "roofline": roofline, "kernels": kernels, "layer_roofline": layer_roof,
         "stage_us": {n: round(float(v) * 1e3, 1) for n, v in zip(STAGES, stage_ms)},
-        # the per-stage times (and the roofline's kernel time) come from a
-        # second timed loop of the same steps with stage events recorded
+        # the per-stage times (and the kernels' times) come from a second
+        # timed loop of the same steps with stage events recorded
         "stage_events_ms_per_step": ms_events / args.steps,
-        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": cfg.T * cfg.d * 2,
-                "d2h_bytes_per_step": cfg.T * cfg.d * 2},
-        "gpu_launches": args.steps * pkg.kernels_per_forward(
-            cfg, cfg.T, fmt, args.routed),
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": T * d * 2,
+                "d2h_bytes_per_step": T * d * 2},
+        "gpu_launches": args.steps * pkg.kernels_per_forward(cfg, T, fmt, routed),
         "clocks": clocks,
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.routed:
-        line["cpu_baseline"] = cpu_baseline(cfg, t, a16=a16)
+    if cpu:
+        rec["cpu_baseline"] = cpu_baseline(cfg, t, a16=a16)
+    del t, ws, out
+    torch.cuda.empty_cache()
+    return rec
+
+
+def dist_barrier():
+    import torch.distributed as dist
+    dist.barrier()
+
+
+# The workloads measured beside the headline in the default run: the
+# prefill chunk and skewed routing (BF16), the NVFP4 batch with quantised
+# and with 16-bit activations, and the dynamic FP8 decode and prefill.
+SUB_WORKLOADS = [("prefill", False), ("skewed", False), ("nvfp4", False), ("nvfp4", True),
+                 ("fp8", False), ("fp8_prefill", False)]
+
+
+def summary(name, rec):
+    """The figures of one sub-workload that the headline line repeats."""
+    gu, dn, lr = rec["kernels"]["gate_up"], rec["kernels"]["down"], rec["layer_roofline"]
+    return {"ms_per_step": rec["ms_per_step"], "tokens_per_s": rec["value"],
+            "layer_hbm_frac": lr["hbm"]["frac"], "layer_tflops": lr["tensor"]["achieved"],
+            "layer_tensor_frac_sustained": lr["tensor"]["frac_sustained"],
+            "layer_tensor_frac_burst": lr["tensor"]["frac_burst"],
+            "layer_roofline_frac": lr["roofline_frac"],
+            "gate_up": {"bound": gu["bound"], "frac": gu["frac"], "us": gu["us"]},
+            "down": {"bound": dn["bound"], "frac": dn["frac"], "us": dn["us"]},
+            "sm_mhz": rec["clocks"].get("sm_mhz"), "reasons": rec["clocks"].get("reasons")}
+
+
+def run_gpu(args, cfg):
+    rank, local, world = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    use_dist = world > 1
+    if use_dist:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    head = measure(cfg, args, dev, rank, world, use_dist, a16=args.a16, routed=args.routed,
+                   graph=args.graph,
+                   cpu=rank == 0 and world == 1 and not args.no_cpu_baseline and not args.routed)
+    line = {"metric": METRIC, "value": head["value"], "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": head["dtype"], "data": "synthetic"}
+    line.update({k: v for k, v in head.items() if k not in ("value", "unit", "ms_per_step",
+                                                             "dtype")})
+    subs = [] if args.headline_only else [
+        (n, a) for n, a in SUB_WORKLOADS if not (n == args.config and a == args.a16)]
+    if subs:
+        line["workloads"] = {}
+        for name, sub_a16 in subs:
+            key = name + ("_a16" if sub_a16 else "")
+            rec = measure(inputs.CONFIGS[name], args, dev, rank, world, use_dist, a16=sub_a16)
+            line["workloads"][key] = rec
+        # the sub-workloads' headline figures, also inside the roofline record
+        line["roofline"]["workloads"] = {k: summary(k, v) for k, v in line["workloads"].items()}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if use_dist:
@@ -529,6 +638,8 @@ def main(argv=None):
                     help="replay the layer call from a CUDA graph (stage times of the last replay)")
     ap.add_argument("--routed", action="store_true",
                     help="time beam_moe_forward_routed on recorded routes (routing replay)")
+    ap.add_argument("--headline-only", action="store_true",
+                    help="measure only --config, without the other workloads")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)
     cfg = inputs.CONFIGS[args.config]
