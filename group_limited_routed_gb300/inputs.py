@@ -9,8 +9,8 @@ top 8, d_ff 2560, scale 2.5; HF release post, section "专家混合": 32 experts
 group).  Distributions: hidden ~ N(0, 1) in BF16; router W_r ~ N(0, 1/d) in
 FP32 stored [E, d]; correction bias ~ U(-0.05, 0.05) in FP32; expert weights
 ~ N(0, 0.02^2) in BF16 stored W_gate/W_up [E, F, d] and W_down [E, d, F]
-(NVFP4 and FP8 expert weights are those draws quantised once, here: they are
-the checkpoint both sides read).
+(NVFP4, FP8 and MXFP8 expert weights are those draws quantised once, here:
+they are the checkpoint both sides read).
 Draw order: hidden, router_w, corr_bias, [skewed experts], w_gate, w_up,
 w_down, one torch.Generator seeded per configuration.  The small configuration
 is drawn on the CPU generator (so any machine reproduces it); the Beam-sized
@@ -36,7 +36,7 @@ class MoEConfig:
     d_ff: int
     routed_scale: float = 2.5
     seed: int = 0
-    weight_fmt: str = "bf16"          # "bf16", "nvfp4" or "fp8"
+    weight_fmt: str = "bf16"          # "bf16", "nvfp4", "fp8" or "mxfp8"
     skew_experts: int = 0             # experts that get +skew_bias
     skew_bias: float = 0.0
     cpu_generator: bool = False       # draw on the CPU generator
@@ -98,6 +98,9 @@ CONFIGS = {
                                      weight_fmt="fp8",
                                      description="Beam expert shapes, 32 FP8 experts (8x4), "
                                                  "T=1024 (profiling case, prefill regime)"),
+    "mxfp8": MoEConfig(name="mxfp8", T=32, seed=13, weight_fmt="mxfp8", **_BEAM,
+                       description="Beam MoE layer decode batch T=32, MXFP8 experts (E4M3 "
+                                   "weights and activations, one E8M0 scale per 32 along K)"),
     # profiling case for the FP8 kernels: 32 experts, decode-sized batch
     "profile_fp8": MoEConfig(name="profile_fp8", T=8, d=5120, n_experts=32, n_groups=8,
                              topk_groups=4, topk=8, d_ff=2560, seed=11, weight_fmt="fp8",
@@ -161,6 +164,22 @@ def quantize_fp8_weight(w: torch.Tensor):
     return q.view(torch.uint8).contiguous(), scale.contiguous()
 
 
+def quantize_mxfp8_weight(w: torch.Tensor):
+    """One expert projection [N, K] (float32) -> (E4M3 codes uint8 [N, K], E8M0
+    scale codes uint8 [N, K/32]).  Each block of 32 along K shares the scale
+    2^X with X = floor(log2(amax)) - 8 (8 being E4M3's largest exponent), the
+    OCP MX conversion; codes round to nearest, ties to even, saturating at
+    448.  Checkpoint-format preparation."""
+    N, K = w.shape
+    blk = w.float().reshape(N, K // 32, 32)
+    amax = blk.abs().amax(dim=-1)
+    _, e = torch.frexp(amax)                      # amax = m 2^e, m in [0.5, 1)
+    x = torch.where(amax > 0, e - 1 - 8, torch.full_like(e, -127)).clamp(-127, 127)
+    scaled = torch.ldexp(blk, -x.unsqueeze(-1).float())
+    q = scaled.clamp(-448.0, 448.0).to(torch.float8_e4m3fn)
+    return q.view(torch.uint8).reshape(N, K).contiguous(), (x + 127).to(torch.uint8).contiguous()
+
+
 def generate(cfg: MoEConfig, device="cuda", T: int | None = None,
              weights: bool = True) -> dict:
     """Draw one configuration's tensors on ``device``.
@@ -168,7 +187,8 @@ def generate(cfg: MoEConfig, device="cuda", T: int | None = None,
     Returns hidden [T,d] bf16, router_w [E,d] f32, corr_bias [E] f32 and, with
     ``weights``, w_gate/w_up [E,F,d] and w_down [E,d,F] in BF16 or, for the
     NVFP4 format, dicts {'q','sf','gs'} per projection, for the FP8 format
-    dicts {'q' uint8 [E,N,K], 's' float32 [E,N]}.
+    dicts {'q' uint8 [E,N,K], 's' float32 [E,N]}, for the MXFP8 format dicts
+    {'q' uint8 [E,N,K], 's' uint8 E8M0 codes [E,N,K/32]}.
     """
     T = cfg.T if T is None else T
     g, gdev = _gen(cfg, device)
@@ -201,6 +221,13 @@ def generate(cfg: MoEConfig, device="cuda", T: int | None = None,
                     torch.randn(n, k, generator=g, device=gdev) * 0.02)
                 q[e], sf[e], gs[e:e + 1] = wq, wsf, wgs
             res[name] = {"q": q, "sf": sf, "gs": gs}
+        elif cfg.weight_fmt == "mxfp8":
+            q = torch.empty(E, n, k, dtype=torch.uint8, device=out_dev)
+            sc = torch.empty(E, n, k // 32, dtype=torch.uint8, device=out_dev)
+            for e in range(E):
+                q[e], sc[e] = quantize_mxfp8_weight(
+                    torch.randn(n, k, generator=g, device=gdev) * 0.02)
+            res[name] = {"q": q, "s": sc}
         elif cfg.weight_fmt == "fp8":
             q = torch.empty(E, n, k, dtype=torch.uint8, device=out_dev)
             sc = torch.empty(E, n, dtype=torch.float32, device=out_dev)

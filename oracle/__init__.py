@@ -81,6 +81,12 @@ def _load():
                                                 _P, _P, _P, _P, _P, _P,
                                                 ctypes.c_double, _P, _I64, _P, _P, _P, _P]
         lib.oracle_fp8_quantize_rows.argtypes = [_P, _I64, _I32, _P, _P]
+        lib.oracle_experts_mxfp8.argtypes = [_P, _I64, _I32, _I32, _I32, _I32, _P, _P,
+                                             _P, _P, _P, _P, _P, _P, _I32, ctypes.c_double,
+                                             _P, _I64, _P, _P, _P, _P]
+        lib.oracle_mx_quantize.argtypes = [_P, _I64, _P, _P]
+        lib.oracle_e8m0_value.argtypes = [ctypes.c_uint8]
+        lib.oracle_e8m0_value.restype = ctypes.c_double
         lib.oracle_num_threads.restype = ctypes.c_int
         lib.oracle_set_threads.argtypes = [ctypes.c_int]
         _lib = lib
@@ -113,6 +119,10 @@ def e2m1_value(code: int) -> float:
 
 def e4m3_value(code: int) -> float:
     return float(_load().oracle_e4m3_value(code))
+
+
+def e8m0_value(code: int) -> float:
+    return float(_load().oracle_e8m0_value(code))
 
 
 def e2m1_encode(v: float) -> int:
@@ -440,6 +450,58 @@ def experts_fp8(x_bf16, idx, w, gate, up, down, n_experts: int, act_quant=True,
     if rc:
         raise ValueError(f"oracle_experts_fp8 failed ({rc})")
     return (out, ex) if exact else out
+
+
+def experts_mxfp8(x_bf16, idx, w, gate, up, down, n_experts: int, act_quant=True,
+                  tokens=None, out: np.ndarray | None = None, exact: bool = False,
+                  ties: bool = False, tie_rel: float = FP8_TIE_REL):
+    """MXFP8 experts.  gate/up/down are dicts with per-expert 'q' (E4M3 codes
+    [N, K]) and 's' (E8M0 scale codes [N, K/32]).  act_quant: True quantises
+    both GEMM inputs to MX blocks of 32 (x along d, the FP32 SwiGLU product
+    along F); False keeps BF16 activations.  With ``ties`` (quantised
+    activations only) also returns the near ties of the h quantisation, as
+    experts_fp8 does: (out, exact, slack [T, d], scale_tie [T] bool)."""
+    if ties and not act_quant:
+        raise ValueError("near ties exist only with quantised activations")
+    x = _c(x_bf16, np.uint16)
+    T, d = x.shape
+    idx = _c(idx, np.int32)
+    w = _c(w, np.float32)
+    k = idx.shape[1]
+    keep = []
+    tabs = []
+    for p in (gate, up, down):
+        q, kq = _expert_ptrs(p["q"], n_experts)
+        sc, ks = _expert_ptrs(p["s"], n_experts)
+        keep += kq + ks
+        tabs += [ctypes.cast(q, _P), ctypes.cast(sc, _P)]
+    F = _infer_F(gate["q"], d)
+    if out is None:
+        out = np.zeros((T, d), np.uint16)
+    ex = np.zeros((T, d), np.float64) if (exact or ties) else None
+    slack = np.zeros((T, d), np.float64) if ties else None
+    flag = np.zeros(T, np.uint8) if ties else None
+    tok = None if tokens is None else _c(tokens, np.int64)
+    rc = _load().oracle_experts_mxfp8(_ptr(x), T, d, F, k, n_experts, _ptr(idx), _ptr(w), *tabs,
+                                      1 if act_quant else 0, float(tie_rel), _ptr(tok),
+                                      0 if tok is None else tok.size, _ptr(out), _ptr(ex),
+                                      _ptr(slack), _ptr(flag))
+    if rc:
+        raise ValueError(f"oracle_experts_mxfp8 failed ({rc})")
+    if ties:
+        return out, ex, slack, flag.astype(bool)
+    return (out, ex) if exact else out
+
+
+def mx_quantize(v: np.ndarray):
+    """The MX activation rule (E4M3 elements, one E8M0 scale per 32): returns
+    (codes uint8 [n], scale codes uint8 [n/32])."""
+    v = _c(v, np.float32).reshape(-1)
+    q = np.zeros(v.size, np.uint8)
+    sc = np.zeros(v.size // 32, np.uint8)
+    if _load().oracle_mx_quantize(_ptr(v), v.size, _ptr(q), _ptr(sc)):
+        raise ValueError("length must be a multiple of 32")
+    return q, sc
 
 
 def fp8_quantize_rows(x_bf16):

@@ -122,6 +122,13 @@ static double e4m3_value(uint8_t code) {
   return sign ? -v : v;
 }
 
+/* E8M0 (the shared scale of the MX formats): 8 exponent bits, bias 127, no
+ * sign and no mantissa; code 255 is NaN. */
+static double e8m0_value(uint8_t code) {
+  if (code == 0xFFu) return NAN;
+  return ldexp(1.0, (int)code - 127);
+}
+
 /* Nearest code by exhaustive search over the format's finite magnitudes,
  * ties to the even code (the one whose lowest bit is 0); values beyond the
  * largest finite magnitude saturate to it (satfinite).  Brute force on
@@ -324,8 +331,13 @@ typedef struct {
   /* FP8 weights: E4M3 codes [N, K], one FP32 scale per output row [N]. */
   const uint8_t *const *eg, *const *eu, *const *ed;
   const float *const *seg, *const *seu, *const *sed;
+  /* MXFP8 weights: E4M3 codes [N, K], one E8M0 scale per 32 consecutive
+   * elements along K [N, K/32]. */
+  const uint8_t *const *mg, *const *mu, *const *md;
+  const uint8_t *const *smg, *const *smu, *const *smd;
   int fp4;
   int fp8;
+  int mx;
   int act_quant;
   /* FP8 near ties (optional): per token the summed effect on each output of
    * the h codes that a rounding of h on the other side of a BF16 midpoint
@@ -421,6 +433,73 @@ static void fp8_h_ties(const float *hf, const float *hb, int64_t n, double rel, 
   }
 }
 
+/* One MX block ([OCP] "Microscaling Formats (MX) v1.0", the conversion of a
+ * vector of scalars to an MX block), E4M3 elements: the shared exponent is
+ * X = floor(log2(amax)) - 8 (8 = the largest exponent of E4M3), clamped to
+ * the E8M0 range [-127, 127] (an all-zero block takes -127); each element is
+ * E4M3(v / 2^X), nearest even, saturating at 448.  Writes the scale code, the
+ * element codes (when asked) and the dequantised values code * 2^X. */
+static int mx_shared_exponent(float amax) {
+  if (!(amax > 0.0f)) return -127;
+  int e;
+  frexp((double)amax, &e);             /* amax in [2^(e-1), 2^e) */
+  int x = e - 1 - 8;
+  return x < -127 ? -127 : x > 127 ? 127 : x;
+}
+
+static void mx_block_quantize(const float *v, int n, uint8_t *scale_code, uint8_t *codes,
+                              double *out) {
+  float amax = 0.0f;
+  for (int i = 0; i < n; ++i) {
+    float a = fabsf(v[i]);
+    if (a > amax) amax = a;
+  }
+  const int x = mx_shared_exponent(amax);
+  if (scale_code) *scale_code = (uint8_t)(x + 127);
+  for (int i = 0; i < n; ++i) {
+    const float r = (float)ldexp((double)v[i], -x);   /* exact: a power-of-two scaling */
+    const uint8_t c = e4m3_encode(r);
+    if (codes) codes[i] = c;
+    if (out) out[i] = e4m3_value(c) * ldexp(1.0, x);
+  }
+}
+
+/* Near ties of the MXFP8 path's h quantisation (see fp8_h_ties for the
+ * FP8 path): an FP32 h element whose scaled value lies within rel of an E4M3
+ * rounding midpoint gets in diff the change of its dequantised value if the
+ * neighbouring code were taken; a block whose amax lies within rel of a
+ * power of two (where the shared exponent changes) sets *scale_flag. */
+static void mx_h_ties(const float *hf, int n, double rel, double *diff, int *scale_flag) {
+  float amax = 0.0f;
+  for (int i = 0; i < n; ++i) {
+    float a = fabsf(hf[i]);
+    if (a > amax) amax = a;
+  }
+  if (amax > 0.0f) {
+    int e;
+    const double m = frexp((double)amax, &e);       /* amax = m 2^e, m in [0.5, 1) */
+    if (m - 0.5 <= rel * m || 1.0 - m <= rel * m) *scale_flag = 1;
+  }
+  const int x = mx_shared_exponent(amax);
+  for (int i = 0; i < n; ++i) {
+    diff[i] = 0.0;
+    const double r = fabs(ldexp((double)hf[i], -x));
+    if (r == 0.0 || r >= 448.0) continue;
+    const int c = e4m3_encode((float)r) & 0x7f;
+    const double vc = e4m3_value((uint8_t)c);
+    if (r == vc) continue;
+    const int nb = r > vc ? c + 1 : c - 1;
+    if (nb < 0 || nb > 126) continue;
+    const double vn = e4m3_value((uint8_t)nb);
+    if (fabs(r - 0.5 * (vc + vn)) > rel * r) continue;
+    diff[i] = (hf[i] < 0 ? -1.0 : 1.0) * (vn - vc) * ldexp(1.0, x);
+  }
+}
+
+static double mx_weight(const uint8_t *q, const uint8_t *sc, int64_t row, int64_t col, int64_t K) {
+  return e4m3_tab[q[row * K + col]] * ldexp(1.0, (int)sc[row * (K / 32) + col / 32] - 127);
+}
+
 /* One NVFP4 block of 16: the activation rule used on both GEMM inputs of the
  * NVFP4 path (global scale 1): scale = E4M3(amax / 6), code_i =
  * E2M1(v_i / scale) with FP32 divisions, all-zero codes when the scale
@@ -452,6 +531,7 @@ static int experts_impl(const uint16_t *x, int64_t T, int32_t d, int32_t F,
                         const weights_t *W, const int64_t *tokens,
                         int64_t n_tokens, uint16_t *out, double *out_exact) {
   if (T < 0 || d <= 0 || F <= 0 || k <= 0 || (d % 16) || (F % 16)) return -1;
+  if (W->mx && ((d % 32) || (F % 32))) return -1;
   const int64_t n = tokens ? n_tokens : T;
   int err = 0;
   /* every referenced expert must have its weights */
@@ -463,6 +543,7 @@ static int experts_impl(const uint16_t *x, int64_t T, int32_t d, int32_t F,
       if (e < 0 || e >= E) { err = -1; break; }
       if (W->fp4   ? (!W->qg[e] || !W->qu[e] || !W->qd[e])
           : W->fp8 ? (!W->eg[e] || !W->eu[e] || !W->ed[e])
+          : W->mx  ? (!W->mg[e] || !W->mu[e] || !W->md[e])
                    : (!W->wg[e] || !W->wu[e] || !W->wd[e])) {
         err = -2;
         break;
@@ -500,6 +581,9 @@ static int experts_impl(const uint16_t *x, int64_t T, int32_t d, int32_t F,
         } else if (W->fp4 && W->act_quant) {
           for (int32_t j = 0; j < d; ++j) tmp[j] = (float)bf16_value(xr[j]);
           for (int32_t j = 0; j < d; j += 16) nvfp4_block_roundtrip(tmp + j, xin + j);
+        } else if (W->mx && W->act_quant) {
+          for (int32_t j = 0; j < d; ++j) tmp[j] = (float)bf16_value(xr[j]);
+          for (int32_t j = 0; j < d; j += 32) mx_block_quantize(tmp + j, 32, NULL, NULL, xin + j);
         } else {
           for (int32_t j = 0; j < d; ++j) xin[j] = bf16_value(xr[j]);
         }
@@ -522,6 +606,11 @@ static int experts_impl(const uint16_t *x, int64_t T, int32_t d, int32_t F,
               for (int32_t j = 0; j < d; ++j) {
                 ga += xin[j] * fp8_weight(W->eg[e], W->seg[e], f, j, d);
                 ua += xin[j] * fp8_weight(W->eu[e], W->seu[e], f, j, d);
+              }
+            } else if (W->mx) {
+              for (int32_t j = 0; j < d; ++j) {
+                ga += xin[j] * mx_weight(W->mg[e], W->smg[e], f, j, d);
+                ua += xin[j] * mx_weight(W->mu[e], W->smu[e], f, j, d);
               }
             } else {
               const uint16_t *gr = W->wg[e] + (int64_t)f * d;
@@ -552,6 +641,20 @@ static int experts_impl(const uint16_t *x, int64_t T, int32_t d, int32_t F,
                   slack[r] += fabs(wt * hdiff[tie_f[q]] * fp8_weight(W->ed[e], W->sed[e], r,
                                                                       tie_f[q], F));
             }
+          } else if (W->mx && W->act_quant) {
+            /* the FP32 product itself, per 32 along F */
+            for (int32_t f = 0; f < F; f += 32) mx_block_quantize(hf + f, 32, NULL, NULL, hin + f);
+            if (slack) {
+              int32_t n_tie = 0;
+              for (int32_t f = 0; f < F; f += 32)
+                mx_h_ties(hf + f, 32, W->tie_rel, hdiff + f, &scale_flag);
+              for (int32_t f = 0; f < F; ++f)
+                if (hdiff[f] != 0.0) tie_f[n_tie++] = f;
+              for (int32_t q = 0; q < n_tie; ++q)
+                for (int32_t r = 0; r < d; ++r)
+                  slack[r] += fabs(wt * hdiff[tie_f[q]] * mx_weight(W->md[e], W->smd[e], r,
+                                                                     tie_f[q], F));
+            }
           } else if (W->fp4 && W->act_quant == 2) {
             for (int32_t f = 0; f < F; ++f) hin[f] = f16_round_value((double)hf[f]);
           } else if (W->fp4 && W->act_quant) {
@@ -568,6 +671,9 @@ static int experts_impl(const uint16_t *x, int64_t T, int32_t d, int32_t F,
             } else if (W->fp8) {
               for (int32_t f = 0; f < F; ++f)
                 ya += hin[f] * fp8_weight(W->ed[e], W->sed[e], r, f, F);
+            } else if (W->mx) {
+              for (int32_t f = 0; f < F; ++f)
+                ya += hin[f] * mx_weight(W->md[e], W->smd[e], r, f, F);
             } else {
               const uint16_t *dr = W->wd[e] + (int64_t)r * F;
               for (int32_t f = 0; f < F; ++f) ya += hin[f] * bf16_value(dr[f]);
@@ -736,6 +842,47 @@ int oracle_fp8_quantize_rows(const uint16_t *x, int64_t n, int32_t cols, uint8_t
   return 0;
 }
 
+/* MXFP8 experts (the pages name MXFP8 beside FP8 as a precision Beam runs
+ * in: vLLM post, the SkyRL paragraphs, "MXFP8 RL are supported out of the
+ * box").  [reading] OCP MX format with E4M3 elements: each weight is exactly
+ * code x 2^(scale - 127), one E8M0 scale per 32 consecutive elements along
+ * K.  With act_quant != 0 both GEMM inputs are MX blocks too (mx_block_quantize):
+ * x per 32 along d from its BF16 values, and the FP32 SwiGLU product per 32
+ * along F as it is (the quantisation happens where h is produced, as in the
+ * NVFP4 path).  act_quant = 0 keeps BF16 activations exactly as in the BF16
+ * path.  With tie_slack / scale_tie given (act_quant != 0 only) the near
+ * ties of the h quantisation are reported as for the FP8 path. */
+int oracle_experts_mxfp8(const uint16_t *x, int64_t T, int32_t d, int32_t F,
+                         int32_t k, int32_t E, const int32_t *idx, const float *w,
+                         const uint8_t *const *qg, const uint8_t *const *sg,
+                         const uint8_t *const *qu, const uint8_t *const *su,
+                         const uint8_t *const *qd, const uint8_t *const *sd,
+                         int32_t act_quant, double tie_rel, const int64_t *tokens,
+                         int64_t n_tokens, uint16_t *out, double *out_exact, double *tie_slack,
+                         uint8_t *scale_tie) {
+  if ((tie_slack != NULL) != (scale_tie != NULL)) return -1;
+  if (tie_slack && (!act_quant || !(tie_rel >= 0.0))) return -1;
+  weights_t W;
+  memset(&W, 0, sizeof W);
+  W.mg = qg; W.smg = sg;
+  W.mu = qu; W.smu = su;
+  W.md = qd; W.smd = sd;
+  W.mx = 1;
+  W.act_quant = act_quant;
+  W.tie_rel = tie_rel;
+  W.tie_slack = tie_slack;
+  W.scale_tie = scale_tie;
+  return experts_impl(x, T, d, F, k, E, idx, w, &W, tokens, n_tokens, out, out_exact);
+}
+
+/* The MX activation rule on a row of n values (n % 32 == 0): E4M3 codes and
+ * one E8M0 scale code per 32. */
+int oracle_mx_quantize(const float *v, int64_t n, uint8_t *q, uint8_t *sc) {
+  if (n < 0 || n % 32) return -1;
+  for (int64_t b = 0; b < n / 32; ++b) mx_block_quantize(v + 32 * b, 32, sc + b, q + 32 * b, NULL);
+  return 0;
+}
+
 /* ------------------------------------------------------------------------ */
 /* The sublayer boundary after the MoE branch                                */
 /* ------------------------------------------------------------------------ */
@@ -785,6 +932,7 @@ int oracle_boundary(const uint16_t *m, const uint16_t *h, const uint16_t *g_post
 /* ------------------------------------------------------------------------ */
 double oracle_e2m1_value(uint8_t code) { return e2m1_value(code); }
 double oracle_e4m3_value(uint8_t code) { return e4m3_value(code); }
+double oracle_e8m0_value(uint8_t code) { return e8m0_value(code); }
 uint8_t oracle_e2m1_encode(float v) { return e2m1_encode(v); }
 uint8_t oracle_e4m3_encode(float v) { return e4m3_encode(v); }
 uint16_t oracle_bf16_round(float v) { return bf16_round(v); }

@@ -842,3 +842,170 @@ def test_fp8_near_tie_slack_matches_torch_restatement():
     assert n_ties > 0
     assert np.array_equal(flag, want_flag)
     assert np.allclose(slack, want.numpy(), rtol=1e-12, atol=1e-18)
+
+
+# ------------------------------------------------------------------ MXFP8
+def test_e8m0_all_256_codes_vs_torch():
+    ref = torch.arange(256, dtype=torch.int32).to(torch.uint8).view(torch.float8_e8m0fnu)
+    ref = ref.double().numpy()
+    for c in range(256):
+        v = oracle.e8m0_value(c)
+        assert (math.isnan(v) and math.isnan(ref[c])) or v == ref[c], (c, v, ref[c])
+
+
+def _mx_torch(v: torch.Tensor):
+    """The MX conversion restated with torch (OCP MX v1.0, E4M3 elements):
+    per 32 values X = floor(log2(amax)) - 8 from torch.frexp, clamped to
+    [-127, 127] (-127 for an all-zero block); elements by torch's
+    float8_e4m3fn cast of v * 2^-X after clamping to +-448.  Returns (codes,
+    scale codes, dequantised float64 values)."""
+    b = v.float().reshape(-1, 32)
+    amax = b.abs().amax(dim=1)
+    _, e = torch.frexp(amax)
+    x = torch.where(amax > 0, e - 1 - 8, torch.full_like(e, -127)).clamp(-127, 127)
+    q = torch.ldexp(b, -x.unsqueeze(1).float()).clamp(-448.0, 448.0).to(torch.float8_e4m3fn)
+    deq = q.double() * torch.ldexp(torch.ones_like(x, dtype=torch.float64), x.double()).unsqueeze(1)
+    return q.view(torch.uint8).reshape(-1), (x + 127).to(torch.uint8), deq.reshape(v.shape)
+
+
+def test_mx_activation_quantizer_vs_torch():
+    v = (RNG.standard_normal(32 * 600) * np.repeat(np.exp(RNG.uniform(-20, 12, 600)), 32))
+    v = v.astype(np.float32)
+    v[:32] = 0.0                                   # all-zero block
+    v[32:64] = 1.0
+    v[32] = 1.999                                  # 1.999 / 2^-8 = 511.7: saturates at 448
+    v[64:96] = np.float32(2.0 ** -140)             # below E8M0's range: X clamps to -127
+    q, sc = oracle.mx_quantize(v)
+    qr, scr, _ = _mx_torch(torch.from_numpy(v))
+    assert np.array_equal(sc, scr.numpy())
+    dec = np.array([oracle.e4m3_value(int(c)) for c in q])
+    decr = np.array([oracle.e4m3_value(int(c)) for c in qr.numpy()])
+    assert np.array_equal(dec, decr)
+    assert sc[1] == 127 - 8 and dec[32] == 448.0
+    assert sc[2] == 0
+
+
+def test_mxfp8_generator_weights_round_trip_grid_values():
+    """Weights already on an MXFP8 grid (E4M3 values times a power of two per
+    32, each block reaching 448) come back unchanged from the generator's
+    quantiser."""
+    n, kk = 6, 128
+    codes = RNG.integers(0, 127, (n, kk)) | (RNG.integers(0, 2, (n, kk)) << 7)
+    vals = np.vectorize(oracle.e4m3_value)(codes)
+    vals[:, ::32] = 448.0
+    scale = 2.0 ** RNG.integers(-20, -5, (n, kk // 32))
+    w = torch.from_numpy(vals * np.repeat(scale, 32, axis=1)).float()
+    q, s = inputs.quantize_mxfp8_weight(w)
+    back = np.vectorize(oracle.e4m3_value)(q.numpy()) * np.repeat(
+        np.vectorize(oracle.e8m0_value)(s.numpy()), 32, axis=1)
+    assert np.array_equal(back, w.double().numpy())
+
+
+def _mx_weights(E, n, kk):
+    codes = (RNG.integers(0, 127, (E, n, kk)) | (RNG.integers(0, 2, (E, n, kk)) << 7))
+    codes = codes.astype(np.uint8)
+    sc = RNG.integers(127 - 14, 127 - 8, (E, n, kk // 32)).astype(np.uint8)
+    deq = np.vectorize(oracle.e4m3_value)(codes) * np.repeat(
+        np.ldexp(1.0, sc.astype(np.int64) - 127), 32, axis=2)
+    return {"q": codes, "s": sc}, torch.from_numpy(deq)
+
+
+def test_mxfp8_weights_equal_bf16_when_exactly_representable():
+    """E4M3 values (4 significant bits) times a power of two are BF16 values,
+    so with BF16 activations the MXFP8 and BF16 oracle paths agree bit for
+    bit: this pins the weight decoding (codes and per-32 scales)."""
+    T, d, F, E = 6, 64, 64, 8
+    x = _bf16_matrix((T, d))
+    r = _route(RNG.standard_normal((T, E)), np.zeros(E), 4, 2, 3)
+    proj, deq = {}, {}
+    for name, (n, kk) in (("g", (F, d)), ("u", (F, d)), ("d", (d, F))):
+        proj[name], full = _mx_weights(E, n, kk)
+        t = full.to(torch.bfloat16)
+        assert torch.equal(t.double(), full)
+        deq[name] = inputs.bf16_bits(t)
+    a = oracle.experts_mxfp8(inputs.bf16_bits(x), r["idx"], r["w"], proj["g"], proj["u"],
+                             proj["d"], E, act_quant=False)
+    b = oracle.experts_bf16(inputs.bf16_bits(x), r["idx"], r["w"], deq["g"], deq["u"], deq["d"], E)
+    assert np.array_equal(a, b)
+
+
+def test_mxfp8_activation_experts_match_dense_torch():
+    """MXFP8 weights and MX activations: the expert layer against a dense
+    torch FP64 restatement that quantises x (from BF16) and the FP32 SwiGLU
+    product (no BF16 rounding first) with _mx_torch.  Planting a BF16
+    rounding of h, or E4M3's largest exponent 7 instead of 8, fails it."""
+    T, d, F, E = 5, 64, 64, 8
+    x = _bf16_matrix((T, d))
+    r = _route(RNG.standard_normal((T, E)), np.zeros(E), 4, 2, 3)
+    proj, deq = {}, {}
+    for name, (n, kk) in (("g", (F, d)), ("u", (F, d)), ("d", (d, F))):
+        proj[name], deq[name] = _mx_weights(E, n, kk)
+    out, ex = oracle.experts_mxfp8(inputs.bf16_bits(x), r["idx"], r["w"], proj["g"], proj["u"],
+                                   proj["d"], E, act_quant=True, exact=True)
+    xq = _mx_torch(x.float().reshape(-1))[2].reshape(T, d)
+    ref = torch.zeros(T, d, dtype=torch.float64)
+    for t in range(T):
+        for j in range(3):
+            e = int(r["idx"][t, j])
+            g = (xq[t] @ deq["g"][e].T).float().double()
+            u = (xq[t] @ deq["u"][e].T).float().double()
+            hq = _mx_torch((g / (1 + torch.exp(-g)) * u).float())[2]
+            ref[t] += float(r["w"][t, j]) * (hq @ deq["d"][e].T)
+    assert np.allclose(ex, ref.numpy(), rtol=1e-12, atol=1e-12)
+    assert np.array_equal(out, bf16_nearest(ref.numpy()))
+
+
+def test_mxfp8_near_tie_slack_matches_torch_restatement():
+    """The MX h near ties restated with torch: an element whose scaled FP32
+    value lies within rel of the midpoint between its E4M3 value and the next
+    one on its side adds |w * (value change) * W_d[., f]| to its token's
+    outputs; a block whose amax lies within rel of a power of two flags the
+    token."""
+    T, d, F, E = 5, 64, 64, 8
+    rel = 2.0 ** -8
+    x = _bf16_matrix((T, d))
+    r = _route(RNG.standard_normal((T, E)), np.zeros(E), 4, 2, 3)
+    proj, deq = {}, {}
+    for name, (n, kk) in (("g", (F, d)), ("u", (F, d)), ("d", (d, F))):
+        proj[name], deq[name] = _mx_weights(E, n, kk)
+    out, ex, slack, flag = oracle.experts_mxfp8(inputs.bf16_bits(x), r["idx"], r["w"], proj["g"],
+                                                proj["u"], proj["d"], E, act_quant=True,
+                                                ties=True, tie_rel=rel)
+    mags = torch.tensor([oracle.e4m3_value(c) for c in range(127)], dtype=torch.float64)
+    xq = _mx_torch(x.float().reshape(-1))[2].reshape(T, d)
+    want = torch.zeros(T, d, dtype=torch.float64)
+    want_flag = np.zeros(T, bool)
+    n_ties = 0
+    for t in range(T):
+        for j in range(3):
+            e = int(r["idx"][t, j])
+            g = (xq[t] @ deq["g"][e].T).float().double()
+            u = (xq[t] @ deq["u"][e].T).float().double()
+            hf = (g / (1 + torch.exp(-g)) * u).float()
+            codes, sc, _ = _mx_torch(hf)
+            for b in range(F // 32):
+                blk = hf[32 * b:32 * (b + 1)].double()
+                amax = float(blk.abs().max())
+                m, _ = math.frexp(amax)
+                if amax > 0 and (m - 0.5 <= rel * m or 1.0 - m <= rel * m):
+                    want_flag[t] = True
+                xs = 2.0 ** (int(sc[b]) - 127)
+                for i in range(32):
+                    f = 32 * b + i
+                    rr = abs(float(blk[i])) / xs
+                    c = int(codes[f]) & 0x7F
+                    vc = float(mags[c])
+                    if rr == 0 or rr >= 448 or rr == vc:
+                        continue
+                    nb = c + 1 if rr > vc else c - 1
+                    if not 0 <= nb <= 126:
+                        continue
+                    vn = float(mags[nb])
+                    if abs(rr - (vc + vn) / 2) <= rel * rr:
+                        n_ties += 1
+                        sgn = -1.0 if float(blk[i]) < 0 else 1.0
+                        want[t] += (float(r["w"][t, j]) * sgn * (vn - vc) * xs
+                                    * deq["d"][e][:, f]).abs()
+    assert n_ties > 0
+    assert np.array_equal(flag, want_flag)
+    assert np.allclose(slack, want.numpy(), rtol=1e-12, atol=1e-18)
