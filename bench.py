@@ -9,8 +9,8 @@ GEMM, down GEMM, combine) on one batch of the workload, with every
 input resident in device memory.  Metric: layer tokens/s.  The headline is
 --config (the decode batch by default); the default run also measures the
 prefill chunk, the skewed routing, the NVFP4 batch (quantised and 16-bit
-activations) and the dynamic FP8 decode and prefill batches in the same
-process with the same steps, each as a record under "workloads" (a summary
+activations), the dynamic FP8 decode and prefill batches and the MXFP8
+decode batch in the same process with the same steps, each as a record under "workloads" (a summary
 of each also under "roofline").  The expert weights
 a step touches (about 12 GB for the decode batch) are far larger than L2, so
 no flush is needed between steps.  Timing: CUDA events on the launching
@@ -50,7 +50,7 @@ STAGES = ["router", "select", "permute", "gather", "gate_up", "down", "combine"]
 # the dominant kernel of each expert format (its gate/up GEMM) and the source
 # files that define it; a stored traffic counter holds while they are unchanged
 DOMINANT = {"bf16": "gate_up", "nvfp4": "fp4_gate_up", "a16": "w4a16_gate_up",
-            "fp8": "fp8_gate_up"}
+            "fp8": "fp8_gate_up", "mxfp8": "mx_gate_up"}
 DOMINANT_SRC = {k: [os.path.join(ROOT, "group_limited_routed_gb300", "csrc", f) for f in v]
                 for k, v in {
                     "gate_up": ("expert_gemm_kernel.cuh", "expert_gemm.cuh", "gemm_common.cuh",
@@ -59,6 +59,7 @@ DOMINANT_SRC = {k: [os.path.join(ROOT, "group_limited_routed_gb300", "csrc", f) 
                     "w4a16_gate_up": ("w4a16.cu", "gemm_common.cuh", "common.cuh", "ptx.cuh"),
                     "fp8_gate_up": ("expert_gemm_kernel.cuh", "expert_gemm.cuh",
                                     "gemm_common.cuh", "common.cuh", "ptx.cuh"),
+                    "mx_gate_up": ("nvfp4.cu", "gemm_common.cuh", "common.cuh", "ptx.cuh"),
                 }.items()}
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 
@@ -192,7 +193,7 @@ def oracle_sample(cfg, t, n_tokens: int, seed: int = 0, a16: bool = False):
         proj = [{"q": {e: p["q"][e].cpu().numpy() for e in need},
                  "sf": {e: p["sf"][e].cpu().numpy() for e in need},
                  "gs": p["gs"].cpu().numpy()} for p in (t["w_gate"], t["w_up"], t["w_down"])]
-    elif cfg.weight_fmt == "fp8":
+    elif cfg.weight_fmt in ("fp8", "mxfp8"):
         proj = [{"q": {e: p["q"][e].cpu().numpy() for e in need},
                  "s": {e: p["s"][e].cpu().numpy() for e in need}}
                 for p in (t["w_gate"], t["w_up"], t["w_down"])]
@@ -206,6 +207,8 @@ def oracle_sample(cfg, t, n_tokens: int, seed: int = 0, a16: bool = False):
                              act_quant=oracle.ACT_F16 if a16 else oracle.ACT_NVFP4)
     elif cfg.weight_fmt == "fp8":
         oracle.experts_fp8(x[rows], r["idx"], r["w"], *proj, cfg.n_experts, act_quant=True)
+    elif cfg.weight_fmt == "mxfp8":
+        oracle.experts_mxfp8(x[rows], r["idx"], r["w"], *proj, cfg.n_experts, act_quant=True)
     else:
         oracle.experts_bf16(x[rows], r["idx"], r["w"], *proj, cfg.n_experts)
     return time.perf_counter() - t0, len(rows)
@@ -300,7 +303,7 @@ def config_record(cfg, touched, routed=False, a16=False, graph=False):
 
 # Nominal dense tensor rate of each expert format relative to BF16 on GB300
 # (2.25 PFLOP/s BF16, 4.5 FP8, 13.5 FP4); W4A16 multiplies in F16.
-TC_RATIO = {"bf16": 1.0, "fp8": 2.0, "nvfp4": 6.0, "a16": 1.0}
+TC_RATIO = {"bf16": 1.0, "fp8": 2.0, "nvfp4": 6.0, "a16": 1.0, "mxfp8": 2.0}
 NOMINAL_HBM_GBS = 7900.0
 
 
@@ -348,9 +351,11 @@ def measure(cfg, args, dev, rank, world, use_dist, *, a16=False, routed=False, g
     t = inputs.generate(cfg.replace(seed=cfg.seed + 1000 * rank) if rank else cfg, dev)
     fp4 = cfg.weight_fmt == "nvfp4"
     fp8 = cfg.weight_fmt == "fp8"
+    mx = cfg.weight_fmt == "mxfp8"
     a16 = fp4 and a16
-    fmt_name = ("a16" if a16 else "nvfp4") if fp4 else "fp8" if fp8 else "bf16"
-    fmt = (pkg.NVFP4_A16 if a16 else pkg.NVFP4) if fp4 else pkg.FP8 if fp8 else 0
+    fmt_name = ("a16" if a16 else "nvfp4") if fp4 else "fp8" if fp8 else "mxfp8" if mx else "bf16"
+    fmt = ((pkg.NVFP4_A16 if a16 else pkg.NVFP4) if fp4 else pkg.FP8 if fp8
+           else pkg.MXFP8 if mx else 0)
     ws = pkg.Workspace(cfg, cfg.T, dev, weight_fmt=fmt)
     stream = torch.cuda.current_stream()
     out = torch.empty(cfg.T, cfg.d, dtype=torch.bfloat16, device=dev)
@@ -368,6 +373,12 @@ def measure(cfg, args, dev, rank, world, use_dist, *, a16=False, routed=False, g
         def layer(x, o):
             return pkg.forward_fp8(cfg, x, t["router_w"], t["corr_bias"], *wts, out=o, ws=ws,
                                    stream=torch.cuda.current_stream())
+    elif mx:
+        wts = [pkg.Mxfp8Weight.of(t[n]) for n in ("w_gate", "w_up", "w_down")]
+
+        def layer(x, o):
+            return pkg.forward_mxfp8(cfg, x, t["router_w"], t["corr_bias"], *wts, out=o, ws=ws,
+                                     stream=torch.cuda.current_stream())
     elif routed:
         # routing replay: the routes are recorded once, the timed steps run
         # the experts and the combine on them
@@ -488,15 +499,17 @@ def measure(cfg, args, dev, rank, world, use_dist, *, a16=False, routed=False, g
     T, d, F, E, k = cfg.T, cfg.d, cfg.d_ff, cfg.n_experts, cfg.topk
     TK = T * k
     # weight bytes of one projection of one expert: BF16, E2M1 + E4M3 per 16,
-    # or E4M3 + one FP32 scale per output row
-    E_b = d * F // 2 + d * F // 16 if fp4 else d * F if fp8 else d * F * 2
+    # E4M3 + one FP32 scale per output row, or E4M3 + E8M0 per 32
+    E_b = (d * F // 2 + d * F // 16 if fp4 else d * F if fp8 else d * F + d * F // 32 if mx
+           else d * F * 2)
     gu_w = touched * 2 * (E_b + (4 * F if fp8 else 0))
     dn_w = touched * (E_b + (4 * d if fp8 else 0))
     hidden_b = T * d * 2
     # the implementation's own buffers (not algorithmic bytes): token rows in
     # expert order, h, the FP32 expert rows y
-    x_row = d * (0.5625 if fp4 and not a16 else 1 if fp8 else 2)
-    h_row = F * (0.5625 if fp4 and not a16 else 2)
+    # (MXFP8: a byte per element and a 16-byte scale slot per 128)
+    x_row = d * (0.5625 if fp4 and not a16 else 1 if fp8 else 1.125 if mx else 2)
+    h_row = F * (0.5625 if fp4 and not a16 else 1.125 if mx else 2)
     small = TK <= 4 * E
     gu_inter = {"token_rows_read": TK * x_row, "h_written": TK * h_row}
     if fp8:
@@ -531,7 +544,7 @@ def measure(cfg, args, dev, rank, world, use_dist, *, a16=False, routed=False, g
         "roofline_frac": max(layer_bytes / (pk["hbm_gbs"] * 1e9),
                              layer_flops / (sus * 1e12)) / lsec,
         "intermediate_bytes": {
-            "scatter": 0 if small or fp4 else int(T * x_row + TK * x_row),
+            "scatter": 0 if small or fp4 or mx else int(T * x_row + TK * x_row),
             "gate_up": int(sum(gu_inter.values())), "down": int(sum(dn_inter.values())),
             "combine": int(TK * d * 4 + T * d * 2)}}
     gu = kernels["gate_up"]
@@ -546,7 +559,8 @@ def measure(cfg, args, dev, rank, world, use_dist, *, a16=False, routed=False, g
     rec = {
         "value": value, "unit": UNIT, "ms_per_step": layer_ms,
         "dtype": ("nvfp4 weights x f16 activations" if a16 else "nvfp4 (e2m1 x e4m3 per 16)")
-        if fp4 else "fp8 (e4m3, fp32 scale per row)" if fp8 else "bf16",
+        if fp4 else "fp8 (e4m3, fp32 scale per row)" if fp8
+        else "mxfp8 (e4m3 x e8m0 per 32)" if mx else "bf16",
         "config": config_record(cfg, touched, routed, a16, graph),
         "roofline": roofline, "kernels": kernels, "layer_roofline": layer_roof,
         "stage_us": {n: round(float(v) * 1e3, 1) for n, v in zip(STAGES, stage_ms)},
@@ -572,9 +586,10 @@ def dist_barrier():
 
 # The workloads measured beside the headline in the default run: the
 # prefill chunk and skewed routing (BF16), the NVFP4 batch with quantised
-# and with 16-bit activations, and the dynamic FP8 decode and prefill.
+# and with 16-bit activations, the dynamic FP8 decode and prefill, and the
+# MXFP8 decode batch.
 SUB_WORKLOADS = [("prefill", False), ("skewed", False), ("nvfp4", False), ("nvfp4", True),
-                 ("fp8", False), ("fp8_prefill", False)]
+                 ("fp8", False), ("fp8_prefill", False), ("mxfp8", False)]
 
 
 def summary(name, rec):

@@ -17,7 +17,8 @@ def __getattr__(name):
                 "forward_nvfp4", "pack_scales", "Fp4Weight", "NVFP4", "ep_dispatch",
                 "ep_experts", "ep_combine", "EpWorkspace", "forward_boundary",
                 "forward_nvfp4_a16", "NVFP4_A16", "ep_experts_nvfp4", "forward_fp8",
-                "Fp8Weight", "FP8", "fp8_quantize_rows", "ep_experts_fp8", "BF16"):
+                "Fp8Weight", "FP8", "fp8_quantize_rows", "ep_experts_fp8", "BF16",
+                "forward_mxfp8", "Mxfp8Weight", "MXFP8"):
         from . import api
         return getattr(api, name)
     raise AttributeError(name)

@@ -37,7 +37,8 @@ EXPORTS = ("beam_moe_workspace_size", "beam_moe_workspace_layout", "beam_moe_rou
            "beam_moe_forward_boundary", "beam_moe_forward_nvfp4_a16",
            "beam_moe_ep_experts_nvfp4", "beam_moe_forward_fp8", "beam_moe_fp8_quantize_rows",
            "beam_moe_ep_experts_fp8", "beam_moe_forward_nvfp4_boundary",
-           "beam_moe_forward_nvfp4_a16_boundary", "beam_moe_forward_fp8_boundary")
+           "beam_moe_forward_nvfp4_a16_boundary", "beam_moe_forward_fp8_boundary",
+           "beam_moe_forward_mxfp8", "beam_moe_forward_mxfp8_boundary")
 
 
 class BeamError(RuntimeError):
@@ -65,6 +66,10 @@ class _Fp4Weight(ctypes.Structure):
 
 class _Fp8Weight(ctypes.Structure):
     _fields_ = [("q", ctypes.c_void_p), ("scale", ctypes.c_void_p)]
+
+
+class _Mxfp8Weight(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("sf", ctypes.c_void_p)]
 
 
 def library_path() -> str:
@@ -108,6 +113,10 @@ def lib():
         L.beam_moe_forward_fp8.argtypes = [cfgp, _P, _P, _P, fp8p, fp8p, fp8p, _P, _I64, _P,
                                            _SZ, _P]
         L.beam_moe_forward_fp8.restype = _ST
+        mxp = ctypes.POINTER(_Mxfp8Weight)
+        L.beam_moe_forward_mxfp8.argtypes = [cfgp, _P, _P, _P, mxp, mxp, mxp, _P, _I64, _P,
+                                             _SZ, _P]
+        L.beam_moe_forward_mxfp8.restype = _ST
         L.beam_moe_fp8_quantize_rows.argtypes = [_P, _I64, ctypes.c_int32, _P, _P, _P]
         L.beam_moe_ep_experts_fp8.argtypes = [cfgp, ctypes.c_int32, ctypes.c_int32, _P, _P, _P,
                                               fp8p, fp8p, fp8p, _P, _I64, _P, _SZ, _P]
@@ -128,7 +137,8 @@ def lib():
         L.beam_moe_forward_boundary.restype = _ST
         for name, wp in (("beam_moe_forward_nvfp4_boundary", fp4p),
                          ("beam_moe_forward_nvfp4_a16_boundary", fp4p),
-                         ("beam_moe_forward_fp8_boundary", fp8p)):
+                         ("beam_moe_forward_fp8_boundary", fp8p),
+                         ("beam_moe_forward_mxfp8_boundary", mxp)):
             f = getattr(L, name)
             f.argtypes = [cfgp, _P, _P, _P, wp, wp, wp, _P, _I64, ctypes.POINTER(_Boundary), _P,
                           _SZ, _P]
@@ -290,7 +300,8 @@ def forward_boundary(cfg, hidden, router_w, corr_bias, w_gate, w_up, w_down, res
     (out, next_input); ``residual`` is overwritten with the new stream.
 
     The expert format follows the weights: BF16 tensors, ``Fp4Weight`` (NVFP4
-    activations, or F16 ones with ``a16=True``) or ``Fp8Weight``."""
+    activations, or F16 ones with ``a16=True``), ``Fp8Weight`` or
+    ``Mxfp8Weight``."""
     T = hidden.shape[0]
     dev = hidden.device
     if isinstance(w_gate, Fp4Weight):
@@ -299,6 +310,9 @@ def forward_boundary(cfg, hidden, router_w, corr_bias, w_gate, w_up, w_down, res
         wts = tuple(ctypes.byref(x._c) for x in (w_gate, w_up, w_down))
     elif isinstance(w_gate, Fp8Weight):
         fmt, name = FP8, "beam_moe_forward_fp8_boundary"
+        wts = tuple(ctypes.byref(x._c) for x in (w_gate, w_up, w_down))
+    elif isinstance(w_gate, Mxfp8Weight):
+        fmt, name = MXFP8, "beam_moe_forward_mxfp8_boundary"
         wts = tuple(ctypes.byref(x._c) for x in (w_gate, w_up, w_down))
     else:
         fmt, name = BF16, "beam_moe_forward_boundary"
@@ -364,8 +378,9 @@ NVFP4_A16 = 2
 
 
 def pack_scales(sf: torch.Tensor, stream=None) -> torch.Tensor:
-    """E4M3 block scales [..., rows, S] (uint8, row-major) -> the blocked order
-    the tensor cores take (beam_moe_nvfp4_pack_scales); same shape and dtype."""
+    """Block scales [..., rows, S] (uint8, row-major: E4M3 for NVFP4, E8M0 for
+    MXFP8) -> the blocked order the tensor cores take
+    (beam_moe_nvfp4_pack_scales); same shape and dtype."""
     src = sf.contiguous()
     S = src.shape[-1]
     rows = src.numel() // S
@@ -460,6 +475,41 @@ def forward_fp8(cfg, hidden, router_w, corr_bias, gate: Fp8Weight, up: Fp8Weight
                                       ctypes.byref(gate._c), ctypes.byref(up._c),
                                       ctypes.byref(down._c), o.data_ptr(), T, ws.ptr, ws.nbytes,
                                       _stream(stream)), "beam_moe_forward_fp8")
+    return o
+
+
+MXFP8 = 4
+
+
+class Mxfp8Weight:
+    """One MXFP8 projection: E4M3 codes q [E, N, K] (uint8) and E8M0 scales,
+    one per 32 along K, given row-major [E, N, K/32] and kept in the blocked
+    order the tensor cores take (beam_moe_nvfp4_pack_scales)."""
+
+    def __init__(self, q: torch.Tensor, sf_rowmajor: torch.Tensor, stream=None):
+        self.q = q.contiguous()
+        self.sf = pack_scales(sf_rowmajor, stream)
+        self._c = _Mxfp8Weight(_dev(self.q, torch.uint8, "q"), self.sf.data_ptr())
+
+    @classmethod
+    def of(cls, d: dict, stream=None) -> "Mxfp8Weight":
+        return cls(d["q"], d["s"], stream)
+
+
+def forward_mxfp8(cfg, hidden, router_w, corr_bias, gate: Mxfp8Weight, up: Mxfp8Weight,
+                  down: Mxfp8Weight, out=None, ws: Workspace | None = None, stream=None):
+    """The whole layer with MXFP8 experts (activations quantised to MX blocks)."""
+    T = hidden.shape[0]
+    if ws is None:
+        ws = Workspace(cfg, max(int(T), 1), hidden.device, weight_fmt=MXFP8)
+    o = torch.empty(T, cfg.d, dtype=torch.bfloat16, device=hidden.device) if out is None else out
+    c = _cfg(cfg)
+    _check(lib().beam_moe_forward_mxfp8(ctypes.byref(c), _dev(hidden, torch.bfloat16, "hidden"),
+                                        _dev(router_w, torch.float32, "router_w"),
+                                        _dev(corr_bias, torch.float32, "corr_bias"),
+                                        ctypes.byref(gate._c), ctypes.byref(up._c),
+                                        ctypes.byref(down._c), o.data_ptr(), T, ws.ptr, ws.nbytes,
+                                        _stream(stream)), "beam_moe_forward_mxfp8")
     return o
 
 

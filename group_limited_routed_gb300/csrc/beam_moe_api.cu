@@ -161,7 +161,7 @@ struct Layout {
 
 bool known_fmt(int32_t fmt) {
   return fmt == BEAM_WEIGHTS_BF16 || fmt == BEAM_WEIGHTS_NVFP4 || fmt == BEAM_WEIGHTS_NVFP4_A16 ||
-         fmt == BEAM_WEIGHTS_FP8;
+         fmt == BEAM_WEIGHTS_FP8 || fmt == BEAM_WEIGHTS_MXFP8;
 }
 
 // NVFP4 token-block width: the token scales are read row-major, 32 rows at most
@@ -171,6 +171,7 @@ Layout make_layout(const beam_moe_config_t& c, int64_t T_max, int32_t fmt = BEAM
   const bool fp4 = fmt == BEAM_WEIGHTS_NVFP4;
   const bool a16 = fmt == BEAM_WEIGHTS_NVFP4_A16;  // F16 token rows gathered into x_perm
   const bool fp8 = fmt == BEAM_WEIGHTS_FP8;         // E4M3 token rows (gathered when large)
+  const bool mx = fmt == BEAM_WEIGHTS_MXFP8;        // MX token rows and h (codes + scales)
   const int64_t E = c.n_experts, k = c.topk;
   const int64_t TK = T_max * k;
   const int64_t rows = std::max<int64_t>(TK, kMinRows);
@@ -202,14 +203,18 @@ Layout make_layout(const beam_moe_config_t& c, int64_t T_max, int32_t fmt = BEAM
   // gathered token rows: F16 (W4A16), E4M3 (FP8) or BF16, the last two only
   // for batches that do not gather inside the gate/up GEMM
   const size_t xrow = static_cast<size_t>(rows) * c.d;
-  L.x_perm = take(a16 ? xrow * 2 : fp4 || small_batch(c, TK) ? 0 : fp8 ? xrow : xrow * 2);
-  L.h = take(fp4 ? 0 : static_cast<size_t>(rows) * c.d_ff * 2);
+  L.x_perm = take(a16 ? xrow * 2 : fp4 || mx || small_batch(c, TK) ? 0 : fp8 ? xrow : xrow * 2);
+  L.h = take(fp4 || mx ? 0 : static_cast<size_t>(rows) * c.d_ff * 2);
   L.y = take(static_cast<size_t>(rows) * c.d * 4);
   L.router_planes = take(T_max >= kTensorRouterMinT ? static_cast<size_t>(E) * 3 * c.d * 2 : 0);
-  L.x_fp4 = take(fp4 ? static_cast<size_t>(rows) * c.d / 2 : 0);
-  L.x_sf = take(fp4 ? static_cast<size_t>(rows) * c.d / 4 : 0);
-  L.h_fp4 = take(fp4 ? static_cast<size_t>(rows) * c.d_ff / 2 : 0);
-  L.h_sf = take(fp4 ? static_cast<size_t>(rows) * c.d_ff / 4 : 0);
+  // block-scaled token rows and h: NVFP4 codes (half a byte) and a scale slot
+  // per 64 elements, or MXFP8 codes (a byte) and a scale slot per 128
+  L.x_fp4 = take(fp4 ? static_cast<size_t>(rows) * c.d / 2 : mx ? xrow : 0);
+  L.x_sf = take(fp4 ? static_cast<size_t>(rows) * c.d / 4 : mx ? xrow / 8 : 0);
+  L.h_fp4 = take(fp4 ? static_cast<size_t>(rows) * c.d_ff / 2
+                     : mx ? static_cast<size_t>(rows) * c.d_ff : 0);
+  L.h_sf = take(fp4 ? static_cast<size_t>(rows) * c.d_ff / 4
+                    : mx ? static_cast<size_t>(rows) * c.d_ff / 8 : 0);
   L.x_fp8 = take(fp8 ? static_cast<size_t>(T_max) * c.d : 0);
   L.x_scale = take(fp8 ? static_cast<size_t>(T_max) * 4 : 0);
   L.h_fp8 = take(fp8 ? static_cast<size_t>(rows) * c.d_ff : 0);
@@ -247,6 +252,8 @@ beam_status_t common_checks(const beam_moe_config_t* cfg, int64_t T, void* ws, s
   if (!valid_cfg(cfg) || T < 0 || T > (int64_t(1) << 31) / 64) return BEAM_ERR_INVALID_ARG;
   if ((fmt == BEAM_WEIGHTS_NVFP4 || fmt == BEAM_WEIGHTS_NVFP4_A16) && (cfg->d % 256 || cfg->d_ff % 256))
     return BEAM_ERR_INVALID_ARG;
+  // the MXFP8 down GEMM takes its weight rows in pairs of 128-row blocks
+  if (fmt == BEAM_WEIGHTS_MXFP8 && cfg->d % 256) return BEAM_ERR_INVALID_ARG;
   *empty = (T == 0);
   if (*empty) return BEAM_OK;
   if (!aligned16(ws)) return BEAM_ERR_INVALID_ARG;
@@ -554,6 +561,84 @@ beam_status_t run_experts_nvfp4(const beam_moe_config_t& c, const void* hidden, 
   return cuda_status(cudaGetLastError());
 }
 
+// permute + MX token rows + MXFP8 gate/up (quantising h to MX) + MXFP8 down
+// + combine
+beam_status_t run_experts_mxfp8(const beam_moe_config_t& c, const void* hidden, const int32_t* idx,
+                                const float* w, const beam_mxfp8_weight_t& gate,
+                                const beam_mxfp8_weight_t& up, const beam_mxfp8_weight_t& down,
+                                void* out, int64_t T, void* ws, const Layout& L,
+                                const DevInfo& dev, cudaStream_t s, bool permuted = false,
+                                const beam::BoundaryArgs* boundary = nullptr) {
+  const int64_t TK = T * c.topk;
+  const int64_t rows = std::max<int64_t>(TK, kMinRows);
+  const int nt = fp4_tile(c, TK);
+  const beam::PermuteArgs pa = permute_args(c, idx, w, T, ws, L);
+  if (!permuted) {
+    if (launch_permutation(pa, ws, L, dev, s) != BEAM_OK) return BEAM_ERR_CUDA;
+    record(3, s);
+  }
+  uint8_t* xq = at<uint8_t>(ws, L.x_fp4);
+  uint8_t* xsf = at<uint8_t>(ws, L.x_sf);
+  uint8_t* hq = at<uint8_t>(ws, L.h_fp4);
+  uint8_t* hsf = at<uint8_t>(ws, L.h_sf);
+  float* y = at<float>(ws, L.y);
+  beam::launch_quantize_tokens_mx(static_cast<const uint16_t*>(hidden), pa.pair_row, T, c.topk,
+                                  c.d, xq, xsf, s);
+  record(4, s);
+  if (cudaGetLastError() != cudaSuccess) return BEAM_ERR_CUDA;
+
+  const int64_t EF = static_cast<int64_t>(c.n_experts) * c.d_ff;
+  const int64_t ED = static_cast<int64_t>(c.n_experts) * c.d;
+  CUtensorMap tm_g, tm_u, tm_d, tm_x, tm_xsf, tm_h, tm_hsf;
+  if (!tmap_u8(&tm_g, gate.q, EF, c.d, 128, 128) || !tmap_u8(&tm_u, up.q, EF, c.d, 128, 128) ||
+      !tmap_u8(&tm_d, down.q, ED, c.d_ff, 128, 128) || !tmap_u8(&tm_x, xq, rows, c.d, 128, nt) ||
+      !tmap_u8(&tm_xsf, xsf, rows, c.d / 8, 16, 32) ||
+      !tmap_u8(&tm_h, hq, rows, c.d_ff, 128, nt) ||
+      !tmap_u8(&tm_hsf, hsf, rows, c.d_ff / 8, 16, 32))
+    return BEAM_ERR_CUDA;
+  beam::Fp4GemmArgs fa{};
+  fa.counts = pa.counts;
+  fa.offsets = pa.offsets;
+  fa.perm_w = pa.perm_w;
+  fa.E = c.n_experts;
+  fa.status = at<uint32_t>(ws, L.status);
+  fa.wait_limit_ns = g_wait_ns;
+  fa.weight_evict_first = small_batch(c, TK) ? 1 : 0;
+  auto grid_for = [&](int m_blocks) {
+    const int64_t tiles = static_cast<int64_t>(m_blocks) * (c.n_experts + (TK + nt - 1) / nt);
+    return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(dev.sms, tiles)));
+  };
+  fa.sfa0 = gate.sf;
+  fa.sfa1 = up.sf;
+  fa.hq = hq;
+  fa.hsf = hsf;
+  fa.out_ld = c.d_ff;
+  fa.rows_per_expert = c.d_ff;
+  fa.m_blocks = c.d_ff / 128;
+  fa.k_blocks = c.d / 128;
+  if (beam::launch_mxfp8_gemm(true, nt, tm_g, tm_u, tm_x, tm_xsf, fa, grid_for(fa.m_blocks), s) !=
+      cudaSuccess)
+    return BEAM_ERR_CUDA;
+  record(5, s);
+  fa.sfa0 = down.sf;
+  fa.sfa1 = nullptr;
+  fa.hq = nullptr;
+  fa.hsf = nullptr;
+  fa.y = y;
+  fa.out_ld = c.d;
+  fa.rows_per_expert = c.d;
+  fa.m_blocks = c.d / 256;  // pairs of 128-row weight blocks
+  fa.k_blocks = c.d_ff / 128;
+  if (beam::launch_mxfp8_gemm(false, nt, tm_d, tm_d, tm_h, tm_hsf, fa, grid_for(fa.m_blocks), s) !=
+      cudaSuccess)
+    return BEAM_ERR_CUDA;
+  record(6, s);
+  if (finish_combine(c, y, pa.pair_row, T, out, nullptr, boundary, s) != cudaSuccess)
+    return BEAM_ERR_CUDA;
+  record(7, s);
+  return cuda_status(cudaGetLastError());
+}
+
 // permute + E4M3 token rows (+ gather) + FP8 gate/up (BF16 h) + E4M3 h rows
 // + FP8 down + combine.  With y_pairs given, the down GEMM writes each
 // pair's weighted FP32 row there (pair order) and there is no combine; idx
@@ -737,6 +822,10 @@ bool valid_fp4_weight(const beam_fp4_weight_t* w) {
 
 bool valid_fp8_weight(const beam_fp8_weight_t* w) {
   return w && aligned16(w->q) && aligned16(w->scale);
+}
+
+bool valid_mxfp8_weight(const beam_mxfp8_weight_t* w) {
+  return w && aligned16(w->q) && aligned16(w->sf);
 }
 
 // The boundary's own argument checks that need no pointer (they come before
@@ -1060,6 +1149,33 @@ beam_status_t beam_moe_forward_fp8_boundary(const beam_moe_config_t* cfg, const 
       });
 }
 
+beam_status_t beam_moe_forward_mxfp8(const beam_moe_config_t* cfg, const void* hidden,
+                                     const float* router_w, const float* corr_bias,
+                                     const beam_mxfp8_weight_t* gate,
+                                     const beam_mxfp8_weight_t* up,
+                                     const beam_mxfp8_weight_t* down, void* out, int64_t T,
+                                     void* workspace, size_t ws_bytes, void* stream) {
+  return beam_moe_forward_mxfp8_boundary(cfg, hidden, router_w, corr_bias, gate, up, down, out, T,
+                                         nullptr, workspace, ws_bytes, stream);
+}
+
+beam_status_t beam_moe_forward_mxfp8_boundary(const beam_moe_config_t* cfg, const void* hidden,
+                                              const float* router_w, const float* corr_bias,
+                                              const beam_mxfp8_weight_t* gate,
+                                              const beam_mxfp8_weight_t* up,
+                                              const beam_mxfp8_weight_t* down, void* out,
+                                              int64_t T, const beam_moe_boundary_t* boundary,
+                                              void* workspace, size_t ws_bytes, void* stream) {
+  return forward_quantised(
+      cfg, BEAM_WEIGHTS_MXFP8, hidden, router_w, corr_bias, gate, up, down, out, T, boundary,
+      workspace, ws_bytes, stream, valid_mxfp8_weight,
+      [&](const int32_t* idx, const float* w, const Layout& L, const DevInfo& dev,
+          cudaStream_t s, bool permuted, const beam::BoundaryArgs* ba) {
+        return run_experts_mxfp8(*cfg, hidden, idx, w, *gate, *up, *down, out, T, workspace, L,
+                                 dev, s, permuted, ba);
+      });
+}
+
 beam_status_t beam_moe_fp8_quantize_rows(const void* x, int64_t n, int32_t cols, uint8_t* q,
                                          float* scale, void* stream) {
   if (n < 0 || n > INT32_MAX || cols <= 0 || cols % 8) return BEAM_ERR_INVALID_ARG;
@@ -1308,7 +1424,7 @@ int32_t beam_moe_kernels_per_forward(const beam_moe_config_t* cfg, int64_t T, in
   // token rows and h (and gathers the token codes for larger batches)
   const bool small = small_batch(*cfg, T * cfg->topk);
   const int experts = weight_fmt == BEAM_WEIGHTS_FP8    ? 6 + (small ? 0 : 1)
-                      : weight_fmt != BEAM_WEIGHTS_BF16 ? 5
+                      : weight_fmt != BEAM_WEIGHTS_BF16 ? 5  // NVFP4, W4A16, MXFP8
                                                         : 4 + (small ? 0 : 1);
   if (routed) return experts;
   // routing: router (+ plane split), select; decode-sized batches run router,

@@ -105,24 +105,26 @@ cudaError_t launch_router_tc(const CUtensorMap& w_planes, const CUtensorMap& x, 
 // The K split launch_router_tc uses for T tokens on num_sms SMs (>= 1).
 int router_tc_ksplit(int64_t T, int32_t E, int32_t d, int num_sms);
 
-// ---------------------------------------------------------------- NVFP4
+// ------------------------------------------------------- NVFP4 and MXFP8
+// Arguments of the block-scaled grouped GEMMs (NVFP4, or MXFP8 where noted).
 struct Fp4GemmArgs {
   const int32_t* counts;
   const int32_t* offsets;
   const float* perm_w;     // [rows] routing weight (down)
-  const uint8_t* sfa0;     // blocked E4M3 weight scales (gate or down)
-  const uint8_t* sfa1;     // blocked E4M3 weight scales (up)
-  const float* gs0;        // [E] FP32 scale (gate or down)
-  const float* gs1;        // [E] FP32 scale (up)
-  uint8_t* hq;             // gate/up out: h codes [rows, F/2]
-  uint8_t* hsf;            // gate/up out: h scales [rows, F/4] (16-byte slot per 64)
+  const uint8_t* sfa0;     // blocked E4M3 (MXFP8: E8M0) weight scales (gate or down)
+  const uint8_t* sfa1;     // blocked weight scales (up)
+  const float* gs0;        // [E] FP32 scale (gate or down); unused for MXFP8
+  const float* gs1;        // [E] FP32 scale (up); unused for MXFP8
+  uint8_t* hq;             // gate/up out: h codes [rows, F/2] (MXFP8: [rows, F])
+  uint8_t* hsf;            // gate/up out: h scales [rows, F/4], a 16-byte slot per 64
+                           // (MXFP8: [rows, F/8], a 16-byte slot per 128)
   float* y;                // down out: [rows, d]
   const int32_t* out_rows; // down: output row of each permuted row (nullptr: the same row)
   int32_t out_ld;          // F (gate/up) or d (down), in elements
   int32_t E;
   int32_t rows_per_expert;
   int32_t m_blocks;
-  int32_t k_blocks;        // K / 256
+  int32_t k_blocks;        // K / 256 (MXFP8: K / 128)
   int32_t weight_evict_first;
   uint32_t* status;
   uint64_t wait_limit_ns;
@@ -173,5 +175,14 @@ void launch_quantize_tokens(const uint16_t* x, const int32_t* pair_row, int64_t 
 cudaError_t launch_fp4_gemm(bool gateup, int nt, const CUtensorMap& a0, const CUtensorMap& a1,
                             const CUtensorMap& b, const CUtensorMap& sfb, const Fp4GemmArgs& p,
                             int grid, cudaStream_t s);
+// token rows x [T, d] -> MX codes [rows, d] and E8M0 scales [rows, d/8] (one
+// 16-byte slot, 4 scales + padding, per 128 elements) of each token's k
+// permuted rows pair_row[t * k + j] (k <= 32)
+void launch_quantize_tokens_mx(const uint16_t* x, const int32_t* pair_row, int64_t T, int32_t k,
+                               int32_t d, uint8_t* xq, uint8_t* xsf, cudaStream_t s);
+// the MXFP8 grouped GEMM (E4M3 x E4M3, E8M0 per 32), as launch_fp4_gemm
+cudaError_t launch_mxfp8_gemm(bool gateup, int nt, const CUtensorMap& a0, const CUtensorMap& a1,
+                              const CUtensorMap& b, const CUtensorMap& sfb, const Fp4GemmArgs& p,
+                              int grid, cudaStream_t s);
 
 }  // namespace beam

@@ -11,6 +11,21 @@
 // h is quantised the same way along d_ff inside the gate/up epilogue.  The
 // per-expert FP32 scales multiply the accumulators in the epilogues.
 //
+// MXFP8 experts share this kernel (FMT = kFmtMxfp8): E4M3 weights with one
+// E8M0 scale per 32 elements along K (the OCP MX format; the pages list MXFP8
+// beside FP8: "vLLM 实现 Reflection Beam 501B MoE 模型 Day 0 支持", the SkyRL
+// paragraphs), both GEMM inputs quantised to MX blocks of 32 (x from its
+// BF16 values, h from the FP32 SwiGLU product in the gate/up epilogue) with
+// the OCP conversion: shared exponent X = floor(log2(amax)) - 8, codes
+// E4M3(v * 2^-X), nearest even, saturating.  The MMAs are
+// kind::mxf8f6f4.block_scale (UE8M0, one scale per 32, K = 32 per MMA).  A
+// stage holds 128 K values; each row's four scales of a stage (one per MMA)
+// sit in one 32-bit TMEM word, and each MMA picks its byte through the scale
+// IDs of its instruction descriptor.  The weight scales use the same
+// 128-row x 4-scale blocked order as the NVFP4 ones (one 512-byte block per
+// stage); the token scales take one 16-byte slot per 128 elements (4 scales,
+// then padding).
+//
 // Scale factors reach the tensor cores through TMEM (tcgen05.cp).  For
 // 128 weight rows the MMA wants row r's four scales of a 64-wide K chunk at
 // lane r % 32, column base + r / 32: the weight scales are stored in that
@@ -41,8 +56,10 @@ using gemm::token_blocks;
 
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int BM = 128;
-constexpr int BK_BYTES = 128;         // 256 FP4 elements of K per stage
-constexpr int KCHUNK = 64;            // K per MMA
+constexpr int BK_BYTES = 128;         // K per stage: 256 FP4 or 128 E4M3 elements
+constexpr int kMmaBytes = 32;         // K bytes per MMA: 64 FP4 or 32 E4M3 elements
+constexpr int kFmtNvfp4 = 0;
+constexpr int kFmtMxfp8 = 1;
 constexpr int kThreads = 192;
 constexpr int kMaxE = 256;
 constexpr uint32_t kTileBudget = 216 * 1024;
@@ -66,6 +83,21 @@ __device__ __forceinline__ float e4m3_value(uint8_t c) {
 
 __device__ __forceinline__ uint8_t to_e2m1(float v) {
   return static_cast<uint8_t>(__nv_cvt_float_to_fp4(v, __NV_E2M1, cudaRoundNearest)) & 0xF;
+}
+
+// The shared exponent of an MX block of E4M3 elements: floor(log2(amax)) - 8
+// (8 = E4M3's largest exponent), clamped to E8M0's [-127, 127]; -127 when
+// amax is 0 or subnormal (floor(log2) < -126 there).  amax >= 0.
+__device__ __forceinline__ int mx_exponent(float amax) {
+  const int ex = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu);
+  if (ex == 0) return -127;
+  return max(-127, min(127, ex - 127 - 8));
+}
+
+// 2^-x as an FP32 for x in [-127, 119] (the exponents mx_exponent returns
+// for finite amax): a normal number, so v * 2^-x is exact.
+__device__ __forceinline__ float pow2_neg(int x) {
+  return __uint_as_float(static_cast<uint32_t>(127 - x) << 23);
 }
 
 // ---------------------------------------------------------- pack scales
@@ -133,7 +165,60 @@ __global__ void __launch_bounds__(128) quantize_tokens_kernel(const uint16_t* __
   }
 }
 
-// --------------------------------------------------------------- FP4 GEMM
+// Token t's hidden row as MX blocks of 32 along d (E4M3 codes, E8M0 scale),
+// quantised once and written to each of its k permuted rows (pair_row[t * k
+// + j]; -1 for an invalid routed index, skipped).  xq [rows, d] codes; xsf
+// [rows, d/8]: per 128 elements a 16-byte slot holding their 4 scales (then
+// padding).  One thread per block of 32.
+__global__ void __launch_bounds__(128) quantize_tokens_mx_kernel(const uint16_t* __restrict__ x,
+                                                                 const int32_t* __restrict__ pair_row,
+                                                                 int32_t k, int32_t d,
+                                                                 uint8_t* __restrict__ xq,
+                                                                 uint8_t* __restrict__ xsf) {
+  const int64_t t = blockIdx.x;
+  __shared__ int64_t s_row[32];
+  if (threadIdx.x < k) s_row[threadIdx.x] = pair_row[t * k + threadIdx.x];
+  __syncthreads();
+  const uint4* src = reinterpret_cast<const uint4*>(x + t * d);
+  for (int blk = threadIdx.x; blk < d / 32; blk += blockDim.x) {
+    uint32_t w[16];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint4 a = src[4 * blk + i];
+      w[4 * i] = a.x;
+      w[4 * i + 1] = a.y;
+      w[4 * i + 2] = a.z;
+      w[4 * i + 3] = a.w;
+    }
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(w[i] << 16)),
+                               fabsf(__uint_as_float(w[i] & 0xffff0000u))));
+    const int xe = mx_exponent(amax);
+    const float inv = pow2_neg(xe);
+    uint32_t q[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint32_t lo0 = to_e4m3(__uint_as_float(w[2 * i] << 16) * inv);
+      const uint32_t hi0 = to_e4m3(__uint_as_float(w[2 * i] & 0xffff0000u) * inv);
+      const uint32_t lo1 = to_e4m3(__uint_as_float(w[2 * i + 1] << 16) * inv);
+      const uint32_t hi1 = to_e4m3(__uint_as_float(w[2 * i + 1] & 0xffff0000u) * inv);
+      q[i] = lo0 | (hi0 << 8) | (lo1 << 16) | (hi1 << 24);
+    }
+    const uint8_t sc = static_cast<uint8_t>(xe + 127);
+    for (int j = 0; j < k; ++j) {
+      const int64_t row = s_row[j];
+      if (row < 0) continue;  // an invalid routed index has no permuted row
+      uint4* dst = reinterpret_cast<uint4*>(xq + row * d + 32 * blk);
+      dst[0] = make_uint4(q[0], q[1], q[2], q[3]);
+      dst[1] = make_uint4(q[4], q[5], q[6], q[7]);
+      xsf[row * (d / 8) + (blk / 4) * 16 + (blk % 4)] = sc;
+    }
+  }
+}
+
+// ------------------------------------------------- block-scaled GEMM
 // Kinds: the gate/up GEMM (gate and up weight tiles of the same rows, one
 // token tile), the down GEMM (one weight tile), and the down GEMM over pairs
 // of adjacent 128-row weight blocks sharing one token tile (twice the weight
@@ -142,14 +227,18 @@ constexpr int kKindDown = 0;
 constexpr int kKindGateUp = 1;
 constexpr int kKindDownPair = 2;
 
-template <int NT, int KIND>
+template <int NT, int KIND, int FMT>
 struct Cfg {
   static constexpr bool GATEUP = KIND == kKindGateUp;
   static constexpr int NUM_A = KIND == kKindDown ? 1 : 2;
+  // 512-byte scale blocks per operand and stage: NVFP4 one per MMA (four
+  // scales of 16 per row), MXFP8 one per stage (one scale of 32 per row and
+  // MMA, the four MMAs' in one word)
+  static constexpr int SBS = FMT == kFmtNvfp4 ? 4 : 1;
   static constexpr uint32_t A_BYTES = BM * BK_BYTES;           // 16 KB
   static constexpr uint32_t B_BYTES = NT * BK_BYTES;
-  static constexpr uint32_t SFA_BYTES = 2048;                  // 128 rows x 16 scales
-  static constexpr uint32_t SFB_BYTES = 2048;                  // 4 chunks x 32 rows x 16 B
+  static constexpr uint32_t SFA_BYTES = 512 * SBS;             // 128 rows x 4 B per block
+  static constexpr uint32_t SFB_BYTES = 512 * SBS;             // 32 rows x 16 B per block
   static constexpr uint32_t OFF_B = NUM_A * A_BYTES;
   static constexpr uint32_t OFF_SFA = OFF_B + B_BYTES;
   static constexpr uint32_t OFF_SFB = OFF_SFA + NUM_A * SFA_BYTES;
@@ -158,7 +247,7 @@ struct Cfg {
   static constexpr int STAGES_RAW = static_cast<int>(kTileBudget / STAGE_BYTES);
   static constexpr int STAGES = STAGES_RAW > 16 ? 16 : STAGES_RAW;
   static constexpr uint32_t ACC_COLS = NUM_A * NT;
-  static constexpr uint32_t SF_COLS = NUM_A * 16 + 16;         // one stage's scales
+  static constexpr uint32_t SF_COLS = 4 * SBS * (NUM_A + 1);   // one stage's scales
   static constexpr uint32_t SF_BASE = 2 * ACC_COLS;
   static constexpr uint32_t TMEM_COLS = pow2_at_least(SF_BASE + 2 * SF_COLS);
   static constexpr uint32_t NUM_BARS = 2 * STAGES + 5;
@@ -170,13 +259,14 @@ struct Cfg {
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 };
 
-template <int NT, int KIND>
+template <int NT, int KIND, int FMT>
 __global__ void __launch_bounds__(kThreads, 1)
     fp4_gemm_kernel(const __grid_constant__ CUtensorMap tm_a0,
                     const __grid_constant__ CUtensorMap tm_a1,
                     const __grid_constant__ CUtensorMap tm_b,
                     const __grid_constant__ CUtensorMap tm_sfb, const Fp4GemmArgs p) {
-  using C = Cfg<NT, KIND>;
+  using C = Cfg<NT, KIND, FMT>;
+  constexpr bool MX = FMT == kFmtMxfp8;
   constexpr bool GATEUP = C::GATEUP;
   constexpr bool PAIR = KIND == kKindDownPair;
   extern __shared__ uint8_t smem_raw[];
@@ -253,8 +343,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem_base = *tmem_slot;
   const int num_tiles = s_start[E];
   const Waiter W{abort_flag, p.status, p.wait_limit_ns};
-  // weight scales: blocks of 128 rows x 4 scales; a stage takes 4 blocks
-  const int64_t sf_blocks_per_row_tile = p.k_blocks * 4;
+  // weight scales: blocks of 128 rows x 4 scales; a stage takes SBS blocks
+  const int64_t sf_blocks_per_row_tile = static_cast<int64_t>(p.k_blocks) * C::SBS;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -281,7 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t fb = full_bar(stage);
           ptx::mbar_arrive_expect_tx(fb, C::TX_BYTES);
           ptx::tma_load_2d(st, &tm_a0, fb, kb * BK_BYTES, a_row, pol_w);
-          const int64_t sf_off = (sf_row_tile * sf_blocks_per_row_tile + 4 * kb) * 512;
+          const int64_t sf_off = (sf_row_tile * sf_blocks_per_row_tile + C::SBS * kb) * 512;
           ptx::bulk_load(st + C::OFF_SFA, p.sfa0 + sf_off, C::SFA_BYTES, fb);
           if (GATEUP) {
             ptx::tma_load_2d(st + C::A_BYTES, &tm_a1, fb, kb * BK_BYTES, a_row, pol_w);
@@ -294,9 +384,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           ptx::tma_load_2d(st + C::OFF_B, &tm_b, fb, kb * BK_BYTES, ti.row0, pol_b);
 #pragma unroll
-          for (int c = 0; c < 4; ++c)
-            ptx::tma_load_2d(st + C::OFF_SFB + 512 * c, &tm_sfb, fb, (4 * kb + c) * 16, ti.row0,
-                             pol_b);
+          for (int c = 0; c < C::SBS; ++c)
+            ptx::tma_load_2d(st + C::OFF_SFB + 512 * c, &tm_sfb, fb, (C::SBS * kb + c) * 16,
+                             ti.row0, pol_b);
           last_parity[stage] = static_cast<int>(phase);
           if (++stage == C::STAGES) {
             stage = 0;
@@ -320,7 +410,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
         const TileInfo ti = decode_tile<NT>(tile, s_start, s_cnt, s_off, E);
         if (ti.nvalid <= 0) continue;
-        const uint32_t idesc = ptx::idesc_fp4_f32(BM, static_cast<uint32_t>(ti.n_mma));
+        const uint32_t idesc = MX ? ptx::idesc_mx8_f32(BM, static_cast<uint32_t>(ti.n_mma))
+                                  : ptx::idesc_fp4_f32(BM, static_cast<uint32_t>(ti.n_mma));
         if (!W.wait(tempty_bar(acc), acc_phase ^ 1u)) break;
         ptx::tc_fence_after();
         const uint32_t d0 = tmem_base + acc * C::ACC_COLS;
@@ -332,26 +423,36 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::tc_fence_after();
           const uint32_t st = tiles + stage * C::STAGE_BYTES;
           const uint32_t sf_col = tmem_base + C::SF_BASE + sf_slot * C::SF_COLS;
-          // scales of this stage into TMEM (in issue order with the MMAs)
+          // scales of this stage into TMEM (in issue order with the MMAs):
+          // each 512-byte block to 4 columns
 #pragma unroll
           for (int a = 0; a < C::NUM_A; ++a)
 #pragma unroll
-            for (int c = 0; c < 4; ++c)
-              ptx::tmem_cp_32x128b_x4(sf_col + 16 * a + 4 * c,
+            for (int c = 0; c < C::SBS; ++c)
+              ptx::tmem_cp_32x128b_x4(sf_col + 4 * C::SBS * a + 4 * c,
                                       ptx::sdesc_rows16(st + C::OFF_SFA + a * C::SFA_BYTES + 512 * c));
-          const uint32_t sfb_col = sf_col + 16 * C::NUM_A;
+          const uint32_t sfb_col = sf_col + 4 * C::SBS * C::NUM_A;
 #pragma unroll
-          for (int c = 0; c < 4; ++c)
+          for (int c = 0; c < C::SBS; ++c)
             ptx::tmem_cp_32x128b_x4(sfb_col + 4 * c, ptx::sdesc_rows16(st + C::OFF_SFB + 512 * c));
 #pragma unroll
-          for (int c = 0; c < BK_BYTES * 2 / KCHUNK; ++c) {
+          for (int c = 0; c < BK_BYTES / kMmaBytes; ++c) {
             const uint32_t accum = (kb | c) ? 1u : 0u;
-            const uint64_t bd = ptx::sdesc_sw128(st + C::OFF_B + 32 * c);
-            ptx::mma_fp4(d0, ptx::sdesc_sw128(st + 32 * c), bd, idesc, sf_col + 4 * c,
-                         sfb_col + 4 * c, accum);
-            if (C::NUM_A == 2)
-              ptx::mma_fp4(d0 + NT, ptx::sdesc_sw128(st + C::A_BYTES + 32 * c), bd, idesc,
-                           sf_col + 16 + 4 * c, sfb_col + 4 * c, accum);
+            const uint64_t bd = ptx::sdesc_sw128(st + C::OFF_B + kMmaBytes * c);
+            if constexpr (MX) {
+              // MMA c takes byte c of each row's scale word
+              const uint32_t id = idesc | ptx::idesc_sf_ids(c, c);
+              ptx::mma_mx8(d0, ptx::sdesc_sw128(st + kMmaBytes * c), bd, id, sf_col, sfb_col, accum);
+              if (C::NUM_A == 2)
+                ptx::mma_mx8(d0 + NT, ptx::sdesc_sw128(st + C::A_BYTES + kMmaBytes * c), bd, id,
+                             sf_col + 4, sfb_col, accum);
+            } else {
+              ptx::mma_fp4(d0, ptx::sdesc_sw128(st + kMmaBytes * c), bd, idesc, sf_col + 4 * c,
+                           sfb_col + 4 * c, accum);
+              if (C::NUM_A == 2)
+                ptx::mma_fp4(d0 + NT, ptx::sdesc_sw128(st + C::A_BYTES + kMmaBytes * c), bd, idesc,
+                             sf_col + 16 + 4 * c, sfb_col + 4 * c, accum);
+            }
           }
           ptx::mma_commit(empty_bar(stage));
           sf_slot ^= 1;
@@ -381,12 +482,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::tc_fence_after();
       const uint32_t tq = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * C::ACC_COLS;
       const int col = ti.mblock * BM + m;
-      const float gs0 = p.gs0[ti.expert];
+      const float gs0 = MX ? 1.f : p.gs0[ti.expert];
 #pragma unroll 1
       for (int c0 = 0; c0 < ti.nvalid; c0 += 16) {
         uint32_t ra[16];
         ptx::tmem_ld16(tq + c0, ra);
-        if constexpr (GATEUP) {
+        if constexpr (GATEUP && MX) {
+          uint32_t rb[16];
+          ptx::tmem_ld16(tq + NT + c0, rb);
+          ptx::tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            if (c0 + j < ti.nvalid) {  // uniform across the warp
+              const int64_t row = ti.row0 + c0 + j;
+              const float g = __uint_as_float(ra[j]);
+              const float u = __uint_as_float(rb[j]);
+              const float h = g / (1.0f + expf(-g)) * u;
+              // an MX block of 32 along d_ff: the warp's 32 lanes
+              float amax = fabsf(h);
+#pragma unroll
+              for (int o = 16; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
+              const int xe = mx_exponent(amax);
+              p.hq[row * p.out_ld + col] = to_e4m3(h * pow2_neg(xe));
+              if (lane == 0)
+                p.hsf[row * (p.out_ld / 8) + (col / 128) * 16 + (col / 32) % 4] =
+                    static_cast<uint8_t>(xe + 127);
+            }
+          }
+        } else if constexpr (GATEUP) {
           const float gs1 = p.gs1[ti.expert];
           uint32_t rb[16];
           ptx::tmem_ld16(tq + NT + c0, rb);
@@ -455,13 +578,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int NT, int KIND>
+template <int NT, int KIND, int FMT>
 cudaError_t launch_fp4_impl(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b,
                             const CUtensorMap& sfb, const Fp4GemmArgs& p, int grid,
                             cudaStream_t s) {
-  using C = Cfg<NT, KIND>;
-  auto kern = fp4_gemm_kernel<NT, KIND>;
-  const cudaError_t err = smem_limit_once<fp4_gemm_kernel<NT, KIND>>(C::SMEM_BYTES);
+  using C = Cfg<NT, KIND, FMT>;
+  auto kern = fp4_gemm_kernel<NT, KIND, FMT>;
+  const cudaError_t err = smem_limit_once<fp4_gemm_kernel<NT, KIND, FMT>>(C::SMEM_BYTES);
   if (err != cudaSuccess) return err;
   kern<<<grid, kThreads, C::SMEM_BYTES, s>>>(a0, a1, b, sfb, p);
   return cudaGetLastError();
@@ -488,11 +611,30 @@ cudaError_t launch_fp4_gemm(bool gateup, int nt, const CUtensorMap& a0, const CU
   // the down GEMM takes weight rows in pairs of 128-row blocks (m_blocks
   // counts pairs)
   if (gateup) {
-    if (nt == 16) return launch_fp4_impl<16, kKindGateUp>(a0, a1, b, sfb, p, grid, s);
-    if (nt == 32) return launch_fp4_impl<32, kKindGateUp>(a0, a1, b, sfb, p, grid, s);
+    if (nt == 16) return launch_fp4_impl<16, kKindGateUp, kFmtNvfp4>(a0, a1, b, sfb, p, grid, s);
+    if (nt == 32) return launch_fp4_impl<32, kKindGateUp, kFmtNvfp4>(a0, a1, b, sfb, p, grid, s);
   } else {
-    if (nt == 16) return launch_fp4_impl<16, kKindDownPair>(a0, a0, b, sfb, p, grid, s);
-    if (nt == 32) return launch_fp4_impl<32, kKindDownPair>(a0, a0, b, sfb, p, grid, s);
+    if (nt == 16) return launch_fp4_impl<16, kKindDownPair, kFmtNvfp4>(a0, a0, b, sfb, p, grid, s);
+    if (nt == 32) return launch_fp4_impl<32, kKindDownPair, kFmtNvfp4>(a0, a0, b, sfb, p, grid, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
+void launch_quantize_tokens_mx(const uint16_t* x, const int32_t* pair_row, int64_t T, int32_t k,
+                               int32_t d, uint8_t* xq, uint8_t* xsf, cudaStream_t s) {
+  if (T <= 0) return;
+  quantize_tokens_mx_kernel<<<static_cast<unsigned>(T), 128, 0, s>>>(x, pair_row, k, d, xq, xsf);
+}
+
+cudaError_t launch_mxfp8_gemm(bool gateup, int nt, const CUtensorMap& a0, const CUtensorMap& a1,
+                              const CUtensorMap& b, const CUtensorMap& sfb, const Fp4GemmArgs& p,
+                              int grid, cudaStream_t s) {
+  if (gateup) {
+    if (nt == 16) return launch_fp4_impl<16, kKindGateUp, kFmtMxfp8>(a0, a1, b, sfb, p, grid, s);
+    if (nt == 32) return launch_fp4_impl<32, kKindGateUp, kFmtMxfp8>(a0, a1, b, sfb, p, grid, s);
+  } else {
+    if (nt == 16) return launch_fp4_impl<16, kKindDownPair, kFmtMxfp8>(a0, a0, b, sfb, p, grid, s);
+    if (nt == 32) return launch_fp4_impl<32, kKindDownPair, kFmtMxfp8>(a0, a0, b, sfb, p, grid, s);
   }
   return cudaErrorInvalidValue;
 }

@@ -152,6 +152,23 @@ __device__ __forceinline__ void mma_fp4(uint32_t d_tmem, uint64_t a_desc, uint64
       : "memory");
 }
 
+// D[tmem] (+)= (A * SFA)[smem] * (B * SFB)[smem]^T, kind::mxf8f6f4: E4M3 A
+// and B (K-major), one UE8M0 scale per 32 elements along K (scale_vec::1X),
+// FP32 D.  K per instruction = 32.  Row r's scale is a byte of the 32-bit
+// TMEM word at lane r % 32 (of any lane quarter) and column sf + r / 32; the
+// scale-factor IDs of the instruction descriptor pick the byte.
+__device__ __forceinline__ void mma_mx8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                        uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                        uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X "
+      "[%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
 // Copy 32 rows x 16 bytes of shared memory into TMEM (4 columns), the same
 // rows into each of the four lane quarters (lane 32q + j <- row j).
 __device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t src_desc) {
@@ -238,6 +255,18 @@ __host__ __device__ constexpr uint32_t idesc_e4m3_f32(uint32_t M, uint32_t N) {
 // K-major), UE4M3 scales (bit 23 = 0), FP32 D; N >> 3 at bit 17, M >> 4 at 24.
 __host__ __device__ constexpr uint32_t idesc_fp4_f32(uint32_t M, uint32_t N) {
   return (1u << 7) | (1u << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+
+// Instruction descriptor, kind::mxf8f6f4: E4M3 A and B (format code 0, both
+// K-major), UE8M0 scales (bit 23 = 1), FP32 D; N >> 3 at bit 17, M >> 4 at 24.
+__host__ __device__ constexpr uint32_t idesc_mx8_f32(uint32_t M, uint32_t N) {
+  return ((N >> 3) << 17) | (1u << 23) | ((M >> 4) << 24);
+}
+
+// Scale-factor IDs of a block-scaled instruction descriptor: the byte of the
+// 32-bit scale word used for A (bits 29-30) and for B (bits 4-5).
+__host__ __device__ constexpr uint32_t idesc_sf_ids(uint32_t a_id, uint32_t b_id) {
+  return (a_id << 29) | (b_id << 4);
 }
 
 }  // namespace ptx

@@ -89,6 +89,7 @@ typedef struct {
 #define BEAM_WEIGHTS_NVFP4 1
 #define BEAM_WEIGHTS_NVFP4_A16 2 /* NVFP4 weights, 16-bit activations */
 #define BEAM_WEIGHTS_FP8 3       /* dynamic FP8: E4M3 weights and activations */
+#define BEAM_WEIGHTS_MXFP8 4     /* MXFP8: E4M3 with E8M0 scales per 32, weights and activations */
 
 /* Bytes of device workspace a call with up to T_max tokens needs (256-byte
  * aligned).  Returns 0 for an invalid configuration. */
@@ -117,6 +118,10 @@ typedef struct {
                              16-byte slot, 4 scales then padding             */
   size_t h_fp4;         /*   SwiGLU activations [T*topk, F/2]                  */
   size_t h_sf;          /*   and their scales [T*topk, F/4], same slots        */
+                        /* MXFP8 path: the same four buffers hold E4M3 codes
+                           [T*topk, d] and [T*topk, F] and E8M0 scales
+                           [T*topk, d/8] and [T*topk, F/8] (per 128 elements
+                           a 16-byte slot, 4 scales then padding)            */
   size_t y;             /* FP32 [T*topk, d] weighted expert outputs           */
   size_t x_fp8;         /* FP8 path: token rows, E4M3 codes [T, d]            */
   size_t x_scale;       /*   their FP32 scales [T]                            */
@@ -233,8 +238,8 @@ typedef struct {
   const float *global_scale;    /* [E] FP32                                        */
 } beam_fp4_weight_t;
 
-/* Reorders row-major E4M3 block scales [rows, S] (rows % 128 == 0,
- * S % 4 == 0) into blocks of 128 rows x 4 scales, 512 bytes each, block
+/* Reorders row-major block scales [rows, S] (E4M3 for NVFP4, E8M0 for MXFP8;
+ * rows % 128 == 0, S % 4 == 0) into blocks of 128 rows x 4 scales, 512 bytes each, block
  * (row/128, s/4) at ((row/128) * (S/4) + s/4) * 512 and byte
  * (r % 32) * 16 + (r / 32) * 4 + s % 4 inside it (r = row % 128): the order in
  * which the tensor cores take weight scales.  Run once per weight tensor when
@@ -300,6 +305,36 @@ beam_status_t beam_moe_forward_fp8(const beam_moe_config_t *cfg, const void *hid
                                    const beam_fp8_weight_t *down, void *out, int64_t T,
                                    void *workspace, size_t ws_bytes, void *stream);
 
+/* MXFP8 expert weights of one projection (OCP MX format with E4M3
+ * elements; the pages list MXFP8 beside FP8 as a precision Beam runs in:
+ * "vLLM 实现 Reflection Beam 501B MoE 模型 Day 0 支持", the SkyRL paragraphs).
+ * A weight is code x 2^(scale - 127), one E8M0 scale per 32 consecutive
+ * elements along K. */
+typedef struct {
+  const uint8_t *q;     /* E4M3 codes [E, N, K]                                */
+  const uint8_t *sf;    /* E8M0 scales of the [E*N, K/32] row-major matrix, in the
+                           blocked order beam_moe_nvfp4_pack_scales writes for
+                           S = K/32 (the same 128-row x 4-scale blocks)      */
+} beam_mxfp8_weight_t;
+
+/* The whole layer with MXFP8 experts.  Router and selection as in
+ * beam_moe_forward; both expert GEMM inputs are quantised to MX blocks of 32
+ * (x along d from its BF16 values before the gate/up GEMM, the FP32 SwiGLU
+ * product along d_ff before the down GEMM) with the OCP MX conversion:
+ * shared exponent X = floor(log2(amax)) - 8 clamped to [-127, 127] (-127 for
+ * an all-zero block), codes E4M3(value * 2^-X), round to nearest even,
+ * saturating at 448.  The GEMMs run as block-scaled E4M3 MMAs (one E8M0
+ * scale per 32) with FP32 accumulation; the rest (FP32 routing weights, FP32
+ * combine in slot order, one BF16 rounding) is beam_moe_forward's.  Extra
+ * shape rule: d % 256 == 0.  Workspace: beam_moe_workspace_size(cfg, T,
+ * BEAM_WEIGHTS_MXFP8). */
+beam_status_t beam_moe_forward_mxfp8(const beam_moe_config_t *cfg, const void *hidden,
+                                     const float *router_w, const float *corr_bias,
+                                     const beam_mxfp8_weight_t *gate,
+                                     const beam_mxfp8_weight_t *up,
+                                     const beam_mxfp8_weight_t *down, void *out, int64_t T,
+                                     void *workspace, size_t ws_bytes, void *stream);
+
 /* The FP8 path's activation rule on its own: BF16 rows x [n, cols] ->
  * E4M3 codes q [n, cols] and FP32 scales [n] (cols % 8 == 0; all pointers
  * 16-byte aligned device memory).  n == 0 launches nothing. */
@@ -336,6 +371,13 @@ beam_status_t beam_moe_forward_fp8_boundary(const beam_moe_config_t *cfg, const 
                                             const beam_fp8_weight_t *down, void *out, int64_t T,
                                             const beam_moe_boundary_t *boundary, void *workspace,
                                             size_t ws_bytes, void *stream);
+beam_status_t beam_moe_forward_mxfp8_boundary(const beam_moe_config_t *cfg, const void *hidden,
+                                              const float *router_w, const float *corr_bias,
+                                              const beam_mxfp8_weight_t *gate,
+                                              const beam_mxfp8_weight_t *up,
+                                              const beam_mxfp8_weight_t *down, void *out,
+                                              int64_t T, const beam_moe_boundary_t *boundary,
+                                              void *workspace, size_t ws_bytes, void *stream);
 
 /* ---------------------------------------------------- expert parallelism
  * Expert parallelism over n_ranks ranks ("SGLang 原生支持 Reflection 的 Beam
@@ -455,7 +497,8 @@ beam_status_t beam_moe_set_debug(uint32_t wait_limit_us, int32_t withhold_first_
  * beam_moe_forward (and beam_moe_forward_noalloc) for weight_fmt
  * BEAM_WEIGHTS_BF16, beam_moe_forward_nvfp4 for BEAM_WEIGHTS_NVFP4,
  * beam_moe_forward_nvfp4_a16 for BEAM_WEIGHTS_NVFP4_A16,
- * beam_moe_forward_fp8 for BEAM_WEIGHTS_FP8, and with
+ * beam_moe_forward_fp8 for BEAM_WEIGHTS_FP8, beam_moe_forward_mxfp8 for
+ * BEAM_WEIGHTS_MXFP8, and with
  * routed != 0 beam_moe_forward_routed (BF16 only).  Returns 0 for an invalid
  * configuration, T <= 0 or an unknown combination.  Host-only. */
 int32_t beam_moe_kernels_per_forward(const beam_moe_config_t *cfg, int64_t T, int32_t weight_fmt,

@@ -47,13 +47,15 @@ def _weights(t, fmt):
         return [t[n] for n in names]
     if fmt == "fp8":
         return [pkg.Fp8Weight.of(t[n]) for n in names]
+    if fmt == "mxfp8":
+        return [pkg.Mxfp8Weight.of(t[n]) for n in names]
     return [pkg.Fp4Weight.of(t[n]) for n in names]
 
 
 def _plain(cfg, t, fmt, wts):
     args = (cfg, t["hidden"], t["router_w"], t["corr_bias"], *wts)
     return {"bf16": pkg.forward, "fp8": pkg.forward_fp8, "nvfp4": pkg.forward_nvfp4,
-            "a16": pkg.forward_nvfp4_a16}[fmt](*args)
+            "a16": pkg.forward_nvfp4_a16, "mxfp8": pkg.forward_mxfp8}[fmt](*args)
 
 
 def _check(cfg, t, n, seed, fmt="bf16"):
@@ -109,13 +111,13 @@ def test_boundary_beam_decode():
     _check(cfg, t, 40, seed=3)
 
 
-@pytest.mark.parametrize("fmt", ["fp8", "nvfp4", "a16"])
+@pytest.mark.parametrize("fmt", ["fp8", "nvfp4", "a16", "mxfp8"])
 @pytest.mark.parametrize("T,n", [(20, 2), (70, 33)])
 def test_boundary_after_quantised_experts(fmt, T, n):
-    """The NVFP4, W4A16 and FP8 layers end in the same FP32 expert rows and
+    """The NVFP4, W4A16, FP8 and MXFP8 layers end in the same FP32 expert rows and
     the same combine kernel: T = 20 takes the 16-row token blocks, T = 70
     the 256-row ones (T * topk > 4 * E)."""
-    d = 256 if fmt in ("nvfp4", "a16") else 128
+    d = 256 if fmt in ("nvfp4", "a16", "mxfp8") else 128
     cfg = inputs.MoEConfig(name=f"bnd_{fmt}", T=T, d=d, d_ff=d, seed=40 + T,
                            weight_fmt="nvfp4" if fmt == "a16" else fmt, n_experts=32, n_groups=4,
                            topk_groups=2, topk=4, routed_scale=2.5)

@@ -1,6 +1,6 @@
 """GPU parity at the smallest layer shapes each expert format accepts: K loops
-of one or two blocks in every GEMM (BF16 and FP8 at d = d_ff = 128, NVFP4
-and W4A16 at 256), 32 experts in 4 groups of 8, top-2 groups, top-4, and
+of one or two blocks in every GEMM (BF16 and FP8 at d = d_ff = 128, NVFP4,
+W4A16 and MXFP8 at 256), 32 experts in 4 groups of 8, top-2 groups, top-4, and
 ragged token counts on both sides of the 16-row / 256-row block switch
 (T * topk > 4 * E from T = 33 on).  Bounds: the BF16 path's 1e-2 * RMS,
 NVFP4's 2e-2 * RMS, FP8's 1e-2 * RMS plus the oracle's near-tie slack of
@@ -39,10 +39,10 @@ def _proj(t, need, keys):
             for n in ("w_gate", "w_up", "w_down")}
 
 
-@pytest.mark.parametrize("fmt", ["bf16", "fp8", "nvfp4", "a16"])
+@pytest.mark.parametrize("fmt", ["bf16", "fp8", "nvfp4", "a16", "mxfp8"])
 @pytest.mark.parametrize("T", [1, 20, 33, 70])
 def test_smallest_shapes(fmt, T):
-    d = 256 if fmt in ("nvfp4", "a16") else 128
+    d = 256 if fmt in ("nvfp4", "a16", "mxfp8") else 128
     cfg = _cfg(fmt, T, d, seed=7 * T + len(fmt))
     t = _to(inputs.generate(cfg, "cpu"), "cuda")
     lg, r = oracle_route(cfg, t)
@@ -55,6 +55,10 @@ def test_smallest_shapes(fmt, T):
         ws = pkg.Workspace(cfg, T, weight_fmt=pkg.FP8)
         out = pkg.forward_fp8(*args, *[pkg.Fp8Weight.of(t[n]) for n in ("w_gate", "w_up",
                                                                          "w_down")], ws=ws)
+    elif fmt == "mxfp8":
+        ws = pkg.Workspace(cfg, T, weight_fmt=pkg.MXFP8)
+        out = pkg.forward_mxfp8(*args, *[pkg.Mxfp8Weight.of(t[n]) for n in ("w_gate", "w_up",
+                                                                             "w_down")], ws=ws)
     else:
         a16 = fmt == "a16"
         ws = pkg.Workspace(cfg, T, weight_fmt=pkg.NVFP4_A16 if a16 else pkg.NVFP4)
@@ -69,9 +73,10 @@ def test_smallest_shapes(fmt, T):
     need = sorted({int(e) for e in oi.reshape(-1)})
     if fmt == "bf16":
         check_out(out, oracle_out(cfg, t, oi, ow))
-    elif fmt == "fp8":
+    elif fmt in ("fp8", "mxfp8"):
         p = _proj(t, need, ("q", "s"))
-        bits, exact, slack, scale_tie = oracle.experts_fp8(
+        fn = oracle.experts_fp8 if fmt == "fp8" else oracle.experts_mxfp8
+        bits, exact, slack, scale_tie = fn(
             x, oi, ow, p["w_gate"], p["w_up"], p["w_down"], cfg.n_experts, act_quant=True,
             exact=True, ties=True)
         rms = float(np.sqrt((exact ** 2).mean()))
@@ -89,13 +94,13 @@ def test_smallest_shapes(fmt, T):
         check_out(out, ref, tol=1e-2 if a16 else 2e-2)
 
 
-@pytest.mark.parametrize("fmt", ["bf16", "fp8", "nvfp4", "a16"])
+@pytest.mark.parametrize("fmt", ["bf16", "fp8", "nvfp4", "a16", "mxfp8"])
 def test_repeated_calls_are_bit_identical(fmt):
     """Every reduction runs in a fixed order: two calls on the same inputs
     give the same bits, at both token-block widths (the W4A16 partial sums of
     its four MMA issuers included)."""
     for T in (20, 70):
-        d = 256 if fmt in ("nvfp4", "a16") else 128
+        d = 256 if fmt in ("nvfp4", "a16", "mxfp8") else 128
         cfg = _cfg(fmt, T, d, seed=3 * T + len(fmt))
         t = _to(inputs.generate(cfg, "cpu"), "cuda")
         args = (cfg, t["hidden"], t["router_w"], t["corr_bias"])
@@ -104,6 +109,9 @@ def test_repeated_calls_are_bit_identical(fmt):
         elif fmt == "fp8":
             wts = [pkg.Fp8Weight.of(t[n]) for n in ("w_gate", "w_up", "w_down")]
             run = lambda: pkg.forward_fp8(*args, *wts)
+        elif fmt == "mxfp8":
+            wts = [pkg.Mxfp8Weight.of(t[n]) for n in ("w_gate", "w_up", "w_down")]
+            run = lambda: pkg.forward_mxfp8(*args, *wts)
         else:
             wts = [pkg.Fp4Weight.of(t[n]) for n in ("w_gate", "w_up", "w_down")]
             fwd = pkg.forward_nvfp4_a16 if fmt == "a16" else pkg.forward_nvfp4
