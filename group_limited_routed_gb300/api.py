@@ -16,7 +16,10 @@ import torch
 from .config import BeamMoEConfig, CConfig
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_LIB_PATH = os.path.join(_HERE, "_build", "libbeam_moe.so")
+# BEAM_MOE_DEVICE_CHECKS=1 loads the debug build with device-side bounds
+# checks (group_limited_routed_gb300.build.build(checked=True)) instead
+_LIB_PATH = os.path.join(_HERE, "_build_checked" if os.environ.get("BEAM_MOE_DEVICE_CHECKS") == "1"
+                         else "_build", "libbeam_moe.so")
 _lock = threading.Lock()
 _lib = None
 

@@ -1,4 +1,5 @@
-"""Builds libbeam_moe.so in-tree with nvcc for sm_103a (no CMake).
+"""Builds libbeam_moe.so in-tree with nvcc for sm_103a (no CMake), and on
+request its debug twin with device-side bounds checks.
 
 Each .cu file compiles in parallel to an object; the objects link into one
 shared library with the CUDA runtime linked statically, so the library loads
@@ -17,6 +18,10 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libbeam_moe.so")
+# the debug build with device-side bounds checks (BEAM_DEVICE_CHECKS=1): a
+# separate library, loaded instead of LIB when BEAM_MOE_DEVICE_CHECKS=1 is set
+BUILD_CHECKED = os.path.join(HERE, "_build_checked")
+LIB_CHECKED = os.path.join(BUILD_CHECKED, "libbeam_moe.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -36,23 +41,31 @@ def _deps() -> list[str]:
             + [os.path.join(ROOT, "include", "beam_moe.h"), __file__])
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(p) <= t for p in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | None = None) -> str:
-    if not force and up_to_date():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | None = None,
+          checked: bool = False) -> str:
+    """Compile every .cu file for sm_103a and link libbeam_moe.so; with
+    `checked`, the debug build with device-side bounds checks into its own
+    folder (it leaves the default library alone)."""
+    out_dir = BUILD_CHECKED if checked else BUILD
+    lib = LIB_CHECKED if checked else LIB
+    if not force and up_to_date(lib):
+        return lib
+    os.makedirs(out_dir, exist_ok=True)
     cc = nvcc()
     flags = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
                     "-I", os.path.join(ROOT, "include")] + list(extra_flags or [])
+    if checked:
+        flags.append("-DBEAM_DEVICE_CHECKS=1")
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(BUILD, os.path.basename(src) + ".o")
+        obj = os.path.join(out_dir, os.path.basename(src) + ".o")
         cmd = [cc, *flags, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -63,15 +76,15 @@ def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | N
 
     with cf.ThreadPoolExecutor(max_workers=max(1, min(8, os.cpu_count() or 1))) as ex:
         objs = list(ex.map(compile_one, sources()))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [cc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs, "-ldl", "-lpthread", "-lrt"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
     import sys
-    print(build(force="--force" in sys.argv, verbose=True))
+    print(build(force="--force" in sys.argv, verbose=True, checked="--checked" in sys.argv))

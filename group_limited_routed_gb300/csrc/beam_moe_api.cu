@@ -369,12 +369,12 @@ beam_status_t run_route(const beam_moe_config_t& c, const void* hidden, const fl
 // given (expert parallelism) there is no combine here.
 cudaError_t finish_combine(const beam_moe_config_t& c, const float* y, const int32_t* pair_row,
                            int64_t T, void* out, const float* y_pairs,
-                           const beam::BoundaryArgs* boundary, cudaStream_t s) {
+                           const beam::BoundaryArgs* boundary, uint32_t* status, cudaStream_t s) {
   if (y_pairs) return cudaSuccess;
   if (boundary)
     return beam::launch_combine_boundary(y, pair_row, T, c.topk, c.d,
-                                         static_cast<uint16_t*>(out), *boundary, s);
-  beam::launch_combine(y, pair_row, T, c.topk, c.d, static_cast<uint16_t*>(out), s);
+                                         static_cast<uint16_t*>(out), *boundary, status, s);
+  beam::launch_combine(y, pair_row, T, c.topk, c.d, static_cast<uint16_t*>(out), status, s);
   return cudaGetLastError();
 }
 
@@ -404,7 +404,7 @@ beam_status_t run_experts(const beam_moe_config_t& c, const void* hidden, const 
   uint16_t* xp = at<uint16_t>(ws, L.x_perm);
   if (!row_gather)
     beam::launch_scatter_tokens(static_cast<const uint16_t*>(hidden), pa.pair_row, T, c.topk, c.d,
-                                xp, s);
+                                xp, status, s);
   record(4, s);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return BEAM_ERR_CUDA;
@@ -445,6 +445,9 @@ beam_status_t run_experts(const beam_moe_config_t& c, const void* hidden, const 
   ga.m_blocks = c.d_ff / 128;
   ga.k_blocks = c.d / 64;
   ga.b_k_blocks = ga.k_blocks;
+  ga.a_rows = static_cast<int32_t>(EF);
+  ga.b_rows = static_cast<int32_t>(row_gather ? T : rows);
+  ga.out_rows_cap = static_cast<int32_t>(rows);
   err = beam::launch_grouped_gemm(beam::kModeGateUp, nt_gu, tm_wg, tm_wu, tm_xp, ga,
                                   grid_for(ga.m_blocks, nt_gu), s);
   if (err != cudaSuccess) return BEAM_ERR_CUDA;
@@ -462,12 +465,15 @@ beam_status_t run_experts(const beam_moe_config_t& c, const void* hidden, const 
   ga.m_blocks = pair ? c.d / 256 : c.d / 128;
   ga.k_blocks = c.d_ff / 64;
   ga.b_k_blocks = ga.k_blocks;
+  ga.a_rows = static_cast<int32_t>(ED);
+  ga.b_rows = static_cast<int32_t>(rows);
+  ga.out_rows_cap = static_cast<int32_t>(y_pairs ? TK : rows);
   err = beam::launch_grouped_gemm(pair ? beam::kModeDownPair : beam::kModeDown, nt_dn, tm_wd, tm_wd,
                                   tm_h, ga, grid_for(ga.m_blocks, nt_dn), s);
   if (err != cudaSuccess) return BEAM_ERR_CUDA;
   record(6, s);
 
-  if (finish_combine(c, y, pa.pair_row, T, out, y_pairs, boundary, s) != cudaSuccess)
+  if (finish_combine(c, y, pa.pair_row, T, out, y_pairs, boundary, pa.status, s) != cudaSuccess)
     return BEAM_ERR_CUDA;
   record(7, s);
   return cuda_status(cudaGetLastError());
@@ -499,7 +505,7 @@ beam_status_t run_experts_nvfp4(const beam_moe_config_t& c, const void* hidden, 
   uint8_t* hsf = at<uint8_t>(ws, L.h_sf);
   float* y = at<float>(ws, L.y);
   beam::launch_quantize_tokens(static_cast<const uint16_t*>(hidden), pa.pair_row, T, c.topk, c.d,
-                               xq, xsf, s);
+                               xq, xsf, status, s);
   record(4, s);
   if (cudaGetLastError() != cudaSuccess) return BEAM_ERR_CUDA;
 
@@ -535,6 +541,9 @@ beam_status_t run_experts_nvfp4(const beam_moe_config_t& c, const void* hidden, 
   fa.rows_per_expert = c.d_ff;
   fa.m_blocks = c.d_ff / 128;
   fa.k_blocks = c.d / 256;
+  fa.a_rows = static_cast<int32_t>(EF);
+  fa.b_rows = static_cast<int32_t>(rows);
+  fa.out_rows_cap = static_cast<int32_t>(rows);
   if (beam::launch_fp4_gemm(true, nt, tm_g, tm_u, tm_x, tm_xsf, fa, grid_for(fa.m_blocks), s) !=
       cudaSuccess)
     return BEAM_ERR_CUDA;
@@ -551,11 +560,13 @@ beam_status_t run_experts_nvfp4(const beam_moe_config_t& c, const void* hidden, 
   fa.rows_per_expert = c.d;
   fa.m_blocks = c.d / 256;  // pairs of 128-row weight blocks
   fa.k_blocks = c.d_ff / 256;
+  fa.a_rows = static_cast<int32_t>(ED);
+  fa.out_rows_cap = static_cast<int32_t>(y_pairs ? TK : rows);
   if (beam::launch_fp4_gemm(false, nt, tm_d, tm_d, tm_h, tm_hsf, fa, grid_for(fa.m_blocks), s) !=
       cudaSuccess)
     return BEAM_ERR_CUDA;
   record(6, s);
-  if (finish_combine(c, y, pa.pair_row, T, out, y_pairs, boundary, s) != cudaSuccess)
+  if (finish_combine(c, y, pa.pair_row, T, out, y_pairs, boundary, pa.status, s) != cudaSuccess)
     return BEAM_ERR_CUDA;
   record(7, s);
   return cuda_status(cudaGetLastError());
@@ -583,7 +594,7 @@ beam_status_t run_experts_mxfp8(const beam_moe_config_t& c, const void* hidden, 
   uint8_t* hsf = at<uint8_t>(ws, L.h_sf);
   float* y = at<float>(ws, L.y);
   beam::launch_quantize_tokens_mx(static_cast<const uint16_t*>(hidden), pa.pair_row, T, c.topk,
-                                  c.d, xq, xsf, s);
+                                  c.d, xq, xsf, pa.status, s);
   record(4, s);
   if (cudaGetLastError() != cudaSuccess) return BEAM_ERR_CUDA;
 
@@ -616,6 +627,9 @@ beam_status_t run_experts_mxfp8(const beam_moe_config_t& c, const void* hidden, 
   fa.rows_per_expert = c.d_ff;
   fa.m_blocks = c.d_ff / 128;
   fa.k_blocks = c.d / 128;
+  fa.a_rows = static_cast<int32_t>(EF);
+  fa.b_rows = static_cast<int32_t>(rows);
+  fa.out_rows_cap = static_cast<int32_t>(rows);
   if (beam::launch_mxfp8_gemm(true, nt, tm_g, tm_u, tm_x, tm_xsf, fa, grid_for(fa.m_blocks), s) !=
       cudaSuccess)
     return BEAM_ERR_CUDA;
@@ -629,11 +643,13 @@ beam_status_t run_experts_mxfp8(const beam_moe_config_t& c, const void* hidden, 
   fa.rows_per_expert = c.d;
   fa.m_blocks = c.d / 256;  // pairs of 128-row weight blocks
   fa.k_blocks = c.d_ff / 128;
+  fa.a_rows = static_cast<int32_t>(ED);
+  fa.out_rows_cap = static_cast<int32_t>(rows);
   if (beam::launch_mxfp8_gemm(false, nt, tm_d, tm_d, tm_h, tm_hsf, fa, grid_for(fa.m_blocks), s) !=
       cudaSuccess)
     return BEAM_ERR_CUDA;
   record(6, s);
-  if (finish_combine(c, y, pa.pair_row, T, out, nullptr, boundary, s) != cudaSuccess)
+  if (finish_combine(c, y, pa.pair_row, T, out, nullptr, boundary, pa.status, s) != cudaSuccess)
     return BEAM_ERR_CUDA;
   record(7, s);
   return cuda_status(cudaGetLastError());
@@ -670,7 +686,7 @@ beam_status_t run_experts_fp8(const beam_moe_config_t& c, const void* hidden, co
   uint8_t* xp = at<uint8_t>(ws, L.x_perm);
   if (!row_gather)
     beam::launch_scatter_tokens(reinterpret_cast<const uint16_t*>(xq), pa.pair_row, T, c.topk,
-                                c.d / 2, reinterpret_cast<uint16_t*>(xp), s);
+                                c.d / 2, reinterpret_cast<uint16_t*>(xp), pa.status, s);
   record(4, s);
   if (cudaGetLastError() != cudaSuccess) return BEAM_ERR_CUDA;
 
@@ -709,6 +725,9 @@ beam_status_t run_experts_fp8(const beam_moe_config_t& c, const void* hidden, co
   ga.m_blocks = c.d_ff / 128;
   ga.k_blocks = c.d / 128;
   ga.b_k_blocks = ga.k_blocks;
+  ga.a_rows = static_cast<int32_t>(EF);
+  ga.b_rows = static_cast<int32_t>(row_gather ? T : rows);
+  ga.out_rows_cap = static_cast<int32_t>(rows);
   ga.a0_scale = gate.scale;
   ga.a1_scale = up.scale;
   ga.b_scale = xs;  // per token
@@ -727,6 +746,9 @@ beam_status_t run_experts_fp8(const beam_moe_config_t& c, const void* hidden, co
   ga.m_blocks = pair ? c.d / 256 : c.d / 128;
   ga.k_blocks = c.d_ff / 128;
   ga.b_k_blocks = ga.k_blocks;
+  ga.a_rows = static_cast<int32_t>(ED);
+  ga.b_rows = static_cast<int32_t>(rows);
+  ga.out_rows_cap = static_cast<int32_t>(y_pairs ? TK : rows);
   ga.a0_scale = down.scale;
   ga.a1_scale = nullptr;
   ga.b_scale = hs;  // per permuted row
@@ -734,7 +756,7 @@ beam_status_t run_experts_fp8(const beam_moe_config_t& c, const void* hidden, co
                                 tm_h, ga, grid_for(ga.m_blocks, nt_dn), s, true) != cudaSuccess)
     return BEAM_ERR_CUDA;
   record(6, s);
-  if (finish_combine(c, y, pa.pair_row, T, out, y_pairs, boundary, s) != cudaSuccess)
+  if (finish_combine(c, y, pa.pair_row, T, out, y_pairs, boundary, pa.status, s) != cudaSuccess)
     return BEAM_ERR_CUDA;
   record(7, s);
   return cuda_status(cudaGetLastError());
@@ -792,6 +814,9 @@ beam_status_t run_experts_w4a16(const beam_moe_config_t& c, const void* hidden, 
   ga.rows_per_expert = c.d_ff;
   ga.m_blocks = c.d_ff / 128;
   ga.k_blocks = c.d / 256;
+  ga.a_rows = static_cast<int32_t>(EF);
+  ga.b_rows = static_cast<int32_t>(rows);
+  ga.out_rows_cap = static_cast<int32_t>(rows);
   if (beam::launch_w4a16_gemm(true, nt, tm_g, tm_u, tm_x, ga, grid_for(ga.m_blocks), s) !=
       cudaSuccess)
     return BEAM_ERR_CUDA;
@@ -806,11 +831,13 @@ beam_status_t run_experts_w4a16(const beam_moe_config_t& c, const void* hidden, 
   ga.rows_per_expert = c.d;
   ga.m_blocks = c.d / 128;
   ga.k_blocks = c.d_ff / 256;
+  ga.a_rows = static_cast<int32_t>(ED);
+  ga.out_rows_cap = static_cast<int32_t>(rows);
   if (beam::launch_w4a16_gemm(false, nt, tm_d, tm_d, tm_h, ga, grid_for(ga.m_blocks), s) !=
       cudaSuccess)
     return BEAM_ERR_CUDA;
   record(6, s);
-  if (finish_combine(c, y, pa.pair_row, T, out, nullptr, boundary, s) != cudaSuccess)
+  if (finish_combine(c, y, pa.pair_row, T, out, nullptr, boundary, pa.status, s) != cudaSuccess)
     return BEAM_ERR_CUDA;
   record(7, s);
   return cuda_status(cudaGetLastError());
@@ -897,16 +924,46 @@ beam_status_t forward_quantised(const beam_moe_config_t* cfg, int32_t fmt, const
 constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;  // 32 MiB
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 
+// The context current on the calling thread (the driver's cuCtxGetCurrent,
+// fetched through the runtime like the tensor-map encoder); nullptr if the
+// query fails.
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+
+CUcontext current_context() {
+  static CtxGetCurrentFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CtxGetCurrentFn>(f);
+  });
+  CUcontext c = nullptr;
+  if (!fn || fn(&c) != CUDA_SUCCESS) return nullptr;
+  return c;
+}
+
+// The array's device address on the current device, looked up once per
+// device and context: a new context on the device (after cudaDeviceReset,
+// say) loads the module again at another address, so the cached one is
+// dropped when the current context is not the one it was taken in.
 void* noalloc_scratch_address() {
   static void* addr[64] = {};
+  static CUcontext ctx[64] = {};
   static std::mutex mu;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  CUcontext cur = current_context();  // none yet on a thread that has not used the device
   std::lock_guard<std::mutex> lock(mu);
-  if (!addr[dev]) {
+  if (!cur || !addr[dev] || ctx[dev] != cur) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
+    cur = current_context();  // the lookup made the device's context current
+    if (!cur) return nullptr;
     addr[dev] = p;
+    ctx[dev] = cur;
   }
   return addr[dev];
 }
@@ -1378,7 +1435,7 @@ beam_status_t beam_moe_ep_combine(const beam_moe_config_t* cfg, const float* y_b
   if (!aligned16(y_back) || !aligned16(out)) return BEAM_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   beam::launch_combine(y_back, at<int32_t>(workspace, L.pair_row), T, cfg->topk, cfg->d,
-                       static_cast<uint16_t*>(out), s);
+                       static_cast<uint16_t*>(out), at<uint32_t>(workspace, L.status), s);
   record(7, s);
   return cuda_status(cudaGetLastError());
 }

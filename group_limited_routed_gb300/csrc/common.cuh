@@ -15,6 +15,28 @@ __device__ __forceinline__ void latch_status(uint32_t* status, uint32_t code) {
   atomicCAS(status, 0u, code);
 }
 
+// Bounds checks of the debug build.  Compiled with -DBEAM_DEVICE_CHECKS=1
+// (build(checked=True)), every checked index -- a permuted row, a TMA
+// coordinate, a TMEM column, a tile -- that falls outside its buffer
+// latches BEAM_ERR_DEVICE_CHECK in the call's status word, and the caller
+// skips the access (or clamps a copy's coordinates, so that the barrier the
+// copy signals still completes).  Nothing traps.  The default build compiles
+// the checks out: in_bounds() is then `true`.
+#ifndef BEAM_DEVICE_CHECKS
+#define BEAM_DEVICE_CHECKS 0
+#endif
+
+__device__ __forceinline__ bool in_bounds(bool ok, uint32_t* status) {
+#if BEAM_DEVICE_CHECKS
+  if (!ok) latch_status(status, kStatusDeviceCheck);
+  return ok;
+#else
+  (void)ok;
+  (void)status;
+  return true;
+#endif
+}
+
 // ---------------------------------------------------------------- routing
 struct RouterArgs {
   const uint16_t* x;       // [T, d] bf16
@@ -69,11 +91,12 @@ cudaError_t launch_fused_route(const RouterArgs& ra, int ksplit, const SelectArg
 void launch_gather(const uint16_t* x, const int32_t* perm_src, const int32_t* n_valid, int64_t TK,
                    int32_t k, int32_t d, uint16_t* x_perm, cudaStream_t s);
 // token rows x [T, n16 16-bit words] -> each token's k permuted rows
-// pair_row[t * k + j] of x_perm (each row read once; k <= 32)
+// pair_row[t * k + j] of x_perm (each row read once; k <= 32).  `status`
+// receives the debug build's bounds-check failures.
 void launch_scatter_tokens(const uint16_t* x, const int32_t* pair_row, int64_t T, int32_t k,
-                           int32_t n16, uint16_t* x_perm, cudaStream_t s);
+                           int32_t n16, uint16_t* x_perm, uint32_t* status, cudaStream_t s);
 void launch_combine(const float* y, const int32_t* pair_row, int64_t T, int32_t k, int32_t d,
-                    uint16_t* out, cudaStream_t s);
+                    uint16_t* out, uint32_t* status, cudaStream_t s);
 
 // the decoder's sublayer boundary after the layer: post-norm, depth-scaled
 // residual add, next pre-norm
@@ -89,7 +112,7 @@ struct BoundaryArgs {
 // shared memory per block
 cudaError_t launch_combine_boundary(const float* y, const int32_t* pair_row, int64_t T, int32_t k,
                                     int32_t d, uint16_t* out, const BoundaryArgs& b,
-                                    cudaStream_t s);
+                                    uint32_t* status, cudaStream_t s);
 
 // W_r [E, d] FP32 -> planes [E, 3d] BF16 (hi | mid | lo, W = hi + mid + lo to
 // within 2^-24 relative).
@@ -128,6 +151,11 @@ struct Fp4GemmArgs {
   int32_t weight_evict_first;
   uint32_t* status;
   uint64_t wait_limit_ns;
+  // extents for the debug build's bounds checks: weight rows (E * N), token
+  // operand rows, output rows
+  int32_t a_rows;
+  int32_t b_rows;
+  int32_t out_rows_cap;
 };
 
 // ---------------------------------------------------------------- W4A16
@@ -149,6 +177,10 @@ struct W4a16GemmArgs {
   int32_t weight_evict_first;
   uint32_t* status;
   uint64_t wait_limit_ns;
+  // extents for the debug build's bounds checks (as Fp4GemmArgs)
+  int32_t a_rows;
+  int32_t b_rows;
+  int32_t out_rows_cap;
 };
 // permuted token rows -> F16 [rows, d] (saturating at 65504)
 void launch_gather_f16(const uint16_t* x, const int32_t* perm_src, const int32_t* n_valid,
@@ -169,7 +201,8 @@ void launch_quantize_e4m3_rows(const uint16_t* x, const int32_t* n_valid, int64_
 // 16-byte slot, 4 scales + padding, per 64 elements) of each token's k
 // permuted rows pair_row[t * k + j]; each token is quantised once (k <= 32)
 void launch_quantize_tokens(const uint16_t* x, const int32_t* pair_row, int64_t T, int32_t k,
-                            int32_t d, uint8_t* xq, uint8_t* xsf, cudaStream_t s);
+                            int32_t d, uint8_t* xq, uint8_t* xsf, uint32_t* status,
+                            cudaStream_t s);
 // block-scaled FP4 grouped GEMM, nt = 16 | 32; sfb maps the token scales; the
 // down GEMM works on pairs of adjacent 128-row weight blocks (m_blocks = d / 256)
 cudaError_t launch_fp4_gemm(bool gateup, int nt, const CUtensorMap& a0, const CUtensorMap& a1,
@@ -179,7 +212,8 @@ cudaError_t launch_fp4_gemm(bool gateup, int nt, const CUtensorMap& a0, const CU
 // 16-byte slot, 4 scales + padding, per 128 elements) of each token's k
 // permuted rows pair_row[t * k + j] (k <= 32)
 void launch_quantize_tokens_mx(const uint16_t* x, const int32_t* pair_row, int64_t T, int32_t k,
-                               int32_t d, uint8_t* xq, uint8_t* xsf, cudaStream_t s);
+                               int32_t d, uint8_t* xq, uint8_t* xsf, uint32_t* status,
+                               cudaStream_t s);
 // the MXFP8 grouped GEMM (E4M3 x E4M3, E8M0 per 32), as launch_fp4_gemm
 cudaError_t launch_mxfp8_gemm(bool gateup, int nt, const CUtensorMap& a0, const CUtensorMap& a1,
                               const CUtensorMap& b, const CUtensorMap& sfb, const Fp4GemmArgs& p,

@@ -38,6 +38,12 @@ struct GemmArgs {
   const float* a0_scale;
   const float* a1_scale;
   const float* b_scale;
+  // extents for the debug build's bounds checks: weight rows of the A tensor
+  // map (E * rows_per_expert), rows of the token tensor map, rows of the
+  // output buffer
+  int32_t a_rows;
+  int32_t b_rows;
+  int32_t out_rows_cap;
 };
 
 // Persistent grouped GEMM; `nt` is the token-block width, 16 or 256 (the

@@ -145,6 +145,7 @@ __global__ void __launch_bounds__(threads_for(NT, MODE), 1)
   int32_t* misc = reinterpret_cast<int32_t*>(bars + C::NUM_BARS);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc);
   volatile int32_t* abort_flag = misc + 1;
+  int32_t* s_total = misc + 2;  // permuted rows of all experts (offsets[E])
   int32_t* s_cnt = misc + 4;
   int32_t* s_off = s_cnt + kMaxE;
   int32_t* s_start = s_off + kMaxE;
@@ -177,6 +178,7 @@ __global__ void __launch_bounds__(threads_for(NT, MODE), 1)
     }
     ptx::mbar_init(done_bar, 1);
     *abort_flag = 0;
+    *s_total = p.offsets[E];
     ptx::fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
@@ -215,6 +217,16 @@ __global__ void __launch_bounds__(threads_for(NT, MODE), 1)
   const uint32_t tmem_base = *tmem_slot;
   const int num_tiles = s_start[E];
   const Waiter W{abort_flag, p.status, p.wait_limit_ns};
+  // a tile to work on: rows to process, and (debug build) every index of it
+  // inside its buffers; every role decides alike, so a bad tile is skipped
+  // by all of them
+  auto use_tile = [&](const TileInfo& ti) {
+    if (ti.nvalid <= 0) return false;
+    return in_bounds(ti.expert >= 0 && ti.expert < E && ti.mblock >= 0 &&
+                         ti.mblock < p.m_blocks && ti.row0 >= 0 &&
+                         ti.row0 + ti.nvalid <= *s_total && ti.n_mma <= NT,
+                     p.status);
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------ weight producer
@@ -230,8 +242,11 @@ __global__ void __launch_bounds__(threads_for(NT, MODE), 1)
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
         const TileInfo ti = decode_tile<NT>(tile, s_start, s_cnt, s_off, E);
-        if (ti.nvalid <= 0) continue;
-        const int a_row = ti.expert * p.rows_per_expert + ti.mblock * (PAIR ? 2 * BM : BM);
+        if (!use_tile(ti)) continue;
+        int a_row = ti.expert * p.rows_per_expert + ti.mblock * (PAIR ? 2 * BM : BM);
+        // the box's rows inside the weight tensor (else read row 0: the stage
+        // still fills and the tile's result is void)
+        if (!in_bounds(a_row + (PAIR ? 2 * BM : BM) <= p.a_rows, p.status)) a_row = 0;
         for (int kb = 0; kb < p.k_blocks; ++kb) {
           if (!W.wait(emptyA(stage), phase ^ 1u)) {
             ok = false;
@@ -277,15 +292,20 @@ __global__ void __launch_bounds__(threads_for(NT, MODE), 1)
     bool ok = true;
     for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
       const TileInfo ti = decode_tile<NT>(tile, s_start, s_cnt, s_off, E);
-      if (ti.nvalid <= 0) continue;
+      if (!use_tile(ti)) continue;
       int tok[RPL];
       if constexpr (ROW_GATHER) {
 #pragma unroll
         for (int j = 0; j < RPL; ++j) {
           const int r = lane + 32 * j;
           tok[j] = r < ti.nvalid ? p.perm_src[ti.row0 + r] / p.topk : -1;
+          // a row of the hidden states (else row 0 is read into its place)
+          if (r < ti.nvalid && !in_bounds(tok[j] >= 0 && tok[j] < p.b_rows, p.status)) tok[j] = 0;
         }
       }
+      // (tile loads: the block's first row inside the gathered copy; a row
+      // gather addresses the hidden states by token instead, checked above)
+      const int b_row0 = ROW_GATHER || in_bounds(ti.row0 < p.b_rows, p.status) ? ti.row0 : 0;
       const uint32_t tx_bytes =
           ROW_GATHER ? static_cast<uint32_t>(ti.nvalid) * kRowBytes : C::B_STAGE;
       for (int kb = 0; kb < p.k_blocks; ++kb) {
@@ -299,7 +319,7 @@ __global__ void __launch_bounds__(threads_for(NT, MODE), 1)
         const uint32_t st = b_ring + stage * C::B_STAGE;
         if (lane == 0) {
           ptx::mbar_arrive_expect_tx(fullB(stage), tx_bytes);
-          if (!ROW_GATHER) ptx::tma_load_2d(st, &tm_b, fullB(stage), kb * KE, ti.row0, pol_b);
+          if (!ROW_GATHER) ptx::tma_load_2d(st, &tm_b, fullB(stage), kb * KE, b_row0, pol_b);
         }
         if constexpr (ROW_GATHER) {
           __syncwarp();
@@ -333,10 +353,12 @@ __global__ void __launch_bounds__(threads_for(NT, MODE), 1)
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
         const TileInfo ti = decode_tile<NT>(tile, s_start, s_cnt, s_off, E);
-        if (ti.nvalid <= 0) continue;
+        if (!use_tile(ti)) continue;
         const uint32_t idesc = idesc_m | (static_cast<uint32_t>(ti.n_mma >> 3) << 17);
         if (!W.wait(tempty_bar(acc), acc_phase ^ 1u)) break;
         ptx::tc_fence_after();
+        // the accumulators' TMEM columns inside the allocation
+        in_bounds(acc * C::ACC_COLS + C::NUM_A * ti.n_mma <= C::TMEM_COLS, p.status);
         const uint32_t d0 = tmem_base + acc * C::ACC_COLS;
         for (int kb = 0; kb < p.k_blocks; ++kb) {
           if (!W.wait(fullA(sa), pa) || !W.wait(fullB(sb), pb)) {
@@ -397,7 +419,7 @@ __global__ void __launch_bounds__(threads_for(NT, MODE), 1)
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
       const TileInfo ti = decode_tile<NT>(tile, s_start, s_cnt, s_off, E);
-      if (ti.nvalid <= 0) continue;
+      if (!use_tile(ti)) continue;
       if (!W.wait(tfull_bar(acc), acc_phase)) break;
       ptx::tc_fence_after();
       const uint32_t tq = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * C::ACC_COLS;
@@ -413,6 +435,8 @@ __global__ void __launch_bounds__(threads_for(NT, MODE), 1)
       }
 #pragma unroll 1
       for (int c0 = col_begin; c0 < min(ti.nvalid, col_begin + COLS_PER_WARP); c0 += 16) {
+        // the chunk's TMEM columns inside its accumulator
+        if (!in_bounds(c0 + 16 <= NT, p.status)) break;
         uint32_t ra[16];
         ptx::tmem_ld16(tq + c0, ra);
         // per-token factors of the chunk's 16 columns, one column per lane
@@ -440,6 +464,10 @@ __global__ void __launch_bounds__(threads_for(NT, MODE), 1)
           for (int j = 0; j < 16; ++j) {
             // c0 + j < ti.nvalid is the same on every lane of the warp
             if (c0 + j < ti.nvalid) {
+              // (the same on every lane: the shuffle below needs all of them)
+              const int64_t hrow = ti.row0 + c0 + j;
+              if (!in_bounds(hrow < p.out_rows_cap && (ti.mblock + 1) * BM <= p.out_ld, p.status))
+                continue;
               float g = __uint_as_float(ra[j]);
               float u = __uint_as_float(rb[j]);
               if constexpr (F8) {
@@ -450,7 +478,7 @@ __global__ void __launch_bounds__(threads_for(NT, MODE), 1)
               // fast exp and divide: relative error near 1e-6, far below the
               // BF16 rounding of h that follows
               const float h = __fdividef(g, 1.0f + __expf(-g)) * u;
-              p.h_out[static_cast<int64_t>(ti.row0 + c0 + j) * p.out_ld + col] = f32_to_bf16(h);
+              p.h_out[hrow * p.out_ld + col] = f32_to_bf16(h);
             }
           }
         } else if constexpr (PAIR) {
@@ -464,6 +492,9 @@ __global__ void __launch_bounds__(threads_for(NT, MODE), 1)
             if (c0 + j < ti.nvalid) {
               const float w = __shfl_sync(kFull, lfac, j);
               const int orow = __shfl_sync(kFull, lorow, j);
+              if (!in_bounds(orow >= 0 && orow < p.out_rows_cap && pcol + BM < p.out_ld,
+                             p.status))
+                continue;
               float* dst = p.f32_out + static_cast<int64_t>(orow) * p.out_ld + pcol;
               // streaming stores: the FP32 rows are read once, by the
               // combine, and would otherwise push tiles out of L2
@@ -478,6 +509,8 @@ __global__ void __launch_bounds__(threads_for(NT, MODE), 1)
             if (c0 + j < ti.nvalid) {
               const float w = __shfl_sync(kFull, lfac, j);
               const int orow = __shfl_sync(kFull, lorow, j);
+              if (!in_bounds(orow >= 0 && orow < p.out_rows_cap && col < p.out_ld, p.status))
+                continue;
               __stcs(p.f32_out + static_cast<int64_t>(orow) * p.out_ld + col,
                      F8 ? __uint_as_float(ra[j]) * sw0 * w : __uint_as_float(ra[j]) * w);
             }

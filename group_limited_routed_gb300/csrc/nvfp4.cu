@@ -128,10 +128,15 @@ __global__ void __launch_bounds__(128) quantize_tokens_kernel(const uint16_t* __
                                                               const int32_t* __restrict__ pair_row,
                                                               int32_t k, int32_t d,
                                                               uint8_t* __restrict__ xq,
-                                                              uint8_t* __restrict__ xsf) {
+                                                              uint8_t* __restrict__ xsf,
+                                                              uint32_t* status) {
   const int64_t t = blockIdx.x;
   __shared__ int64_t s_row[32];
-  if (threadIdx.x < k) s_row[threadIdx.x] = pair_row[t * k + threadIdx.x];
+  if (threadIdx.x < k) {
+    const int64_t row = pair_row[t * k + threadIdx.x];
+    s_row[threadIdx.x] =
+        in_bounds(row < static_cast<int64_t>(gridDim.x) * k, status) ? row : -1;
+  }
   __syncthreads();
   const uint4* src = reinterpret_cast<const uint4*>(x + t * d);
   for (int blk = threadIdx.x; blk < d / 16; blk += blockDim.x) {
@@ -174,10 +179,15 @@ __global__ void __launch_bounds__(128) quantize_tokens_mx_kernel(const uint16_t*
                                                                  const int32_t* __restrict__ pair_row,
                                                                  int32_t k, int32_t d,
                                                                  uint8_t* __restrict__ xq,
-                                                                 uint8_t* __restrict__ xsf) {
+                                                                 uint8_t* __restrict__ xsf,
+                                                                 uint32_t* status) {
   const int64_t t = blockIdx.x;
   __shared__ int64_t s_row[32];
-  if (threadIdx.x < k) s_row[threadIdx.x] = pair_row[t * k + threadIdx.x];
+  if (threadIdx.x < k) {
+    const int64_t row = pair_row[t * k + threadIdx.x];
+    s_row[threadIdx.x] =
+        in_bounds(row < static_cast<int64_t>(gridDim.x) * k, status) ? row : -1;
+  }
   __syncthreads();
   const uint4* src = reinterpret_cast<const uint4*>(x + t * d);
   for (int blk = threadIdx.x; blk < d / 32; blk += blockDim.x) {
@@ -278,6 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   int32_t* misc = reinterpret_cast<int32_t*>(bars + C::NUM_BARS);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc);
   volatile int32_t* abort_flag = misc + 1;
+  int32_t* s_total = misc + 2;  // permuted rows of all experts (offsets[E])
   int32_t* s_cnt = misc + 4;
   int32_t* s_off = s_cnt + kMaxE;
   int32_t* s_start = s_off + kMaxE;
@@ -304,6 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     ptx::mbar_init(done_bar, 1);
     *abort_flag = 0;
+    *s_total = p.offsets[E];
     ptx::fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
@@ -343,6 +355,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem_base = *tmem_slot;
   const int num_tiles = s_start[E];
   const Waiter W{abort_flag, p.status, p.wait_limit_ns};
+  // a tile to work on (see expert_gemm_kernel): rows to process, and (debug
+  // build) every index of it inside its buffers, decided alike by every role
+  auto use_tile = [&](const TileInfo& ti) {
+    if (ti.nvalid <= 0) return false;
+    return in_bounds(ti.expert >= 0 && ti.expert < E && ti.mblock >= 0 &&
+                         ti.mblock < p.m_blocks && ti.row0 >= 0 &&
+                         ti.row0 + ti.nvalid <= *s_total && ti.n_mma <= NT,
+                     p.status);
+  };
   // weight scales: blocks of 128 rows x 4 scales; a stage takes SBS blocks
   const int64_t sf_blocks_per_row_tile = static_cast<int64_t>(p.k_blocks) * C::SBS;
 
@@ -359,8 +380,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
         const TileInfo ti = decode_tile<NT>(tile, s_start, s_cnt, s_off, E);
-        if (ti.nvalid <= 0) continue;
-        const int a_row = ti.expert * p.rows_per_expert + ti.mblock * (PAIR ? 2 * BM : BM);
+        if (!use_tile(ti)) continue;
+        int a_row = ti.expert * p.rows_per_expert + ti.mblock * (PAIR ? 2 * BM : BM);
+        // the boxes' rows (and so their scale blocks) inside the weight
+        // tensor, the token box's first row inside the token operand
+        if (!in_bounds(a_row + (PAIR ? 2 * BM : BM) <= p.a_rows, p.status)) a_row = 0;
+        const int b_row0 = in_bounds(ti.row0 < p.b_rows, p.status) ? ti.row0 : 0;
         const int64_t sf_row_tile = a_row / BM;
         for (int kb = 0; kb < p.k_blocks; ++kb) {
           if (!W.wait(empty_bar(stage), phase ^ 1u)) {
@@ -382,11 +407,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::bulk_load(st + C::OFF_SFA + C::SFA_BYTES,
                            p.sfa0 + sf_off + sf_blocks_per_row_tile * 512, C::SFA_BYTES, fb);
           }
-          ptx::tma_load_2d(st + C::OFF_B, &tm_b, fb, kb * BK_BYTES, ti.row0, pol_b);
+          ptx::tma_load_2d(st + C::OFF_B, &tm_b, fb, kb * BK_BYTES, b_row0, pol_b);
 #pragma unroll
           for (int c = 0; c < C::SBS; ++c)
             ptx::tma_load_2d(st + C::OFF_SFB + 512 * c, &tm_sfb, fb, (C::SBS * kb + c) * 16,
-                             ti.row0, pol_b);
+                             b_row0, pol_b);
           last_parity[stage] = static_cast<int>(phase);
           if (++stage == C::STAGES) {
             stage = 0;
@@ -409,11 +434,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
         const TileInfo ti = decode_tile<NT>(tile, s_start, s_cnt, s_off, E);
-        if (ti.nvalid <= 0) continue;
+        if (!use_tile(ti)) continue;
         const uint32_t idesc = MX ? ptx::idesc_mx8_f32(BM, static_cast<uint32_t>(ti.n_mma))
                                   : ptx::idesc_fp4_f32(BM, static_cast<uint32_t>(ti.n_mma));
         if (!W.wait(tempty_bar(acc), acc_phase ^ 1u)) break;
         ptx::tc_fence_after();
+        // the accumulators below the scale columns
+        in_bounds(acc * C::ACC_COLS + C::NUM_A * ti.n_mma <= C::SF_BASE, p.status);
         const uint32_t d0 = tmem_base + acc * C::ACC_COLS;
         for (int kb = 0; kb < p.k_blocks; ++kb) {
           if (!W.wait(full_bar(stage), phase)) {
@@ -477,7 +504,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
       const TileInfo ti = decode_tile<NT>(tile, s_start, s_cnt, s_off, E);
-      if (ti.nvalid <= 0) continue;
+      if (!use_tile(ti)) continue;
       if (!W.wait(tfull_bar(acc), acc_phase)) break;
       ptx::tc_fence_after();
       const uint32_t tq = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * C::ACC_COLS;
@@ -485,6 +512,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float gs0 = MX ? 1.f : p.gs0[ti.expert];
 #pragma unroll 1
       for (int c0 = 0; c0 < ti.nvalid; c0 += 16) {
+        // the chunk's TMEM columns inside its accumulator
+        if (!in_bounds(c0 + 16 <= NT, p.status)) break;
         uint32_t ra[16];
         ptx::tmem_ld16(tq + c0, ra);
         if constexpr (GATEUP && MX) {
@@ -495,6 +524,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < 16; ++j) {
             if (c0 + j < ti.nvalid) {  // uniform across the warp
               const int64_t row = ti.row0 + c0 + j;
+              // uniform too (the shuffles below need every lane)
+              if (!in_bounds(row < p.out_rows_cap && (ti.mblock + 1) * BM <= p.out_ld, p.status))
+                continue;
               const float g = __uint_as_float(ra[j]);
               const float u = __uint_as_float(rb[j]);
               const float h = g / (1.0f + expf(-g)) * u;
@@ -518,6 +550,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < 16; ++j) {
             if (c0 + j < ti.nvalid) {  // uniform across the warp
               const int64_t row = ti.row0 + c0 + j;
+              if (!in_bounds(row < p.out_rows_cap && (ti.mblock + 1) * BM <= p.out_ld, p.status))
+                continue;
               const float g = __uint_as_float(ra[j]) * gs0;
               const float u = __uint_as_float(rb[j]) * gs1;
               const float h = g / (1.0f + expf(-g)) * u;
@@ -546,6 +580,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (c0 + j < ti.nvalid) {
               const int row = ti.row0 + c0 + j;
               const int orow = p.out_rows ? p.out_rows[row] : row;
+              if (!in_bounds(orow >= 0 && orow < p.out_rows_cap && pcol + BM < p.out_ld,
+                             p.status))
+                continue;
               const float wr = gs0 * p.perm_w[row];
               p.y[static_cast<int64_t>(orow) * p.out_ld + pcol] = __uint_as_float(ra[j]) * wr;
               p.y[static_cast<int64_t>(orow) * p.out_ld + pcol + BM] = __uint_as_float(rb[j]) * wr;
@@ -557,6 +594,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < 16; ++j) {
             if (c0 + j < ti.nvalid) {
               const int row = ti.row0 + c0 + j;
+              if (!in_bounds(row < p.out_rows_cap && col < p.out_ld, p.status)) continue;
               p.y[static_cast<int64_t>(row) * p.out_ld + col] =
                   __uint_as_float(ra[j]) * gs0 * p.perm_w[row];
             }
@@ -600,9 +638,11 @@ void launch_pack_scales(const uint8_t* src, int64_t rows, int64_t S, uint8_t* ds
 }
 
 void launch_quantize_tokens(const uint16_t* x, const int32_t* pair_row, int64_t T, int32_t k,
-                            int32_t d, uint8_t* xq, uint8_t* xsf, cudaStream_t s) {
+                            int32_t d, uint8_t* xq, uint8_t* xsf, uint32_t* status,
+                            cudaStream_t s) {
   if (T <= 0) return;
-  quantize_tokens_kernel<<<static_cast<unsigned>(T), 128, 0, s>>>(x, pair_row, k, d, xq, xsf);
+  quantize_tokens_kernel<<<static_cast<unsigned>(T), 128, 0, s>>>(x, pair_row, k, d, xq, xsf,
+                                                                  status);
 }
 
 cudaError_t launch_fp4_gemm(bool gateup, int nt, const CUtensorMap& a0, const CUtensorMap& a1,
@@ -621,9 +661,11 @@ cudaError_t launch_fp4_gemm(bool gateup, int nt, const CUtensorMap& a0, const CU
 }
 
 void launch_quantize_tokens_mx(const uint16_t* x, const int32_t* pair_row, int64_t T, int32_t k,
-                               int32_t d, uint8_t* xq, uint8_t* xsf, cudaStream_t s) {
+                               int32_t d, uint8_t* xq, uint8_t* xsf, uint32_t* status,
+                               cudaStream_t s) {
   if (T <= 0) return;
-  quantize_tokens_mx_kernel<<<static_cast<unsigned>(T), 128, 0, s>>>(x, pair_row, k, d, xq, xsf);
+  quantize_tokens_mx_kernel<<<static_cast<unsigned>(T), 128, 0, s>>>(x, pair_row, k, d, xq, xsf,
+                                                                     status);
 }
 
 cudaError_t launch_mxfp8_gemm(bool gateup, int nt, const CUtensorMap& a0, const CUtensorMap& a1,

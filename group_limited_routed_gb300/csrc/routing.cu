@@ -542,9 +542,12 @@ __device__ __forceinline__ void permute_expert(const PermuteArgs& a, int e) {
     for (int j = 0; j < kPermPer; ++j) {
       if (mask & (1u << j)) {
         const int64_t i = i0 + j;
-        a.perm_src[row] = static_cast<int>(i);
-        a.pair_row[i] = row;
-        a.perm_w[row] = a.w[i];
+        // the permuted row inside [0, TK)
+        if (in_bounds(row >= 0 && row < a.TK, a.status)) {
+          a.perm_src[row] = static_cast<int>(i);
+          a.pair_row[i] = row;
+          a.perm_w[row] = a.w[i];
+        }
         ++row;
       }
     }
@@ -654,9 +657,12 @@ __global__ void __launch_bounds__(256) permute_sort_kernel(PermuteArgs a, int32_
           total += x;
         }
         const int pos = s_h[v] + before + rank;
-        a.perm_src[pos] = static_cast<int>(i);
-        a.pair_row[i] = pos;
-        a.perm_w[pos] = a.w[i];
+        // the permuted row inside [0, TK)
+        if (in_bounds(pos >= 0 && pos < a.TK, a.status)) {
+          a.perm_src[pos] = static_cast<int>(i);
+          a.pair_row[i] = pos;
+          a.perm_w[pos] = a.w[i];
+        }
       }
       __syncthreads();
       if (valid && before + rank + 1 == total) s_h[v] += total;
@@ -674,10 +680,16 @@ __global__ void __launch_bounds__(256) permute_sort_kernel(PermuteArgs a, int32_
 __global__ void __launch_bounds__(128) scatter_tokens_kernel(const uint16_t* __restrict__ x,
                                                              const int32_t* __restrict__ pair_row,
                                                              int32_t k, int32_t n16,
-                                                             uint16_t* __restrict__ xp) {
+                                                             uint16_t* __restrict__ xp,
+                                                             uint32_t* status) {
   const int64_t t = blockIdx.x;
   __shared__ int64_t s_row[32];
-  if (threadIdx.x < k) s_row[threadIdx.x] = pair_row[t * k + threadIdx.x];
+  if (threadIdx.x < k) {
+    const int64_t row = pair_row[t * k + threadIdx.x];
+    // a row of x_perm: fewer than T * k of them
+    s_row[threadIdx.x] =
+        in_bounds(row < static_cast<int64_t>(gridDim.x) * k, status) ? row : -1;
+  }
   __syncthreads();
   const uint4* src = reinterpret_cast<const uint4*>(x + t * n16);
   constexpr int U = 8;
@@ -728,7 +740,8 @@ __global__ void __launch_bounds__(128) gather_kernel(const uint16_t* __restrict_
 __global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ y,
                                                       const int32_t* __restrict__ pair_row,
                                                       int32_t k, int32_t d,
-                                                      uint16_t* __restrict__ out) {
+                                                      uint16_t* __restrict__ out,
+                                                      uint32_t* status) {
   const int64_t t = blockIdx.x;
   const int c8 = blockIdx.y * blockDim.x + threadIdx.x;
   if (c8 >= d / 8) return;
@@ -741,7 +754,11 @@ __global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ 
   for (int s0 = 0; s0 < k; s0 += kAhead) {
     int row[kAhead];
 #pragma unroll
-    for (int j = 0; j < kAhead; ++j) row[j] = s0 + j < k ? pair_row[t * k + s0 + j] : -1;
+    for (int j = 0; j < kAhead; ++j) {
+      row[j] = s0 + j < k ? pair_row[t * k + s0 + j] : -1;
+      // a row of y: fewer than T * k of them
+      if (!in_bounds(row[j] < static_cast<int64_t>(gridDim.x) * k, status)) row[j] = -1;
+    }
     float4 a[kAhead], b[kAhead];
 #pragma unroll
     for (int j = 0; j < kAhead; ++j) {
@@ -800,7 +817,7 @@ __global__ void __launch_bounds__(256) combine_boundary_kernel(const float* __re
                                                                const int32_t* __restrict__ pair_row,
                                                                int32_t k, int32_t d,
                                                                uint16_t* __restrict__ out,
-                                                               BoundaryArgs b) {
+                                                               BoundaryArgs b, uint32_t* status) {
   extern __shared__ float s_v[];  // [d] the token's current values
   __shared__ float s_red[32];
   const int64_t t = blockIdx.x;
@@ -812,7 +829,7 @@ __global__ void __launch_bounds__(256) combine_boundary_kernel(const float* __re
     for (int i = 0; i < 8; ++i) acc[i] = 0.f;
     for (int sl = 0; sl < k; ++sl) {
       const int row = pair_row[t * k + sl];
-      if (row < 0) continue;
+      if (row < 0 || !in_bounds(row < static_cast<int64_t>(gridDim.x) * k, status)) continue;
       const float4* src = reinterpret_cast<const float4*>(y + static_cast<int64_t>(row) * d) + 2 * c8;
       const float4 a = src[0];
       const float4 c = src[1];
@@ -974,12 +991,13 @@ cudaError_t launch_fused_route(const RouterArgs& ra, int ksplit, const SelectArg
 
 cudaError_t launch_combine_boundary(const float* y, const int32_t* pair_row, int64_t T, int32_t k,
                                     int32_t d, uint16_t* out, const BoundaryArgs& b,
-                                    cudaStream_t s) {
+                                    uint32_t* status, cudaStream_t s) {
   const size_t smem = static_cast<size_t>(d) * sizeof(float);
   // the largest row the entry point accepts (d <= 51200)
   const cudaError_t e = smem_limit_once<combine_boundary_kernel>(200 * 1024);
   if (e != cudaSuccess) return e;
-  combine_boundary_kernel<<<static_cast<unsigned>(T), 256, smem, s>>>(y, pair_row, k, d, out, b);
+  combine_boundary_kernel<<<static_cast<unsigned>(T), 256, smem, s>>>(y, pair_row, k, d, out, b,
+                                                                      status);
   return cudaGetLastError();
 }
 
@@ -1013,15 +1031,16 @@ void launch_gather(const uint16_t* x, const int32_t* perm_src, const int32_t* n_
 }
 
 void launch_scatter_tokens(const uint16_t* x, const int32_t* pair_row, int64_t T, int32_t k,
-                           int32_t n16, uint16_t* x_perm, cudaStream_t s) {
+                           int32_t n16, uint16_t* x_perm, uint32_t* status, cudaStream_t s) {
   if (T <= 0) return;
-  scatter_tokens_kernel<<<static_cast<unsigned>(T), 128, 0, s>>>(x, pair_row, k, n16, x_perm);
+  scatter_tokens_kernel<<<static_cast<unsigned>(T), 128, 0, s>>>(x, pair_row, k, n16, x_perm,
+                                                                 status);
 }
 
 void launch_combine(const float* y, const int32_t* pair_row, int64_t T, int32_t k, int32_t d,
-                    uint16_t* out, cudaStream_t s) {
+                    uint16_t* out, uint32_t* status, cudaStream_t s) {
   dim3 grid(static_cast<unsigned>(T), (d / 8 + 127) / 128);
-  combine_kernel<<<grid, 128, 0, s>>>(y, pair_row, k, d, out);
+  combine_kernel<<<grid, 128, 0, s>>>(y, pair_row, k, d, out, status);
 }
 
 }  // namespace beam

@@ -210,6 +210,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   int32_t* misc = reinterpret_cast<int32_t*>(bars + C::NUM_BARS);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc);
   volatile int32_t* abort_flag = misc + 1;
+  int32_t* s_total = misc + 2;  // permuted rows of all experts (offsets[E])
   int32_t* s_cnt = misc + 4;
   int32_t* s_off = s_cnt + kMaxE;
   int32_t* s_start = s_off + kMaxE;
@@ -243,6 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     ptx::mbar_init(done_bar, NI);
     *abort_flag = 0;
+    *s_total = p.offsets[E];
     ptx::fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
@@ -282,6 +284,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int num_tiles = s_start[E];
   const Waiter W{abort_flag, p.status, p.wait_limit_ns};
   const int64_t sf_blocks_per_row_tile = p.k_blocks * 4;
+  // a tile to work on (see expert_gemm_kernel): rows to process, and (debug
+  // build) every index of it inside its buffers, decided alike by every role
+  auto use_tile = [&](const TileInfo& ti) {
+    if (ti.nvalid <= 0) return false;
+    return in_bounds(ti.expert >= 0 && ti.expert < E && ti.mblock >= 0 &&
+                         ti.mblock < p.m_blocks && ti.row0 >= 0 &&
+                         ti.row0 + ti.nvalid <= *s_total && ti.n_mma <= NT,
+                     p.status);
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -297,8 +308,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
         const TileInfo ti = decode_tile<NT>(tile, s_start, s_cnt, s_off, E);
-        if (ti.nvalid <= 0) continue;
-        const int a_row = ti.expert * p.rows_per_expert + ti.mblock * BM;
+        if (!use_tile(ti)) continue;
+        int a_row = ti.expert * p.rows_per_expert + ti.mblock * BM;
+        // the boxes' rows (and so their scale blocks) inside the weight
+        // tensor, the token box's first row inside the token operand
+        if (!in_bounds(a_row + BM <= p.a_rows, p.status)) a_row = 0;
+        const int b_row0 = in_bounds(ti.row0 < p.b_rows, p.status) ? ti.row0 : 0;
         const int64_t sf_row_tile = a_row / BM;
         for (int kb = 0; kb < p.k_blocks; ++kb) {
           if (!W.wait(empty_bar(stage), phase ^ 1u)) {
@@ -318,7 +333,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int j = 0; j < 4; ++j)
             ptx::tma_load_2d(st + C::OFF_B + j * C::B_SUB, &tm_b, fb, (4 * kb + j) * KSUB,
-                             ti.row0, pol_b);
+                             b_row0, pol_b);
           last_parity[stage] = static_cast<int>(phase);
           if (++stage == C::STAGES) {
             stage = 0;
@@ -345,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
         const TileInfo ti = decode_tile<NT>(tile, s_start, s_cnt, s_off, E);
-        if (ti.nvalid <= 0) continue;
+        if (!use_tile(ti)) continue;
         const uint32_t idesc = idesc_f16_f32(BM, static_cast<uint32_t>(ti.n_mma));
         if (!W.wait(tempty_bar(acc), acc_phase ^ 1u)) break;
         ptx::tc_fence_after();
@@ -418,7 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
       const TileInfo ti = decode_tile<NT>(tile, s_start, s_cnt, s_off, E);
-      if (ti.nvalid <= 0) continue;
+      if (!use_tile(ti)) continue;
       for (int kb = 0; ok && kb < p.k_blocks; ++kb) {
         if (!W.wait(full_bar(stage), phase)) {
           ok = false;
@@ -481,7 +496,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
       const TileInfo ti = decode_tile<NT>(tile, s_start, s_cnt, s_off, E);
-      if (ti.nvalid <= 0) continue;
+      if (!use_tile(ti)) continue;
       if (!W.wait(tfull_bar(acc), acc_phase)) break;
       ptx::tc_fence_after();
       const uint32_t tq = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * C::ACC_COLS;
@@ -489,6 +504,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float gs0 = p.gs0[ti.expert];
 #pragma unroll 1
       for (int c0 = 0; c0 < ti.nvalid; c0 += 16) {
+        // the chunk's TMEM columns inside its accumulators
+        if (!in_bounds(c0 + 16 <= NT, p.status)) break;
         // the issuers' partial sums, added in issuer order
         uint32_t r[kIssuers][16];
 #pragma unroll
@@ -499,6 +516,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             if (c0 + j < ti.nvalid) {
+              if (!in_bounds(ti.row0 + c0 + j < p.out_rows_cap && col < p.out_ld, p.status))
+                continue;
               float ga = __uint_as_float(r[0][j]), ua = __uint_as_float(r[1][j]);
 #pragma unroll
               for (int i = 2; i < kIssuers; i += 2) {
@@ -516,6 +535,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < 16; ++j) {
             if (c0 + j < ti.nvalid) {
               const int row = ti.row0 + c0 + j;
+              if (!in_bounds(row < p.out_rows_cap && col < p.out_ld, p.status)) continue;
               float acc = __uint_as_float(r[0][j]);
 #pragma unroll
               for (int i = 1; i < kIssuers; ++i) acc += __uint_as_float(r[i][j]);

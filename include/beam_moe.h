@@ -212,7 +212,11 @@ beam_status_t beam_moe_forward_boundary(const beam_moe_config_t *cfg, const void
  *     (Beam shapes: up to 128 tokens).
  *   - The first call on a device looks up the array's device address (one
  *     cudaGetSymbolAddress with that device current); make that first call
- *     before any stream capture.
+ *     before any stream capture.  The address is kept per device and
+ *     context: a call in a new context on the device (after
+ *     cudaDeviceReset, for instance) looks it up again.  (The other
+ *     entry points' once-per-device kernel set-up is not redone after a
+ *     device reset: their calls then fail with BEAM_ERR_CUDA.)
  *   - Every call shares the one array and it keeps the previous call's
  *     contents; the call clears the status word it needs at zero.  Calls
  *     whose work overlaps on the GPU (other streams, other host threads) race
