@@ -143,6 +143,16 @@ bool small_batch(const beam_moe_config_t& c, int64_t TK) { return TK <= 4LL * c.
 int gateup_tile(const beam_moe_config_t& c, int64_t TK) { return small_batch(c, TK) ? 16 : 256; }
 int down_tile(const beam_moe_config_t& c, int64_t TK) { return small_batch(c, TK) ? 16 : 256; }
 
+// 256-token blocks run on clusters of two CTAs sharing M = 256 MMAs
+// (expert_gemm_pair_kernel.cuh) when the weight rows divide into the pair
+// tiles: 256 rows of d_ff for gate/up, 512 rows of d for down.
+bool pair_gateup(const beam_moe_config_t& c, int64_t TK) {
+  return !small_batch(c, TK) && c.d_ff % 256 == 0;
+}
+bool pair_down(const beam_moe_config_t& c, int64_t TK) {
+  return !small_batch(c, TK) && c.d % 512 == 0;
+}
+
 bool tensor_router(const beam_moe_config_t& c, int64_t T) {
   return T >= kTensorRouterMinT && c.n_experts % 128 == 0;
 }
@@ -414,10 +424,13 @@ beam_status_t run_experts(const beam_moe_config_t& c, const void* hidden, const 
   uint16_t* h = at<uint16_t>(ws, L.h);
   float* y = at<float>(ws, L.y);
   CUtensorMap tm_wg, tm_wu, tm_wd, tm_xp, tm_h;
+  // token boxes: one row (row gather), a whole block, or half a block for
+  // the CTA pairs
+  const bool pgu = pair_gateup(c, TK), pdn = pair_down(c, TK);
   if (!tmap_bf16(&tm_wg, w_gate, EF, c.d, 128) || !tmap_bf16(&tm_wu, w_up, EF, c.d, 128) ||
       !tmap_bf16(&tm_wd, w_down, ED, c.d_ff, 128) || !(row_gather ? tmap_bf16(&tm_xp, hidden, T, c.d, 1)
-                  : tmap_bf16(&tm_xp, xp, rows, c.d, nt_gu)) ||
-      !tmap_bf16(&tm_h, h, rows, c.d_ff, nt_dn))
+                  : tmap_bf16(&tm_xp, xp, rows, c.d, pgu ? nt_gu / 2 : nt_gu)) ||
+      !tmap_bf16(&tm_h, h, rows, c.d_ff, pdn ? nt_dn / 2 : nt_dn))
     return BEAM_ERR_CUDA;
 
   GemmArgs ga{};
@@ -448,8 +461,14 @@ beam_status_t run_experts(const beam_moe_config_t& c, const void* hidden, const 
   ga.a_rows = static_cast<int32_t>(EF);
   ga.b_rows = static_cast<int32_t>(row_gather ? T : rows);
   ga.out_rows_cap = static_cast<int32_t>(rows);
-  err = beam::launch_grouped_gemm(beam::kModeGateUp, nt_gu, tm_wg, tm_wu, tm_xp, ga,
-                                  grid_for(ga.m_blocks, nt_gu), s);
+  if (pgu) {
+    ga.m_blocks = c.d_ff / 256;
+    err = beam::launch_grouped_gemm_pair(true, tm_wg, tm_wu, tm_xp, ga,
+                                         grid_for(ga.m_blocks, nt_gu), s);
+  } else {
+    err = beam::launch_grouped_gemm(beam::kModeGateUp, nt_gu, tm_wg, tm_wu, tm_xp, ga,
+                                    grid_for(ga.m_blocks, nt_gu), s);
+  }
   if (err != cudaSuccess) return BEAM_ERR_CUDA;
   record(5, s);
 
@@ -468,8 +487,14 @@ beam_status_t run_experts(const beam_moe_config_t& c, const void* hidden, const 
   ga.a_rows = static_cast<int32_t>(ED);
   ga.b_rows = static_cast<int32_t>(rows);
   ga.out_rows_cap = static_cast<int32_t>(y_pairs ? TK : rows);
-  err = beam::launch_grouped_gemm(pair ? beam::kModeDownPair : beam::kModeDown, nt_dn, tm_wd, tm_wd,
-                                  tm_h, ga, grid_for(ga.m_blocks, nt_dn), s);
+  if (pdn) {
+    ga.m_blocks = c.d / 512;
+    err = beam::launch_grouped_gemm_pair(false, tm_wd, tm_wd, tm_h, ga,
+                                         grid_for(ga.m_blocks, nt_dn), s);
+  } else {
+    err = beam::launch_grouped_gemm(pair ? beam::kModeDownPair : beam::kModeDown, nt_dn, tm_wd,
+                                    tm_wd, tm_h, ga, grid_for(ga.m_blocks, nt_dn), s);
+  }
   if (err != cudaSuccess) return BEAM_ERR_CUDA;
   record(6, s);
 
@@ -697,10 +722,12 @@ beam_status_t run_experts_fp8(const beam_moe_config_t& c, const void* hidden, co
   float* hs = at<float>(ws, L.h_scale);
   float* y = at<float>(ws, L.y);
   CUtensorMap tm_g, tm_u, tm_d, tm_x, tm_h;
+  const bool pgu = pair_gateup(c, TK), pdn = pair_down(c, TK);
   if (!tmap_u8(&tm_g, gate.q, EF, c.d, 128, 128) || !tmap_u8(&tm_u, up.q, EF, c.d, 128, 128) ||
       !tmap_u8(&tm_d, down.q, ED, c.d_ff, 128, 128) ||
-      !(row_gather ? tmap_u8(&tm_x, xq, T, c.d, 128, 1) : tmap_u8(&tm_x, xp, rows, c.d, 128, nt_gu)) ||
-      !tmap_u8(&tm_h, hq, rows, c.d_ff, 128, nt_dn))
+      !(row_gather ? tmap_u8(&tm_x, xq, T, c.d, 128, 1)
+                   : tmap_u8(&tm_x, xp, rows, c.d, 128, pgu ? nt_gu / 2 : nt_gu)) ||
+      !tmap_u8(&tm_h, hq, rows, c.d_ff, 128, pdn ? nt_dn / 2 : nt_dn))
     return BEAM_ERR_CUDA;
 
   GemmArgs ga{};
@@ -731,8 +758,11 @@ beam_status_t run_experts_fp8(const beam_moe_config_t& c, const void* hidden, co
   ga.a0_scale = gate.scale;
   ga.a1_scale = up.scale;
   ga.b_scale = xs;  // per token
-  if (beam::launch_grouped_gemm(beam::kModeGateUp, nt_gu, tm_g, tm_u, tm_x, ga,
-                                grid_for(ga.m_blocks, nt_gu), s, true) != cudaSuccess)
+  if (pgu) ga.m_blocks = c.d_ff / 256;
+  if ((pgu ? beam::launch_grouped_gemm_pair(true, tm_g, tm_u, tm_x, ga,
+                                            grid_for(ga.m_blocks, nt_gu), s, true)
+           : beam::launch_grouped_gemm(beam::kModeGateUp, nt_gu, tm_g, tm_u, tm_x, ga,
+                                       grid_for(ga.m_blocks, nt_gu), s, true)) != cudaSuccess)
     return BEAM_ERR_CUDA;
   record(5, s);
 
@@ -752,8 +782,12 @@ beam_status_t run_experts_fp8(const beam_moe_config_t& c, const void* hidden, co
   ga.a0_scale = down.scale;
   ga.a1_scale = nullptr;
   ga.b_scale = hs;  // per permuted row
-  if (beam::launch_grouped_gemm(pair ? beam::kModeDownPair : beam::kModeDown, nt_dn, tm_d, tm_d,
-                                tm_h, ga, grid_for(ga.m_blocks, nt_dn), s, true) != cudaSuccess)
+  if (pdn) ga.m_blocks = c.d / 512;
+  if ((pdn ? beam::launch_grouped_gemm_pair(false, tm_d, tm_d, tm_h, ga,
+                                            grid_for(ga.m_blocks, nt_dn), s, true)
+           : beam::launch_grouped_gemm(pair ? beam::kModeDownPair : beam::kModeDown, nt_dn, tm_d,
+                                       tm_d, tm_h, ga, grid_for(ga.m_blocks, nt_dn), s, true)) !=
+      cudaSuccess)
     return BEAM_ERR_CUDA;
   record(6, s);
   if (finish_combine(c, y, pa.pair_row, T, out, y_pairs, boundary, pa.status, s) != cudaSuccess)

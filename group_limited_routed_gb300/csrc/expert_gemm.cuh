@@ -54,4 +54,14 @@ cudaError_t launch_grouped_gemm(int mode, int nt, const CUtensorMap& a0, const C
                                 const CUtensorMap& b, const GemmArgs& a, int grid,
                                 cudaStream_t s, bool f8 = false);
 
+// The same GEMMs for 256-token blocks on clusters of two CTAs that share
+// M = 256 MMAs (expert_gemm_pair_kernel.cuh): gate/up over 256-row blocks of
+// F (m_blocks = d_ff / 256), down over 512-row blocks of d, two 256-row
+// accumulators (m_blocks = d / 512).  The token tensor map's box is 128
+// rows (each CTA stages half a block).
+// At most max_pairs clusters; as many as can be resident.
+cudaError_t launch_grouped_gemm_pair(bool gateup, const CUtensorMap& a0, const CUtensorMap& a1,
+                                     const CUtensorMap& b, const GemmArgs& a, int max_pairs,
+                                     cudaStream_t s, bool f8 = false);
+
 }  // namespace beam
