@@ -53,12 +53,12 @@ DOMINANT = {"bf16": "gate_up", "nvfp4": "fp4_gate_up", "a16": "w4a16_gate_up",
             "fp8": "fp8_gate_up", "mxfp8": "mx_gate_up"}
 DOMINANT_SRC = {k: [os.path.join(ROOT, "group_limited_routed_gb300", "csrc", f) for f in v]
                 for k, v in {
-                    "gate_up": ("expert_gemm_kernel.cuh", "expert_gemm.cuh", "gemm_common.cuh",
-                                "common.cuh", "ptx.cuh"),
+                    "gate_up": ("expert_gemm_kernel.cuh", "expert_gemm_pair_kernel.cuh",
+                                "expert_gemm.cuh", "gemm_common.cuh", "common.cuh", "ptx.cuh"),
                     "fp4_gate_up": ("nvfp4.cu", "gemm_common.cuh", "common.cuh", "ptx.cuh"),
                     "w4a16_gate_up": ("w4a16.cu", "gemm_common.cuh", "common.cuh", "ptx.cuh"),
-                    "fp8_gate_up": ("expert_gemm_kernel.cuh", "expert_gemm.cuh",
-                                    "gemm_common.cuh", "common.cuh", "ptx.cuh"),
+                    "fp8_gate_up": ("expert_gemm_kernel.cuh", "expert_gemm_pair_kernel.cuh",
+                                    "expert_gemm.cuh", "gemm_common.cuh", "common.cuh", "ptx.cuh"),
                     "mx_gate_up": ("nvfp4.cu", "gemm_common.cuh", "common.cuh", "ptx.cuh"),
                 }.items()}
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")

@@ -101,6 +101,11 @@ CONFIGS = {
     "mxfp8": MoEConfig(name="mxfp8", T=32, seed=13, weight_fmt="mxfp8", **_BEAM,
                        description="Beam MoE layer decode batch T=32, MXFP8 experts (E4M3 "
                                    "weights and activations, one E8M0 scale per 32 along K)"),
+    # profiling case for the MXFP8 kernels: 32 experts, decode-sized batch
+    "profile_mxfp8": MoEConfig(name="profile_mxfp8", T=8, d=5120, n_experts=32, n_groups=8,
+                               topk_groups=4, topk=8, d_ff=2560, seed=15, weight_fmt="mxfp8",
+                               description="Beam expert shapes, 32 MXFP8 experts (8x4), T=8 "
+                                           "(profiling case)"),
     # profiling case for the FP8 kernels: 32 experts, decode-sized batch
     "profile_fp8": MoEConfig(name="profile_fp8", T=8, d=5120, n_experts=32, n_groups=8,
                              topk_groups=4, topk=8, d_ff=2560, seed=11, weight_fmt="fp8",
