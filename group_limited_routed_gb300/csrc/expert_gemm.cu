@@ -34,22 +34,25 @@ cudaError_t launch_pair_impl(const CUtensorMap& a0, const CUtensorMap& a1, const
   const cudaError_t err =
       smem_limit_once<expert_gemm_pair_kernel<MODE, F8>>(static_cast<int>(C::SMEM_BYTES));
   if (err != cudaSuccess) return err;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = kProgrammaticLaunch;
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(C::THREADS);
   cfg.dynamicSmemBytes = C::SMEM_BYTES;
   cfg.stream = s;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 1;  // the occupancy query takes the cluster shape only
   cfg.gridDim = dim3(2);
   // a persistent grid of as many pairs as can be resident (whole waves)
   const int resident = pair_clusters_once<expert_gemm_pair_kernel<MODE, F8>>(cfg);
   if (resident <= 0) return cudaErrorUnknown;
   cfg.gridDim = dim3(static_cast<unsigned>(2 * std::max(1, std::min(resident, max_pairs))));
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, expert_gemm_pair_kernel<MODE, F8>, a0, a1, b, p);
 }
 
@@ -57,11 +60,10 @@ template <int NT, int MODE, bool F8>
 cudaError_t launch_impl(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b,
                         const GemmArgs& p, int grid, cudaStream_t s) {
   using C = Cfg<NT, MODE>;
-  auto kern = expert_gemm_kernel<NT, MODE, F8>;
   const cudaError_t err = smem_limit_once<expert_gemm_kernel<NT, MODE, F8>>(C::SMEM_BYTES);
   if (err != cudaSuccess) return err;
-  kern<<<grid, C::THREADS, C::SMEM_BYTES, s>>>(a0, a1, b, p);
-  return cudaGetLastError();
+  return launch_dependent(expert_gemm_kernel<NT, MODE, F8>, dim3(grid), dim3(C::THREADS),
+                          C::SMEM_BYTES, s, a0, a1, b, p);
 }
 
 }  // namespace

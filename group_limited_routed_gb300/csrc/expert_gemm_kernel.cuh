@@ -178,7 +178,6 @@ __global__ void __launch_bounds__(threads_for(NT, MODE), 1)
     }
     ptx::mbar_init(done_bar, 1);
     *abort_flag = 0;
-    *s_total = p.offsets[E];
     ptx::fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
@@ -190,6 +189,17 @@ __global__ void __launch_bounds__(threads_for(NT, MODE), 1)
     ptx::tmem_alloc(ptx::smem_addr(tmem_slot), C::TMEM_COLS);
     ptx::tmem_relinquish();
   }
+  // Launched behind the previous kernel (programmatic dependent launch).
+  // gate/up's tile list comes from the permutation right before it, so it
+  // waits here, then lets the down GEMM start: down CTAs take the SMs that
+  // gate/up CTAs leave.  The down GEMM's list comes from that same
+  // permutation, complete before gate/up let it start: it reads the list and
+  // streams weights at once, and only its token producer waits (for h).
+  if (GATEUP) {
+    ptx::grid_dep_wait();
+    ptx::grid_dep_launch();
+  }
+  if (threadIdx.x == 0) *s_total = p.offsets[E];
   for (int e = threadIdx.x; e < E; e += C::THREADS) {
     s_cnt[e] = p.counts[e];
     s_off[e] = p.offsets[e];
@@ -283,6 +293,10 @@ __global__ void __launch_bounds__(threads_for(NT, MODE), 1)
     // otherwise lane 0 loads the whole token tile (x gathered into expert
     // order, or h).
     constexpr int RPL = (NT + 31) / 32;  // token rows per lane
+    // h comes from the kernel before this one.  The combine after this
+    // kernel is not let in early: tens of thousands of its blocks waiting on
+    // the SMs slowed this GEMM at prefill sizes.
+    if (!GATEUP) ptx::grid_dep_wait();
     const uint64_t pol_b = ptx::policy_evict_last();
     int last_parity[C::SB];
 #pragma unroll

@@ -139,7 +139,6 @@ __global__ void __launch_bounds__(PairCfg<MODE>::THREADS, 1)
     }
     ptx::mbar_init(done_bar, 1);
     *abort_flag = 0;
-    *s_total = p.offsets[E];
     ptx::fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
@@ -151,6 +150,14 @@ __global__ void __launch_bounds__(PairCfg<MODE>::THREADS, 1)
     ptx::tmem_alloc_pair(ptx::smem_addr(tmem_slot), C::TMEM_COLS);
     ptx::tmem_relinquish_pair();
   }
+  // programmatic dependent launch, as in the single-CTA kernel: gate/up
+  // waits for the permutation here; the down GEMM reads its tile list at
+  // once and only its token producer waits (for h)
+  if (GATEUP) {
+    ptx::grid_dep_wait();
+    ptx::grid_dep_launch();
+  }
+  if (threadIdx.x == 0) *s_total = p.offsets[E];
   for (int e = threadIdx.x; e < E; e += C::THREADS) {
     s_cnt[e] = p.counts[e];
     s_off[e] = p.offsets[e];
@@ -196,6 +203,7 @@ __global__ void __launch_bounds__(PairCfg<MODE>::THREADS, 1)
     // producer arms with both halves' byte count.
     if (lane == 0) {
       const bool weights = warp == 0;
+      if (!GATEUP && !weights) ptx::grid_dep_wait();  // h: the kernel before this one
       const uint32_t stage_bytes = weights ? C::A_STAGE : C::B_STAGE;
       const uint32_t ring = weights ? a_ring : b_ring;
       const uint64_t pol = weights ? (p.weight_evict_first ? ptx::policy_evict_first()

@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <mutex>
+#include <utility>
 
 namespace beam {
 
@@ -46,6 +47,36 @@ int blocks_per_sm_once(int threads) {
     cached[dev] = v;
   }
   return cached[dev];
+}
+
+// ------------------------------------------- programmatic dependent launch
+// The layer's later kernels (expert GEMMs, combine) are launched with
+// programmatic stream serialization (SGLang post "SGLang 原生支持 Reflection 的
+// Beam 并驱动其生产 API", section "Fusion Optimizations": a kernel sets up and
+// loads weights before its dependency wait).  Such a kernel may start while
+// the kernel before it still runs, so each one executes griddepcontrol.wait
+// before it reads anything that kernel writes, and writes nothing that kernel
+// reads.  Reads before the wait are allowed only of data written two or more
+// kernels earlier: the one kernel here that lets its successor start early
+// (the gate/up GEMM, for the down GEMM) does so after its own wait, so by
+// then all earlier kernels have completed.  A kernel that never triggers
+// lets its successor start when it completes.
+constexpr int kProgrammaticLaunch = 1;
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t s, Args&&... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = kProgrammaticLaunch;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
 }  // namespace beam

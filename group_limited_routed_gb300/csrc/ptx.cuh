@@ -53,6 +53,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // ---------------------------------------------------------------- TMA
+// Programmatic dependent launch.  grid_dep_wait returns once the grid this
+// one was launched behind has completed and its writes are visible (at once
+// for a grid launched without the programmatic-serialization attribute);
+// grid_dep_launch lets the stream's next grid start its blocks (the first
+// call in a CTA counts, later ones do nothing).
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
 }

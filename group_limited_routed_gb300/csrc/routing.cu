@@ -19,6 +19,7 @@
 
 #include "common.cuh"
 #include "launch_once.cuh"
+#include "ptx.cuh"
 
 namespace beam {
 namespace {
@@ -742,6 +743,7 @@ __global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ 
                                                       int32_t k, int32_t d,
                                                       uint16_t* __restrict__ out,
                                                       uint32_t* status) {
+  ptx::grid_dep_wait();  // y comes from the kernel before this one
   const int64_t t = blockIdx.x;
   const int c8 = blockIdx.y * blockDim.x + threadIdx.x;
   if (c8 >= d / 8) return;
@@ -820,6 +822,7 @@ __global__ void __launch_bounds__(256) combine_boundary_kernel(const float* __re
                                                                BoundaryArgs b, uint32_t* status) {
   extern __shared__ float s_v[];  // [d] the token's current values
   __shared__ float s_red[32];
+  ptx::grid_dep_wait();  // y comes from the kernel before this one
   const int64_t t = blockIdx.x;
   const int n8 = d / 8;
   float ss = 0.f;
@@ -996,9 +999,8 @@ cudaError_t launch_combine_boundary(const float* y, const int32_t* pair_row, int
   // the largest row the entry point accepts (d <= 51200)
   const cudaError_t e = smem_limit_once<combine_boundary_kernel>(200 * 1024);
   if (e != cudaSuccess) return e;
-  combine_boundary_kernel<<<static_cast<unsigned>(T), 256, smem, s>>>(y, pair_row, k, d, out, b,
-                                                                      status);
-  return cudaGetLastError();
+  return launch_dependent(combine_boundary_kernel, dim3(static_cast<unsigned>(T)), dim3(256), smem,
+                          s, y, pair_row, k, d, out, b, status);
 }
 
 void launch_ep_pack(const int32_t* idx, const int32_t* perm_src, const float* perm_w,
@@ -1040,7 +1042,7 @@ void launch_scatter_tokens(const uint16_t* x, const int32_t* pair_row, int64_t T
 void launch_combine(const float* y, const int32_t* pair_row, int64_t T, int32_t k, int32_t d,
                     uint16_t* out, uint32_t* status, cudaStream_t s) {
   dim3 grid(static_cast<unsigned>(T), (d / 8 + 127) / 128);
-  combine_kernel<<<grid, 128, 0, s>>>(y, pair_row, k, d, out, status);
+  launch_dependent(combine_kernel, grid, dim3(128), 0, s, y, pair_row, k, d, out, status);
 }
 
 }  // namespace beam

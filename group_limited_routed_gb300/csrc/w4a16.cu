@@ -58,13 +58,22 @@ constexpr int kEpiWarp0 = 2 + kConvWarps;             // first of the 4 epilogue
 // pipe idle (four issuers: gate/up 1051 -> 748 us, down 760 -> 559 us on
 // the 128-token NVFP4 batch; eight gave no more).
 constexpr int kIssuers = 4;
-// gate/up: the two converter warps of a lane quarter take alternate 64-wide
-// slices whole (a warp's TMEM stores wait behind the queued MMAs, and the
-// other warp converts meanwhile: gate/up 747 -> 709 us on the 128-token
-// batch); down: both convert half of every slice (one projection per slice
-// leaves too little work to overlap: 557 -> 574 us when split by slices).
-template <bool GATEUP>
-constexpr bool kConvSplitSlices = GATEUP;
+// Kernel modes: gate/up (W_g and W_u tiles of the same rows), down over one
+// 128-row W_d block, down over two adjacent 128-row W_d blocks that share the
+// token tile (the two blocks then take the places of gate and up).
+constexpr int kW4Down = 0;
+constexpr int kW4GateUp = 1;
+constexpr int kW4DownPair = 2;
+template <int MODE>
+constexpr int kNumA = MODE == kW4Down ? 1 : 2;
+// With two weight tiles per stage the two converter warps of a lane quarter
+// take alternate 64-wide slices whole (a warp's TMEM stores wait behind the
+// queued MMAs, and the other warp converts meanwhile: gate/up 747 -> 709 us
+// on the 128-token batch); with one, both convert half of every slice (one
+// tile per slice leaves too little work to overlap: 557 -> 574 us when split
+// by slices).
+template <int MODE>
+constexpr bool kConvSplitSlices = kNumA<MODE> == 2;
 constexpr int kIssuer1 = kEpiWarp0 + 4;  // warps of issuers 1..kIssuers-1
 constexpr int kThreads = 32 * (kIssuer1 + kIssuers - 1);
 constexpr uint32_t kTileBudget = 216 * 1024;
@@ -76,9 +85,9 @@ constexpr uint32_t pow2_at_least(uint32_t v) {
   return p;
 }
 
-template <int NT, bool GATEUP>
+template <int NT, int MODE>
 struct Cfg {
-  static constexpr int NUM_A = GATEUP ? 2 : 1;
+  static constexpr int NUM_A = kNumA<MODE>;
   static constexpr int NUM_ACC = kIssuers;  // one accumulator per issuer
   static constexpr uint32_t A_BYTES = BM * KS_BYTES;     // 16 KB of codes per projection
   static constexpr uint32_t SFA_BYTES = 2048;            // 4 blocks of 128 rows x 4 scales
@@ -104,7 +113,7 @@ struct Cfg {
   static_assert(TMEM_COLS <= 512, "TMEM columns");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
   static_assert(STAGES >= 2, "two stages at least");
-  static_assert(!kConvSplitSlices<GATEUP> || RA % 2 == 0,
+  static_assert(!kConvSplitSlices<MODE> || RA % 2 == 0,
                 "slices alternate between two converter warps: an even ring");
 };
 
@@ -195,12 +204,16 @@ __global__ void __launch_bounds__(128) gather_f16_kernel(const uint16_t* __restr
 }
 
 // ---------------------------------------------------------------- GEMM
-template <int NT, bool GATEUP>
+template <int NT, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     w4a16_gemm_kernel(const __grid_constant__ CUtensorMap tm_a0,
                       const __grid_constant__ CUtensorMap tm_a1,
                       const __grid_constant__ CUtensorMap tm_b, const W4a16GemmArgs p) {
-  using C = Cfg<NT, GATEUP>;
+  using C = Cfg<NT, MODE>;
+  constexpr bool GATEUP = MODE == kW4GateUp;
+  constexpr bool PAIR = MODE == kW4DownPair;
+  constexpr bool TWO_A = C::NUM_A == 2;
+  constexpr bool SPLIT = kConvSplitSlices<MODE>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = ptx::smem_addr(smem_raw);
   const uint32_t pad = (1024u - (raw_addr & 1023u)) & 1023u;
@@ -235,7 +248,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(empty_bar(s), NI + kConvWarps);  // the MMA commits and the converters
     }
     for (int a = 0; a < C::RA; ++a) {
-      ptx::mbar_init(afull_bar(a), kConvSplitSlices<GATEUP> ? kConvWarps / 2 : kConvWarps);
+      ptx::mbar_init(afull_bar(a), SPLIT ? kConvWarps / 2 : kConvWarps);
       ptx::mbar_init(aempty_bar(a), NI);
     }
     for (int a = 0; a < 2; ++a) {
@@ -309,10 +322,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
         const TileInfo ti = decode_tile<NT>(tile, s_start, s_cnt, s_off, E);
         if (!use_tile(ti)) continue;
-        int a_row = ti.expert * p.rows_per_expert + ti.mblock * BM;
+        int a_row = ti.expert * p.rows_per_expert + ti.mblock * (PAIR ? 2 * BM : BM);
         // the boxes' rows (and so their scale blocks) inside the weight
         // tensor, the token box's first row inside the token operand
-        if (!in_bounds(a_row + BM <= p.a_rows, p.status)) a_row = 0;
+        if (!in_bounds(a_row + (PAIR ? 2 * BM : BM) <= p.a_rows, p.status)) a_row = 0;
         const int b_row0 = in_bounds(ti.row0 < p.b_rows, p.status) ? ti.row0 : 0;
         const int64_t sf_row_tile = a_row / BM;
         for (int kb = 0; kb < p.k_blocks; ++kb) {
@@ -329,6 +342,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (GATEUP) {
             ptx::tma_load_2d(st + C::A_BYTES, &tm_a1, fb, kb * KS_BYTES, a_row, pol_w);
             ptx::bulk_load(st + C::OFF_SFA + C::SFA_BYTES, p.sfa1 + sf_off, C::SFA_BYTES, fb);
+          }
+          if (PAIR) {  // the next 128-row block and its scales (the next row tile)
+            ptx::tma_load_2d(st + C::A_BYTES, &tm_a0, fb, kb * KS_BYTES, a_row + BM, pol_w);
+            ptx::bulk_load(st + C::OFF_SFA + C::SFA_BYTES,
+                           p.sfa0 + sf_off + sf_blocks_per_row_tile * 512, C::SFA_BYTES, fb);
           }
 #pragma unroll
           for (int j = 0; j < 4; ++j)
@@ -349,8 +367,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1 || warp >= kIssuer1) {
     // --------------------------------------------------------- MMA issuers
     // issuer i (warp 1 for i = 0, then warps 14, 15, 16) accumulates into
-    // accumulator i: gate/up projection i % 2, K part i / 2 of each slice;
-    // down K part i
+    // accumulator i: with two weight tiles, tile i % 2 (gate or up; the first
+    // or second W_d block) and K part i / 2 of each slice; with one, K part i
     const int issuer = warp == 1 ? 0 : warp - kIssuer1 + 1;
     if (lane == 0) {
       int stage = 0, ra = 0;
@@ -379,10 +397,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::tc_fence_after();
             const uint32_t a0 = tmem_base + C::A_BASE + ra * C::A_COLS;
             // this issuer's K steps (of the slice's four) and projection
-            constexpr int PARTS = GATEUP ? kIssuers / 2 : kIssuers;
+            constexpr int PARTS = TWO_A ? kIssuers / 2 : kIssuers;
             constexpr int KK = (KSUB / 16) / PARTS;
-            const int proj = GATEUP ? issuer % 2 : 0;
-            const int part = GATEUP ? issuer / 2 : issuer;
+            const int proj = TWO_A ? issuer % 2 : 0;
+            const int part = TWO_A ? issuer / 2 : issuer;
 #pragma unroll
             for (int i = 0; i < KK; ++i) {
               const int kk = part * KK + i;
@@ -425,11 +443,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
     int stage = 0;
     uint32_t phase = 0;
-    // global index of this warp's next slice: gate/up alternates the slices
-    // between the two warps of a lane quarter (each converts whole slices),
-    // down has both convert a half of every slice
-    uint32_t gs = kConvSplitSlices<GATEUP> ? static_cast<uint32_t>(grp) : 0u;
-    constexpr int JSTEP = kConvSplitSlices<GATEUP> ? 2 : 1;
+    // global index of this warp's next slice: with two weight tiles the
+    // slices alternate between the two warps of a lane quarter (each converts
+    // whole slices), with one both convert a half of every slice
+    uint32_t gs = SPLIT ? static_cast<uint32_t>(grp) : 0u;
+    constexpr int JSTEP = SPLIT ? 2 : 1;
     bool ok = true;
     for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
       const TileInfo ti = decode_tile<NT>(tile, s_start, s_cnt, s_off, E);
@@ -440,7 +458,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         const uint8_t* st = smem + stage * C::STAGE_BYTES;
-        for (int j = kConvSplitSlices<GATEUP> ? grp : 0; j < 4; j += JSTEP) {
+        for (int j = SPLIT ? grp : 0; j < 4; j += JSTEP) {
           const int slot = static_cast<int>(gs % C::RA);
           const uint32_t sph = (gs / C::RA) & 1u;
           if (!W.wait(aempty_bar(slot), sph ^ 1u)) {
@@ -455,8 +473,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t sf4 = *reinterpret_cast<const uint32_t*>(
                 st + C::OFF_SFA + a * C::SFA_BYTES + j * 512 + (m & 31) * 16 + (m >> 5) * 4);
 #pragma unroll
-            for (int hh = 0; hh < (kConvSplitSlices<GATEUP> ? 2 : 1); ++hh) {
-              const int half = kConvSplitSlices<GATEUP> ? hh : grp;
+            for (int hh = 0; hh < (SPLIT ? 2 : 1); ++hh) {
+              const int half = SPLIT ? hh : grp;
               const uint4 c =
                   *reinterpret_cast<const uint4*>(row + (((2 * j + half) ^ (m & 7)) << 4));
               const uint32_t s0 = scale_pair(static_cast<uint8_t>(sf4 >> (16 * half)));
@@ -500,7 +518,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!W.wait(tfull_bar(acc), acc_phase)) break;
       ptx::tc_fence_after();
       const uint32_t tq = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * C::ACC_COLS;
-      const int col = ti.mblock * BM + m;
+      const int col = ti.mblock * (PAIR ? 2 * BM : BM) + m;
       const float gs0 = p.gs0[ti.expert];
 #pragma unroll 1
       for (int c0 = 0; c0 < ti.nvalid; c0 += 16) {
@@ -528,6 +546,23 @@ __global__ void __launch_bounds__(kThreads, 1)
               const float u = ua * gs1;
               const float h = __fdividef(g, 1.0f + __expf(-g)) * u;
               p.h_out[static_cast<int64_t>(ti.row0 + c0 + j) * p.out_ld + col] = f32_to_f16_sat(h);
+            }
+          }
+        } else if constexpr (PAIR) {
+          // block b's partial sums: issuers b, b + 2, ... in issuer order
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            if (c0 + j < ti.nvalid) {
+              const int row = ti.row0 + c0 + j;
+              if (!in_bounds(row < p.out_rows_cap && col + BM < p.out_ld, p.status)) continue;
+              const float wr = p.perm_w[row];
+#pragma unroll
+              for (int b = 0; b < 2; ++b) {
+                float acc = __uint_as_float(r[b][j]);
+#pragma unroll
+                for (int i = b + 2; i < kIssuers; i += 2) acc += __uint_as_float(r[i][j]);
+                p.y_out[static_cast<int64_t>(row) * p.out_ld + col + b * BM] = acc * gs0 * wr;
+              }
             }
           }
         } else {
@@ -559,12 +594,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int NT, bool GATEUP>
+template <int NT, int MODE>
 cudaError_t launch_impl(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b,
                         const W4a16GemmArgs& p, int grid, cudaStream_t s) {
-  using C = Cfg<NT, GATEUP>;
-  auto kern = w4a16_gemm_kernel<NT, GATEUP>;
-  const cudaError_t err = smem_limit_once<w4a16_gemm_kernel<NT, GATEUP>>(C::SMEM_BYTES);
+  using C = Cfg<NT, MODE>;
+  auto kern = w4a16_gemm_kernel<NT, MODE>;
+  const cudaError_t err = smem_limit_once<w4a16_gemm_kernel<NT, MODE>>(C::SMEM_BYTES);
   if (err != cudaSuccess) return err;
   kern<<<grid, kThreads, C::SMEM_BYTES, s>>>(a0, a1, b, p);
   return cudaGetLastError();
@@ -579,13 +614,16 @@ void launch_gather_f16(const uint16_t* x, const int32_t* perm_src, const int32_t
 
 cudaError_t launch_w4a16_gemm(bool gateup, int nt, const CUtensorMap& a0, const CUtensorMap& a1,
                               const CUtensorMap& b, const W4a16GemmArgs& p, int grid,
-                              cudaStream_t s) {
+                              cudaStream_t s, bool pair) {
   if (gateup) {
-    if (nt == 16) return launch_impl<16, true>(a0, a1, b, p, grid, s);
-    if (nt == 32) return launch_impl<32, true>(a0, a1, b, p, grid, s);
+    if (nt == 16) return launch_impl<16, kW4GateUp>(a0, a1, b, p, grid, s);
+    if (nt == 32) return launch_impl<32, kW4GateUp>(a0, a1, b, p, grid, s);
+  } else if (pair) {
+    if (nt == 16) return launch_impl<16, kW4DownPair>(a0, a0, b, p, grid, s);
+    if (nt == 32) return launch_impl<32, kW4DownPair>(a0, a0, b, p, grid, s);
   } else {
-    if (nt == 16) return launch_impl<16, false>(a0, a0, b, p, grid, s);
-    if (nt == 32) return launch_impl<32, false>(a0, a0, b, p, grid, s);
+    if (nt == 16) return launch_impl<16, kW4Down>(a0, a0, b, p, grid, s);
+    if (nt == 32) return launch_impl<32, kW4Down>(a0, a0, b, p, grid, s);
   }
   return cudaErrorInvalidValue;
 }
