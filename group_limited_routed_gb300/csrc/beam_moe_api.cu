@@ -863,14 +863,14 @@ beam_status_t run_experts_w4a16(const beam_moe_config_t& c, const void* hidden, 
   ga.y_out = y;
   ga.out_ld = c.d;
   ga.rows_per_expert = c.d;
-  // pairs of adjacent 128-row W_d blocks share each token tile: two weight
-  // tiles per stage, as in gate/up, keep the converters and MMA issuers busy
-  const bool pair = c.d % 256 == 0;
-  ga.m_blocks = pair ? c.d / 256 : c.d / 128;
+  // pairs of adjacent 128-row W_d blocks share each token tile (d % 256 == 0
+  // here): two weight tiles per stage, as in gate/up, keep the converters
+  // and MMA issuers busy
+  ga.m_blocks = c.d / 256;
   ga.k_blocks = c.d_ff / 256;
   ga.a_rows = static_cast<int32_t>(ED);
   ga.out_rows_cap = static_cast<int32_t>(rows);
-  if (beam::launch_w4a16_gemm(false, nt, tm_d, tm_d, tm_h, ga, grid_for(ga.m_blocks), s, pair) !=
+  if (beam::launch_w4a16_gemm(false, nt, tm_d, tm_d, tm_h, ga, grid_for(ga.m_blocks), s) !=
       cudaSuccess)
     return BEAM_ERR_CUDA;
   record(6, s);

@@ -186,11 +186,11 @@ struct W4a16GemmArgs {
 void launch_gather_f16(const uint16_t* x, const int32_t* perm_src, const int32_t* n_valid,
                        int64_t TK, int32_t k, int32_t d, uint16_t* x16, cudaStream_t s);
 // NVFP4 weights x F16 activations grouped GEMM, nt = 16 | 32; b maps F16 rows
-// (box 64 x nt, 128-byte swizzle); the down GEMM with `pair` works on pairs of
-// adjacent 128-row weight blocks (m_blocks = d / 256)
+// (box 64 x nt, 128-byte swizzle); the down GEMM works on pairs of adjacent
+// 128-row weight blocks (m_blocks = d / 256)
 cudaError_t launch_w4a16_gemm(bool gateup, int nt, const CUtensorMap& a0, const CUtensorMap& a1,
                               const CUtensorMap& b, const W4a16GemmArgs& p, int grid,
-                              cudaStream_t s, bool pair = false);
+                              cudaStream_t s);
 
 // [rows, S] row-major E4M3 scales -> 128-row x 4-scale blocks (see nvfp4.cu)
 void launch_pack_scales(const uint8_t* src, int64_t rows, int64_t S, uint8_t* dst, cudaStream_t s);

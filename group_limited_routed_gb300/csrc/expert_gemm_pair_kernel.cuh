@@ -225,9 +225,12 @@ __global__ void __launch_bounds__(PairCfg<MODE>::THREADS, 1)
           row = ti.expert * p.rows_per_expert + ti.mblock * TILE_ROWS + static_cast<int>(rank) * BM;
           if (!in_bounds(row + (PAIR ? 2 * BM : 0) + BM <= p.a_rows, p.status)) row = 0;
         } else {
-          // this CTA's half of the block: rows [r N/2, r N/2 + N/2)
-          row = ti.row0 + static_cast<int>(rank) * (ti.n_mma / 2);
-          if (!in_bounds(row < p.b_rows, p.status)) row = 0;
+          // this CTA's half of the block: rows [r N/2, r N/2 + N/2); a half
+          // with no valid row (a block of at most N/2 rows) may start at the
+          // operand's end: its load is padding (zero fill), never read
+          const int first = static_cast<int>(rank) * (ti.n_mma / 2);
+          row = ti.row0 + first;
+          if (!in_bounds(first >= ti.nvalid || row < p.b_rows, p.status)) row = 0;
         }
         for (int kb = 0; kb < p.k_blocks; ++kb) {
           const uint32_t empty = weights ? emptyA(stage) : emptyB(stage);

@@ -11,11 +11,12 @@
 //     (exact inside F16's normal range, saturating at 65504), and the SwiGLU
 //     product h is rounded to F16 for the down GEMM.
 // The weight tiles stay packed in shared memory (0.5 byte per weight); eight
-// converter warps (two per TMEM lane quarter: for gate/up each takes
-// alternate 64-wide K slices whole, for down each half of every slice)
-// expand each row's K slice to F16 pairs in registers and store it into
-// tensor memory, where the MMA reads its A operand.  So shared memory
-// carries only the packed codes and the token tiles.
+// converter warps (two per TMEM lane quarter, taking alternate 64-wide K
+// slices whole) expand each row's K slice of both weight tiles of a stage
+// to F16 pairs in registers and store it into tensor memory, where the MMA
+// reads its A operand.  So shared memory carries only the packed codes and
+// the token tiles.  A stage holds two weight tiles: gate and up, or for the
+// down GEMM two adjacent 128-row blocks of W_d that share the token tile.
 //
 // At decode-sized batches this path issues many tiny MMAs: an F16 MMA covers
 // K = 16 per instruction (the block-scaled FP4 MMA of the NVFP4 path covers
@@ -58,22 +59,16 @@ constexpr int kEpiWarp0 = 2 + kConvWarps;             // first of the 4 epilogue
 // pipe idle (four issuers: gate/up 1051 -> 748 us, down 760 -> 559 us on
 // the 128-token NVFP4 batch; eight gave no more).
 constexpr int kIssuers = 4;
-// Kernel modes: gate/up (W_g and W_u tiles of the same rows), down over one
-// 128-row W_d block, down over two adjacent 128-row W_d blocks that share the
-// token tile (the two blocks then take the places of gate and up).
-constexpr int kW4Down = 0;
+// Kernel modes: gate/up (W_g and W_u tiles of the same rows), down over two
+// adjacent 128-row W_d blocks that share the token tile (the two blocks take
+// the places of gate and up; m_blocks = d / 256, d % 256 == 0 for NVFP4).
+// The two converter warps of a lane quarter take alternate 64-wide slices
+// whole: a warp's TMEM stores wait behind the queued MMAs, and the other warp
+// converts meanwhile (gate/up 747 -> 709 us on the 128-token batch; the down
+// GEMM over single 128-row blocks, with half of every slice per warp, took
+// 569 us against 377 us over pairs of blocks).
 constexpr int kW4GateUp = 1;
 constexpr int kW4DownPair = 2;
-template <int MODE>
-constexpr int kNumA = MODE == kW4Down ? 1 : 2;
-// With two weight tiles per stage the two converter warps of a lane quarter
-// take alternate 64-wide slices whole (a warp's TMEM stores wait behind the
-// queued MMAs, and the other warp converts meanwhile: gate/up 747 -> 709 us
-// on the 128-token batch); with one, both convert half of every slice (one
-// tile per slice leaves too little work to overlap: 557 -> 574 us when split
-// by slices).
-template <int MODE>
-constexpr bool kConvSplitSlices = kNumA<MODE> == 2;
 constexpr int kIssuer1 = kEpiWarp0 + 4;  // warps of issuers 1..kIssuers-1
 constexpr int kThreads = 32 * (kIssuer1 + kIssuers - 1);
 constexpr uint32_t kTileBudget = 216 * 1024;
@@ -87,7 +82,7 @@ constexpr uint32_t pow2_at_least(uint32_t v) {
 
 template <int NT, int MODE>
 struct Cfg {
-  static constexpr int NUM_A = kNumA<MODE>;
+  static constexpr int NUM_A = 2;
   static constexpr int NUM_ACC = kIssuers;  // one accumulator per issuer
   static constexpr uint32_t A_BYTES = BM * KS_BYTES;     // 16 KB of codes per projection
   static constexpr uint32_t SFA_BYTES = 2048;            // 4 blocks of 128 rows x 4 scales
@@ -113,7 +108,7 @@ struct Cfg {
   static_assert(TMEM_COLS <= 512, "TMEM columns");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
   static_assert(STAGES >= 2, "two stages at least");
-  static_assert(!kConvSplitSlices<MODE> || RA % 2 == 0,
+  static_assert(RA % 2 == 0,
                 "slices alternate between two converter warps: an even ring");
 };
 
@@ -212,8 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   using C = Cfg<NT, MODE>;
   constexpr bool GATEUP = MODE == kW4GateUp;
   constexpr bool PAIR = MODE == kW4DownPair;
-  constexpr bool TWO_A = C::NUM_A == 2;
-  constexpr bool SPLIT = kConvSplitSlices<MODE>;
+  static_assert(GATEUP || PAIR, "kernel mode");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = ptx::smem_addr(smem_raw);
   const uint32_t pad = (1024u - (raw_addr & 1023u)) & 1023u;
@@ -248,7 +242,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(empty_bar(s), NI + kConvWarps);  // the MMA commits and the converters
     }
     for (int a = 0; a < C::RA; ++a) {
-      ptx::mbar_init(afull_bar(a), SPLIT ? kConvWarps / 2 : kConvWarps);
+      ptx::mbar_init(afull_bar(a), kConvWarps / 2);
       ptx::mbar_init(aempty_bar(a), NI);
     }
     for (int a = 0; a < 2; ++a) {
@@ -367,8 +361,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1 || warp >= kIssuer1) {
     // --------------------------------------------------------- MMA issuers
     // issuer i (warp 1 for i = 0, then warps 14, 15, 16) accumulates into
-    // accumulator i: with two weight tiles, tile i % 2 (gate or up; the first
-    // or second W_d block) and K part i / 2 of each slice; with one, K part i
+    // accumulator i: weight tile i % 2 (gate or up; the first or second W_d
+    // block) and K part i / 2 of each slice
     const int issuer = warp == 1 ? 0 : warp - kIssuer1 + 1;
     if (lane == 0) {
       int stage = 0, ra = 0;
@@ -397,10 +391,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::tc_fence_after();
             const uint32_t a0 = tmem_base + C::A_BASE + ra * C::A_COLS;
             // this issuer's K steps (of the slice's four) and projection
-            constexpr int PARTS = TWO_A ? kIssuers / 2 : kIssuers;
+            constexpr int PARTS = kIssuers / 2;
             constexpr int KK = (KSUB / 16) / PARTS;
-            const int proj = TWO_A ? issuer % 2 : 0;
-            const int part = TWO_A ? issuer / 2 : issuer;
+            const int proj = issuer % 2;
+            const int part = issuer / 2;
 #pragma unroll
             for (int i = 0; i < KK; ++i) {
               const int kk = part * KK + i;
@@ -433,21 +427,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp < kEpiWarp0) {
     // ----------------------------------------------------------- converters
-    // Thread row m (its warp's TMEM lane quarter) expands one half of its
-    // row's 64-wide K slices: 16 code bytes (chunk 2j + half of the 128-byte
-    // swizzled row) and 2 scales (blocked order) -> 16 F16 pairs -> 16 TMEM
-    // columns.
+    // Thread row m (its warp's TMEM lane quarter) expands its row's 64-wide
+    // K slice j of both weight tiles: per tile 32 code bytes (chunks 2j and
+    // 2j + 1 of the 128-byte swizzled row) and 4 scales (blocked order) ->
+    // 32 F16 pairs -> 32 TMEM columns.
     const int q = warp & 3;
     const int grp = (warp - 2) >> 2;  // which of the two converter warps of lane quarter q
     const int m = q * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
     int stage = 0;
     uint32_t phase = 0;
-    // global index of this warp's next slice: with two weight tiles the
-    // slices alternate between the two warps of a lane quarter (each converts
-    // whole slices), with one both convert a half of every slice
-    uint32_t gs = SPLIT ? static_cast<uint32_t>(grp) : 0u;
-    constexpr int JSTEP = SPLIT ? 2 : 1;
+    // global index of this warp's next slice: the slices alternate between
+    // the two warps of a lane quarter, each converting whole slices
+    uint32_t gs = static_cast<uint32_t>(grp);
+    constexpr int JSTEP = 2;
     bool ok = true;
     for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
       const TileInfo ti = decode_tile<NT>(tile, s_start, s_cnt, s_off, E);
@@ -458,7 +451,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         const uint8_t* st = smem + stage * C::STAGE_BYTES;
-        for (int j = SPLIT ? grp : 0; j < 4; j += JSTEP) {
+        for (int j = grp; j < 4; j += JSTEP) {
           const int slot = static_cast<int>(gs % C::RA);
           const uint32_t sph = (gs / C::RA) & 1u;
           if (!W.wait(aempty_bar(slot), sph ^ 1u)) {
@@ -473,8 +466,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t sf4 = *reinterpret_cast<const uint32_t*>(
                 st + C::OFF_SFA + a * C::SFA_BYTES + j * 512 + (m & 31) * 16 + (m >> 5) * 4);
 #pragma unroll
-            for (int hh = 0; hh < (SPLIT ? 2 : 1); ++hh) {
-              const int half = SPLIT ? hh : grp;
+            for (int half = 0; half < 2; ++half) {
               const uint4 c =
                   *reinterpret_cast<const uint4*>(row + (((2 * j + half) ^ (m & 7)) << 4));
               const uint32_t s0 = scale_pair(static_cast<uint8_t>(sf4 >> (16 * half)));
@@ -548,7 +540,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               p.h_out[static_cast<int64_t>(ti.row0 + c0 + j) * p.out_ld + col] = f32_to_f16_sat(h);
             }
           }
-        } else if constexpr (PAIR) {
+        } else {
           // block b's partial sums: issuers b, b + 2, ... in issuer order
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
@@ -563,18 +555,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int i = b + 2; i < kIssuers; i += 2) acc += __uint_as_float(r[i][j]);
                 p.y_out[static_cast<int64_t>(row) * p.out_ld + col + b * BM] = acc * gs0 * wr;
               }
-            }
-          }
-        } else {
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            if (c0 + j < ti.nvalid) {
-              const int row = ti.row0 + c0 + j;
-              if (!in_bounds(row < p.out_rows_cap && col < p.out_ld, p.status)) continue;
-              float acc = __uint_as_float(r[0][j]);
-#pragma unroll
-              for (int i = 1; i < kIssuers; ++i) acc += __uint_as_float(r[i][j]);
-              p.y_out[static_cast<int64_t>(row) * p.out_ld + col] = acc * gs0 * p.perm_w[row];
             }
           }
         }
@@ -614,16 +594,13 @@ void launch_gather_f16(const uint16_t* x, const int32_t* perm_src, const int32_t
 
 cudaError_t launch_w4a16_gemm(bool gateup, int nt, const CUtensorMap& a0, const CUtensorMap& a1,
                               const CUtensorMap& b, const W4a16GemmArgs& p, int grid,
-                              cudaStream_t s, bool pair) {
+                              cudaStream_t s) {
   if (gateup) {
     if (nt == 16) return launch_impl<16, kW4GateUp>(a0, a1, b, p, grid, s);
     if (nt == 32) return launch_impl<32, kW4GateUp>(a0, a1, b, p, grid, s);
-  } else if (pair) {
+  } else {
     if (nt == 16) return launch_impl<16, kW4DownPair>(a0, a0, b, p, grid, s);
     if (nt == 32) return launch_impl<32, kW4DownPair>(a0, a0, b, p, grid, s);
-  } else {
-    if (nt == 16) return launch_impl<16, kW4Down>(a0, a0, b, p, grid, s);
-    if (nt == 32) return launch_impl<32, kW4Down>(a0, a0, b, p, grid, s);
   }
   return cudaErrorInvalidValue;
 }
