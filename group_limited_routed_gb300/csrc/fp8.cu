@@ -17,6 +17,8 @@
 #include <cstdint>
 
 #include "common.cuh"
+#include "launch_once.cuh"
+#include "ptx.cuh"
 
 namespace beam {
 namespace {
@@ -40,6 +42,11 @@ __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
 __global__ void __launch_bounds__(kThreads) quantize_e4m3_rows_kernel(
     const uint16_t* __restrict__ x, const int32_t* __restrict__ n_valid, int32_t cols,
     uint8_t* __restrict__ q, float* __restrict__ scale) {
+  // programmatic dependent launch: the rows (and n_valid) come from the
+  // kernels before this one; once they are visible the next GEMM may start
+  // its weight loads
+  ptx::grid_dep_wait();
+  ptx::grid_dep_launch();
   const int64_t row = blockIdx.x;
   if (n_valid && row >= *n_valid) return;
   const uint4* in = reinterpret_cast<const uint4*>(x + row * cols);
@@ -80,6 +87,8 @@ template <int V>
 __global__ void __launch_bounds__(kThreads) quantize_e4m3_rows_warp_kernel(
     const uint16_t* __restrict__ x, const int32_t* __restrict__ n_valid, int64_t rows,
     int32_t cols, uint8_t* __restrict__ q, float* __restrict__ scale) {
+  ptx::grid_dep_wait();  // as quantize_e4m3_rows_kernel
+  ptx::grid_dep_launch();
   const int64_t row = static_cast<int64_t>(blockIdx.x) * (kThreads / 32) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   // row is the same on every lane of the warp: whole warps leave together
@@ -122,8 +131,8 @@ template <int V>
 void launch_warp(const uint16_t* x, const int32_t* n_valid, int64_t rows, int32_t cols,
                  uint8_t* q, float* scale, cudaStream_t s) {
   const int64_t blocks = (rows + kThreads / 32 - 1) / (kThreads / 32);
-  quantize_e4m3_rows_warp_kernel<V>
-      <<<static_cast<unsigned>(blocks), kThreads, 0, s>>>(x, n_valid, rows, cols, q, scale);
+  launch_dependent(quantize_e4m3_rows_warp_kernel<V>, dim3(static_cast<unsigned>(blocks)),
+                   dim3(kThreads), 0, s, x, n_valid, rows, cols, q, scale);
 }
 
 }  // namespace
@@ -142,8 +151,8 @@ void launch_quantize_e4m3_rows(const uint16_t* x, const int32_t* n_valid, int64_
     if (v <= 8) return launch_warp<8>(x, n_valid, rows, cols, q, scale, s);
     return launch_warp<12>(x, n_valid, rows, cols, q, scale, s);
   }
-  quantize_e4m3_rows_kernel<<<static_cast<unsigned>(rows), kThreads, 0, s>>>(x, n_valid, cols, q,
-                                                                            scale);
+  launch_dependent(quantize_e4m3_rows_kernel, dim3(static_cast<unsigned>(rows)), dim3(kThreads), 0,
+                   s, x, n_valid, cols, q, scale);
 }
 
 }  // namespace beam

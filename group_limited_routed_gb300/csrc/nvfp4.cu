@@ -130,6 +130,10 @@ __global__ void __launch_bounds__(128) quantize_tokens_kernel(const uint16_t* __
                                                               uint8_t* __restrict__ xq,
                                                               uint8_t* __restrict__ xsf,
                                                               uint32_t* status) {
+  // programmatic dependent launch: pair_row comes from the permutation just
+  // before; once it is visible the gate/up GEMM may start its weight loads
+  ptx::grid_dep_wait();
+  ptx::grid_dep_launch();
   const int64_t t = blockIdx.x;
   __shared__ int64_t s_row[32];
   if (threadIdx.x < k) {
@@ -181,6 +185,9 @@ __global__ void __launch_bounds__(128) quantize_tokens_mx_kernel(const uint16_t*
                                                                  uint8_t* __restrict__ xq,
                                                                  uint8_t* __restrict__ xsf,
                                                                  uint32_t* status) {
+  // as quantize_tokens_kernel
+  ptx::grid_dep_wait();
+  ptx::grid_dep_launch();
   const int64_t t = blockIdx.x;
   __shared__ int64_t s_row[32];
   if (threadIdx.x < k) {
@@ -378,6 +385,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
+      // Programmatic dependent launch: the token rows (x or h) come from the
+      // kernel before this one, the weights and the tile list do not (the
+      // list is the permutation's, complete before that kernel let this one
+      // start).  The first tile's first stages get their weight loads before
+      // the dependency wait and their token loads after it.
+      bool waited = false;
+      auto token_loads = [&](int stg, int kb, int b_row0) {
+        const uint32_t st = tiles + stg * C::STAGE_BYTES;
+        const uint32_t fb = full_bar(stg);
+        ptx::tma_load_2d(st + C::OFF_B, &tm_b, fb, kb * BK_BYTES, b_row0, pol_b);
+#pragma unroll
+        for (int c = 0; c < C::SBS; ++c)
+          ptx::tma_load_2d(st + C::OFF_SFB + 512 * c, &tm_sfb, fb, (C::SBS * kb + c) * 16, b_row0,
+                           pol_b);
+      };
+      auto dependency_wait = [&](int npre, int b_row0) {
+        ptx::grid_dep_wait();
+        ptx::grid_dep_launch();
+        waited = true;
+        for (int j = 0; j < npre; ++j) token_loads(j, j, b_row0);  // stage j holds K block j
+      };
       for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
         const TileInfo ti = decode_tile<NT>(tile, s_start, s_cnt, s_off, E);
         if (!use_tile(ti)) continue;
@@ -387,7 +415,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!in_bounds(a_row + (PAIR ? 2 * BM : BM) <= p.a_rows, p.status)) a_row = 0;
         const int b_row0 = in_bounds(ti.row0 < p.b_rows, p.status) ? ti.row0 : 0;
         const int64_t sf_row_tile = a_row / BM;
+        // the first tile starts at stage 0: its first npre K blocks fill
+        // stages 0 .. npre - 1 before the wait
+        const int npre = waited ? 0 : min(C::STAGES, p.k_blocks);
         for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (!waited && kb == npre) dependency_wait(npre, b_row0);
           if (!W.wait(empty_bar(stage), phase ^ 1u)) {
             ok = false;
             break;
@@ -407,17 +439,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::bulk_load(st + C::OFF_SFA + C::SFA_BYTES,
                            p.sfa0 + sf_off + sf_blocks_per_row_tile * 512, C::SFA_BYTES, fb);
           }
-          ptx::tma_load_2d(st + C::OFF_B, &tm_b, fb, kb * BK_BYTES, b_row0, pol_b);
-#pragma unroll
-          for (int c = 0; c < C::SBS; ++c)
-            ptx::tma_load_2d(st + C::OFF_SFB + 512 * c, &tm_sfb, fb, (C::SBS * kb + c) * 16,
-                             b_row0, pol_b);
+          if (waited) token_loads(stage, kb, b_row0);
           last_parity[stage] = static_cast<int>(phase);
           if (++stage == C::STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
+        // a first tile of at most STAGES K blocks: its token loads follow here
+        if (ok && !waited) dependency_wait(npre, b_row0);
       }
 #pragma unroll
       for (int s = 0; s < C::STAGES; ++s)
@@ -621,11 +651,10 @@ cudaError_t launch_fp4_impl(const CUtensorMap& a0, const CUtensorMap& a1, const 
                             const CUtensorMap& sfb, const Fp4GemmArgs& p, int grid,
                             cudaStream_t s) {
   using C = Cfg<NT, KIND, FMT>;
-  auto kern = fp4_gemm_kernel<NT, KIND, FMT>;
   const cudaError_t err = smem_limit_once<fp4_gemm_kernel<NT, KIND, FMT>>(C::SMEM_BYTES);
   if (err != cudaSuccess) return err;
-  kern<<<grid, kThreads, C::SMEM_BYTES, s>>>(a0, a1, b, sfb, p);
-  return cudaGetLastError();
+  return launch_dependent(fp4_gemm_kernel<NT, KIND, FMT>, dim3(grid), dim3(kThreads), C::SMEM_BYTES,
+                          s, a0, a1, b, sfb, p);
 }
 
 }  // namespace
@@ -641,8 +670,8 @@ void launch_quantize_tokens(const uint16_t* x, const int32_t* pair_row, int64_t 
                             int32_t d, uint8_t* xq, uint8_t* xsf, uint32_t* status,
                             cudaStream_t s) {
   if (T <= 0) return;
-  quantize_tokens_kernel<<<static_cast<unsigned>(T), 128, 0, s>>>(x, pair_row, k, d, xq, xsf,
-                                                                  status);
+  launch_dependent(quantize_tokens_kernel, dim3(static_cast<unsigned>(T)), dim3(128), 0, s, x,
+                   pair_row, k, d, xq, xsf, status);
 }
 
 cudaError_t launch_fp4_gemm(bool gateup, int nt, const CUtensorMap& a0, const CUtensorMap& a1,
@@ -664,8 +693,8 @@ void launch_quantize_tokens_mx(const uint16_t* x, const int32_t* pair_row, int64
                                int32_t d, uint8_t* xq, uint8_t* xsf, uint32_t* status,
                                cudaStream_t s) {
   if (T <= 0) return;
-  quantize_tokens_mx_kernel<<<static_cast<unsigned>(T), 128, 0, s>>>(x, pair_row, k, d, xq, xsf,
-                                                                     status);
+  launch_dependent(quantize_tokens_mx_kernel, dim3(static_cast<unsigned>(T)), dim3(128), 0, s, x,
+                   pair_row, k, d, xq, xsf, status);
 }
 
 cudaError_t launch_mxfp8_gemm(bool gateup, int nt, const CUtensorMap& a0, const CUtensorMap& a1,

@@ -179,6 +179,11 @@ __global__ void __launch_bounds__(128) gather_f16_kernel(const uint16_t* __restr
                                                          const int32_t* __restrict__ n_valid,
                                                          int32_t k, int32_t d,
                                                          uint16_t* __restrict__ x16) {
+  // programmatic dependent launch: perm_src and n_valid come from the
+  // permutation just before; once they are visible the gate/up GEMM may
+  // start its weight loads
+  ptx::grid_dep_wait();
+  ptx::grid_dep_launch();
   const int64_t row = blockIdx.x;
   if (row >= *n_valid) return;
   const int64_t t = perm_src[row] / k;
@@ -313,6 +318,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
+      // Programmatic dependent launch, as in the NVFP4 GEMM: the token rows
+      // come from the kernel before this one; the first tile's first stages
+      // get their weight loads before the dependency wait, their token loads
+      // after it.
+      bool waited = false;
+      auto token_loads = [&](int stg, int kb, int b_row0) {
+        const uint32_t st = tiles + stg * C::STAGE_BYTES;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          ptx::tma_load_2d(st + C::OFF_B + j * C::B_SUB, &tm_b, full_bar(stg), (4 * kb + j) * KSUB,
+                           b_row0, pol_b);
+      };
+      auto dependency_wait = [&](int npre, int b_row0) {
+        ptx::grid_dep_wait();
+        ptx::grid_dep_launch();
+        waited = true;
+        for (int j = 0; j < npre; ++j) token_loads(j, j, b_row0);  // stage j holds K block j
+      };
       for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
         const TileInfo ti = decode_tile<NT>(tile, s_start, s_cnt, s_off, E);
         if (!use_tile(ti)) continue;
@@ -322,7 +345,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!in_bounds(a_row + (PAIR ? 2 * BM : BM) <= p.a_rows, p.status)) a_row = 0;
         const int b_row0 = in_bounds(ti.row0 < p.b_rows, p.status) ? ti.row0 : 0;
         const int64_t sf_row_tile = a_row / BM;
+        const int npre = waited ? 0 : min(C::STAGES, p.k_blocks);
         for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (!waited && kb == npre) dependency_wait(npre, b_row0);
           if (!W.wait(empty_bar(stage), phase ^ 1u)) {
             ok = false;
             break;
@@ -342,16 +367,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::bulk_load(st + C::OFF_SFA + C::SFA_BYTES,
                            p.sfa0 + sf_off + sf_blocks_per_row_tile * 512, C::SFA_BYTES, fb);
           }
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            ptx::tma_load_2d(st + C::OFF_B + j * C::B_SUB, &tm_b, fb, (4 * kb + j) * KSUB,
-                             b_row0, pol_b);
+          if (waited) token_loads(stage, kb, b_row0);
           last_parity[stage] = static_cast<int>(phase);
           if (++stage == C::STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
+        // a first tile of at most STAGES K blocks: its token loads follow here
+        if (ok && !waited) dependency_wait(npre, b_row0);
       }
 #pragma unroll
       for (int s = 0; s < C::STAGES; ++s)
@@ -578,18 +602,18 @@ template <int NT, int MODE>
 cudaError_t launch_impl(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b,
                         const W4a16GemmArgs& p, int grid, cudaStream_t s) {
   using C = Cfg<NT, MODE>;
-  auto kern = w4a16_gemm_kernel<NT, MODE>;
   const cudaError_t err = smem_limit_once<w4a16_gemm_kernel<NT, MODE>>(C::SMEM_BYTES);
   if (err != cudaSuccess) return err;
-  kern<<<grid, kThreads, C::SMEM_BYTES, s>>>(a0, a1, b, p);
-  return cudaGetLastError();
+  return launch_dependent(w4a16_gemm_kernel<NT, MODE>, dim3(grid), dim3(kThreads), C::SMEM_BYTES, s,
+                          a0, a1, b, p);
 }
 
 }  // namespace
 
 void launch_gather_f16(const uint16_t* x, const int32_t* perm_src, const int32_t* n_valid,
                        int64_t TK, int32_t k, int32_t d, uint16_t* x16, cudaStream_t s) {
-  gather_f16_kernel<<<static_cast<unsigned>(TK), 128, 0, s>>>(x, perm_src, n_valid, k, d, x16);
+  launch_dependent(gather_f16_kernel, dim3(static_cast<unsigned>(TK)), dim3(128), 0, s, x, perm_src,
+                   n_valid, k, d, x16);
 }
 
 cudaError_t launch_w4a16_gemm(bool gateup, int nt, const CUtensorMap& a0, const CUtensorMap& a1,
