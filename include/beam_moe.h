@@ -43,7 +43,15 @@
  *     n_experts / n_groups), T >= 0.
  *   - All work is enqueued on `stream` (a cudaStream_t; NULL = the legacy
  *     default stream).  No entry point synchronises or copies between host
- *     and device, except beam_moe_check_status.
+ *     and device, except beam_moe_check_status.  Kernels after a call's
+ *     first one are launched with programmatic stream serialization (SGLang
+ *     post, "Fusion Optimizations"): each may start before the kernel ahead
+ *     of it on the stream has finished, and waits on the device
+ *     (griddepcontrol.wait) before it reads anything that kernel writes, so
+ *     the order against the caller's own work on the stream is that of
+ *     ordinary launches.  A caller's kernel launched after a call with the
+ *     same attribute may likewise start early, and must wait the same way
+ *     before it reads the call's outputs.
  *   - Every entry point returns a status and never aborts or prints.  Invalid
  *     arguments are rejected before anything is launched (outputs untouched).
  *     T == 0 with a valid cfg returns BEAM_OK at once: nothing is launched
