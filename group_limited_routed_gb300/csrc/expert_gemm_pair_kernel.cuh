@@ -373,51 +373,79 @@ __global__ void __launch_bounds__(PairCfg<MODE>::THREADS, 1)
         if constexpr (GATEUP) sw1 = p.a1_scale[wrow];
         if constexpr (PAIR) sw1 = p.a0_scale[wrow + 2 * BM];
       }
-#pragma unroll 1
-      for (int c0 = col_begin; c0 < min(ti.nvalid, col_begin + COLS_PER_WARP); c0 += 16) {
-        if (!in_bounds(c0 + 16 <= kPairNT, p.status)) break;
-        uint32_t ra[16];
-        ptx::tmem_ld16(tq + c0, ra);
-        // per-token factors of the chunk's 16 columns, one column per lane,
-        // handed out by shuffles (as in the single-CTA kernel)
-        const int lrow = ti.row0 + c0 + (lane & 15);
-        const bool lvalid = c0 + (lane & 15) < ti.nvalid;
-        float lfac = 1.f;
-        int lorow = lrow;
-        if constexpr (GATEUP) {
-          if constexpr (F8)
-            if (lvalid) lfac = p.b_scale[p.perm_src[lrow] / p.topk];
-        } else {
-          if (lvalid) {
-            lfac = F8 ? p.b_scale[lrow] * p.perm_w[lrow] : p.perm_w[lrow];
-            if (p.out_rows) lorow = p.out_rows[lrow];
-          }
-        }
-        if constexpr (GATEUP) {
-          uint32_t rb[16];
+      if constexpr (GATEUP) {
+        // h of this lane's weight row for the warp's 64 tokens, kept in
+        // registers as BF16 pairs: the accumulator is freed as soon as it
+        // has been read, before any store, so the next tile's MMAs do not
+        // wait for the h stores
+        uint32_t hp[COLS_PER_WARP / 2];
+#pragma unroll
+        for (int cc = 0; cc < COLS_PER_WARP; cc += 16) {
+          const int c0 = col_begin + cc;
+          if (c0 >= ti.nvalid) break;  // the same on every lane of the warp
+          uint32_t ra[16], rb[16];
+          ptx::tmem_ld16(tq + c0, ra);
           ptx::tmem_ld16(tq + kPairNT + c0, rb);
+          // per-token factors of the chunk's 16 columns, one column per
+          // lane, handed out by shuffles (as in the single-CTA kernel)
+          float lfac = 1.f;
+          if constexpr (F8)
+            if (c0 + (lane & 15) < ti.nvalid) lfac = p.b_scale[p.perm_src[ti.row0 + c0 + (lane & 15)] / p.topk];
           ptx::tmem_wait_ld();
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            if (c0 + j < ti.nvalid) {  // the same on every lane of the warp
-              const int64_t hrow = ti.row0 + c0 + j;
-              // the same on every lane too (the shuffle below needs them all)
-              if (!in_bounds(hrow < p.out_rows_cap && (ti.mblock + 1) * TILE_ROWS <= p.out_ld,
-                             p.status))
-                continue;
-              float g = __uint_as_float(ra[j]);
-              float u = __uint_as_float(rb[j]);
+          for (int j = 0; j < 16; j += 2) {
+            float hv[2];
+#pragma unroll
+            for (int u2 = 0; u2 < 2; ++u2) {
+              float g = __uint_as_float(ra[j + u2]);
+              float u = __uint_as_float(rb[j + u2]);
               if constexpr (F8) {
-                const float sx = __shfl_sync(kFull, lfac, j);
+                const float sx = __shfl_sync(kFull, lfac, j + u2);
                 g *= sw0 * sx;
                 u *= sw1 * sx;
               }
               // fast exp and divide, as in the single-CTA kernel
-              const float h = __fdividef(g, 1.0f + __expf(-g)) * u;
-              p.h_out[hrow * p.out_ld + col] = f32_to_bf16(h);
+              hv[u2] = __fdividef(g, 1.0f + __expf(-g)) * u;
+            }
+            hp[(cc + j) / 2] = static_cast<uint32_t>(f32_to_bf16(hv[0])) |
+                               (static_cast<uint32_t>(f32_to_bf16(hv[1])) << 16);
+          }
+        }
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive_cluster(ptx::map_to_rank(tempty_bar(acc), 0));
+#pragma unroll
+        for (int cc = 0; cc < COLS_PER_WARP; cc += 16) {
+          const int c0 = col_begin + cc;
+          if (c0 >= ti.nvalid) break;
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            if (c0 + j < ti.nvalid) {  // the same on every lane of the warp
+              const int64_t hrow = ti.row0 + c0 + j;
+              if (!in_bounds(hrow < p.out_rows_cap && (ti.mblock + 1) * TILE_ROWS <= p.out_ld,
+                             p.status))
+                continue;
+              p.h_out[hrow * p.out_ld + col] =
+                  static_cast<uint16_t>(hp[(cc + j) / 2] >> (16 * ((cc + j) & 1)));
             }
           }
-        } else {
+        }
+      } else {
+#pragma unroll 1
+        for (int c0 = col_begin; c0 < min(ti.nvalid, col_begin + COLS_PER_WARP); c0 += 16) {
+          if (!in_bounds(c0 + 16 <= kPairNT, p.status)) break;
+          uint32_t ra[16];
+          ptx::tmem_ld16(tq + c0, ra);
+          // per-token factors of the chunk's 16 columns, one column per lane,
+          // handed out by shuffles (as in the single-CTA kernel)
+          const int lrow = ti.row0 + c0 + (lane & 15);
+          const bool lvalid = c0 + (lane & 15) < ti.nvalid;
+          float lfac = 1.f;
+          int lorow = lrow;
+          if (lvalid) {
+            lfac = F8 ? p.b_scale[lrow] * p.perm_w[lrow] : p.perm_w[lrow];
+            if (p.out_rows) lorow = p.out_rows[lrow];
+          }
           uint32_t rb[16];
           if constexpr (PAIR) ptx::tmem_ld16(tq + kPairNT + c0, rb);
           ptx::tmem_wait_ld();
@@ -439,10 +467,10 @@ __global__ void __launch_bounds__(PairCfg<MODE>::THREADS, 1)
             }
           }
         }
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive_cluster(ptx::map_to_rank(tempty_bar(acc), 0));
       }
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive_cluster(ptx::map_to_rank(tempty_bar(acc), 0));
       if (++acc == C::ACC_BUFS) {
         acc = 0;
         acc_phase ^= 1u;
