@@ -96,9 +96,12 @@ struct Cfg {
   static constexpr uint32_t ACC_COLS = NUM_ACC * NT;
   static constexpr uint32_t A_COLS = NUM_A * (KSUB / 2);  // one converted slice
   static constexpr uint32_t A_BASE = 2 * ACC_COLS;
-  // converted slices in flight: as many as the 512 TMEM columns hold, up to 12
+  // converted slices in flight: four.  Each converter warp's TMEM stores
+  // wait behind the MMAs already queued, so a deeper ring lengthens that
+  // wait (128-token NVFP4 batch: 6 slots 1.190 ms per layer, 4 slots
+  // 1.142 ms, 2 slots 1.167 ms)
   static constexpr int RA_RAW = static_cast<int>((512 - A_BASE) / A_COLS);
-  static constexpr int RA = RA_RAW > 12 ? 12 : RA_RAW;
+  static constexpr int RA = 4;
   static constexpr uint32_t TMEM_COLS = pow2_at_least(A_BASE + RA * A_COLS);
   static constexpr uint32_t NUM_BARS = 2 * STAGES + 2 * RA + 5;
   static constexpr uint32_t MISC_BYTES = 16 + 4 * (3 * kMaxE + 1);
@@ -108,6 +111,7 @@ struct Cfg {
   static_assert(TMEM_COLS <= 512, "TMEM columns");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
   static_assert(STAGES >= 2, "two stages at least");
+  static_assert(RA <= RA_RAW, "TMEM holds the accumulators and RA converted slices");
   static_assert(RA % 2 == 0,
                 "slices alternate between two converter warps: an even ring");
 };
