@@ -18,9 +18,13 @@
 //
 // So each SM holds half of the token block instead of all of it: a gate/up
 // stage is 32 KB of weights plus 16 KB of tokens (four stages in flight
-// instead of three), a down stage 16 + 16 KB (six stages, and its one
-// 256-column accumulator fits twice in TMEM, so the MMA never waits for the
-// epilogue), for the same MMA work per SM and stage.
+// instead of three), for the same MMA work per SM and stage.  The down GEMM
+// (kModeDownPair) takes 512 weight rows per tile as two 256-row
+// accumulators, the same stage shape.  The template also covers one 256-row
+// accumulator per tile (kModeDown: 16 + 16 KB stages, the accumulator fits
+// twice in TMEM); the launcher does not instantiate it, as it measured
+// slower on the Beam shapes, and shapes whose d is not a multiple of 512
+// take the single-CTA kernels.
 //
 // Protocol (every wait bounded, as in the single-CTA kernel):
 //   - TMEM is allocated and freed collectively by one warp of each CTA;
