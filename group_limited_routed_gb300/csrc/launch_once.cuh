@@ -50,17 +50,18 @@ int blocks_per_sm_once(int threads) {
 }
 
 // ------------------------------------------- programmatic dependent launch
-// The layer's later kernels (expert GEMMs, combine) are launched with
-// programmatic stream serialization (SGLang post "SGLang 原生支持 Reflection 的
-// Beam 并驱动其生产 API", section "Fusion Optimizations": a kernel sets up and
-// loads weights before its dependency wait).  Such a kernel may start while
-// the kernel before it still runs, so each one executes griddepcontrol.wait
-// before it reads anything that kernel writes, and writes nothing that kernel
-// reads.  Reads before the wait are allowed only of data written two or more
-// kernels earlier: the one kernel here that lets its successor start early
-// (the gate/up GEMM, for the down GEMM) does so after its own wait, so by
-// then all earlier kernels have completed.  A kernel that never triggers
-// lets its successor start when it completes.
+// The layer's later kernels (token-row quantisation and gathers, expert
+// GEMMs, combine) are launched with programmatic stream serialization
+// (SGLang post "SGLang 原生支持 Reflection 的 Beam 并驱动其生产 API", section
+// "Fusion Optimizations": a kernel sets up and loads weights before its
+// dependency wait).  Such a kernel may start while the kernel before it
+// still runs, so each one executes griddepcontrol.wait before it reads
+// anything that kernel writes, and writes nothing that kernel reads.  Reads
+// before the wait (a GEMM's tile list and weights) are allowed only of data
+// written two or more kernels earlier: every kernel here that lets its
+// successor start early (griddepcontrol.launch_dependents) does so after its
+// own wait, so by then all earlier kernels have completed.  A kernel that
+// never triggers lets its successor start when it completes.
 constexpr int kProgrammaticLaunch = 1;
 
 template <typename... KArgs, typename... Args>
